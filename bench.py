@@ -1,0 +1,524 @@
+"""Benchmark of the NVFP4 routed-expert MoE layer on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one call of the layer (route + permutation, gate/up + SwiGLU,
+down + weighted combine) over one batch of seeded synthetic tokens whose
+inputs are already resident in HBM.  The default workload is the
+decode-shaped layer (288 experts, top-8, d=4096, ffn=1536) at T=64; the
+line also carries a sweep over T in {1, 8, 32, 64}.  The L2 is flushed (a
+256 MB write) between timed steps, outside the timed events.
+
+Under torchrun every rank runs its own batch on its own GPU (no collective
+on the data path); the reported time is the max over ranks and the value
+counts the tokens of all ranks ("weak" scaling).
+
+--impl reference times the CPU oracle (the plain C restatement used by the
+tests) on the machine's host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from serving_nvfp4_routed_gb300 import synth  # noqa: E402
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+EXPERT_BYTES = lambda d, F: 3 * d * F * 9 // 16  # codes (1/2 B) + e4m3 scales (1/16 B) per weight
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (host logic; tested with gloo on CPU)
+# ---------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(value: float, device=None) -> float:
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def aggregate(units_per_rank: float, ms_per_rank: float, world: int, device=None):
+    """Whole-job throughput: all ranks' units over the slowest rank's time."""
+    ms = reduce_max(ms_per_rank, device)
+    return units_per_rank * world / (ms / 1e3), ms
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+WORKLOADS = {
+    "decode1": (synth.decode(1), "w4a16", "normal", 0.0),
+    "decode8": (synth.decode(8), "w4a16", "normal", 0.0),
+    "decode32": (synth.decode(32), "w4a16", "normal", 0.0),
+    "decode64": (synth.decode(64), "w4a16", "normal", 0.0),
+    "prefill_w4a16": (synth.PREFILL_W4A16, "w4a16", "normal", 0.05),
+    "prefill_w4a4": (synth.PREFILL_W4A4, "w4a4", "normal", 0.05),
+    "skew_w4a16": (synth.SKEW, "w4a16", "zipf", 0.0),
+    "skew_w4a4": (synth.SKEW, "w4a4", "zipf", 0.0),
+    "skew_masked_w4a16": (synth.SKEW, "w4a16", "zipf_masked", 0.0),
+}
+
+
+def peaks():
+    try:
+        p = json.load(open(PEAKS_FILE))
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "serving_nvfp4_routed_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, fn), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    try:
+        t = json.load(open(TRAFFIC_FILE))
+        ent = t[kernel][workload]
+        if ent.get("source_hash") == kernel_source_hash():
+            return float(ent["bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+def synthetic_input_scales(x: torch.Tensor, E: int):
+    """Static input scales for timing runs: p99 of the 16-block max |x| of
+    the batch, x 1.05, / 2688, the same for every expert; the down-side
+    scale assumes h blocks of about the same size.  (Parity tests calibrate
+    per expert with the oracle instead; the scales only move saturation.)"""
+    bam = x[: min(1024, x.shape[0])].float().abs().view(-1, 16).amax(1)
+    p99 = torch.quantile(bam[: 1 << 20].cpu(), 0.99).item()
+    is13 = torch.full((E,), p99 * 1.05 / 2688.0, dtype=torch.float32, device=x.device)
+    is2 = torch.full((E,), 4.0 * 1.05 / 2688.0, dtype=torch.float32, device=x.device)
+    return is13, is2
+
+
+class Layer:
+    """Resident weights + a rotation of input batches for one workload."""
+
+    def __init__(self, name, lib, device, seed, n_batches=4):
+        self.name = name
+        self.shape, self.mode, self.kind, self.outlier = WORKLOADS[name]
+        s = self.shape
+        self.lib = lib
+        self.device = device
+        banks = {}
+        for nm, (N, K), sd in (("gate", (s.F, s.d), 3), ("up", (s.F, s.d), 4), ("down", (s.d, s.F), 5)):
+            w = synth.make_weights(s.E, N, K, seed * 10 + sd, device)
+            banks[nm] = lib.nvfp4_quantize_weights(w)
+            del w
+        torch.cuda.empty_cache()
+        self.w = lib.MoEWeights(banks["gate"], banks["up"], banks["down"])
+        self.batches = []
+        for b in range(n_batches):
+            x = synth.make_x(s.T, s.d, seed * 100 + 2 * b, device, self.outlier)
+            lg = synth.make_logits(s.T, s.E, seed * 100 + 2 * b + 1, device, self.kind)
+            self.batches.append((x, lg))
+        self.is13 = self.is2 = None
+        if self.mode == "w4a4":
+            self.is13, self.is2 = synthetic_input_scales(self.batches[0][0], s.E)
+        self.ws = lib.moe_workspace(s.T, s.E, s.k, s.d, s.F, self.mode, device)
+        self.out = torch.empty(s.T, s.d, dtype=torch.bfloat16, device=device)
+
+    def step(self, i, x=None, lg=None):
+        if x is None:
+            x, lg = self.batches[i % len(self.batches)]
+        s = self.shape
+        if self.mode == "w4a16":
+            return self.lib.nvfp4_moe_w4a16(x, lg, s.k, self.w, out=self.out, ws=self.ws)
+        return self.lib.nvfp4_moe_w4a4(x, lg, s.k, self.w, self.is13, self.is2, out=self.out, ws=self.ws)
+
+    def touched_experts(self, i):
+        s = self.shape
+        self.step(i)
+        v = self.lib.moe_workspace_views(self.ws, s.T, s.E, s.k, s.d, s.F, self.mode)
+        counts = torch.diff(v["offsets"]).cpu()
+        return int((counts > 0).sum().item())
+
+    def algorithmic_bytes(self, touched):
+        s = self.shape
+        R = s.T * s.k
+        w = touched * EXPERT_BYTES(s.d, s.F)
+        io = s.T * s.d * 2 + s.T * s.E * 4 + s.T * s.d * 2
+        return w + io, R
+
+    def gateup_bytes(self, touched):
+        s = self.shape
+        R = s.T * s.k
+        w = touched * 2 * s.F * s.d * 9 // 16
+        if self.mode == "w4a16":
+            act = s.T * s.d * 2 + R * s.F * 2
+        else:
+            act = R * s.d * 9 // 16 + R * s.F * 9 // 16
+        return w + act
+
+    def flops(self):
+        s = self.shape
+        return 6.0 * s.T * s.k * s.d * s.F
+
+
+def time_steps(layer, steps, flush, start=0):
+    """Per-step CUDA-event time (ms) of `steps` calls, L2 flushed between."""
+    stream = torch.cuda.current_stream()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
+        evs[i][0].record(stream)
+        layer.step(start + i)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def time_e2e(layer, steps, flush):
+    """Same metric with host buffers: pinned H2D of x and logits, the layer,
+    D2H of the output, all inside the timed events."""
+    s = layer.shape
+    hx = [b[0].cpu().pin_memory() for b in layer.batches]
+    hl = [b[1].cpu().pin_memory() for b in layer.batches]
+    dx = torch.empty_like(layer.batches[0][0])
+    dl = torch.empty_like(layer.batches[0][1])
+    hout = torch.empty(s.T, s.d, dtype=torch.bfloat16).pin_memory()
+    stream = torch.cuda.current_stream()
+    times = []
+    for i in range(steps):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        dx.copy_(hx[i % len(hx)], non_blocking=True)
+        dl.copy_(hl[i % len(hl)], non_blocking=True)
+        out = layer.step(i, dx, dl)
+        hout.copy_(out, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    h2d = dx.numel() * dx.element_size() + dl.numel() * dl.element_size()
+    d2h = hout.numel() * hout.element_size()
+    return statistics.mean(times), h2d, d2h
+
+
+def cpu_baseline(layer, seed, n_tokens=8):
+    """The oracle (plain C, fp64, OpenMP on the host cores) on a bounded
+    sample of the workload: `n_tokens` tokens of the first batch in a seeded
+    order.  The weights of the sampled tokens' experts are quantised by the
+    oracle itself first (untimed: load-time work, not part of a layer call)."""
+    from oracle import oracle as orc
+
+    s = layer.shape
+    x, lg = layer.batches[0]
+    r = orc.route(lg.cpu().numpy(), s.k)
+    xb = synth.bf16_bits(x)
+    rng = np.random.default_rng(seed)
+    tok = np.sort(rng.permutation(s.T)[: min(n_tokens, s.T)]).astype(np.int32)
+    experts = np.unique(r["ids"][tok])
+    ob = {}
+    for nm, (N, K), sd in (("gate", (s.F, s.d), 3), ("up", (s.F, s.d), 4), ("down", (s.d, s.F), 5)):
+        w = synth.make_weights(s.E, N, K, seed * 10 + sd, layer.device)
+        codes = np.zeros((s.E, N, K // 2), np.uint8)
+        scales = np.zeros((s.E, N, K // 16), np.uint8)
+        ws2 = np.zeros(s.E, np.float32)
+        for e in experts:
+            codes[e], scales[e], ws2[e] = orc.quantize_tensor(synth.bf16_bits(w[int(e)]))
+        ob[nm] = (codes, scales, ws2)
+        del w
+    torch.cuda.empty_cache()
+    is13 = None if layer.is13 is None else layer.is13.cpu().numpy()
+    is2 = None if layer.is2 is None else layer.is2.cpu().numpy()
+    t0 = time.perf_counter()
+    orc.moe_layer(layer.mode, xb, r["ids"], r["w"], ob, tokens=tok, is13=is13, is2=is2)
+    elapsed = time.perf_counter() - t0
+    return {"value": len(tok) / elapsed, "unit": "tokens/s", "cores": orc.num_threads(), "kind": "oracle",
+            "sample": f"{len(tok)} of the {s.T} tokens of the {layer.name} batch (seeded choice), "
+                      f"{elapsed:.1f} s of oracle time over their {len(tok) * s.k} (token, expert) pairs; "
+                      f"expert weights quantised by the oracle beforehand, untimed"}
+
+
+def workload_config(layer, flush_mb):
+    s = layer.shape
+    desc = {"w4a16": "W4A16", "w4a4": "W4A4"}[layer.mode]
+    return {"workload": f"{layer.name}: routed-expert NVFP4 layer {desc}, E={s.E} top-{s.k} d={s.d} "
+                        f"ffn={s.F} T={s.T}, logits {layer.kind}",
+            "T": s.T, "E": s.E, "top_k": s.k, "d": s.d, "ffn": s.F, "mode": layer.mode,
+            "l2": f"flushed between steps ({flush_mb} MB write), outside the timed events",
+            "parallelism": "independent replicas (one batch per GPU)"}
+
+
+def run_ours(args):
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    from serving_nvfp4_routed_gb300 import build as nvbuild
+
+    if rank == 0:
+        nvbuild.build()
+    barrier()
+    import serving_nvfp4_routed_gb300 as lib
+
+    hbm, bf16, peak_kind = peaks()
+    flush_mb = 256
+    flush = torch.empty(flush_mb << 20, dtype=torch.uint8, device=dev)
+    seed = 1001 + 17 * rank
+    layer = Layer(args.workload, lib, dev, seed)
+
+    for i in range(args.warmup):
+        layer.step(i)
+    torch.cuda.synchronize()
+    touched = layer.touched_experts(0)
+
+    launches0 = lib.launch_count()
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        times = time_steps(layer, args.steps, flush)
+    torch.cuda.synchronize()
+    barrier()
+    launches = lib.launch_count() - launches0
+    ms = statistics.mean(times)
+    value, ms_max = aggregate(layer.shape.T, ms, world, dev)
+
+    # per-kernel times (CUDA events around each launch, same stream, same steps)
+    lib.profile_enable(True)
+    time_steps(layer, args.steps, flush)
+    lib.profile_enable(False)
+    prof = lib.profile_collect()
+    e2e_ms, h2d, d2h = time_e2e(layer, max(3, args.steps), flush)
+    e2e_value, _ = aggregate(layer.shape.T, e2e_ms, world, dev)
+
+    total_bytes, R = layer.algorithmic_bytes(touched)
+    gu_name = "gemv_gateup_w4a16" if layer.mode == "w4a16" else "gemv_gateup_w4a4"
+    kernels = {k: {"launches": v[0], "ms_per_launch": v[1] / max(1, v[0])} for k, v in prof.items()}
+    dom = max(kernels, key=lambda k: kernels[k]["ms_per_launch"] * kernels[k]["launches"]) if kernels else gu_name
+    if dom.startswith("gemv_down"):
+        s = layer.shape
+        dom_bytes = touched * s.d * s.F * 9 // 16 + (R * s.F * 2 if layer.mode == "w4a16" else R * s.F * 9 // 16)
+    else:
+        dom_bytes = layer.gateup_bytes(touched)
+    dom_ms = kernels.get(dom, {"ms_per_launch": float("nan")})["ms_per_launch"]
+    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+    layer_gbs = total_bytes / (ms / 1e3) / 1e9
+
+    line = {
+        "metric": "MoE-layer tokens/s (decode-shaped routed NVFP4 layer)",
+        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e2m1+e4m3 weights, f16 mma, f32 accumulate" if layer.mode == "w4a16"
+                 else "e2m1+e4m3 weights and activations, f16 mma, f32 accumulate",
+        "data": "synthetic (seeded N(0,1) x and logits, N(0,0.02) bf16 weights quantised by the library)",
+        "config": workload_config(layer, flush_mb),
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "peak_kind": f"{peak_kind} (copy bandwidth, burst)",
+                     "traffic": recorded_traffic(dom, args.workload), "algorithmic_bytes_per_launch": dom_bytes,
+                     "layer_gbs": layer_gbs, "layer_frac": layer_gbs / hbm,
+                     "touched_experts": touched},
+        "kernels": kernels,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    if args.sweep and args.workload == "decode64":
+        sweep = {}
+        for T in synth.DECODE_T:
+            if T == 64:
+                sweep["decode64"] = {"tokens_per_s": layer.shape.T / (ms / 1e3), "layer_frac": layer_gbs / hbm}
+                continue
+            sl = Layer(f"decode{T}", lib, dev, seed + T)
+            for i in range(args.warmup):
+                sl.step(i)
+            tch = sl.touched_experts(0)
+            tt = statistics.mean(time_steps(sl, args.steps, flush))
+            b, _ = sl.algorithmic_bytes(tch)
+            sweep[f"decode{T}"] = {"tokens_per_s": T / (tt / 1e3), "ms": tt, "touched_experts": tch,
+                                   "layer_gbs": b / (tt / 1e3) / 1e9, "layer_frac": b / (tt / 1e3) / 1e9 / hbm}
+            del sl
+            torch.cuda.empty_cache()
+        line["sweep"] = sweep
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(layer, seed, n_tokens=args.cpu_tokens)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    world, rank, local = dist_env()
+    if rank != 0:
+        return
+    from oracle import oracle as orc
+
+    orc.build()
+    dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
+    shape, mode, kind, outlier = WORKLOADS[args.workload]
+    seed = 1001
+    x = synth.make_x(shape.T, shape.d, seed * 100, dev, outlier)
+    lg = synth.make_logits(shape.T, shape.E, seed * 100 + 1, dev, kind)
+    r = orc.route(lg.cpu().numpy(), shape.k)
+    xb = synth.bf16_bits(x)
+    gen = {nm: (N, K, sd) for nm, (N, K), sd in
+           (("gate", (shape.F, shape.d), 3), ("up", (shape.F, shape.d), 4), ("down", (shape.d, shape.F), 5))}
+    per_step = max(1, min(shape.T, args.ref_tokens))
+    rng = np.random.default_rng(seed)
+    tok_all = rng.permutation(shape.T)[: per_step * (args.warmup + args.steps)] % shape.T
+    experts = np.unique(r["ids"][tok_all])
+    ob = {}
+    for nm, (N, K, sd) in gen.items():
+        w = synth.make_weights(shape.E, N, K, seed * 10 + sd, dev)
+        codes = np.zeros((shape.E, N, K // 2), np.uint8)
+        scales = np.zeros((shape.E, N, K // 16), np.uint8)
+        ws2 = np.zeros(shape.E, np.float32)
+        for e in experts:
+            codes[e], scales[e], ws2[e] = orc.quantize_tensor(synth.bf16_bits(w[int(e)]))
+        ob[nm] = (codes, scales, ws2)
+        del w
+    is13 = is2 = None
+    if mode == "w4a4":
+        a, b = synthetic_input_scales(x, shape.E)
+        is13, is2 = a.cpu().numpy(), b.cpu().numpy()
+    times = []
+    for i in range(args.warmup + args.steps):
+        tok = np.sort(tok_all[i * per_step:(i + 1) * per_step]).astype(np.int32)
+        t0 = time.perf_counter()
+        orc.moe_layer(mode, xb, r["ids"], r["w"], ob, tokens=tok, is13=is13, is2=is2)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    ms = statistics.mean(times) * 1e3
+    value = per_step / (ms / 1e3)
+    cores = orc.num_threads()
+    line = {"impl": "reference", "metric": "MoE-layer tokens/s (decode-shaped routed NVFP4 layer)",
+            "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64 (CPU oracle)", "data": "synthetic",
+            "config": {"workload": f"{args.workload} (same seeds and shapes as the GPU arm)", "T": shape.T,
+                       "E": shape.E, "top_k": shape.k, "d": shape.d, "ffn": shape.F, "mode": mode},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{per_step} tokens per step of the {shape.T}-token batch"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode64")
+    ap.add_argument("--no-sweep", dest="sweep", action="store_false")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-tokens", type=int, default=8)
+    ap.add_argument("--ref-tokens", type=int, default=4)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,208 @@
+/*
+ * nvfp4moe.h -- C ABI of libnvfp4moe: the routed-expert MoE layer over a
+ * ModelOpt NVFP4 checkpoint as stored, on one GB300 (sm_103a).
+ *
+ * The format (TensorFold issue #308, "GLM-5.3-Flash on CUDA: read
+ * nvidia/GLM-5.3-Flash-NVFP4 (ModelOpt NVFP4) as stored, W4A16", section "The
+ * checkpoint"): a weight tensor [N, K] is stored as
+ *   codes  uint8 [N, K/2]   two e2m1 codes per byte, EVEN k in the LOW nibble
+ *   scales uint8 [N, K/16]  one e4m3 scale per 16 consecutive k ("fn": bias 7,
+ *                           max 448, 0x7F NaN), row-major as stored
+ *   weight_scale_2 float    one fp32 tensor scale
+ * and the weight value is  e2m1(q) * e4m3(s) * weight_scale_2.
+ * A static fp32 input_scale per linear is stored for W4A4.
+ *
+ * Conventions for every call below
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller; the
+ *     library never allocates, frees or keeps a pointer after returning.
+ *     Tensors are row-major and contiguous.  bf16 tensors are passed as
+ *     uint16_t bit patterns.
+ *   - Every pointer must be 16-byte aligned (NVFP4_ERR_ALIGN otherwise).
+ *   - Calls are asynchronous on the caller's CUDA stream (0 = legacy default
+ *     stream) and return before the work is done.  The return value reports
+ *     host-side validation and launch errors only.
+ *   - Host validation happens before any launch: bad shapes, NULL pointers,
+ *     misalignment and a too-small workspace are rejected and nothing is
+ *     enqueued.  Problems only the device can see (a user-supplied expert id
+ *     out of range) are written to the optional int32 status word d_status
+ *     as an nvfp4_status value; kernels never trap.
+ *   - K (the reduction length of a GEMM) must be a multiple of 64; N (output
+ *     features) a multiple of 16; row counts M or T may be 0 (no-op).
+ *   - Inputs must be finite; NaN/Inf behaviour is unspecified.
+ *   - Workspace contents are scratch owned by the call until it completes on
+ *     the stream; two calls that overlap on the GPU must not share one.
+ */
+#ifndef NVFP4MOE_H
+#define NVFP4MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* cudaStream_t;
+
+typedef enum {
+    NVFP4_OK = 0,
+    NVFP4_ERR_INVALID_ARG = 1, /* NULL pointer, negative size, bad enum       */
+    NVFP4_ERR_SHAPE = 2,       /* K % 64, N % 16, top_k > E, E > 1024, ...     */
+    NVFP4_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned             */
+    NVFP4_ERR_WORKSPACE = 4,   /* ws_bytes smaller than the size query's       */
+    NVFP4_ERR_UNSUPPORTED = 5, /* no device / not sm_100-family                */
+    NVFP4_ERR_CUDA = 6,        /* a CUDA launch failed (cudaGetLastError)      */
+    NVFP4_ERR_TIMEOUT = 7,     /* a bounded device wait gave up (d_status)     */
+    NVFP4_ERR_DEVICE_INPUT = 8 /* device saw an out-of-range id (d_status)     */
+} nvfp4_status;
+
+/* One stacked NVFP4 tensor bank: codes [E, N, K/2], scales [E, N, K/16],
+ * weight_scale_2 [E] (E = 1 for a single tensor). */
+typedef struct {
+    const uint8_t* codes;
+    const uint8_t* scales;
+    const float* weight_scale_2;
+} nvfp4_w;
+
+/* The routed experts of one layer (model card "GLM-5.3-Flash-NVFP4-W4A4-
+ * Experts", "Quantization boundary": gate_proj, up_proj, down_proj per
+ * expert).  gate/up: N = F, K = d; down: N = d, K = F. */
+typedef struct {
+    nvfp4_w gate, up, down;
+    int E, d, F;
+} nvfp4_moe_weights;
+
+/* ------------------------------------------------------------------------
+ * nvfp4_quantize_weights -- ModelOpt's NVFP4 recipe, applied to each of
+ * `batch` bf16 tensors [N, K] (TensorFold #308, "What the branch does": BF16
+ * experts packed to NVFP4 by ModelOpt's recipe at load, one projection at a
+ * time).  Per tensor b:
+ *   weight_scale_2[b] = amax / 2688                      (fp32, 2688 = 6*448)
+ *   per 16-block: s = e4m3_rn_sat((block_amax / 6) / weight_scale_2[b])
+ *   per element:  q = e2m1_rn_sat(w / (e4m3(s) * weight_scale_2[b]))
+ * (IEEE fp32 round-to-nearest division and product in exactly this order; a
+ * block whose scale rounds to 0 gets all-zero codes.)
+ *   w       [batch, N, K] bf16     codes [batch, N, K/2]   scales [batch, N, K/16]
+ *   weight_scale_2 [batch] fp32
+ *   ws      scratch of at least nvfp4_quantize_weights_workspace_size() bytes
+ * K must be a multiple of 16.  Two device passes (global amax, then codes).
+ * --------------------------------------------------------------------- */
+nvfp4_status nvfp4_quantize_weights(const uint16_t* w_bf16, int batch, int N, int K,
+                                    uint8_t* codes, uint8_t* scales, float* weight_scale_2,
+                                    void* ws, size_t ws_bytes, cudaStream_t stream);
+size_t nvfp4_quantize_weights_workspace_size(int batch, int N, int K);
+
+/* ------------------------------------------------------------------------
+ * nvfp4_quantize_act -- static-scale NVFP4 quantisation of activation rows
+ * (TensorFold #308 "The checkpoint": input_scale stored for static
+ * activations; W4A4 model card: calibrated static activation scales).
+ * Output row r (0 <= r < M) quantises source row
+ *     src(r) = row_to_slot ? row_to_slot[r] / top_k : r
+ * of x [*, K] with tensor scale
+ *     gs(r) = expert_offsets ? input_scale[e] where offsets[e] <= r < offsets[e+1]
+ *                            : input_scale[0]
+ * using the same block rule as the weight recipe with gs in place of
+ * weight_scale_2 (block scales above 448 saturate to 448, codes to +-6).
+ *   codes [M, K/2], scales [M, K/16].  K % 16 == 0.  E <= 1024.
+ * --------------------------------------------------------------------- */
+nvfp4_status nvfp4_quantize_act(const uint16_t* x_bf16, int M, int K,
+                                const int32_t* row_to_slot, int top_k,
+                                const float* input_scale, const int32_t* expert_offsets, int E,
+                                uint8_t* codes, uint8_t* scales, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * moe_route_permute -- the BF16 router's logits to expert-contiguous rows
+ * (TensorFold #308: router BF16, routed experts through one grouped
+ * kernel).  Per token t: softmax over the E logits, the top_k experts in
+ * descending order (ties -> lower expert id), and their weights
+ * renormalised over the chosen top_k (computed in fp64, stored fp32):
+ *   topk_ids [T, top_k] int32, topk_w [T, top_k] fp32.
+ * Then a stable permutation of the R = T*top_k (token, slot) pairs by
+ * expert (order: expert, token, slot):
+ *   expert_offsets [E+1]: first row of each expert, offsets[E] = R
+ *   row_to_slot [R]: row -> t*top_k + slot;  slot_to_row [R]: the inverse.
+ * Per-expert histogram, warp-scan prefix sum and scatter; the result is
+ * deterministic (no atomics decide an order).  E <= 1024, top_k <= 32.
+ *   ws: at least moe_route_permute_workspace_size(T, E, top_k) bytes.
+ * --------------------------------------------------------------------- */
+nvfp4_status moe_route_permute(const float* logits, int T, int E, int top_k,
+                               int32_t* topk_ids, float* topk_w, int32_t* expert_offsets,
+                               int32_t* row_to_slot, int32_t* slot_to_row,
+                               void* ws, size_t ws_bytes, cudaStream_t stream);
+size_t moe_route_permute_workspace_size(int T, int E, int top_k);
+
+/* ------------------------------------------------------------------------
+ * nvfp4_moe_w4a16 / nvfp4_moe_w4a4 -- the routed-expert layer.
+ * TensorFold #308 "What the branch does": routed experts run through a
+ * grouped NVFP4 expert kernel over bf16 rows (W4A16) with weight_scale_2 as
+ * the per-expert multiplier; the checkpoint's own FP4 x FP4 math (W4A4)
+ * quantises the activations with the stored static input_scale.  Per token
+ * t and slot j with e = topk_ids[t, j]:
+ *   G = bf16(ws2_g[e] * x W_g[e]^T)   U = bf16(ws2_u[e] * x W_u[e]^T)
+ *   h = bf16(silu(G) * U)
+ *   Y = ws2_d[e] * h W_d[e]^T         (fp32)
+ *   out[t] = bf16(sum_j topk_w[t, j] * Y_j)
+ * W4A4: x is first quantised per (t, e) with input_scale_w13[e]; h with
+ * input_scale_w2[e]; the GEMMs multiply FP4 x FP4 with fp32 accumulation.
+ *   x [T, d] bf16, logits [T, E] fp32, out [T, d] bf16.
+ *   logits == NULL: the routing arrays already in the workspace (written by
+ *   an earlier call or by moe_route_permute into the views that
+ *   nvfp4_moe_workspace_views returns) are used; out-of-range expert ids
+ *   are then reported through d_status (NVFP4_ERR_DEVICE_INPUT).
+ *   ws: at least nvfp4_moe_workspace_size(T, E, top_k, d, F, mode) bytes
+ *   (mode 0 = W4A16, 1 = W4A4); d_status: optional device int32.
+ * Shapes: d % 64 == 0, F % 64 == 0, E <= 1024, 1 <= top_k <= min(E, 32).
+ * --------------------------------------------------------------------- */
+nvfp4_status nvfp4_moe_w4a16(const uint16_t* x_bf16, int T, const float* logits, int top_k,
+                             const nvfp4_moe_weights* w, uint16_t* out_bf16,
+                             void* ws, size_t ws_bytes, int32_t* d_status, cudaStream_t stream);
+nvfp4_status nvfp4_moe_w4a4(const uint16_t* x_bf16, int T, const float* logits, int top_k,
+                            const nvfp4_moe_weights* w, const float* input_scale_w13,
+                            const float* input_scale_w2, uint16_t* out_bf16,
+                            void* ws, size_t ws_bytes, int32_t* d_status, cudaStream_t stream);
+size_t nvfp4_moe_workspace_size(int T, int E, int top_k, int d, int F, int mode);
+
+/* Device pointers to the routing arrays inside an nvfp4_moe workspace (the
+ * same arrays moe_route_permute produces), so that a caller can read them
+ * back or fill them.  Any output pointer may be NULL. */
+nvfp4_status nvfp4_moe_workspace_views(void* ws, int T, int E, int top_k, int d, int F, int mode,
+                                       int32_t** topk_ids, float** topk_w,
+                                       int32_t** expert_offsets, int32_t** row_to_slot,
+                                       int32_t** slot_to_row);
+
+/* ------------------------------------------------------------------------
+ * nvfp4_linear -- dense NVFP4 linear over bf16 rows (TensorFold #308: the
+ * dense MLP runs on Fp4Linear, gate and up apart since their tensor scales
+ * differ).
+ *   w_up == NULL:  out [M, N] = bf16(ws2 * x W^T)
+ *   w_up != NULL:  out [M, N] = bf16(silu(bf16(ws2 * x W^T)) * bf16(ws2_up * x W_up^T))
+ * x [M, K] bf16, w / w_up single tensors [N, K] (E = 1).  K % 64 == 0,
+ * N % 16 == 0.  ws: at least nvfp4_linear_workspace_size(M, K, N) bytes.
+ * --------------------------------------------------------------------- */
+nvfp4_status nvfp4_linear(const uint16_t* x_bf16, int M, int K, const nvfp4_w* w, int N,
+                          const nvfp4_w* w_up, uint16_t* out_bf16,
+                          void* ws, size_t ws_bytes, cudaStream_t stream);
+size_t nvfp4_linear_workspace_size(int M, int K, int N);
+
+/* ------------------------------------------------------------------------
+ * Helpers.
+ * nvfp4_status_string: a static, human-readable name of a status.
+ * nvfp4_launch_count: number of kernels this library has launched in this
+ *   process (all devices, all streams), for accounting.
+ * nvfp4_profile_enable(1): from now on, every launch is bracketed by CUDA
+ *   events on its stream; nvfp4_profile_collect synchronises on those events,
+ *   writes per-kernel-name totals (name, launches, milliseconds) for up to
+ *   `max` names, resets the totals and returns the number of names.
+ *   names must hold max * 64 chars.  Timing adds event records between
+ *   launches; turn it off (0) for headline measurements.
+ * --------------------------------------------------------------------- */
+const char* nvfp4_status_string(nvfp4_status s);
+uint64_t nvfp4_launch_count(void);
+void nvfp4_profile_enable(int on);
+int nvfp4_profile_collect(int max, char* names, int* launches, double* ms);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NVFP4MOE_H */

@@ -316,6 +316,10 @@ void orc_moe_layer(int mode, const uint16_t* x, int64_t T, int64_t d, int64_t F,
                    const int32_t* tokens, int64_t n_tokens, float* out, float* h_out) {
     (void)T;
     (void)E;
+    /* Y_j of every (token, slot) pair, then the weighted sum over the slots
+     * in slot order.  Pairs are independent, so they are spread over the
+     * threads; the sum itself is sequential. */
+    double* Y = (double*)malloc(sizeof(double) * (size_t)(n_tokens * k * d));
 #pragma omp parallel
     {
         float* xrow = (float*)malloc(sizeof(float) * (size_t)d);
@@ -325,45 +329,50 @@ void orc_moe_layer(int mode, const uint16_t* x, int64_t T, int64_t d, int64_t F,
         float* h = (float*)malloc(sizeof(float) * (size_t)F);
         double* ha = (double*)malloc(sizeof(double) * (size_t)F);
         double* y = (double*)malloc(sizeof(double) * (size_t)d);
-        double* acc = (double*)malloc(sizeof(double) * (size_t)d);
 #pragma omp for schedule(dynamic, 1)
-        for (int64_t i = 0; i < n_tokens; ++i) {
+        for (int64_t pair = 0; pair < n_tokens * k; ++pair) {
+            int64_t i = pair / k;
+            int j = (int)(pair % k);
             int64_t t = tokens[i];
-            for (int64_t n = 0; n < d; ++n) acc[n] = 0.0;
+            int e = ids[t * k + j];
             for (int64_t n = 0; n < d; ++n) xrow[n] = bf16_bits_to_float(x[t * d + n]);
-            for (int j = 0; j < k; ++j) {
-                int e = ids[t * k + j];
-                double xscale = 1.0;
-                if (mode == 1) {
-                    quant_dequant(xrow, d, is13[e], xa);
-                    xscale = (double)is13[e];
-                } else {
-                    for (int64_t n = 0; n < d; ++n) xa[n] = (double)xrow[n];
-                }
-                nvfp4_matvec(xa, gq + (int64_t)e * F * (d / 2), gs + (int64_t)e * F * (d / 16), F, d, sg);
-                nvfp4_matvec(xa, uq + (int64_t)e * F * (d / 2), us + (int64_t)e * F * (d / 16), F, d, su);
-                for (int64_t f = 0; f < F; ++f) {
-                    double G = orc_round_bf16(sg[f] * xscale * (double)g_ws2[e]);
-                    double U = orc_round_bf16(su[f] * xscale * (double)u_ws2[e]);
-                    h[f] = (float)orc_round_bf16(silu(G) * U);
-                }
-                if (h_out)
-                    for (int64_t f = 0; f < F; ++f) h_out[(i * k + j) * F + f] = h[f];
-                double hscale = 1.0;
-                if (mode == 1) {
-                    quant_dequant(h, F, is2[e], ha);
-                    hscale = (double)is2[e];
-                } else {
-                    for (int64_t f = 0; f < F; ++f) ha[f] = (double)h[f];
-                }
-                nvfp4_matvec(ha, dq + (int64_t)e * d * (F / 2), ds + (int64_t)e * d * (F / 16), d, F, y);
-                for (int64_t n = 0; n < d; ++n)
-                    acc[n] += (double)w[t * k + j] * (y[n] * hscale * (double)d_ws2[e]);
+            double xscale = 1.0;
+            if (mode == 1) {
+                quant_dequant(xrow, d, is13[e], xa);
+                xscale = (double)is13[e];
+            } else {
+                for (int64_t n = 0; n < d; ++n) xa[n] = (double)xrow[n];
             }
-            for (int64_t n = 0; n < d; ++n) out[i * d + n] = (float)orc_round_bf16(acc[n]);
+            nvfp4_matvec(xa, gq + (int64_t)e * F * (d / 2), gs + (int64_t)e * F * (d / 16), F, d, sg);
+            nvfp4_matvec(xa, uq + (int64_t)e * F * (d / 2), us + (int64_t)e * F * (d / 16), F, d, su);
+            for (int64_t f = 0; f < F; ++f) {
+                double G = orc_round_bf16(sg[f] * xscale * (double)g_ws2[e]);
+                double U = orc_round_bf16(su[f] * xscale * (double)u_ws2[e]);
+                h[f] = (float)orc_round_bf16(silu(G) * U);
+            }
+            if (h_out)
+                for (int64_t f = 0; f < F; ++f) h_out[(i * k + j) * F + f] = h[f];
+            double hscale = 1.0;
+            if (mode == 1) {
+                quant_dequant(h, F, is2[e], ha);
+                hscale = (double)is2[e];
+            } else {
+                for (int64_t f = 0; f < F; ++f) ha[f] = (double)h[f];
+            }
+            nvfp4_matvec(ha, dq + (int64_t)e * d * (F / 2), ds + (int64_t)e * d * (F / 16), d, F, y);
+            for (int64_t n = 0; n < d; ++n) Y[pair * d + n] = y[n] * hscale * (double)d_ws2[e];
         }
-        free(xrow); free(xa); free(sg); free(su); free(h); free(ha); free(y); free(acc);
+        free(xrow); free(xa); free(sg); free(su); free(h); free(ha); free(y);
     }
+    for (int64_t i = 0; i < n_tokens; ++i) {
+        int64_t t = tokens[i];
+        for (int64_t n = 0; n < d; ++n) {
+            double acc = 0.0;
+            for (int j = 0; j < k; ++j) acc += (double)w[t * k + j] * Y[(i * k + j) * d + n];
+            out[i * d + n] = (float)orc_round_bf16(acc);
+        }
+    }
+    free(Y);
 }
 
 /*

@@ -13,6 +13,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import platform
 import subprocess
 import threading
 
@@ -20,7 +21,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "nvfp4_oracle.c")
-_OUT_DIR = os.path.join(_HERE, "_build")
+_OUT_DIR = os.path.join(_HERE, "_build", platform.machine())
 _SO = os.path.join(_OUT_DIR, "liboracle.so")
 _lock = threading.Lock()
 _lib = None

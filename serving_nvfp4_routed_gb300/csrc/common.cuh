@@ -1,0 +1,170 @@
+// common.cuh -- device helpers and host bookkeeping shared by the kernels of
+// libnvfp4moe.  Nothing here is shared with the CPU oracle.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "nvfp4moe.h"
+
+namespace nvfp4 {
+
+// ---------------------------------------------------------------------------
+// host: launch accounting and optional per-kernel event timing
+// ---------------------------------------------------------------------------
+void launch_begin(const char* name, cudaStream_t s);
+void launch_end(const char* name, cudaStream_t s);
+int num_sms();
+int device_cc_major();
+
+#define NVFP4_LAUNCH(name, stream, ...)            \
+    do {                                           \
+        ::nvfp4::launch_begin(name, stream);       \
+        __VA_ARGS__;                               \
+        ::nvfp4::launch_end(name, stream);         \
+    } while (0)
+
+inline nvfp4_status last_launch_status() {
+    return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Carves consecutive 256-byte-aligned regions out of a workspace.
+struct Carver {
+    char* base;
+    size_t off = 0;
+    explicit Carver(void* b) : base(static_cast<char*>(b)) {}
+    template <class T>
+    T* take(size_t count) {
+        off = align_up(off, 256);
+        T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+        off += count * sizeof(T);
+        return p;
+    }
+};
+
+// ---------------------------------------------------------------------------
+// device: number formats (inline PTX conversions of sm_100-family)
+// ---------------------------------------------------------------------------
+
+// fp32 -> e4m3 byte, round to nearest even, saturating to +-448.
+__device__ __forceinline__ uint32_t f32_to_e4m3(float v) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(v));
+    return r & 0xFFu;
+}
+
+// Two e4m3 bytes (low byte first) -> f16x2 (exact: every e4m3 value is an f16).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
+    uint32_t r;
+    uint16_t in = static_cast<uint16_t>(two_bytes);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(in));
+    return r;
+}
+
+__device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
+    uint32_t h2 = e4m3x2_to_f16x2(b & 0xFFu);
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
+}
+
+// Eight fp32 -> eight e2m1 codes (round to nearest even, saturating to +-6),
+// element i in bits [4i, 4i+4).  The sign bit of every input is kept in its
+// code, so a value that rounds to zero from below gives -0 (code 8).
+__device__ __forceinline__ uint32_t f32x8_to_e2m1x8(const float v[8]) {
+    uint32_t r;
+    asm("{\n"
+        ".reg .b8 b0, b1, b2, b3;\n"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n"
+        "mov.b32 %0, {b0, b1, b2, b3};\n"
+        "}"
+        : "=r"(r)
+        : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+    uint32_t sign = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sign |= (__float_as_uint(v[i]) >> 31) << (4 * i + 3);
+    return r | sign;
+}
+
+// Eight e2m1 codes (one 32-bit word, element 0 in the low nibble) -> four
+// f16x2 words, out[i] = (element 2i in the low half, element 2i+1 high).
+__device__ __forceinline__ void e2m1x8_to_f16x8(uint32_t w, uint32_t out[4]) {
+    asm("{\n"
+        ".reg .b8 b0, b1, b2, b3;\n"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n"
+        "}"
+        : "=r"(out[0]), "=r"(out[1]), "=r"(out[2]), "=r"(out[3])
+        : "r"(w));
+}
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+    __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+    return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// Broadcast the f16 in the low (hi=0) or high (hi=1) half to both halves.
+__device__ __forceinline__ uint32_t f16x2_bcast(uint32_t v, int hi) {
+    uint32_t h = hi ? (v >> 16) : (v & 0xFFFFu);
+    return h | (h << 16);
+}
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b16) { return __uint_as_float(b16 << 16); }
+
+__device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float v) {
+    __nv_bfloat16 b = __float2bfloat16_rn(v);
+    return *reinterpret_cast<uint16_t*>(&b);
+}
+
+__device__ __forceinline__ float round_bf16(float v) { return bf16_bits_to_f32(f32_to_bf16_bits(v)); }
+
+// 2^e as an fp32 (e in [-126, 127]).
+__device__ __forceinline__ float exp2i(int e) { return __uint_as_float(static_cast<uint32_t>(127 + e) << 23); }
+
+// Power-of-two exponent s for a row with max |x| = amax such that
+// amax * 2^-s lies in [2^14, 2^15): the row then fits f16 with its largest
+// element near the top of the f16 range.
+__device__ __forceinline__ int row_exponent(float amax) {
+    if (!(amax > 0.0f)) return 0;
+    int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF) - 127;
+    if (e < -126) e = -126;  // subnormal amax
+    int s = e - 14;
+    return s < -100 ? -100 : (s > 100 ? 100 : s);
+}
+
+// Warp-level mma: D(16x8 f32) += A(16x16 f16, row) * B(16x8 f16, col).
+__device__ __forceinline__ void mma_16816(float c[4], const uint32_t a[4], const uint32_t b[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Non-negative float atomic max through its bit pattern (monotone for >= 0).
+__device__ __forceinline__ void atomic_max_nonneg(float* addr, float v) {
+    atomicMax(reinterpret_cast<unsigned int*>(addr), __float_as_uint(v));
+}
+
+}  // namespace nvfp4

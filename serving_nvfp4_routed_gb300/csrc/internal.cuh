@@ -1,0 +1,80 @@
+// internal.cuh -- host-side launchers shared between the library's .cu files.
+#pragma once
+
+#include "common.cuh"
+
+namespace nvfp4 {
+
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 32;
+constexpr int kGemvTokTile = 8;  // tokens per work item of the decode-shaped kernel
+
+// Routing outputs plus the grouping metadata the expert kernels walk.
+struct RouteArrays {
+    int32_t* ids;          // [T*k]
+    float* w;              // [T*k]
+    int32_t* offsets;      // [E+1]
+    int32_t* row_to_slot;  // [R]
+    int32_t* slot_to_row;  // [R]
+    int32_t* active;       // [E]   experts with rows, ascending
+    int32_t* n_active;     // [1]
+    int32_t* tile_start;   // [E+1] prefix over active experts of ceil(rows / kGemvTokTile)
+    int32_t* counts;       // [n_blocks * E] scratch for the multi-block path
+};
+
+size_t route_scratch_words(int T, int E, int top_k);
+// logits != nullptr: top-k + permutation.  logits == nullptr: ids/w are
+// given; validates them (status) and builds the permutation.
+void launch_route(const float* logits, int T, int E, int top_k, RouteArrays ra, int32_t* d_status,
+                  cudaStream_t s);
+
+void launch_zero(void* p, size_t bytes, cudaStream_t s);
+void launch_quantize_act(const uint16_t* x, int M, int K, const int32_t* row_to_slot, int top_k,
+                         const float* input_scale, const int32_t* offsets, int E, uint8_t* codes,
+                         uint8_t* scales, cudaStream_t s);
+
+// ---- decode-shaped grouped GEMM (mma.sync, weights streamed from HBM) ----
+enum BMode { B_BF16 = 0, B_NVFP4 = 1 };
+enum OutMode { OUT_H = 0, OUT_HQ = 1, OUT_COMBINE = 2, OUT_BF16 = 3 };
+
+struct GemvArgs {
+    int K, N, top_k;
+    int nproj;                      // 2: gate+up (SwiGLU epilogue), 1: single projection
+    const int32_t* offsets;         // [E+1]
+    const int32_t* active;          // [E]
+    const int32_t* n_active;        // [1]
+    const int32_t* tile_start;      // [E+1]
+    const int32_t* row_to_slot;     // [R] (nullptr: row == token, top_k ignored)
+    const uint8_t* a_codes[2];      // [E, N, K/2]
+    const uint8_t* a_scales[2];     // [E, N, K/16]
+    const float* a_ws2[2];          // [E]
+    // B_BF16: bf16 rows with a per-row max |v| (row index = token when
+    // b_by_token, else the permuted row)
+    const uint16_t* b_bf16;
+    const float* b_amax;
+    int b_by_token;
+    // B_NVFP4: quantised permuted rows and the expert's input scale
+    const uint8_t* b_codes;
+    const uint8_t* b_scales;
+    const float* b_gs;              // [E]
+    // epilogue
+    uint16_t* h_out;                // OUT_H: [R, N] bf16
+    float* h_amax;                  // OUT_H: [R] running max |h| (zeroed before)
+    uint8_t* hq_out;                // OUT_HQ: [R, N/2]
+    uint8_t* hs_out;                // OUT_HQ: [R, N/16]
+    const float* hq_gs;             // OUT_HQ: [E] next input scale
+    float* acc_out;                 // OUT_COMBINE: [T, N] fp32 (zeroed before)
+    const float* topk_w;            // OUT_COMBINE: [T*k]
+    uint16_t* y_out;                // OUT_BF16: [R, N]
+    int* work_counter;              // zeroed before the launch
+};
+
+void launch_gemv(int bmode, int outmode, const GemvArgs& a, int max_work, cudaStream_t s);
+
+// prep for W4A16: per-token max |x|, zero the fp32 accumulator, the h
+// amax array and the work counters.
+void launch_moe_prep(const uint16_t* x, int T, int d, float* x_amax, float* acc, int R, float* h_amax,
+                     int* counters, int n_counters, cudaStream_t s);
+void launch_finalize(const float* acc, size_t n, uint16_t* out, cudaStream_t s);
+
+}  // namespace nvfp4

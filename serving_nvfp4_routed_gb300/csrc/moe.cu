@@ -1,0 +1,309 @@
+// moe.cu -- the routed-expert layer (W4A16 and W4A4) and the dense NVFP4
+// linear: host validation, workspace layout and the launch sequence.
+//
+// TensorFold issue #308 "GLM-5.3-Flash on CUDA: read nvidia/GLM-5.3-Flash-NVFP4
+// (ModelOpt NVFP4) as stored, W4A16": "What the branch does" (grouped routed
+// experts over bf16 rows with weight_scale_2 per expert; dense MLP with gate
+// and up apart; FP4 x FP4 as the checkpoint's own math) and "The checkpoint"
+// (static input_scale).  Launch sequence of one layer call:
+//   route (+ permutation) -> prep (x row max | act-quant) -> gate/up + SwiGLU
+//   -> down + weighted combine (fp32 red.add) -> bf16 finalize
+#include <climits>
+
+#include "common.cuh"
+#include "internal.cuh"
+
+namespace nvfp4 {
+
+namespace {
+
+constexpr int kCounters = 8;
+
+struct MoeWs {
+    RouteArrays ra;
+    float* x_amax;    // [T]        W4A16
+    uint16_t* h;      // [R, F]     W4A16
+    float* h_amax;    // [R]        W4A16
+    uint8_t* xq;      // [R, d/2]   W4A4
+    uint8_t* xs;      // [R, d/16]  W4A4
+    uint8_t* hq;      // [R, F/2]   W4A4
+    uint8_t* hs;      // [R, F/16]  W4A4
+    float* acc;       // [T, d]
+    int* counters;    // [kCounters]
+};
+
+MoeWs carve_moe(void* base, int T, int E, int k, int d, int F, int mode, size_t* bytes) {
+    Carver c(base);
+    const size_t R = (size_t)T * k;
+    MoeWs w{};
+    w.ra.ids = c.take<int32_t>(R + 1);
+    w.ra.w = c.take<float>(R + 1);
+    w.ra.offsets = c.take<int32_t>(E + 1);
+    w.ra.row_to_slot = c.take<int32_t>(R + 1);
+    w.ra.slot_to_row = c.take<int32_t>(R + 1);
+    w.ra.active = c.take<int32_t>(E);
+    w.ra.n_active = c.take<int32_t>(4);
+    w.ra.tile_start = c.take<int32_t>(E + 1);
+    w.ra.counts = c.take<int32_t>(route_scratch_words(T, E, k) + 1);
+    w.counters = c.take<int>(kCounters);
+    w.acc = c.take<float>((size_t)T * d);
+    if (mode == 0) {
+        w.x_amax = c.take<float>(T + 1);
+        w.h = c.take<uint16_t>(R * F);
+        w.h_amax = c.take<float>(R + 1);
+    } else {
+        w.xq = c.take<uint8_t>(R * (d / 2));
+        w.xs = c.take<uint8_t>(R * (d / 16));
+        w.hq = c.take<uint8_t>(R * (F / 2));
+        w.hs = c.take<uint8_t>(R * (F / 16));
+    }
+    if (bytes) *bytes = align_up(c.off, 256);
+    return w;
+}
+
+bool w_ok(const nvfp4_w& w) { return w.codes && w.scales && w.weight_scale_2; }
+bool w_aligned(const nvfp4_w& w) {
+    return aligned16(w.codes) && aligned16(w.scales) && aligned16(w.weight_scale_2);
+}
+
+nvfp4_status check_moe(const uint16_t* x, int T, int top_k, const nvfp4_moe_weights* w, const void* out,
+                       const void* ws, size_t ws_bytes, int mode) {
+    if (!w) return NVFP4_ERR_INVALID_ARG;
+    if (T < 0 || w->E < 1 || w->d < 1 || w->F < 1) return NVFP4_ERR_INVALID_ARG;
+    if (w->E > kMaxExperts || top_k < 1 || top_k > kMaxTopK || top_k > w->E) return NVFP4_ERR_SHAPE;
+    if (w->d % 64 != 0 || w->F % 64 != 0) return NVFP4_ERR_SHAPE;
+    if ((size_t)T * top_k > (size_t)INT_MAX / 2) return NVFP4_ERR_SHAPE;
+    if (T == 0) return NVFP4_OK;
+    if (!x || !out || !ws || !w_ok(w->gate) || !w_ok(w->up) || !w_ok(w->down)) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(out) || !aligned16(ws) || !w_aligned(w->gate) || !w_aligned(w->up) ||
+        !w_aligned(w->down))
+        return NVFP4_ERR_ALIGN;
+    if (ws_bytes < nvfp4_moe_workspace_size(T, w->E, top_k, w->d, w->F, mode)) return NVFP4_ERR_WORKSPACE;
+    return NVFP4_OK;
+}
+
+GemvArgs base_args(const MoeWs& ws, int top_k) {
+    GemvArgs a{};
+    a.top_k = top_k;
+    a.offsets = ws.ra.offsets;
+    a.active = ws.ra.active;
+    a.n_active = ws.ra.n_active;
+    a.tile_start = ws.ra.tile_start;
+    a.row_to_slot = ws.ra.row_to_slot;
+    a.topk_w = ws.ra.w;
+    return a;
+}
+
+int gemv_max_work(int R, int E, int N) {
+    long long tiles = (long long)(R + kGemvTokTile - 1) / kGemvTokTile + std::min(E, R);
+    long long w = tiles * (N / 16);
+    return (int)std::min<long long>(w, INT_MAX / 2);
+}
+
+nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, int top_k,
+                     const nvfp4_moe_weights* w, const float* is13, const float* is2, uint16_t* out, void* wsp,
+                     size_t ws_bytes, int32_t* d_status, cudaStream_t s) {
+    nvfp4_status st = check_moe(x, T, top_k, w, out, wsp, ws_bytes, mode);
+    if (st != NVFP4_OK || T == 0) return st;
+    if (mode == 1) {
+        if (!is13 || !is2) return NVFP4_ERR_INVALID_ARG;
+        if (!aligned16(is13) || !aligned16(is2)) return NVFP4_ERR_ALIGN;
+    }
+    if (d_status && !aligned16(d_status)) return NVFP4_ERR_ALIGN;
+    const int E = w->E, d = w->d, F = w->F, R = T * top_k;
+    MoeWs ws = carve_moe(wsp, T, E, top_k, d, F, mode, nullptr);
+
+    launch_route(logits, T, E, top_k, ws.ra, d_status, s);
+    launch_moe_prep(mode == 0 ? x : nullptr, T, d, ws.x_amax, ws.acc, top_k, ws.h_amax, ws.counters, kCounters,
+                    s);
+    if (mode == 1)
+        launch_quantize_act(x, R, d, ws.ra.row_to_slot, top_k, is13, ws.ra.offsets, E, ws.xq, ws.xs, s);
+
+    GemvArgs a = base_args(ws, top_k);
+    // gate/up + SwiGLU
+    a.K = d;
+    a.N = F;
+    a.nproj = 2;
+    a.a_codes[0] = w->gate.codes;  a.a_scales[0] = w->gate.scales;  a.a_ws2[0] = w->gate.weight_scale_2;
+    a.a_codes[1] = w->up.codes;    a.a_scales[1] = w->up.scales;    a.a_ws2[1] = w->up.weight_scale_2;
+    a.work_counter = ws.counters + 0;
+    if (mode == 0) {
+        a.b_bf16 = x;
+        a.b_amax = ws.x_amax;
+        a.b_by_token = 1;
+        a.h_out = ws.h;
+        a.h_amax = ws.h_amax;
+        launch_gemv(B_BF16, OUT_H, a, gemv_max_work(R, E, F), s);
+    } else {
+        a.b_codes = ws.xq;
+        a.b_scales = ws.xs;
+        a.b_gs = is13;
+        a.hq_out = ws.hq;
+        a.hs_out = ws.hs;
+        a.hq_gs = is2;
+        launch_gemv(B_NVFP4, OUT_HQ, a, gemv_max_work(R, E, F), s);
+    }
+    // down + weighted combine
+    GemvArgs b = base_args(ws, top_k);
+    b.K = F;
+    b.N = d;
+    b.nproj = 1;
+    b.a_codes[0] = w->down.codes;  b.a_scales[0] = w->down.scales;  b.a_ws2[0] = w->down.weight_scale_2;
+    b.a_codes[1] = w->down.codes;  b.a_scales[1] = w->down.scales;  b.a_ws2[1] = w->down.weight_scale_2;
+    b.work_counter = ws.counters + 1;
+    b.acc_out = ws.acc;
+    if (mode == 0) {
+        b.b_bf16 = ws.h;
+        b.b_amax = ws.h_amax;
+        b.b_by_token = 0;
+        launch_gemv(B_BF16, OUT_COMBINE, b, gemv_max_work(R, E, d), s);
+    } else {
+        b.b_codes = ws.hq;
+        b.b_scales = ws.hs;
+        b.b_gs = is2;
+        launch_gemv(B_NVFP4, OUT_COMBINE, b, gemv_max_work(R, E, d), s);
+    }
+    launch_finalize(ws.acc, (size_t)T * d, out, s);
+    return last_launch_status();
+}
+
+// ---- dense linear ----
+struct LinWs {
+    float* x_amax;     // [M]
+    int32_t* meta;     // offsets[2], active[1], n_active[1], tile_start[2]
+    int* counters;
+};
+
+LinWs carve_lin(void* base, int M, size_t* bytes) {
+    Carver c(base);
+    LinWs l;
+    l.x_amax = c.take<float>(M + 1);
+    l.meta = c.take<int32_t>(8);
+    l.counters = c.take<int>(kCounters);
+    if (bytes) *bytes = align_up(c.off, 256);
+    return l;
+}
+
+__global__ void linear_prep_kernel(const uint16_t* __restrict__ x, int M, int K, float* __restrict__ x_amax,
+                                   int32_t* meta, int* counters) {
+    const int m = blockIdx.x;
+    if (m == 0 && threadIdx.x == 0) {
+        meta[0] = 0;                                 // offsets[0]
+        meta[1] = M;                                 // offsets[1]
+        meta[2] = 0;                                 // active[0] = expert 0
+        meta[3] = 1;                                 // n_active
+        meta[4] = 0;                                 // tile_start[0]
+        meta[5] = (M + kGemvTokTile - 1) / kGemvTokTile;  // tile_start[1]
+    }
+    if (m == 0 && threadIdx.x < kCounters) counters[threadIdx.x] = 0;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)m * K);
+    float mx = 0.0f;
+    for (int i = threadIdx.x; i < K / 8; i += blockDim.x) {
+        uint4 u = __ldg(src + i);
+        uint32_t ww[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            mx = fmaxf(mx, fmaxf(fabsf(bf16_bits_to_f32(ww[j] & 0xFFFFu)), fabsf(bf16_bits_to_f32(ww[j] >> 16))));
+    }
+    mx = warp_max(mx);
+    __shared__ float red[32];
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.0f;
+        v = warp_max(v);
+        if (threadIdx.x == 0) x_amax[m] = v;
+    }
+}
+
+}  // namespace
+
+}  // namespace nvfp4
+
+using namespace nvfp4;
+
+extern "C" size_t nvfp4_moe_workspace_size(int T, int E, int top_k, int d, int F, int mode) {
+    if (T < 0 || E < 1 || top_k < 1 || d < 1 || F < 1 || (mode != 0 && mode != 1)) return 0;
+    size_t b = 0;
+    carve_moe(nullptr, T, E, top_k, d, F, mode, &b);
+    return b;
+}
+
+extern "C" nvfp4_status nvfp4_moe_workspace_views(void* ws, int T, int E, int top_k, int d, int F, int mode,
+                                                  int32_t** topk_ids, float** topk_w, int32_t** expert_offsets,
+                                                  int32_t** row_to_slot, int32_t** slot_to_row) {
+    if (!ws || T < 0 || E < 1 || top_k < 1 || d < 1 || F < 1 || (mode != 0 && mode != 1))
+        return NVFP4_ERR_INVALID_ARG;
+    MoeWs w = carve_moe(ws, T, E, top_k, d, F, mode, nullptr);
+    if (topk_ids) *topk_ids = w.ra.ids;
+    if (topk_w) *topk_w = w.ra.w;
+    if (expert_offsets) *expert_offsets = w.ra.offsets;
+    if (row_to_slot) *row_to_slot = w.ra.row_to_slot;
+    if (slot_to_row) *slot_to_row = w.ra.slot_to_row;
+    return NVFP4_OK;
+}
+
+extern "C" nvfp4_status nvfp4_moe_w4a16(const uint16_t* x, int T, const float* logits, int top_k,
+                                        const nvfp4_moe_weights* w, uint16_t* out, void* ws, size_t ws_bytes,
+                                        int32_t* d_status, cudaStream_t stream) {
+    return run_moe(0, x, T, logits, top_k, w, nullptr, nullptr, out, ws, ws_bytes, d_status, stream);
+}
+
+extern "C" nvfp4_status nvfp4_moe_w4a4(const uint16_t* x, int T, const float* logits, int top_k,
+                                       const nvfp4_moe_weights* w, const float* is13, const float* is2,
+                                       uint16_t* out, void* ws, size_t ws_bytes, int32_t* d_status,
+                                       cudaStream_t stream) {
+    return run_moe(1, x, T, logits, top_k, w, is13, is2, out, ws, ws_bytes, d_status, stream);
+}
+
+extern "C" size_t nvfp4_linear_workspace_size(int M, int K, int N) {
+    (void)K;
+    (void)N;
+    if (M < 0) return 0;
+    size_t b = 0;
+    carve_lin(nullptr, M, &b);
+    return b;
+}
+
+extern "C" nvfp4_status nvfp4_linear(const uint16_t* x, int M, int K, const nvfp4_w* w, int N,
+                                     const nvfp4_w* w_up, uint16_t* out, void* ws, size_t ws_bytes,
+                                     cudaStream_t stream) {
+    if (M < 0 || K < 1 || N < 1 || !w) return NVFP4_ERR_INVALID_ARG;
+    if (K % 64 != 0 || N % 16 != 0) return NVFP4_ERR_SHAPE;
+    if (M == 0) return NVFP4_OK;
+    if (!x || !out || !ws || !w_ok(*w) || (w_up && !w_ok(*w_up))) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(out) || !aligned16(ws) || !w_aligned(*w) || (w_up && !w_aligned(*w_up)))
+        return NVFP4_ERR_ALIGN;
+    if (ws_bytes < nvfp4_linear_workspace_size(M, K, N)) return NVFP4_ERR_WORKSPACE;
+    LinWs l = carve_lin(ws, M, nullptr);
+    NVFP4_LAUNCH("linear_prep", stream,
+                 linear_prep_kernel<<<M, 256, 0, stream>>>(x, M, K, l.x_amax, l.meta, l.counters));
+    GemvArgs a{};
+    a.K = K;
+    a.N = N;
+    a.top_k = 1;
+    a.offsets = l.meta + 0;
+    a.active = l.meta + 2;
+    a.n_active = l.meta + 3;
+    a.tile_start = l.meta + 4;
+    a.row_to_slot = nullptr;
+    a.a_codes[0] = w->codes;  a.a_scales[0] = w->scales;  a.a_ws2[0] = w->weight_scale_2;
+    a.a_codes[1] = w->codes;  a.a_scales[1] = w->scales;  a.a_ws2[1] = w->weight_scale_2;
+    a.b_bf16 = x;
+    a.b_amax = l.x_amax;
+    a.b_by_token = 1;
+    a.work_counter = l.counters;
+    const int max_work = gemv_max_work(M, 1, N);
+    if (w_up) {
+        a.nproj = 2;
+        a.a_codes[1] = w_up->codes;  a.a_scales[1] = w_up->scales;  a.a_ws2[1] = w_up->weight_scale_2;
+        a.h_out = out;
+        a.h_amax = nullptr;
+        launch_gemv(B_BF16, OUT_H, a, max_work, stream);
+    } else {
+        a.nproj = 1;
+        a.y_out = out;
+        launch_gemv(B_BF16, OUT_BF16, a, max_work, stream);
+    }
+    return last_launch_status();
+}

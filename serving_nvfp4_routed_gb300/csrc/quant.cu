@@ -1,0 +1,219 @@
+// quant.cu -- NVFP4 quantisation on the GPU: the ModelOpt weight recipe
+// (global amax pass, then block scales and codes) and static-scale
+// activation quantisation.
+//
+// Format: TensorFold issue #308, "GLM-5.3-Flash on CUDA: read
+// nvidia/GLM-5.3-Flash-NVFP4 (ModelOpt NVFP4) as stored, W4A16", section "The
+// checkpoint" (e2m1 codes, e4m3 scale per 16 inputs, fp32 weight_scale_2,
+// static input_scale); recipe: section "What the branch does" (experts
+// packed by ModelOpt's recipe at load, one projection at a time).
+//
+// Each thread owns 8 consecutive inputs (one 16-byte load of bf16); the two
+// threads of a 16-block exchange their partial block amax with one shuffle.
+// The scale arithmetic is IEEE fp32 round-to-nearest in the recipe's order:
+//   sf = (bam / 6) / gs;  s = e4m3_rn_sat(sf);  q = e2m1_rn_sat(v / (S * gs))
+// so that codes and scales are bit-identical to the format's definition.
+#include "common.cuh"
+#include "internal.cuh"
+
+namespace nvfp4 {
+
+__global__ void zero_words_kernel(uint32_t* p, size_t n) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+        p[i] = 0u;
+}
+
+void launch_zero(void* p, size_t bytes, cudaStream_t s) {
+    size_t n = bytes / 4;
+    if (n == 0) return;
+    int grid = (int)std::min<size_t>((n + 255) / 256, (size_t)num_sms() * 8);
+    NVFP4_LAUNCH("zero_words", s, zero_words_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<uint32_t*>(p), n));
+}
+
+// Per-tensor max |w| over `batch` tensors of n_per elements each.
+__global__ void tensor_amax_kernel(const uint16_t* __restrict__ w, size_t n_per, float* __restrict__ amax) {
+    const int b = blockIdx.y;
+    const uint4* src = reinterpret_cast<const uint4*>(w + (size_t)b * n_per);
+    const size_t n8 = n_per / 8;
+    float m = 0.0f;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
+        uint4 u = __ldg(src + i);
+        uint32_t ww[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            m = fmaxf(m, fabsf(bf16_bits_to_f32(ww[j] & 0xFFFFu)));
+            m = fmaxf(m, fabsf(bf16_bits_to_f32(ww[j] >> 16)));
+        }
+    }
+    m = warp_max(m);
+    __shared__ float red[32];
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        float v = threadIdx.x < blockDim.x / 32 ? red[threadIdx.x] : 0.0f;
+        v = warp_max(v);
+        if (threadIdx.x == 0) atomic_max_nonneg(amax + b, v);
+    }
+}
+
+// Block quantisation of 8 values held by this thread, given the 16-block's
+// amax and the tensor scale gs.  Returns the 8 packed codes and the scale byte.
+__device__ __forceinline__ void quant_half_block(const float v[8], float bam, float gs, uint32_t& codes,
+                                                 uint32_t& sbyte) {
+    sbyte = 0u;
+    codes = 0u;
+    if (gs > 0.0f) {
+        float sf = __fdiv_rn(__fdiv_rn(bam, 6.0f), gs);
+        sbyte = f32_to_e4m3(sf);
+        float S = e4m3_to_f32(sbyte);
+        if (S != 0.0f) {
+            float denom = __fmul_rn(S, gs);
+            float q[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) q[i] = __fdiv_rn(v[i], denom);
+            codes = f32x8_to_e2m1x8(q);
+        }
+    }
+}
+
+__device__ __forceinline__ void load_bf16x8(const uint16_t* p, float v[8], float& amax) {
+    uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+    uint32_t ww[4] = {u.x, u.y, u.z, u.w};
+    amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        v[2 * j] = bf16_bits_to_f32(ww[j] & 0xFFFFu);
+        v[2 * j + 1] = bf16_bits_to_f32(ww[j] >> 16);
+        amax = fmaxf(amax, fmaxf(fabsf(v[2 * j]), fabsf(v[2 * j + 1])));
+    }
+}
+
+__global__ void quantize_weights_kernel(const uint16_t* __restrict__ w, size_t n_per, int batch,
+                                        const float* __restrict__ amax, uint8_t* __restrict__ codes,
+                                        uint8_t* __restrict__ scales, float* __restrict__ ws2_out) {
+    const size_t halves_per = n_per / 8;
+    const size_t total = halves_per * (size_t)batch;
+    // warp-uniform trip count (the pair shuffle needs every lane); lanes past
+    // the end recompute element 0 and store nothing
+    for (size_t base = blockIdx.x * (size_t)blockDim.x + (threadIdx.x & ~31u); base < total;
+         base += (size_t)gridDim.x * blockDim.x) {
+        const size_t i = base + (threadIdx.x & 31);
+        const bool live = i < total;
+        const size_t ii = live ? i : 0;
+        const int b = (int)(ii / halves_per);
+        const float gs = __fdiv_rn(amax[b], 2688.0f);
+        float v[8], m;
+        load_bf16x8(w + ii * 8, v, m);
+        float bam = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        uint32_t c, s;
+        quant_half_block(v, bam, gs, c, s);
+        if (live) {
+            reinterpret_cast<uint32_t*>(codes)[ii] = c;
+            if ((ii & 1) == 0) scales[ii / 2] = (uint8_t)s;
+            if (ii - (size_t)b * halves_per == 0) ws2_out[b] = gs;
+        }
+    }
+}
+
+// Output row r quantises source row src(r) with the input scale of the
+// expert whose row range holds r.
+__global__ void quantize_act_kernel(const uint16_t* __restrict__ x, int M, int K,
+                                    const int32_t* __restrict__ row_to_slot, int top_k,
+                                    const float* __restrict__ input_scale,
+                                    const int32_t* __restrict__ offsets, int E,
+                                    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+    const int halves_per_row = K / 8;
+    const size_t total = (size_t)M * halves_per_row;
+    for (size_t base = blockIdx.x * (size_t)blockDim.x + (threadIdx.x & ~31u); base < total;
+         base += (size_t)gridDim.x * blockDim.x) {
+        const size_t i = base + (threadIdx.x & 31);
+        const bool live = i < total;
+        const size_t ii = live ? i : 0;
+        const int r = (int)(ii / halves_per_row);
+        const int part = (int)(ii % halves_per_row);
+        const int src = row_to_slot ? row_to_slot[r] / top_k : r;
+        float gs;
+        if (offsets) {
+            int lo = 0, hi = E;  // find e with offsets[e] <= r < offsets[e+1]
+            while (hi - lo > 1) {
+                int mid = (lo + hi) >> 1;
+                if (offsets[mid] <= r) lo = mid; else hi = mid;
+            }
+            gs = input_scale[lo];
+        } else {
+            gs = input_scale[0];
+        }
+        float v[8], m;
+        load_bf16x8(x + (size_t)src * K + (size_t)part * 8, v, m);
+        float bam = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        uint32_t c, s;
+        quant_half_block(v, bam, gs, c, s);
+        if (live) {
+            reinterpret_cast<uint32_t*>(codes)[ii] = c;
+            if ((ii & 1) == 0) scales[ii / 2] = (uint8_t)s;
+        }
+    }
+}
+
+void launch_quantize_act(const uint16_t* x, int M, int K, const int32_t* row_to_slot, int top_k,
+                         const float* input_scale, const int32_t* offsets, int E, uint8_t* codes,
+                         uint8_t* scales, cudaStream_t s) {
+    size_t total = (size_t)M * (K / 8);
+    if (total == 0) return;
+    int grid = (int)std::min<size_t>((total + 255) / 256, (size_t)num_sms() * 16);
+    NVFP4_LAUNCH("quantize_act", s,
+                 quantize_act_kernel<<<grid, 256, 0, s>>>(x, M, K, row_to_slot, top_k, input_scale,
+                                                          offsets, E, codes, scales));
+}
+
+}  // namespace nvfp4
+
+using namespace nvfp4;
+
+extern "C" size_t nvfp4_quantize_weights_workspace_size(int batch, int N, int K) {
+    (void)N;
+    (void)K;
+    return align_up((size_t)(batch > 0 ? batch : 0) * sizeof(float), 256);
+}
+
+extern "C" nvfp4_status nvfp4_quantize_weights(const uint16_t* w, int batch, int N, int K, uint8_t* codes,
+                                               uint8_t* scales, float* weight_scale_2, void* ws,
+                                               size_t ws_bytes, cudaStream_t stream) {
+    if (batch < 0 || N < 0 || K < 0) return NVFP4_ERR_INVALID_ARG;
+    if (K % 16 != 0) return NVFP4_ERR_SHAPE;
+    if ((size_t)batch * N * K == 0) return NVFP4_OK;
+    if (!w || !codes || !scales || !weight_scale_2 || !ws) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned16(w) || !aligned16(codes) || !aligned16(scales) || !aligned16(weight_scale_2) ||
+        !aligned16(ws))
+        return NVFP4_ERR_ALIGN;
+    if (ws_bytes < nvfp4_quantize_weights_workspace_size(batch, N, K)) return NVFP4_ERR_WORKSPACE;
+    float* amax = static_cast<float*>(ws);
+    launch_zero(amax, sizeof(float) * batch, stream);
+    const size_t n_per = (size_t)N * K;
+    int gx = (int)std::max<size_t>(1, std::min<size_t>((n_per / 8 + 255) / 256, (size_t)num_sms() * 8 / std::max(1, batch) + 1));
+    NVFP4_LAUNCH("tensor_amax", stream,
+                 tensor_amax_kernel<<<dim3(gx, batch), 256, 0, stream>>>(w, n_per, amax));
+    size_t total = n_per / 8 * batch;
+    int grid = (int)std::min<size_t>((total + 255) / 256, (size_t)num_sms() * 16);
+    NVFP4_LAUNCH("quantize_weights", stream,
+                 quantize_weights_kernel<<<grid, 256, 0, stream>>>(w, n_per, batch, amax, codes, scales,
+                                                                   weight_scale_2));
+    return last_launch_status();
+}
+
+extern "C" nvfp4_status nvfp4_quantize_act(const uint16_t* x, int M, int K, const int32_t* row_to_slot,
+                                           int top_k, const float* input_scale,
+                                           const int32_t* expert_offsets, int E, uint8_t* codes,
+                                           uint8_t* scales, cudaStream_t stream) {
+    if (M < 0 || K < 0) return NVFP4_ERR_INVALID_ARG;
+    if (K % 16 != 0) return NVFP4_ERR_SHAPE;
+    if (M == 0 || K == 0) return NVFP4_OK;
+    if (!x || !input_scale || !codes || !scales) return NVFP4_ERR_INVALID_ARG;
+    if (row_to_slot && top_k < 1) return NVFP4_ERR_INVALID_ARG;
+    if (expert_offsets && (E < 1 || E > 1024)) return NVFP4_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(codes) || !aligned16(scales) || !aligned16(input_scale) ||
+        (row_to_slot && !aligned16(row_to_slot)) || (expert_offsets && !aligned16(expert_offsets)))
+        return NVFP4_ERR_ALIGN;
+    launch_quantize_act(x, M, K, row_to_slot, top_k, input_scale, expert_offsets, E, codes, scales, stream);
+    return last_launch_status();
+}

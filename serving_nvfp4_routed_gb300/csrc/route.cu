@@ -1,0 +1,329 @@
+// route.cu -- router logits -> top-k experts -> expert-contiguous rows.
+//
+// TensorFold issue #308 "GLM-5.3-Flash on CUDA: read nvidia/GLM-5.3-Flash-NVFP4
+// (ModelOpt NVFP4) as stored, W4A16", "The checkpoint": the router is BF16
+// (its fp32 logits are this file's input); "What the branch does": the routed
+// experts run through one grouped kernel, which needs each expert's rows
+// contiguous.  Router function (softmax, top-k with ties to the lower id,
+// weights renormalised over the k chosen) is the plain reading.
+//
+// Top-k: one warp per token, logits in registers, k rounds of a warp arg-max.
+// Weights: exp(l - l_max) / sum over the k, in fp64 (so they match an fp64
+// evaluation to the last fp32 bit).
+// Permutation (stable: expert, token, slot): a per-expert histogram, a
+// warp-scan exclusive prefix sum, and a scatter in which each row's position
+// is its expert's base + the count of equal experts before it -- within a warp
+// by __match_any_sync, across warps by per-warp counts in shared memory.  No
+// atomic decides an order, so the result is deterministic.
+#include <climits>
+
+#include "common.cuh"
+#include "internal.cuh"
+
+namespace nvfp4 {
+
+namespace {
+
+constexpr int kRoundRows = 1024;   // rows per scatter round (one per thread)
+constexpr int kSmallMaxRows = 8192;
+constexpr int kChunkRows = 8192;   // rows per block in the multi-block path
+
+template <int MAXL>
+__device__ void warp_topk(const float* __restrict__ lg, int E, int k, int32_t* __restrict__ ids,
+                          float* __restrict__ w) {
+    const int lane = threadIdx.x & 31;
+    float v[MAXL];
+    uint32_t taken = 0;
+#pragma unroll
+    for (int i = 0; i < MAXL; ++i) {
+        const int e = lane + 32 * i;
+        float x = e < E ? lg[e] : -INFINITY;
+        v[i] = (x != x) ? -INFINITY : x;  // NaN never ranks above a number
+        if (e >= E) taken |= 1u << i;
+    }
+    float my_v = 0.0f;
+    int my_id = 0;
+    for (int j = 0; j < k; ++j) {
+        float bv = -INFINITY;
+        int bi = INT_MAX;
+#pragma unroll
+        for (int i = 0; i < MAXL; ++i) {
+            const int e = lane + 32 * i;
+            if (!((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
+                bv = v[i];
+                bi = e;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (ov > bv || (ov == bv && oi < bi)) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        if (lane == j) {
+            my_v = bv;
+            my_id = bi;
+        }
+    }
+    const double m = (double)__shfl_sync(0xffffffffu, my_v, 0);
+    const double ex = lane < k ? exp((double)my_v - m) : 0.0;
+    double sum = 0.0;
+    for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, ex, j);
+    if (lane < k) {
+        ids[lane] = my_id;
+        w[lane] = (float)(ex / sum);
+    }
+}
+
+__device__ void topk_dispatch(const float* lg, int E, int k, int32_t* ids, float* w) {
+    if (E <= 64) warp_topk<2>(lg, E, k, ids, w);
+    else if (E <= 128) warp_topk<4>(lg, E, k, ids, w);
+    else if (E <= 320) warp_topk<10>(lg, E, k, ids, w);
+    else if (E <= 512) warp_topk<16>(lg, E, k, ids, w);
+    else warp_topk<32>(lg, E, k, ids, w);
+}
+
+// Exclusive scan of one int per thread over the block (blockDim multiple of 32).
+__device__ int block_exclusive_scan(int v, int* tmp32, int& total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) tmp32[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int s = lane < nw ? tmp32[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += y;
+        }
+        tmp32[lane] = s;
+    }
+    __syncthreads();
+    const int prefix = (warp > 0 ? tmp32[warp - 1] : 0) + x - v;
+    total = tmp32[nw - 1];
+    __syncthreads();
+    return prefix;
+}
+
+// offsets / active list / gemv tile prefix from per-expert counts c (thread e
+// holds expert e; blockDim >= E).
+__device__ void write_group_meta(int c, int E, const RouteArrays& ra, int* tmp32, int& off_out) {
+    const int e = threadIdx.x;
+    int total;
+    const int off = block_exclusive_scan(e < E ? c : 0, tmp32, total);
+    if (e < E) ra.offsets[e] = off;
+    if (e == 0) ra.offsets[E] = total;
+    const int flag = (e < E && c > 0) ? 1 : 0;
+    int na;
+    const int aidx = block_exclusive_scan(flag, tmp32, na);
+    const int tiles = flag ? (c + kGemvTokTile - 1) / kGemvTokTile : 0;
+    int tt;
+    const int tpre = block_exclusive_scan(tiles, tmp32, tt);
+    if (flag) {
+        ra.active[aidx] = e;
+        ra.tile_start[aidx] = tpre;
+    }
+    if (e == 0) {
+        *ra.n_active = na;
+        ra.tile_start[na] = tt;
+    }
+    off_out = off;
+}
+
+// Scatter rows [row0, row1) in rounds of blockDim rows; run[e] holds the next
+// free position of expert e (shared), wh is [32][E] per-warp round counts.
+__device__ void scatter_rows(int row0, int row1, int E, const int32_t* __restrict__ ids, int* run,
+                             uint8_t* wh, const RouteArrays& ra) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    for (int base = row0; base < row1; base += blockDim.x) {
+        const int r = base + threadIdx.x;
+        const int e = r < row1 ? ids[r] : -1;
+        const unsigned mask = __match_any_sync(0xffffffffu, e);
+        const int rank = __popc(mask & ((1u << lane) - 1u));
+        if (e >= 0 && rank == 0) wh[warp * E + e] = (uint8_t)__popc(mask);
+        __syncthreads();
+        if (e >= 0) {
+            int pos = run[e] + rank;
+            for (int w2 = 0; w2 < warp; ++w2) pos += wh[w2 * E + e];
+            ra.row_to_slot[pos] = r;
+            ra.slot_to_row[r] = pos;
+        }
+        __syncthreads();
+        for (int e2 = threadIdx.x; e2 < E; e2 += blockDim.x) {
+            int s = 0;
+            for (int w2 = 0; w2 < nw; ++w2) {
+                s += wh[w2 * E + e2];
+                wh[w2 * E + e2] = 0;
+            }
+            run[e2] += s;
+        }
+        __syncthreads();
+    }
+}
+
+// ids given by the caller: report and clamp out-of-range ids (so no later
+// kernel indexes out of bounds).
+__device__ void validate_ids(int32_t* ids, int R, int E, int32_t* status) {
+    for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < R; r += gridDim.x * blockDim.x) {
+        int e = ids[r];
+        if (e < 0 || e >= E) {
+            ids[r] = 0;
+            if (status) atomicExch(status, (int)NVFP4_ERR_DEVICE_INPUT);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(1024) route_small_kernel(const float* __restrict__ logits, int T, int E,
+                                                           int k, RouteArrays ra, int32_t* status) {
+    __shared__ int run[kMaxExperts];
+    __shared__ uint8_t wh[32 * kMaxExperts];
+    __shared__ int tmp32[32];
+    const int R = T * k;
+    const int warp = threadIdx.x >> 5;
+    if (logits) {
+        for (int t = warp; t < T; t += blockDim.x >> 5)
+            topk_dispatch(logits + (size_t)t * E, E, k, ra.ids + (size_t)t * k, ra.w + (size_t)t * k);
+    } else {
+        validate_ids(ra.ids, R, E, status);
+    }
+    for (int i = threadIdx.x; i < E; i += blockDim.x) run[i] = 0;
+    for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) wh[i] = 0;
+    __syncthreads();
+    for (int r = threadIdx.x; r < R; r += blockDim.x) atomicAdd(&run[ra.ids[r]], 1);
+    __syncthreads();
+    const int c = threadIdx.x < E ? run[threadIdx.x] : 0;
+    int off;
+    write_group_meta(c, E, ra, tmp32, off);
+    if (threadIdx.x < E) run[threadIdx.x] = off;
+    __syncthreads();
+    scatter_rows(0, R, E, ra.ids, run, wh, ra);
+}
+
+__global__ void topk_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* ids, float* w) {
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t < T) topk_dispatch(logits + (size_t)t * E, E, k, ids + (size_t)t * k, w + (size_t)t * k);
+}
+
+__global__ void validate_ids_kernel(int32_t* ids, int R, int E, int32_t* status) {
+    validate_ids(ids, R, E, status);
+}
+
+__global__ void __launch_bounds__(1024) perm_count_kernel(const int32_t* __restrict__ ids, int R, int E,
+                                                          int32_t* counts) {
+    __shared__ int hist[kMaxExperts];
+    for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    const int r0 = blockIdx.x * kChunkRows, r1 = min(R, r0 + kChunkRows);
+    for (int r = r0 + threadIdx.x; r < r1; r += blockDim.x) atomicAdd(&hist[ids[r]], 1);
+    __syncthreads();
+    for (int i = threadIdx.x; i < E; i += blockDim.x) counts[(size_t)blockIdx.x * E + i] = hist[i];
+}
+
+__global__ void __launch_bounds__(1024) perm_scan_kernel(int nb, int E, int32_t* counts, RouteArrays ra) {
+    __shared__ int tmp32[32];
+    const int e = threadIdx.x;
+    int run = 0;
+    if (e < E) {
+        for (int b = 0; b < nb; ++b) {
+            int c = counts[(size_t)b * E + e];
+            counts[(size_t)b * E + e] = run;
+            run += c;
+        }
+    }
+    int off;
+    write_group_meta(run, E, ra, tmp32, off);
+    if (e < E)
+        for (int b = 0; b < nb; ++b) counts[(size_t)b * E + e] += off;
+}
+
+__global__ void __launch_bounds__(1024) perm_scatter_kernel(int R, int E, const int32_t* __restrict__ counts,
+                                                            RouteArrays ra) {
+    __shared__ int run[kMaxExperts];
+    __shared__ uint8_t wh[32 * kMaxExperts];
+    for (int i = threadIdx.x; i < E; i += blockDim.x) run[i] = counts[(size_t)blockIdx.x * E + i];
+    for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) wh[i] = 0;
+    __syncthreads();
+    const int r0 = blockIdx.x * kChunkRows, r1 = min(R, r0 + kChunkRows);
+    scatter_rows(r0, r1, E, ra.ids, run, wh, ra);
+}
+
+}  // namespace
+
+size_t route_scratch_words(int T, int E, int top_k) {
+    size_t R = (size_t)T * top_k;
+    size_t nb = (R + kChunkRows - 1) / kChunkRows;
+    return nb * (size_t)E;
+}
+
+void launch_route(const float* logits, int T, int E, int k, RouteArrays ra, int32_t* d_status, cudaStream_t s) {
+    const int R = T * k;
+    if (R <= kSmallMaxRows) {
+        NVFP4_LAUNCH("route_small", s, route_small_kernel<<<1, 1024, 0, s>>>(logits, T, E, k, ra, d_status));
+        return;
+    }
+    if (logits) {
+        NVFP4_LAUNCH("route_topk", s,
+                     topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(logits, T, E, k, ra.ids, ra.w));
+    } else {
+        NVFP4_LAUNCH("route_validate", s,
+                     validate_ids_kernel<<<(R + 255) / 256, 256, 0, s>>>(ra.ids, R, E, d_status));
+    }
+    const int nb = (R + kChunkRows - 1) / kChunkRows;
+    NVFP4_LAUNCH("route_count", s, perm_count_kernel<<<nb, 1024, 0, s>>>(ra.ids, R, E, ra.counts));
+    NVFP4_LAUNCH("route_scan", s, perm_scan_kernel<<<1, 1024, 0, s>>>(nb, E, ra.counts, ra));
+    NVFP4_LAUNCH("route_scatter", s, perm_scatter_kernel<<<nb, 1024, 0, s>>>(R, E, ra.counts, ra));
+}
+
+// Route workspace layout (shared with the MoE workspace's routing block).
+struct RouteWs {
+    int32_t *active, *n_active, *tile_start, *counts;
+};
+static RouteWs carve_route_ws(Carver& c, int T, int E, int k) {
+    RouteWs r;
+    r.active = c.take<int32_t>(E);
+    r.n_active = c.take<int32_t>(4);
+    r.tile_start = c.take<int32_t>(E + 1);
+    r.counts = c.take<int32_t>(route_scratch_words(T, E, k) + 1);
+    return r;
+}
+
+}  // namespace nvfp4
+
+using namespace nvfp4;
+
+extern "C" size_t moe_route_permute_workspace_size(int T, int E, int top_k) {
+    if (T < 0 || E < 1 || top_k < 1) return 0;
+    Carver c(nullptr);
+    carve_route_ws(c, T, E, top_k);
+    return align_up(c.off, 256);
+}
+
+extern "C" nvfp4_status moe_route_permute(const float* logits, int T, int E, int top_k, int32_t* topk_ids,
+                                          float* topk_w, int32_t* expert_offsets, int32_t* row_to_slot,
+                                          int32_t* slot_to_row, void* ws, size_t ws_bytes,
+                                          cudaStream_t stream) {
+    if (T < 0) return NVFP4_ERR_INVALID_ARG;
+    if (E < 1 || E > kMaxExperts || top_k < 1 || top_k > kMaxTopK || top_k > E) return NVFP4_ERR_SHAPE;
+    if ((size_t)T * top_k > (size_t)INT_MAX / 2) return NVFP4_ERR_SHAPE;
+    if (!logits || !topk_ids || !topk_w || !expert_offsets || !row_to_slot || !slot_to_row || !ws)
+        return NVFP4_ERR_INVALID_ARG;
+    if (!aligned16(logits) || !aligned16(topk_ids) || !aligned16(topk_w) || !aligned16(expert_offsets) ||
+        !aligned16(row_to_slot) || !aligned16(slot_to_row) || !aligned16(ws))
+        return NVFP4_ERR_ALIGN;
+    if (ws_bytes < moe_route_permute_workspace_size(T, E, top_k)) return NVFP4_ERR_WORKSPACE;
+    Carver c(ws);
+    RouteWs rw = carve_route_ws(c, T, E, top_k);
+    RouteArrays ra{topk_ids, topk_w, expert_offsets, row_to_slot, slot_to_row,
+                   rw.active, rw.n_active, rw.tile_start, rw.counts};
+    launch_route(logits, T, E, top_k, ra, nullptr, stream);
+    return last_launch_status();
+}
