@@ -1,5 +1,6 @@
 // api_common.cu -- status strings, launch accounting and optional per-kernel
 // event timing for libnvfp4moe.
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -61,6 +62,15 @@ void launch_end(const char* name, cudaStream_t s) {
         g_pending.push_back({name, g_open, stop});
         g_open = nullptr;
     }
+}
+
+bool pdl_enabled() {
+    static int v = -1;
+    if (v < 0) {
+        const char* e = std::getenv("NVFP4_NO_PDL");
+        v = (e && e[0] && e[0] != '0') ? 0 : 1;
+    }
+    return v == 1;
 }
 
 int num_sms() {

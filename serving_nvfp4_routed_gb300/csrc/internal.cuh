@@ -20,6 +20,8 @@ struct RouteArrays {
     int32_t* n_active;     // [1]
     int32_t* tile_start;   // [E+1] prefix over active experts of ceil(rows / kGemvTokTile)
     int32_t* counts;       // [n_blocks * E] scratch for the multi-block path
+    int32_t* clear;        // [n_clear] zeroed by the route launch (work and completion counters)
+    int n_clear;
 };
 
 size_t route_scratch_words(int T, int E, int top_k);
@@ -40,6 +42,7 @@ enum OutMode { OUT_H = 0, OUT_HQ = 1, OUT_COMBINE = 2, OUT_BF16 = 3 };
 struct GemvArgs {
     int K, N, top_k;
     int nproj;                      // 2: gate+up (SwiGLU epilogue), 1: single projection
+    int ksplit;                     // warps of a CTA splitting K (1, 2, 4 or 8)
     const int32_t* offsets;         // [E+1]
     const int32_t* active;          // [E]
     const int32_t* n_active;        // [1]
@@ -48,10 +51,9 @@ struct GemvArgs {
     const uint8_t* a_codes[2];      // [E, N, K/2]
     const uint8_t* a_scales[2];     // [E, N, K/16]
     const float* a_ws2[2];          // [E]
-    // B_BF16: bf16 rows with a per-row max |v| (row index = token when
-    // b_by_token, else the permuted row)
+    // B_BF16: bf16 rows (row index = token when b_by_token, else the permuted
+    // row); each CTA takes a row's max |v| while staging it
     const uint16_t* b_bf16;
-    const float* b_amax;
     int b_by_token;
     // B_NVFP4: quantised permuted rows and the expert's input scale
     const uint8_t* b_codes;
@@ -59,22 +61,25 @@ struct GemvArgs {
     const float* b_gs;              // [E]
     // epilogue
     uint16_t* h_out;                // OUT_H: [R, N] bf16
-    float* h_amax;                  // OUT_H: [R] running max |h| (zeroed before)
     uint8_t* hq_out;                // OUT_HQ: [R, N/2]
     uint8_t* hs_out;                // OUT_HQ: [R, N/16]
     const float* hq_gs;             // OUT_HQ: [E] next input scale
-    float* acc_out;                 // OUT_COMBINE: [T, N] fp32 (zeroed before)
+    float* acc_out;                 // OUT_COMBINE: [T, N] fp32 (zeroed by the gate/up launch)
     const float* topk_w;            // OUT_COMBINE: [T*k]
+    int* tok_done;                  // OUT_COMBINE: [T] completed contributions (zeroed before)
+    int done_target;                // OUT_COMBINE: contributions per token
+    uint16_t* out_bf16;             // OUT_COMBINE: [T, N] final bf16 rows
     uint16_t* y_out;                // OUT_BF16: [R, N]
+    float* zero_buf;                // zeroed (grid-stride) at kernel start, may be null
+    size_t zero_words;
     int* work_counter;              // zeroed before the launch
 };
 
+// ksplit chosen from the expected number of work items
+int gemv_pick_ksplit(int expected_tiles, int N, int nproj);
+size_t gemv_smem_bytes(int K);
+bool gemv_supported_k(int K);
 void launch_gemv(int bmode, int outmode, const GemvArgs& a, int max_work, cudaStream_t s);
 
-// prep for W4A16: per-token max |x|, zero the fp32 accumulator, the h
-// amax array and the work counters.
-void launch_moe_prep(const uint16_t* x, int T, int d, float* x_amax, float* acc, int R, float* h_amax,
-                     int* counters, int n_counters, cudaStream_t s);
-void launch_finalize(const float* acc, size_t n, uint16_t* out, cudaStream_t s);
-
+// W4A16 prep and the counters the kernels use are zeroed by the route launch.
 }  // namespace nvfp4

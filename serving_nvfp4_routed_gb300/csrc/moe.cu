@@ -6,8 +6,11 @@
 // experts over bf16 rows with weight_scale_2 per expert; dense MLP with gate
 // and up apart; FP4 x FP4 as the checkpoint's own math) and "The checkpoint"
 // (static input_scale).  Launch sequence of one layer call:
-//   route (+ permutation) -> prep (x row max | act-quant) -> gate/up + SwiGLU
-//   -> down + weighted combine (fp32 red.add) -> bf16 finalize
+//   route + permutation (also clears the counters)
+//   [W4A4: static-scale act-quant of the permuted rows]
+//   gate/up + SwiGLU (also zeroes the fp32 combine accumulator)
+//   down + weighted combine (fp32 red.add); the CTA that adds a token's last
+//   contribution writes that token's bf16 output row
 #include <climits>
 
 #include "common.cuh"
@@ -21,15 +24,13 @@ constexpr int kCounters = 8;
 
 struct MoeWs {
     RouteArrays ra;
-    float* x_amax;    // [T]        W4A16
     uint16_t* h;      // [R, F]     W4A16
-    float* h_amax;    // [R]        W4A16
     uint8_t* xq;      // [R, d/2]   W4A4
     uint8_t* xs;      // [R, d/16]  W4A4
     uint8_t* hq;      // [R, F/2]   W4A4
     uint8_t* hs;      // [R, F/16]  W4A4
     float* acc;       // [T, d]
-    int* counters;    // [kCounters]
+    int* clear;       // [kCounters + T]: work counters, then per-token completion counts
 };
 
 MoeWs carve_moe(void* base, int T, int E, int k, int d, int F, int mode, size_t* bytes) {
@@ -45,12 +46,12 @@ MoeWs carve_moe(void* base, int T, int E, int k, int d, int F, int mode, size_t*
     w.ra.n_active = c.take<int32_t>(4);
     w.ra.tile_start = c.take<int32_t>(E + 1);
     w.ra.counts = c.take<int32_t>(route_scratch_words(T, E, k) + 1);
-    w.counters = c.take<int>(kCounters);
+    w.clear = c.take<int>(kCounters + (size_t)T);
+    w.ra.clear = w.clear;
+    w.ra.n_clear = kCounters + T;
     w.acc = c.take<float>((size_t)T * d);
     if (mode == 0) {
-        w.x_amax = c.take<float>(T + 1);
         w.h = c.take<uint16_t>(R * F);
-        w.h_amax = c.take<float>(R + 1);
     } else {
         w.xq = c.take<uint8_t>(R * (d / 2));
         w.xs = c.take<uint8_t>(R * (d / 16));
@@ -71,7 +72,8 @@ nvfp4_status check_moe(const uint16_t* x, int T, int top_k, const nvfp4_moe_weig
     if (!w) return NVFP4_ERR_INVALID_ARG;
     if (T < 0 || w->E < 1 || w->d < 1 || w->F < 1) return NVFP4_ERR_INVALID_ARG;
     if (w->E > kMaxExperts || top_k < 1 || top_k > kMaxTopK || top_k > w->E) return NVFP4_ERR_SHAPE;
-    if (w->d % 64 != 0 || w->F % 64 != 0) return NVFP4_ERR_SHAPE;
+    if (w->d % 64 != 0 || w->F % 64 != 0 || !gemv_supported_k(w->d) || !gemv_supported_k(w->F))
+        return NVFP4_ERR_SHAPE;
     if ((size_t)T * top_k > (size_t)INT_MAX / 2) return NVFP4_ERR_SHAPE;
     if (T == 0) return NVFP4_OK;
     if (!x || !out || !ws || !w_ok(w->gate) || !w_ok(w->up) || !w_ok(w->down)) return NVFP4_ERR_INVALID_ARG;
@@ -100,6 +102,8 @@ int gemv_max_work(int R, int E, int N) {
     return (int)std::min<long long>(w, INT_MAX / 2);
 }
 
+int expected_tiles(int R, int E) { return std::max(std::min(E, R), R / kGemvTokTile); }
+
 nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, int top_k,
                      const nvfp4_moe_weights* w, const float* is13, const float* is2, uint16_t* out, void* wsp,
                      size_t ws_bytes, int32_t* d_status, cudaStream_t s) {
@@ -114,25 +118,25 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
     MoeWs ws = carve_moe(wsp, T, E, top_k, d, F, mode, nullptr);
 
     launch_route(logits, T, E, top_k, ws.ra, d_status, s);
-    launch_moe_prep(mode == 0 ? x : nullptr, T, d, ws.x_amax, ws.acc, top_k, ws.h_amax, ws.counters, kCounters,
-                    s);
     if (mode == 1)
         launch_quantize_act(x, R, d, ws.ra.row_to_slot, top_k, is13, ws.ra.offsets, E, ws.xq, ws.xs, s);
 
+    const int tiles = expected_tiles(R, E);
     GemvArgs a = base_args(ws, top_k);
-    // gate/up + SwiGLU
+    // gate/up + SwiGLU (also zeroes the fp32 combine accumulator)
     a.K = d;
     a.N = F;
     a.nproj = 2;
+    a.ksplit = gemv_pick_ksplit(tiles, F, 2);
     a.a_codes[0] = w->gate.codes;  a.a_scales[0] = w->gate.scales;  a.a_ws2[0] = w->gate.weight_scale_2;
     a.a_codes[1] = w->up.codes;    a.a_scales[1] = w->up.scales;    a.a_ws2[1] = w->up.weight_scale_2;
-    a.work_counter = ws.counters + 0;
+    a.work_counter = ws.clear + 0;
+    a.zero_buf = ws.acc;
+    a.zero_words = (size_t)T * d;
     if (mode == 0) {
         a.b_bf16 = x;
-        a.b_amax = ws.x_amax;
         a.b_by_token = 1;
         a.h_out = ws.h;
-        a.h_amax = ws.h_amax;
         launch_gemv(B_BF16, OUT_H, a, gemv_max_work(R, E, F), s);
     } else {
         a.b_codes = ws.xq;
@@ -143,18 +147,21 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
         a.hq_gs = is2;
         launch_gemv(B_NVFP4, OUT_HQ, a, gemv_max_work(R, E, F), s);
     }
-    // down + weighted combine
+    // down + weighted combine; the last contribution to a token writes its bf16 row
     GemvArgs b = base_args(ws, top_k);
     b.K = F;
     b.N = d;
     b.nproj = 1;
+    b.ksplit = gemv_pick_ksplit(tiles, d, 1);
     b.a_codes[0] = w->down.codes;  b.a_scales[0] = w->down.scales;  b.a_ws2[0] = w->down.weight_scale_2;
     b.a_codes[1] = w->down.codes;  b.a_scales[1] = w->down.scales;  b.a_ws2[1] = w->down.weight_scale_2;
-    b.work_counter = ws.counters + 1;
+    b.work_counter = ws.clear + 1;
     b.acc_out = ws.acc;
+    b.tok_done = ws.clear + kCounters;
+    b.done_target = top_k * (d / (16 * (8 / b.ksplit)));
+    b.out_bf16 = out;
     if (mode == 0) {
         b.b_bf16 = ws.h;
-        b.b_amax = ws.h_amax;
         b.b_by_token = 0;
         launch_gemv(B_BF16, OUT_COMBINE, b, gemv_max_work(R, E, d), s);
     } else {
@@ -163,57 +170,34 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
         b.b_gs = is2;
         launch_gemv(B_NVFP4, OUT_COMBINE, b, gemv_max_work(R, E, d), s);
     }
-    launch_finalize(ws.acc, (size_t)T * d, out, s);
     return last_launch_status();
 }
 
 // ---- dense linear ----
 struct LinWs {
-    float* x_amax;     // [M]
     int32_t* meta;     // offsets[2], active[1], n_active[1], tile_start[2]
     int* counters;
 };
 
-LinWs carve_lin(void* base, int M, size_t* bytes) {
+LinWs carve_lin(void* base, size_t* bytes) {
     Carver c(base);
     LinWs l;
-    l.x_amax = c.take<float>(M + 1);
     l.meta = c.take<int32_t>(8);
     l.counters = c.take<int>(kCounters);
     if (bytes) *bytes = align_up(c.off, 256);
     return l;
 }
 
-__global__ void linear_prep_kernel(const uint16_t* __restrict__ x, int M, int K, float* __restrict__ x_amax,
-                                   int32_t* meta, int* counters) {
-    const int m = blockIdx.x;
-    if (m == 0 && threadIdx.x == 0) {
-        meta[0] = 0;                                 // offsets[0]
-        meta[1] = M;                                 // offsets[1]
-        meta[2] = 0;                                 // active[0] = expert 0
-        meta[3] = 1;                                 // n_active
-        meta[4] = 0;                                 // tile_start[0]
+__global__ void linear_prep_kernel(int M, int32_t* meta, int* counters) {
+    if (threadIdx.x == 0) {
+        meta[0] = 0;                                      // offsets[0]
+        meta[1] = M;                                      // offsets[1]
+        meta[2] = 0;                                      // active[0] = expert 0
+        meta[3] = 1;                                      // n_active
+        meta[4] = 0;                                      // tile_start[0]
         meta[5] = (M + kGemvTokTile - 1) / kGemvTokTile;  // tile_start[1]
     }
-    if (m == 0 && threadIdx.x < kCounters) counters[threadIdx.x] = 0;
-    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)m * K);
-    float mx = 0.0f;
-    for (int i = threadIdx.x; i < K / 8; i += blockDim.x) {
-        uint4 u = __ldg(src + i);
-        uint32_t ww[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            mx = fmaxf(mx, fmaxf(fabsf(bf16_bits_to_f32(ww[j] & 0xFFFFu)), fabsf(bf16_bits_to_f32(ww[j] >> 16))));
-    }
-    mx = warp_max(mx);
-    __shared__ float red[32];
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
-    __syncthreads();
-    if (threadIdx.x < 32) {
-        float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.0f;
-        v = warp_max(v);
-        if (threadIdx.x == 0) x_amax[m] = v;
-    }
+    if (threadIdx.x < kCounters) counters[threadIdx.x] = 0;
 }
 
 }  // namespace
@@ -261,7 +245,7 @@ extern "C" size_t nvfp4_linear_workspace_size(int M, int K, int N) {
     (void)N;
     if (M < 0) return 0;
     size_t b = 0;
-    carve_lin(nullptr, M, &b);
+    carve_lin(nullptr, &b);
     return b;
 }
 
@@ -269,15 +253,14 @@ extern "C" nvfp4_status nvfp4_linear(const uint16_t* x, int M, int K, const nvfp
                                      const nvfp4_w* w_up, uint16_t* out, void* ws, size_t ws_bytes,
                                      cudaStream_t stream) {
     if (M < 0 || K < 1 || N < 1 || !w) return NVFP4_ERR_INVALID_ARG;
-    if (K % 64 != 0 || N % 16 != 0) return NVFP4_ERR_SHAPE;
+    if (K % 64 != 0 || N % 16 != 0 || !gemv_supported_k(K)) return NVFP4_ERR_SHAPE;
     if (M == 0) return NVFP4_OK;
     if (!x || !out || !ws || !w_ok(*w) || (w_up && !w_ok(*w_up))) return NVFP4_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(out) || !aligned16(ws) || !w_aligned(*w) || (w_up && !w_aligned(*w_up)))
         return NVFP4_ERR_ALIGN;
     if (ws_bytes < nvfp4_linear_workspace_size(M, K, N)) return NVFP4_ERR_WORKSPACE;
-    LinWs l = carve_lin(ws, M, nullptr);
-    NVFP4_LAUNCH("linear_prep", stream,
-                 linear_prep_kernel<<<M, 256, 0, stream>>>(x, M, K, l.x_amax, l.meta, l.counters));
+    LinWs l = carve_lin(ws, nullptr);
+    NVFP4_LAUNCH("linear_prep", stream, linear_prep_kernel<<<1, 32, 0, stream>>>(M, l.meta, l.counters));
     GemvArgs a{};
     a.K = K;
     a.N = N;
@@ -290,18 +273,19 @@ extern "C" nvfp4_status nvfp4_linear(const uint16_t* x, int M, int K, const nvfp
     a.a_codes[0] = w->codes;  a.a_scales[0] = w->scales;  a.a_ws2[0] = w->weight_scale_2;
     a.a_codes[1] = w->codes;  a.a_scales[1] = w->scales;  a.a_ws2[1] = w->weight_scale_2;
     a.b_bf16 = x;
-    a.b_amax = l.x_amax;
     a.b_by_token = 1;
     a.work_counter = l.counters;
+    const int tiles = (M + kGemvTokTile - 1) / kGemvTokTile;
     const int max_work = gemv_max_work(M, 1, N);
     if (w_up) {
         a.nproj = 2;
+        a.ksplit = gemv_pick_ksplit(tiles, N, 2);
         a.a_codes[1] = w_up->codes;  a.a_scales[1] = w_up->scales;  a.a_ws2[1] = w_up->weight_scale_2;
         a.h_out = out;
-        a.h_amax = nullptr;
         launch_gemv(B_BF16, OUT_H, a, max_work, stream);
     } else {
         a.nproj = 1;
+        a.ksplit = gemv_pick_ksplit(tiles, N, 1);
         a.y_out = out;
         launch_gemv(B_BF16, OUT_BF16, a, max_work, stream);
     }

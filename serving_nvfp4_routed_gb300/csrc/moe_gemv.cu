@@ -93,170 +93,241 @@ __device__ __forceinline__ uint32_t e2m1x2_byte(float lo, float hi) {
     return (r & 0xFFu) | ((__float_as_uint(lo) >> 31) << 3) | ((__float_as_uint(hi) >> 31) << 7);
 }
 
-template <int CK, int BMODE, int OUTMODE, int NPROJ, int NW>
-__global__ void __launch_bounds__(NW * 32) gemv_kernel(const GemvArgs a) {
-    using C = Chunk<CK>;
-    __shared__ float s_red[NW][NPROJ * 4][32];
-    __shared__ int s_work;
+// Shared-memory layout of the staged B rows: row g holds K f16 values as K/8
+// 16-byte granules; granule q is stored at bsw(q, g) so that the B-fragment
+// reads of a warp (lane (g, c) reads granule c*CK/32 + j of its row) hit 8
+// distinct 16-byte bank groups in every quarter-warp phase.
+template <int CK>
+__device__ __forceinline__ int bsw(int q, int g) {
+    if constexpr (CK == 256) return q ^ ((((q >> 3) & 3) << 1) | (g & 1));
+    else return q ^ (g & 1);
+}
 
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+struct Item {
+    int e, row0, nrows, fb;
+};
+
+template <int CK, int BMODE, int OUTMODE, int NPROJ>
+__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
+    using C = Chunk<CK>;
+    constexpr int U = NPROJ == 2 ? 2 : 4;  // chunks whose weight loads are in flight together
+    extern __shared__ uint4 Bs[];          // [kGemvTokTile][K/8] granules of f16
+    __shared__ float s_red[kWarps - 1][NPROJ * 4][32];
+    __shared__ float s_rowscale[kGemvTokTile];
+    __shared__ unsigned s_amax[kGemvTokTile];
+    __shared__ int s_next;
+    __shared__ int s_fin[kGemvTokTile];
+
+    grid_dep_wait();
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, c = lane & 3;
+    const int KSPL = a.ksplit, WF = kWarps / KSPL;
+    const int wf = warp / KSPL, ks = warp % KSPL;
+
+    if (a.zero_buf) {
+        float4* z = reinterpret_cast<float4*>(a.zero_buf);
+        for (size_t i = blockIdx.x * (size_t)kThreads + tid; i < a.zero_words / 4; i += (size_t)gridDim.x * kThreads)
+            z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+
     const int n_active = *a.n_active;
     const int total_tiles = a.tile_start[n_active];
-    const int n_slabs = a.N / 16;
-    const int total = total_tiles * n_slabs;
-    const int nchunks = a.K / CK;
+    const int FB = 16 * WF;
+    const int n_fb = a.N / FB;
+    const int total = total_tiles * n_fb;
+    const int nch = a.K / CK;
+    const int Kg = a.K / 8;
     const size_t K2 = (size_t)a.K / 2, K16 = (size_t)a.K / 16;
 
-    for (;;) {
-        if (threadIdx.x == 0) s_work = atomicAdd(a.work_counter, 1);
-        __syncthreads();
-        const int w = s_work;
-        __syncthreads();
-        if (w >= total) break;
-        const int slab = w % n_slabs, tile = w / n_slabs;
+    auto decode = [&](int item, Item& it) {
+        it.fb = item % n_fb;
+        const int tile = item / n_fb;
         int lo = 0, hi = n_active;  // largest ai with tile_start[ai] <= tile
         while (hi - lo > 1) {
-            int mid = (lo + hi) >> 1;
+            const int mid = (lo + hi) >> 1;
             if (a.tile_start[mid] <= tile) lo = mid; else hi = mid;
         }
-        const int e = a.active[lo];
-        const int row0 = a.offsets[e] + (tile - a.tile_start[lo]) * kGemvTokTile;
-        const int nrows = min(kGemvTokTile, a.offsets[e + 1] - row0);
-        const int n0 = slab * 16;
+        it.e = a.active[lo];
+        it.row0 = a.offsets[it.e] + (tile - a.tile_start[lo]) * kGemvTokTile;
+        it.nrows = min(kGemvTokTile, a.offsets[it.e + 1] - it.row0);
+    };
 
-        // this lane's B row (token column g of the n-tile)
-        const bool bvalid = g < nrows;
-        const int r_b = row0 + (bvalid ? g : 0);
-        int brow = r_b;
-        float bscale = 1.0f;
-        if constexpr (BMODE == B_BF16) {
-            if (a.b_by_token) brow = a.row_to_slot ? a.row_to_slot[r_b] / a.top_k : r_b;
-            bscale = exp2i(-row_exponent(a.b_amax[brow]));
+    uint32_t acw[U][NPROJ][2][C::CW];
+    uint32_t asw[U][NPROJ][2];
+    auto load_batch = [&](const Item& it, int chb) {
+        const int n0 = it.fb * FB + wf * 16;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int ch = chb + u * KSPL;
+            if (ch < nch) {
+                const size_t kb = (size_t)ch * CK + (size_t)c * C::TS;
+#pragma unroll
+                for (int p = 0; p < NPROJ; ++p)
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const size_t row = (size_t)it.e * a.N + n0 + g + 8 * hf;
+                        load_codes<CK>(a.a_codes[p] + row * K2 + kb / 2, acw[u][p][hf]);
+                        asw[u][p][hf] = load_scales<CK>(a.a_scales[p] + row * K16 + kb / 16);
+                    }
+            }
         }
+    };
 
+    if (tid == 0) s_next = atomicAdd(a.work_counter, 1);
+    if (tid < kGemvTokTile) s_amax[tid] = 0u;
+    __syncthreads();
+    int item = s_next;
+    Item cur{};
+    if (item < total) {
+        decode(item, cur);
+        load_batch(cur, ks);
+    }
+
+    while (item < total) {
+        // ---- stage the B rows of this item; the warps w with w % nrows == j stage row j
+        {
+            const int j = warp % cur.nrows, gi = warp / cur.nrows;
+            const int gsz = (kWarps - j + cur.nrows - 1) / cur.nrows;
+            const int r = cur.row0 + j;
+            uint4* dst = Bs + (size_t)j * Kg;
+            if constexpr (BMODE == B_BF16) {
+                const int brow = a.b_by_token ? (a.row_to_slot ? a.row_to_slot[r] / a.top_k : r) : r;
+                const uint4* src = reinterpret_cast<const uint4*>(a.b_bf16 + (size_t)brow * a.K);
+                float m = 0.0f;
+                for (int q = gi * 32 + lane; q < Kg; q += gsz * 32) {
+                    const uint4 u = __ldg(src + q);
+                    const uint32_t ww[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        m = fmaxf(m, fmaxf(fabsf(bf16_bits_to_f32(ww[i] & 0xFFFFu)),
+                                           fabsf(bf16_bits_to_f32(ww[i] >> 16))));
+                    dst[bsw<CK>(q, j)] = u;
+                }
+                m = warp_max(m);
+                if (lane == 0) atomicMax(&s_amax[j], __float_as_uint(m));
+                __syncthreads();
+                const int sexp = row_exponent(__uint_as_float(s_amax[j]));
+                const float down = exp2i(-sexp);
+                if (gi == 0 && lane == 0) s_rowscale[j] = exp2i(sexp);
+                for (int q = gi * 32 + lane; q < Kg; q += gsz * 32) {
+                    const int qs = bsw<CK>(q, j);
+                    const uint4 u = dst[qs];
+                    uint4 o;
+                    o.x = bf16x2_scaled_to_f16x2(u.x, down);
+                    o.y = bf16x2_scaled_to_f16x2(u.y, down);
+                    o.z = bf16x2_scaled_to_f16x2(u.z, down);
+                    o.w = bf16x2_scaled_to_f16x2(u.w, down);
+                    dst[qs] = o;
+                }
+            } else {
+                const uint8_t* codes = a.b_codes + (size_t)r * K2;
+                const uint8_t* scales = a.b_scales + (size_t)r * K16;
+                for (int b = gi * 32 + lane; b < a.K / 16; b += gsz * 32) {  // 16-block: 8 code bytes, 1 scale
+                    const uint2 cw = __ldg(reinterpret_cast<const uint2*>(codes) + b);
+                    const uint32_t S = f16x2_bcast(e4m3x2_to_f16x2(__ldg(scales + b)), 0);
+                    uint32_t f0[4], f1[4];
+                    e2m1x8_to_f16x8(cw.x, f0);
+                    e2m1x8_to_f16x8(cw.y, f1);
+                    dst[bsw<CK>(2 * b, j)] =
+                        make_uint4(hmul2_u32(f0[0], S), hmul2_u32(f0[1], S), hmul2_u32(f0[2], S), hmul2_u32(f0[3], S));
+                    dst[bsw<CK>(2 * b + 1, j)] =
+                        make_uint4(hmul2_u32(f1[0], S), hmul2_u32(f1[1], S), hmul2_u32(f1[2], S), hmul2_u32(f1[3], S));
+                }
+            }
+        }
+        __syncthreads();
+        if (tid == 0) s_next = atomicAdd(a.work_counter, 1);  // next item, fetched while computing
+
+        // ---- stream this warp's 16 features over its share of K
+        const int n0 = cur.fb * FB + wf * 16;
         float acc[NPROJ][4];
 #pragma unroll
         for (int p = 0; p < NPROJ; ++p)
 #pragma unroll
             for (int i = 0; i < 4; ++i) acc[p][i] = 0.0f;
-
-        for (int ch = warp; ch < nchunks; ch += NW) {
-            const size_t kb = (size_t)ch * CK + (size_t)c * C::TS;
-            uint32_t acw[NPROJ][2][C::CW];
-            uint32_t asw[NPROJ][2];
+        const uint4* brow_s = Bs + (size_t)g * Kg;
+        for (int chb = ks; chb < nch; chb += U * KSPL) {
+            if (chb != ks) load_batch(cur, chb);
 #pragma unroll
-            for (int p = 0; p < NPROJ; ++p)
+            for (int u = 0; u < U; ++u) {
+                const int ch = chb + u * KSPL;
+                if (ch >= nch) break;
+                const int qb = (ch * CK + c * C::TS) / 8;
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    const size_t row = (size_t)e * a.N + n0 + g + 8 * hf;
-                    load_codes<CK>(a.a_codes[p] + row * K2 + kb / 2, acw[p][hf]);
-                    asw[p][hf] = load_scales<CK>(a.a_scales[p] + row * K16 + kb / 16);
-                }
-            uint32_t bw[C::TS / 2];  // B_BF16: bf16x2 words; B_NVFP4: code words then scale word
-            uint32_t bsw = 0;
-            if constexpr (BMODE == B_BF16) {
-                if (bvalid) {
-                    const uint4* src = reinterpret_cast<const uint4*>(a.b_bf16 + (size_t)brow * a.K + kb);
+                for (int jj = 0; jj < C::KS; jj += 2) {
+                    const uint4 bq = brow_s[bsw<CK>(qb + jj / 2, g)];
+                    const uint32_t b0[2] = {bq.x, bq.y};
+                    const uint32_t b1[2] = {bq.z, bq.w};
 #pragma unroll
-                    for (int i = 0; i < C::TS / 8; ++i) {
-                        uint4 u = __ldg(src + i);
-                        bw[4 * i] = u.x; bw[4 * i + 1] = u.y; bw[4 * i + 2] = u.z; bw[4 * i + 3] = u.w;
+                    for (int p = 0; p < NPROJ; ++p) {
+                        uint32_t r0[4], r1[4];
+                        deq_word(acw[u][p][0][jj >> 1], asw[u][p][0], jj, r0);
+                        deq_word(acw[u][p][1][jj >> 1], asw[u][p][1], jj, r1);
+                        const uint32_t af0[4] = {r0[0], r1[0], r0[1], r1[1]};
+                        const uint32_t af1[4] = {r0[2], r1[2], r0[3], r1[3]};
+                        mma_16816(acc[p], af0, b0);
+                        mma_16816(acc[p], af1, b1);
                     }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < C::TS / 2; ++i) bw[i] = 0u;
-                }
-            } else {
-                if (bvalid) {
-                    load_codes<CK>(a.b_codes + (size_t)r_b * K2 + kb / 2, bw);
-                    bsw = load_scales<CK>(a.b_scales + (size_t)r_b * K16 + kb / 16);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < C::CW; ++i) bw[i] = 0u;
-                }
-            }
-#pragma unroll
-            for (int jj = 0; jj < C::KS; jj += 2) {
-                uint32_t bq[4];  // B words for steps jj (bq[0], bq[1]) and jj+1 (bq[2], bq[3])
-                if constexpr (BMODE == B_BF16) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) bq[i] = bf16x2_scaled_to_f16x2(bw[2 * jj + i], bscale);
-                } else {
-                    deq_word(bw[jj >> 1], bsw, jj, bq);
-                }
-#pragma unroll
-                for (int p = 0; p < NPROJ; ++p) {
-                    uint32_t r0[4], r1[4];
-                    deq_word(acw[p][0][jj >> 1], asw[p][0], jj, r0);
-                    deq_word(acw[p][1][jj >> 1], asw[p][1], jj, r1);
-                    const uint32_t af0[4] = {r0[0], r1[0], r0[1], r1[1]};
-                    const uint32_t af1[4] = {r0[2], r1[2], r0[3], r1[3]};
-                    const uint32_t b0[2] = {bq[0], bq[1]};
-                    const uint32_t b1[2] = {bq[2], bq[3]};
-                    mma_16816(acc[p], af0, b0);
-                    mma_16816(acc[p], af1, b1);
                 }
             }
         }
-
-        // cross-warp reduction of the partial sums
-#pragma unroll
-        for (int p = 0; p < NPROJ; ++p)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) s_red[warp][p * 4 + i][lane] = acc[p][i];
-        __syncthreads();
-        if (warp == 0) {
+        const bool owner = ks == 0;
+        if (KSPL > 1 && !owner) {
 #pragma unroll
             for (int p = 0; p < NPROJ; ++p)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    float s = 0.0f;
-#pragma unroll
-                    for (int w2 = 0; w2 < NW; ++w2) s += s_red[w2][p * 4 + i][lane];
-                    acc[p][i] = s;
-                }
+                for (int i = 0; i < 4; ++i) s_red[wf * (KSPL - 1) + ks - 1][p * 4 + i][lane] = acc[p][i];
+        }
+        __syncthreads();
 
-            // epilogue: column cc of this lane is permuted row row0 + 2c + cc
+        // ---- the next item's first weight batch goes out before this item's epilogue
+        const int nitem = s_next;
+        Item nxt{};
+        if (nitem < total) {
+            decode(nitem, nxt);
+            load_batch(nxt, ks);
+        }
+        if (KSPL > 1 && owner) {
+            for (int k2 = 0; k2 < KSPL - 1; ++k2)
+#pragma unroll
+                for (int p = 0; p < NPROJ; ++p)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) acc[p][i] += s_red[wf * (KSPL - 1) + k2][p * 4 + i][lane];
+        }
+
+        // ---- epilogue: column cc of this lane is permuted row row0 + 2c + cc
+        const int e = cur.e, row0 = cur.row0, nrows = cur.nrows;
+        if (owner) {
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 const int col = 2 * c + cc;
                 const bool valid = col < nrows;
                 const int r = row0 + (valid ? col : 0);
-                float rs;  // scale taking the accumulator to x W^T (without ws2)
-                if constexpr (BMODE == B_BF16) {
-                    int br = r;
-                    if (a.b_by_token) br = a.row_to_slot ? a.row_to_slot[r] / a.top_k : r;
-                    rs = exp2i(row_exponent(a.b_amax[br]));
-                } else {
-                    rs = a.b_gs[e];
-                }
+                float rs;  // takes the accumulator to x W^T (without the tensor scale)
+                if constexpr (BMODE == B_BF16) rs = valid ? s_rowscale[col] : 0.0f;
+                else rs = a.b_gs[e];
                 if constexpr (OUTMODE == OUT_H || OUTMODE == OUT_HQ) {
-                    const float wg = a.a_ws2[0][e], wu = a.a_ws2[1][e];
+                    const float wg = a.a_ws2[0][e], wu = a.a_ws2[NPROJ - 1][e];
                     float hv[2];
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {
                         const float G = round_bf16(__fmul_rn(__fmul_rn(acc[0][2 * hf + cc], rs), wg));
-                        const float U = round_bf16(__fmul_rn(__fmul_rn(acc[NPROJ - 1][2 * hf + cc], rs), wu));
+                        const float Uv = round_bf16(__fmul_rn(__fmul_rn(acc[NPROJ - 1][2 * hf + cc], rs), wu));
                         const float sg = G / (1.0f + expf(-G));
-                        hv[hf] = round_bf16(sg * U);
+                        hv[hf] = valid ? round_bf16(sg * Uv) : 0.0f;
                     }
                     if constexpr (OUTMODE == OUT_H) {
                         if (valid) {
 #pragma unroll
                             for (int hf = 0; hf < 2; ++hf)
-                                a.h_out[(size_t)r * a.N + n0 + g + 8 * hf] =
-                                    f32_to_bf16_bits(hv[hf]);
-                        }
-                        if (a.h_amax) {
-                            float m = valid ? fmaxf(fabsf(hv[0]), fabsf(hv[1])) : 0.0f;
-                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
-                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-                            if (valid && g == 0) atomic_max_nonneg(a.h_amax + r, m);
+                                a.h_out[(size_t)r * a.N + n0 + g + 8 * hf] = f32_to_bf16_bits(hv[hf]);
                         }
                     } else {
-                        // NVFP4 requantisation of h: this 16-feature slab is one block
+                        // NVFP4 requantisation of h: this warp's 16 features are one block
                         const float gs2 = a.hq_gs[e];
                         float m = fmaxf(fabsf(hv[0]), fabsf(hv[1]));
                         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
@@ -306,23 +377,58 @@ __global__ void __launch_bounds__(NW * 32) gemv_kernel(const GemvArgs a) {
                 }
             }
         }
-        __syncthreads();
-    }
-}
 
-constexpr int kNW = 8;
+        if constexpr (OUTMODE == OUT_COMBINE) {
+            // the CTA that adds the last contribution to a token turns its
+            // fp32 row into the bf16 output row
+            __threadfence();
+            __syncthreads();
+            if (tid < kGemvTokTile) {
+                int t = -1;
+                if (tid < nrows) {
+                    const int tt = a.row_to_slot[row0 + tid] / a.top_k;
+                    if (atomicAdd(a.tok_done + tt, 1) == a.done_target - 1) t = tt;
+                }
+                s_fin[tid] = t;
+            }
+            __syncthreads();
+            for (int i = 0; i < nrows; ++i) {
+                const int t = s_fin[i];
+                if (t < 0) continue;
+                __threadfence();
+                const float4* src = reinterpret_cast<const float4*>(a.acc_out + (size_t)t * a.N);
+                uint2* dst = reinterpret_cast<uint2*>(a.out_bf16 + (size_t)t * a.N);
+                for (int jx = tid; jx < a.N / 4; jx += kThreads) {
+                    const float4 v = __ldcg(src + jx);
+                    uint2 o;
+                    o.x = (uint32_t)f32_to_bf16_bits(v.x) | ((uint32_t)f32_to_bf16_bits(v.y) << 16);
+                    o.y = (uint32_t)f32_to_bf16_bits(v.z) | ((uint32_t)f32_to_bf16_bits(v.w) << 16);
+                    dst[jx] = o;
+                }
+            }
+        }
+        if (tid < kGemvTokTile) s_amax[tid] = 0u;
+        __syncthreads();
+        item = nitem;
+        cur = nxt;
+    }
+    grid_dep_launch();
+}
 
 template <int CK, int BMODE, int OUTMODE, int NPROJ>
 void launch_t(const GemvArgs& a, int max_work, cudaStream_t s, const char* name) {
-    auto kern = gemv_kernel<CK, BMODE, OUTMODE, NPROJ, kNW>;
+    auto kern = gemv_kernel<CK, BMODE, OUTMODE, NPROJ>;
     static int per_sm = 0;
     if (per_sm == 0) {
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gemv_smem_bytes(12288));
         int v = 0;
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kern, kNW * 32, 0);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kern, kThreads, gemv_smem_bytes(4096));
         per_sm = v > 0 ? v : 1;
     }
-    int grid = std::max(1, std::min(max_work, per_sm * num_sms()));
-    NVFP4_LAUNCH(name, s, kern<<<grid, kNW * 32, 0, s>>>(a));
+    const size_t smem = gemv_smem_bytes(a.K);
+    const int occ = smem > gemv_smem_bytes(4096) ? 1 : per_sm;
+    const int grid = std::max(1, std::min(max_work, occ * num_sms()));
+    NVFP4_LAUNCH(name, s, launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, a));
 }
 
 template <int CK>
@@ -340,66 +446,24 @@ void launch_ck(int bmode, int outmode, const GemvArgs& a, int max_work, cudaStre
 
 }  // namespace
 
+size_t gemv_smem_bytes(int K) { return (size_t)kGemvTokTile * K * 2; }
+
+bool gemv_supported_k(int K) { return K > 0 && K % 64 == 0 && K <= 12288; }
+
+int gemv_pick_ksplit(int expected_tiles, int N, int nproj) {
+    (void)nproj;
+    const long long want = num_sms();  // at least one work item per SM before K is split
+    for (int wf = kWarps; wf >= 1; wf >>= 1) {
+        const int FB = 16 * wf;
+        if (N % FB != 0) continue;
+        if ((long long)expected_tiles * (N / FB) >= want) return kWarps / wf;
+    }
+    return kWarps;  // wf = 1: 16 features per CTA, K split over all warps
+}
+
 void launch_gemv(int bmode, int outmode, const GemvArgs& a, int max_work, cudaStream_t s) {
     if (a.K % 256 == 0) launch_ck<256>(bmode, outmode, a, max_work, s);
     else launch_ck<64>(bmode, outmode, a, max_work, s);
-}
-
-// ---------------------------------------------------------------------------
-// small helper kernels of the MoE call
-// ---------------------------------------------------------------------------
-__global__ void moe_prep_kernel(const uint16_t* __restrict__ x, int T, int d, float* __restrict__ x_amax,
-                                float* __restrict__ acc, int k, float* __restrict__ h_amax, int* counters,
-                                int n_counters) {
-    const int t = blockIdx.x;
-    if (t == 0 && threadIdx.x < n_counters) counters[threadIdx.x] = 0;
-    float4* a4 = reinterpret_cast<float4*>(acc + (size_t)t * d);
-    for (int i = threadIdx.x; i < d / 4; i += blockDim.x) a4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (h_amax && threadIdx.x < k) h_amax[(size_t)t * k + threadIdx.x] = 0.0f;
-    if (x_amax) {
-        const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
-        float m = 0.0f;
-        for (int i = threadIdx.x; i < d / 8; i += blockDim.x) {
-            uint4 u = __ldg(src + i);
-            uint32_t ww[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                m = fmaxf(m, fmaxf(fabsf(bf16_bits_to_f32(ww[j] & 0xFFFFu)), fabsf(bf16_bits_to_f32(ww[j] >> 16))));
-        }
-        m = warp_max(m);
-        __shared__ float red[32];
-        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
-        __syncthreads();
-        if (threadIdx.x < 32) {
-            float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.0f;
-            v = warp_max(v);
-            if (threadIdx.x == 0) x_amax[t] = v;
-        }
-    }
-}
-
-void launch_moe_prep(const uint16_t* x, int T, int d, float* x_amax, float* acc, int k, float* h_amax,
-                     int* counters, int n_counters, cudaStream_t s) {
-    NVFP4_LAUNCH("moe_prep", s,
-                 moe_prep_kernel<<<std::max(T, 1), 256, 0, s>>>(x, T, d, x_amax, acc, k, h_amax, counters,
-                                                                n_counters));
-}
-
-__global__ void finalize_kernel(const float* __restrict__ acc, size_t n4, uint16_t* __restrict__ out) {
-    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
-        float4 v = reinterpret_cast<const float4*>(acc)[i];
-        uint2 o;
-        o.x = (uint32_t)f32_to_bf16_bits(v.x) | ((uint32_t)f32_to_bf16_bits(v.y) << 16);
-        o.y = (uint32_t)f32_to_bf16_bits(v.z) | ((uint32_t)f32_to_bf16_bits(v.w) << 16);
-        reinterpret_cast<uint2*>(out)[i] = o;
-    }
-}
-
-void launch_finalize(const float* acc, size_t n, uint16_t* out, cudaStream_t s) {
-    size_t n4 = n / 4;
-    if (n4 == 0) return;
-    int grid = (int)std::min<size_t>((n4 + 255) / 256, (size_t)num_sms() * 8);
-    NVFP4_LAUNCH("finalize", s, finalize_kernel<<<grid, 256, 0, s>>>(acc, n4, out));
 }
 
 }  // namespace nvfp4

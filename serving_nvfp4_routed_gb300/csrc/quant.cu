@@ -19,6 +19,7 @@
 namespace nvfp4 {
 
 __global__ void zero_words_kernel(uint32_t* p, size_t n) {
+    grid_dep_wait();
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
         p[i] = 0u;
 }
@@ -27,7 +28,7 @@ void launch_zero(void* p, size_t bytes, cudaStream_t s) {
     size_t n = bytes / 4;
     if (n == 0) return;
     int grid = (int)std::min<size_t>((n + 255) / 256, (size_t)num_sms() * 8);
-    NVFP4_LAUNCH("zero_words", s, zero_words_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<uint32_t*>(p), n));
+    NVFP4_LAUNCH("zero_words", s, launch_pdl(zero_words_kernel, dim3(grid), dim3(256), 0, s, reinterpret_cast<uint32_t*>(p), n));
 }
 
 // Per-tensor max |w| over `batch` tensors of n_per elements each.
@@ -122,6 +123,7 @@ __global__ void quantize_act_kernel(const uint16_t* __restrict__ x, int M, int K
                                     const float* __restrict__ input_scale,
                                     const int32_t* __restrict__ offsets, int E,
                                     uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+    grid_dep_wait();
     const int halves_per_row = K / 8;
     const size_t total = (size_t)M * halves_per_row;
     for (size_t base = blockIdx.x * (size_t)blockDim.x + (threadIdx.x & ~31u); base < total;
@@ -162,8 +164,8 @@ void launch_quantize_act(const uint16_t* x, int M, int K, const int32_t* row_to_
     if (total == 0) return;
     int grid = (int)std::min<size_t>((total + 255) / 256, (size_t)num_sms() * 16);
     NVFP4_LAUNCH("quantize_act", s,
-                 quantize_act_kernel<<<grid, 256, 0, s>>>(x, M, K, row_to_slot, top_k, input_scale,
-                                                          offsets, E, codes, scales));
+                 launch_pdl(quantize_act_kernel, dim3(grid), dim3(256), 0, s, x, M, K, row_to_slot, top_k, input_scale,
+                            offsets, E, codes, scales));
 }
 
 }  // namespace nvfp4

@@ -8,8 +8,7 @@
 // weights renormalised over the k chosen) is the plain reading.
 //
 // Top-k: one warp per token, logits in registers, k rounds of a warp arg-max.
-// Weights: exp(l - l_max) / sum over the k, in fp64 (so they match an fp64
-// evaluation to the last fp32 bit).
+// Weights: exp(l - l_max) / sum over the k, in fp32.
 // Permutation (stable: expert, token, slot): a per-expert histogram, a
 // warp-scan exclusive prefix sum, and a scatter in which each row's position
 // is its expert's base + the count of equal experts before it -- within a warp
@@ -24,7 +23,6 @@ namespace nvfp4 {
 
 namespace {
 
-constexpr int kRoundRows = 1024;   // rows per scatter round (one per thread)
 constexpr int kSmallMaxRows = 8192;
 constexpr int kChunkRows = 8192;   // rows per block in the multi-block path
 
@@ -69,13 +67,15 @@ __device__ void warp_topk(const float* __restrict__ lg, int E, int k, int32_t* _
             my_id = bi;
         }
     }
-    const double m = (double)__shfl_sync(0xffffffffu, my_v, 0);
-    const double ex = lane < k ? exp((double)my_v - m) : 0.0;
-    double sum = 0.0;
+    // fp32: exp(l_j - l_max), summed over the k in slot order, divided
+    // (fp64 runs at a small fraction of the fp32 rate on this part)
+    const float m = __shfl_sync(0xffffffffu, my_v, 0);
+    const float ex = lane < k ? expf(my_v - m) : 0.0f;
+    float sum = 0.0f;
     for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, ex, j);
     if (lane < k) {
         ids[lane] = my_id;
-        w[lane] = (float)(ex / sum);
+        w[lane] = __fdiv_rn(ex, sum);
     }
 }
 
@@ -182,21 +182,19 @@ __device__ void validate_ids(int32_t* ids, int R, int E, int32_t* status) {
     }
 }
 
-__global__ void __launch_bounds__(1024) route_small_kernel(const float* __restrict__ logits, int T, int E,
-                                                           int k, RouteArrays ra, int32_t* status) {
+// Permutation of R <= kSmallMaxRows rows in one CTA (ids already written by
+// topk_kernel, or given by the caller and validated here).
+__global__ void __launch_bounds__(1024) route_perm_small_kernel(int T, int E, int k, int given_ids, RouteArrays ra,
+                                                                int32_t* status) {
     __shared__ int run[kMaxExperts];
     __shared__ uint8_t wh[32 * kMaxExperts];
     __shared__ int tmp32[32];
+    grid_dep_wait();
     const int R = T * k;
-    const int warp = threadIdx.x >> 5;
-    if (logits) {
-        for (int t = warp; t < T; t += blockDim.x >> 5)
-            topk_dispatch(logits + (size_t)t * E, E, k, ra.ids + (size_t)t * k, ra.w + (size_t)t * k);
-    } else {
-        validate_ids(ra.ids, R, E, status);
-    }
+    if (given_ids) validate_ids(ra.ids, R, E, status);
     for (int i = threadIdx.x; i < E; i += blockDim.x) run[i] = 0;
     for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) wh[i] = 0;
+    for (int i = threadIdx.x; i < ra.n_clear; i += blockDim.x) ra.clear[i] = 0;
     __syncthreads();
     for (int r = threadIdx.x; r < R; r += blockDim.x) atomicAdd(&run[ra.ids[r]], 1);
     __syncthreads();
@@ -206,20 +204,26 @@ __global__ void __launch_bounds__(1024) route_small_kernel(const float* __restri
     if (threadIdx.x < E) run[threadIdx.x] = off;
     __syncthreads();
     scatter_rows(0, R, E, ra.ids, run, wh, ra);
+    grid_dep_launch();
 }
 
+// One warp per token.
 __global__ void topk_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* ids, float* w) {
+    grid_dep_wait();
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t < T) topk_dispatch(logits + (size_t)t * E, E, k, ids + (size_t)t * k, w + (size_t)t * k);
+    grid_dep_launch();
 }
 
 __global__ void validate_ids_kernel(int32_t* ids, int R, int E, int32_t* status) {
+    grid_dep_wait();
     validate_ids(ids, R, E, status);
 }
 
 __global__ void __launch_bounds__(1024) perm_count_kernel(const int32_t* __restrict__ ids, int R, int E,
                                                           int32_t* counts) {
     __shared__ int hist[kMaxExperts];
+    grid_dep_wait();
     for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
     __syncthreads();
     const int r0 = blockIdx.x * kChunkRows, r1 = min(R, r0 + kChunkRows);
@@ -230,6 +234,7 @@ __global__ void __launch_bounds__(1024) perm_count_kernel(const int32_t* __restr
 
 __global__ void __launch_bounds__(1024) perm_scan_kernel(int nb, int E, int32_t* counts, RouteArrays ra) {
     __shared__ int tmp32[32];
+    grid_dep_wait();
     const int e = threadIdx.x;
     int run = 0;
     if (e < E) {
@@ -243,12 +248,14 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int nb, int E, int32_t*
     write_group_meta(run, E, ra, tmp32, off);
     if (e < E)
         for (int b = 0; b < nb; ++b) counts[(size_t)b * E + e] += off;
+    for (int i = threadIdx.x; i < ra.n_clear; i += blockDim.x) ra.clear[i] = 0;
 }
 
 __global__ void __launch_bounds__(1024) perm_scatter_kernel(int R, int E, const int32_t* __restrict__ counts,
                                                             RouteArrays ra) {
     __shared__ int run[kMaxExperts];
     __shared__ uint8_t wh[32 * kMaxExperts];
+    grid_dep_wait();
     for (int i = threadIdx.x; i < E; i += blockDim.x) run[i] = counts[(size_t)blockIdx.x * E + i];
     for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) wh[i] = 0;
     __syncthreads();
@@ -266,21 +273,27 @@ size_t route_scratch_words(int T, int E, int top_k) {
 
 void launch_route(const float* logits, int T, int E, int k, RouteArrays ra, int32_t* d_status, cudaStream_t s) {
     const int R = T * k;
+    if (logits) {
+        // one warp per token, 8 tokens per CTA: the top-k work spreads over SMs
+        NVFP4_LAUNCH("route_topk", s,
+                     launch_pdl(topk_kernel, dim3((T + 7) / 8), dim3(256), 0, s, logits, T, E, k, ra.ids, ra.w));
+    }
     if (R <= kSmallMaxRows) {
-        NVFP4_LAUNCH("route_small", s, route_small_kernel<<<1, 1024, 0, s>>>(logits, T, E, k, ra, d_status));
+        NVFP4_LAUNCH("route_perm", s,
+                     launch_pdl(route_perm_small_kernel, dim3(1), dim3(1024), 0, s, T, E, k, logits ? 0 : 1, ra,
+                                d_status));
         return;
     }
-    if (logits) {
-        NVFP4_LAUNCH("route_topk", s,
-                     topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(logits, T, E, k, ra.ids, ra.w));
-    } else {
+    if (!logits) {
         NVFP4_LAUNCH("route_validate", s,
-                     validate_ids_kernel<<<(R + 255) / 256, 256, 0, s>>>(ra.ids, R, E, d_status));
+                     launch_pdl(validate_ids_kernel, dim3((R + 255) / 256), dim3(256), 0, s, ra.ids, R, E, d_status));
     }
     const int nb = (R + kChunkRows - 1) / kChunkRows;
-    NVFP4_LAUNCH("route_count", s, perm_count_kernel<<<nb, 1024, 0, s>>>(ra.ids, R, E, ra.counts));
-    NVFP4_LAUNCH("route_scan", s, perm_scan_kernel<<<1, 1024, 0, s>>>(nb, E, ra.counts, ra));
-    NVFP4_LAUNCH("route_scatter", s, perm_scatter_kernel<<<nb, 1024, 0, s>>>(R, E, ra.counts, ra));
+    NVFP4_LAUNCH("route_count", s,
+                 launch_pdl(perm_count_kernel, dim3(nb), dim3(1024), 0, s, (const int32_t*)ra.ids, R, E, ra.counts));
+    NVFP4_LAUNCH("route_scan", s, launch_pdl(perm_scan_kernel, dim3(1), dim3(1024), 0, s, nb, E, ra.counts, ra));
+    NVFP4_LAUNCH("route_scatter", s,
+                 launch_pdl(perm_scatter_kernel, dim3(nb), dim3(1024), 0, s, R, E, (const int32_t*)ra.counts, ra));
 }
 
 // Route workspace layout (shared with the MoE workspace's routing block).
@@ -314,7 +327,8 @@ extern "C" nvfp4_status moe_route_permute(const float* logits, int T, int E, int
     if (T < 0) return NVFP4_ERR_INVALID_ARG;
     if (E < 1 || E > kMaxExperts || top_k < 1 || top_k > kMaxTopK || top_k > E) return NVFP4_ERR_SHAPE;
     if ((size_t)T * top_k > (size_t)INT_MAX / 2) return NVFP4_ERR_SHAPE;
-    if (!logits || !topk_ids || !topk_w || !expert_offsets || !row_to_slot || !slot_to_row || !ws)
+    // T == 0: nothing is read; the offsets are still written (all zero)
+    if ((T > 0 && (!logits || !topk_ids || !topk_w || !row_to_slot || !slot_to_row)) || !expert_offsets || !ws)
         return NVFP4_ERR_INVALID_ARG;
     if (!aligned16(logits) || !aligned16(topk_ids) || !aligned16(topk_w) || !aligned16(expert_offsets) ||
         !aligned16(row_to_slot) || !aligned16(slot_to_row) || !aligned16(ws))
@@ -323,7 +337,11 @@ extern "C" nvfp4_status moe_route_permute(const float* logits, int T, int E, int
     Carver c(ws);
     RouteWs rw = carve_route_ws(c, T, E, top_k);
     RouteArrays ra{topk_ids, topk_w, expert_offsets, row_to_slot, slot_to_row,
-                   rw.active, rw.n_active, rw.tile_start, rw.counts};
+                   rw.active, rw.n_active, rw.tile_start, rw.counts, nullptr, 0};
+    if (T == 0) {
+        launch_zero(expert_offsets, sizeof(int32_t) * (E + 1), stream);
+        return last_launch_status();
+    }
     launch_route(logits, T, E, top_k, ra, nullptr, stream);
     return last_launch_status();
 }

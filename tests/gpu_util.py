@@ -12,7 +12,20 @@ def bf16_to_f32(t: torch.Tensor) -> np.ndarray:
     return t.detach().float().cpu().numpy()
 
 
+def bf16_ulp(v: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 values at |v| (8 significant bits)."""
+    a = np.abs(np.asarray(v, np.float64))
+    e = np.floor(np.log2(np.where(a > 0, a, 2.0 ** -133)))
+    return np.exp2(np.maximum(e, -126) - 7)
+
+
 def assert_layer_close(got: np.ndarray, ref: np.ndarray, what=""):
+    """rel L2 <= 5e-3, and every element within 2e-2 * rms(ref) of the
+    oracle or on a bf16 neighbour of it: the kernels sum in fp32 in another
+    order than the oracle's fp64 sum, so a value within ~2^-24 of a bf16
+    rounding midpoint can land on the adjacent bf16 value at the final
+    rounding; for an element above ~2.6 * rms that one step alone exceeds
+    2e-2 * rms."""
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     assert got.shape == ref.shape
@@ -20,9 +33,13 @@ def assert_layer_close(got: np.ndarray, ref: np.ndarray, what=""):
     rms = np.sqrt(np.mean(ref ** 2))
     assert rms > 0
     rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
-    mabs = np.abs(got - ref).max()
-    assert rel <= REL_L2 and mabs <= MAX_ABS_RMS * rms, f"{what}: rel_l2={rel:.3g} max_abs/rms={mabs / rms:.3g}"
-    return rel, mabs / rms
+    err = np.abs(got - ref)
+    allowed = np.maximum(MAX_ABS_RMS * rms, bf16_ulp(ref) * 1.0000001)
+    worst = np.argmax(err / allowed)
+    assert rel <= REL_L2 and np.all(err <= allowed), (
+        f"{what}: rel_l2={rel:.3g} max_abs/rms={err.max() / rms:.3g} worst: got {got.flat[worst]} "
+        f"ref {ref.flat[worst]}")
+    return rel, err.max() / rms
 
 
 def oracle_bank(orc, banks: dict, experts=None):

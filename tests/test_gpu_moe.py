@@ -138,7 +138,7 @@ def test_zero_tokens():
     assert out.shape == (0, s.d)
 
 
-@pytest.mark.parametrize("M,K,N", [(7, 256, 128), (64, 1024, 512), (130, 512, 96)])
+@pytest.mark.parametrize("M,K,N", [(7, 256, 128), (64, 1024, 512), (130, 512, 192)])
 def test_dense_linear_and_mlp(orc, M, K, N):
     x = synth.make_x(M, K, seed=M, device="cuda", outlier_frac=0.05)
     wg = synth.make_weights(1, N, K, 10 + M, "cuda")[0]
