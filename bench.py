@@ -145,6 +145,7 @@ WORKLOADS = {
     "skew_w4a16": (synth.SKEW, "w4a16", "zipf", 0.0),
     "skew_w4a4": (synth.SKEW, "w4a4", "zipf", 0.0),
     "skew_masked_w4a16": (synth.SKEW, "w4a16", "zipf_masked", 0.0),
+    "dense": (None, "w4a16", "dense", 0.05),
 }
 
 
@@ -249,6 +250,47 @@ class Layer:
     def flops(self):
         s = self.shape
         return 6.0 * s.T * s.k * s.d * s.F
+
+
+class DenseLayer:
+    """Dense NVFP4 MLP (gate and up with different tensor scales, SwiGLU,
+    down): two nvfp4_linear calls per step."""
+
+    def __init__(self, name, lib, device, seed, n_batches=2):
+        self.name = name
+        d, F, M = synth.DENSE["d"], synth.DENSE["F"], synth.DENSE["M"]
+        self.shape = synth.MoEShape(M, d, 1, 1, F)
+        self.mode = "w4a16"
+        self.kind = "dense"
+        self.lib = lib
+        self.device = device
+        self.wg = lib.nvfp4_quantize_weights(synth.make_weights(1, F, d, seed * 10 + 3, device)[0])
+        self.wu = lib.nvfp4_quantize_weights(synth.make_weights(1, F, d, seed * 10 + 4, device)[0] * 2)
+        self.wd = lib.nvfp4_quantize_weights(synth.make_weights(1, d, F, seed * 10 + 5, device)[0])
+        torch.cuda.empty_cache()
+        self.batches = [(synth.make_x(M, d, seed * 100 + 2 * b, device, 0.05), None) for b in range(n_batches)]
+        self.h = torch.empty(M, F, dtype=torch.bfloat16, device=device)
+        self.out = torch.empty(M, d, dtype=torch.bfloat16, device=device)
+        self.ws1 = torch.empty(lib.load().nvfp4_linear_workspace_size(M, d, F), dtype=torch.uint8, device=device)
+        self.ws2 = torch.empty(lib.load().nvfp4_linear_workspace_size(M, F, d), dtype=torch.uint8, device=device)
+        self.is13 = self.is2 = None
+
+    def step(self, i, x=None, lg=None):
+        if x is None:
+            x = self.batches[i % len(self.batches)][0]
+        self.lib.nvfp4_linear(x, self.wg, self.wu, out=self.h, ws=self.ws1)
+        return self.lib.nvfp4_linear(self.h, self.wd, out=self.out, ws=self.ws2)
+
+    def touched_experts(self, i):
+        return 1
+
+    def algorithmic_bytes(self, touched):
+        s = self.shape
+        return 3 * s.d * s.F * 9 // 16 + 2 * s.T * s.d * 2, s.T
+
+    def flops(self):
+        s = self.shape
+        return 6.0 * s.T * s.d * s.F
 
 
 def time_steps(layer, steps, flush, start=0):
@@ -358,7 +400,7 @@ def run_ours(args):
     flush_mb = 256
     flush = torch.empty(flush_mb << 20, dtype=torch.uint8, device=dev)
     seed = 1001 + 17 * rank
-    layer = Layer(args.workload, lib, dev, seed)
+    layer = (DenseLayer if args.workload == "dense" else Layer)(args.workload, lib, dev, seed)
 
     for i in range(args.warmup):
         layer.step(i)
@@ -385,17 +427,35 @@ def run_ours(args):
     e2e_value, _ = aggregate(layer.shape.T, e2e_ms, world, dev)
 
     total_bytes, R = layer.algorithmic_bytes(touched)
-    gu_name = "gemv_gateup_w4a16" if layer.mode == "w4a16" else "gemv_gateup_w4a4"
     kernels = {k: {"launches": v[0], "ms_per_launch": v[1] / max(1, v[0])} for k, v in prof.items()}
-    dom = max(kernels, key=lambda k: kernels[k]["ms_per_launch"] * kernels[k]["launches"]) if kernels else gu_name
-    if dom.startswith("gemv_down"):
-        s = layer.shape
-        dom_bytes = touched * s.d * s.F * 9 // 16 + (R * s.F * 2 if layer.mode == "w4a16" else R * s.F * 9 // 16)
-    else:
-        dom_bytes = layer.gateup_bytes(touched)
+    dom = max(kernels, key=lambda k: kernels[k]["ms_per_launch"] * kernels[k]["launches"]) if kernels else "?"
+    s_ = layer.shape
     dom_ms = kernels.get(dom, {"ms_per_launch": float("nan")})["ms_per_launch"]
-    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+    if dom.startswith("tc_"):
+        # tensor-bound: f16 MMA (the bf16/f16 dense rate), flops of one launch
+        nproj = 2 if "gateup" in dom else 1
+        rows = R if layer.kind != "dense" else s_.T
+        if layer.kind == "dense":
+            dom_flops = 2.0 * rows * s_.d * s_.F * nproj
+        else:
+            dom_flops = 2.0 * rows * s_.d * s_.F * nproj
+        achieved = dom_flops / (dom_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": bf16, "unit": "TFLOP/s",
+                "frac": achieved / bf16, "peak_kind": f"{peak_kind} bf16 dense (f16 runs at the same rate), burst",
+                "traffic": recorded_traffic(dom, args.workload), "algorithmic_flops_per_launch": dom_flops}
+    else:
+        if dom.startswith("gemv_down"):
+            dom_bytes = touched * s_.d * s_.F * 9 // 16 + (R * s_.F * 2 if layer.mode == "w4a16" else R * s_.F * 9 // 16)
+        else:
+            dom_bytes = layer.gateup_bytes(touched)
+        achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "peak_kind": f"{peak_kind} (copy bandwidth, burst)",
+                "traffic": recorded_traffic(dom, args.workload), "algorithmic_bytes_per_launch": dom_bytes}
     layer_gbs = total_bytes / (ms / 1e3) / 1e9
+    layer_tflops = layer.flops() / (ms / 1e3) / 1e12
+    roof.update({"layer_gbs": layer_gbs, "layer_frac_hbm": layer_gbs / hbm, "layer_tflops": layer_tflops,
+                 "layer_frac_bf16": layer_tflops / bf16, "touched_experts": touched})
 
     line = {
         "metric": "MoE-layer tokens/s (decode-shaped routed NVFP4 layer)",
@@ -405,11 +465,7 @@ def run_ours(args):
                  else "e2m1+e4m3 weights and activations, f16 mma, f32 accumulate",
         "data": "synthetic (seeded N(0,1) x and logits, N(0,0.02) bf16 weights quantised by the library)",
         "config": workload_config(layer, flush_mb),
-        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "peak_kind": f"{peak_kind} (copy bandwidth, burst)",
-                     "traffic": recorded_traffic(dom, args.workload), "algorithmic_bytes_per_launch": dom_bytes,
-                     "layer_gbs": layer_gbs, "layer_frac": layer_gbs / hbm,
-                     "touched_experts": touched},
+        "roofline": roof,
         "kernels": kernels,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},
@@ -433,7 +489,7 @@ def run_ours(args):
             del sl
             torch.cuda.empty_cache()
         line["sweep"] = sweep
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and args.workload != "dense":
         line["cpu_baseline"] = cpu_baseline(layer, seed, n_tokens=args.cpu_tokens)
     if rank == 0:
         print(json.dumps(line), flush=True)

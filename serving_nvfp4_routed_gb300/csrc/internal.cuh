@@ -7,7 +7,8 @@ namespace nvfp4 {
 
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
-constexpr int kGemvTokTile = 8;  // tokens per work item of the decode-shaped kernel
+constexpr int kGemvTokTile = 8;   // rows per work item of the decode-shaped kernel
+constexpr int kTcTokTile = 128;   // rows per work unit of the tensor-core kernel
 
 // Routing outputs plus the grouping metadata the expert kernels walk.
 struct RouteArrays {
@@ -19,6 +20,7 @@ struct RouteArrays {
     int32_t* active;       // [E]   experts with rows, ascending
     int32_t* n_active;     // [1]
     int32_t* tile_start;   // [E+1] prefix over active experts of ceil(rows / kGemvTokTile)
+    int32_t* tile_start_tc;  // [E+1] prefix over active experts of ceil(rows / kTcTokTile)
     int32_t* counts;       // [n_blocks * E] scratch for the multi-block path
     int32_t* clear;        // [n_clear] zeroed by the route launch (work and completion counters)
     int n_clear;
@@ -81,5 +83,32 @@ size_t gemv_smem_bytes(int K);
 bool gemv_supported_k(int K);
 void launch_gemv(int bmode, int outmode, const GemvArgs& a, int max_work, cudaStream_t s);
 
-// W4A16 prep and the counters the kernels use are zeroed by the route launch.
+// ---- prompt-shaped grouped GEMM (tcgen05, accumulators in TMEM) ----
+enum TcOut { TC_OUT_H = 0, TC_OUT_COMBINE = 1, TC_OUT_BF16 = 2 };
+
+struct TcArgs {
+    int K, N, top_k;
+    const int32_t* offsets;      // [E+1]
+    const int32_t* active;       // [E]
+    const int32_t* n_active;     // [1]
+    const int32_t* tile_start;   // [E+1] prefix of ceil(rows / kTcTokTile) over active experts
+    const int32_t* row_to_slot;  // [R] (nullptr: row == token)
+    const uint8_t* a_codes[2];   // [E, N, K/2]
+    const uint8_t* a_scales[2];  // [E, N, K/16]
+    const float* a_ws2[2];       // [E]
+    const uint16_t* b_f16;       // f16 rows, value = f16 * 2^b_exp[row]
+    const int32_t* b_exp;
+    int b_by_token;              // B row = token of the permuted row (x) or the row itself (h)
+    uint16_t* h_out;             // TC_OUT_H: [R, N] bf16 SwiGLU
+    float* acc_out;              // TC_OUT_COMBINE: [T, N] fp32, zeroed before
+    const float* topk_w;         // TC_OUT_COMBINE: [T*k]
+    uint16_t* y_out;             // TC_OUT_BF16: [R, N]
+    int32_t* status;             // optional: NVFP4_ERR_TIMEOUT if a bounded wait expired
+};
+
+size_t tc_smem_bytes(int nproj);
+void launch_tc_gemm(int outmode, int nproj, const TcArgs& a, int max_units, cudaStream_t s);
+void launch_rows_to_f16(const uint16_t* src, int rows, int K, uint16_t* dst, int32_t* exps, float* zero_rows,
+                        int zero_len, cudaStream_t s);
+void launch_acc_to_bf16(const float* acc, size_t n, uint16_t* out, cudaStream_t s);
 }  // namespace nvfp4

@@ -12,6 +12,8 @@
 //   down + weighted combine (fp32 red.add); the CTA that adds a token's last
 //   contribution writes that token's bf16 output row
 #include <climits>
+#include <cstdlib>
+#include <cstring>
 
 #include "common.cuh"
 #include "internal.cuh"
@@ -31,7 +33,32 @@ struct MoeWs {
     uint8_t* hs;      // [R, F/16]  W4A4
     float* acc;       // [T, d]
     int* clear;       // [kCounters + T]: work counters, then per-token completion counts
+    // prompt-shaped (tensor-core) path, W4A16
+    uint16_t* xh;     // [T, d]  f16 x * 2^-s
+    int32_t* x_exp;   // [T]
+    uint16_t* hh;     // [R, F]  f16 h * 2^-s
+    int32_t* h_exp;   // [R]
 };
+
+bool tc_possible(int mode, int d, int F) { return mode == 0 && d % 128 == 0 && F % 128 == 0; }
+
+// NVFP4_PATH=gemv|tc forces a path (tests exercise both at every size).
+int forced_path() {
+    const char* e = std::getenv("NVFP4_PATH");
+    if (!e) return -1;
+    if (!std::strcmp(e, "gemv")) return 0;
+    if (!std::strcmp(e, "tc")) return 1;
+    return -1;
+}
+
+// Tensor cores once the experts average 32 or more routed rows.
+bool use_tc(int mode, int T, int E, int k, int d, int F) {
+    if (!tc_possible(mode, d, F)) return false;
+    const int f = forced_path();
+    if (f >= 0) return f == 1;
+    const long long R = (long long)T * k;
+    return R >= 32LL * std::min<long long>(E, R);
+}
 
 MoeWs carve_moe(void* base, int T, int E, int k, int d, int F, int mode, size_t* bytes) {
     Carver c(base);
@@ -45,6 +72,7 @@ MoeWs carve_moe(void* base, int T, int E, int k, int d, int F, int mode, size_t*
     w.ra.active = c.take<int32_t>(E);
     w.ra.n_active = c.take<int32_t>(4);
     w.ra.tile_start = c.take<int32_t>(E + 1);
+    w.ra.tile_start_tc = c.take<int32_t>(E + 1);
     w.ra.counts = c.take<int32_t>(route_scratch_words(T, E, k) + 1);
     w.clear = c.take<int>(kCounters + (size_t)T);
     w.ra.clear = w.clear;
@@ -52,6 +80,12 @@ MoeWs carve_moe(void* base, int T, int E, int k, int d, int F, int mode, size_t*
     w.acc = c.take<float>((size_t)T * d);
     if (mode == 0) {
         w.h = c.take<uint16_t>(R * F);
+        if (tc_possible(mode, d, F)) {
+            w.xh = c.take<uint16_t>((size_t)T * d);
+            w.x_exp = c.take<int32_t>(T + 1);
+            w.hh = c.take<uint16_t>(R * F);
+            w.h_exp = c.take<int32_t>(R + 1);
+        }
     } else {
         w.xq = c.take<uint8_t>(R * (d / 2));
         w.xs = c.take<uint8_t>(R * (d / 16));
@@ -121,6 +155,47 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
     if (mode == 1)
         launch_quantize_act(x, R, d, ws.ra.row_to_slot, top_k, is13, ws.ra.offsets, E, ws.xq, ws.xs, s);
 
+    if (use_tc(mode, T, E, top_k, d, F)) {
+        // x -> f16 rows (and zero the combine accumulator)
+        launch_rows_to_f16(x, T, d, ws.xh, ws.x_exp, ws.acc, d, s);
+        TcArgs t{};
+        t.top_k = top_k;
+        t.offsets = ws.ra.offsets;
+        t.active = ws.ra.active;
+        t.n_active = ws.ra.n_active;
+        t.tile_start = ws.ra.tile_start_tc;
+        t.row_to_slot = ws.ra.row_to_slot;
+        t.topk_w = ws.ra.w;
+        t.status = d_status;
+        const int max_units = (R / kTcTokTile + std::min(E, R) + 1) * (std::max(d, F) / 128);
+        // gate/up + SwiGLU -> h (bf16)
+        t.K = d;
+        t.N = F;
+        t.a_codes[0] = w->gate.codes;  t.a_scales[0] = w->gate.scales;  t.a_ws2[0] = w->gate.weight_scale_2;
+        t.a_codes[1] = w->up.codes;    t.a_scales[1] = w->up.scales;    t.a_ws2[1] = w->up.weight_scale_2;
+        t.b_f16 = ws.xh;
+        t.b_exp = ws.x_exp;
+        t.b_by_token = 1;
+        t.h_out = ws.h;
+        launch_tc_gemm(TC_OUT_H, 2, t, max_units, s);
+        // h -> f16 rows
+        launch_rows_to_f16(ws.h, R, F, ws.hh, ws.h_exp, nullptr, 0, s);
+        // down + weighted combine
+        TcArgs u = t;
+        u.K = F;
+        u.N = d;
+        u.a_codes[0] = w->down.codes;  u.a_scales[0] = w->down.scales;  u.a_ws2[0] = w->down.weight_scale_2;
+        u.a_codes[1] = u.a_codes[0];   u.a_scales[1] = u.a_scales[0];   u.a_ws2[1] = u.a_ws2[0];
+        u.b_f16 = ws.hh;
+        u.b_exp = ws.h_exp;
+        u.b_by_token = 0;
+        u.h_out = nullptr;
+        u.acc_out = ws.acc;
+        launch_tc_gemm(TC_OUT_COMBINE, 1, u, max_units, s);
+        launch_acc_to_bf16(ws.acc, (size_t)T * d, out, s);
+        return last_launch_status();
+    }
+
     const int tiles = expected_tiles(R, E);
     GemvArgs a = base_args(ws, top_k);
     // gate/up + SwiGLU (also zeroes the fp32 combine accumulator)
@@ -175,20 +250,36 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
 
 // ---- dense linear ----
 struct LinWs {
-    int32_t* meta;     // offsets[2], active[1], n_active[1], tile_start[2]
+    int32_t* meta;     // offsets[2], active[1], n_active[1], tile_start[2], tile_start_tc[2]
     int* counters;
+    uint16_t* xh;      // [M, K] (tensor-core path)
+    int32_t* x_exp;    // [M]
 };
 
-LinWs carve_lin(void* base, size_t* bytes) {
+bool lin_tc_possible(int N) { return N % 128 == 0; }
+
+bool use_tc_linear(int M, int N) {
+    if (!lin_tc_possible(N)) return false;
+    const int f = forced_path();
+    if (f >= 0) return f == 1;
+    return M >= 128;
+}
+
+LinWs carve_lin(void* base, int M, int K, int N, size_t* bytes) {
     Carver c(base);
-    LinWs l;
+    LinWs l{};
     l.meta = c.take<int32_t>(8);
     l.counters = c.take<int>(kCounters);
+    if (lin_tc_possible(N)) {
+        l.xh = c.take<uint16_t>((size_t)M * K);
+        l.x_exp = c.take<int32_t>(M + 1);
+    }
     if (bytes) *bytes = align_up(c.off, 256);
     return l;
 }
 
 __global__ void linear_prep_kernel(int M, int32_t* meta, int* counters) {
+    grid_dep_wait();
     if (threadIdx.x == 0) {
         meta[0] = 0;                                      // offsets[0]
         meta[1] = M;                                      // offsets[1]
@@ -196,6 +287,8 @@ __global__ void linear_prep_kernel(int M, int32_t* meta, int* counters) {
         meta[3] = 1;                                      // n_active
         meta[4] = 0;                                      // tile_start[0]
         meta[5] = (M + kGemvTokTile - 1) / kGemvTokTile;  // tile_start[1]
+        meta[6] = 0;                                      // tile_start_tc[0]
+        meta[7] = (M + kTcTokTile - 1) / kTcTokTile;      // tile_start_tc[1]
     }
     if (threadIdx.x < kCounters) counters[threadIdx.x] = 0;
 }
@@ -241,11 +334,9 @@ extern "C" nvfp4_status nvfp4_moe_w4a4(const uint16_t* x, int T, const float* lo
 }
 
 extern "C" size_t nvfp4_linear_workspace_size(int M, int K, int N) {
-    (void)K;
-    (void)N;
-    if (M < 0) return 0;
+    if (M < 0 || K < 0 || N < 0) return 0;
     size_t b = 0;
-    carve_lin(nullptr, &b);
+    carve_lin(nullptr, M, K, N, &b);
     return b;
 }
 
@@ -259,8 +350,36 @@ extern "C" nvfp4_status nvfp4_linear(const uint16_t* x, int M, int K, const nvfp
     if (!aligned16(x) || !aligned16(out) || !aligned16(ws) || !w_aligned(*w) || (w_up && !w_aligned(*w_up)))
         return NVFP4_ERR_ALIGN;
     if (ws_bytes < nvfp4_linear_workspace_size(M, K, N)) return NVFP4_ERR_WORKSPACE;
-    LinWs l = carve_lin(ws, nullptr);
-    NVFP4_LAUNCH("linear_prep", stream, linear_prep_kernel<<<1, 32, 0, stream>>>(M, l.meta, l.counters));
+    LinWs l = carve_lin(ws, M, K, N, nullptr);
+    NVFP4_LAUNCH("linear_prep", stream, launch_pdl(linear_prep_kernel, dim3(1), dim3(32), 0, stream, M, l.meta,
+                                                   l.counters));
+    if (use_tc_linear(M, N)) {
+        launch_rows_to_f16(x, M, K, l.xh, l.x_exp, nullptr, 0, stream);
+        TcArgs t{};
+        t.K = K;
+        t.N = N;
+        t.top_k = 1;
+        t.offsets = l.meta + 0;
+        t.active = l.meta + 2;
+        t.n_active = l.meta + 3;
+        t.tile_start = l.meta + 6;
+        t.row_to_slot = nullptr;
+        t.a_codes[0] = w->codes;  t.a_scales[0] = w->scales;  t.a_ws2[0] = w->weight_scale_2;
+        t.a_codes[1] = w->codes;  t.a_scales[1] = w->scales;  t.a_ws2[1] = w->weight_scale_2;
+        t.b_f16 = l.xh;
+        t.b_exp = l.x_exp;
+        t.b_by_token = 1;
+        const int max_units = ((M + kTcTokTile - 1) / kTcTokTile) * (N / 128);
+        if (w_up) {
+            t.a_codes[1] = w_up->codes;  t.a_scales[1] = w_up->scales;  t.a_ws2[1] = w_up->weight_scale_2;
+            t.h_out = out;
+            launch_tc_gemm(TC_OUT_H, 2, t, max_units, stream);
+        } else {
+            t.y_out = out;
+            launch_tc_gemm(TC_OUT_BF16, 1, t, max_units, stream);
+        }
+        return last_launch_status();
+    }
     GemvArgs a{};
     a.K = K;
     a.N = N;

@@ -1,0 +1,391 @@
+// moe_tc.cu -- prompt-shaped grouped NVFP4 expert GEMM on the 5th-generation
+// tensor cores (tcgen05, accumulators in tensor memory).
+//
+// TensorFold issue #308 "GLM-5.3-Flash on CUDA: read nvidia/GLM-5.3-Flash-NVFP4
+// (ModelOpt NVFP4) as stored, W4A16": "What the branch does" (routed experts
+// as one grouped kernel over bf16 rows, weight_scale_2 per expert; dense MLP
+// with gate and up apart) and "Questions", item 4 (prompts get their own
+// kernel, whose sums run in a different order from decode's).
+//
+// Work unit = (expert e, 128 output features f0.., 128 routed rows row0..):
+//   D[f, j] = sum_k W[e, f, k] * B[row0 + j, k]         (swap-AB: weights are A)
+// A: the NVFP4 weights, dequantised e2m1*e4m3 -> f16 (exact) by four
+//    producer warps straight into the 128-byte-swizzled K-major smem layout
+//    the MMA reads; B: f16 rows (x or h times a per-row power of two, exact
+//    for the inputs here) gathered by cp.async into the same layout; both
+//    through a ring of smem stages guarded by mbarriers.
+// One thread issues tcgen05.mma kind::f16 (M=128, N=128, K=16) into fp32
+// accumulators in TMEM, double-buffered so that the epilogue of one unit
+// overlaps the MMAs of the next; four epilogue warps (one TMEM lane quarter
+// each) read the accumulators with tcgen05.ld and apply SwiGLU, the
+// weighted combine (red.add) or a plain bf16 store.
+// Every mbarrier wait is bounded (about 2 s): on expiry the kernel records
+// NVFP4_ERR_TIMEOUT in the status word, every role leaves its loop, and the
+// CTA still frees its tensor memory before it exits.
+#include "common.cuh"
+#include "internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace nvfp4 {
+
+namespace {
+
+using namespace tc;
+
+constexpr int BM = 128, BN = kTcTokTile, BK = 64;  // features, rows, K per stage
+constexpr int kTileBytes = 128 * 128;                  // 128 rows x 64 f16
+constexpr int kTcWarps = 12;
+constexpr int kTcThreads = kTcWarps * 32;
+// warp roles
+constexpr int kWarpMma = 0, kWarpB = 1, kWarpEpi = 4, kWarpDeq = 8;
+constexpr int kPD = 4;  // k-stages of weights a dequant thread keeps in flight
+
+template <int NPROJ>
+struct Cfg {
+    static constexpr int kStages = NPROJ == 2 ? 4 : 6;
+    static constexpr int kStageBytes = (NPROJ + 1) * kTileBytes;
+    static constexpr int kSmem = kStages * kStageBytes + 1024;
+    static constexpr uint32_t kTmemCols = NPROJ == 2 ? 512 : 256;  // 2 accumulator buffers
+};
+
+struct Unit {
+    int e, row0, row_end, f0;
+};
+
+__device__ __forceinline__ Unit decode_unit(const TcArgs& a, int u, int n_active, int n_ft) {
+    int lo = 0, hi = n_active;  // largest ai with tile_start[ai] * n_ft <= u
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (a.tile_start[mid] * n_ft <= u) lo = mid; else hi = mid;
+    }
+    const int e = a.active[lo];
+    const int ntt = a.tile_start[lo + 1] - a.tile_start[lo];
+    const int local = u - a.tile_start[lo] * n_ft;
+    Unit un;
+    un.e = e;
+    un.f0 = (local / ntt) * BM;
+    un.row0 = a.offsets[e] + (local % ntt) * BN;
+    un.row_end = a.offsets[e + 1];
+    return un;
+}
+
+__device__ __forceinline__ int brow_of(const TcArgs& a, int row) {
+    return a.b_by_token ? (a.row_to_slot ? a.row_to_slot[row] / a.top_k : row) : row;
+}
+
+template <int OUT, int NPROJ>
+__global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const TcArgs a) {
+    using CF = Cfg<NPROJ>;
+    constexpr int S = CF::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ __align__(8) uint64_t bar_full_a[S], bar_full_b[S], bar_empty[S], bar_acc_full[2], bar_acc_empty[2];
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_abort;
+    __shared__ int s_brow[BN];
+
+    grid_dep_wait();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_u32(&bar_full_a[s]), 128);
+            mbar_init(smem_u32(&bar_full_b[s]), 32);
+            mbar_init(smem_u32(&bar_empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&bar_acc_full[b]), 1);
+            mbar_init(smem_u32(&bar_acc_empty[b]), 128);
+        }
+        s_abort = 0;
+        mbar_fence_init();
+    }
+    if (warp == kWarpMma) tmem_alloc(smem_u32(&s_tmem), CF::kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    volatile int* abort_flag = &s_abort;
+
+    const int n_active = *a.n_active;
+    const int n_ft = a.N / BM;
+    const int total = a.tile_start[n_active] * n_ft;
+    const int nk = a.K / BK;
+
+    if (warp == kWarpMma) {
+        // ---------------- MMA issue (one elected lane) ----------------
+        const uint32_t idesc = idesc_f16_f32(BM, BN);
+        int kcg = 0, it = 0;
+        for (int u = blockIdx.x; u < total; u += gridDim.x, ++it) {
+            const int as = it & 1;
+            bool ok = mbar_wait(smem_u32(&bar_acc_empty[as]), ((it >> 1) & 1) ^ 1, abort_flag, a.status);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
+            const uint32_t d_base = tmem + as * (NPROJ * BN);
+            for (int kc = 0; kc < nk; ++kc, ++kcg) {
+                const int s = kcg % S;
+                const uint32_t ph = (kcg / S) & 1;
+                ok = mbar_wait(smem_u32(&bar_full_a[s]), ph, abort_flag, a.status) &&
+                     mbar_wait(smem_u32(&bar_full_b[s]), ph, abort_flag, a.status);
+                if (!__all_sync(0xffffffffu, ok)) goto mma_done;
+                tc_fence_after();
+                fence_proxy_async();
+                if (lane == 0) {
+                    const uint32_t sb = smem_u32(smem + s * CF::kStageBytes);
+                    const uint64_t bdesc = sdesc_sw128(sb + NPROJ * kTileBytes);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+#pragma unroll
+                        for (int p = 0; p < NPROJ; ++p)
+                            mma_f16(d_base + p * BN, sdesc_sw128(sb + p * kTileBytes) + 2 * kk, bdesc + 2 * kk,
+                                    idesc, (kc | kk) != 0);
+                    mma_commit(smem_u32(&bar_empty[s]));
+                }
+                __syncwarp();
+            }
+            if (lane == 0) mma_commit(smem_u32(&bar_acc_full[as]));
+            __syncwarp();
+        }
+    mma_done:;
+    } else if (warp == kWarpB) {
+        // ---------------- B producer: gathered f16 rows via cp.async ----------------
+        int kcg = 0;
+        for (int u = blockIdx.x; u < total; u += gridDim.x) {
+            const Unit un = decode_unit(a, u, n_active, n_ft);
+            __syncwarp();
+            for (int i = lane; i < BN; i += 32) {
+                const int row = un.row0 + i;
+                s_brow[i] = row < un.row_end ? brow_of(a, row) : -1;
+            }
+            __syncwarp();
+            for (int kc = 0; kc < nk; ++kc, ++kcg) {
+                const int s = kcg % S;
+                const uint32_t ph = (kcg / S) & 1;
+                const bool ok = mbar_wait(smem_u32(&bar_empty[s]), ph ^ 1, abort_flag, a.status);
+                if (!__all_sync(0xffffffffu, ok)) goto b_done;
+                const uint32_t bt = smem_u32(smem + s * CF::kStageBytes + NPROJ * kTileBytes);
+                const int c = lane & 7;
+#pragma unroll 8
+                for (int i = 0; i < BN / 4; ++i) {
+                    const int rr = (lane >> 3) + 4 * i;
+                    const int br = s_brow[rr];
+                    const uint16_t* src = a.b_f16 + (size_t)(br < 0 ? 0 : br) * a.K + (size_t)kc * BK + c * 8;
+                    cp_async16(bt + rr * 128 + ((c ^ (rr & 7)) << 4), src, br < 0 ? 0u : 16u);
+                }
+                cp_async_arrive_noinc(smem_u32(&bar_full_b[s]));
+            }
+        }
+    b_done:;
+    } else if (warp >= kWarpEpi && warp < kWarpEpi + 4) {
+        // ---------------- epilogue: TMEM -> registers -> global ----------------
+        const int q = warp - kWarpEpi;  // TMEM lane quarter
+        const int et = q * 32 + lane;   // feature within the unit
+        int it = 0;
+        for (int u = blockIdx.x; u < total; u += gridDim.x, ++it) {
+            const Unit un = decode_unit(a, u, n_active, n_ft);
+            const int as = it & 1;
+            const bool ok = mbar_wait(smem_u32(&bar_acc_full[as]), (it >> 1) & 1, abort_flag, a.status);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
+            const int f = un.f0 + et;
+            const float w0 = a.a_ws2[0][un.e];
+            const float w1 = a.a_ws2[NPROJ - 1][un.e];
+            const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + as * (NPROJ * BN);
+            for (int cb = 0; cb < BN / 32; ++cb) {
+                uint32_t r0[32], r1[32];
+                tmem_ld32(tb + cb * 32, r0);
+                if constexpr (NPROJ == 2) tmem_ld32(tb + BN + cb * 32, r1);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int row = un.row0 + cb * 32 + j;
+                    if (row >= un.row_end) continue;
+                    const int br = brow_of(a, row);
+                    const float rs = exp2i(a.b_exp[br]);
+                    if constexpr (OUT == TC_OUT_H) {
+                        const float G = round_bf16(__fmul_rn(__fmul_rn(__uint_as_float(r0[j]), rs), w0));
+                        const float U = round_bf16(__fmul_rn(__fmul_rn(__uint_as_float(r1[j]), rs), w1));
+                        const float h = round_bf16(G / (1.0f + expf(-G)) * U);
+                        a.h_out[(size_t)row * a.N + f] = f32_to_bf16_bits(h);
+                    } else if constexpr (OUT == TC_OUT_COMBINE) {
+                        const int slot = a.row_to_slot[row];
+                        const float y = __fmul_rn(__fmul_rn(__uint_as_float(r0[j]), rs), w0);
+                        atomicAdd(a.acc_out + (size_t)(slot / a.top_k) * a.N + f, a.topk_w[slot] * y);
+                    } else {
+                        a.y_out[(size_t)row * a.N + f] =
+                            f32_to_bf16_bits(__fmul_rn(__fmul_rn(__uint_as_float(r0[j]), rs), w0));
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bar_acc_empty[as]));
+        }
+    } else if (warp >= kWarpDeq) {
+        // ---------------- A producer: NVFP4 weights -> f16 smem tiles ----------------
+        const int dt = threadIdx.x - kWarpDeq * 32;  // tile row
+        const size_t K2 = (size_t)a.K / 2, K16 = (size_t)a.K / 16;
+        uint32_t ring[kPD][NPROJ][9];
+        int kcg = 0;
+        for (int u = blockIdx.x; u < total; u += gridDim.x) {
+            const Unit un = decode_unit(a, u, n_active, n_ft);
+            const uint8_t* cp[NPROJ];
+            const uint8_t* sp[NPROJ];
+#pragma unroll
+            for (int p = 0; p < NPROJ; ++p) {
+                const size_t rowg = (size_t)un.e * a.N + un.f0 + dt;
+                cp[p] = a.a_codes[p] + rowg * K2;
+                sp[p] = a.a_scales[p] + rowg * K16;
+            }
+            auto load = [&](int slot, int kc) {
+#pragma unroll
+                for (int p = 0; p < NPROJ; ++p) {
+                    const uint4 c0 = __ldg(reinterpret_cast<const uint4*>(cp[p] + (size_t)kc * 32));
+                    const uint4 c1 = __ldg(reinterpret_cast<const uint4*>(cp[p] + (size_t)kc * 32) + 1);
+                    ring[slot][p][0] = c0.x; ring[slot][p][1] = c0.y; ring[slot][p][2] = c0.z; ring[slot][p][3] = c0.w;
+                    ring[slot][p][4] = c1.x; ring[slot][p][5] = c1.y; ring[slot][p][6] = c1.z; ring[slot][p][7] = c1.w;
+                    ring[slot][p][8] = __ldg(reinterpret_cast<const uint32_t*>(sp[p] + (size_t)kc * 4));
+                }
+            };
+#pragma unroll
+            for (int i = 0; i < kPD; ++i)
+                if (i < nk) load(i, i);
+            for (int kc0 = 0; kc0 < nk; kc0 += kPD) {
+#pragma unroll
+                for (int uu = 0; uu < kPD; ++uu) {
+                    const int kc = kc0 + uu;
+                    if (kc >= nk) break;
+                    const int s = kcg % S;
+                    const uint32_t ph = (kcg / S) & 1;
+                    const bool ok = mbar_wait(smem_u32(&bar_empty[s]), ph ^ 1, abort_flag, a.status);
+                    if (!__all_sync(0xffffffffu, ok)) goto deq_done;
+                    uint8_t* st = smem + s * CF::kStageBytes;
+#pragma unroll
+                    for (int p = 0; p < NPROJ; ++p) {
+                        uint8_t* rowp = st + p * kTileBytes + dt * 128;
+                        const uint32_t sw = ring[uu][p][8];
+#pragma unroll
+                        for (int w = 0; w < 8; ++w) {
+                            const int blk = w >> 1;
+                            const uint32_t S2 = f16x2_bcast(e4m3x2_to_f16x2((sw >> (16 * (blk >> 1))) & 0xFFFFu), blk & 1);
+                            uint32_t f[4];
+                            e2m1x8_to_f16x8(ring[uu][p][w], f);
+                            *reinterpret_cast<uint4*>(rowp + ((w ^ (dt & 7)) << 4)) =
+                                make_uint4(hmul2_u32(f[0], S2), hmul2_u32(f[1], S2), hmul2_u32(f[2], S2),
+                                           hmul2_u32(f[3], S2));
+                        }
+                    }
+                    fence_proxy_async();
+                    mbar_arrive(smem_u32(&bar_full_a[s]));
+                    if (kc + kPD < nk) load(uu, kc + kPD);
+                    ++kcg;
+                }
+            }
+        }
+    deq_done:;
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kWarpMma) {
+        tc_fence_after();
+        tmem_dealloc(tmem, CF::kTmemCols);
+    }
+    grid_dep_launch();
+}
+
+template <int OUT, int NPROJ>
+void launch_tc_t(const TcArgs& a, int max_units, cudaStream_t s, const char* name) {
+    auto kern = tc_gemm_kernel<OUT, NPROJ>;
+    static bool init = false;
+    if (!init) {
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<NPROJ>::kSmem);
+        init = true;
+    }
+    const int grid = std::max(1, std::min(max_units, num_sms()));
+    NVFP4_LAUNCH(name, s, launch_pdl(kern, dim3(grid), dim3(kTcThreads), (size_t)Cfg<NPROJ>::kSmem, s, a));
+}
+
+// ---------------------------------------------------------------------------
+// bf16 rows -> f16 rows times 2^-s(row), s from the row's max |v| so that the
+// row max lands in [2^14, 2^15); exp[row] = s.  Optionally zeroes a float
+// row of the same index (the combine accumulator).
+// ---------------------------------------------------------------------------
+__global__ void rows_to_f16_kernel(const uint16_t* __restrict__ src, int rows, int K, uint16_t* __restrict__ dst,
+                                   int32_t* __restrict__ exps, float* __restrict__ zero_rows, int zero_len) {
+    grid_dep_wait();
+    __shared__ float red[32];
+    for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+        const uint4* s4 = reinterpret_cast<const uint4*>(src + (size_t)r * K);
+        float m = 0.0f;
+        for (int i = threadIdx.x; i < K / 8; i += blockDim.x) {
+            const uint4 u = __ldg(s4 + i);
+            const uint32_t ww[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                m = fmaxf(m, fmaxf(fabsf(bf16_bits_to_f32(ww[j] & 0xFFFFu)), fabsf(bf16_bits_to_f32(ww[j] >> 16))));
+        }
+        m = warp_max(m);
+        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+        __syncthreads();
+        float v = (threadIdx.x & 31) < (blockDim.x >> 5) ? red[threadIdx.x & 31] : 0.0f;
+        v = warp_max(v);
+        const int sexp = row_exponent(v);
+        const float down = exp2i(-sexp);
+        if (threadIdx.x == 0) exps[r] = sexp;
+        uint4* d4 = reinterpret_cast<uint4*>(dst + (size_t)r * K);
+        for (int i = threadIdx.x; i < K / 8; i += blockDim.x) {
+            const uint4 u = __ldg(s4 + i);
+            uint4 o;
+            o.x = f32x2_to_f16x2(bf16_bits_to_f32(u.x & 0xFFFFu) * down, bf16_bits_to_f32(u.x >> 16) * down);
+            o.y = f32x2_to_f16x2(bf16_bits_to_f32(u.y & 0xFFFFu) * down, bf16_bits_to_f32(u.y >> 16) * down);
+            o.z = f32x2_to_f16x2(bf16_bits_to_f32(u.z & 0xFFFFu) * down, bf16_bits_to_f32(u.z >> 16) * down);
+            o.w = f32x2_to_f16x2(bf16_bits_to_f32(u.w & 0xFFFFu) * down, bf16_bits_to_f32(u.w >> 16) * down);
+            d4[i] = o;
+        }
+        if (zero_rows) {
+            float4* z = reinterpret_cast<float4*>(zero_rows + (size_t)r * zero_len);
+            for (int i = threadIdx.x; i < zero_len / 4; i += blockDim.x) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        __syncthreads();
+    }
+    grid_dep_launch();
+}
+
+__global__ void acc_to_bf16_kernel(const float* __restrict__ acc, size_t n4, uint16_t* __restrict__ out) {
+    grid_dep_wait();
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
+        const float4 v = reinterpret_cast<const float4*>(acc)[i];
+        uint2 o;
+        o.x = (uint32_t)f32_to_bf16_bits(v.x) | ((uint32_t)f32_to_bf16_bits(v.y) << 16);
+        o.y = (uint32_t)f32_to_bf16_bits(v.z) | ((uint32_t)f32_to_bf16_bits(v.w) << 16);
+        reinterpret_cast<uint2*>(out)[i] = o;
+    }
+    grid_dep_launch();
+}
+
+}  // namespace
+
+size_t tc_smem_bytes(int nproj) { return nproj == 2 ? Cfg<2>::kSmem : Cfg<1>::kSmem; }
+
+void launch_tc_gemm(int outmode, int nproj, const TcArgs& a, int max_units, cudaStream_t s) {
+    if (outmode == TC_OUT_H && nproj == 2) return launch_tc_t<TC_OUT_H, 2>(a, max_units, s, "tc_gateup_w4a16");
+    if (outmode == TC_OUT_COMBINE) return launch_tc_t<TC_OUT_COMBINE, 1>(a, max_units, s, "tc_down_w4a16");
+    if (outmode == TC_OUT_BF16) return launch_tc_t<TC_OUT_BF16, 1>(a, max_units, s, "tc_linear_w4a16");
+}
+
+void launch_rows_to_f16(const uint16_t* src, int rows, int K, uint16_t* dst, int32_t* exps, float* zero_rows,
+                        int zero_len, cudaStream_t s) {
+    if (rows <= 0) return;
+    const int grid = std::min(rows, num_sms() * 8);
+    NVFP4_LAUNCH("rows_to_f16", s,
+                 launch_pdl(rows_to_f16_kernel, dim3(grid), dim3(256), 0, s, src, rows, K, dst, exps, zero_rows,
+                            zero_len));
+}
+
+void launch_acc_to_bf16(const float* acc, size_t n, uint16_t* out, cudaStream_t s) {
+    const size_t n4 = n / 4;
+    if (n4 == 0) return;
+    const int grid = (int)std::min<size_t>((n4 + 255) / 256, (size_t)num_sms() * 8);
+    NVFP4_LAUNCH("acc_to_bf16", s, launch_pdl(acc_to_bf16_kernel, dim3(grid), dim3(256), 0, s, acc, n4, out));
+}
+
+}  // namespace nvfp4

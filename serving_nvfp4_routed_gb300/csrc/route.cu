@@ -128,13 +128,18 @@ __device__ void write_group_meta(int c, int E, const RouteArrays& ra, int* tmp32
     const int tiles = flag ? (c + kGemvTokTile - 1) / kGemvTokTile : 0;
     int tt;
     const int tpre = block_exclusive_scan(tiles, tmp32, tt);
+    const int tiles_tc = flag ? (c + kTcTokTile - 1) / kTcTokTile : 0;
+    int tt_tc;
+    const int tpre_tc = block_exclusive_scan(tiles_tc, tmp32, tt_tc);
     if (flag) {
         ra.active[aidx] = e;
         ra.tile_start[aidx] = tpre;
+        if (ra.tile_start_tc) ra.tile_start_tc[aidx] = tpre_tc;
     }
     if (e == 0) {
         *ra.n_active = na;
         ra.tile_start[na] = tt;
+        if (ra.tile_start_tc) ra.tile_start_tc[na] = tt_tc;
     }
     off_out = off;
 }
@@ -337,7 +342,7 @@ extern "C" nvfp4_status moe_route_permute(const float* logits, int T, int E, int
     Carver c(ws);
     RouteWs rw = carve_route_ws(c, T, E, top_k);
     RouteArrays ra{topk_ids, topk_w, expert_offsets, row_to_slot, slot_to_row,
-                   rw.active, rw.n_active, rw.tile_start, rw.counts, nullptr, 0};
+                   rw.active, rw.n_active, rw.tile_start, nullptr, rw.counts, nullptr, 0};
     if (T == 0) {
         launch_zero(expert_offsets, sizeof(int32_t) * (E + 1), stream);
         return last_launch_status();

@@ -26,7 +26,18 @@ def _setup(orc, shape, seed, outlier=0.0, kind="normal", experts_for=None):
     return inp, gw, ob, r, np.asarray(tokens, np.int32)
 
 
-def test_tiny_w4a16(orc):
+@pytest.fixture(params=["auto", "gemv", "tc"])
+def path(request, monkeypatch):
+    """Run the test with the library's own choice of kernel and with each
+    kernel forced (the tensor-core path needs d and F multiples of 128)."""
+    if request.param == "auto":
+        monkeypatch.delenv("NVFP4_PATH", raising=False)
+    else:
+        monkeypatch.setenv("NVFP4_PATH", request.param)
+    return request.param
+
+
+def test_tiny_w4a16(orc, path):
     s = synth.TINY
     inp, gw, ob, r, tok = _setup(orc, s, seed=1000)
     out = lib.nvfp4_moe_w4a16(inp["x"], inp["logits"], s.k, gw)
@@ -47,7 +58,7 @@ def test_tiny_w4a4(orc):
 
 @pytest.mark.parametrize("T,E,k,d,F", [(13, 8, 2, 256, 128), (40, 16, 4, 512, 256), (3, 5, 5, 192, 64),
                                        (100, 32, 8, 1024, 320)])
-def test_ragged_shapes_both_modes(orc, T, E, k, d, F):
+def test_ragged_shapes_both_modes(orc, T, E, k, d, F, path):
     s = synth.MoEShape(T, d, E, k, F)
     inp, gw, ob, r, tok = _setup(orc, s, seed=T + E, outlier=0.05)
     xb = synth.bf16_bits(inp["x"])
@@ -138,8 +149,8 @@ def test_zero_tokens():
     assert out.shape == (0, s.d)
 
 
-@pytest.mark.parametrize("M,K,N", [(7, 256, 128), (64, 1024, 512), (130, 512, 192)])
-def test_dense_linear_and_mlp(orc, M, K, N):
+@pytest.mark.parametrize("M,K,N", [(7, 256, 128), (64, 1024, 512), (130, 512, 192), (300, 256, 384)])
+def test_dense_linear_and_mlp(orc, M, K, N, path):
     x = synth.make_x(M, K, seed=M, device="cuda", outlier_frac=0.05)
     wg = synth.make_weights(1, N, K, 10 + M, "cuda")[0]
     wu = synth.make_weights(1, N, K, 20 + M, "cuda")[0] * 3  # different tensor scale
@@ -154,3 +165,54 @@ def test_dense_linear_and_mlp(orc, M, K, N):
     href_bits = synth.bf16_bits(torch.from_numpy(href).to(torch.bfloat16))  # the oracle's own h
     yref = orc.linear(href_bits, od[0], od[1], od[2])
     assert_layer_close(bf16_to_f32(y), yref, "down")
+
+
+@pytest.mark.parametrize("kind,mode", [("normal", "w4a16"), ("zipf", "w4a16"), ("zipf_masked", "w4a16"),
+                                       ("normal", "w4a4")])
+def test_prefill_sampled(orc, decode_bank, kind, mode):
+    """Prompt-shaped layers at full size (T=4096 for W4A16, skewed popularity
+    at T=16384, W4A4 at T=8192 with 5 % outlier rows); the oracle evaluates
+    a seeded sample of tokens."""
+    banks, gw = decode_bank
+    T = {"normal": 4096 if mode == "w4a16" else 8192, "zipf": 16384, "zipf_masked": 16384}[kind]
+    s = synth.MoEShape(T, 4096, 288, 8, 1536)
+    x = synth.make_x(T, s.d, 3001 + T, "cuda", outlier_frac=0.05)
+    logits = synth.make_logits(T, s.E, 3002 + T, "cuda", kind=kind)
+    r = orc.route(logits.cpu().numpy(), s.k)
+    rng = np.random.default_rng(T)
+    tok = np.sort(rng.choice(T, size=2, replace=False)).astype(np.int32)
+    if kind != "normal":
+        # include the most popular expert's first token
+        top = np.argmax(np.diff(r["offsets"]))
+        tok = np.unique(np.append(tok, np.where((r["ids"] == top).any(1))[0][0])).astype(np.int32)
+    experts = np.unique(r["ids"][tok])
+    ob = oracle_bank(orc, banks, experts)
+    if mode == "w4a16":
+        out = lib.nvfp4_moe_w4a16(x, logits, s.k, gw)
+        ref = orc.moe_layer("w4a16", synth.bf16_bits(x), r["ids"], r["w"], ob, tokens=tok)
+    else:
+        rs = np.random.default_rng(6)
+        is13 = (rs.uniform(0.5, 1.5, s.E) * 20.0 / 2688).astype(np.float32)
+        is2 = (rs.uniform(0.5, 1.5, s.E) * 4.0 / 2688).astype(np.float32)
+        out = lib.nvfp4_moe_w4a4(x, logits, s.k, gw, torch.from_numpy(is13).cuda(), torch.from_numpy(is2).cuda())
+        ref = orc.moe_layer("w4a4", synth.bf16_bits(x), r["ids"], r["w"], ob, tokens=tok, is13=is13, is2=is2)
+    assert_layer_close(bf16_to_f32(out)[tok], ref, f"prefill {kind} {mode}")
+
+
+def test_dense_mlp_full_size_sampled(orc):
+    """Dense NVFP4 MLP d=4096, ffn=12288, 8192 tokens; gate and up carry
+    different tensor scales; the oracle checks sampled rows."""
+    M, K, N = 8192, 4096, 12288
+    x = synth.make_x(M, K, seed=4001, device="cuda", outlier_frac=0.05)
+    wg = synth.make_weights(1, N, K, 4002, "cuda")[0]
+    wu = synth.make_weights(1, N, K, 4003, "cuda")[0] * 2
+    wd = synth.make_weights(1, K, N, 4004, "cuda")[0]
+    qg, qu, qd = (lib.nvfp4_quantize_weights(w) for w in (wg, wu, wd))
+    h = lib.nvfp4_linear(x, qg, qu)
+    y = lib.nvfp4_linear(h, qd)
+    rows = np.array([0, 4097, 8191])
+    og, ou, od = (orc.quantize_tensor(synth.bf16_bits(w)) for w in (wg, wu, wd))
+    href = orc.linear(synth.bf16_bits(x)[rows], og[0], og[1], og[2], wup=ou)
+    assert_layer_close(bf16_to_f32(h)[rows], href, "dense gate/up")
+    yref = orc.linear(synth.bf16_bits(torch.from_numpy(href).to(torch.bfloat16)), od[0], od[1], od[2])
+    assert_layer_close(bf16_to_f32(y)[rows], yref, "dense down")
