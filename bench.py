@@ -312,9 +312,9 @@ def time_e2e(layer, steps, flush):
     D2H of the output, all inside the timed events."""
     s = layer.shape
     hx = [b[0].cpu().pin_memory() for b in layer.batches]
-    hl = [b[1].cpu().pin_memory() for b in layer.batches]
+    hl = [b[1].cpu().pin_memory() if b[1] is not None else None for b in layer.batches]
     dx = torch.empty_like(layer.batches[0][0])
-    dl = torch.empty_like(layer.batches[0][1])
+    dl = torch.empty_like(layer.batches[0][1]) if layer.batches[0][1] is not None else None
     hout = torch.empty(s.T, s.d, dtype=torch.bfloat16).pin_memory()
     stream = torch.cuda.current_stream()
     times = []
@@ -324,13 +324,14 @@ def time_e2e(layer, steps, flush):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         dx.copy_(hx[i % len(hx)], non_blocking=True)
-        dl.copy_(hl[i % len(hl)], non_blocking=True)
+        if dl is not None:
+            dl.copy_(hl[i % len(hl)], non_blocking=True)
         out = layer.step(i, dx, dl)
         hout.copy_(out, non_blocking=True)
         b.record(stream)
         b.synchronize()
         times.append(a.elapsed_time(b))
-    h2d = dx.numel() * dx.element_size() + dl.numel() * dl.element_size()
+    h2d = dx.numel() * dx.element_size() + (dl.numel() * dl.element_size() if dl is not None else 0)
     d2h = hout.numel() * hout.element_size()
     return statistics.mean(times), h2d, d2h
 

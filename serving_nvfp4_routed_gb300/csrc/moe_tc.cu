@@ -9,16 +9,19 @@
 //
 // Work unit = (expert e, 128 output features f0.., 128 routed rows row0..):
 //   D[f, j] = sum_k W[e, f, k] * B[row0 + j, k]         (swap-AB: weights are A)
-// A: the NVFP4 weights, dequantised e2m1*e4m3 -> f16 (exact) by four
-//    producer warps straight into the 128-byte-swizzled K-major smem layout
-//    the MMA reads; B: f16 rows (x or h times a per-row power of two, exact
-//    for the inputs here) gathered by cp.async into the same layout; both
-//    through a ring of smem stages guarded by mbarriers.
-// One thread issues tcgen05.mma kind::f16 (M=128, N=128, K=16) into fp32
-// accumulators in TMEM, double-buffered so that the epilogue of one unit
-// overlaps the MMAs of the next; four epilogue warps (one TMEM lane quarter
-// each) read the accumulators with tcgen05.ld and apply SwiGLU, the
-// weighted combine (red.add) or a plain bf16 store.
+// A: the NVFP4 weights.  Each of four producer warps owns 32 tile rows; a
+//    thread streams its row's codes and scales through a private cp.async
+//    ring in shared memory, dequantises e2m1*e4m3 -> f16 (exact) in
+//    registers and writes the f16 row straight into tensor memory with
+//    tcgen05.st -- the A operand never occupies shared memory, which keeps
+//    shared-memory capacity and bandwidth for the B rows.
+// B: f16 rows (x or h times a per-row power of two, exact for the inputs
+//    here) gathered by cp.async into the 128-byte-swizzled K-major smem
+//    layout.  Both operands flow through mbarrier-guarded stage rings.
+// One thread issues tcgen05.mma kind::f16 (M=128, N=128, K=16, A from
+// TMEM) into fp32 accumulators in TMEM; four epilogue warps (one TMEM lane
+// quarter each) read them with tcgen05.ld and apply SwiGLU, the weighted
+// combine (red.add) or a plain bf16 store.
 // Every mbarrier wait is bounded (about 2 s): on expiry the kernel records
 // NVFP4_ERR_TIMEOUT in the status word, every role leaves its loop, and the
 // CTA still frees its tensor memory before it exits.
@@ -36,16 +39,24 @@ constexpr int BM = 128, BN = kTcTokTile, BK = 64;  // features, rows, K per stag
 constexpr int kTileBytes = 128 * 128;                  // 128 rows x 64 f16
 constexpr int kTcWarps = 12;
 constexpr int kTcThreads = kTcWarps * 32;
-// warp roles
-constexpr int kWarpMma = 0, kWarpB = 1, kWarpEpi = 4, kWarpDeq = 8;
-constexpr int kPD = 4;  // k-stages of weights a dequant thread keeps in flight
+// warp roles: 0 MMA issue, 1-2 B gather, 3 idle, 4-7 epilogue, 8-11 A dequant
+constexpr int kWarpMma = 0, kWarpB = 1, kNumBWarps = 2, kWarpEpi = 4, kWarpDeq = 8;
 
+// Tensor memory (512 columns x 128 lanes x 32 bit): the fp32 accumulators
+// (NPROJ x BN columns per buffer) and a ring of f16 weight stages (A operand,
+// NPROJ x 32 columns per stage: 64 K values of each of the 128 rows).
 template <int NPROJ>
 struct Cfg {
-    static constexpr int kStages = NPROJ == 2 ? 4 : 6;
-    static constexpr int kStageBytes = (NPROJ + 1) * kTileBytes;
-    static constexpr int kSmem = kStages * kStageBytes + 1024;
-    static constexpr uint32_t kTmemCols = NPROJ == 2 ? 512 : 256;  // 2 accumulator buffers
+    static constexpr int kNAcc = NPROJ == 2 ? 1 : 2;      // accumulator buffers
+    static constexpr int kSA = NPROJ == 2 ? 4 : 8;        // f16 weight stages in TMEM
+    static constexpr int kAccCols = NPROJ * BN;
+    static constexpr int kACols = NPROJ * (BK / 2);
+    static constexpr uint32_t kTmemCols = 512;
+    static_assert(kNAcc * kAccCols + kSA * kACols <= 512, "TMEM budget");
+    static constexpr int kSB = NPROJ == 2 ? 6 : 8;        // token-row stages in smem (gathered from L2)
+    static constexpr int kRaw = NPROJ == 2 ? 10 : 12;     // weight-code stages in flight per thread
+    static constexpr int kRawSlot = NPROJ * (2 * 128 * 16 + 128 * 4);
+    static constexpr int kSmem = kSB * kTileBytes + kRaw * kRawSlot + 1024;
 };
 
 struct Unit {
@@ -76,25 +87,35 @@ __device__ __forceinline__ int brow_of(const TcArgs& a, int row) {
 template <int OUT, int NPROJ>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const TcArgs a) {
     using CF = Cfg<NPROJ>;
-    constexpr int S = CF::kStages;
+    constexpr int SA = CF::kSA, SB = CF::kSB, NACC = CF::kNAcc;
+    constexpr int RD = CF::kRaw;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ __align__(8) uint64_t bar_full_a[S], bar_full_b[S], bar_empty[S], bar_acc_full[2], bar_acc_empty[2];
+    uint8_t* smem_b = smem;                              // [SB] f16 token-row tiles
+    uint8_t* raw = smem_b + SB * kTileBytes;             // per-thread weight-code ring
+    __shared__ __align__(8) uint64_t bar_full_a[SA], bar_empty_a[SA], bar_full_b[SB], bar_empty_b[SB];
+    __shared__ __align__(8) uint64_t bar_acc_full[2], bar_acc_empty[2];
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
     __shared__ int s_brow[BN];
+    __shared__ float s_rs[2][BN];   // epilogue: 2^exp of the column's B row (0 if the column is empty)
+    __shared__ int s_tok[2][BN];    // epilogue: token of the column (combine)
+    __shared__ float s_wt[2][BN];   // epilogue: routing weight of the column (combine)
 
     grid_dep_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(smem_u32(&bar_full_a[s]), 128);
-            mbar_init(smem_u32(&bar_full_b[s]), 32);
-            mbar_init(smem_u32(&bar_empty[s]), 1);
+        for (int s = 0; s < SA; ++s) {
+            mbar_init(smem_u32(&bar_full_a[s]), 4);  // one arrive per dequant warp (its 32 rows)
+            mbar_init(smem_u32(&bar_empty_a[s]), 1);
+        }
+        for (int s = 0; s < SB; ++s) {
+            mbar_init(smem_u32(&bar_full_b[s]), 32 * kNumBWarps);
+            mbar_init(smem_u32(&bar_empty_b[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&bar_acc_full[b]), 1);
-            mbar_init(smem_u32(&bar_acc_empty[b]), 128);
+            mbar_init(smem_u32(&bar_acc_empty[b]), 4);  // one arrive per epilogue warp
         }
         s_abort = 0;
         mbar_fence_init();
@@ -104,6 +125,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const TcArgs a) 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
+    const uint32_t tmem_a = tmem + NACC * CF::kAccCols;  // first column of the weight stages
     volatile int* abort_flag = &s_abort;
 
     const int n_active = *a.n_active;
@@ -116,29 +138,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const TcArgs a) 
         const uint32_t idesc = idesc_f16_f32(BM, BN);
         int kcg = 0, it = 0;
         for (int u = blockIdx.x; u < total; u += gridDim.x, ++it) {
-            const int as = it & 1;
-            bool ok = mbar_wait(smem_u32(&bar_acc_empty[as]), ((it >> 1) & 1) ^ 1, abort_flag, a.status);
-            if (!__all_sync(0xffffffffu, ok)) break;
+            const int as = it % NACC;
+            if (!warp_wait(smem_u32(&bar_acc_empty[as]), ((it / NACC) & 1) ^ 1, abort_flag, a.status)) break;
             tc_fence_after();
-            const uint32_t d_base = tmem + as * (NPROJ * BN);
+            const uint32_t d_base = tmem + as * CF::kAccCols;
             for (int kc = 0; kc < nk; ++kc, ++kcg) {
-                const int s = kcg % S;
-                const uint32_t ph = (kcg / S) & 1;
-                ok = mbar_wait(smem_u32(&bar_full_a[s]), ph, abort_flag, a.status) &&
-                     mbar_wait(smem_u32(&bar_full_b[s]), ph, abort_flag, a.status);
-                if (!__all_sync(0xffffffffu, ok)) goto mma_done;
+                const int sa = kcg % SA, sb = kcg % SB;
+                if (!warp_wait(smem_u32(&bar_full_a[sa]), (kcg / SA) & 1, abort_flag, a.status) ||
+                    !warp_wait(smem_u32(&bar_full_b[sb]), (kcg / SB) & 1, abort_flag, a.status))
+                    goto mma_done;
                 tc_fence_after();
                 fence_proxy_async();
                 if (lane == 0) {
-                    const uint32_t sb = smem_u32(smem + s * CF::kStageBytes);
-                    const uint64_t bdesc = sdesc_sw128(sb + NPROJ * kTileBytes);
+                    const uint32_t a_stage = tmem_a + sa * CF::kACols;
+                    const uint64_t bdesc = sdesc_sw128(smem_u32(smem_b + sb * kTileBytes));
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
 #pragma unroll
                         for (int p = 0; p < NPROJ; ++p)
-                            mma_f16(d_base + p * BN, sdesc_sw128(sb + p * kTileBytes) + 2 * kk, bdesc + 2 * kk,
-                                    idesc, (kc | kk) != 0);
-                    mma_commit(smem_u32(&bar_empty[s]));
+                            mma_f16_ta(d_base + p * BN, a_stage + p * (BK / 2) + kk * 8, bdesc + 2 * kk, idesc,
+                                       (kc | kk) != 0);
+                    mma_commit(smem_u32(&bar_empty_a[sa]));
+                    mma_commit(smem_u32(&bar_empty_b[sb]));
                 }
                 __syncwarp();
             }
@@ -146,27 +167,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const TcArgs a) 
             __syncwarp();
         }
     mma_done:;
-    } else if (warp == kWarpB) {
-        // ---------------- B producer: gathered f16 rows via cp.async ----------------
+    } else if (warp >= kWarpB && warp < kWarpB + kNumBWarps) {
+        // ---------------- B producers: gathered f16 rows via cp.async ----------------
+        const int wb = warp - kWarpB;  // rows wb*64 .. wb*64+63
         int kcg = 0;
         for (int u = blockIdx.x; u < total; u += gridDim.x) {
             const Unit un = decode_unit(a, u, n_active, n_ft);
             __syncwarp();
-            for (int i = lane; i < BN; i += 32) {
-                const int row = un.row0 + i;
-                s_brow[i] = row < un.row_end ? brow_of(a, row) : -1;
+            for (int i = lane; i < BN / kNumBWarps; i += 32) {
+                const int rr = wb * (BN / kNumBWarps) + i;
+                const int row = un.row0 + rr;
+                s_brow[rr] = row < un.row_end ? brow_of(a, row) : -1;
             }
             __syncwarp();
             for (int kc = 0; kc < nk; ++kc, ++kcg) {
-                const int s = kcg % S;
-                const uint32_t ph = (kcg / S) & 1;
-                const bool ok = mbar_wait(smem_u32(&bar_empty[s]), ph ^ 1, abort_flag, a.status);
-                if (!__all_sync(0xffffffffu, ok)) goto b_done;
-                const uint32_t bt = smem_u32(smem + s * CF::kStageBytes + NPROJ * kTileBytes);
+                const int s = kcg % SB;
+                if (!warp_wait(smem_u32(&bar_empty_b[s]), ((kcg / SB) & 1) ^ 1, abort_flag, a.status)) goto b_done;
+                const uint32_t bt = smem_u32(smem_b + s * kTileBytes);
                 const int c = lane & 7;
-#pragma unroll 8
-                for (int i = 0; i < BN / 4; ++i) {
-                    const int rr = (lane >> 3) + 4 * i;
+#pragma unroll
+                for (int i = 0; i < BN / kNumBWarps / 4; ++i) {
+                    const int rr = wb * (BN / kNumBWarps) + (lane >> 3) + 4 * i;
                     const int br = s_brow[rr];
                     const uint16_t* src = a.b_f16 + (size_t)(br < 0 ? 0 : br) * a.K + (size_t)kc * BK + c * 8;
                     cp_async16(bt + rr * 128 + ((c ^ (rr & 7)) << 4), src, br < 0 ? 0u : 16u);
@@ -178,38 +199,56 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const TcArgs a) 
     } else if (warp >= kWarpEpi && warp < kWarpEpi + 4) {
         // ---------------- epilogue: TMEM -> registers -> global ----------------
         const int q = warp - kWarpEpi;  // TMEM lane quarter
-        const int et = q * 32 + lane;   // feature within the unit
+        const int et = q * 32 + lane;   // feature within the unit, and the column this thread describes
         int it = 0;
         for (int u = blockIdx.x; u < total; u += gridDim.x, ++it) {
             const Unit un = decode_unit(a, u, n_active, n_ft);
-            const int as = it & 1;
-            const bool ok = mbar_wait(smem_u32(&bar_acc_full[as]), (it >> 1) & 1, abort_flag, a.status);
-            if (!__all_sync(0xffffffffu, ok)) break;
+            const int as = it & 1;           // column-table buffer
+            const int acc = it % NACC;       // accumulator buffer
+            {   // per-column row data of this unit, one column per thread
+                const int row = un.row0 + et;
+                float rs = 0.0f, wt = 0.0f;
+                int tok = 0;
+                if (row < un.row_end) {
+                    rs = exp2i(a.b_exp[brow_of(a, row)]);
+                    if constexpr (OUT == TC_OUT_COMBINE) {
+                        const int slot = a.row_to_slot[row];
+                        tok = slot / a.top_k;
+                        wt = a.topk_w[slot];
+                    }
+                }
+                s_rs[as][et] = rs;
+                s_tok[as][et] = tok;
+                s_wt[as][et] = wt;
+            }
+            named_bar(1, 128);
+            if (!warp_wait(smem_u32(&bar_acc_full[acc]), (it / NACC) & 1, abort_flag, a.status, 128)) break;
             tc_fence_after();
             const int f = un.f0 + et;
             const float w0 = a.a_ws2[0][un.e];
             const float w1 = a.a_ws2[NPROJ - 1][un.e];
-            const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + as * (NPROJ * BN);
+            const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + acc * CF::kAccCols;
+            const int ncol = min(BN, un.row_end - un.row0);
             for (int cb = 0; cb < BN / 32; ++cb) {
+                if (cb * 32 >= ncol) break;  // warp-uniform
                 uint32_t r0[32], r1[32];
                 tmem_ld32(tb + cb * 32, r0);
                 if constexpr (NPROJ == 2) tmem_ld32(tb + BN + cb * 32, r1);
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                    const int row = un.row0 + cb * 32 + j;
-                    if (row >= un.row_end) continue;
-                    const int br = brow_of(a, row);
-                    const float rs = exp2i(a.b_exp[br]);
+                    const int col = cb * 32 + j;
+                    if (col >= ncol) continue;
+                    const int row = un.row0 + col;
+                    const float rs = s_rs[as][col];
                     if constexpr (OUT == TC_OUT_H) {
                         const float G = round_bf16(__fmul_rn(__fmul_rn(__uint_as_float(r0[j]), rs), w0));
                         const float U = round_bf16(__fmul_rn(__fmul_rn(__uint_as_float(r1[j]), rs), w1));
                         const float h = round_bf16(G / (1.0f + expf(-G)) * U);
                         a.h_out[(size_t)row * a.N + f] = f32_to_bf16_bits(h);
                     } else if constexpr (OUT == TC_OUT_COMBINE) {
-                        const int slot = a.row_to_slot[row];
                         const float y = __fmul_rn(__fmul_rn(__uint_as_float(r0[j]), rs), w0);
-                        atomicAdd(a.acc_out + (size_t)(slot / a.top_k) * a.N + f, a.topk_w[slot] * y);
+                        atomicAdd(a.acc_out + (size_t)s_tok[as][col] * a.N + f, s_wt[as][col] * y);
                     } else {
                         a.y_out[(size_t)row * a.N + f] =
                             f32_to_bf16_bits(__fmul_rn(__fmul_rn(__uint_as_float(r0[j]), rs), w0));
@@ -217,70 +256,96 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const TcArgs a) 
                 }
             }
             tc_fence_before();
-            mbar_arrive(smem_u32(&bar_acc_empty[as]));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bar_acc_empty[acc]));
         }
     } else if (warp >= kWarpDeq) {
         // ---------------- A producer: NVFP4 weights -> f16 smem tiles ----------------
+        // Each thread owns one tile row.  Its codes and scales stream through
+        // a private ring of RD smem slots by cp.async (RD - 1 k-stages ahead),
+        // then are dequantised into the shared f16 stage.
         const int dt = threadIdx.x - kWarpDeq * 32;  // tile row
+        const int dwarp = warp - kWarpDeq;            // TMEM lane quarter of this warp
         const size_t K2 = (size_t)a.K / 2, K16 = (size_t)a.K / 16;
-        uint32_t ring[kPD][NPROJ][9];
-        int kcg = 0;
-        for (int u = blockIdx.x; u < total; u += gridDim.x) {
-            const Unit un = decode_unit(a, u, n_active, n_ft);
-            const uint8_t* cp[NPROJ];
-            const uint8_t* sp[NPROJ];
-#pragma unroll
-            for (int p = 0; p < NPROJ; ++p) {
+        auto raw_codes = [&](int slot, int p, int part) -> uint8_t* {
+            return raw + slot * CF::kRawSlot + ((p * 2 + part) * 128 + dt) * 16;
+        };
+        auto raw_scale = [&](int slot, int p) -> uint8_t* {
+            return raw + slot * CF::kRawSlot + NPROJ * 2 * 128 * 16 + (p * 128 + dt) * 4;
+        };
+        // issue side of the ring: walks this CTA's units and k-stages ahead of the consumer
+        int iu = blockIdx.x, ikc = 0;
+        const uint8_t* icp[NPROJ];
+        const uint8_t* isp[NPROJ];
+        auto set_issue_unit = [&]() {
+            if (iu < total) {
+                const Unit un = decode_unit(a, iu, n_active, n_ft);
                 const size_t rowg = (size_t)un.e * a.N + un.f0 + dt;
-                cp[p] = a.a_codes[p] + rowg * K2;
-                sp[p] = a.a_scales[p] + rowg * K16;
-            }
-            auto load = [&](int slot, int kc) {
 #pragma unroll
                 for (int p = 0; p < NPROJ; ++p) {
-                    const uint4 c0 = __ldg(reinterpret_cast<const uint4*>(cp[p] + (size_t)kc * 32));
-                    const uint4 c1 = __ldg(reinterpret_cast<const uint4*>(cp[p] + (size_t)kc * 32) + 1);
-                    ring[slot][p][0] = c0.x; ring[slot][p][1] = c0.y; ring[slot][p][2] = c0.z; ring[slot][p][3] = c0.w;
-                    ring[slot][p][4] = c1.x; ring[slot][p][5] = c1.y; ring[slot][p][6] = c1.z; ring[slot][p][7] = c1.w;
-                    ring[slot][p][8] = __ldg(reinterpret_cast<const uint32_t*>(sp[p] + (size_t)kc * 4));
-                }
-            };
-#pragma unroll
-            for (int i = 0; i < kPD; ++i)
-                if (i < nk) load(i, i);
-            for (int kc0 = 0; kc0 < nk; kc0 += kPD) {
-#pragma unroll
-                for (int uu = 0; uu < kPD; ++uu) {
-                    const int kc = kc0 + uu;
-                    if (kc >= nk) break;
-                    const int s = kcg % S;
-                    const uint32_t ph = (kcg / S) & 1;
-                    const bool ok = mbar_wait(smem_u32(&bar_empty[s]), ph ^ 1, abort_flag, a.status);
-                    if (!__all_sync(0xffffffffu, ok)) goto deq_done;
-                    uint8_t* st = smem + s * CF::kStageBytes;
-#pragma unroll
-                    for (int p = 0; p < NPROJ; ++p) {
-                        uint8_t* rowp = st + p * kTileBytes + dt * 128;
-                        const uint32_t sw = ring[uu][p][8];
-#pragma unroll
-                        for (int w = 0; w < 8; ++w) {
-                            const int blk = w >> 1;
-                            const uint32_t S2 = f16x2_bcast(e4m3x2_to_f16x2((sw >> (16 * (blk >> 1))) & 0xFFFFu), blk & 1);
-                            uint32_t f[4];
-                            e2m1x8_to_f16x8(ring[uu][p][w], f);
-                            *reinterpret_cast<uint4*>(rowp + ((w ^ (dt & 7)) << 4)) =
-                                make_uint4(hmul2_u32(f[0], S2), hmul2_u32(f[1], S2), hmul2_u32(f[2], S2),
-                                           hmul2_u32(f[3], S2));
-                        }
-                    }
-                    fence_proxy_async();
-                    mbar_arrive(smem_u32(&bar_full_a[s]));
-                    if (kc + kPD < nk) load(uu, kc + kPD);
-                    ++kcg;
+                    icp[p] = a.a_codes[p] + rowg * K2;
+                    isp[p] = a.a_scales[p] + rowg * K16;
                 }
             }
+        };
+        auto issue = [&](int slot) {
+            if (iu < total) {
+#pragma unroll
+                for (int p = 0; p < NPROJ; ++p) {
+                    const uint8_t* c = icp[p] + (size_t)ikc * 32;
+                    cp_async16(smem_u32(raw_codes(slot, p, 0)), c, 16u);
+                    cp_async16(smem_u32(raw_codes(slot, p, 1)), c + 16, 16u);
+                    cp_async4(smem_u32(raw_scale(slot, p)), isp[p] + (size_t)ikc * 4);
+                }
+                if (++ikc == nk) {
+                    ikc = 0;
+                    iu += gridDim.x;
+                    set_issue_unit();
+                }
+            }
+            cp_async_commit();
+        };
+        set_issue_unit();
+        for (int i = 0; i < RD - 1; ++i) issue(i);
+        int kcg = 0;
+        for (int u = blockIdx.x; u < total; u += gridDim.x) {
+            for (int kc = 0; kc < nk; ++kc, ++kcg) {
+                issue((kcg + RD - 1) % RD);
+                cp_async_wait<RD - 1>();
+                const int s = kcg % SA;
+                if (!warp_wait(smem_u32(&bar_empty_a[s]), ((kcg / SA) & 1) ^ 1, abort_flag, a.status)) goto deq_done;
+                tc_fence_after();
+                const int slot = kcg % RD;
+                // TMEM lane = this thread's tile row; 32 columns per projection
+                const uint32_t ta = tmem_a + ((uint32_t)(dwarp * 32) << 16) + s * CF::kACols;
+#pragma unroll
+                for (int p = 0; p < NPROJ; ++p) {
+                    const uint4 c0 = *reinterpret_cast<const uint4*>(raw_codes(slot, p, 0));
+                    const uint4 c1 = *reinterpret_cast<const uint4*>(raw_codes(slot, p, 1));
+                    const uint32_t sw = *reinterpret_cast<const uint32_t*>(raw_scale(slot, p));
+                    const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                    const uint32_t S01 = e4m3x2_to_f16x2(sw & 0xFFFFu), S23 = e4m3x2_to_f16x2(sw >> 16);
+                    const uint32_t Sb[4] = {f16x2_bcast(S01, 0), f16x2_bcast(S01, 1), f16x2_bcast(S23, 0),
+                                            f16x2_bcast(S23, 1)};
+                    uint32_t v[32];
+#pragma unroll
+                    for (int w = 0; w < 8; ++w) {
+                        uint32_t f[4];
+                        e2m1x8_to_f16x8(cw[w], f);
+                        const uint32_t S2 = Sb[w >> 1];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) v[4 * w + i] = hmul2_u32(f[i], S2);
+                    }
+                    tmem_st32(ta + p * (BK / 2), v);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bar_full_a[s]));
+            }
         }
-    deq_done:;
+    deq_done:
+        cp_async_wait<0>();
     }
 
     tc_fence_before();
