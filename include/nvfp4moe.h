@@ -94,6 +94,32 @@ nvfp4_status nvfp4_quantize_weights(const uint16_t* w_bf16, int batch, int N, in
 size_t nvfp4_quantize_weights_workspace_size(int batch, int N, int K);
 
 /* ------------------------------------------------------------------------
+ * nvfp4_quantize_weights_noalloc -- the same recipe and outputs as
+ * nvfp4_quantize_weights, for callers that cannot allocate device memory
+ * (the pages have no counterpart: a convenience of this library).
+ * Such callers include code that may not call cudaMalloc because another
+ * component owns the device's memory (a pool planned ahead), plain C
+ * loaders with no allocator of their own, and loops that must not call
+ * cudaMalloc because it can implicitly synchronise the device.  Instead of
+ * a caller workspace it uses a fixed scratch array (one float per tensor,
+ * at most nvfp4_quantize_weights_noalloc_max_batch() = 4096 tensors per
+ * call, 16 KB of device memory on every GPU that loads the library, held
+ * until the process exits) and allocates nothing.
+ *   - batch above the maximum: NVFP4_ERR_SHAPE, nothing enqueued.
+ *   - The first call on a device (with that device current) looks up the
+ *     array's device address (cudaGetSymbolAddress) and caches it; make
+ *     that first call before any stream capture.
+ *   - All calls on a device share the one array: calls that can overlap on
+ *     the GPU (other streams, other host threads) race; order them.
+ *   - The scratch is cleared on each call; outputs as for
+ *     nvfp4_quantize_weights.
+ * --------------------------------------------------------------------- */
+nvfp4_status nvfp4_quantize_weights_noalloc(const uint16_t* w_bf16, int batch, int N, int K,
+                                            uint8_t* codes, uint8_t* scales, float* weight_scale_2,
+                                            cudaStream_t stream);
+int nvfp4_quantize_weights_noalloc_max_batch(void);
+
+/* ------------------------------------------------------------------------
  * nvfp4_quantize_act -- static-scale NVFP4 quantisation of activation rows
  * (TensorFold #308 "The checkpoint": input_scale stored for static
  * activations; W4A4 model card: calibrated static activation scales).

@@ -26,7 +26,8 @@ EXPORTS = ("nvfp4_quantize_weights", "nvfp4_quantize_weights_workspace_size", "n
            "moe_route_permute", "moe_route_permute_workspace_size", "nvfp4_moe_w4a16", "nvfp4_moe_w4a4",
            "nvfp4_moe_workspace_size", "nvfp4_moe_workspace_views", "nvfp4_linear",
            "nvfp4_linear_workspace_size", "nvfp4_status_string", "nvfp4_launch_count",
-           "nvfp4_profile_enable", "nvfp4_profile_collect")
+           "nvfp4_profile_enable", "nvfp4_profile_collect", "nvfp4_quantize_weights_noalloc",
+           "nvfp4_quantize_weights_noalloc_max_batch")
 
 
 class Nvfp4Error(RuntimeError):
@@ -61,6 +62,8 @@ def load(path: str = LIB_PATH):
         L.nvfp4_quantize_weights.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, sz, vp]
         L.nvfp4_quantize_weights_workspace_size.argtypes = [i32, i32, i32]
         L.nvfp4_quantize_weights_workspace_size.restype = sz
+        L.nvfp4_quantize_weights_noalloc.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp]
+        L.nvfp4_quantize_weights_noalloc_max_batch.restype = i32
         L.nvfp4_quantize_act.argtypes = [vp, i32, i32, vp, i32, vp, vp, i32, vp, vp, vp]
         L.moe_route_permute.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]
         L.moe_route_permute_workspace_size.argtypes = [i32, i32, i32]
