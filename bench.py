@@ -157,10 +157,18 @@ def peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def kernel_source_hash():
+KERNEL_SOURCES = {
+    "gemv": ("moe_gemv.cu", "common.cuh", "internal.cuh"),
+    "tc": ("moe_tc.cu", "tc_ptx.cuh", "common.cuh", "internal.cuh"),
+}
+
+
+def kernel_source_hash(kernel: str):
+    """Hash of the source files a kernel is built from (its recorded DRAM
+    traffic is only reported while they are unchanged)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "serving_nvfp4_routed_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
+    for fn in KERNEL_SOURCES["tc" if kernel.startswith("tc_") else "gemv"]:
         h.update(open(os.path.join(csrc, fn), "rb").read())
     return h.hexdigest()[:16]
 
@@ -169,7 +177,7 @@ def recorded_traffic(kernel: str, workload: str):
     try:
         t = json.load(open(TRAFFIC_FILE))
         ent = t[kernel][workload]
-        if ent.get("source_hash") == kernel_source_hash():
+        if ent.get("source_hash") == kernel_source_hash(kernel):
             return float(ent["bytes_per_launch"])
     except Exception:
         pass

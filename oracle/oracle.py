@@ -43,33 +43,37 @@ def _P(t):
     return ctypes.POINTER(t)
 
 
+def bind(L):
+    """Declare the C signatures on a loaded oracle library."""
+    i64, i32, f32 = ctypes.c_int64, ctypes.c_int, ctypes.c_float
+    vp = ctypes.c_void_p
+    L.orc_round_bf16.argtypes = [ctypes.c_double]
+    L.orc_round_bf16.restype = ctypes.c_double
+    L.orc_e2m1_decode.argtypes = [i32]
+    L.orc_e2m1_decode.restype = ctypes.c_double
+    L.orc_e2m1_encode.argtypes = [f32]
+    L.orc_e2m1_encode.restype = i32
+    L.orc_e4m3_decode.argtypes = [i32]
+    L.orc_e4m3_decode.restype = ctypes.c_double
+    L.orc_e4m3_encode_nonneg.argtypes = [f32]
+    L.orc_e4m3_encode_nonneg.restype = i32
+    L.orc_quantize_tensor.argtypes = [vp, i64, i64, vp, vp, vp]
+    L.orc_quantize_rows.argtypes = [vp, i64, i64, vp, vp, vp]
+    L.orc_dequantize.argtypes = [vp, vp, i64, i64, vp]
+    L.orc_route.argtypes = [vp, i64, i32, i32, vp, vp, vp, vp, vp]
+    L.orc_moe_layer.argtypes = [i32, vp, i64, i64, i64, i32, i32, vp, vp,
+                                vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                vp, vp, vp, i64, vp, vp]
+    L.orc_linear.argtypes = [vp, i64, i64, vp, vp, f32, i64, vp, vp, f32, vp]
+    L.orc_num_threads.restype = i32
+    return L
+
+
 def lib():
     global _lib
     with _lock:
         if _lib is None:
-            L = ctypes.CDLL(build())
-            i64, i32, f32 = ctypes.c_int64, ctypes.c_int, ctypes.c_float
-            vp = ctypes.c_void_p
-            L.orc_round_bf16.argtypes = [ctypes.c_double]
-            L.orc_round_bf16.restype = ctypes.c_double
-            L.orc_e2m1_decode.argtypes = [i32]
-            L.orc_e2m1_decode.restype = ctypes.c_double
-            L.orc_e2m1_encode.argtypes = [f32]
-            L.orc_e2m1_encode.restype = i32
-            L.orc_e4m3_decode.argtypes = [i32]
-            L.orc_e4m3_decode.restype = ctypes.c_double
-            L.orc_e4m3_encode_nonneg.argtypes = [f32]
-            L.orc_e4m3_encode_nonneg.restype = i32
-            L.orc_quantize_tensor.argtypes = [vp, i64, i64, vp, vp, vp]
-            L.orc_quantize_rows.argtypes = [vp, i64, i64, vp, vp, vp]
-            L.orc_dequantize.argtypes = [vp, vp, i64, i64, vp]
-            L.orc_route.argtypes = [vp, i64, i32, i32, vp, vp, vp, vp, vp]
-            L.orc_moe_layer.argtypes = [i32, vp, i64, i64, i64, i32, i32, vp, vp,
-                                        vp, vp, vp, vp, vp, vp, vp, vp, vp,
-                                        vp, vp, vp, i64, vp, vp]
-            L.orc_linear.argtypes = [vp, i64, i64, vp, vp, f32, i64, vp, vp, f32, vp]
-            L.orc_num_threads.restype = i32
-            _lib = L
+            _lib = bind(ctypes.CDLL(build()))
     return _lib
 
 
