@@ -160,6 +160,7 @@ def peaks():
 KERNEL_SOURCES = {
     "gemv": ("moe_gemv.cu", "common.cuh", "internal.cuh"),
     "tc": ("moe_tc.cu", "tc_ptx.cuh", "common.cuh", "internal.cuh"),
+    "tcm": ("moe_tcm.cu", "tc_ptx.cuh", "common.cuh", "internal.cuh"),
 }
 
 
@@ -168,7 +169,8 @@ def kernel_source_hash(kernel: str):
     traffic is only reported while they are unchanged)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "serving_nvfp4_routed_gb300", "csrc")
-    for fn in KERNEL_SOURCES["tc" if kernel.startswith("tc_") else "gemv"]:
+    family = kernel.split("_")[0]
+    for fn in KERNEL_SOURCES[family if family in KERNEL_SOURCES else "gemv"]:
         h.update(open(os.path.join(csrc, fn), "rb").read())
     return h.hexdigest()[:16]
 
@@ -440,7 +442,7 @@ def run_ours(args):
     dom = max(kernels, key=lambda k: kernels[k]["ms_per_launch"] * kernels[k]["launches"]) if kernels else "?"
     s_ = layer.shape
     dom_ms = kernels.get(dom, {"ms_per_launch": float("nan")})["ms_per_launch"]
-    if dom.startswith("tc_"):
+    if dom.startswith(("tc_", "tcm_")):
         # tensor-bound: f16 MMA (the bf16/f16 dense rate), flops of one launch
         nproj = 2 if "gateup" in dom else 1
         rows = R if layer.kind != "dense" else s_.T

@@ -1,6 +1,8 @@
 // internal.cuh -- host-side launchers shared between the library's .cu files.
 #pragma once
 
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace nvfp4 {
@@ -111,9 +113,30 @@ struct TcArgs {
     int32_t* status;             // optional: NVFP4_ERR_TIMEOUT if a bounded wait expired
 };
 
+// ---- prompt-shaped gate/up with the routed rows as M (tcgen05, N = 256) ----
+struct TcmArgs {
+    CUtensorMap tmap_x;          // f16 rows in expert order [R, K], box 64 x 128, 128-byte swizzle
+    int K, F;
+    const int32_t* offsets;      // [E+1]
+    const int32_t* active;       // [E]
+    const int32_t* n_active;     // [1]
+    const int32_t* tile_start;   // [E+1] prefix of ceil(rows / 128) over active experts
+    const uint8_t* a_codes[2];   // gate, up [E, F, K/2]
+    const uint8_t* a_scales[2];  // [E, F, K/16]
+    const float* a_ws2[2];       // [E]
+    const int32_t* x_exp;        // [R] value of an f16 row = f16 * 2^x_exp[row]
+    uint16_t* h_out;             // [R, F] bf16 SwiGLU
+    int32_t* status;
+};
+bool make_tmap_rows_f16(CUtensorMap* map, const void* base, int rows, int K);
+void launch_tcm_gateup(const TcmArgs& a, int max_units, cudaStream_t s);
+
 size_t tc_smem_bytes(int nproj);
 void launch_tc_gemm(int outmode, int nproj, const TcArgs& a, int max_units, cudaStream_t s);
+// dst row r = f16(src row (map ? map[r] / map_div : r) * 2^-s), exps[r] = s;
+// optionally zeroes row r of zero_rows (length zero_len) for r < zero_count.
 void launch_rows_to_f16(const uint16_t* src, int rows, int K, uint16_t* dst, int32_t* exps, float* zero_rows,
-                        int zero_len, cudaStream_t s);
+                        int zero_len, cudaStream_t s, const int32_t* map = nullptr, int map_div = 1,
+                        int zero_count = -1);
 void launch_acc_to_bf16(const float* acc, size_t n, uint16_t* out, cudaStream_t s);
 }  // namespace nvfp4

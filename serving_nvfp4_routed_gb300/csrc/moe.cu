@@ -34,8 +34,8 @@ struct MoeWs {
     float* acc;       // [T, d]
     int* clear;       // [kCounters + T]: work counters, then per-token completion counts
     // prompt-shaped (tensor-core) path, W4A16
-    uint16_t* xh;     // [T, d]  f16 x * 2^-s
-    int32_t* x_exp;   // [T]
+    uint16_t* xp;     // [R, d]  f16 x * 2^-s, rows in expert order
+    int32_t* xp_exp;  // [R]
     uint16_t* hh;     // [R, F]  f16 h * 2^-s
     int32_t* h_exp;   // [R]
 };
@@ -81,8 +81,8 @@ MoeWs carve_moe(void* base, int T, int E, int k, int d, int F, int mode, size_t*
     if (mode == 0) {
         w.h = c.take<uint16_t>(R * F);
         if (tc_possible(mode, d, F)) {
-            w.xh = c.take<uint16_t>((size_t)T * d);
-            w.x_exp = c.take<int32_t>(T + 1);
+            w.xp = c.take<uint16_t>(R * d);
+            w.xp_exp = c.take<int32_t>(R + 1);
             w.hh = c.take<uint16_t>(R * F);
             w.h_exp = c.take<int32_t>(R + 1);
         }
@@ -156,32 +156,36 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
         launch_quantize_act(x, R, d, ws.ra.row_to_slot, top_k, is13, ws.ra.offsets, E, ws.xq, ws.xs, s);
 
     if (use_tc(mode, T, E, top_k, d, F)) {
-        // x -> f16 rows (and zero the combine accumulator)
-        launch_rows_to_f16(x, T, d, ws.xh, ws.x_exp, ws.acc, d, s);
-        TcArgs t{};
-        t.top_k = top_k;
-        t.offsets = ws.ra.offsets;
-        t.active = ws.ra.active;
-        t.n_active = ws.ra.n_active;
-        t.tile_start = ws.ra.tile_start_tc;
-        t.row_to_slot = ws.ra.row_to_slot;
-        t.topk_w = ws.ra.w;
-        t.status = d_status;
+        // x -> f16 rows in expert order (and zero the combine accumulator)
+        launch_rows_to_f16(x, R, d, ws.xp, ws.xp_exp, ws.acc, d, s, ws.ra.row_to_slot, top_k, T);
         const int max_units = (R / kTcTokTile + std::min(E, R) + 1) * (std::max(d, F) / 128);
         // gate/up + SwiGLU -> h (bf16)
-        t.K = d;
-        t.N = F;
-        t.a_codes[0] = w->gate.codes;  t.a_scales[0] = w->gate.scales;  t.a_ws2[0] = w->gate.weight_scale_2;
-        t.a_codes[1] = w->up.codes;    t.a_scales[1] = w->up.scales;    t.a_ws2[1] = w->up.weight_scale_2;
-        t.b_f16 = ws.xh;
-        t.b_exp = ws.x_exp;
-        t.b_by_token = 1;
-        t.h_out = ws.h;
-        launch_tc_gemm(TC_OUT_H, 2, t, max_units, s);
+        TcmArgs g{};
+        if (!make_tmap_rows_f16(&g.tmap_x, ws.xp, R, d)) return NVFP4_ERR_CUDA;
+        g.K = d;
+        g.F = F;
+        g.offsets = ws.ra.offsets;
+        g.active = ws.ra.active;
+        g.n_active = ws.ra.n_active;
+        g.tile_start = ws.ra.tile_start_tc;
+        g.a_codes[0] = w->gate.codes;  g.a_scales[0] = w->gate.scales;  g.a_ws2[0] = w->gate.weight_scale_2;
+        g.a_codes[1] = w->up.codes;    g.a_scales[1] = w->up.scales;    g.a_ws2[1] = w->up.weight_scale_2;
+        g.x_exp = ws.xp_exp;
+        g.h_out = ws.h;
+        g.status = d_status;
+        launch_tcm_gateup(g, max_units, s);
         // h -> f16 rows
         launch_rows_to_f16(ws.h, R, F, ws.hh, ws.h_exp, nullptr, 0, s);
         // down + weighted combine
-        TcArgs u = t;
+        TcArgs u{};
+        u.top_k = top_k;
+        u.offsets = ws.ra.offsets;
+        u.active = ws.ra.active;
+        u.n_active = ws.ra.n_active;
+        u.tile_start = ws.ra.tile_start_tc;
+        u.row_to_slot = ws.ra.row_to_slot;
+        u.topk_w = ws.ra.w;
+        u.status = d_status;
         u.K = F;
         u.N = d;
         u.a_codes[0] = w->down.codes;  u.a_scales[0] = w->down.scales;  u.a_ws2[0] = w->down.weight_scale_2;
@@ -371,9 +375,19 @@ extern "C" nvfp4_status nvfp4_linear(const uint16_t* x, int M, int K, const nvfp
         t.b_by_token = 1;
         const int max_units = ((M + kTcTokTile - 1) / kTcTokTile) * (N / 128);
         if (w_up) {
-            t.a_codes[1] = w_up->codes;  t.a_scales[1] = w_up->scales;  t.a_ws2[1] = w_up->weight_scale_2;
-            t.h_out = out;
-            launch_tc_gemm(TC_OUT_H, 2, t, max_units, stream);
+            TcmArgs g{};
+            if (!make_tmap_rows_f16(&g.tmap_x, l.xh, M, K)) return NVFP4_ERR_CUDA;
+            g.K = K;
+            g.F = N;
+            g.offsets = t.offsets;
+            g.active = t.active;
+            g.n_active = t.n_active;
+            g.tile_start = t.tile_start;
+            g.a_codes[0] = w->codes;     g.a_scales[0] = w->scales;     g.a_ws2[0] = w->weight_scale_2;
+            g.a_codes[1] = w_up->codes;  g.a_scales[1] = w_up->scales;  g.a_ws2[1] = w_up->weight_scale_2;
+            g.x_exp = l.x_exp;
+            g.h_out = out;
+            launch_tcm_gateup(g, max_units, stream);
         } else {
             t.y_out = out;
             launch_tc_gemm(TC_OUT_BF16, 1, t, max_units, stream);

@@ -375,11 +375,13 @@ void launch_tc_t(const TcArgs& a, int max_units, cudaStream_t s, const char* nam
 // row of the same index (the combine accumulator).
 // ---------------------------------------------------------------------------
 __global__ void rows_to_f16_kernel(const uint16_t* __restrict__ src, int rows, int K, uint16_t* __restrict__ dst,
-                                   int32_t* __restrict__ exps, float* __restrict__ zero_rows, int zero_len) {
+                                   int32_t* __restrict__ exps, float* __restrict__ zero_rows, int zero_len,
+                                   const int32_t* __restrict__ map, int map_div, int zero_count) {
     grid_dep_wait();
     __shared__ float red[32];
     for (int r = blockIdx.x; r < rows; r += gridDim.x) {
-        const uint4* s4 = reinterpret_cast<const uint4*>(src + (size_t)r * K);
+        const int sr = map ? map[r] / map_div : r;
+        const uint4* s4 = reinterpret_cast<const uint4*>(src + (size_t)sr * K);
         float m = 0.0f;
         for (int i = threadIdx.x; i < K / 8; i += blockDim.x) {
             const uint4 u = __ldg(s4 + i);
@@ -406,7 +408,7 @@ __global__ void rows_to_f16_kernel(const uint16_t* __restrict__ src, int rows, i
             o.w = f32x2_to_f16x2(bf16_bits_to_f32(u.w & 0xFFFFu) * down, bf16_bits_to_f32(u.w >> 16) * down);
             d4[i] = o;
         }
-        if (zero_rows) {
+        if (zero_rows && r < zero_count) {
             float4* z = reinterpret_cast<float4*>(zero_rows + (size_t)r * zero_len);
             for (int i = threadIdx.x; i < zero_len / 4; i += blockDim.x) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
@@ -438,12 +440,13 @@ void launch_tc_gemm(int outmode, int nproj, const TcArgs& a, int max_units, cuda
 }
 
 void launch_rows_to_f16(const uint16_t* src, int rows, int K, uint16_t* dst, int32_t* exps, float* zero_rows,
-                        int zero_len, cudaStream_t s) {
+                        int zero_len, cudaStream_t s, const int32_t* map, int map_div, int zero_count) {
     if (rows <= 0) return;
+    if (zero_count < 0) zero_count = rows;
     const int grid = std::min(rows, num_sms() * 8);
     NVFP4_LAUNCH("rows_to_f16", s,
                  launch_pdl(rows_to_f16_kernel, dim3(grid), dim3(256), 0, s, src, rows, K, dst, exps, zero_rows,
-                            zero_len));
+                            zero_len, map, map_div, zero_count));
 }
 
 void launch_acc_to_bf16(const float* acc, size_t n, uint16_t* out, cudaStream_t s) {
