@@ -113,23 +113,34 @@ struct TcArgs {
     int32_t* status;             // optional: NVFP4_ERR_TIMEOUT if a bounded wait expired
 };
 
-// ---- prompt-shaped gate/up with the routed rows as M (tcgen05, N = 256) ----
+// ---- prompt-shaped grouped GEMMs with the routed rows as M (tcgen05, N = 256) ----
+enum TcmEpi { TCM_SWIGLU = 0, TCM_COMBINE = 1, TCM_BF16 = 2 };
+
 struct TcmArgs {
-    CUtensorMap tmap_x;          // f16 rows in expert order [R, K], box 64 x 128, 128-byte swizzle
-    int K, F;
+    CUtensorMap tmap_x;          // f16 rows [R, K] (expert order), box 64 x 128, 128-byte swizzle
+    CUtensorMap tmap_wc[2];      // weight codes [E*N, K/2] uint8, box 32 x 128
+    CUtensorMap tmap_ws[2];      // weight scales [E*N, K/16] uint8, box 16 x 128
+    int K, N, top_k;             // N: features of one projection (gate/up: F, down: d)
     const int32_t* offsets;      // [E+1]
     const int32_t* active;       // [E]
     const int32_t* n_active;     // [1]
     const int32_t* tile_start;   // [E+1] prefix of ceil(rows / 128) over active experts
-    const uint8_t* a_codes[2];   // gate, up [E, F, K/2]
-    const uint8_t* a_scales[2];  // [E, F, K/16]
+    const uint8_t* a_codes[2];   // weights [E, N, K/2] (SwiGLU: gate, up)
+    const uint8_t* a_scales[2];  // [E, N, K/16]
     const float* a_ws2[2];       // [E]
     const int32_t* x_exp;        // [R] value of an f16 row = f16 * 2^x_exp[row]
-    uint16_t* h_out;             // [R, F] bf16 SwiGLU
-    int32_t* status;
+    uint16_t* h_out;             // TCM_SWIGLU: [R, N] bf16
+    float* acc_out;              // TCM_COMBINE: [T, N] fp32, zeroed before
+    const int32_t* row_to_slot;  // TCM_COMBINE: [R]
+    const float* topk_w;         // TCM_COMBINE: [T*k]
+    uint16_t* y_out;             // TCM_BF16: [R, N]
+    int32_t* status;             // NVFP4_ERR_TIMEOUT if a bounded wait expired
 };
 bool make_tmap_rows_f16(CUtensorMap* map, const void* base, int rows, int K);
-void launch_tcm_gateup(const TcmArgs& a, int max_units, cudaStream_t s);
+bool tcm_supported(int epi, int N, int K);
+// Fills tmap_wc / tmap_ws from a_codes / a_scales (rows = E * N, K = a->K).
+bool tcm_set_weights(TcmArgs* a, long long rows);
+void launch_tcm(int epi, const TcmArgs& a, int max_units, cudaStream_t s);
 
 size_t tc_smem_bytes(int nproj);
 void launch_tc_gemm(int outmode, int nproj, const TcArgs& a, int max_units, cudaStream_t s);

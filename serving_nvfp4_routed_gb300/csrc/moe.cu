@@ -158,12 +158,12 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
     if (use_tc(mode, T, E, top_k, d, F)) {
         // x -> f16 rows in expert order (and zero the combine accumulator)
         launch_rows_to_f16(x, R, d, ws.xp, ws.xp_exp, ws.acc, d, s, ws.ra.row_to_slot, top_k, T);
-        const int max_units = (R / kTcTokTile + std::min(E, R) + 1) * (std::max(d, F) / 128);
+        const int max_tiles = R / kTcTokTile + std::min(E, R) + 1;
         // gate/up + SwiGLU -> h (bf16)
         TcmArgs g{};
-        if (!make_tmap_rows_f16(&g.tmap_x, ws.xp, R, d)) return NVFP4_ERR_CUDA;
         g.K = d;
-        g.F = F;
+        g.N = F;
+        g.top_k = top_k;
         g.offsets = ws.ra.offsets;
         g.active = ws.ra.active;
         g.n_active = ws.ra.n_active;
@@ -173,29 +173,67 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
         g.x_exp = ws.xp_exp;
         g.h_out = ws.h;
         g.status = d_status;
-        launch_tcm_gateup(g, max_units, s);
+        if (tcm_supported(TCM_SWIGLU, F, d)) {
+            if (!make_tmap_rows_f16(&g.tmap_x, ws.xp, R, d) || !tcm_set_weights(&g, (long long)E * F))
+                return NVFP4_ERR_CUDA;
+            launch_tcm(TCM_SWIGLU, g, max_tiles * (F / 128), s);
+        } else {
+            TcArgs t{};
+            t.top_k = top_k;
+            t.offsets = ws.ra.offsets;
+            t.active = ws.ra.active;
+            t.n_active = ws.ra.n_active;
+            t.tile_start = ws.ra.tile_start_tc;
+            t.row_to_slot = nullptr;
+            t.status = d_status;
+            t.K = d;
+            t.N = F;
+            for (int p = 0; p < 2; ++p) {
+                t.a_codes[p] = g.a_codes[p];  t.a_scales[p] = g.a_scales[p];  t.a_ws2[p] = g.a_ws2[p];
+            }
+            t.b_f16 = ws.xp;
+            t.b_exp = ws.xp_exp;
+            t.b_by_token = 0;
+            t.h_out = ws.h;
+            launch_tc_gemm(TC_OUT_H, 2, t, max_tiles * (F / 128), s);
+        }
         // h -> f16 rows
         launch_rows_to_f16(ws.h, R, F, ws.hh, ws.h_exp, nullptr, 0, s);
         // down + weighted combine
-        TcArgs u{};
-        u.top_k = top_k;
-        u.offsets = ws.ra.offsets;
-        u.active = ws.ra.active;
-        u.n_active = ws.ra.n_active;
-        u.tile_start = ws.ra.tile_start_tc;
-        u.row_to_slot = ws.ra.row_to_slot;
-        u.topk_w = ws.ra.w;
-        u.status = d_status;
-        u.K = F;
-        u.N = d;
-        u.a_codes[0] = w->down.codes;  u.a_scales[0] = w->down.scales;  u.a_ws2[0] = w->down.weight_scale_2;
-        u.a_codes[1] = u.a_codes[0];   u.a_scales[1] = u.a_scales[0];   u.a_ws2[1] = u.a_ws2[0];
-        u.b_f16 = ws.hh;
-        u.b_exp = ws.h_exp;
-        u.b_by_token = 0;
-        u.h_out = nullptr;
-        u.acc_out = ws.acc;
-        launch_tc_gemm(TC_OUT_COMBINE, 1, u, max_units, s);
+        if (tcm_supported(TCM_COMBINE, d, F)) {
+            TcmArgs u = g;
+            u.K = F;
+            u.N = d;
+            u.a_codes[0] = w->down.codes;  u.a_scales[0] = w->down.scales;  u.a_ws2[0] = w->down.weight_scale_2;
+            u.a_codes[1] = u.a_codes[0];   u.a_scales[1] = u.a_scales[0];   u.a_ws2[1] = u.a_ws2[0];
+            u.x_exp = ws.h_exp;
+            u.h_out = nullptr;
+            u.acc_out = ws.acc;
+            u.row_to_slot = ws.ra.row_to_slot;
+            u.topk_w = ws.ra.w;
+            if (!make_tmap_rows_f16(&u.tmap_x, ws.hh, R, F) || !tcm_set_weights(&u, (long long)E * d))
+                return NVFP4_ERR_CUDA;
+            launch_tcm(TCM_COMBINE, u, max_tiles * (d / 256), s);
+        } else {
+            TcArgs u{};
+            u.top_k = top_k;
+            u.offsets = ws.ra.offsets;
+            u.active = ws.ra.active;
+            u.n_active = ws.ra.n_active;
+            u.tile_start = ws.ra.tile_start_tc;
+            u.row_to_slot = ws.ra.row_to_slot;
+            u.topk_w = ws.ra.w;
+            u.status = d_status;
+            u.K = F;
+            u.N = d;
+            u.a_codes[0] = w->down.codes;  u.a_scales[0] = w->down.scales;  u.a_ws2[0] = w->down.weight_scale_2;
+            u.a_codes[1] = u.a_codes[0];   u.a_scales[1] = u.a_scales[0];   u.a_ws2[1] = u.a_ws2[0];
+            u.b_f16 = ws.hh;
+            u.b_exp = ws.h_exp;
+            u.b_by_token = 0;
+            u.acc_out = ws.acc;
+            launch_tc_gemm(TC_OUT_COMBINE, 1, u, max_tiles * (d / 128), s);
+        }
         launch_acc_to_bf16(ws.acc, (size_t)T * d, out, s);
         return last_launch_status();
     }
@@ -374,20 +412,34 @@ extern "C" nvfp4_status nvfp4_linear(const uint16_t* x, int M, int K, const nvfp
         t.b_exp = l.x_exp;
         t.b_by_token = 1;
         const int max_units = ((M + kTcTokTile - 1) / kTcTokTile) * (N / 128);
-        if (w_up) {
-            TcmArgs g{};
+        TcmArgs g{};
+        const bool tcm = tcm_supported(w_up ? TCM_SWIGLU : TCM_BF16, N, K);
+        if (tcm) {
             if (!make_tmap_rows_f16(&g.tmap_x, l.xh, M, K)) return NVFP4_ERR_CUDA;
             g.K = K;
-            g.F = N;
+            g.N = N;
+            g.top_k = 1;
             g.offsets = t.offsets;
             g.active = t.active;
             g.n_active = t.n_active;
             g.tile_start = t.tile_start;
-            g.a_codes[0] = w->codes;     g.a_scales[0] = w->scales;     g.a_ws2[0] = w->weight_scale_2;
-            g.a_codes[1] = w_up->codes;  g.a_scales[1] = w_up->scales;  g.a_ws2[1] = w_up->weight_scale_2;
+            g.a_codes[0] = w->codes;  g.a_scales[0] = w->scales;  g.a_ws2[0] = w->weight_scale_2;
+            g.a_codes[1] = w->codes;  g.a_scales[1] = w->scales;  g.a_ws2[1] = w->weight_scale_2;
             g.x_exp = l.x_exp;
+        }
+        if (tcm && w_up) {
+            g.a_codes[1] = w_up->codes;  g.a_scales[1] = w_up->scales;  g.a_ws2[1] = w_up->weight_scale_2;
             g.h_out = out;
-            launch_tcm_gateup(g, max_units, stream);
+            if (!tcm_set_weights(&g, N)) return NVFP4_ERR_CUDA;
+            launch_tcm(TCM_SWIGLU, g, max_units, stream);
+        } else if (tcm) {
+            g.y_out = out;
+            if (!tcm_set_weights(&g, N)) return NVFP4_ERR_CUDA;
+            launch_tcm(TCM_BF16, g, (max_units + 1) / 2, stream);
+        } else if (w_up) {
+            t.a_codes[1] = w_up->codes;  t.a_scales[1] = w_up->scales;  t.a_ws2[1] = w_up->weight_scale_2;
+            t.h_out = out;
+            launch_tc_gemm(TC_OUT_H, 2, t, max_units, stream);
         } else {
             t.y_out = out;
             launch_tc_gemm(TC_OUT_BF16, 1, t, max_units, stream);

@@ -1,26 +1,37 @@
-// moe_tcm.cu -- prompt-shaped gate/up + SwiGLU with the routed rows as the
-// MMA's M dimension and gate and up stacked as one N = 256 operand.
+// moe_tcm.cu -- prompt-shaped grouped NVFP4 expert GEMMs on the 5th-generation
+// tensor cores with the routed rows as the MMA's M dimension.
 //
 // TensorFold issue #308 "GLM-5.3-Flash on CUDA: read nvidia/GLM-5.3-Flash-NVFP4
 // (ModelOpt NVFP4) as stored, W4A16": "What the branch does" (routed experts
-// as one grouped kernel over bf16 rows, weight_scale_2 per expert) and
-// "Questions", item 4 (prompts get their own kernel).
+// as one grouped kernel over bf16 rows, weight_scale_2 per expert; dense MLP
+// with gate and up apart) and "Questions", item 4 (prompts get their own
+// kernel, whose sums run in a different order from decode's).
 //
-// Unit = (expert e, 128 features f0.., 128 routed rows row0.. of e):
-//   D[j, n] = sum_k X[row0 + j, k] * Wn[k],  n < 128: gate row f0 + n,
-//                                           n >= 128: up row f0 + n - 128
-// One tcgen05.mma kind::f16 (M = 128, N = 256, K = 16) costs about the same
-// as one with N = 128, so stacking gate and up in N halves the instruction
-// count, and makes both halves of a SwiGLU pair land in the same TMEM lane.
-// A (rows): f16 copies of x in expert order, one 128 x 64 tile per k-stage
-//    by TMA (128-byte swizzle) -- one elected thread, async proxy.
-// B (weights): eight producer warps, one weight row per thread, stream the
-//    row's e2m1 codes and e4m3 scales through a register ring, dequantise to
-//    f16 (exact) and store the row into the 128-byte-swizzled K-major tile.
+// Unit = (expert e, one 256-wide slice of B rows, 128 routed rows of e):
+//   D[j, n] = sum_k X[row0 + j, k] * B[n, k]
+//   SwiGLU: B rows 0..127 = gate rows f0.., 128..255 = up rows f0.. of e, so
+//           the two halves of a SwiGLU pair sit in one TMEM lane;
+//   combine / bf16: B rows = 256 consecutive rows f0.. of one projection.
+// One tcgen05.mma kind::f16 with M = 128, N = 256, K = 16 runs at the full
+// dense rate; N = 128 takes the same time, hence the 256-wide B.
+// A (rows): f16 copies of the activations (a per-row power of two taken out,
+//    exact), a 128 x 64 tile per k-stage by TMA with 128-byte swizzle, in a
+//    ring of SA stages.
+// B (weights): the stored e2m1 codes (128 rows x 32 bytes per box) and e4m3
+//    scales (128 rows x 16 bytes, four k-stages) arrive by TMA in rings of
+//    SR and SS slots; sixteen producer warps, half a B row per thread,
+//    dequantise them to f16 (exact) into the 128-byte-swizzled K-major tile,
+//    ring of SB.
 // One thread issues the MMAs into fp32 accumulators in TMEM (two buffers of
-// 256 columns); four epilogue warps read them (one row per thread: G in
-// columns 0..127, U in 128..255) and write h = bf16(silu(bf16 G) * bf16 U).
-// mbarrier waits are bounded (about 2 s) and report NVFP4_ERR_TIMEOUT.
+// 256 columns) and commits each k-stage to one "stage done" barrier that
+// frees both rings.  Four epilogue warps read a buffer (one row per thread).
+// A producer that reads a TMA-filled slot with ordinary loads issues a proxy
+// fence before it releases the slot: without it the slot's next TMA fill was
+// seen to land before those loads had read it.
+// The CTA's work list (expert, rows, slice) is decoded once into shared
+// memory at the start.  Every mbarrier wait is bounded (about 2 s): on
+// expiry the kernel records NVFP4_ERR_TIMEOUT, every role leaves its loop
+// and the CTA still frees its tensor memory.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -35,55 +46,62 @@ namespace {
 
 using namespace tc;
 
-constexpr int BM = 128;           // routed rows per unit (MMA M)
-constexpr int BF = 128;           // features per unit (gate + up = MMA N = 256)
-constexpr int BN = 2 * BF;
-constexpr int BK = 64;            // K per stage
-constexpr int kStages = 4;
-constexpr int kABytes = BM * BK * 2;  // 16 KB
-constexpr int kBBytes = BN * BK * 2;  // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kSmem = kStages * kStageBytes + 1024;
-constexpr int kWarps = 16;
+constexpr int BM = 128;            // routed rows per unit (MMA M)
+constexpr int BN = 256;            // B rows per unit (MMA N)
+constexpr int BK = 64;             // K per stage (one 128-byte swizzle row of f16)
+constexpr int SA = 3;              // A (rows) ring depth
+constexpr int SB = 4;              // B (f16 weights) ring depth
+constexpr int SR = 4;              // raw weight codes ring depth (k-stages)
+constexpr int SS = 2;              // raw weight scales ring depth (groups of four k-stages)
+constexpr int SD = SA > SB ? SA : SB;  // "stage done" barriers
+constexpr int kABytes = BM * BK * 2;   // 16 KB
+constexpr int kBBytes = BN * BK * 2;   // 32 KB
+constexpr int kRawBytes = BN * BK / 2; // 8 KB: two boxes of 128 rows x 32 bytes
+constexpr int kScBytes = BN * 16;      // 4 KB: two boxes of 128 rows x 16 bytes
+constexpr int kMaxUnits = 256;         // units per CTA (the host sizes the grid for it)
+constexpr int kTileCopy = kMaxExperts + 1;
+constexpr int kSmem =
+    1024 + SA * kABytes + SB * kBBytes + SR * kRawBytes + SS * kScBytes + kMaxUnits * 16 + kTileCopy * 4;
+constexpr int kWarps = 24;
 constexpr int kThreads = kWarps * 32;
-constexpr int kWarpMma = 0, kWarpTma = 1, kWarpEpi = 4, kWarpDeq = 8, kDeqWarps = 8;
-constexpr int kPD = 6;            // k-stages of weight codes in flight per dequant thread
-constexpr uint32_t kTmemCols = 512;  // two 256-column accumulators
+constexpr int kWarpMma = 0, kWarpTmaA = 1, kWarpTmaB = 2, kWarpEpi = 4, kWarpDeq = 8, kDeqWarps = 16;
+constexpr uint32_t kTmemCols = 512;    // two 256-column accumulators
 
-struct Unit {
-    int e, row0, row_end, f0;
-};
-
-__device__ __forceinline__ Unit decode_unit(const TcmArgs& a, int u, int n_active, int n_ft) {
-    int lo = 0, hi = n_active;
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (a.tile_start[mid] * n_ft <= u) lo = mid; else hi = mid;
-    }
-    const int e = a.active[lo];
-    const int ntt = a.tile_start[lo + 1] - a.tile_start[lo];
-    const int local = u - a.tile_start[lo] * n_ft;
-    Unit un;
-    un.e = e;
-    un.f0 = (local / ntt) * BF;
-    un.row0 = a.offsets[e] + (local % ntt) * BM;
-    un.row_end = a.offsets[e + 1];
-    return un;
+// Waits until k-stage j's MMAs completed (j < 0: nothing to wait for).
+__device__ __forceinline__ bool wait_done(const uint64_t* done, long long j, volatile int* abort_flag,
+                                          int32_t* status) {
+    if (j < 0) return true;
+    return mbar_wait(smem_u32(&done[j % SD]), (uint32_t)((j / SD) & 1), abort_flag, status);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) tcm_gateup_kernel(const __grid_constant__ TcmArgs a) {
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant__ TcmArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ __align__(8) uint64_t bar_full[kStages], bar_empty[kStages], bar_acc_full[2], bar_acc_empty[2];
+    uint8_t* ring_a = smem;
+    uint8_t* ring_b = ring_a + SA * kABytes;
+    uint8_t* ring_r = ring_b + SB * kBBytes;
+    uint8_t* ring_s = ring_r + SR * kRawBytes;
+    int4* s_units = reinterpret_cast<int4*>(ring_s + SS * kScBytes);  // {e, row0, row_end, f0}
+    int* s_tiles = reinterpret_cast<int*>(s_units + kMaxUnits);
+    __shared__ __align__(8) uint64_t bar_afull[SA], bar_bfull[SB], bar_done[SD], bar_acc_full[2], bar_acc_empty[2];
+    __shared__ __align__(8) uint64_t bar_rfull[SR], bar_rempty[SR], bar_sfull[SS], bar_sempty[SS];
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
     grid_dep_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(smem_u32(&bar_full[s]), 1 + kDeqWarps);  // TMA producer + one arrive per dequant warp
-            mbar_init(smem_u32(&bar_empty[s]), 1);
+        for (int s = 0; s < SA; ++s) mbar_init(smem_u32(&bar_afull[s]), 1);
+        for (int s = 0; s < SB; ++s) mbar_init(smem_u32(&bar_bfull[s]), kDeqWarps);
+        for (int s = 0; s < SD; ++s) mbar_init(smem_u32(&bar_done[s]), 1);
+        for (int s = 0; s < SR; ++s) {
+            mbar_init(smem_u32(&bar_rfull[s]), 1);
+            mbar_init(smem_u32(&bar_rempty[s]), kDeqWarps);
+        }
+        for (int s = 0; s < SS; ++s) {
+            mbar_init(smem_u32(&bar_sfull[s]), 1);
+            mbar_init(smem_u32(&bar_sempty[s]), kDeqWarps);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&bar_acc_full[b]), 1);
@@ -93,101 +111,212 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_gateup_kernel(const __grid_co
         mbar_fence_init();
     }
     if (warp == kWarpMma) tmem_alloc(smem_u32(&s_tmem), kTmemCols);
+
+    // ---- this CTA's work list ----
+    const int n_active = *a.n_active;
+    const int n_nt = EPI == TCM_SWIGLU ? a.N / (BN / 2) : a.N / BN;  // B slices per expert
+    for (int i = threadIdx.x; i <= n_active; i += kThreads) s_tiles[i] = a.tile_start[i];
+    __syncthreads();
+    const int total = s_tiles[n_active] * n_nt;
+    const int my_units = blockIdx.x < total ? (total - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    for (int t = threadIdx.x; t < my_units && t < kMaxUnits; t += kThreads) {
+        const int u = blockIdx.x + t * gridDim.x;
+        int lo = 0, hi = n_active;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (s_tiles[mid] * n_nt <= u) lo = mid; else hi = mid;
+        }
+        const int e = a.active[lo];
+        const int ntt = s_tiles[lo + 1] - s_tiles[lo];
+        const int local = u - s_tiles[lo] * n_nt;
+        const int f0 = (local / ntt) * (EPI == TCM_SWIGLU ? BN / 2 : BN);
+        const int row0 = a.offsets[e] + (local % ntt) * BM;
+        s_units[t] = make_int4(e, row0, a.offsets[e + 1], f0);
+    }
+    if (threadIdx.x == 0 && my_units > kMaxUnits) {
+        s_abort = 1;
+        if (a.status) atomicExch(a.status, (int)NVFP4_ERR_SHAPE);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
     volatile int* abort_flag = &s_abort;
-
-    const int n_active = *a.n_active;
-    const int n_ft = a.F / BF;
-    const int total = a.tile_start[n_active] * n_ft;
+    const int n_units = *abort_flag ? 0 : my_units;
     const int nk = a.K / BK;
-    const int my_units = blockIdx.x < total ? (total - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-    const long long n_items = (long long)my_units * nk;  // (unit, k-stage) pairs of this CTA
 
     if (warp == kWarpMma) {
-        // ---------------- MMA issue ----------------
-        const uint32_t idesc = idesc_f16_f32(BM, BN);
-        long long i = 0;
-        for (int it = 0; it < my_units; ++it) {
-            const int acc = it & 1;
-            if (!warp_wait(smem_u32(&bar_acc_empty[acc]), ((it >> 1) & 1) ^ 1, abort_flag, a.status)) break;
-            tc_fence_after();
-            const uint32_t d = tmem + acc * BN;
-            for (int kc = 0; kc < nk; ++kc, ++i) {
-                const int s = (int)(i % kStages);
-                if (!warp_wait(smem_u32(&bar_full[s]), (uint32_t)((i / kStages) & 1), abort_flag, a.status))
-                    goto mma_done;
+        // ---------------- MMA issue (one thread) ----------------
+        if (lane == 0) {
+            const uint32_t idesc = idesc_f16_f32(BM, BN);
+            long long i = 0;
+            for (int it = 0; it < n_units; ++it) {
+                const int acc = it & 1;
+                if (!mbar_wait(smem_u32(&bar_acc_empty[acc]), ((it >> 1) & 1) ^ 1, abort_flag, a.status)) break;
                 tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t sa = smem_u32(smem + s * kStageBytes);
-                    const uint64_t adesc = sdesc_sw128(sa), bdesc = sdesc_sw128(sa + kABytes);
+                const uint32_t d = tmem + acc * BN;
+                bool ok = true;
+                for (int kc = 0; kc < nk; ++kc, ++i) {
+                    const int sa = (int)(i % SA), sb = (int)(i % SB);
+                    if (!mbar_wait(smem_u32(&bar_afull[sa]), (uint32_t)((i / SA) & 1), abort_flag, a.status) ||
+                        !mbar_wait(smem_u32(&bar_bfull[sb]), (uint32_t)((i / SB) & 1), abort_flag, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t adesc = sdesc_sw128(smem_u32(ring_a + sa * kABytes));
+                    const uint64_t bdesc = sdesc_sw128(smem_u32(ring_b + sb * kBBytes));
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
                         mma_f16(d, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kc | kk) != 0);
-                    mma_commit(smem_u32(&bar_empty[s]));
+                    mma_commit(smem_u32(&bar_done[i % SD]));
                 }
-                __syncwarp();
+                if (!ok) break;
+                mma_commit(smem_u32(&bar_acc_full[acc]));
             }
-            if (lane == 0) mma_commit(smem_u32(&bar_acc_full[acc]));
-            __syncwarp();
         }
-    mma_done:;
-    } else if (warp == kWarpTma) {
-        // ---------------- A producer: routed rows by TMA ----------------
-        long long i = 0;
-        for (int it = 0; it < my_units; ++it) {
-            const Unit un = decode_unit(a, blockIdx.x + it * gridDim.x, n_active, n_ft);
-            for (int kc = 0; kc < nk; ++kc, ++i) {
-                const int s = (int)(i % kStages);
-                if (!warp_wait(smem_u32(&bar_empty[s]), (uint32_t)(((i / kStages) & 1) ^ 1), abort_flag, a.status))
-                    goto tma_done;
-                if (lane == 0) {
-                    const uint32_t bar = smem_u32(&bar_full[s]);
+        __syncwarp();
+    } else if (warp == kWarpTmaB) {
+        // ---------------- raw weights by TMA (one thread) ----------------
+        if (lane == 0) {
+            long long i = 0, g = 0;
+            bool ok = true;
+            for (int it = 0; it < n_units && ok; ++it) {
+                const int4 un = s_units[it];
+                // B rows 0..127 and 128..255: (map, row) of each half
+                const int y0 = un.x * a.N + un.w;
+                const int y1 = EPI == TCM_SWIGLU ? y0 : y0 + BN / 2;
+                const void* mc1 = EPI == TCM_SWIGLU ? (const void*)&a.tmap_wc[1] : (const void*)&a.tmap_wc[0];
+                const void* ms1 = EPI == TCM_SWIGLU ? (const void*)&a.tmap_ws[1] : (const void*)&a.tmap_ws[0];
+                for (int kc = 0; kc < nk; ++kc, ++i) {
+                    if ((kc & 3) == 0) {
+                        const int ss = (int)(g % SS);
+                        if (!mbar_wait(smem_u32(&bar_sempty[ss]), (uint32_t)(((g / SS) & 1) ^ 1), abort_flag,
+                                       a.status)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t bar = smem_u32(&bar_sfull[ss]);
+                        mbar_arrive_expect_tx(bar, kScBytes);
+                        uint8_t* dst = ring_s + ss * kScBytes;
+                        tma_load_2d(smem_u32(dst), &a.tmap_ws[0], kc * 4, y0, bar);
+                        tma_load_2d(smem_u32(dst + kScBytes / 2), ms1, kc * 4, y1, bar);
+                        ++g;
+                    }
+                    const int sr = (int)(i % SR);
+                    if (!mbar_wait(smem_u32(&bar_rempty[sr]), (uint32_t)(((i / SR) & 1) ^ 1), abort_flag,
+                                   a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t bar = smem_u32(&bar_rfull[sr]);
+                    mbar_arrive_expect_tx(bar, kRawBytes);
+                    uint8_t* dst = ring_r + sr * kRawBytes;
+                    tma_load_2d(smem_u32(dst), &a.tmap_wc[0], kc * 32, y0, bar);
+                    tma_load_2d(smem_u32(dst + kRawBytes / 2), mc1, kc * 32, y1, bar);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == kWarpTmaA) {
+        // ---------------- A producer: routed rows by TMA (one thread) ----------------
+        if (lane == 0) {
+            long long i = 0;
+            for (int it = 0; it < n_units; ++it) {
+                const int row0 = s_units[it].y;
+                bool ok = true;
+                for (int kc = 0; kc < nk; ++kc, ++i) {
+                    if (!wait_done(bar_done, i - SA, abort_flag, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t bar = smem_u32(&bar_afull[i % SA]);
                     mbar_arrive_expect_tx(bar, kABytes);
-                    tma_load_2d(smem_u32(smem + s * kStageBytes), &a.tmap_x, kc * BK, un.row0, bar);
+                    tma_load_2d(smem_u32(ring_a + (i % SA) * kABytes), &a.tmap_x, kc * BK, row0, bar);
                 }
-                __syncwarp();
+                if (!ok) break;
             }
         }
-    tma_done:;
+        __syncwarp();
     } else if (warp >= kWarpEpi && warp < kWarpEpi + 4) {
         // ---------------- epilogue: one routed row per thread ----------------
         const int q = warp - kWarpEpi;
         const int rr = q * 32 + lane;  // row within the unit = TMEM lane
-        for (int it = 0; it < my_units; ++it) {
-            const Unit un = decode_unit(a, blockIdx.x + it * gridDim.x, n_active, n_ft);
+        for (int it = 0; it < n_units; ++it) {
+            const int4 un = s_units[it];
             const int acc = it & 1;
-            const int row = un.row0 + rr;
-            const bool valid = row < un.row_end;
-            const float rs = valid ? exp2i(a.x_exp[row]) : 0.0f;
-            const float wg = a.a_ws2[0][un.e], wu = a.a_ws2[1][un.e];
-            if (!warp_wait(smem_u32(&bar_acc_full[acc]), (it >> 1) & 1, abort_flag, a.status, 128)) break;
+            const int row = un.y + rr;
+            const bool valid = row < un.z;
+            float rs = 0.0f, wt = 0.0f;
+            size_t tok = 0;
+            if (valid) {
+                rs = exp2i(a.x_exp[row]);
+                if constexpr (EPI == TCM_COMBINE) {
+                    const int slot = a.row_to_slot[row];
+                    tok = (size_t)(slot / a.top_k);
+                    wt = a.topk_w[slot];
+                }
+            }
+            const float w0 = a.a_ws2[0][un.x], w1 = a.a_ws2[1][un.x];
+            if (!mbar_wait(smem_u32(&bar_acc_full[acc]), (it >> 1) & 1, abort_flag, a.status, 64)) break;
             tc_fence_after();
             const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + acc * BN;
-            for (int cb = 0; cb < BF / 32; ++cb) {
-                uint32_t g[32], u[32];
-                tmem_ld32(tb + cb * 32, g);
-                tmem_ld32(tb + BF + cb * 32, u);
-                tmem_ld_wait();
-                if (valid) {
-                    uint32_t packed[16];
+            if constexpr (EPI == TCM_SWIGLU) {
+                for (int cb = 0; cb < BN / 32; ++cb) {
+                    uint32_t g[16], u[16];
+                    tmem_ld16(tb + cb * 16, g);
+                    tmem_ld16(tb + BN / 2 + cb * 16, u);
+                    tmem_ld_wait();
+                    if (valid) {
+                        uint32_t packed[8];
 #pragma unroll
-                    for (int j = 0; j < 32; j += 2) {
-                        float hv[2];
+                        for (int j = 0; j < 16; j += 2) {
+                            float hv[2];
 #pragma unroll
-                        for (int t = 0; t < 2; ++t) {
-                            const float G = round_bf16(__fmul_rn(__fmul_rn(__uint_as_float(g[j + t]), rs), wg));
-                            const float U = round_bf16(__fmul_rn(__fmul_rn(__uint_as_float(u[j + t]), rs), wu));
-                            hv[t] = G / (1.0f + expf(-G)) * U;
+                            for (int t = 0; t < 2; ++t) {
+                                const float G = round_bf16(__fmul_rn(__fmul_rn(__uint_as_float(g[j + t]), rs), w0));
+                                const float U = round_bf16(__fmul_rn(__fmul_rn(__uint_as_float(u[j + t]), rs), w1));
+                                hv[t] = G / (1.0f + expf(-G)) * U;
+                            }
+                            packed[j / 2] =
+                                (uint32_t)f32_to_bf16_bits(hv[0]) | ((uint32_t)f32_to_bf16_bits(hv[1]) << 16);
                         }
-                        packed[j / 2] = (uint32_t)f32_to_bf16_bits(hv[0]) | ((uint32_t)f32_to_bf16_bits(hv[1]) << 16);
+                        uint4* dst = reinterpret_cast<uint4*>(a.h_out + (size_t)row * a.N + un.w + cb * 16);
+                        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
                     }
-                    uint4* dst = reinterpret_cast<uint4*>(a.h_out + (size_t)row * a.F + un.f0 + cb * 32);
+                }
+            } else {
+                for (int cb = 0; cb < BN / 32; ++cb) {
+                    uint32_t r[32];
+                    tmem_ld32(tb + cb * 32, r);
+                    tmem_ld_wait();
+                    if (valid) {
+                        if constexpr (EPI == TCM_COMBINE) {
+                            float4* dst = reinterpret_cast<float4*>(a.acc_out + tok * a.N + un.w + cb * 32);
 #pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+                            for (int v = 0; v < 8; ++v) {
+                                float y[4];
+#pragma unroll
+                                for (int t = 0; t < 4; ++t)
+                                    y[t] = wt * __fmul_rn(__fmul_rn(__uint_as_float(r[4 * v + t]), rs), w0);
+                                atomicAdd(dst + v, make_float4(y[0], y[1], y[2], y[3]));
+                            }
+                        } else {
+                            uint32_t packed[16];
+#pragma unroll
+                            for (int j = 0; j < 32; j += 2) {
+                                const float y0 = __fmul_rn(__fmul_rn(__uint_as_float(r[j]), rs), w0);
+                                const float y1 = __fmul_rn(__fmul_rn(__uint_as_float(r[j + 1]), rs), w0);
+                                packed[j / 2] = (uint32_t)f32_to_bf16_bits(y0) | ((uint32_t)f32_to_bf16_bits(y1) << 16);
+                            }
+                            uint4* dst = reinterpret_cast<uint4*>(a.y_out + (size_t)row * a.N + un.w + cb * 32);
+#pragma unroll
+                            for (int v = 0; v < 4; ++v)
+                                dst[v] =
+                                    make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+                        }
+                    }
                 }
             }
             tc_fence_before();
@@ -195,68 +324,65 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_gateup_kernel(const __grid_co
             if (lane == 0) mbar_arrive(smem_u32(&bar_acc_empty[acc]));
         }
     } else if (warp >= kWarpDeq) {
-        // ---------------- B producer: NVFP4 weight rows -> f16 tile rows ----------------
-        const int j = threadIdx.x - kWarpDeq * 32;  // B row: 0..127 gate, 128..255 up
-        const int p = j / BF;
-        const size_t K2 = (size_t)a.K / 2, K16 = (size_t)a.K / 16;
-        // issue side of the register ring, kPD (unit, k-stage) items ahead
-        int iu = 0, ikc = 0;
-        const uint8_t* icp = nullptr;
-        const uint8_t* isp = nullptr;
-        auto set_unit = [&]() {
-            if (iu < my_units) {
-                const Unit un = decode_unit(a, blockIdx.x + iu * gridDim.x, n_active, n_ft);
-                const size_t rowg = (size_t)un.e * a.F + un.f0 + (j % BF);
-                icp = a.a_codes[p] + rowg * K2;
-                isp = a.a_scales[p] + rowg * K16;
-            }
-        };
-        uint32_t ring[kPD][9];
-        auto issue = [&](uint32_t (&r)[9]) {
-            if (iu < my_units) {
-                const uint4 c0 = __ldg(reinterpret_cast<const uint4*>(icp + (size_t)ikc * 32));
-                const uint4 c1 = __ldg(reinterpret_cast<const uint4*>(icp + (size_t)ikc * 32) + 1);
-                r[0] = c0.x; r[1] = c0.y; r[2] = c0.z; r[3] = c0.w;
-                r[4] = c1.x; r[5] = c1.y; r[6] = c1.z; r[7] = c1.w;
-                r[8] = __ldg(reinterpret_cast<const uint32_t*>(isp + (size_t)ikc * 4));
-                if (++ikc == nk) {
-                    ikc = 0;
-                    ++iu;
-                    set_unit();
+        // ---------------- B producer: raw NVFP4 rows -> f16 tile rows ----------------
+        const int dj = threadIdx.x - kWarpDeq * 32;
+        const int j = dj & (BN - 1);  // B row of the unit
+        const int h = dj / BN;        // which 32 of the stage's 64 k values
+        long long i = 0, g = 0;
+        bool ok = true;
+        uint32_t sc4[4] = {0u, 0u, 0u, 0u};
+        for (int it = 0; it < n_units && ok; ++it) {
+            for (int kc = 0; kc < nk; ++kc, ++i) {
+                if ((kc & 3) == 0) {
+                    // this row's scales for the next four k-stages
+                    const int ss = (int)(g % SS);
+                    if (!mbar_wait(smem_u32(&bar_sfull[ss]), (uint32_t)((g / SS) & 1), abort_flag, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint4 v = *reinterpret_cast<const uint4*>(ring_s + ss * kScBytes + j * 16);
+                    sc4[0] = v.x; sc4[1] = v.y; sc4[2] = v.z; sc4[3] = v.w;
+                    // the slot is refilled by TMA (async proxy): order these
+                    // generic-proxy reads before that write
+                    fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&bar_sempty[ss]));
+                    ++g;
                 }
-            }
-        };
-        set_unit();
+                const int sr = (int)(i % SR);
+                if (!mbar_wait(smem_u32(&bar_rfull[sr]), (uint32_t)((i / SR) & 1), abort_flag, a.status)) {
+                    ok = false;
+                    break;
+                }
+                const uint4 c = *reinterpret_cast<const uint4*>(ring_r + sr * kRawBytes + j * 32 + h * 16);
+                fence_proxy_async();  // as above: read before the slot's next TMA fill
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bar_rempty[sr]));
+                const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+                if (!wait_done(bar_done, i - SB, abort_flag, a.status)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* rowp = ring_b + (i % SB) * kBBytes + j * 128;
+                const int q4 = kc & 3;
+                const uint32_t sw = q4 == 0 ? sc4[0] : q4 == 1 ? sc4[1] : q4 == 2 ? sc4[2] : sc4[3];
+                // the two 16-value blocks of this half: scales (2h, 2h + 1)
+                const uint32_t S01 = e4m3x2_to_f16x2(h ? (sw >> 16) : (sw & 0xFFFFu));
+                const uint32_t Sb[2] = {f16x2_bcast(S01, 0), f16x2_bcast(S01, 1)};
 #pragma unroll
-        for (int uu = 0; uu < kPD; ++uu) issue(ring[uu]);
-        for (long long i0 = 0; i0 < n_items; i0 += kPD) {
-#pragma unroll
-            for (int uu = 0; uu < kPD; ++uu) {
-                const long long i = i0 + uu;
-                if (i >= n_items) break;
-                const int s = (int)(i % kStages);
-                if (!warp_wait(smem_u32(&bar_empty[s]), (uint32_t)(((i / kStages) & 1) ^ 1), abort_flag, a.status))
-                    goto deq_done;
-                uint8_t* rowp = smem + s * kStageBytes + kABytes + j * 128;
-                const uint32_t sw = ring[uu][8];
-                const uint32_t S01 = e4m3x2_to_f16x2(sw & 0xFFFFu), S23 = e4m3x2_to_f16x2(sw >> 16);
-                const uint32_t Sb[4] = {f16x2_bcast(S01, 0), f16x2_bcast(S01, 1), f16x2_bcast(S23, 0),
-                                        f16x2_bcast(S23, 1)};
-#pragma unroll
-                for (int w = 0; w < 8; ++w) {
+                for (int w = 0; w < 4; ++w) {
                     uint32_t f[4];
-                    e2m1x8_to_f16x8(ring[uu][w], f);
+                    e2m1x8_to_f16x8(cw[w], f);
                     const uint32_t S2 = Sb[w >> 1];
-                    *reinterpret_cast<uint4*>(rowp + ((w ^ (j & 7)) << 4)) =
+                    const int chunk = h * 4 + w;  // 16-byte chunk of the 128-byte row
+                    *reinterpret_cast<uint4*>(rowp + ((chunk ^ (j & 7)) << 4)) =
                         make_uint4(hmul2_u32(f[0], S2), hmul2_u32(f[1], S2), hmul2_u32(f[2], S2), hmul2_u32(f[3], S2));
                 }
                 fence_proxy_async();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&bar_full[s]));
-                issue(ring[uu]);
+                if (lane == 0) mbar_arrive(smem_u32(&bar_bfull[i % SB]));
             }
         }
-    deq_done:;
     }
 
     tc_fence_before();
@@ -271,17 +397,35 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_gateup_kernel(const __grid_co
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
+template <int EPI>
+void launch_tcm_t(const TcmArgs& a, int max_units, cudaStream_t s, const char* name) {
+    auto kern = tcm_kernel<EPI>;
+    static bool init = false;
+    if (!init) {
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        init = true;
+    }
+    int grid = std::max(1, std::min(max_units, num_sms()));
+    grid = std::max(grid, (max_units + kMaxUnits - 1) / kMaxUnits);
+    NVFP4_LAUNCH(name, s, launch_pdl(kern, dim3(grid), dim3(kThreads), (size_t)kSmem, s, a));
+}
+
 }  // namespace
 
-bool make_tmap_rows_f16(CUtensorMap* map, const void* base, int rows, int K) {
+void init_encode() {
     std::call_once(g_encode_once, []() {
         cudaDriverEntryPointQueryResult q;
         void* fn = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
             g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     });
-    if (!g_encode) return false;
+}
+
+bool make_tmap_rows_f16(CUtensorMap* map, const void* base, int rows, int K) {
+    init_encode();
+    if (!g_encode || rows < 1 || K % BK != 0 || !aligned16(base)) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
     const cuuint32_t box[2] = {BK, BM};
@@ -291,15 +435,44 @@ bool make_tmap_rows_f16(CUtensorMap* map, const void* base, int rows, int K) {
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-void launch_tcm_gateup(const TcmArgs& a, int max_units, cudaStream_t s) {
-    static bool init = false;
-    if (!init) {
-        cudaFuncSetAttribute(tcm_gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-        init = true;
-    }
-    const int grid = std::max(1, std::min(max_units, num_sms()));
-    NVFP4_LAUNCH("tcm_gateup_w4a16", s,
-                 launch_pdl(tcm_gateup_kernel, dim3(grid), dim3(kThreads), (size_t)kSmem, s, a));
+// The stored codes [rows, K/2] and scales [rows, K/16] of an NVFP4 tensor as
+// uint8 tensor maps: boxes of 128 rows x 32 bytes (one k-stage of codes) and
+// 128 rows x 16 bytes (four k-stages of scales), no swizzle.
+bool make_tmap_weights(CUtensorMap* codes, CUtensorMap* scales, const uint8_t* c, const uint8_t* sc, long long rows,
+                       int K) {
+    if (!g_encode || rows < 1 || K % 256 != 0 || !aligned16(c) || !aligned16(sc)) return false;
+    const cuuint32_t estr[2] = {1, 1};
+    const cuuint64_t cd[2] = {(cuuint64_t)K / 2, (cuuint64_t)rows};
+    const cuuint64_t cs[1] = {(cuuint64_t)K / 2};
+    const cuuint32_t cb[2] = {32, 128};
+    if (g_encode(codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(c), cd, cs, cb, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    const cuuint64_t sd[2] = {(cuuint64_t)K / 16, (cuuint64_t)rows};
+    const cuuint64_t ss[1] = {(cuuint64_t)K / 16};
+    const cuuint32_t sb[2] = {16, 128};
+    return g_encode(scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(sc), sd, ss, sb, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool tcm_supported(int epi, int N, int K) {
+    return K % 256 == 0 && (epi == TCM_SWIGLU ? N % (BN / 2) == 0 : N % BN == 0);
+}
+
+bool tcm_set_weights(TcmArgs* a, long long rows) {
+    init_encode();
+    for (int p = 0; p < 2; ++p)
+        if (!make_tmap_weights(&a->tmap_wc[p], &a->tmap_ws[p], a->a_codes[p], a->a_scales[p], rows, a->K))
+            return false;
+    return true;
+}
+
+void launch_tcm(int epi, const TcmArgs& a, int max_units, cudaStream_t s) {
+    if (epi == TCM_SWIGLU) return launch_tcm_t<TCM_SWIGLU>(a, max_units, s, "tcm_gateup_w4a16");
+    if (epi == TCM_COMBINE) return launch_tcm_t<TCM_COMBINE>(a, max_units, s, "tcm_down_w4a16");
+    return launch_tcm_t<TCM_BF16>(a, max_units, s, "tcm_linear_w4a16");
 }
 
 }  // namespace nvfp4

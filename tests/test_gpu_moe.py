@@ -210,9 +210,26 @@ def test_dense_mlp_full_size_sampled(orc):
     qg, qu, qd = (lib.nvfp4_quantize_weights(w) for w in (wg, wu, wd))
     h = lib.nvfp4_linear(x, qg, qu)
     y = lib.nvfp4_linear(h, qd)
-    rows = np.array([0, 4097, 8191])
+    # rows from many 128-row tiles: a CTA's later work units get checked too
+    rows = np.unique(np.append(np.random.default_rng(4005).choice(M, 22, replace=False), [0, M - 1]))
     og, ou, od = (orc.quantize_tensor(synth.bf16_bits(w)) for w in (wg, wu, wd))
     href = orc.linear(synth.bf16_bits(x)[rows], og[0], og[1], og[2], wup=ou)
     assert_layer_close(bf16_to_f32(h)[rows], href, "dense gate/up")
     yref = orc.linear(synth.bf16_bits(torch.from_numpy(href).to(torch.bfloat16)), od[0], od[1], od[2])
     assert_layer_close(bf16_to_f32(y)[rows], yref, "dense down")
+
+
+def test_linear_many_units_per_cta(orc):
+    """Single-projection linear with 8192 rows, K=1536, N=4096: every CTA of
+    the prompt-shaped kernel works through several (row tile, column slice)
+    units, so ring slots are refilled many times; sampled rows from many
+    tiles against the oracle."""
+    M, K, N = 8192, 1536, 4096
+    x = synth.make_x(M, K, seed=4101, device="cuda", outlier_frac=0.05)
+    w = synth.make_weights(1, N, K, 4102, "cuda")[0]
+    q = lib.nvfp4_quantize_weights(w)
+    y = lib.nvfp4_linear(x, q)
+    rows = np.unique(np.append(np.random.default_rng(4103).choice(M, 30, replace=False), [0, M - 1]))
+    oq = orc.quantize_tensor(synth.bf16_bits(w))
+    yref = orc.linear(synth.bf16_bits(x)[rows], oq[0], oq[1], oq[2])
+    assert_layer_close(bf16_to_f32(y)[rows], yref, "linear K=1536 N=4096")
