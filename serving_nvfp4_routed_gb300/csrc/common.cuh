@@ -134,6 +134,15 @@ __device__ __forceinline__ void e2m1x8_to_f16x8(uint32_t w, uint32_t out[4]) {
         : "r"(w));
 }
 
+// e2m1 codes of two values as one byte (lo in the low nibble), sign kept.
+__device__ __forceinline__ uint32_t e2m1x2_byte(float lo, float hi) {
+    uint32_t r;
+    asm("{\n.reg .b8 b;\ncvt.rn.satfinite.e2m1x2.f32 b, %1, %2;\nmov.b32 %0, {b, b, b, b};\n}"
+        : "=r"(r)
+        : "f"(hi), "f"(lo));
+    return (r & 0xFFu) | ((__float_as_uint(lo) >> 31) << 3) | ((__float_as_uint(hi) >> 31) << 7);
+}
+
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
     __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
     return *reinterpret_cast<uint32_t*>(&r);

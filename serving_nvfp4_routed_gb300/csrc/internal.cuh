@@ -114,10 +114,15 @@ struct TcArgs {
 };
 
 // ---- prompt-shaped grouped GEMMs with the routed rows as M (tcgen05, N = 256) ----
-enum TcmEpi { TCM_SWIGLU = 0, TCM_COMBINE = 1, TCM_BF16 = 2 };
+// SWIGLU: h = bf16(silu(bf16 G) * bf16 U); SWIGLU_Q: h requantised to NVFP4
+// (codes + e4m3 block scales under hq_gs); COMBINE: weighted red.add into
+// the fp32 accumulator; BF16: plain bf16 rows.
+enum TcmEpi { TCM_SWIGLU = 0, TCM_COMBINE = 1, TCM_BF16 = 2, TCM_SWIGLU_Q = 3 };
 
 struct TcmArgs {
     CUtensorMap tmap_x;          // f16 rows [R, K] (expert order), box 64 x 128, 128-byte swizzle
+    CUtensorMap tmap_ac;         // NVFP4 rows instead (a_nvfp4): codes [R, K/2], box 32 x 128
+    CUtensorMap tmap_as;         //   and e4m3 scales [R, K/16], box 16 x 128
     CUtensorMap tmap_wc[2];      // weight codes [E*N, K/2] uint8, box 32 x 128
     CUtensorMap tmap_ws[2];      // weight scales [E*N, K/16] uint8, box 16 x 128
     int K, N, top_k;             // N: features of one projection (gate/up: F, down: d)
@@ -129,18 +134,25 @@ struct TcmArgs {
     const uint8_t* a_scales[2];  // [E, N, K/16]
     const float* a_ws2[2];       // [E]
     const int32_t* x_exp;        // [R] value of an f16 row = f16 * 2^x_exp[row]
+    const float* x_gs;           // NVFP4 rows: [E] global scale of the rows of expert e
     uint16_t* h_out;             // TCM_SWIGLU: [R, N] bf16
     float* acc_out;              // TCM_COMBINE: [T, N] fp32, zeroed before
     const int32_t* row_to_slot;  // TCM_COMBINE: [R]
     const float* topk_w;         // TCM_COMBINE: [T*k]
     uint16_t* y_out;             // TCM_BF16: [R, N]
+    uint8_t* hq_out;             // TCM_SWIGLU_Q: [R, N/2] codes
+    uint8_t* hs_out;             //   [R, N/16] e4m3 block scales
+    const float* hq_gs;          //   [E] global scale they are taken under
     int32_t* status;             // NVFP4_ERR_TIMEOUT if a bounded wait expired
 };
 bool make_tmap_rows_f16(CUtensorMap* map, const void* base, int rows, int K);
 bool tcm_supported(int epi, int N, int K);
 // Fills tmap_wc / tmap_ws from a_codes / a_scales (rows = E * N, K = a->K).
 bool tcm_set_weights(TcmArgs* a, long long rows);
-void launch_tcm(int epi, const TcmArgs& a, int max_units, cudaStream_t s);
+// Fills tmap_ac / tmap_as: NVFP4 activation rows [rows, a->K].
+bool tcm_set_act(TcmArgs* a, const uint8_t* codes, const uint8_t* scales, long long rows);
+// a_nvfp4: A rows are NVFP4 (tmap_ac / tmap_as, x_gs), else f16 (tmap_x, x_exp).
+void launch_tcm(int epi, int a_nvfp4, const TcmArgs& a, int max_units, cudaStream_t s);
 
 size_t tc_smem_bytes(int nproj);
 void launch_tc_gemm(int outmode, int nproj, const TcArgs& a, int max_units, cudaStream_t s);

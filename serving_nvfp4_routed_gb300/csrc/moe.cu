@@ -60,6 +60,15 @@ bool use_tc(int mode, int T, int E, int k, int d, int F) {
     return R >= 32LL * std::min<long long>(E, R);
 }
 
+// W4A4 on the tensor cores: NVFP4 activation rows fed to the same kernel.
+bool use_tc_w4a4(int T, int E, int k, int d, int F) {
+    if (!tcm_supported(TCM_SWIGLU_Q, F, d) || !tcm_supported(TCM_COMBINE, d, F)) return false;
+    const int f = forced_path();
+    if (f >= 0) return f == 1;
+    const long long R = (long long)T * k;
+    return R >= 32LL * std::min<long long>(E, R);
+}
+
 MoeWs carve_moe(void* base, int T, int E, int k, int d, int F, int mode, size_t* bytes) {
     Carver c(base);
     const size_t R = (size_t)T * k;
@@ -155,6 +164,45 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
     if (mode == 1)
         launch_quantize_act(x, R, d, ws.ra.row_to_slot, top_k, is13, ws.ra.offsets, E, ws.xq, ws.xs, s);
 
+    if (mode == 1 && use_tc_w4a4(T, E, top_k, d, F)) {
+        const int max_tiles = R / kTcTokTile + std::min(E, R) + 1;
+        launch_zero(ws.acc, sizeof(float) * (size_t)T * d, s);
+        // gate/up + SwiGLU, h requantised under the down projection's input scale
+        TcmArgs g{};
+        g.K = d;
+        g.N = F;
+        g.top_k = top_k;
+        g.offsets = ws.ra.offsets;
+        g.active = ws.ra.active;
+        g.n_active = ws.ra.n_active;
+        g.tile_start = ws.ra.tile_start_tc;
+        g.a_codes[0] = w->gate.codes;  g.a_scales[0] = w->gate.scales;  g.a_ws2[0] = w->gate.weight_scale_2;
+        g.a_codes[1] = w->up.codes;    g.a_scales[1] = w->up.scales;    g.a_ws2[1] = w->up.weight_scale_2;
+        g.x_gs = is13;
+        g.hq_out = ws.hq;
+        g.hs_out = ws.hs;
+        g.hq_gs = is2;
+        g.status = d_status;
+        if (!tcm_set_weights(&g, (long long)E * F) || !tcm_set_act(&g, ws.xq, ws.xs, R)) return NVFP4_ERR_CUDA;
+        launch_tcm(TCM_SWIGLU_Q, 1, g, max_tiles * (F / 128), s);
+        // down + weighted combine
+        TcmArgs u = g;
+        u.K = F;
+        u.N = d;
+        u.a_codes[0] = w->down.codes;  u.a_scales[0] = w->down.scales;  u.a_ws2[0] = w->down.weight_scale_2;
+        u.a_codes[1] = u.a_codes[0];   u.a_scales[1] = u.a_scales[0];   u.a_ws2[1] = u.a_ws2[0];
+        u.x_gs = is2;
+        u.hq_out = nullptr;
+        u.hs_out = nullptr;
+        u.acc_out = ws.acc;
+        u.row_to_slot = ws.ra.row_to_slot;
+        u.topk_w = ws.ra.w;
+        if (!tcm_set_weights(&u, (long long)E * d) || !tcm_set_act(&u, ws.hq, ws.hs, R)) return NVFP4_ERR_CUDA;
+        launch_tcm(TCM_COMBINE, 1, u, max_tiles * (d / 256), s);
+        launch_acc_to_bf16(ws.acc, (size_t)T * d, out, s);
+        return last_launch_status();
+    }
+
     if (use_tc(mode, T, E, top_k, d, F)) {
         // x -> f16 rows in expert order (and zero the combine accumulator)
         launch_rows_to_f16(x, R, d, ws.xp, ws.xp_exp, ws.acc, d, s, ws.ra.row_to_slot, top_k, T);
@@ -176,7 +224,7 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
         if (tcm_supported(TCM_SWIGLU, F, d)) {
             if (!make_tmap_rows_f16(&g.tmap_x, ws.xp, R, d) || !tcm_set_weights(&g, (long long)E * F))
                 return NVFP4_ERR_CUDA;
-            launch_tcm(TCM_SWIGLU, g, max_tiles * (F / 128), s);
+            launch_tcm(TCM_SWIGLU, 0, g, max_tiles * (F / 128), s);
         } else {
             TcArgs t{};
             t.top_k = top_k;
@@ -213,7 +261,7 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
             u.topk_w = ws.ra.w;
             if (!make_tmap_rows_f16(&u.tmap_x, ws.hh, R, F) || !tcm_set_weights(&u, (long long)E * d))
                 return NVFP4_ERR_CUDA;
-            launch_tcm(TCM_COMBINE, u, max_tiles * (d / 256), s);
+            launch_tcm(TCM_COMBINE, 0, u, max_tiles * (d / 256), s);
         } else {
             TcArgs u{};
             u.top_k = top_k;
@@ -431,11 +479,11 @@ extern "C" nvfp4_status nvfp4_linear(const uint16_t* x, int M, int K, const nvfp
             g.a_codes[1] = w_up->codes;  g.a_scales[1] = w_up->scales;  g.a_ws2[1] = w_up->weight_scale_2;
             g.h_out = out;
             if (!tcm_set_weights(&g, N)) return NVFP4_ERR_CUDA;
-            launch_tcm(TCM_SWIGLU, g, max_units, stream);
+            launch_tcm(TCM_SWIGLU, 0, g, max_units, stream);
         } else if (tcm) {
             g.y_out = out;
             if (!tcm_set_weights(&g, N)) return NVFP4_ERR_CUDA;
-            launch_tcm(TCM_BF16, g, (max_units + 1) / 2, stream);
+            launch_tcm(TCM_BF16, 0, g, (max_units + 1) / 2, stream);
         } else if (w_up) {
             t.a_codes[1] = w_up->codes;  t.a_scales[1] = w_up->scales;  t.a_ws2[1] = w_up->weight_scale_2;
             t.h_out = out;

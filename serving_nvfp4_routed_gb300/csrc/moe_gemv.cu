@@ -84,14 +84,6 @@ __device__ __forceinline__ uint32_t bf16x2_scaled_to_f16x2(uint32_t u, float sc)
     return f32x2_to_f16x2(bf16_bits_to_f32(u & 0xFFFFu) * sc, bf16_bits_to_f32(u >> 16) * sc);
 }
 
-// e2m1 codes of two values as one byte (lo in the low nibble), sign kept.
-__device__ __forceinline__ uint32_t e2m1x2_byte(float lo, float hi) {
-    uint32_t r;
-    asm("{\n.reg .b8 b;\ncvt.rn.satfinite.e2m1x2.f32 b, %1, %2;\nmov.b32 %0, {b, b, b, b};\n}"
-        : "=r"(r)
-        : "f"(hi), "f"(lo));
-    return (r & 0xFFu) | ((__float_as_uint(lo) >> 31) << 3) | ((__float_as_uint(hi) >> 31) << 7);
-}
 
 // Shared-memory layout of the staged B rows: row g holds K f16 values as K/8
 // 16-byte granules; granule q is stored at bsw(q, g) so that the B-fragment

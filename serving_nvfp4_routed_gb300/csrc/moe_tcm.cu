@@ -16,7 +16,9 @@
 // dense rate; N = 128 takes the same time, hence the 256-wide B.
 // A (rows): f16 copies of the activations (a per-row power of two taken out,
 //    exact), a 128 x 64 tile per k-stage by TMA with 128-byte swizzle, in a
-//    ring of SA stages.
+//    ring of SA stages; or (W4A4) NVFP4 rows whose codes and scales ride in
+//    the weight rings below and are dequantised to f16 (exact) by the same
+//    producer warps, the expert's global scale applied in the epilogue.
 // B (weights): the stored e2m1 codes (128 rows x 32 bytes per box) and e4m3
 //    scales (128 rows x 16 bytes, four k-stages) arrive by TMA in rings of
 //    SR and SS slots; sixteen producer warps, half a B row per thread,
@@ -50,39 +52,50 @@ constexpr int BM = 128;            // routed rows per unit (MMA M)
 constexpr int BN = 256;            // B rows per unit (MMA N)
 constexpr int BK = 64;             // K per stage (one 128-byte swizzle row of f16)
 constexpr int SA = 3;              // A (rows) ring depth
-constexpr int SB = 4;              // B (f16 weights) ring depth
-constexpr int SR = 4;              // raw weight codes ring depth (k-stages)
-constexpr int SS = 2;              // raw weight scales ring depth (groups of four k-stages)
-constexpr int SD = SA > SB ? SA : SB;  // "stage done" barriers
+constexpr int SR = 4;              // raw codes ring depth (k-stages)
+constexpr int SS = 2;              // raw scales ring depth (groups of four k-stages)
 constexpr int kABytes = BM * BK * 2;   // 16 KB
 constexpr int kBBytes = BN * BK * 2;   // 32 KB
-constexpr int kRawBytes = BN * BK / 2; // 8 KB: two boxes of 128 rows x 32 bytes
-constexpr int kScBytes = BN * 16;      // 4 KB: two boxes of 128 rows x 16 bytes
+constexpr int kRawB = BN * BK / 2;     // 8 KB: two boxes of 128 weight rows x 32 bytes
+constexpr int kRawA = BM * BK / 2;     // 4 KB: NVFP4 rows, 128 x 32 bytes
+constexpr int kScB = BN * 16;          // 4 KB: two boxes of 128 weight rows x 16 bytes
+constexpr int kScA = BM * 16;          // 2 KB
 constexpr int kMaxUnits = 256;         // units per CTA (the host sizes the grid for it)
 constexpr int kTileCopy = kMaxExperts + 1;
-constexpr int kSmem =
-    1024 + SA * kABytes + SB * kBBytes + SR * kRawBytes + SS * kScBytes + kMaxUnits * 16 + kTileCopy * 4;
+// Ring geometry of each A kind (AQ = 1: NVFP4 rows).
+template <int AQ>
+struct Geo {
+    static constexpr int SB = AQ ? 3 : 4;  // f16 weight tiles
+    static constexpr int SD = SA > SB ? SA : SB;  // "stage done" barriers
+    static constexpr int kRaw = kRawB + (AQ ? kRawA : 0);
+    static constexpr int kSc = kScB + (AQ ? kScA : 0);
+    static constexpr int kSmem =
+        1024 + SA * kABytes + SB * kBBytes + SR * kRaw + SS * kSc + kMaxUnits * 16 + kTileCopy * 4;
+};
 constexpr int kWarps = 24;
 constexpr int kThreads = kWarps * 32;
 constexpr int kWarpMma = 0, kWarpTmaA = 1, kWarpTmaB = 2, kWarpEpi = 4, kWarpDeq = 8, kDeqWarps = 16;
 constexpr uint32_t kTmemCols = 512;    // two 256-column accumulators
 
 // Waits until k-stage j's MMAs completed (j < 0: nothing to wait for).
+template <int SD>
 __device__ __forceinline__ bool wait_done(const uint64_t* done, long long j, volatile int* abort_flag,
                                           int32_t* status) {
     if (j < 0) return true;
     return mbar_wait(smem_u32(&done[j % SD]), (uint32_t)((j / SD) & 1), abort_flag, status);
 }
 
-template <int EPI>
+template <int EPI, int AQ>
 __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant__ TcmArgs a) {
+    using G = Geo<AQ>;
+    constexpr int SB = G::SB, SD = G::SD, kRaw = G::kRaw, kSc = G::kSc;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* ring_a = smem;
     uint8_t* ring_b = ring_a + SA * kABytes;
     uint8_t* ring_r = ring_b + SB * kBBytes;
-    uint8_t* ring_s = ring_r + SR * kRawBytes;
-    int4* s_units = reinterpret_cast<int4*>(ring_s + SS * kScBytes);  // {e, row0, row_end, f0}
+    uint8_t* ring_s = ring_r + SR * kRaw;
+    int4* s_units = reinterpret_cast<int4*>(ring_s + SS * kSc);  // {e, row0, row_end, f0}
     int* s_tiles = reinterpret_cast<int*>(s_units + kMaxUnits);
     __shared__ __align__(8) uint64_t bar_afull[SA], bar_bfull[SB], bar_done[SD], bar_acc_full[2], bar_acc_empty[2];
     __shared__ __align__(8) uint64_t bar_rfull[SR], bar_rempty[SR], bar_sfull[SS], bar_sempty[SS];
@@ -92,7 +105,7 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant_
     grid_dep_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < SA; ++s) mbar_init(smem_u32(&bar_afull[s]), 1);
+        for (int s = 0; s < SA; ++s) mbar_init(smem_u32(&bar_afull[s]), AQ ? kDeqWarps : 1);
         for (int s = 0; s < SB; ++s) mbar_init(smem_u32(&bar_bfull[s]), kDeqWarps);
         for (int s = 0; s < SD; ++s) mbar_init(smem_u32(&bar_done[s]), 1);
         for (int s = 0; s < SR; ++s) {
@@ -114,7 +127,8 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant_
 
     // ---- this CTA's work list ----
     const int n_active = *a.n_active;
-    const int n_nt = EPI == TCM_SWIGLU ? a.N / (BN / 2) : a.N / BN;  // B slices per expert
+    constexpr bool kPair = EPI == TCM_SWIGLU || EPI == TCM_SWIGLU_Q;  // gate + up halves
+    const int n_nt = kPair ? a.N / (BN / 2) : a.N / BN;  // B slices per expert
     for (int i = threadIdx.x; i <= n_active; i += kThreads) s_tiles[i] = a.tile_start[i];
     __syncthreads();
     const int total = s_tiles[n_active] * n_nt;
@@ -129,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant_
         const int e = a.active[lo];
         const int ntt = s_tiles[lo + 1] - s_tiles[lo];
         const int local = u - s_tiles[lo] * n_nt;
-        const int f0 = (local / ntt) * (EPI == TCM_SWIGLU ? BN / 2 : BN);
+        const int f0 = (local / ntt) * (kPair ? BN / 2 : BN);
         const int row0 = a.offsets[e] + (local % ntt) * BM;
         s_units[t] = make_int4(e, row0, a.offsets[e + 1], f0);
     }
@@ -185,9 +199,9 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant_
                 const int4 un = s_units[it];
                 // B rows 0..127 and 128..255: (map, row) of each half
                 const int y0 = un.x * a.N + un.w;
-                const int y1 = EPI == TCM_SWIGLU ? y0 : y0 + BN / 2;
-                const void* mc1 = EPI == TCM_SWIGLU ? (const void*)&a.tmap_wc[1] : (const void*)&a.tmap_wc[0];
-                const void* ms1 = EPI == TCM_SWIGLU ? (const void*)&a.tmap_ws[1] : (const void*)&a.tmap_ws[0];
+                const int y1 = kPair ? y0 : y0 + BN / 2;
+                const void* mc1 = kPair ? (const void*)&a.tmap_wc[1] : (const void*)&a.tmap_wc[0];
+                const void* ms1 = kPair ? (const void*)&a.tmap_ws[1] : (const void*)&a.tmap_ws[0];
                 for (int kc = 0; kc < nk; ++kc, ++i) {
                     if ((kc & 3) == 0) {
                         const int ss = (int)(g % SS);
@@ -197,10 +211,11 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant_
                             break;
                         }
                         const uint32_t bar = smem_u32(&bar_sfull[ss]);
-                        mbar_arrive_expect_tx(bar, kScBytes);
-                        uint8_t* dst = ring_s + ss * kScBytes;
+                        mbar_arrive_expect_tx(bar, kSc);
+                        uint8_t* dst = ring_s + ss * kSc;
                         tma_load_2d(smem_u32(dst), &a.tmap_ws[0], kc * 4, y0, bar);
-                        tma_load_2d(smem_u32(dst + kScBytes / 2), ms1, kc * 4, y1, bar);
+                        tma_load_2d(smem_u32(dst + kScB / 2), ms1, kc * 4, y1, bar);
+                        if constexpr (AQ) tma_load_2d(smem_u32(dst + kScB), &a.tmap_as, kc * 4, un.y, bar);
                         ++g;
                     }
                     const int sr = (int)(i % SR);
@@ -210,23 +225,24 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant_
                         break;
                     }
                     const uint32_t bar = smem_u32(&bar_rfull[sr]);
-                    mbar_arrive_expect_tx(bar, kRawBytes);
-                    uint8_t* dst = ring_r + sr * kRawBytes;
+                    mbar_arrive_expect_tx(bar, kRaw);
+                    uint8_t* dst = ring_r + sr * kRaw;
                     tma_load_2d(smem_u32(dst), &a.tmap_wc[0], kc * 32, y0, bar);
-                    tma_load_2d(smem_u32(dst + kRawBytes / 2), mc1, kc * 32, y1, bar);
+                    tma_load_2d(smem_u32(dst + kRawB / 2), mc1, kc * 32, y1, bar);
+                    if constexpr (AQ) tma_load_2d(smem_u32(dst + kRawB), &a.tmap_ac, kc * 32, un.y, bar);
                 }
             }
         }
         __syncwarp();
     } else if (warp == kWarpTmaA) {
-        // ---------------- A producer: routed rows by TMA (one thread) ----------------
-        if (lane == 0) {
+        // ---------------- A producer: routed f16 rows by TMA (one thread) ----------------
+        if (!AQ && lane == 0) {
             long long i = 0;
             for (int it = 0; it < n_units; ++it) {
                 const int row0 = s_units[it].y;
                 bool ok = true;
                 for (int kc = 0; kc < nk; ++kc, ++i) {
-                    if (!wait_done(bar_done, i - SA, abort_flag, a.status)) {
+                    if (!wait_done<SD>(bar_done, i - SA, abort_flag, a.status)) {
                         ok = false;
                         break;
                     }
@@ -250,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant_
             float rs = 0.0f, wt = 0.0f;
             size_t tok = 0;
             if (valid) {
-                rs = exp2i(a.x_exp[row]);
+                rs = AQ ? a.x_gs[un.x] : exp2i(a.x_exp[row]);
                 if constexpr (EPI == TCM_COMBINE) {
                     const int slot = a.row_to_slot[row];
                     tok = (size_t)(slot / a.top_k);
@@ -261,7 +277,43 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant_
             if (!mbar_wait(smem_u32(&bar_acc_full[acc]), (it >> 1) & 1, abort_flag, a.status, 64)) break;
             tc_fence_after();
             const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + acc * BN;
-            if constexpr (EPI == TCM_SWIGLU) {
+            if constexpr (EPI == TCM_SWIGLU_Q) {
+                // h in 16-feature blocks, requantised to NVFP4 under hq_gs[e]
+                const float gs2 = a.hq_gs[un.x];
+                for (int cb = 0; cb < BN / 32; ++cb) {
+                    uint32_t g[16], u[16];
+                    tmem_ld16(tb + cb * 16, g);
+                    tmem_ld16(tb + BN / 2 + cb * 16, u);
+                    tmem_ld_wait();
+                    if (valid) {
+                        float hv[16];
+                        float m = 0.0f;
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) {
+                            const float G = round_bf16(__fmul_rn(__fmul_rn(__uint_as_float(g[t]), rs), w0));
+                            const float U = round_bf16(__fmul_rn(__fmul_rn(__uint_as_float(u[t]), rs), w1));
+                            hv[t] = round_bf16(G / (1.0f + expf(-G)) * U);
+                            m = fmaxf(m, fabsf(hv[t]));
+                        }
+                        uint32_t sbyte = 0, q0 = 0, q1 = 0;
+                        if (gs2 > 0.0f) {
+                            sbyte = f32_to_e4m3(__fdiv_rn(__fdiv_rn(m, 6.0f), gs2));
+                            const float S = e4m3_to_f32(sbyte);
+                            if (S != 0.0f) {
+                                const float den = __fmul_rn(S, gs2);
+#pragma unroll
+                                for (int t = 0; t < 8; t += 2) {
+                                    q0 |= e2m1x2_byte(__fdiv_rn(hv[t], den), __fdiv_rn(hv[t + 1], den)) << (4 * t);
+                                    q1 |= e2m1x2_byte(__fdiv_rn(hv[8 + t], den), __fdiv_rn(hv[9 + t], den)) << (4 * t);
+                                }
+                            }
+                        }
+                        const int f = un.w + cb * 16;
+                        *reinterpret_cast<uint2*>(a.hq_out + (size_t)row * (a.N / 2) + f / 2) = make_uint2(q0, q1);
+                        a.hs_out[(size_t)row * (a.N / 16) + f / 16] = (uint8_t)sbyte;
+                    }
+                }
+            } else if constexpr (EPI == TCM_SWIGLU) {
                 for (int cb = 0; cb < BN / 32; ++cb) {
                     uint32_t g[16], u[16];
                     tmem_ld16(tb + cb * 16, g);
@@ -324,13 +376,15 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant_
             if (lane == 0) mbar_arrive(smem_u32(&bar_acc_empty[acc]));
         }
     } else if (warp >= kWarpDeq) {
-        // ---------------- B producer: raw NVFP4 rows -> f16 tile rows ----------------
+        // ---------------- producers: raw NVFP4 rows -> f16 tile rows ----------------
         const int dj = threadIdx.x - kWarpDeq * 32;
         const int j = dj & (BN - 1);  // B row of the unit
         const int h = dj / BN;        // which 32 of the stage's 64 k values
+        const int ra = dj >> 2;       // AQ: A row of the unit
+        const int ab = dj & 3;        // AQ: its 16-value block of the stage
         long long i = 0, g = 0;
         bool ok = true;
-        uint32_t sc4[4] = {0u, 0u, 0u, 0u};
+        uint32_t sc4[4] = {0u, 0u, 0u, 0u}, asc4[4] = {0u, 0u, 0u, 0u};
         for (int it = 0; it < n_units && ok; ++it) {
             for (int kc = 0; kc < nk; ++kc, ++i) {
                 if ((kc & 3) == 0) {
@@ -340,8 +394,12 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant_
                         ok = false;
                         break;
                     }
-                    const uint4 v = *reinterpret_cast<const uint4*>(ring_s + ss * kScBytes + j * 16);
+                    const uint4 v = *reinterpret_cast<const uint4*>(ring_s + ss * kSc + j * 16);
                     sc4[0] = v.x; sc4[1] = v.y; sc4[2] = v.z; sc4[3] = v.w;
+                    if constexpr (AQ) {
+                        const uint4 va = *reinterpret_cast<const uint4*>(ring_s + ss * kSc + kScB + ra * 16);
+                        asc4[0] = va.x; asc4[1] = va.y; asc4[2] = va.z; asc4[3] = va.w;
+                    }
                     // the slot is refilled by TMA (async proxy): order these
                     // generic-proxy reads before that write
                     fence_proxy_async();
@@ -354,12 +412,15 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant_
                     ok = false;
                     break;
                 }
-                const uint4 c = *reinterpret_cast<const uint4*>(ring_r + sr * kRawBytes + j * 32 + h * 16);
+                const uint4 c = *reinterpret_cast<const uint4*>(ring_r + sr * kRaw + j * 32 + h * 16);
+                uint2 ca = make_uint2(0u, 0u);
+                if constexpr (AQ) ca = *reinterpret_cast<const uint2*>(ring_r + sr * kRaw + kRawB + ra * 32 + ab * 8);
                 fence_proxy_async();  // as above: read before the slot's next TMA fill
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&bar_rempty[sr]));
                 const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
-                if (!wait_done(bar_done, i - SB, abort_flag, a.status)) {
+                // the A and B slots of this stage are free once stage i - min(SA, SB) is done
+                if (!wait_done<SD>(bar_done, i - (AQ ? (SA < SB ? SA : SB) : SB), abort_flag, a.status)) {
                     ok = false;
                     break;
                 }
@@ -378,9 +439,26 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant_
                     *reinterpret_cast<uint4*>(rowp + ((chunk ^ (j & 7)) << 4)) =
                         make_uint4(hmul2_u32(f[0], S2), hmul2_u32(f[1], S2), hmul2_u32(f[2], S2), hmul2_u32(f[3], S2));
                 }
+                if constexpr (AQ) {
+                    uint8_t* arow = ring_a + (i % SA) * kABytes + ra * 128;
+                    const uint32_t aw = q4 == 0 ? asc4[0] : q4 == 1 ? asc4[1] : q4 == 2 ? asc4[2] : asc4[3];
+                    const uint32_t SA2 = f16x2_bcast(e4m3x2_to_f16x2((aw >> (8 * ab)) & 0xFFu), 0);
+                    const uint32_t caw[2] = {ca.x, ca.y};
+#pragma unroll
+                    for (int w = 0; w < 2; ++w) {
+                        uint32_t f[4];
+                        e2m1x8_to_f16x8(caw[w], f);
+                        const int chunk = ab * 2 + w;
+                        *reinterpret_cast<uint4*>(arow + ((chunk ^ (ra & 7)) << 4)) = make_uint4(
+                            hmul2_u32(f[0], SA2), hmul2_u32(f[1], SA2), hmul2_u32(f[2], SA2), hmul2_u32(f[3], SA2));
+                    }
+                }
                 fence_proxy_async();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&bar_bfull[i % SB]));
+                if (lane == 0) {
+                    mbar_arrive(smem_u32(&bar_bfull[i % SB]));
+                    if constexpr (AQ) mbar_arrive(smem_u32(&bar_afull[i % SA]));
+                }
             }
         }
     }
@@ -397,17 +475,18 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant_
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
-template <int EPI>
+template <int EPI, int AQ>
 void launch_tcm_t(const TcmArgs& a, int max_units, cudaStream_t s, const char* name) {
-    auto kern = tcm_kernel<EPI>;
+    auto kern = tcm_kernel<EPI, AQ>;
+    constexpr int smem = Geo<AQ>::kSmem;
     static bool init = false;
     if (!init) {
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         init = true;
     }
     int grid = std::max(1, std::min(max_units, num_sms()));
     grid = std::max(grid, (max_units + kMaxUnits - 1) / kMaxUnits);
-    NVFP4_LAUNCH(name, s, launch_pdl(kern, dim3(grid), dim3(kThreads), (size_t)kSmem, s, a));
+    NVFP4_LAUNCH(name, s, launch_pdl(kern, dim3(grid), dim3(kThreads), (size_t)smem, s, a));
 }
 
 }  // namespace
@@ -458,7 +537,8 @@ bool make_tmap_weights(CUtensorMap* codes, CUtensorMap* scales, const uint8_t* c
 }
 
 bool tcm_supported(int epi, int N, int K) {
-    return K % 256 == 0 && (epi == TCM_SWIGLU ? N % (BN / 2) == 0 : N % BN == 0);
+    const bool pair = epi == TCM_SWIGLU || epi == TCM_SWIGLU_Q;
+    return K % 256 == 0 && (pair ? N % (BN / 2) == 0 : N % BN == 0);
 }
 
 bool tcm_set_weights(TcmArgs* a, long long rows) {
@@ -469,10 +549,20 @@ bool tcm_set_weights(TcmArgs* a, long long rows) {
     return true;
 }
 
-void launch_tcm(int epi, const TcmArgs& a, int max_units, cudaStream_t s) {
-    if (epi == TCM_SWIGLU) return launch_tcm_t<TCM_SWIGLU>(a, max_units, s, "tcm_gateup_w4a16");
-    if (epi == TCM_COMBINE) return launch_tcm_t<TCM_COMBINE>(a, max_units, s, "tcm_down_w4a16");
-    return launch_tcm_t<TCM_BF16>(a, max_units, s, "tcm_linear_w4a16");
+bool tcm_set_act(TcmArgs* a, const uint8_t* codes, const uint8_t* scales, long long rows) {
+    init_encode();
+    return make_tmap_weights(&a->tmap_ac, &a->tmap_as, codes, scales, rows, a->K);
+}
+
+void launch_tcm(int epi, int a_nvfp4, const TcmArgs& a, int max_units, cudaStream_t s) {
+    if (a_nvfp4) {
+        if (epi == TCM_SWIGLU_Q) return launch_tcm_t<TCM_SWIGLU_Q, 1>(a, max_units, s, "tcm_gateup_w4a4");
+        if (epi == TCM_COMBINE) return launch_tcm_t<TCM_COMBINE, 1>(a, max_units, s, "tcm_down_w4a4");
+        return;
+    }
+    if (epi == TCM_SWIGLU) return launch_tcm_t<TCM_SWIGLU, 0>(a, max_units, s, "tcm_gateup_w4a16");
+    if (epi == TCM_COMBINE) return launch_tcm_t<TCM_COMBINE, 0>(a, max_units, s, "tcm_down_w4a16");
+    if (epi == TCM_BF16) return launch_tcm_t<TCM_BF16, 0>(a, max_units, s, "tcm_linear_w4a16");
 }
 
 }  // namespace nvfp4

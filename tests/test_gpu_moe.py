@@ -233,3 +233,20 @@ def test_linear_many_units_per_cta(orc):
     oq = orc.quantize_tensor(synth.bf16_bits(w))
     yref = orc.linear(synth.bf16_bits(x)[rows], oq[0], oq[1], oq[2])
     assert_layer_close(bf16_to_f32(y)[rows], yref, "linear K=1536 N=4096")
+
+
+@pytest.mark.parametrize("T,E,k,d,F", [(512, 16, 4, 512, 256), (300, 6, 2, 1024, 384)])
+def test_prompt_w4a4_tensor_cores(orc, T, E, k, d, F, monkeypatch):
+    """W4A4 through the prompt-shaped tensor-core kernels (forced), several
+    work units per expert, against the oracle on every token."""
+    monkeypatch.setenv("NVFP4_PATH", "tc")
+    s = synth.MoEShape(T, d, E, k, F)
+    inp, gw, ob, r, tok = _setup(orc, s, seed=T + 7, outlier=0.05)
+    xb = synth.bf16_bits(inp["x"])
+    is13, is2 = calib.calibrate(xb, inp["logits"].cpu().numpy(), k, ob)
+    st = torch.zeros(4, dtype=torch.int32, device="cuda")
+    out = lib.nvfp4_moe_w4a4(inp["x"], inp["logits"], k, gw, torch.from_numpy(is13).cuda(),
+                             torch.from_numpy(is2).cuda(), d_status=st)
+    ref = orc.moe_layer("w4a4", xb, r["ids"], r["w"], ob, is13=is13, is2=is2)
+    assert_layer_close(bf16_to_f32(out), ref, "prompt w4a4")
+    assert st[0].item() == 0
