@@ -21,7 +21,8 @@
 //    producer warps, the expert's global scale applied in the epilogue.
 // B (weights): the stored e2m1 codes (128 rows x 32 bytes per box) and e4m3
 //    scales (128 rows x 16 bytes, four k-stages) arrive by TMA in rings of
-//    SR and SS slots; sixteen producer warps, half a B row per thread,
+//    SR and SS slots; sixteen producer warps in two groups that take
+//    alternate k-stages (so two stages are in flight), one B row per thread,
 //    dequantise them to f16 (exact) into the 128-byte-swizzled K-major tile,
 //    ring of SB.
 // One thread issues the MMAs into fp32 accumulators in TMEM (two buffers of
@@ -75,6 +76,12 @@ struct Geo {
 constexpr int kWarps = 24;
 constexpr int kThreads = kWarps * 32;
 constexpr int kWarpMma = 0, kWarpTmaA = 1, kWarpTmaB = 2, kWarpEpi = 4, kWarpDeq = 8, kDeqWarps = 16;
+constexpr int kGroups = 2;                      // producer groups, one per k-stage residue
+constexpr int kGroupWarps = kDeqWarps / kGroups;  // warps that produce one k-stage
+
+__device__ __forceinline__ uint32_t pick4(const uint32_t (&v)[4], int q) {
+    return q == 0 ? v[0] : q == 1 ? v[1] : q == 2 ? v[2] : v[3];
+}
 constexpr uint32_t kTmemCols = 512;    // two 256-column accumulators
 
 // Waits until k-stage j's MMAs completed (j < 0: nothing to wait for).
@@ -105,12 +112,12 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant_
     grid_dep_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < SA; ++s) mbar_init(smem_u32(&bar_afull[s]), AQ ? kDeqWarps : 1);
-        for (int s = 0; s < SB; ++s) mbar_init(smem_u32(&bar_bfull[s]), kDeqWarps);
+        for (int s = 0; s < SA; ++s) mbar_init(smem_u32(&bar_afull[s]), AQ ? kGroupWarps : 1);
+        for (int s = 0; s < SB; ++s) mbar_init(smem_u32(&bar_bfull[s]), kGroupWarps);
         for (int s = 0; s < SD; ++s) mbar_init(smem_u32(&bar_done[s]), 1);
         for (int s = 0; s < SR; ++s) {
             mbar_init(smem_u32(&bar_rfull[s]), 1);
-            mbar_init(smem_u32(&bar_rempty[s]), kDeqWarps);
+            mbar_init(smem_u32(&bar_rempty[s]), kGroupWarps);
         }
         for (int s = 0; s < SS; ++s) {
             mbar_init(smem_u32(&bar_sfull[s]), 1);
@@ -377,87 +384,93 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant_
         }
     } else if (warp >= kWarpDeq) {
         // ---------------- producers: raw NVFP4 rows -> f16 tile rows ----------------
-        const int dj = threadIdx.x - kWarpDeq * 32;
-        const int j = dj & (BN - 1);  // B row of the unit
-        const int h = dj / BN;        // which 32 of the stage's 64 k values
-        const int ra = dj >> 2;       // AQ: A row of the unit
-        const int ab = dj & 3;        // AQ: its 16-value block of the stage
-        long long i = 0, g = 0;
+        // Group grp takes the k-stages q = grp, grp + kGroups, ... of every
+        // four (a scale group); its 256 threads own one B row each and (W4A4)
+        // half an A row each.  Scale slots are read by every producer warp.
+        const int dw = warp - kWarpDeq;
+        const int grp = dw / kGroupWarps;
+        const int j = (dw % kGroupWarps) * 32 + lane;  // B row of the unit
+        const int ra = j >> 1, ah = j & 1;             // W4A4: A row, which 32 of its 64 k values
+        const int ng = nk / 4;
+        long long gg = 0;
         bool ok = true;
-        uint32_t sc4[4] = {0u, 0u, 0u, 0u}, asc4[4] = {0u, 0u, 0u, 0u};
         for (int it = 0; it < n_units && ok; ++it) {
-            for (int kc = 0; kc < nk; ++kc, ++i) {
-                if ((kc & 3) == 0) {
-                    // this row's scales for the next four k-stages
-                    const int ss = (int)(g % SS);
-                    if (!mbar_wait(smem_u32(&bar_sfull[ss]), (uint32_t)((g / SS) & 1), abort_flag, a.status)) {
-                        ok = false;
-                        break;
-                    }
+            for (int kg = 0; kg < ng && ok; ++kg, ++gg) {
+                // this thread's scales for the four k-stages of the group
+                const int ss = (int)(gg % SS);
+                if (!mbar_wait(smem_u32(&bar_sfull[ss]), (uint32_t)((gg / SS) & 1), abort_flag, a.status)) {
+                    ok = false;
+                    break;
+                }
+                uint32_t sc4[4], asc4[4] = {0u, 0u, 0u, 0u};
+                {
                     const uint4 v = *reinterpret_cast<const uint4*>(ring_s + ss * kSc + j * 16);
                     sc4[0] = v.x; sc4[1] = v.y; sc4[2] = v.z; sc4[3] = v.w;
                     if constexpr (AQ) {
                         const uint4 va = *reinterpret_cast<const uint4*>(ring_s + ss * kSc + kScB + ra * 16);
                         asc4[0] = va.x; asc4[1] = va.y; asc4[2] = va.z; asc4[3] = va.w;
                     }
-                    // the slot is refilled by TMA (async proxy): order these
-                    // generic-proxy reads before that write
+                }
+                // The raw slots are refilled by TMA (async proxy): the proxy
+                // fence after this stage's smem stores also orders these
+                // reads (and the code reads below) before that refill, so
+                // the slots are released together with the f16 tile.
+                bool release_scales = true;
+                for (int q = grp; q < 4; q += kGroups) {
+                    const long long i = (long long)it * nk + kg * 4 + q;
+                    const int sr = (int)(i % SR);
+                    if (!mbar_wait(smem_u32(&bar_rfull[sr]), (uint32_t)((i / SR) & 1), abort_flag, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint4 c0 = *reinterpret_cast<const uint4*>(ring_r + sr * kRaw + j * 32);
+                    const uint4 c1 = *reinterpret_cast<const uint4*>(ring_r + sr * kRaw + j * 32 + 16);
+                    uint4 ca = make_uint4(0u, 0u, 0u, 0u);
+                    if constexpr (AQ) ca = *reinterpret_cast<const uint4*>(ring_r + sr * kRaw + kRawB + ra * 32 + ah * 16);
+                    // the A and B slots of stage i are free once stage i - min(SA, SB) is done
+                    if (!wait_done<SD>(bar_done, i - (AQ ? (SA < SB ? SA : SB) : SB), abort_flag, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* rowp = ring_b + (i % SB) * kBBytes + j * 128;
+                    const uint32_t sw = pick4(sc4, q);
+                    const uint32_t S01 = e4m3x2_to_f16x2(sw & 0xFFFFu), S23 = e4m3x2_to_f16x2(sw >> 16);
+                    const uint32_t Sb[4] = {f16x2_bcast(S01, 0), f16x2_bcast(S01, 1), f16x2_bcast(S23, 0),
+                                            f16x2_bcast(S23, 1)};
+                    const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+                    for (int w = 0; w < 8; ++w) {
+                        uint32_t f[4];
+                        e2m1x8_to_f16x8(cw[w], f);
+                        const uint32_t S2 = Sb[w >> 1];
+                        *reinterpret_cast<uint4*>(rowp + ((w ^ (j & 7)) << 4)) = make_uint4(
+                            hmul2_u32(f[0], S2), hmul2_u32(f[1], S2), hmul2_u32(f[2], S2), hmul2_u32(f[3], S2));
+                    }
+                    if constexpr (AQ) {
+                        uint8_t* arow = ring_a + (i % SA) * kABytes + ra * 128;
+                        const uint32_t aw = pick4(asc4, q);
+                        const uint32_t SA01 = e4m3x2_to_f16x2(ah ? (aw >> 16) : (aw & 0xFFFFu));
+                        const uint32_t Sa[2] = {f16x2_bcast(SA01, 0), f16x2_bcast(SA01, 1)};
+                        const uint32_t caw[4] = {ca.x, ca.y, ca.z, ca.w};
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            uint32_t f[4];
+                            e2m1x8_to_f16x8(caw[w], f);
+                            const uint32_t S2 = Sa[w >> 1];
+                            const int chunk = ah * 4 + w;
+                            *reinterpret_cast<uint4*>(arow + ((chunk ^ (ra & 7)) << 4)) = make_uint4(
+                                hmul2_u32(f[0], S2), hmul2_u32(f[1], S2), hmul2_u32(f[2], S2), hmul2_u32(f[3], S2));
+                        }
+                    }
                     fence_proxy_async();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&bar_sempty[ss]));
-                    ++g;
-                }
-                const int sr = (int)(i % SR);
-                if (!mbar_wait(smem_u32(&bar_rfull[sr]), (uint32_t)((i / SR) & 1), abort_flag, a.status)) {
-                    ok = false;
-                    break;
-                }
-                const uint4 c = *reinterpret_cast<const uint4*>(ring_r + sr * kRaw + j * 32 + h * 16);
-                uint2 ca = make_uint2(0u, 0u);
-                if constexpr (AQ) ca = *reinterpret_cast<const uint2*>(ring_r + sr * kRaw + kRawB + ra * 32 + ab * 8);
-                fence_proxy_async();  // as above: read before the slot's next TMA fill
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&bar_rempty[sr]));
-                const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
-                // the A and B slots of this stage are free once stage i - min(SA, SB) is done
-                if (!wait_done<SD>(bar_done, i - (AQ ? (SA < SB ? SA : SB) : SB), abort_flag, a.status)) {
-                    ok = false;
-                    break;
-                }
-                uint8_t* rowp = ring_b + (i % SB) * kBBytes + j * 128;
-                const int q4 = kc & 3;
-                const uint32_t sw = q4 == 0 ? sc4[0] : q4 == 1 ? sc4[1] : q4 == 2 ? sc4[2] : sc4[3];
-                // the two 16-value blocks of this half: scales (2h, 2h + 1)
-                const uint32_t S01 = e4m3x2_to_f16x2(h ? (sw >> 16) : (sw & 0xFFFFu));
-                const uint32_t Sb[2] = {f16x2_bcast(S01, 0), f16x2_bcast(S01, 1)};
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    uint32_t f[4];
-                    e2m1x8_to_f16x8(cw[w], f);
-                    const uint32_t S2 = Sb[w >> 1];
-                    const int chunk = h * 4 + w;  // 16-byte chunk of the 128-byte row
-                    *reinterpret_cast<uint4*>(rowp + ((chunk ^ (j & 7)) << 4)) =
-                        make_uint4(hmul2_u32(f[0], S2), hmul2_u32(f[1], S2), hmul2_u32(f[2], S2), hmul2_u32(f[3], S2));
-                }
-                if constexpr (AQ) {
-                    uint8_t* arow = ring_a + (i % SA) * kABytes + ra * 128;
-                    const uint32_t aw = q4 == 0 ? asc4[0] : q4 == 1 ? asc4[1] : q4 == 2 ? asc4[2] : asc4[3];
-                    const uint32_t SA2 = f16x2_bcast(e4m3x2_to_f16x2((aw >> (8 * ab)) & 0xFFu), 0);
-                    const uint32_t caw[2] = {ca.x, ca.y};
-#pragma unroll
-                    for (int w = 0; w < 2; ++w) {
-                        uint32_t f[4];
-                        e2m1x8_to_f16x8(caw[w], f);
-                        const int chunk = ab * 2 + w;
-                        *reinterpret_cast<uint4*>(arow + ((chunk ^ (ra & 7)) << 4)) = make_uint4(
-                            hmul2_u32(f[0], SA2), hmul2_u32(f[1], SA2), hmul2_u32(f[2], SA2), hmul2_u32(f[3], SA2));
+                    if (lane == 0) {
+                        mbar_arrive(smem_u32(&bar_bfull[i % SB]));
+                        if constexpr (AQ) mbar_arrive(smem_u32(&bar_afull[i % SA]));
+                        mbar_arrive(smem_u32(&bar_rempty[sr]));
+                        if (release_scales) mbar_arrive(smem_u32(&bar_sempty[ss]));
                     }
-                }
-                fence_proxy_async();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(smem_u32(&bar_bfull[i % SB]));
-                    if constexpr (AQ) mbar_arrive(smem_u32(&bar_afull[i % SA]));
+                    release_scales = false;
                 }
             }
         }

@@ -29,17 +29,30 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// As mbar_try, but the thread may be suspended in hardware (up to about
+// hint_ns) until the phase completes, instead of spinning on issue slots.
+__device__ __forceinline__ bool mbar_try_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\nselp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
 
 // A wait that gives up: after ~2 s of cycles (or once another role gave up)
 // it records NVFP4_ERR_TIMEOUT and returns false, so that no kernel of the
-// library can hang the GPU on a barrier that never completes.
+// library can hang the GPU on a barrier that never completes.  Between
+// checks the thread sleeps in the barrier (hardware suspend, bounded).
 constexpr long long kWaitCycles = 4000000000LL;
+constexpr uint32_t kSuspendNs = 200000;
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* status,
                                           int sleep_ns = 0) {
     if (mbar_try(bar, parity)) return true;
     const long long t0 = clock64();
     for (;;) {
-        if (mbar_try(bar, parity)) return true;
+        if (mbar_try_sleep(bar, parity, kSuspendNs)) return true;
         if (sleep_ns) __nanosleep(sleep_ns);
         if (*abort_flag) return false;
         if (clock64() - t0 > kWaitCycles) {
