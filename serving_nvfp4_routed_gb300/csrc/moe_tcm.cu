@@ -21,10 +21,10 @@
 //    producer warps, the expert's global scale applied in the epilogue.
 // B (weights): the stored e2m1 codes (128 rows x 32 bytes per box) and e4m3
 //    scales (128 rows x 16 bytes, four k-stages) arrive by TMA in rings of
-//    SR and SS slots; sixteen producer warps in two groups that take
-//    alternate k-stages (so two stages are in flight), one B row per thread,
-//    dequantise them to f16 (exact) into the 128-byte-swizzled K-major tile,
-//    ring of SB.
+//    SR and SS slots; sixteen producer warps in four groups, each taking
+//    every fourth k-stage (so four stages are in flight), two B rows per
+//    thread, dequantise them to f16 (exact) into the 128-byte-swizzled
+//    K-major tile, ring of SB.
 // One thread issues the MMAs into fp32 accumulators in TMEM (two buffers of
 // 256 columns) and commits each k-stage to one "stage done" barrier that
 // frees both rings.  Four epilogue warps read a buffer (one row per thread).
@@ -63,11 +63,17 @@ constexpr int kScB = BN * 16;          // 4 KB: two boxes of 128 weight rows x 1
 constexpr int kScA = BM * 16;          // 2 KB
 constexpr int kMaxUnits = 256;         // units per CTA (the host sizes the grid for it)
 constexpr int kTileCopy = kMaxExperts + 1;
+constexpr int kGroups = 4;                      // producer groups, one per k-stage residue
+constexpr int kGroupWarps = 16 / kGroups;  // warps that produce one k-stage
+static_assert(SR % kGroups == 0, "each raw slot must belong to one producer group");
 // Ring geometry of each A kind (AQ = 1: NVFP4 rows).
 template <int AQ>
 struct Geo {
     static constexpr int SB = AQ ? 3 : 4;  // f16 weight tiles
-    static constexpr int SD = SA > SB ? SA : SB;  // "stage done" barriers
+    static constexpr int SD0 = SA > SB ? SA : SB;
+    // "stage done" barriers: at least every ring depth and the k-stage stride
+    // between two waits of one producer group, so that parity waits stay in phase
+    static constexpr int SD = SD0 > kGroups ? SD0 : kGroups;
     static constexpr int kRaw = kRawB + (AQ ? kRawA : 0);
     static constexpr int kSc = kScB + (AQ ? kScA : 0);
     static constexpr int kSmem =
@@ -76,12 +82,7 @@ struct Geo {
 constexpr int kWarps = 24;
 constexpr int kThreads = kWarps * 32;
 constexpr int kWarpMma = 0, kWarpTmaA = 1, kWarpTmaB = 2, kWarpEpi = 4, kWarpDeq = 8, kDeqWarps = 16;
-constexpr int kGroups = 2;                      // producer groups, one per k-stage residue
-constexpr int kGroupWarps = kDeqWarps / kGroups;  // warps that produce one k-stage
 
-__device__ __forceinline__ uint32_t pick4(const uint32_t (&v)[4], int q) {
-    return q == 0 ? v[0] : q == 1 ? v[1] : q == 2 ? v[2] : v[3];
-}
 constexpr uint32_t kTmemCols = 512;    // two 256-column accumulators
 
 // Waits until k-stage j's MMAs completed (j < 0: nothing to wait for).
@@ -384,60 +385,59 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant_
         }
     } else if (warp >= kWarpDeq) {
         // ---------------- producers: raw NVFP4 rows -> f16 tile rows ----------------
-        // Group grp takes the k-stages q = grp, grp + kGroups, ... of every
-        // four (a scale group); its 256 threads own one B row each and (W4A4)
-        // half an A row each.  Scale slots are read by every producer warp.
+        // Group grp takes k-stage grp of every scale group (four k-stages);
+        // its 128 threads own two B rows each and (W4A4) one A row each.
+        // The proxy fence after the stage's smem stores also orders the
+        // reads of the TMA-filled raw slots before their next fill, so the
+        // raw slots are released together with the f16 tiles.
         const int dw = warp - kWarpDeq;
-        const int grp = dw / kGroupWarps;
-        const int j = (dw % kGroupWarps) * 32 + lane;  // B row of the unit
-        const int ra = j >> 1, ah = j & 1;             // W4A4: A row, which 32 of its 64 k values
+        const int grp = dw / kGroupWarps;              // = the k-stage q of each scale group
+        const int tg = (dw % kGroupWarps) * 32 + lane;  // 0..127: B rows tg and tg + 128, A row tg
         const int ng = nk / 4;
         long long gg = 0;
         bool ok = true;
         for (int it = 0; it < n_units && ok; ++it) {
             for (int kg = 0; kg < ng && ok; ++kg, ++gg) {
-                // this thread's scales for the four k-stages of the group
                 const int ss = (int)(gg % SS);
                 if (!mbar_wait(smem_u32(&bar_sfull[ss]), (uint32_t)((gg / SS) & 1), abort_flag, a.status)) {
                     ok = false;
                     break;
                 }
-                uint32_t sc4[4], asc4[4] = {0u, 0u, 0u, 0u};
-                {
-                    const uint4 v = *reinterpret_cast<const uint4*>(ring_s + ss * kSc + j * 16);
-                    sc4[0] = v.x; sc4[1] = v.y; sc4[2] = v.z; sc4[3] = v.w;
-                    if constexpr (AQ) {
-                        const uint4 va = *reinterpret_cast<const uint4*>(ring_s + ss * kSc + kScB + ra * 16);
-                        asc4[0] = va.x; asc4[1] = va.y; asc4[2] = va.z; asc4[3] = va.w;
-                    }
+                const int q = grp;
+                const uint32_t sw0 = *reinterpret_cast<const uint32_t*>(ring_s + ss * kSc + tg * 16 + q * 4);
+                const uint32_t sw1 = *reinterpret_cast<const uint32_t*>(ring_s + ss * kSc + (tg + 128) * 16 + q * 4);
+                uint32_t asw = 0;
+                if constexpr (AQ) asw = *reinterpret_cast<const uint32_t*>(ring_s + ss * kSc + kScB + tg * 16 + q * 4);
+                const long long i = (long long)it * nk + kg * 4 + q;
+                const int sr = (int)(i % SR);
+                if (!mbar_wait(smem_u32(&bar_rfull[sr]), (uint32_t)((i / SR) & 1), abort_flag, a.status)) {
+                    ok = false;
+                    break;
                 }
-                // The raw slots are refilled by TMA (async proxy): the proxy
-                // fence after this stage's smem stores also orders these
-                // reads (and the code reads below) before that refill, so
-                // the slots are released together with the f16 tile.
-                bool release_scales = true;
-                for (int q = grp; q < 4; q += kGroups) {
-                    const long long i = (long long)it * nk + kg * 4 + q;
-                    const int sr = (int)(i % SR);
-                    if (!mbar_wait(smem_u32(&bar_rfull[sr]), (uint32_t)((i / SR) & 1), abort_flag, a.status)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint4 c0 = *reinterpret_cast<const uint4*>(ring_r + sr * kRaw + j * 32);
-                    const uint4 c1 = *reinterpret_cast<const uint4*>(ring_r + sr * kRaw + j * 32 + 16);
-                    uint4 ca = make_uint4(0u, 0u, 0u, 0u);
-                    if constexpr (AQ) ca = *reinterpret_cast<const uint4*>(ring_r + sr * kRaw + kRawB + ra * 32 + ah * 16);
-                    // the A and B slots of stage i are free once stage i - min(SA, SB) is done
-                    if (!wait_done<SD>(bar_done, i - (AQ ? (SA < SB ? SA : SB) : SB), abort_flag, a.status)) {
-                        ok = false;
-                        break;
-                    }
+                uint4 c[4];
+                c[0] = *reinterpret_cast<const uint4*>(ring_r + sr * kRaw + tg * 32);
+                c[1] = *reinterpret_cast<const uint4*>(ring_r + sr * kRaw + tg * 32 + 16);
+                c[2] = *reinterpret_cast<const uint4*>(ring_r + sr * kRaw + (tg + 128) * 32);
+                c[3] = *reinterpret_cast<const uint4*>(ring_r + sr * kRaw + (tg + 128) * 32 + 16);
+                uint4 ca0 = make_uint4(0u, 0u, 0u, 0u), ca1 = ca0;
+                if constexpr (AQ) {
+                    ca0 = *reinterpret_cast<const uint4*>(ring_r + sr * kRaw + kRawB + tg * 32);
+                    ca1 = *reinterpret_cast<const uint4*>(ring_r + sr * kRaw + kRawB + tg * 32 + 16);
+                }
+                if (!wait_done<SD>(bar_done, i - (AQ ? (SA < SB ? SA : SB) : SB), abort_flag, a.status)) {
+                    ok = false;
+                    break;
+                }
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const int j = tg + rr * 128;
                     uint8_t* rowp = ring_b + (i % SB) * kBBytes + j * 128;
-                    const uint32_t sw = pick4(sc4, q);
+                    const uint32_t sw = rr ? sw1 : sw0;
                     const uint32_t S01 = e4m3x2_to_f16x2(sw & 0xFFFFu), S23 = e4m3x2_to_f16x2(sw >> 16);
                     const uint32_t Sb[4] = {f16x2_bcast(S01, 0), f16x2_bcast(S01, 1), f16x2_bcast(S23, 0),
                                             f16x2_bcast(S23, 1)};
-                    const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                    const uint4 x0 = c[2 * rr], x1 = c[2 * rr + 1];
+                    const uint32_t cw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
                     for (int w = 0; w < 8; ++w) {
                         uint32_t f[4];
@@ -446,31 +446,29 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant_
                         *reinterpret_cast<uint4*>(rowp + ((w ^ (j & 7)) << 4)) = make_uint4(
                             hmul2_u32(f[0], S2), hmul2_u32(f[1], S2), hmul2_u32(f[2], S2), hmul2_u32(f[3], S2));
                     }
-                    if constexpr (AQ) {
-                        uint8_t* arow = ring_a + (i % SA) * kABytes + ra * 128;
-                        const uint32_t aw = pick4(asc4, q);
-                        const uint32_t SA01 = e4m3x2_to_f16x2(ah ? (aw >> 16) : (aw & 0xFFFFu));
-                        const uint32_t Sa[2] = {f16x2_bcast(SA01, 0), f16x2_bcast(SA01, 1)};
-                        const uint32_t caw[4] = {ca.x, ca.y, ca.z, ca.w};
+                }
+                if constexpr (AQ) {
+                    uint8_t* arow = ring_a + (i % SA) * kABytes + tg * 128;
+                    const uint32_t SA01 = e4m3x2_to_f16x2(asw & 0xFFFFu), SA23 = e4m3x2_to_f16x2(asw >> 16);
+                    const uint32_t Sa[4] = {f16x2_bcast(SA01, 0), f16x2_bcast(SA01, 1), f16x2_bcast(SA23, 0),
+                                            f16x2_bcast(SA23, 1)};
+                    const uint32_t caw[8] = {ca0.x, ca0.y, ca0.z, ca0.w, ca1.x, ca1.y, ca1.z, ca1.w};
 #pragma unroll
-                        for (int w = 0; w < 4; ++w) {
-                            uint32_t f[4];
-                            e2m1x8_to_f16x8(caw[w], f);
-                            const uint32_t S2 = Sa[w >> 1];
-                            const int chunk = ah * 4 + w;
-                            *reinterpret_cast<uint4*>(arow + ((chunk ^ (ra & 7)) << 4)) = make_uint4(
-                                hmul2_u32(f[0], S2), hmul2_u32(f[1], S2), hmul2_u32(f[2], S2), hmul2_u32(f[3], S2));
-                        }
+                    for (int w = 0; w < 8; ++w) {
+                        uint32_t f[4];
+                        e2m1x8_to_f16x8(caw[w], f);
+                        const uint32_t S2 = Sa[w >> 1];
+                        *reinterpret_cast<uint4*>(arow + ((w ^ (tg & 7)) << 4)) = make_uint4(
+                            hmul2_u32(f[0], S2), hmul2_u32(f[1], S2), hmul2_u32(f[2], S2), hmul2_u32(f[3], S2));
                     }
-                    fence_proxy_async();
-                    __syncwarp();
-                    if (lane == 0) {
-                        mbar_arrive(smem_u32(&bar_bfull[i % SB]));
-                        if constexpr (AQ) mbar_arrive(smem_u32(&bar_afull[i % SA]));
-                        mbar_arrive(smem_u32(&bar_rempty[sr]));
-                        if (release_scales) mbar_arrive(smem_u32(&bar_sempty[ss]));
-                    }
-                    release_scales = false;
+                }
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(smem_u32(&bar_bfull[i % SB]));
+                    if constexpr (AQ) mbar_arrive(smem_u32(&bar_afull[i % SA]));
+                    mbar_arrive(smem_u32(&bar_rempty[sr]));
+                    mbar_arrive(smem_u32(&bar_sempty[ss]));
                 }
             }
         }
