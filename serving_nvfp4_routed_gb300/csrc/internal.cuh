@@ -146,6 +146,9 @@ struct TcmArgs {
     int32_t* status;             // NVFP4_ERR_TIMEOUT if a bounded wait expired
 };
 bool make_tmap_rows_f16(CUtensorMap* map, const void* base, int rows, int K);
+// 2-D uint8 tensor map over [rows, inner_bytes] (row pitch = inner_bytes).
+bool encode_tmap_u8(CUtensorMap* map, const void* base, unsigned long long inner_bytes, unsigned long long rows,
+                    unsigned box_inner, unsigned box_rows, bool swizzle128);
 bool tcm_supported(int epi, int N, int K);
 // Fills tmap_wc / tmap_ws from a_codes / a_scales (rows = E * N, K = a->K).
 bool tcm_set_weights(TcmArgs* a, long long rows);
@@ -153,6 +156,14 @@ bool tcm_set_weights(TcmArgs* a, long long rows);
 bool tcm_set_act(TcmArgs* a, const uint8_t* codes, const uint8_t* scales, long long rows);
 // a_nvfp4: A rows are NVFP4 (tmap_ac / tmap_as, x_gs), else f16 (tmap_x, x_exp).
 void launch_tcm(int epi, int a_nvfp4, const TcmArgs& a, int max_units, cudaStream_t s);
+
+// ---- W4A4 prompt-shaped grouped GEMM on the block-scaled FP4 tensor cores ----
+// Same arguments as TcmArgs (NVFP4 rows: a_codes / x_gs); epi TCM_SWIGLU_Q or
+// TCM_COMBINE.  Needs K % 256 == 0 and N % 64 (SwiGLU) / N % 128 (combine).
+bool tcq_supported(int epi, int N, int K);
+// Encodes the tensor maps this kernel uses (rows_w = E * N, rows_x = R).
+bool tcq_set_maps(TcmArgs* a, const uint8_t* x_codes, const uint8_t* x_scales, long long rows_x, long long rows_w);
+void launch_tcq(int epi, const TcmArgs& a, int max_units, cudaStream_t s);
 
 size_t tc_smem_bytes(int nproj);
 void launch_tc_gemm(int outmode, int nproj, const TcArgs& a, int max_units, cudaStream_t s);

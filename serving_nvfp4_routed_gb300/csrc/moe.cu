@@ -183,8 +183,15 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
         g.hs_out = ws.hs;
         g.hq_gs = is2;
         g.status = d_status;
-        if (!tcm_set_weights(&g, (long long)E * F) || !tcm_set_act(&g, ws.xq, ws.xs, R)) return NVFP4_ERR_CUDA;
-        launch_tcm(TCM_SWIGLU_Q, 1, g, max_tiles * (F / 128), s);
+        // block-scaled FP4 MMA when the shapes allow it, else f16 MMA of dequantised tiles
+        const bool fp4 = tcq_supported(TCM_SWIGLU_Q, F, d) && tcq_supported(TCM_COMBINE, d, F);
+        if (fp4) {
+            if (!tcq_set_maps(&g, ws.xq, ws.xs, R, (long long)E * F)) return NVFP4_ERR_CUDA;
+            launch_tcq(TCM_SWIGLU_Q, g, max_tiles * (F / 64), s);
+        } else {
+            if (!tcm_set_weights(&g, (long long)E * F) || !tcm_set_act(&g, ws.xq, ws.xs, R)) return NVFP4_ERR_CUDA;
+            launch_tcm(TCM_SWIGLU_Q, 1, g, max_tiles * (F / 128), s);
+        }
         // down + weighted combine
         TcmArgs u = g;
         u.K = F;
@@ -197,8 +204,13 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
         u.acc_out = ws.acc;
         u.row_to_slot = ws.ra.row_to_slot;
         u.topk_w = ws.ra.w;
-        if (!tcm_set_weights(&u, (long long)E * d) || !tcm_set_act(&u, ws.hq, ws.hs, R)) return NVFP4_ERR_CUDA;
-        launch_tcm(TCM_COMBINE, 1, u, max_tiles * (d / 256), s);
+        if (fp4) {
+            if (!tcq_set_maps(&u, ws.hq, ws.hs, R, (long long)E * d)) return NVFP4_ERR_CUDA;
+            launch_tcq(TCM_COMBINE, u, max_tiles * (d / 128), s);
+        } else {
+            if (!tcm_set_weights(&u, (long long)E * d) || !tcm_set_act(&u, ws.hq, ws.hs, R)) return NVFP4_ERR_CUDA;
+            launch_tcm(TCM_COMBINE, 1, u, max_tiles * (d / 256), s);
+        }
         launch_acc_to_bf16(ws.acc, (size_t)T * d, out, s);
         return last_launch_status();
     }

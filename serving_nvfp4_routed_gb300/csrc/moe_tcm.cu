@@ -52,7 +52,6 @@ using namespace tc;
 constexpr int BM = 128;            // routed rows per unit (MMA M)
 constexpr int BN = 256;            // B rows per unit (MMA N)
 constexpr int BK = 64;             // K per stage (one 128-byte swizzle row of f16)
-constexpr int SA = 3;              // A (rows) ring depth
 constexpr int SR = 4;              // raw codes ring depth (k-stages)
 constexpr int SS = 2;              // raw scales ring depth (groups of four k-stages)
 constexpr int kABytes = BM * BK * 2;   // 16 KB
@@ -69,7 +68,8 @@ static_assert(SR % kGroups == 0, "each raw slot must belong to one producer grou
 // Ring geometry of each A kind (AQ = 1: NVFP4 rows).
 template <int AQ>
 struct Geo {
-    static constexpr int SB = AQ ? 3 : 4;  // f16 weight tiles
+    static constexpr int SA = AQ ? 3 : 4;  // A (row) tiles
+    static constexpr int SB = 3;           // f16 weight tiles
     static constexpr int SD0 = SA > SB ? SA : SB;
     // "stage done" barriers: at least every ring depth and the k-stage stride
     // between two waits of one producer group, so that parity waits stay in phase
@@ -96,7 +96,7 @@ __device__ __forceinline__ bool wait_done(const uint64_t* done, long long j, vol
 template <int EPI, int AQ>
 __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant__ TcmArgs a) {
     using G = Geo<AQ>;
-    constexpr int SB = G::SB, SD = G::SD, kRaw = G::kRaw, kSc = G::kSc;
+    constexpr int SA = G::SA, SB = G::SB, SD = G::SD, kRaw = G::kRaw, kSc = G::kSc;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* ring_a = smem;
@@ -511,6 +511,19 @@ void init_encode() {
             q == cudaDriverEntryPointSuccess)
             g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     });
+}
+
+bool encode_tmap_u8(CUtensorMap* map, const void* base, unsigned long long inner_bytes, unsigned long long rows,
+                    unsigned box_inner, unsigned box_rows, bool swizzle128) {
+    init_encode();
+    if (!g_encode || rows < 1 || inner_bytes % 16 != 0 || !aligned16(base)) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)inner_bytes, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)inner_bytes};
+    const cuuint32_t box[2] = {box_inner, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool make_tmap_rows_f16(CUtensorMap* map, const void* base, int rows, int K) {

@@ -1,0 +1,382 @@
+// moe_tcq.cu -- W4A4 prompt-shaped grouped GEMMs on the block-scaled FP4
+// tensor cores: tcgen05.mma kind::mxf4nvf4 with e4m3 scales per 16 values
+// (scale_vec::4X), both operands exactly as stored.
+//
+// W4A4 model card "GLM-5.3-Flash-NVFP4-W4A4-Experts", "Quantization
+// boundary" (routed experts quantise their inputs with a static per-expert
+// input_scale to the checkpoint's e2m1 + e4m3 format) and TensorFold issue
+// #308, "The checkpoint" (weights: e2m1 codes, e4m3 scale per 16 inputs,
+// fp32 weight_scale_2).  Each product of an e2m1 code pair and its two block
+// scales is exact; the MMA sums them in fp32 and the epilogue applies the
+// two fp32 tensor scales, as for the f16 kernels.
+//
+// Unit = (expert e, 128 B rows, 128 routed rows of e):
+//   D[j, n] = sum_k X[row0 + j, k] * B[n, k]
+//   SwiGLU: B rows 0..63 = gate rows f0.., 64..127 = up rows f0..;
+//   combine: B rows = 128 consecutive rows f0.. of the down projection.
+// One MMA has M = 128, N = 128, K = 64 and runs at the full FP4 rate.
+// A k-stage covers K = 256: the rows' codes (128 bytes per row, 128-byte
+// swizzle) and e4m3 scales (16 bytes per row) of A and B arrive by TMA into
+// one smem slot of a ring of S.  Four scale warps copy the slot's scales
+// into tensor memory where the MMA reads them:
+//   A scales of row m, MMA j: lane m, column 4j + m/32 of the slot's area;
+//   B scales of row n, MMA j: lanes n%32 (every lane quarter), column
+//   16 + 4j + n/32.
+// Each 32-bit TMEM word holds the four block scales of one row and one MMA
+// (bytes = blocks in k order), which is the stored order of the scales.
+// One thread issues the MMAs into two 128-column fp32 accumulators; four
+// epilogue warps read them (one routed row per thread).  mbarrier waits are
+// bounded (about 2 s) and report NVFP4_ERR_TIMEOUT.
+#include "common.cuh"
+#include "internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace nvfp4 {
+
+namespace {
+
+using namespace tc;
+
+constexpr int BM = 128, BN = 128;
+constexpr int KS = 256;                    // k per stage
+constexpr int S = 5;                       // stage ring depth
+constexpr int kA = BM * KS / 2;            // 16 KB codes
+constexpr int kB = BN * KS / 2;            // 16 KB codes
+constexpr int kSA = BM * KS / 16;          // 2 KB scales
+constexpr int kSB = BN * KS / 16;          // 2 KB scales
+constexpr int kStage = kA + kB + kSA + kSB;  // 36 KB
+static_assert(kStage % 1024 == 0, "stage slots keep 1024-byte alignment");
+constexpr int kMaxUnits = 512;
+constexpr int kTileCopy = kMaxExperts + 1;
+constexpr int kSmem = 1024 + S * kStage + kMaxUnits * 16 + kTileCopy * 4;
+constexpr int kWarps = 12;
+constexpr int kThreads = kWarps * 32;
+constexpr int kWarpMma = 0, kWarpTma = 1, kWarpEpi = 4, kWarpSf = 8;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSfCol0 = 2 * BN;       // scale areas after the two accumulators
+constexpr uint32_t kSfCols = 32;           // per stage: A 16 columns, B 16 columns
+static_assert(kSfCol0 + S * kSfCols <= kTmemCols, "tensor memory budget");
+
+// Instruction descriptor, kind::mxf4nvf4: A and B e2m1 (format 1, bits 7-9
+// and 10-12), K-major, N >> 3 in bits 17-22, scale type ue4m3 (bit 23 = 0),
+// M >> 4 in bits 24-28; scale-factor selectors 0.
+constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+
+__device__ __forceinline__ void mma_fp4(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t sfa, uint32_t sfb,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %5, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %6, [%3], [%4], p;\n}" ::"r"(
+            d),
+        "l"(adesc), "l"(bdesc), "r"(sfa), "r"(sfb), "r"(accumulate), "n"(kIdesc)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+__device__ __forceinline__ bool wait_done(const uint64_t* done, long long j, volatile int* abort_flag,
+                                          int32_t* status) {
+    if (j < 0) return true;
+    return mbar_wait(smem_u32(&done[j % S]), (uint32_t)((j / S) & 1), abort_flag, status);
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1) tcq_kernel(const __grid_constant__ TcmArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    int4* s_units = reinterpret_cast<int4*>(smem + S * kStage);  // {e, row0, row_end, f0}
+    int* s_tiles = reinterpret_cast<int*>(s_units + kMaxUnits);
+    __shared__ __align__(8) uint64_t bar_full[S], bar_sf[S], bar_done[S], bar_acc_full[2], bar_acc_empty[2];
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_abort;
+
+    grid_dep_wait();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_u32(&bar_full[s]), 1);
+            mbar_init(smem_u32(&bar_sf[s]), 4);
+            mbar_init(smem_u32(&bar_done[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&bar_acc_full[b]), 1);
+            mbar_init(smem_u32(&bar_acc_empty[b]), 4);
+        }
+        s_abort = 0;
+        mbar_fence_init();
+    }
+    if (warp == kWarpMma) tmem_alloc(smem_u32(&s_tmem), kTmemCols);
+
+    // ---- this CTA's work list ----
+    constexpr bool kPair = EPI == TCM_SWIGLU_Q;
+    constexpr int kSlice = kPair ? BN / 2 : BN;  // output features per unit
+    const int n_active = *a.n_active;
+    const int n_nt = a.N / kSlice;
+    for (int i = threadIdx.x; i <= n_active; i += kThreads) s_tiles[i] = a.tile_start[i];
+    __syncthreads();
+    const int total = s_tiles[n_active] * n_nt;
+    const int my_units = blockIdx.x < total ? (total - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    for (int t = threadIdx.x; t < my_units && t < kMaxUnits; t += kThreads) {
+        const int u = blockIdx.x + t * gridDim.x;
+        int lo = 0, hi = n_active;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (s_tiles[mid] * n_nt <= u) lo = mid; else hi = mid;
+        }
+        const int e = a.active[lo];
+        const int ntt = s_tiles[lo + 1] - s_tiles[lo];
+        const int local = u - s_tiles[lo] * n_nt;
+        s_units[t] = make_int4(e, a.offsets[e] + (local % ntt) * BM, a.offsets[e + 1], (local / ntt) * kSlice);
+    }
+    if (threadIdx.x == 0 && my_units > kMaxUnits) {
+        s_abort = 1;
+        if (a.status) atomicExch(a.status, (int)NVFP4_ERR_SHAPE);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    volatile int* abort_flag = &s_abort;
+    const int n_units = *abort_flag ? 0 : my_units;
+    const int nk = a.K / KS;
+
+    if (warp == kWarpMma) {
+        // ---------------- MMA issue (one thread) ----------------
+        if (lane == 0) {
+            long long i = 0;
+            for (int it = 0; it < n_units; ++it) {
+                const int acc = it & 1;
+                if (!mbar_wait(smem_u32(&bar_acc_empty[acc]), ((it >> 1) & 1) ^ 1, abort_flag, a.status)) break;
+                tc_fence_after();
+                const uint32_t d = tmem + acc * BN;
+                bool ok = true;
+                for (int kc = 0; kc < nk; ++kc, ++i) {
+                    const int s = (int)(i % S);
+                    const uint32_t par = (uint32_t)((i / S) & 1);
+                    if (!mbar_wait(smem_u32(&bar_full[s]), par, abort_flag, a.status) ||
+                        !mbar_wait(smem_u32(&bar_sf[s]), par, abort_flag, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + s * kStage);
+                    const uint64_t adesc = sdesc_sw128(sa), bdesc = sdesc_sw128(sa + kA);
+                    const uint32_t sf = tmem + kSfCol0 + s * kSfCols;
+#pragma unroll
+                    for (int j = 0; j < KS / 64; ++j)
+                        mma_fp4(d, adesc + 2 * j, bdesc + 2 * j, sf + 4 * j, sf + 16 + 4 * j, (kc | j) != 0);
+                    mma_commit(smem_u32(&bar_done[s]));
+                }
+                if (!ok) break;
+                mma_commit(smem_u32(&bar_acc_full[acc]));
+            }
+        }
+        __syncwarp();
+    } else if (warp == kWarpTma) {
+        // ---------------- operands by TMA (one thread) ----------------
+        if (lane == 0) {
+            long long i = 0;
+            bool ok = true;
+            for (int it = 0; it < n_units && ok; ++it) {
+                const int4 un = s_units[it];
+                const int y0 = un.x * a.N + un.w;
+                const int y1 = kPair ? y0 : y0 + BN / 2;
+                const void* mc1 = kPair ? (const void*)&a.tmap_wc[1] : (const void*)&a.tmap_wc[0];
+                const void* ms1 = kPair ? (const void*)&a.tmap_ws[1] : (const void*)&a.tmap_ws[0];
+                for (int kc = 0; kc < nk; ++kc, ++i) {
+                    if (!wait_done(bar_done, i - S, abort_flag, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    const int s = (int)(i % S);
+                    const uint32_t bar = smem_u32(&bar_full[s]);
+                    const uint32_t dst = smem_u32(smem + s * kStage);
+                    mbar_arrive_expect_tx(bar, kStage);
+                    tma_load_2d(dst, &a.tmap_ac, kc * (KS / 2), un.y, bar);
+                    tma_load_2d(dst + kA, &a.tmap_wc[0], kc * (KS / 2), y0, bar);
+                    tma_load_2d(dst + kA + kB / 2, mc1, kc * (KS / 2), y1, bar);
+                    tma_load_2d(dst + kA + kB, &a.tmap_as, kc * (KS / 16), un.y, bar);
+                    tma_load_2d(dst + kA + kB + kSA, &a.tmap_ws[0], kc * (KS / 16), y0, bar);
+                    tma_load_2d(dst + kA + kB + kSA + kSB / 2, ms1, kc * (KS / 16), y1, bar);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp >= kWarpSf) {
+        // ---------------- scales: smem -> tensor memory ----------------
+        const int q = warp - kWarpSf;  // lane quarter
+        const int m = q * 32 + lane;   // A row of this thread
+        const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
+        long long i = 0;
+        bool ok = true;
+        for (int it = 0; it < n_units && ok; ++it) {
+            for (int kc = 0; kc < nk; ++kc, ++i) {
+                const int s = (int)(i % S);
+                if (!mbar_wait(smem_u32(&bar_full[s]), (uint32_t)((i / S) & 1), abort_flag, a.status) ||
+                    !wait_done(bar_done, i - S, abort_flag, a.status)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t* sc = smem + s * kStage + kA + kB;
+                const uint4 va = *reinterpret_cast<const uint4*>(sc + m * 16);
+                uint4 vb[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) vb[c] = *reinterpret_cast<const uint4*>(sc + kSA + (c * 32 + lane) * 16);
+                // the slot is refilled by TMA (async proxy) once these MMAs are done
+                fence_proxy_async();
+                uint32_t ra[16], rb[16];
+                const uint32_t wa[4] = {va.x, va.y, va.z, va.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        ra[4 * j + c] = wa[j];  // column 4j + quarter holds this row's MMA-j scales
+                        const uint32_t wb[4] = {vb[c].x, vb[c].y, vb[c].z, vb[c].w};
+                        rb[4 * j + c] = wb[j];  // column 4j + c holds row 32c + lane
+                    }
+                }
+                const uint32_t col = kSfCol0 + s * kSfCols;
+                tmem_st16(tq + col, ra);
+                tmem_st16(tq + col + 16, rb);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bar_sf[s]));
+            }
+        }
+    } else if (warp >= kWarpEpi && warp < kWarpEpi + 4) {
+        // ---------------- epilogue: one routed row per thread ----------------
+        const int q = warp - kWarpEpi;
+        const int rr = q * 32 + lane;
+        for (int it = 0; it < n_units; ++it) {
+            const int4 un = s_units[it];
+            const int acc = it & 1;
+            const int row = un.y + rr;
+            const bool valid = row < un.z;
+            float wt = 0.0f;
+            size_t tok = 0;
+            if constexpr (EPI == TCM_COMBINE) {
+                if (valid) {
+                    const int slot = a.row_to_slot[row];
+                    tok = (size_t)(slot / a.top_k);
+                    wt = a.topk_w[slot];
+                }
+            }
+            const float rs = a.x_gs[un.x];
+            const float w0 = a.a_ws2[0][un.x], w1 = a.a_ws2[1][un.x];
+            if (!mbar_wait(smem_u32(&bar_acc_full[acc]), (it >> 1) & 1, abort_flag, a.status, 64)) break;
+            tc_fence_after();
+            const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + acc * BN;
+            if constexpr (EPI == TCM_SWIGLU_Q) {
+                // h in 16-feature blocks, requantised to NVFP4 under hq_gs[e]
+                const float gs2 = a.hq_gs[un.x];
+                for (int cb = 0; cb < BN / 32; ++cb) {
+                    uint32_t g[16], u[16];
+                    tmem_ld16(tb + cb * 16, g);
+                    tmem_ld16(tb + BN / 2 + cb * 16, u);
+                    tmem_ld_wait();
+                    if (valid) {
+                        float hv[16];
+                        float mx = 0.0f;
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) {
+                            const float G = round_bf16(__fmul_rn(__fmul_rn(__uint_as_float(g[t]), rs), w0));
+                            const float U = round_bf16(__fmul_rn(__fmul_rn(__uint_as_float(u[t]), rs), w1));
+                            hv[t] = round_bf16(G / (1.0f + expf(-G)) * U);
+                            mx = fmaxf(mx, fabsf(hv[t]));
+                        }
+                        uint32_t sbyte = 0, q0 = 0, q1 = 0;
+                        if (gs2 > 0.0f) {
+                            sbyte = f32_to_e4m3(__fdiv_rn(__fdiv_rn(mx, 6.0f), gs2));
+                            const float Sv = e4m3_to_f32(sbyte);
+                            if (Sv != 0.0f) {
+                                const float den = __fmul_rn(Sv, gs2);
+#pragma unroll
+                                for (int t = 0; t < 8; t += 2) {
+                                    q0 |= e2m1x2_byte(__fdiv_rn(hv[t], den), __fdiv_rn(hv[t + 1], den)) << (4 * t);
+                                    q1 |= e2m1x2_byte(__fdiv_rn(hv[8 + t], den), __fdiv_rn(hv[9 + t], den)) << (4 * t);
+                                }
+                            }
+                        }
+                        const int f = un.w + cb * 16;
+                        *reinterpret_cast<uint2*>(a.hq_out + (size_t)row * (a.N / 2) + f / 2) = make_uint2(q0, q1);
+                        a.hs_out[(size_t)row * (a.N / 16) + f / 16] = (uint8_t)sbyte;
+                    }
+                }
+            } else {
+                for (int cb = 0; cb < BN / 32; ++cb) {
+                    uint32_t r[32];
+                    tmem_ld32(tb + cb * 32, r);
+                    tmem_ld_wait();
+                    if (valid) {
+                        float4* dst = reinterpret_cast<float4*>(a.acc_out + tok * a.N + un.w + cb * 32);
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) {
+                            float y[4];
+#pragma unroll
+                            for (int t = 0; t < 4; ++t)
+                                y[t] = wt * __fmul_rn(__fmul_rn(__uint_as_float(r[4 * v + t]), rs), w0);
+                            atomicAdd(dst + v, make_float4(y[0], y[1], y[2], y[3]));
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bar_acc_empty[acc]));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kWarpMma) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+    grid_dep_launch();
+}
+
+template <int EPI>
+void launch_tcq_t(const TcmArgs& a, int max_units, cudaStream_t s, const char* name) {
+    auto kern = tcq_kernel<EPI>;
+    static bool init = false;
+    if (!init) {
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        init = true;
+    }
+    int grid = std::max(1, std::min(max_units, num_sms()));
+    grid = std::max(grid, (max_units + kMaxUnits - 1) / kMaxUnits);
+    NVFP4_LAUNCH(name, s, launch_pdl(kern, dim3(grid), dim3(kThreads), (size_t)kSmem, s, a));
+}
+
+}  // namespace
+
+bool tcq_supported(int epi, int N, int K) {
+    return K % KS == 0 && (epi == TCM_SWIGLU_Q ? N % (BN / 2) == 0 : N % BN == 0);
+}
+
+bool tcq_set_maps(TcmArgs* a, const uint8_t* x_codes, const uint8_t* x_scales, long long rows_x, long long rows_w) {
+    const unsigned long long K = (unsigned long long)a->K;
+    if (!encode_tmap_u8(&a->tmap_ac, x_codes, K / 2, rows_x, KS / 2, BM, true) ||
+        !encode_tmap_u8(&a->tmap_as, x_scales, K / 16, rows_x, KS / 16, BM, false))
+        return false;
+    for (int p = 0; p < 2; ++p)
+        if (!encode_tmap_u8(&a->tmap_wc[p], a->a_codes[p], K / 2, rows_w, KS / 2, BN / 2, true) ||
+            !encode_tmap_u8(&a->tmap_ws[p], a->a_scales[p], K / 16, rows_w, KS / 16, BN / 2, false))
+            return false;
+    return true;
+}
+
+void launch_tcq(int epi, const TcmArgs& a, int max_units, cudaStream_t s) {
+    if (epi == TCM_SWIGLU_Q) return launch_tcq_t<TCM_SWIGLU_Q>(a, max_units, s, "tcq_gateup_w4a4");
+    if (epi == TCM_COMBINE) return launch_tcq_t<TCM_COMBINE>(a, max_units, s, "tcq_down_w4a4");
+}
+
+}  // namespace nvfp4
