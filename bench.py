@@ -161,7 +161,11 @@ KERNEL_SOURCES = {
     "gemv": ("moe_gemv.cu", "common.cuh", "internal.cuh"),
     "tc": ("moe_tc.cu", "tc_ptx.cuh", "common.cuh", "internal.cuh"),
     "tcm": ("moe_tcm.cu", "tc_ptx.cuh", "common.cuh", "internal.cuh"),
+    "tcq": ("moe_tcq.cu", "tc_ptx.cuh", "common.cuh", "internal.cuh"),
 }
+# nominal dense FP4 : BF16 tensor rate (13.5 : 2.25 PFLOP/s); the FP4 peak is
+# the measured bf16 peak times this ratio
+FP4_BF16_RATIO = 6.0
 
 
 def kernel_source_hash(kernel: str):
@@ -442,17 +446,19 @@ def run_ours(args):
     dom = max(kernels, key=lambda k: kernels[k]["ms_per_launch"] * kernels[k]["launches"]) if kernels else "?"
     s_ = layer.shape
     dom_ms = kernels.get(dom, {"ms_per_launch": float("nan")})["ms_per_launch"]
-    if dom.startswith(("tc_", "tcm_")):
-        # tensor-bound: f16 MMA (the bf16/f16 dense rate), flops of one launch
+    if dom.startswith(("tc_", "tcm_", "tcq_")):
+        # tensor-bound, flops of one launch: f16 MMA (the bf16/f16 dense rate) or
+        # block-scaled FP4 MMA (tcq_*, against the FP4 dense rate)
         nproj = 2 if "gateup" in dom else 1
         rows = R if layer.kind != "dense" else s_.T
-        if layer.kind == "dense":
-            dom_flops = 2.0 * rows * s_.d * s_.F * nproj
-        else:
-            dom_flops = 2.0 * rows * s_.d * s_.F * nproj
+        dom_flops = 2.0 * rows * s_.d * s_.F * nproj
         achieved = dom_flops / (dom_ms / 1e3) / 1e12
-        roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": bf16, "unit": "TFLOP/s",
-                "frac": achieved / bf16, "peak_kind": f"{peak_kind} bf16 dense (f16 runs at the same rate), burst",
+        fp4 = dom.startswith("tcq_")
+        peak = bf16 * FP4_BF16_RATIO if fp4 else bf16
+        kind = (f"{peak_kind} bf16 dense x nominal FP4/BF16 ratio {FP4_BF16_RATIO:g}, burst" if fp4
+                else f"{peak_kind} bf16 dense (f16 runs at the same rate), burst")
+        roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "peak_kind": kind,
                 "traffic": recorded_traffic(dom, args.workload), "algorithmic_flops_per_launch": dom_flops}
     else:
         if dom.startswith("gemv_down"):
@@ -472,8 +478,10 @@ def run_ours(args):
         "metric": "MoE-layer tokens/s (decode-shaped routed NVFP4 layer)",
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "e2m1+e4m3 weights, f16 mma, f32 accumulate" if layer.mode == "w4a16"
-                 else "e2m1+e4m3 weights and activations, f16 mma, f32 accumulate",
+        "dtype": ("e2m1+e4m3 weights, f16 mma, f32 accumulate" if layer.mode == "w4a16"
+                  else "e2m1+e4m3 weights and activations, block-scaled fp4 mma, f32 accumulate"
+                  if any(k.startswith("tcq_") for k in kernels)
+                  else "e2m1+e4m3 weights and activations, f16 mma, f32 accumulate"),
         "data": "synthetic (seeded N(0,1) x and logits, N(0,0.02) bf16 weights quantised by the library)",
         "config": workload_config(layer, flush_mb),
         "roofline": roof,

@@ -360,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant_
 #pragma unroll
                                 for (int t = 0; t < 4; ++t)
                                     y[t] = wt * __fmul_rn(__fmul_rn(__uint_as_float(r[4 * v + t]), rs), w0);
-                                atomicAdd(dst + v, make_float4(y[0], y[1], y[2], y[3]));
+                                red_add_v4(reinterpret_cast<float*>(dst + v), y[0], y[1], y[2], y[3]);
                             }
                         } else {
                             uint32_t packed[16];

@@ -17,15 +17,16 @@
 // One MMA has M = 128, N = 128, K = 64 and runs at the full FP4 rate.
 // A k-stage covers K = 256: the rows' codes (128 bytes per row, 128-byte
 // swizzle) and e4m3 scales (16 bytes per row) of A and B arrive by TMA into
-// one smem slot of a ring of S.  Four scale warps copy the slot's scales
-// into tensor memory where the MMA reads them:
+// one smem slot of a ring of S.  Two groups of four scale warps (alternate
+// k-stages) copy the slot's scales into tensor memory where the MMA reads
+// them:
 //   A scales of row m, MMA j: lane m, column 4j + m/32 of the slot's area;
 //   B scales of row n, MMA j: lanes n%32 (every lane quarter), column
 //   16 + 4j + n/32.
 // Each 32-bit TMEM word holds the four block scales of one row and one MMA
 // (bytes = blocks in k order), which is the stored order of the scales.
-// One thread issues the MMAs into two 128-column fp32 accumulators; four
-// epilogue warps read them (one routed row per thread).  mbarrier waits are
+// One thread issues the MMAs into two 128-column fp32 accumulators; eight
+// epilogue warps read them (one routed row and half the columns per thread).  mbarrier waits are
 // bounded (about 2 s) and report NVFP4_ERR_TIMEOUT.
 #include "common.cuh"
 #include "internal.cuh"
@@ -39,19 +40,20 @@ using namespace tc;
 
 constexpr int BM = 128, BN = 128;
 constexpr int KS = 256;                    // k per stage
-constexpr int S = 5;                       // stage ring depth
+constexpr int S = 6;                       // stage ring depth (even: each slot has one scale group)
 constexpr int kA = BM * KS / 2;            // 16 KB codes
 constexpr int kB = BN * KS / 2;            // 16 KB codes
 constexpr int kSA = BM * KS / 16;          // 2 KB scales
 constexpr int kSB = BN * KS / 16;          // 2 KB scales
 constexpr int kStage = kA + kB + kSA + kSB;  // 36 KB
 static_assert(kStage % 1024 == 0, "stage slots keep 1024-byte alignment");
-constexpr int kMaxUnits = 512;
+constexpr int kMaxUnits = 320;
 constexpr int kTileCopy = kMaxExperts + 1;
 constexpr int kSmem = 1024 + S * kStage + kMaxUnits * 16 + kTileCopy * 4;
-constexpr int kWarps = 12;
+constexpr int kWarps = 20;
 constexpr int kThreads = kWarps * 32;
-constexpr int kWarpMma = 0, kWarpTma = 1, kWarpEpi = 4, kWarpSf = 8;
+constexpr int kWarpMma = 0, kWarpTma = 1, kWarpEpi = 4, kWarpSf = 8, kSfGroups = 2, kWarpEpi2 = 16;
+static_assert(S % kSfGroups == 0, "each stage slot belongs to one scale group");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol0 = 2 * BN;       // scale areas after the two accumulators
 constexpr uint32_t kSfCols = 32;           // per stage: A 16 columns, B 16 columns
@@ -107,7 +109,7 @@ __global__ void __launch_bounds__(kThreads, 1) tcq_kernel(const __grid_constant_
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&bar_acc_full[b]), 1);
-            mbar_init(smem_u32(&bar_acc_empty[b]), 4);
+            mbar_init(smem_u32(&bar_acc_empty[b]), 8);
         }
         s_abort = 0;
         mbar_fence_init();
@@ -209,15 +211,17 @@ __global__ void __launch_bounds__(kThreads, 1) tcq_kernel(const __grid_constant_
             }
         }
         __syncwarp();
-    } else if (warp >= kWarpSf) {
+    } else if (warp >= kWarpSf && warp < kWarpEpi2) {
         // ---------------- scales: smem -> tensor memory ----------------
-        const int q = warp - kWarpSf;  // lane quarter
-        const int m = q * 32 + lane;   // A row of this thread
+        const int q = (warp - kWarpSf) & 3;  // lane quarter
+        const int grp = (warp - kWarpSf) >> 2;  // takes the k-stages i = grp mod kSfGroups
+        const int m = q * 32 + lane;           // A row of this thread
         const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
         long long i = 0;
         bool ok = true;
         for (int it = 0; it < n_units && ok; ++it) {
             for (int kc = 0; kc < nk; ++kc, ++i) {
+                if ((int)(i % kSfGroups) != grp) continue;
                 const int s = (int)(i % S);
                 if (!mbar_wait(smem_u32(&bar_full[s]), (uint32_t)((i / S) & 1), abort_flag, a.status) ||
                     !wait_done(bar_done, i - S, abort_flag, a.status)) {
@@ -251,9 +255,10 @@ __global__ void __launch_bounds__(kThreads, 1) tcq_kernel(const __grid_constant_
                 if (lane == 0) mbar_arrive(smem_u32(&bar_sf[s]));
             }
         }
-    } else if (warp >= kWarpEpi && warp < kWarpEpi + 4) {
+    } else if ((warp >= kWarpEpi && warp < kWarpEpi + 4) || warp >= kWarpEpi2) {
         // ---------------- epilogue: one routed row per thread ----------------
-        const int q = warp - kWarpEpi;
+        const int q = warp & 3;                // TMEM lane quarter
+        const int half = warp >= kWarpEpi2;    // which half of the unit's columns
         const int rr = q * 32 + lane;
         for (int it = 0; it < n_units; ++it) {
             const int4 un = s_units[it];
@@ -277,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1) tcq_kernel(const __grid_constant_
             if constexpr (EPI == TCM_SWIGLU_Q) {
                 // h in 16-feature blocks, requantised to NVFP4 under hq_gs[e]
                 const float gs2 = a.hq_gs[un.x];
-                for (int cb = 0; cb < BN / 32; ++cb) {
+                for (int cb = 2 * half; cb < 2 * half + 2; ++cb) {
                     uint32_t g[16], u[16];
                     tmem_ld16(tb + cb * 16, g);
                     tmem_ld16(tb + BN / 2 + cb * 16, u);
@@ -311,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1) tcq_kernel(const __grid_constant_
                     }
                 }
             } else {
-                for (int cb = 0; cb < BN / 32; ++cb) {
+                for (int cb = 2 * half; cb < 2 * half + 2; ++cb) {
                     uint32_t r[32];
                     tmem_ld32(tb + cb * 32, r);
                     tmem_ld_wait();
@@ -323,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1) tcq_kernel(const __grid_constant_
 #pragma unroll
                             for (int t = 0; t < 4; ++t)
                                 y[t] = wt * __fmul_rn(__fmul_rn(__uint_as_float(r[4 * v + t]), rs), w0);
-                            atomicAdd(dst + v, make_float4(y[0], y[1], y[2], y[3]));
+                            red_add_v4(reinterpret_cast<float*>(dst + v), y[0], y[1], y[2], y[3]);
                         }
                     }
                 }

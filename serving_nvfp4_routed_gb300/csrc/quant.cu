@@ -117,55 +117,54 @@ __global__ void quantize_weights_kernel(const uint16_t* __restrict__ w, size_t n
 }
 
 // Output row r quantises source row src(r) with the input scale of the
-// expert whose row range holds r.
+// expert whose row range holds r.  One CTA per row (grid-stride): the row's
+// expert and source are found once, each thread takes whole 16-value blocks
+// (coalesced 32-byte loads, 8-byte code and 1-byte scale stores).
 __global__ void quantize_act_kernel(const uint16_t* __restrict__ x, int M, int K,
                                     const int32_t* __restrict__ row_to_slot, int top_k,
                                     const float* __restrict__ input_scale,
                                     const int32_t* __restrict__ offsets, int E,
                                     uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
     grid_dep_wait();
-    const int halves_per_row = K / 8;
-    const size_t total = (size_t)M * halves_per_row;
-    for (size_t base = blockIdx.x * (size_t)blockDim.x + (threadIdx.x & ~31u); base < total;
-         base += (size_t)gridDim.x * blockDim.x) {
-        const size_t i = base + (threadIdx.x & 31);
-        const bool live = i < total;
-        const size_t ii = live ? i : 0;
-        const int r = (int)(ii / halves_per_row);
-        const int part = (int)(ii % halves_per_row);
+    const int nb = K / 16;
+    for (int r = blockIdx.x; r < M; r += gridDim.x) {
         const int src = row_to_slot ? row_to_slot[r] / top_k : r;
         float gs;
         if (offsets) {
             int lo = 0, hi = E;  // find e with offsets[e] <= r < offsets[e+1]
             while (hi - lo > 1) {
-                int mid = (lo + hi) >> 1;
+                const int mid = (lo + hi) >> 1;
                 if (offsets[mid] <= r) lo = mid; else hi = mid;
             }
             gs = input_scale[lo];
         } else {
             gs = input_scale[0];
         }
-        float v[8], m;
-        load_bf16x8(x + (size_t)src * K + (size_t)part * 8, v, m);
-        float bam = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-        uint32_t c, s;
-        quant_half_block(v, bam, gs, c, s);
-        if (live) {
-            reinterpret_cast<uint32_t*>(codes)[ii] = c;
-            if ((ii & 1) == 0) scales[ii / 2] = (uint8_t)s;
+        const uint16_t* xr = x + (size_t)src * K;
+        for (int b = threadIdx.x; b < nb; b += blockDim.x) {
+            float v0[8], v1[8], m0, m1;
+            load_bf16x8(xr + (size_t)b * 16, v0, m0);
+            load_bf16x8(xr + (size_t)b * 16 + 8, v1, m1);
+            const float bam = fmaxf(m0, m1);
+            uint32_t c0, c1, s0, s1;
+            quant_half_block(v0, bam, gs, c0, s0);
+            quant_half_block(v1, bam, gs, c1, s1);
+            *reinterpret_cast<uint2*>(codes + (size_t)r * (K / 2) + (size_t)b * 8) = make_uint2(c0, c1);
+            scales[(size_t)r * nb + b] = (uint8_t)s0;
         }
     }
+    grid_dep_launch();
 }
 
 void launch_quantize_act(const uint16_t* x, int M, int K, const int32_t* row_to_slot, int top_k,
                          const float* input_scale, const int32_t* offsets, int E, uint8_t* codes,
                          uint8_t* scales, cudaStream_t s) {
-    size_t total = (size_t)M * (K / 8);
-    if (total == 0) return;
-    int grid = (int)std::min<size_t>((total + 255) / 256, (size_t)num_sms() * 16);
+    if ((size_t)M * K == 0) return;
+    const int threads = std::min(256, std::max(32, (K / 16 + 31) / 32 * 32));
+    const int grid = std::min(M, num_sms() * (2048 / threads));
     NVFP4_LAUNCH("quantize_act", s,
-                 launch_pdl(quantize_act_kernel, dim3(grid), dim3(256), 0, s, x, M, K, row_to_slot, top_k, input_scale,
-                            offsets, E, codes, scales));
+                 launch_pdl(quantize_act_kernel, dim3(grid), dim3(threads), 0, s, x, M, K, row_to_slot, top_k,
+                            input_scale, offsets, E, codes, scales));
 }
 
 }  // namespace nvfp4
