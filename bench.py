@@ -146,6 +146,9 @@ WORKLOADS = {
     "skew_w4a4": (synth.SKEW, "w4a4", "zipf", 0.0),
     "skew_masked_w4a16": (synth.SKEW, "w4a16", "zipf_masked", 0.0),
     "dense": (None, "w4a16", "dense", 0.05),
+    # small prompt-shaped cases for full-metric ncu captures (not bench lines)
+    "prompt_small_w4a16": (synth.PROMPT_SMALL, "w4a16", "normal", 0.05),
+    "prompt_small_w4a4": (synth.PROMPT_SMALL, "w4a4", "normal", 0.05),
 }
 
 

@@ -52,6 +52,7 @@ struct GemvArgs {
     int K, N, top_k;
     int nproj;                      // 2: gate+up (SwiGLU epilogue), 1: single projection
     int ksplit;                     // warps of a CTA splitting K (1, 2, 4 or 8)
+    int fb_group;                   // feature blocks per work item (they share the staged rows)
     const int32_t* offsets;         // [E+1]
     const int32_t* active;          // [E]
     const int32_t* n_active;        // [1]
@@ -86,6 +87,7 @@ struct GemvArgs {
 
 // ksplit chosen from the expected number of work items
 int gemv_pick_ksplit(int expected_tiles, int N, int nproj);
+int gemv_pick_group(int expected_tiles, int N, int ksplit, int nproj);
 size_t gemv_smem_bytes(int K);
 bool gemv_supported_k(int K);
 void launch_gemv(int bmode, int outmode, const GemvArgs& a, int max_work, cudaStream_t s);

@@ -305,6 +305,7 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
     a.N = F;
     a.nproj = 2;
     a.ksplit = gemv_pick_ksplit(tiles, F, 2);
+    a.fb_group = gemv_pick_group(tiles, F, a.ksplit, 2);
     a.a_codes[0] = w->gate.codes;  a.a_scales[0] = w->gate.scales;  a.a_ws2[0] = w->gate.weight_scale_2;
     a.a_codes[1] = w->up.codes;    a.a_scales[1] = w->up.scales;    a.a_ws2[1] = w->up.weight_scale_2;
     a.work_counter = ws.clear + 0;
@@ -330,12 +331,16 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
     b.N = d;
     b.nproj = 1;
     b.ksplit = gemv_pick_ksplit(tiles, d, 1);
+    b.fb_group = gemv_pick_group(tiles, d, b.ksplit, 1);
     b.a_codes[0] = w->down.codes;  b.a_scales[0] = w->down.scales;  b.a_ws2[0] = w->down.weight_scale_2;
     b.a_codes[1] = w->down.codes;  b.a_scales[1] = w->down.scales;  b.a_ws2[1] = w->down.weight_scale_2;
     b.work_counter = ws.clear + 1;
     b.acc_out = ws.acc;
     b.tok_done = ws.clear + kCounters;
-    b.done_target = top_k * (d / (16 * (8 / b.ksplit)));
+    {   // contributions per token: one per (slot, work item) over the d features
+        const int n_fb = d / (16 * (8 / b.ksplit));
+        b.done_target = top_k * ((n_fb + b.fb_group - 1) / b.fb_group);
+    }
     b.out_bf16 = out;
     if (mode == 0) {
         b.b_bf16 = ws.h;
@@ -525,12 +530,14 @@ extern "C" nvfp4_status nvfp4_linear(const uint16_t* x, int M, int K, const nvfp
     if (w_up) {
         a.nproj = 2;
         a.ksplit = gemv_pick_ksplit(tiles, N, 2);
+        a.fb_group = gemv_pick_group(tiles, N, a.ksplit, 2);
         a.a_codes[1] = w_up->codes;  a.a_scales[1] = w_up->scales;  a.a_ws2[1] = w_up->weight_scale_2;
         a.h_out = out;
         launch_gemv(B_BF16, OUT_H, a, max_work, stream);
     } else {
         a.nproj = 1;
         a.ksplit = gemv_pick_ksplit(tiles, N, 1);
+        a.fb_group = gemv_pick_group(tiles, N, a.ksplit, 1);
         a.y_out = out;
         launch_gemv(B_BF16, OUT_BF16, a, max_work, stream);
     }

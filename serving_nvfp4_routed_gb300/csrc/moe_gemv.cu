@@ -99,7 +99,7 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 
 struct Item {
-    int e, row0, nrows, fb;
+    int e, row0, nrows, fb, fb_end;  // feature blocks [fb, fb_end) share the staged rows
 };
 
 template <int CK, int BMODE, int OUTMODE, int NPROJ>
@@ -130,14 +130,17 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
     const int total_tiles = a.tile_start[n_active];
     const int FB = 16 * WF;
     const int n_fb = a.N / FB;
-    const int total = total_tiles * n_fb;
+    const int G = a.fb_group > 0 ? a.fb_group : 1;  // feature blocks per work item
+    const int n_grp = (n_fb + G - 1) / G;
+    const int total = total_tiles * n_grp;
     const int nch = a.K / CK;
     const int Kg = a.K / 8;
     const size_t K2 = (size_t)a.K / 2, K16 = (size_t)a.K / 16;
 
     auto decode = [&](int item, Item& it) {
-        it.fb = item % n_fb;
-        const int tile = item / n_fb;
+        it.fb = (item % n_grp) * G;
+        it.fb_end = min(n_fb, it.fb + G);
+        const int tile = item / n_grp;
         int lo = 0, hi = n_active;  // largest ai with tile_start[ai] <= tile
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
@@ -233,171 +236,189 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
         }
         __syncthreads();
         if (tid == 0) s_next = atomicAdd(a.work_counter, 1);  // next item, fetched while computing
-
-        // ---- stream this warp's 16 features over its share of K
-        const int n0 = cur.fb * FB + wf * 16;
-        float acc[NPROJ][4];
-#pragma unroll
-        for (int p = 0; p < NPROJ; ++p)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) acc[p][i] = 0.0f;
-        const uint4* brow_s = Bs + (size_t)g * Kg;
-        for (int chb = ks; chb < nch; chb += U * KSPL) {
-            if (chb != ks) load_batch(cur, chb);
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int ch = chb + u * KSPL;
-                if (ch >= nch) break;
-                const int qb = (ch * CK + c * C::TS) / 8;
-#pragma unroll
-                for (int jj = 0; jj < C::KS; jj += 2) {
-                    const uint4 bq = brow_s[bsw<CK>(qb + jj / 2, g)];
-                    const uint32_t b0[2] = {bq.x, bq.y};
-                    const uint32_t b1[2] = {bq.z, bq.w};
-#pragma unroll
-                    for (int p = 0; p < NPROJ; ++p) {
-                        uint32_t r0[4], r1[4];
-                        deq_word(acw[u][p][0][jj >> 1], asw[u][p][0], jj, r0);
-                        deq_word(acw[u][p][1][jj >> 1], asw[u][p][1], jj, r1);
-                        const uint32_t af0[4] = {r0[0], r1[0], r0[1], r1[1]};
-                        const uint32_t af1[4] = {r0[2], r1[2], r0[3], r1[3]};
-                        mma_16816(acc[p], af0, b0);
-                        mma_16816(acc[p], af1, b1);
-                    }
-                }
-            }
-        }
-        const bool owner = ks == 0;
-        if (KSPL > 1 && !owner) {
+        int nitem = total;
+        Item nxt{};
+        for (;;) {  // the feature blocks of this item, all on the staged rows
+            // ---- stream this warp's 16 features over its share of K
+            const int n0 = cur.fb * FB + wf * 16;
+            float acc[NPROJ][4];
 #pragma unroll
             for (int p = 0; p < NPROJ; ++p)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) s_red[wf * (KSPL - 1) + ks - 1][p * 4 + i][lane] = acc[p][i];
-        }
-        __syncthreads();
-
-        // ---- the next item's first weight batch goes out before this item's epilogue
-        const int nitem = s_next;
-        Item nxt{};
-        if (nitem < total) {
-            decode(nitem, nxt);
-            load_batch(nxt, ks);
-        }
-        if (KSPL > 1 && owner) {
-            for (int k2 = 0; k2 < KSPL - 1; ++k2)
+                for (int i = 0; i < 4; ++i) acc[p][i] = 0.0f;
+            const uint4* brow_s = Bs + (size_t)g * Kg;
+            for (int chb = ks; chb < nch; chb += U * KSPL) {
+                if (chb != ks) load_batch(cur, chb);
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int ch = chb + u * KSPL;
+                    if (ch >= nch) break;
+                    const int qb = (ch * CK + c * C::TS) / 8;
+#pragma unroll
+                    for (int jj = 0; jj < C::KS; jj += 2) {
+                        const uint4 bq = brow_s[bsw<CK>(qb + jj / 2, g)];
+                        const uint32_t b0[2] = {bq.x, bq.y};
+                        const uint32_t b1[2] = {bq.z, bq.w};
+#pragma unroll
+                        for (int p = 0; p < NPROJ; ++p) {
+                            uint32_t r0[4], r1[4];
+                            deq_word(acw[u][p][0][jj >> 1], asw[u][p][0], jj, r0);
+                            deq_word(acw[u][p][1][jj >> 1], asw[u][p][1], jj, r1);
+                            const uint32_t af0[4] = {r0[0], r1[0], r0[1], r1[1]};
+                            const uint32_t af1[4] = {r0[2], r1[2], r0[3], r1[3]};
+                            mma_16816(acc[p], af0, b0);
+                            mma_16816(acc[p], af1, b1);
+                        }
+                    }
+                }
+            }
+            const bool owner = ks == 0;
+            if (KSPL > 1 && !owner) {
 #pragma unroll
                 for (int p = 0; p < NPROJ; ++p)
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) acc[p][i] += s_red[wf * (KSPL - 1) + k2][p * 4 + i][lane];
-        }
+                    for (int i = 0; i < 4; ++i) s_red[wf * (KSPL - 1) + ks - 1][p * 4 + i][lane] = acc[p][i];
+            }
+            __syncthreads();
 
-        // ---- epilogue: column cc of this lane is permuted row row0 + 2c + cc
-        const int e = cur.e, row0 = cur.row0, nrows = cur.nrows;
-        if (owner) {
+
+            // ---- the next feature block's (or the next item's) first weight
+            // batch goes out before this block's epilogue
+            // (gate/up items are never grouped: known at compile time)
+            const bool last = NPROJ == 2 || cur.fb + 1 >= cur.fb_end;
+            Item following = cur;
+            if (!last) {
+                following.fb = cur.fb + 1;
+                load_batch(following, ks);
+            } else {
+                nitem = s_next;
+                if (nitem < total) {
+                    decode(nitem, nxt);
+                    load_batch(nxt, ks);
+                }
+            }
+            if (KSPL > 1 && owner) {
+                for (int k2 = 0; k2 < KSPL - 1; ++k2)
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                const int col = 2 * c + cc;
-                const bool valid = col < nrows;
-                const int r = row0 + (valid ? col : 0);
-                float rs;  // takes the accumulator to x W^T (without the tensor scale)
-                if constexpr (BMODE == B_BF16) rs = valid ? s_rowscale[col] : 0.0f;
-                else rs = a.b_gs[e];
-                if constexpr (OUTMODE == OUT_H || OUTMODE == OUT_HQ) {
-                    const float wg = a.a_ws2[0][e], wu = a.a_ws2[NPROJ - 1][e];
-                    float hv[2];
+                    for (int p = 0; p < NPROJ; ++p)
 #pragma unroll
-                    for (int hf = 0; hf < 2; ++hf) {
-                        const float G = round_bf16(__fmul_rn(__fmul_rn(acc[0][2 * hf + cc], rs), wg));
-                        const float Uv = round_bf16(__fmul_rn(__fmul_rn(acc[NPROJ - 1][2 * hf + cc], rs), wu));
-                        const float sg = G / (1.0f + expf(-G));
-                        hv[hf] = valid ? round_bf16(sg * Uv) : 0.0f;
-                    }
-                    if constexpr (OUTMODE == OUT_H) {
-                        if (valid) {
+                        for (int i = 0; i < 4; ++i) acc[p][i] += s_red[wf * (KSPL - 1) + k2][p * 4 + i][lane];
+            }
+
+            // ---- epilogue: column cc of this lane is permuted row row0 + 2c + cc
+            const int e = cur.e, row0 = cur.row0, nrows = cur.nrows;
+            if (owner) {
 #pragma unroll
-                            for (int hf = 0; hf < 2; ++hf)
-                                a.h_out[(size_t)r * a.N + n0 + g + 8 * hf] = f32_to_bf16_bits(hv[hf]);
-                        }
-                    } else {
-                        // NVFP4 requantisation of h: this warp's 16 features are one block
-                        const float gs2 = a.hq_gs[e];
-                        float m = fmaxf(fabsf(hv[0]), fabsf(hv[1]));
-                        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-                        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
-                        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-                        uint32_t sbyte = 0, q[2] = {0u, 0u};
-                        if (gs2 > 0.0f) {
-                            const float sf = __fdiv_rn(__fdiv_rn(m, 6.0f), gs2);
-                            sbyte = f32_to_e4m3(sf);
-                            const float S = e4m3_to_f32(sbyte);
-                            if (S != 0.0f) {
-                                const float den = __fmul_rn(S, gs2);
-                                const uint32_t byte = e2m1x2_byte(__fdiv_rn(hv[0], den), __fdiv_rn(hv[1], den));
-                                q[0] = byte & 0xFu;
-                                q[1] = byte >> 4;
-                            }
-                        }
-                        const uint32_t p0 = __shfl_down_sync(0xffffffffu, q[0], 4);
-                        const uint32_t p1 = __shfl_down_sync(0xffffffffu, q[1], 4);
-                        if (valid && (g & 1) == 0) {
-                            uint8_t* dst = a.hq_out + (size_t)r * (a.N / 2) + n0 / 2;
-                            dst[g / 2] = (uint8_t)(q[0] | (p0 << 4));
-                            dst[g / 2 + 4] = (uint8_t)(q[1] | (p1 << 4));
-                        }
-                        if (valid && g == 0) a.hs_out[(size_t)r * (a.N / 16) + n0 / 16] = (uint8_t)sbyte;
-                    }
-                } else if constexpr (OUTMODE == OUT_COMBINE) {
-                    if (valid) {
-                        const int slot = a.row_to_slot[r];
-                        const int t = slot / a.top_k;
-                        const float wt = a.topk_w[slot];
-                        const float ws = a.a_ws2[0][e];
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int col = 2 * c + cc;
+                    const bool valid = col < nrows;
+                    const int r = row0 + (valid ? col : 0);
+                    float rs;  // takes the accumulator to x W^T (without the tensor scale)
+                    if constexpr (BMODE == B_BF16) rs = valid ? s_rowscale[col] : 0.0f;
+                    else rs = a.b_gs[e];
+                    if constexpr (OUTMODE == OUT_H || OUTMODE == OUT_HQ) {
+                        const float wg = a.a_ws2[0][e], wu = a.a_ws2[NPROJ - 1][e];
+                        float hv[2];
 #pragma unroll
                         for (int hf = 0; hf < 2; ++hf) {
-                            const float y = __fmul_rn(__fmul_rn(acc[0][2 * hf + cc], rs), ws);
-                            atomicAdd(a.acc_out + (size_t)t * a.N + n0 + g + 8 * hf, wt * y);
+                            const float G = round_bf16(__fmul_rn(__fmul_rn(acc[0][2 * hf + cc], rs), wg));
+                            const float Uv = round_bf16(__fmul_rn(__fmul_rn(acc[NPROJ - 1][2 * hf + cc], rs), wu));
+                            const float sg = G / (1.0f + expf(-G));
+                            hv[hf] = valid ? round_bf16(sg * Uv) : 0.0f;
+                        }
+                        if constexpr (OUTMODE == OUT_H) {
+                            if (valid) {
+#pragma unroll
+                                for (int hf = 0; hf < 2; ++hf)
+                                    a.h_out[(size_t)r * a.N + n0 + g + 8 * hf] = f32_to_bf16_bits(hv[hf]);
+                            }
+                        } else {
+                            // NVFP4 requantisation of h: this warp's 16 features are one block
+                            const float gs2 = a.hq_gs[e];
+                            float m = fmaxf(fabsf(hv[0]), fabsf(hv[1]));
+                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+                            uint32_t sbyte = 0, q[2] = {0u, 0u};
+                            if (gs2 > 0.0f) {
+                                const float sf = __fdiv_rn(__fdiv_rn(m, 6.0f), gs2);
+                                sbyte = f32_to_e4m3(sf);
+                                const float S = e4m3_to_f32(sbyte);
+                                if (S != 0.0f) {
+                                    const float den = __fmul_rn(S, gs2);
+                                    const uint32_t byte = e2m1x2_byte(__fdiv_rn(hv[0], den), __fdiv_rn(hv[1], den));
+                                    q[0] = byte & 0xFu;
+                                    q[1] = byte >> 4;
+                                }
+                            }
+                            const uint32_t p0 = __shfl_down_sync(0xffffffffu, q[0], 4);
+                            const uint32_t p1 = __shfl_down_sync(0xffffffffu, q[1], 4);
+                            if (valid && (g & 1) == 0) {
+                                uint8_t* dst = a.hq_out + (size_t)r * (a.N / 2) + n0 / 2;
+                                dst[g / 2] = (uint8_t)(q[0] | (p0 << 4));
+                                dst[g / 2 + 4] = (uint8_t)(q[1] | (p1 << 4));
+                            }
+                            if (valid && g == 0) a.hs_out[(size_t)r * (a.N / 16) + n0 / 16] = (uint8_t)sbyte;
+                        }
+                    } else if constexpr (OUTMODE == OUT_COMBINE) {
+                        if (valid) {
+                            const int slot = a.row_to_slot[r];
+                            const int t = slot / a.top_k;
+                            const float wt = a.topk_w[slot];
+                            const float ws = a.a_ws2[0][e];
+#pragma unroll
+                            for (int hf = 0; hf < 2; ++hf) {
+                                const float y = __fmul_rn(__fmul_rn(acc[0][2 * hf + cc], rs), ws);
+                                atomicAdd(a.acc_out + (size_t)t * a.N + n0 + g + 8 * hf, wt * y);
+                            }
+                        }
+                    } else {  // OUT_BF16
+                        if (valid) {
+                            const float ws = a.a_ws2[0][e];
+#pragma unroll
+                            for (int hf = 0; hf < 2; ++hf)
+                                a.y_out[(size_t)r * a.N + n0 + g + 8 * hf] =
+                                    f32_to_bf16_bits(__fmul_rn(__fmul_rn(acc[0][2 * hf + cc], rs), ws));
                         }
                     }
-                } else {  // OUT_BF16
-                    if (valid) {
-                        const float ws = a.a_ws2[0][e];
-#pragma unroll
-                        for (int hf = 0; hf < 2; ++hf)
-                            a.y_out[(size_t)r * a.N + n0 + g + 8 * hf] =
-                                f32_to_bf16_bits(__fmul_rn(__fmul_rn(acc[0][2 * hf + cc], rs), ws));
+                }
+            }
+
+
+            if (last) {
+                if constexpr (OUTMODE == OUT_COMBINE) {
+                    // the CTA that adds the last contribution to a token turns its
+                    // fp32 row into the bf16 output row
+                    __threadfence();
+                    __syncthreads();
+                    if (tid < kGemvTokTile) {
+                        int t = -1;
+                        if (tid < nrows) {
+                            const int tt = a.row_to_slot[row0 + tid] / a.top_k;
+                            if (atomicAdd(a.tok_done + tt, 1) == a.done_target - 1) t = tt;
+                        }
+                        s_fin[tid] = t;
+                    }
+                    __syncthreads();
+                    for (int i = 0; i < nrows; ++i) {
+                        const int t = s_fin[i];
+                        if (t < 0) continue;
+                        __threadfence();
+                        const float4* src = reinterpret_cast<const float4*>(a.acc_out + (size_t)t * a.N);
+                        uint2* dst = reinterpret_cast<uint2*>(a.out_bf16 + (size_t)t * a.N);
+                        for (int jx = tid; jx < a.N / 4; jx += kThreads) {
+                            const float4 v = __ldcg(src + jx);
+                            uint2 o;
+                            o.x = (uint32_t)f32_to_bf16_bits(v.x) | ((uint32_t)f32_to_bf16_bits(v.y) << 16);
+                            o.y = (uint32_t)f32_to_bf16_bits(v.z) | ((uint32_t)f32_to_bf16_bits(v.w) << 16);
+                            dst[jx] = o;
+                        }
                     }
                 }
+                break;
             }
-        }
-
-        if constexpr (OUTMODE == OUT_COMBINE) {
-            // the CTA that adds the last contribution to a token turns its
-            // fp32 row into the bf16 output row
-            __threadfence();
-            __syncthreads();
-            if (tid < kGemvTokTile) {
-                int t = -1;
-                if (tid < nrows) {
-                    const int tt = a.row_to_slot[row0 + tid] / a.top_k;
-                    if (atomicAdd(a.tok_done + tt, 1) == a.done_target - 1) t = tt;
-                }
-                s_fin[tid] = t;
-            }
-            __syncthreads();
-            for (int i = 0; i < nrows; ++i) {
-                const int t = s_fin[i];
-                if (t < 0) continue;
-                __threadfence();
-                const float4* src = reinterpret_cast<const float4*>(a.acc_out + (size_t)t * a.N);
-                uint2* dst = reinterpret_cast<uint2*>(a.out_bf16 + (size_t)t * a.N);
-                for (int jx = tid; jx < a.N / 4; jx += kThreads) {
-                    const float4 v = __ldcg(src + jx);
-                    uint2 o;
-                    o.x = (uint32_t)f32_to_bf16_bits(v.x) | ((uint32_t)f32_to_bf16_bits(v.y) << 16);
-                    o.y = (uint32_t)f32_to_bf16_bits(v.z) | ((uint32_t)f32_to_bf16_bits(v.w) << 16);
-                    dst[jx] = o;
-                }
-            }
+            __syncthreads();  // s_red and the epilogue's reads finish before the next block
+            cur = following;
         }
         if (tid < kGemvTokTile) s_amax[tid] = 0u;
         __syncthreads();
@@ -441,6 +462,18 @@ void launch_ck(int bmode, int outmode, const GemvArgs& a, int max_work, cudaStre
 size_t gemv_smem_bytes(int K) { return (size_t)kGemvTokTile * K * 2; }
 
 bool gemv_supported_k(int K) { return K > 0 && K % 64 == 0 && K <= 12288; }
+
+// Feature blocks per work item: the down projection (short K) gains from
+// staging its rows once for several blocks; gate/up items are long enough.
+int gemv_pick_group(int expected_tiles, int N, int ksplit, int nproj) {
+    if (nproj != 1) return 1;
+    const int n_fb = N / (16 * (kWarps / ksplit));
+    const long long want = 4LL * num_sms();  // keep about two items per resident CTA
+    int g = 1;
+    for (int c = 2; c <= 4; c *= 2)
+        if ((long long)expected_tiles * ((n_fb + c - 1) / c) >= want) g = c;
+    return g;
+}
 
 int gemv_pick_ksplit(int expected_tiles, int N, int nproj) {
     (void)nproj;

@@ -46,6 +46,9 @@ def decode(T: int) -> MoEShape:
 
 PREFILL_W4A16 = MoEShape(T=4096, d=4096, E=288, k=8, F=1536)
 PREFILL_W4A4 = MoEShape(T=8192, d=4096, E=288, k=8, F=1536)
+# a smaller prompt-shaped layer (about 128 routed rows per expert) for
+# full-metric profiler captures, whose replay cost grows with device memory
+PROMPT_SMALL = MoEShape(T=1024, d=4096, E=64, k=8, F=1536)
 SKEW = MoEShape(T=16384, d=4096, E=288, k=8, F=1536)
 DENSE = dict(M=8192, d=4096, F=12288)
 
