@@ -32,6 +32,8 @@
 //     down projection's row scale), SwiGLU + NVFP4 requantisation of h with
 //     the down input_scale (W4A4), or the weighted top-k combine into an fp32
 //     accumulator with red.add (down projection).
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.cuh"
 
@@ -105,7 +107,11 @@ struct Item {
 template <int CK, int BMODE, int OUTMODE, int NPROJ>
 __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
     using C = Chunk<CK>;
-    constexpr int U = NPROJ == 2 ? 2 : 4;  // chunks whose weight loads are in flight together
+    // chunks whose weight loads are issued together; the single-projection
+    // kernel keeps two such batches in registers so that the next batch is
+    // in flight while one is consumed
+    constexpr int U = 2;
+    constexpr int NBUF = NPROJ == 2 ? 1 : 2;
     extern __shared__ uint4 Bs[];          // [kGemvTokTile][K/8] granules of f16
     __shared__ float s_red[kWarps - 1][NPROJ * 4][32];
     __shared__ float s_rowscale[kGemvTokTile];
@@ -151,9 +157,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
         it.nrows = min(kGemvTokTile, a.offsets[it.e + 1] - it.row0);
     };
 
-    uint32_t acw[U][NPROJ][2][C::CW];
-    uint32_t asw[U][NPROJ][2];
-    auto load_batch = [&](const Item& it, int chb) {
+    uint32_t acw[NBUF][U][NPROJ][2][C::CW];
+    uint32_t asw[NBUF][U][NPROJ][2];
+    auto load_batch = [&](auto buf, const Item& it, int chb) {
+        constexpr int B = decltype(buf)::value;
         const int n0 = it.fb * FB + wf * 16;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -165,8 +172,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {
                         const size_t row = (size_t)it.e * a.N + n0 + g + 8 * hf;
-                        load_codes<CK>(a.a_codes[p] + row * K2 + kb / 2, acw[u][p][hf]);
-                        asw[u][p][hf] = load_scales<CK>(a.a_scales[p] + row * K16 + kb / 16);
+                        load_codes<CK>(a.a_codes[p] + row * K2 + kb / 2, acw[B][u][p][hf]);
+                        asw[B][u][p][hf] = load_scales<CK>(a.a_scales[p] + row * K16 + kb / 16);
                     }
             }
         }
@@ -179,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
     Item cur{};
     if (item < total) {
         decode(item, cur);
-        load_batch(cur, ks);
+        load_batch(std::integral_constant<int, 0>{}, cur, ks);
     }
 
     while (item < total) {
@@ -247,8 +254,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) acc[p][i] = 0.0f;
             const uint4* brow_s = Bs + (size_t)g * Kg;
-            for (int chb = ks; chb < nch; chb += U * KSPL) {
-                if (chb != ks) load_batch(cur, chb);
+            auto compute = [&](auto buf, int chb) {
+                constexpr int B = decltype(buf)::value;
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int ch = chb + u * KSPL;
@@ -262,14 +269,32 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
 #pragma unroll
                         for (int p = 0; p < NPROJ; ++p) {
                             uint32_t r0[4], r1[4];
-                            deq_word(acw[u][p][0][jj >> 1], asw[u][p][0], jj, r0);
-                            deq_word(acw[u][p][1][jj >> 1], asw[u][p][1], jj, r1);
+                            deq_word(acw[B][u][p][0][jj >> 1], asw[B][u][p][0], jj, r0);
+                            deq_word(acw[B][u][p][1][jj >> 1], asw[B][u][p][1], jj, r1);
                             const uint32_t af0[4] = {r0[0], r1[0], r0[1], r1[1]};
                             const uint32_t af1[4] = {r0[2], r1[2], r0[3], r1[3]};
                             mma_16816(acc[p], af0, b0);
                             mma_16816(acc[p], af1, b1);
                         }
                     }
+                }
+            };
+            constexpr std::integral_constant<int, 0> kB0{};
+            if constexpr (NBUF == 1) {
+                for (int chb = ks; chb < nch; chb += U * KSPL) {
+                    if (chb != ks) load_batch(kB0, cur, chb);
+                    compute(kB0, chb);
+                }
+            } else {
+                // batch b starts at chunk ks + b * U * KSPL; buffer b % 2
+                constexpr std::integral_constant<int, NBUF - 1> kB1{};
+                const int step = U * KSPL;
+                for (int chb = ks; chb < nch; chb += 2 * step) {
+                    if (chb + step < nch) load_batch(kB1, cur, chb + step);
+                    compute(kB0, chb);
+                    if (chb + step >= nch) break;
+                    if (chb + 2 * step < nch) load_batch(kB0, cur, chb + 2 * step);
+                    compute(kB1, chb + step);
                 }
             }
             const bool owner = ks == 0;
@@ -289,12 +314,12 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
             Item following = cur;
             if (!last) {
                 following.fb = cur.fb + 1;
-                load_batch(following, ks);
+                load_batch(kB0, following, ks);
             } else {
                 nitem = s_next;
                 if (nitem < total) {
                     decode(nitem, nxt);
-                    load_batch(nxt, ks);
+                    load_batch(kB0, nxt, ks);
                 }
             }
             if (KSPL > 1 && owner) {
