@@ -107,11 +107,11 @@ struct Item {
 template <int CK, int BMODE, int OUTMODE, int NPROJ>
 __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
     using C = Chunk<CK>;
-    // chunks whose weight loads are issued together; the single-projection
-    // kernel keeps two such batches in registers so that the next batch is
-    // in flight while one is consumed
-    constexpr int U = 2;
-    constexpr int NBUF = NPROJ == 2 ? 1 : 2;
+    // U chunks form a batch of weight loads; NBUF batches live in registers
+    // as a ring, so that NBUF - 1 batches are in flight while one is consumed
+    // (the next work item's first batches go out before the epilogue)
+    constexpr int U = 1;
+    constexpr int NBUF = NPROJ == 2 ? 2 : 3;
     extern __shared__ uint4 Bs[];          // [kGemvTokTile][K/8] granules of f16
     __shared__ float s_red[kWarps - 1][NPROJ * 4][32];
     __shared__ float s_rowscale[kGemvTokTile];
@@ -178,6 +178,11 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
             }
         }
     };
+    // the first NBUF - 1 batches of an item's (or feature block's) weights
+    auto prefetch = [&](const Item& it) {
+        load_batch(std::integral_constant<int, 0>{}, it, ks);
+        if constexpr (NBUF > 2) load_batch(std::integral_constant<int, 1>{}, it, ks + U * KSPL);
+    };
 
     if (tid == 0) s_next = atomicAdd(a.work_counter, 1);
     if (tid < kGemvTokTile) s_amax[tid] = 0u;
@@ -186,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
     Item cur{};
     if (item < total) {
         decode(item, cur);
-        load_batch(std::integral_constant<int, 0>{}, cur, ks);
+        prefetch(cur);
     }
 
     while (item < total) {
@@ -279,22 +284,25 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
                     }
                 }
             };
-            constexpr std::integral_constant<int, 0> kB0{};
-            if constexpr (NBUF == 1) {
-                for (int chb = ks; chb < nch; chb += U * KSPL) {
-                    if (chb != ks) load_batch(kB0, cur, chb);
-                    compute(kB0, chb);
-                }
-            } else {
-                // batch b starts at chunk ks + b * U * KSPL; buffer b % 2
-                constexpr std::integral_constant<int, NBUF - 1> kB1{};
+            // batch b starts at chunk ks + b * step and lives in buffer b % NBUF;
+            // batches 0 .. NBUF-2 were loaded by prefetch()
+            {
+                constexpr std::integral_constant<int, 0> kB0{};
+                constexpr std::integral_constant<int, 1> kB1{};
+                constexpr std::integral_constant<int, 2 % NBUF> kB2{};
                 const int step = U * KSPL;
-                for (int chb = ks; chb < nch; chb += 2 * step) {
-                    if (chb + step < nch) load_batch(kB1, cur, chb + step);
+                for (int chb = ks; chb < nch; chb += NBUF * step) {
+                    const int ld = (NBUF - 1) * step;  // distance of the batch loaded ahead
+                    if (chb + ld < nch) load_batch(std::integral_constant<int, NBUF - 1>{}, cur, chb + ld);
                     compute(kB0, chb);
                     if (chb + step >= nch) break;
-                    if (chb + 2 * step < nch) load_batch(kB0, cur, chb + 2 * step);
+                    if (chb + step + ld < nch) load_batch(kB0, cur, chb + step + ld);
                     compute(kB1, chb + step);
+                    if constexpr (NBUF == 3) {
+                        if (chb + 2 * step >= nch) break;
+                        if (chb + 2 * step + ld < nch) load_batch(kB1, cur, chb + 2 * step + ld);
+                        compute(kB2, chb + 2 * step);
+                    }
                 }
             }
             const bool owner = ks == 0;
@@ -314,12 +322,12 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
             Item following = cur;
             if (!last) {
                 following.fb = cur.fb + 1;
-                load_batch(kB0, following, ks);
+                prefetch(following);
             } else {
                 nitem = s_next;
                 if (nitem < total) {
                     decode(nitem, nxt);
-                    load_batch(kB0, nxt, ks);
+                    prefetch(nxt);
                 }
             }
             if (KSPL > 1 && owner) {
