@@ -118,8 +118,9 @@ struct TcArgs {
 // ---- prompt-shaped grouped GEMMs with the routed rows as M (tcgen05, N = 256) ----
 // SWIGLU: h = bf16(silu(bf16 G) * bf16 U); SWIGLU_Q: h requantised to NVFP4
 // (codes + e4m3 block scales under hq_gs); COMBINE: weighted red.add into
-// the fp32 accumulator; BF16: plain bf16 rows.
-enum TcmEpi { TCM_SWIGLU = 0, TCM_COMBINE = 1, TCM_BF16 = 2, TCM_SWIGLU_Q = 3 };
+// the fp32 accumulator; BF16: plain bf16 rows; ROWS: fp32 rows w * y by
+// routed row, summed per token afterwards (launch_sum_rows).
+enum TcmEpi { TCM_SWIGLU = 0, TCM_COMBINE = 1, TCM_BF16 = 2, TCM_SWIGLU_Q = 3, TCM_ROWS = 4 };
 
 struct TcmArgs {
     CUtensorMap tmap_x;          // f16 rows [R, K] (expert order), box 64 x 128, 128-byte swizzle
@@ -142,6 +143,7 @@ struct TcmArgs {
     const int32_t* row_to_slot;  // TCM_COMBINE: [R]
     const float* topk_w;         // TCM_COMBINE: [T*k]
     uint16_t* y_out;             // TCM_BF16: [R, N]
+    float* y_rows;               // TCM_ROWS: [R, N] fp32 w * y by routed row
     uint8_t* hq_out;             // TCM_SWIGLU_Q: [R, N/2] codes
     uint8_t* hs_out;             //   [R, N/16] e4m3 block scales
     const float* hq_gs;          //   [E] global scale they are taken under
@@ -166,6 +168,9 @@ bool tcq_supported(int epi, int N, int K);
 // Encodes the tensor maps this kernel uses (rows_w = E * N, rows_x = R).
 bool tcq_set_maps(TcmArgs* a, const uint8_t* x_codes, const uint8_t* x_scales, long long rows_x, long long rows_w);
 void launch_tcq(int epi, const TcmArgs& a, int max_units, cudaStream_t s);
+// out[t] = bf16(sum over slots j in order of y[slot_to_row[t * k + j]]), rows of d floats.
+void launch_sum_rows(const float* y, const int32_t* slot_to_row, int T, int k, int d, uint16_t* out,
+                     cudaStream_t s);
 
 size_t tc_smem_bytes(int nproj);
 void launch_tc_gemm(int outmode, int nproj, const TcArgs& a, int max_units, cudaStream_t s);

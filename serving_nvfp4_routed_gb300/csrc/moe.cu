@@ -32,6 +32,7 @@ struct MoeWs {
     uint8_t* hq;      // [R, F/2]   W4A4
     uint8_t* hs;      // [R, F/16]  W4A4
     float* acc;       // [T, d]
+    float* yrows;     // [R, d] W4A4 prompt path: w * y rows by routed row
     int* clear;       // [kCounters + T]: work counters, then per-token completion counts
     // prompt-shaped (tensor-core) path, W4A16
     uint16_t* xp;     // [R, d]  f16 x * 2^-s, rows in expert order
@@ -100,6 +101,7 @@ MoeWs carve_moe(void* base, int T, int E, int k, int d, int F, int mode, size_t*
         w.xs = c.take<uint8_t>(R * (d / 16));
         w.hq = c.take<uint8_t>(R * (F / 2));
         w.hs = c.take<uint8_t>(R * (F / 16));
+        if (tcq_supported(TCM_SWIGLU_Q, F, d) && tcq_supported(TCM_ROWS, d, F)) w.yrows = c.take<float>(R * d);
     }
     if (bytes) *bytes = align_up(c.off, 256);
     return w;
@@ -166,7 +168,9 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
 
     if (mode == 1 && use_tc_w4a4(T, E, top_k, d, F)) {
         const int max_tiles = R / kTcTokTile + std::min(E, R) + 1;
-        launch_zero(ws.acc, sizeof(float) * (size_t)T * d, s);
+        // block-scaled FP4 MMA when the shapes allow it, else f16 MMA of dequantised tiles
+        const bool fp4 = ws.yrows != nullptr;
+        if (!fp4) launch_zero(ws.acc, sizeof(float) * (size_t)T * d, s);
         // gate/up + SwiGLU, h requantised under the down projection's input scale
         TcmArgs g{};
         g.K = d;
@@ -183,8 +187,6 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
         g.hs_out = ws.hs;
         g.hq_gs = is2;
         g.status = d_status;
-        // block-scaled FP4 MMA when the shapes allow it, else f16 MMA of dequantised tiles
-        const bool fp4 = tcq_supported(TCM_SWIGLU_Q, F, d) && tcq_supported(TCM_COMBINE, d, F);
         if (fp4) {
             if (!tcq_set_maps(&g, ws.xq, ws.xs, R, (long long)E * F)) return NVFP4_ERR_CUDA;
             launch_tcq(TCM_SWIGLU_Q, g, max_tiles * (F / 64), s);
@@ -205,13 +207,17 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
         u.row_to_slot = ws.ra.row_to_slot;
         u.topk_w = ws.ra.w;
         if (fp4) {
+            // w * y rows by routed row, then each token's slots summed in slot order
+            u.y_rows = ws.yrows;
+            u.acc_out = nullptr;
             if (!tcq_set_maps(&u, ws.hq, ws.hs, R, (long long)E * d)) return NVFP4_ERR_CUDA;
-            launch_tcq(TCM_COMBINE, u, max_tiles * (d / 128), s);
+            launch_tcq(TCM_ROWS, u, max_tiles * (d / 128), s);
+            launch_sum_rows(ws.yrows, ws.ra.slot_to_row, T, top_k, d, out, s);
         } else {
             if (!tcm_set_weights(&u, (long long)E * d) || !tcm_set_act(&u, ws.hq, ws.hs, R)) return NVFP4_ERR_CUDA;
             launch_tcm(TCM_COMBINE, 1, u, max_tiles * (d / 256), s);
+            launch_acc_to_bf16(ws.acc, (size_t)T * d, out, s);
         }
-        launch_acc_to_bf16(ws.acc, (size_t)T * d, out, s);
         return last_launch_status();
     }
 

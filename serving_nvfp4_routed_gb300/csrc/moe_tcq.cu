@@ -13,7 +13,10 @@
 // Unit = (expert e, 128 B rows, 128 routed rows of e):
 //   D[j, n] = sum_k X[row0 + j, k] * B[n, k]
 //   SwiGLU: B rows 0..63 = gate rows f0.., 64..127 = up rows f0..;
-//   combine: B rows = 128 consecutive rows f0.. of the down projection.
+//   down: B rows = 128 consecutive rows f0.. of the down projection; the
+//   epilogue writes fp32 rows w * y by routed row (staged through shared
+//   memory so that every store is a whole 128-byte line) and a second kernel
+//   sums each token's slots in slot order.
 // One MMA has M = 128, N = 128, K = 64 and runs at the full FP4 rate.
 // A k-stage covers K = 256: the rows' codes (128 bytes per row, 128-byte
 // swizzle) and e4m3 scales (16 bytes per row) of A and B arrive by TMA into
@@ -40,7 +43,7 @@ using namespace tc;
 
 constexpr int BM = 128, BN = 128;
 constexpr int KS = 256;                    // k per stage
-constexpr int S = 6;                       // stage ring depth (even: each slot has one scale group)
+constexpr int S = 4;                       // stage ring depth (even: each slot has one scale group)
 constexpr int kA = BM * KS / 2;            // 16 KB codes
 constexpr int kB = BN * KS / 2;            // 16 KB codes
 constexpr int kSA = BM * KS / 16;          // 2 KB scales
@@ -49,7 +52,8 @@ constexpr int kStage = kA + kB + kSA + kSB;  // 36 KB
 static_assert(kStage % 1024 == 0, "stage slots keep 1024-byte alignment");
 constexpr int kMaxUnits = 320;
 constexpr int kTileCopy = kMaxExperts + 1;
-constexpr int kSmem = 1024 + S * kStage + kMaxUnits * 16 + kTileCopy * 4;
+constexpr int kStageRow = 33;               // epilogue staging: 32 rows x 32 floats, padded
+constexpr int kSmem = 1024 + S * kStage + kMaxUnits * 16 + kTileCopy * 4 + 8 * 32 * kStageRow * 4;
 constexpr int kWarps = 20;
 constexpr int kThreads = kWarps * 32;
 constexpr int kWarpMma = 0, kWarpTma = 1, kWarpEpi = 4, kWarpSf = 8, kSfGroups = 2, kWarpEpi2 = 16;
@@ -95,6 +99,7 @@ __global__ void __launch_bounds__(kThreads, 1) tcq_kernel(const __grid_constant_
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     int4* s_units = reinterpret_cast<int4*>(smem + S * kStage);  // {e, row0, row_end, f0}
     int* s_tiles = reinterpret_cast<int*>(s_units + kMaxUnits);
+    float* s_stage = reinterpret_cast<float*>(s_tiles + kTileCopy);  // [8 warps][32][kStageRow]
     __shared__ __align__(8) uint64_t bar_full[S], bar_sf[S], bar_done[S], bar_acc_full[2], bar_acc_empty[2];
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
@@ -267,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1) tcq_kernel(const __grid_constant_
             const bool valid = row < un.z;
             float wt = 0.0f;
             size_t tok = 0;
-            if constexpr (EPI == TCM_COMBINE) {
+            if constexpr (EPI == TCM_COMBINE || EPI == TCM_ROWS) {
                 if (valid) {
                     const int slot = a.row_to_slot[row];
                     tok = (size_t)(slot / a.top_k);
@@ -315,6 +320,23 @@ __global__ void __launch_bounds__(kThreads, 1) tcq_kernel(const __grid_constant_
                         a.hs_out[(size_t)row * (a.N / 16) + f / 16] = (uint8_t)sbyte;
                     }
                 }
+            } else if constexpr (EPI == TCM_ROWS) {
+                // 32 rows x 32 columns per warp and chunk: through shared memory,
+                // then one whole row (128 bytes) per store instruction
+                float* st = s_stage + (size_t)(half * 4 + q) * 32 * kStageRow;
+                const int nvalid = min(32, un.z - (un.y + q * 32));  // rows of this warp in the unit
+                for (int cb = 2 * half; cb < 2 * half + 2; ++cb) {
+                    uint32_t r[32];
+                    tmem_ld32(tb + cb * 32, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        st[lane * kStageRow + c] = wt * __fmul_rn(__fmul_rn(__uint_as_float(r[c]), rs), w0);
+                    __syncwarp();
+                    float* ybase = a.y_rows + (size_t)(un.y + q * 32) * a.N + un.w + cb * 32 + lane;
+                    for (int j = 0; j < nvalid; ++j) ybase[(size_t)j * a.N] = st[j * kStageRow + lane];
+                    __syncwarp();
+                }
             } else {
                 for (int cb = 2 * half; cb < 2 * half + 2; ++cb) {
                     uint32_t r[32];
@@ -344,6 +366,34 @@ __global__ void __launch_bounds__(kThreads, 1) tcq_kernel(const __grid_constant_
     if (warp == kWarpMma) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
+    }
+    grid_dep_launch();
+}
+
+// out[t][f] = bf16(sum_j y[slot_to_row[t*k + j]][f]) in slot order; 8 features per thread.
+__global__ void sum_rows_kernel(const float* __restrict__ y, const int32_t* __restrict__ slot_to_row, int T, int k,
+                                int d, uint16_t* __restrict__ out) {
+    grid_dep_wait();
+    const int per_row = d / 8;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < (size_t)T * per_row;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const size_t t = i / per_row, f = (i % per_row) * 8;
+        float acc[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+        for (int j = 0; j < k; ++j) {
+            const size_t r = (size_t)slot_to_row[t * k + j];
+            const float4* src = reinterpret_cast<const float4*>(y + r * d + f);
+            const float4 p0 = __ldcs(src), p1 = __ldcs(src + 1);
+            acc[0] += p0.x; acc[1] += p0.y; acc[2] += p0.z; acc[3] += p0.w;
+            acc[4] += p1.x; acc[5] += p1.y; acc[6] += p1.z; acc[7] += p1.w;
+        }
+        uint4 o;
+        o.x = (uint32_t)f32_to_bf16_bits(acc[0]) | ((uint32_t)f32_to_bf16_bits(acc[1]) << 16);
+        o.y = (uint32_t)f32_to_bf16_bits(acc[2]) | ((uint32_t)f32_to_bf16_bits(acc[3]) << 16);
+        o.z = (uint32_t)f32_to_bf16_bits(acc[4]) | ((uint32_t)f32_to_bf16_bits(acc[5]) << 16);
+        o.w = (uint32_t)f32_to_bf16_bits(acc[6]) | ((uint32_t)f32_to_bf16_bits(acc[7]) << 16);
+        *reinterpret_cast<uint4*>(out + t * d + f) = o;
     }
     grid_dep_launch();
 }
@@ -382,6 +432,15 @@ bool tcq_set_maps(TcmArgs* a, const uint8_t* x_codes, const uint8_t* x_scales, l
 void launch_tcq(int epi, const TcmArgs& a, int max_units, cudaStream_t s) {
     if (epi == TCM_SWIGLU_Q) return launch_tcq_t<TCM_SWIGLU_Q>(a, max_units, s, "tcq_gateup_w4a4");
     if (epi == TCM_COMBINE) return launch_tcq_t<TCM_COMBINE>(a, max_units, s, "tcq_down_w4a4");
+    if (epi == TCM_ROWS) return launch_tcq_t<TCM_ROWS>(a, max_units, s, "tcq_down_w4a4");
+}
+
+void launch_sum_rows(const float* y, const int32_t* slot_to_row, int T, int k, int d, uint16_t* out,
+                     cudaStream_t s) {
+    const size_t n = (size_t)T * (d / 8);
+    if (n == 0) return;
+    const int grid = (int)std::min<size_t>((n + 255) / 256, (size_t)num_sms() * 8);
+    NVFP4_LAUNCH("sum_rows", s, launch_pdl(sum_rows_kernel, dim3(grid), dim3(256), 0, s, y, slot_to_row, T, k, d, out));
 }
 
 }  // namespace nvfp4
