@@ -312,13 +312,15 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
 #pragma unroll
                     for (int i = 0; i < 4; ++i) s_red[wf * (KSPL - 1) + ks - 1][p * 4 + i][lane] = acc[p][i];
             }
-            __syncthreads();
-
+            // (gate/up items are never grouped: known at compile time)
+            const bool last = NPROJ == 2 || cur.fb + 1 >= cur.fb_end;
+            // Warps that do not split K are independent within a feature block:
+            // they meet only to share partial sums (KSPL > 1) and, at an item's
+            // last block, to read the next item's index.
+            if (KSPL > 1 || last) __syncthreads();
 
             // ---- the next feature block's (or the next item's) first weight
             // batch goes out before this block's epilogue
-            // (gate/up items are never grouped: known at compile time)
-            const bool last = NPROJ == 2 || cur.fb + 1 >= cur.fb_end;
             Item following = cur;
             if (!last) {
                 following.fb = cur.fb + 1;
@@ -450,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
                 }
                 break;
             }
-            __syncthreads();  // s_red and the epilogue's reads finish before the next block
+            if (KSPL > 1) __syncthreads();  // s_red is read before the next block rewrites it
             cur = following;
         }
         if (tid < kGemvTokTile) s_amax[tid] = 0u;
