@@ -225,6 +225,17 @@ size_t nvfp4_linear_workspace_size(int M, int K, int N);
  * --------------------------------------------------------------------- */
 const char* nvfp4_status_string(nvfp4_status s);
 uint64_t nvfp4_launch_count(void);
+
+/* ------------------------------------------------------------------------
+ * nvfp4_selftest_bounded_wait: exercises the failure detection every
+ * kernel of the library relies on (the pages have no counterpart).  One CTA
+ * waits on an mbarrier that nothing arrives on; the bounded wait gives up
+ * after about 2 s of SM clock, stores NVFP4_ERR_TIMEOUT in *d_status and the
+ * kernel returns normally (no trap, no fault; the context stays usable).
+ * d_status: device int32, 16-byte aligned, caller-owned.  Asynchronous on
+ * `stream`; returns NVFP4_ERR_INVALID_ARG / NVFP4_ERR_ALIGN on a bad pointer.
+ * --------------------------------------------------------------------- */
+nvfp4_status nvfp4_selftest_bounded_wait(int32_t* d_status, cudaStream_t stream);
 void nvfp4_profile_enable(int on);
 int nvfp4_profile_collect(int max, char* names, int* launches, double* ms);
 

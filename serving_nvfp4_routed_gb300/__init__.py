@@ -7,4 +7,4 @@ The compute path is the CUDA library under ``csrc/`` (built in-tree by
 from ._lib import (MoEWeights, NVFP4Tensor, Nvfp4Error, launch_count, load, moe_route_permute,  # noqa: F401
                    moe_workspace, moe_workspace_size, moe_workspace_views, nvfp4_linear, nvfp4_moe_w4a4,
                    nvfp4_moe_w4a16, nvfp4_quantize_act, nvfp4_quantize_weights, profile_collect,
-                   profile_enable, status_string)
+                   profile_enable, selftest_bounded_wait, status_string)

@@ -27,7 +27,7 @@ EXPORTS = ("nvfp4_quantize_weights", "nvfp4_quantize_weights_workspace_size", "n
            "nvfp4_moe_workspace_size", "nvfp4_moe_workspace_views", "nvfp4_linear",
            "nvfp4_linear_workspace_size", "nvfp4_status_string", "nvfp4_launch_count",
            "nvfp4_profile_enable", "nvfp4_profile_collect", "nvfp4_quantize_weights_noalloc",
-           "nvfp4_quantize_weights_noalloc_max_batch")
+           "nvfp4_quantize_weights_noalloc_max_batch", "nvfp4_selftest_bounded_wait")
 
 
 class Nvfp4Error(RuntimeError):
@@ -79,6 +79,7 @@ def load(path: str = LIB_PATH):
         L.nvfp4_status_string.argtypes = [i32]
         L.nvfp4_status_string.restype = ctypes.c_char_p
         L.nvfp4_launch_count.restype = ctypes.c_uint64
+        L.nvfp4_selftest_bounded_wait.argtypes = [vp, vp]
         L.nvfp4_profile_enable.argtypes = [i32]
         L.nvfp4_profile_collect.argtypes = [i32, ctypes.c_char_p, ctypes.POINTER(i32),
                                             ctypes.POINTER(ctypes.c_double)]
@@ -291,6 +292,14 @@ def status_string(code: int) -> str:
 
 def launch_count() -> int:
     return int(load().nvfp4_launch_count())
+
+
+def selftest_bounded_wait(d_status, stream=None) -> None:
+    """Launch the library's bounded-wait self-test: a barrier nothing arrives
+    on; the kernel gives up after about 2 s and writes NVFP4_ERR_TIMEOUT (7)
+    into d_status (an int32 CUDA tensor)."""
+    _cuda(d_status)
+    _check("nvfp4_selftest_bounded_wait", load().nvfp4_selftest_bounded_wait(_p(d_status), _stream(stream)))
 
 
 def profile_enable(on: bool = True):
