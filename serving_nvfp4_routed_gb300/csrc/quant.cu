@@ -117,31 +117,40 @@ __global__ void quantize_weights_kernel(const uint16_t* __restrict__ w, size_t n
 }
 
 // Output row r quantises source row src(r) with the input scale of the
-// expert whose row range holds r.  One CTA per row (grid-stride): the row's
-// expert and source are found once, each thread takes whole 16-value blocks
-// (coalesced 32-byte loads, 8-byte code and 1-byte scale stores).
-__global__ void quantize_act_kernel(const uint16_t* __restrict__ x, int M, int K,
-                                    const int32_t* __restrict__ row_to_slot, int top_k,
-                                    const float* __restrict__ input_scale,
-                                    const int32_t* __restrict__ offsets, int E,
-                                    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+// expert whose row range holds r.  One warp per row (8 rows in flight per
+// CTA, grid-stride); the expert offsets are cached in shared memory for the
+// row's lookup; each lane takes whole 16-value blocks (32-byte loads, 8-byte
+// code and 1-byte scale stores).
+constexpr int kQaWarps = 8;
+constexpr int kQaMaxE = 1024;
+
+__global__ void __launch_bounds__(kQaWarps * 32) quantize_act_kernel(
+    const uint16_t* __restrict__ x, int M, int K, const int32_t* __restrict__ row_to_slot, int top_k,
+    const float* __restrict__ input_scale, const int32_t* __restrict__ offsets, int E, uint8_t* __restrict__ codes,
+    uint8_t* __restrict__ scales) {
+    __shared__ int s_off[kQaMaxE + 1];
     grid_dep_wait();
+    const bool cached = offsets && E <= kQaMaxE;
+    if (cached)
+        for (int i = threadIdx.x; i <= E; i += blockDim.x) s_off[i] = offsets[i];
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nb = K / 16;
-    for (int r = blockIdx.x; r < M; r += gridDim.x) {
+    for (int r = blockIdx.x * kQaWarps + warp; r < M; r += gridDim.x * kQaWarps) {
         const int src = row_to_slot ? row_to_slot[r] / top_k : r;
         float gs;
         if (offsets) {
             int lo = 0, hi = E;  // find e with offsets[e] <= r < offsets[e+1]
             while (hi - lo > 1) {
                 const int mid = (lo + hi) >> 1;
-                if (offsets[mid] <= r) lo = mid; else hi = mid;
+                if ((cached ? s_off[mid] : offsets[mid]) <= r) lo = mid; else hi = mid;
             }
             gs = input_scale[lo];
         } else {
             gs = input_scale[0];
         }
         const uint16_t* xr = x + (size_t)src * K;
-        for (int b = threadIdx.x; b < nb; b += blockDim.x) {
+        for (int b = lane; b < nb; b += 32) {
             float v0[8], v1[8], m0, m1;
             load_bf16x8(xr + (size_t)b * 16, v0, m0);
             load_bf16x8(xr + (size_t)b * 16 + 8, v1, m1);
@@ -160,11 +169,10 @@ void launch_quantize_act(const uint16_t* x, int M, int K, const int32_t* row_to_
                          const float* input_scale, const int32_t* offsets, int E, uint8_t* codes,
                          uint8_t* scales, cudaStream_t s) {
     if ((size_t)M * K == 0) return;
-    const int threads = std::min(256, std::max(32, (K / 16 + 31) / 32 * 32));
-    const int grid = std::min(M, num_sms() * (2048 / threads));
+    const int grid = std::min((M + kQaWarps - 1) / kQaWarps, num_sms() * 8);
     NVFP4_LAUNCH("quantize_act", s,
-                 launch_pdl(quantize_act_kernel, dim3(grid), dim3(threads), 0, s, x, M, K, row_to_slot, top_k,
-                            input_scale, offsets, E, codes, scales));
+                 launch_pdl(quantize_act_kernel, dim3(grid), dim3(kQaWarps * 32), 0, s, x, M, K, row_to_slot,
+                            top_k, input_scale, offsets, E, codes, scales));
 }
 
 }  // namespace nvfp4
