@@ -188,14 +188,23 @@ __device__ void validate_ids(int32_t* ids, int R, int E, int32_t* status) {
 }
 
 // Permutation of R <= kSmallMaxRows rows in one CTA (ids already written by
-// topk_kernel, or given by the caller and validated here).
+// topk_kernel, or given by the caller and validated here).  With logits (a
+// few tokens) the CTA also runs the top-k itself, one warp per token, so that
+// a decode step routes in one launch.
+constexpr int kFusedTopkMaxTokens = 64;
+
 __global__ void __launch_bounds__(1024) route_perm_small_kernel(int T, int E, int k, int given_ids, RouteArrays ra,
-                                                                int32_t* status) {
+                                                                int32_t* status, const float* logits) {
     __shared__ int run[kMaxExperts];
     __shared__ uint8_t wh[32 * kMaxExperts];
     __shared__ int tmp32[32];
     grid_dep_wait();
     const int R = T * k;
+    if (logits) {
+        for (int t = threadIdx.x >> 5; t < T; t += blockDim.x >> 5)
+            topk_dispatch(logits + (size_t)t * E, E, k, ra.ids + (size_t)t * k, ra.w + (size_t)t * k);
+        __syncthreads();  // the block reads these ids below
+    }
     if (given_ids) validate_ids(ra.ids, R, E, status);
     for (int i = threadIdx.x; i < E; i += blockDim.x) run[i] = 0;
     for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) wh[i] = 0;
@@ -278,15 +287,16 @@ size_t route_scratch_words(int T, int E, int top_k) {
 
 void launch_route(const float* logits, int T, int E, int k, RouteArrays ra, int32_t* d_status, cudaStream_t s) {
     const int R = T * k;
-    if (logits) {
+    const bool fused = logits && T <= kFusedTopkMaxTokens && R <= kSmallMaxRows;
+    if (logits && !fused) {
         // one warp per token, 8 tokens per CTA: the top-k work spreads over SMs
         NVFP4_LAUNCH("route_topk", s,
                      launch_pdl(topk_kernel, dim3((T + 7) / 8), dim3(256), 0, s, logits, T, E, k, ra.ids, ra.w));
     }
     if (R <= kSmallMaxRows) {
-        NVFP4_LAUNCH("route_perm", s,
+        NVFP4_LAUNCH(fused ? "route" : "route_perm", s,
                      launch_pdl(route_perm_small_kernel, dim3(1), dim3(1024), 0, s, T, E, k, logits ? 0 : 1, ra,
-                                d_status));
+                                d_status, fused ? logits : (const float*)nullptr));
         return;
     }
     if (!logits) {
