@@ -168,7 +168,7 @@ def test_dense_linear_and_mlp(orc, M, K, N, path):
 
 
 @pytest.mark.parametrize("kind,mode", [("normal", "w4a16"), ("zipf", "w4a16"), ("zipf_masked", "w4a16"),
-                                       ("normal", "w4a4")])
+                                       ("normal", "w4a4"), ("zipf", "w4a4")])
 def test_prefill_sampled(orc, decode_bank, kind, mode):
     """Prompt-shaped layers at full size (T=4096 for W4A16, skewed popularity
     at T=16384, W4A4 at T=8192 with 5 % outlier rows); the oracle evaluates
