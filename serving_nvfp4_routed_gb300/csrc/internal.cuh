@@ -162,12 +162,14 @@ bool tcm_set_act(TcmArgs* a, const uint8_t* codes, const uint8_t* scales, long l
 void launch_tcm(int epi, int a_nvfp4, const TcmArgs& a, int max_units, cudaStream_t s);
 
 // ---- W4A4 prompt-shaped grouped GEMM on the block-scaled FP4 tensor cores ----
-// Same arguments as TcmArgs (NVFP4 rows: a_codes / x_gs); epi TCM_SWIGLU_Q or
-// TCM_COMBINE.  Needs K % 256 == 0 and N % 64 (SwiGLU) / N % 128 (combine).
+// Same arguments as TcmArgs (NVFP4 rows: a_codes / x_gs); epi TCM_SWIGLU_Q,
+// TCM_ROWS or TCM_COMBINE.  Needs K % 256 == 0 and N % 16 (SwiGLU) / N % 32.
 bool tcq_supported(int epi, int N, int K);
 // Encodes the tensor maps this kernel uses (rows_w = E * N, rows_x = R).
 bool tcq_set_maps(TcmArgs* a, const uint8_t* x_codes, const uint8_t* x_scales, long long rows_x, long long rows_w);
-void launch_tcq(int epi, const TcmArgs& a, int max_units, cudaStream_t s);
+// max_tiles bounds the 128-row tiles over all experts; the unit count
+// follows from the kernel's column slice.
+void launch_tcq(int epi, const TcmArgs& a, int max_tiles, cudaStream_t s);
 // out[t] = bf16(sum over slots j in order of y[slot_to_row[t * k + j]]), rows of d floats.
 void launch_sum_rows(const float* y, const int32_t* slot_to_row, int T, int k, int d, uint16_t* out,
                      cudaStream_t s);

@@ -189,7 +189,7 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
         g.status = d_status;
         if (fp4) {
             if (!tcq_set_maps(&g, ws.xq, ws.xs, R, (long long)E * F)) return NVFP4_ERR_CUDA;
-            launch_tcq(TCM_SWIGLU_Q, g, max_tiles * (F / 64), s);
+            launch_tcq(TCM_SWIGLU_Q, g, max_tiles, s);
         } else {
             if (!tcm_set_weights(&g, (long long)E * F) || !tcm_set_act(&g, ws.xq, ws.xs, R)) return NVFP4_ERR_CUDA;
             launch_tcm(TCM_SWIGLU_Q, 1, g, max_tiles * (F / 128), s);
@@ -211,7 +211,7 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
             u.y_rows = ws.yrows;
             u.acc_out = nullptr;
             if (!tcq_set_maps(&u, ws.hq, ws.hs, R, (long long)E * d)) return NVFP4_ERR_CUDA;
-            launch_tcq(TCM_ROWS, u, max_tiles * (d / 128), s);
+            launch_tcq(TCM_ROWS, u, max_tiles, s);
             launch_sum_rows(ws.yrows, ws.ra.slot_to_row, T, top_k, d, out, s);
         } else {
             if (!tcm_set_weights(&u, (long long)E * d) || !tcm_set_act(&u, ws.hq, ws.hs, R)) return NVFP4_ERR_CUDA;

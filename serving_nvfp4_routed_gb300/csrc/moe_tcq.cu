@@ -10,27 +10,33 @@
 // scales is exact; the MMA sums them in fp32 and the epilogue applies the
 // two fp32 tensor scales, as for the f16 kernels.
 //
-// Unit = (expert e, 128 B rows, 128 routed rows of e):
+// Unit = (expert e, 192 B rows, 128 routed rows of e):
 //   D[j, n] = sum_k X[row0 + j, k] * B[n, k]
-//   SwiGLU: B rows 0..63 = gate rows f0.., 64..127 = up rows f0..;
-//   down: B rows = 128 consecutive rows f0.. of the down projection; the
-//   epilogue writes fp32 rows w * y by routed row (staged through shared
-//   memory so that every store is a whole 128-byte line) and a second kernel
-//   sums each token's slots in slot order.
-// One MMA has M = 128, N = 128, K = 64 and runs at the full FP4 rate.
+//   SwiGLU: B rows 0..95 = gate rows f0.., 96..191 = up rows f0..;
+//   down: B rows = 192 consecutive rows f0.. of the down projection (the
+//   last unit of a row tile may reach past the expert's rows: those columns
+//   are computed and dropped); the epilogue writes fp32 rows w * y by routed
+//   row (staged through shared memory so that every store is a whole
+//   128-byte line) and a second kernel sums each token's slots in slot order.
+// One MMA has M = 128, N = 192, K = 64 (96 cycles at the full FP4 rate).
+// N = 192 rather than 128: a single issuing warp spends ~100 cycles per MMA
+// on issue, barrier and commit work, which a 64-cycle N = 128 MMA cannot
+// hide (measured on GB300: 2-3x slower than the FP4 rate), while two N = 256
+// accumulators would leave no tensor memory for the scales.
 // A k-stage covers K = 256: the rows' codes (128 bytes per row, 128-byte
 // swizzle) and e4m3 scales (16 bytes per row) of A and B arrive by TMA into
 // one smem slot of a ring of S.  Two groups of four scale warps (alternate
-// k-stages) copy the slot's scales into tensor memory where the MMA reads
-// them:
+// k-stages) copy the stage's scales into one of three tensor-memory scale
+// slots, where the MMA reads them:
 //   A scales of row m, MMA j: lane m, column 4j + m/32 of the slot's area;
 //   B scales of row n, MMA j: lanes n%32 (every lane quarter), column
-//   16 + 4j + n/32.
+//   16 + 6j + n/32.
 // Each 32-bit TMEM word holds the four block scales of one row and one MMA
 // (bytes = blocks in k order), which is the stored order of the scales.
-// One thread issues the MMAs into two 128-column fp32 accumulators; eight
-// epilogue warps read them (one routed row and half the columns per thread).  mbarrier waits are
-// bounded (about 2 s) and report NVFP4_ERR_TIMEOUT.
+// One warp runs the MMA loop (one elected lane issues) into two 192-column
+// fp32 accumulators; eight epilogue warps read them (one routed row and half
+// the columns per thread).  mbarrier waits are bounded (about 2 s) and
+// report NVFP4_ERR_TIMEOUT.
 #include "common.cuh"
 #include "internal.cuh"
 #include "tc_ptx.cuh"
@@ -41,15 +47,16 @@ namespace {
 
 using namespace tc;
 
-constexpr int BM = 128, BN = 128;
+constexpr int BM = 128, BN = 192;
+constexpr int BH = BN / 2;                 // B rows per TMA box (gate or up half)
 constexpr int KS = 256;                    // k per stage
 constexpr int S = 4;                       // stage ring depth (even: each slot has one scale group)
 constexpr int kA = BM * KS / 2;            // 16 KB codes
-constexpr int kB = BN * KS / 2;            // 16 KB codes
+constexpr int kB = BN * KS / 2;            // 24 KB codes
 constexpr int kSA = BM * KS / 16;          // 2 KB scales
-constexpr int kSB = BN * KS / 16;          // 2 KB scales
-constexpr int kStage = kA + kB + kSA + kSB;  // 36 KB
-static_assert(kStage % 1024 == 0, "stage slots keep 1024-byte alignment");
+constexpr int kSB = BN * KS / 16;          // 3 KB scales
+constexpr int kStage = kA + kB + kSA + kSB;  // 45 KB
+static_assert(kStage % 1024 == 0 && (kB / 2) % 1024 == 0, "stage slots and B halves keep 1024-byte alignment");
 constexpr int kMaxUnits = 320;
 constexpr int kTileCopy = kMaxExperts + 1;
 constexpr int kStageRow = 33;               // epilogue staging: 32 rows x 32 floats, padded
@@ -59,9 +66,13 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kWarpMma = 0, kWarpTma = 1, kWarpEpi = 4, kWarpSf = 8, kSfGroups = 2, kWarpEpi2 = 16;
 static_assert(S % kSfGroups == 0, "each stage slot belongs to one scale group");
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSfCol0 = 2 * BN;       // scale areas after the two accumulators
-constexpr uint32_t kSfCols = 32;           // per stage: A 16 columns, B 16 columns
-static_assert(kSfCol0 + S * kSfCols <= kTmemCols, "tensor memory budget");
+constexpr uint32_t kSfCol0 = 2 * BN;       // scale slots after the two accumulators
+constexpr int kSfSlots = 3;                // tensor-memory scale slots (stage i uses slot i % 3)
+constexpr uint32_t kSfB = 16;              // B scales after A's 4 MMAs x 4 columns
+constexpr uint32_t kSfBPerMma = BN / 32;   // 6 columns of B scales per MMA
+constexpr uint32_t kSfCols = kSfB + 4 * kSfBPerMma;  // 40 columns per slot
+static_assert(kSfCol0 + kSfSlots * kSfCols <= kTmemCols, "tensor memory budget");
+static_assert(kSmem <= 227 * 1024, "shared memory budget");
 
 // Instruction descriptor, kind::mxf4nvf4: A and B e2m1 (format 1, bits 7-9
 // and 10-12), K-major, N >> 3 in bits 17-22, scale type ue4m3 (bit 23 = 0),
@@ -85,6 +96,12 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
         "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
 }
 
 __device__ __forceinline__ bool wait_done(const uint64_t* done, long long j, volatile int* abort_flag,
@@ -125,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1) tcq_kernel(const __grid_constant_
     constexpr bool kPair = EPI == TCM_SWIGLU_Q;
     constexpr int kSlice = kPair ? BN / 2 : BN;  // output features per unit
     const int n_active = *a.n_active;
-    const int n_nt = a.N / kSlice;
+    const int n_nt = (a.N + kSlice - 1) / kSlice;
     for (int i = threadIdx.x; i <= n_active; i += kThreads) s_tiles[i] = a.tile_start[i];
     __syncthreads();
     const int total = s_tiles[n_active] * n_nt;
@@ -155,48 +172,55 @@ __global__ void __launch_bounds__(kThreads, 1) tcq_kernel(const __grid_constant_
     const int nk = a.K / KS;
 
     if (warp == kWarpMma) {
-        // ---------------- MMA issue (one thread) ----------------
-        if (lane == 0) {
-            long long i = 0;
-            for (int it = 0; it < n_units; ++it) {
-                const int acc = it & 1;
-                if (!mbar_wait(smem_u32(&bar_acc_empty[acc]), ((it >> 1) & 1) ^ 1, abort_flag, a.status)) break;
+        // ---------------- MMA issue: the warp runs the loop, one lane issues ----------------
+        // The scale warps arrive on bar_sf[s] only after the slot's TMA bytes
+        // landed (they wait on bar_full[s]), so one wait per stage covers both.
+        const uint32_t smem0 = smem_u32(smem);
+        int s = 0, t = 0;
+        uint32_t par = 0;
+        for (int it = 0; it < n_units; ++it) {
+            const int acc = it & 1;
+            if (!warp_wait(smem_u32(&bar_acc_empty[acc]), ((it >> 1) & 1) ^ 1, abort_flag, a.status)) break;
+            tc_fence_after();
+            const uint32_t d = tmem + acc * BN;
+            bool ok = true;
+            for (int kc = 0; kc < nk; ++kc) {
+                if (!warp_wait(smem_u32(&bar_sf[s]), par, abort_flag, a.status)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
-                const uint32_t d = tmem + acc * BN;
-                bool ok = true;
-                for (int kc = 0; kc < nk; ++kc, ++i) {
-                    const int s = (int)(i % S);
-                    const uint32_t par = (uint32_t)((i / S) & 1);
-                    if (!mbar_wait(smem_u32(&bar_full[s]), par, abort_flag, a.status) ||
-                        !mbar_wait(smem_u32(&bar_sf[s]), par, abort_flag, a.status)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t sa = smem_u32(smem + s * kStage);
-                    const uint64_t adesc = sdesc_sw128(sa), bdesc = sdesc_sw128(sa + kA);
-                    const uint32_t sf = tmem + kSfCol0 + s * kSfCols;
+                const uint32_t sa = smem0 + s * kStage;
+                const uint64_t adesc = sdesc_sw128(sa), bdesc = sdesc_sw128(sa + kA);
+                const uint32_t sf = tmem + kSfCol0 + t * kSfCols;
+                if (elect_one()) {
 #pragma unroll
                     for (int j = 0; j < KS / 64; ++j)
-                        mma_fp4(d, adesc + 2 * j, bdesc + 2 * j, sf + 4 * j, sf + 16 + 4 * j, (kc | j) != 0);
+                        mma_fp4(d, adesc + 2 * j, bdesc + 2 * j, sf + 4 * j, sf + kSfB + kSfBPerMma * j, (kc | j) != 0);
                     mma_commit(smem_u32(&bar_done[s]));
                 }
-                if (!ok) break;
-                mma_commit(smem_u32(&bar_acc_full[acc]));
+                __syncwarp();
+                if (++s == S) {
+                    s = 0;
+                    par ^= 1;
+                }
+                if (++t == kSfSlots) t = 0;
             }
+            if (!ok) break;
+            if (elect_one()) mma_commit(smem_u32(&bar_acc_full[acc]));
+            __syncwarp();
         }
-        __syncwarp();
     } else if (warp == kWarpTma) {
         // ---------------- operands by TMA (one thread) ----------------
         if (lane == 0) {
+            const void* mc1 = kPair ? (const void*)&a.tmap_wc[1] : (const void*)&a.tmap_wc[0];
+            const void* ms1 = kPair ? (const void*)&a.tmap_ws[1] : (const void*)&a.tmap_ws[0];
             long long i = 0;
             bool ok = true;
             for (int it = 0; it < n_units && ok; ++it) {
                 const int4 un = s_units[it];
                 const int y0 = un.x * a.N + un.w;
-                const int y1 = kPair ? y0 : y0 + BN / 2;
-                const void* mc1 = kPair ? (const void*)&a.tmap_wc[1] : (const void*)&a.tmap_wc[0];
-                const void* ms1 = kPair ? (const void*)&a.tmap_ws[1] : (const void*)&a.tmap_ws[0];
+                const int y1 = kPair ? y0 : y0 + BH;
                 for (int kc = 0; kc < nk; ++kc, ++i) {
                     if (!wait_done(bar_done, i - S, abort_flag, a.status)) {
                         ok = false;
@@ -228,32 +252,38 @@ __global__ void __launch_bounds__(kThreads, 1) tcq_kernel(const __grid_constant_
             for (int kc = 0; kc < nk; ++kc, ++i) {
                 if ((int)(i % kSfGroups) != grp) continue;
                 const int s = (int)(i % S);
+                // the scale slot i % 3 was last read by the MMAs of stage i - 3
                 if (!mbar_wait(smem_u32(&bar_full[s]), (uint32_t)((i / S) & 1), abort_flag, a.status) ||
-                    !wait_done(bar_done, i - S, abort_flag, a.status)) {
+                    !wait_done(bar_done, i - kSfSlots, abort_flag, a.status)) {
                     ok = false;
                     break;
                 }
                 const uint8_t* sc = smem + s * kStage + kA + kB;
                 const uint4 va = *reinterpret_cast<const uint4*>(sc + m * 16);
-                uint4 vb[4];
+                uint4 vb[BN / 32];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) vb[c] = *reinterpret_cast<const uint4*>(sc + kSA + (c * 32 + lane) * 16);
+                for (int c = 0; c < BN / 32; ++c) vb[c] = *reinterpret_cast<const uint4*>(sc + kSA + (c * 32 + lane) * 16);
                 // the slot is refilled by TMA (async proxy) once these MMAs are done
                 fence_proxy_async();
-                uint32_t ra[16], rb[16];
+                uint32_t ra[16], rb[16], rb2[8];
                 const uint32_t wa[4] = {va.x, va.y, va.z, va.w};
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
+                for (int j = 0; j < 4; ++j)
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        ra[4 * j + c] = wa[j];  // column 4j + quarter holds this row's MMA-j scales
+                    for (int c = 0; c < 4; ++c) ra[4 * j + c] = wa[j];  // column 4j + quarter holds this row's MMA-j scales
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+#pragma unroll
+                    for (int c = 0; c < BN / 32; ++c) {
+                        // column 6j + c holds row 32c + lane
                         const uint32_t wb[4] = {vb[c].x, vb[c].y, vb[c].z, vb[c].w};
-                        rb[4 * j + c] = wb[j];  // column 4j + c holds row 32c + lane
+                        const int k = (int)kSfBPerMma * j + c;
+                        if (k < 16) rb[k] = wb[j]; else rb2[k - 16] = wb[j];
                     }
-                }
-                const uint32_t col = kSfCol0 + s * kSfCols;
+                const uint32_t col = kSfCol0 + (uint32_t)(i % kSfSlots) * kSfCols;
                 tmem_st16(tq + col, ra);
-                tmem_st16(tq + col + 16, rb);
+                tmem_st16(tq + col + kSfB, rb);
+                tmem_st8(tq + col + kSfB + 16, rb2);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
@@ -285,12 +315,15 @@ __global__ void __launch_bounds__(kThreads, 1) tcq_kernel(const __grid_constant_
             tc_fence_after();
             const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + acc * BN;
             if constexpr (EPI == TCM_SWIGLU_Q) {
-                // h in 16-feature blocks, requantised to NVFP4 under hq_gs[e]
+                // h in 16-feature blocks, requantised to NVFP4 under hq_gs[e];
+                // each half of the warps takes 3 of the unit's 6 blocks
                 const float gs2 = a.hq_gs[un.x];
-                for (int cb = 2 * half; cb < 2 * half + 2; ++cb) {
+                for (int cb = 3 * half; cb < 3 * half + 3; ++cb) {
+                    const int f = un.w + cb * 16;
+                    if (f >= a.N) break;  // last unit of a row tile: features past ffn
                     uint32_t g[16], u[16];
                     tmem_ld16(tb + cb * 16, g);
-                    tmem_ld16(tb + BN / 2 + cb * 16, u);
+                    tmem_ld16(tb + BH + cb * 16, u);
                     tmem_ld_wait();
                     if (valid) {
                         float hv[16];
@@ -315,7 +348,6 @@ __global__ void __launch_bounds__(kThreads, 1) tcq_kernel(const __grid_constant_
                                 }
                             }
                         }
-                        const int f = un.w + cb * 16;
                         *reinterpret_cast<uint2*>(a.hq_out + (size_t)row * (a.N / 2) + f / 2) = make_uint2(q0, q1);
                         a.hs_out[(size_t)row * (a.N / 16) + f / 16] = (uint8_t)sbyte;
                     }
@@ -325,7 +357,8 @@ __global__ void __launch_bounds__(kThreads, 1) tcq_kernel(const __grid_constant_
                 // then one whole row (128 bytes) per store instruction
                 float* st = s_stage + (size_t)(half * 4 + q) * 32 * kStageRow;
                 const int nvalid = min(32, un.z - (un.y + q * 32));  // rows of this warp in the unit
-                for (int cb = 2 * half; cb < 2 * half + 2; ++cb) {
+                for (int cb = 3 * half; cb < 3 * half + 3; ++cb) {
+                    if (un.w + cb * 32 >= a.N) break;  // columns past the expert's rows
                     uint32_t r[32];
                     tmem_ld32(tb + cb * 32, r);
                     tmem_ld_wait();
@@ -338,7 +371,8 @@ __global__ void __launch_bounds__(kThreads, 1) tcq_kernel(const __grid_constant_
                     __syncwarp();
                 }
             } else {
-                for (int cb = 2 * half; cb < 2 * half + 2; ++cb) {
+                for (int cb = 3 * half; cb < 3 * half + 3; ++cb) {
+                    if (un.w + cb * 32 >= a.N) break;  // columns past the expert's rows
                     uint32_t r[32];
                     tmem_ld32(tb + cb * 32, r);
                     tmem_ld_wait();
@@ -414,7 +448,7 @@ void launch_tcq_t(const TcmArgs& a, int max_units, cudaStream_t s, const char* n
 }  // namespace
 
 bool tcq_supported(int epi, int N, int K) {
-    return K % KS == 0 && (epi == TCM_SWIGLU_Q ? N % (BN / 2) == 0 : N % BN == 0);
+    return K % KS == 0 && N > 0 && (epi == TCM_SWIGLU_Q ? N % 16 == 0 : N % 32 == 0);
 }
 
 bool tcq_set_maps(TcmArgs* a, const uint8_t* x_codes, const uint8_t* x_scales, long long rows_x, long long rows_w) {
@@ -423,13 +457,15 @@ bool tcq_set_maps(TcmArgs* a, const uint8_t* x_codes, const uint8_t* x_scales, l
         !encode_tmap_u8(&a->tmap_as, x_scales, K / 16, rows_x, KS / 16, BM, false))
         return false;
     for (int p = 0; p < 2; ++p)
-        if (!encode_tmap_u8(&a->tmap_wc[p], a->a_codes[p], K / 2, rows_w, KS / 2, BN / 2, true) ||
-            !encode_tmap_u8(&a->tmap_ws[p], a->a_scales[p], K / 16, rows_w, KS / 16, BN / 2, false))
+        if (!encode_tmap_u8(&a->tmap_wc[p], a->a_codes[p], K / 2, rows_w, KS / 2, BH, true) ||
+            !encode_tmap_u8(&a->tmap_ws[p], a->a_scales[p], K / 16, rows_w, KS / 16, BH, false))
             return false;
     return true;
 }
 
-void launch_tcq(int epi, const TcmArgs& a, int max_units, cudaStream_t s) {
+void launch_tcq(int epi, const TcmArgs& a, int max_tiles, cudaStream_t s) {
+    const int slice = epi == TCM_SWIGLU_Q ? BH : BN;
+    const int max_units = max_tiles * ((a.N + slice - 1) / slice);
     if (epi == TCM_SWIGLU_Q) return launch_tcq_t<TCM_SWIGLU_Q>(a, max_units, s, "tcq_gateup_w4a4");
     if (epi == TCM_COMBINE) return launch_tcq_t<TCM_COMBINE>(a, max_units, s, "tcq_down_w4a4");
     if (epi == TCM_ROWS) return launch_tcq_t<TCM_ROWS>(a, max_units, s, "tcq_down_w4a4");

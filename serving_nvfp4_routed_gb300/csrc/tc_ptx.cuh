@@ -156,6 +156,17 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 
 // The mbarrier receives one arrive once every tcgen05 op issued so far by
 // this thread has completed.
+// One lane of the (converged) warp gets true.  A loop that the whole warp
+// runs with warp-uniform values and whose tcgen05.mma / commit are issued by
+// the elected lane keeps its operands in uniform registers: measured on
+// GB300, the issue path of a single divergent lane costs ~20 cycles per MMA
+// more, which a 64-cycle FP4 MMA cannot hide.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred = 0;
+    asm volatile("{\n.reg .b32 r;\n.reg .pred p;\nelect.sync r|p, 0xffffffff;\nselp.u32 %0, 1, 0, p;\n}" : "=r"(pred));
+    return pred != 0;
+}
+
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
