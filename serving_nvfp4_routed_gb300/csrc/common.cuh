@@ -119,6 +119,19 @@ __device__ __forceinline__ uint32_t f32x8_to_e2m1x8(const float v[8]) {
     return r | sign;
 }
 
+// A quotient fl(v / d) for the e2m1 rounding that follows, given r = fl(1/d).
+// v * r (two roundings) is within 3 ulp of fl(v / d), so both give the same
+// e2m1 code unless the quotient lies within a few ulp of a number whose
+// significand is 1, 1.25, 1.5 or 1.75: a superset of the e2m1 rounding
+// boundaries (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5).  Only there (and for
+// inf / NaN, whose low significand bits are zero) is the correctly rounded
+// division taken, so the code is always that of fl(v / d).
+__device__ __forceinline__ float e2m1_quotient(float v, float d, float r) {
+    const float q = __fmul_rn(v, r);
+    if (((__float_as_uint(q) + 4u) & 0x1FFFFFu) <= 8u) return __fdiv_rn(v, d);
+    return q;
+}
+
 // Eight e2m1 codes (one 32-bit word, element 0 in the low nibble) -> four
 // f16x2 words, out[i] = (element 2i in the low half, element 2i+1 high).
 __device__ __forceinline__ void e2m1x8_to_f16x8(uint32_t w, uint32_t out[4]) {

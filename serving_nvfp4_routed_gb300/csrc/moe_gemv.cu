@@ -380,8 +380,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
                                 sbyte = f32_to_e4m3(sf);
                                 const float S = e4m3_to_f32(sbyte);
                                 if (S != 0.0f) {
-                                    const float den = __fmul_rn(S, gs2);
-                                    const uint32_t byte = e2m1x2_byte(__fdiv_rn(hv[0], den), __fdiv_rn(hv[1], den));
+                                    const float den = __fmul_rn(S, gs2), rden = __frcp_rn(den);
+                                    const uint32_t byte =
+                                        e2m1x2_byte(e2m1_quotient(hv[0], den, rden), e2m1_quotient(hv[1], den, rden));
                                     q[0] = byte & 0xFu;
                                     q[1] = byte >> 4;
                                 }

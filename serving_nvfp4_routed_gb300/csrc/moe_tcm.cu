@@ -308,11 +308,13 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant_
                             sbyte = f32_to_e4m3(__fdiv_rn(__fdiv_rn(m, 6.0f), gs2));
                             const float S = e4m3_to_f32(sbyte);
                             if (S != 0.0f) {
-                                const float den = __fmul_rn(S, gs2);
+                                const float den = __fmul_rn(S, gs2), rden = __frcp_rn(den);
 #pragma unroll
                                 for (int t = 0; t < 8; t += 2) {
-                                    q0 |= e2m1x2_byte(__fdiv_rn(hv[t], den), __fdiv_rn(hv[t + 1], den)) << (4 * t);
-                                    q1 |= e2m1x2_byte(__fdiv_rn(hv[8 + t], den), __fdiv_rn(hv[9 + t], den)) << (4 * t);
+                                    q0 |= e2m1x2_byte(e2m1_quotient(hv[t], den, rden),
+                                                      e2m1_quotient(hv[t + 1], den, rden)) << (4 * t);
+                                    q1 |= e2m1x2_byte(e2m1_quotient(hv[8 + t], den, rden),
+                                                      e2m1_quotient(hv[9 + t], den, rden)) << (4 * t);
                                 }
                             }
                         }

@@ -31,6 +31,10 @@
 //   A scales of row m, MMA j: lane m, column 4j + m/32 of the slot's area;
 //   B scales of row n, MMA j: lanes n%32 (every lane quarter), column
 //   16 + 6j + n/32.
+// Every scale address the MMA takes and every multi-column tcgen05.st here
+// starts on a multiple of 4 columns (B scales: of 2): a layout packing the A
+// scales at column j + m/32 (4-column stores at odd columns, MMA scale
+// addresses at odd columns) stopped with "misaligned address" on GB300.
 // Each 32-bit TMEM word holds the four block scales of one row and one MMA
 // (bytes = blocks in k order), which is the stored order of the scales.
 // One warp runs the MMA loop (one elected lane issues) into two 192-column
@@ -340,11 +344,13 @@ __global__ void __launch_bounds__(kThreads, 1) tcq_kernel(const __grid_constant_
                             sbyte = f32_to_e4m3(__fdiv_rn(__fdiv_rn(mx, 6.0f), gs2));
                             const float Sv = e4m3_to_f32(sbyte);
                             if (Sv != 0.0f) {
-                                const float den = __fmul_rn(Sv, gs2);
+                                const float den = __fmul_rn(Sv, gs2), rden = __frcp_rn(den);
 #pragma unroll
                                 for (int t = 0; t < 8; t += 2) {
-                                    q0 |= e2m1x2_byte(__fdiv_rn(hv[t], den), __fdiv_rn(hv[t + 1], den)) << (4 * t);
-                                    q1 |= e2m1x2_byte(__fdiv_rn(hv[8 + t], den), __fdiv_rn(hv[9 + t], den)) << (4 * t);
+                                    q0 |= e2m1x2_byte(e2m1_quotient(hv[t], den, rden),
+                                                      e2m1_quotient(hv[t + 1], den, rden)) << (4 * t);
+                                    q1 |= e2m1x2_byte(e2m1_quotient(hv[8 + t], den, rden),
+                                                      e2m1_quotient(hv[9 + t], den, rden)) << (4 * t);
                                 }
                             }
                         }

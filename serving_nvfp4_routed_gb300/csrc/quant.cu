@@ -57,29 +57,39 @@ __global__ void tensor_amax_kernel(const uint16_t* __restrict__ w, size_t n_per,
     }
 }
 
+// Scale byte of a 16-block with amax bam under the tensor scale gs, and the
+// block's divisor S * gs (0 when the block quantises to zero codes).
+__device__ __forceinline__ uint32_t block_scale(float bam, float gs, float& denom) {
+    denom = 0.0f;
+    if (!(gs > 0.0f)) return 0u;
+    const uint32_t sbyte = f32_to_e4m3(__fdiv_rn(__fdiv_rn(bam, 6.0f), gs));
+    const float S = e4m3_to_f32(sbyte);
+    if (S != 0.0f) denom = __fmul_rn(S, gs);
+    return sbyte;
+}
+
+// The e2m1 codes of 8 values of a block with divisor denom (packed, element 0
+// in the low nibble): code(fl(v / denom)).
+__device__ __forceinline__ uint32_t quant8(const float v[8], float denom) {
+    if (denom == 0.0f) return 0u;
+    const float r = __frcp_rn(denom);
+    float q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = e2m1_quotient(v[i], denom, r);
+    return f32x8_to_e2m1x8(q);
+}
+
 // Block quantisation of 8 values held by this thread, given the 16-block's
 // amax and the tensor scale gs.  Returns the 8 packed codes and the scale byte.
 __device__ __forceinline__ void quant_half_block(const float v[8], float bam, float gs, uint32_t& codes,
                                                  uint32_t& sbyte) {
-    sbyte = 0u;
-    codes = 0u;
-    if (gs > 0.0f) {
-        float sf = __fdiv_rn(__fdiv_rn(bam, 6.0f), gs);
-        sbyte = f32_to_e4m3(sf);
-        float S = e4m3_to_f32(sbyte);
-        if (S != 0.0f) {
-            float denom = __fmul_rn(S, gs);
-            float q[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) q[i] = __fdiv_rn(v[i], denom);
-            codes = f32x8_to_e2m1x8(q);
-        }
-    }
+    float denom;
+    sbyte = block_scale(bam, gs, denom);
+    codes = quant8(v, denom);
 }
 
-__device__ __forceinline__ void load_bf16x8(const uint16_t* p, float v[8], float& amax) {
-    uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
-    uint32_t ww[4] = {u.x, u.y, u.z, u.w};
+__device__ __forceinline__ void unpack_bf16x8(const uint4 u, float v[8], float& amax) {
+    const uint32_t ww[4] = {u.x, u.y, u.z, u.w};
     amax = 0.0f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -87,6 +97,10 @@ __device__ __forceinline__ void load_bf16x8(const uint16_t* p, float v[8], float
         v[2 * j + 1] = bf16_bits_to_f32(ww[j] >> 16);
         amax = fmaxf(amax, fmaxf(fabsf(v[2 * j]), fabsf(v[2 * j + 1])));
     }
+}
+
+__device__ __forceinline__ void load_bf16x8(const uint16_t* p, float v[8], float& amax) {
+    unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(p)), v, amax);
 }
 
 __global__ void quantize_weights_kernel(const uint16_t* __restrict__ w, size_t n_per, int batch,
@@ -154,10 +168,9 @@ __global__ void __launch_bounds__(kQaWarps * 32) quantize_act_kernel(
             float v0[8], v1[8], m0, m1;
             load_bf16x8(xr + (size_t)b * 16, v0, m0);
             load_bf16x8(xr + (size_t)b * 16 + 8, v1, m1);
-            const float bam = fmaxf(m0, m1);
-            uint32_t c0, c1, s0, s1;
-            quant_half_block(v0, bam, gs, c0, s0);
-            quant_half_block(v1, bam, gs, c1, s1);
+            float denom;
+            const uint32_t s0 = block_scale(fmaxf(m0, m1), gs, denom);
+            const uint32_t c0 = quant8(v0, denom), c1 = quant8(v1, denom);
             *reinterpret_cast<uint2*>(codes + (size_t)r * (K / 2) + (size_t)b * 8) = make_uint2(c0, c1);
             scales[(size_t)r * nb + b] = (uint8_t)s0;
         }

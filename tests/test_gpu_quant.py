@@ -99,3 +99,30 @@ def test_activation_quant_plain_rows(orc):
     oc, os_ = orc.quantize_rows(synth.bf16_bits(x), np.repeat(gs, 5))
     gc, gsc = lib.nvfp4_quantize_act(x, torch.from_numpy(gs).cuda())
     assert np.array_equal(gc.cpu().numpy(), oc) and np.array_equal(gsc.cpu().numpy(), os_)
+
+
+def test_activation_quant_quotients_near_every_boundary(orc):
+    """Blocks whose quotients x / (S * gs) fall exactly on each e2m1 rounding
+    boundary (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5) and within 1-4 fp32 ulp of
+    it on either side: row t uses gs = 2^-6 * (1 + (t - 4) * 2^-23), so the
+    kernel's reciprocal-multiply shortcut must defer to the exact quotient
+    there.  Codes and scales bit-exact against the oracle."""
+    E = T = 9
+    d = 256
+    base = np.array([6, .25, .75, 1.25, 1.75, 2.5, 3.5, 5, -.25, -.75, -1.25, -1.75, -2.5, -3.5, -5, -6])
+    blocks = [base * 2.0 ** j for j in (0, -1, -2, 1)]
+    row = np.concatenate([blocks[b % 4] for b in range(d // 16)]) * 2.0 ** -6
+    x64 = np.tile(row, (T, 1))
+    x = torch.from_numpy(x64).to(torch.bfloat16)
+    assert torch.equal(x.double(), torch.from_numpy(x64))
+    gs = np.array([2.0 ** -6 * (1 + (t - 4) * 2.0 ** -23) for t in range(T)], np.float32)
+    offs = np.arange(E + 1, dtype=np.int32)
+    rts = np.arange(T, dtype=np.int32)
+    oc, os_ = orc.quantize_rows(synth.bf16_bits(x), gs)
+    gc, gsc = lib.nvfp4_quantize_act(x.cuda(), torch.from_numpy(gs).cuda(), M=T,
+                                     row_to_slot=torch.from_numpy(rts).cuda(), top_k=1,
+                                     expert_offsets=torch.from_numpy(offs).cuda())
+    assert np.array_equal(gsc.cpu().numpy(), os_)
+    assert np.array_equal(gc.cpu().numpy(), oc)
+    # the rows differ: the quotients sit on both sides of the boundaries
+    assert len({bytes(oc[t]) for t in range(T)}) > 1
