@@ -506,7 +506,7 @@ int gemv_pick_group(int expected_tiles, int N, int ksplit, int nproj) {
     const int n_fb = N / (16 * (kWarps / ksplit));
     const long long want = 4LL * num_sms();  // keep about two items per resident CTA
     int g = 1;
-    for (int c = 2; c <= 4; c *= 2)
+    for (int c = 2; c <= 8; c *= 2)
         if ((long long)expected_tiles * ((n_fb + c - 1) / c) >= want) g = c;
     return g;
 }
