@@ -417,6 +417,58 @@ __global__ void rows_to_f16_kernel(const uint16_t* __restrict__ src, int rows, i
     grid_dep_launch();
 }
 
+// One warp per row for K <= 32 * 8 * kRowRegs: the row stays in registers
+// between its amax (a warp reduction) and its conversion, so it is read once
+// and no block barrier is needed.
+constexpr int kRowRegs = 16;  // 16-byte words per lane
+constexpr int kRowWarps = 8;
+
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float down) {
+    return f32x2_to_f16x2(bf16_bits_to_f32(w & 0xFFFFu) * down, bf16_bits_to_f32(w >> 16) * down);
+}
+
+__global__ void __launch_bounds__(kRowWarps * 32) rows_to_f16_warp_kernel(
+    const uint16_t* __restrict__ src, int rows, int K, uint16_t* __restrict__ dst, int32_t* __restrict__ exps,
+    float* __restrict__ zero_rows, int zero_len, const int32_t* __restrict__ map, int map_div, int zero_count) {
+    grid_dep_wait();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nw = K / 8;  // 16-byte words per row
+    for (int r = blockIdx.x * kRowWarps + warp; r < rows; r += gridDim.x * kRowWarps) {
+        const int sr = map ? map[r] / map_div : r;
+        const uint4* s4 = reinterpret_cast<const uint4*>(src + (size_t)sr * K);
+        uint4 u[kRowRegs];
+        float m = 0.0f;
+#pragma unroll
+        for (int j = 0; j < kRowRegs; ++j) {
+            const int i = lane + 32 * j;
+            if (i < nw) {
+                u[j] = __ldg(s4 + i);
+                const uint32_t ww[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    m = fmaxf(m, fmaxf(fabsf(bf16_bits_to_f32(ww[q] & 0xFFFFu)), fabsf(bf16_bits_to_f32(ww[q] >> 16))));
+            }
+        }
+        m = warp_max(m);
+        const int sexp = row_exponent(m);
+        const float down = exp2i(-sexp);
+        if (lane == 0) exps[r] = sexp;
+        uint4* d4 = reinterpret_cast<uint4*>(dst + (size_t)r * K);
+#pragma unroll
+        for (int j = 0; j < kRowRegs; ++j) {
+            const int i = lane + 32 * j;
+            if (i < nw)
+                d4[i] = make_uint4(bf16x2_to_f16x2_scaled(u[j].x, down), bf16x2_to_f16x2_scaled(u[j].y, down),
+                                   bf16x2_to_f16x2_scaled(u[j].z, down), bf16x2_to_f16x2_scaled(u[j].w, down));
+        }
+        if (zero_rows && r < zero_count) {
+            float4* z = reinterpret_cast<float4*>(zero_rows + (size_t)r * zero_len);
+            for (int i = lane; i < zero_len / 4; i += 32) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    grid_dep_launch();
+}
+
 __global__ void acc_to_bf16_kernel(const float* __restrict__ acc, size_t n4, uint16_t* __restrict__ out) {
     grid_dep_wait();
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
@@ -443,6 +495,13 @@ void launch_rows_to_f16(const uint16_t* src, int rows, int K, uint16_t* dst, int
                         int zero_len, cudaStream_t s, const int32_t* map, int map_div, int zero_count) {
     if (rows <= 0) return;
     if (zero_count < 0) zero_count = rows;
+    if (K <= 32 * 8 * kRowRegs) {
+        const int grid = std::min((rows + kRowWarps - 1) / kRowWarps, num_sms() * 8);
+        NVFP4_LAUNCH("rows_to_f16", s,
+                     launch_pdl(rows_to_f16_warp_kernel, dim3(grid), dim3(kRowWarps * 32), 0, s, src, rows, K, dst,
+                                exps, zero_rows, zero_len, map, map_div, zero_count));
+        return;
+    }
     const int grid = std::min(rows, num_sms() * 8);
     NVFP4_LAUNCH("rows_to_f16", s,
                  launch_pdl(rows_to_f16_kernel, dim3(grid), dim3(256), 0, s, src, rows, K, dst, exps, zero_rows,
