@@ -24,7 +24,7 @@ namespace nvfp4 {
 namespace {
 
 constexpr int kSmallMaxRows = 8192;
-constexpr int kChunkRows = 8192;   // rows per block in the multi-block path
+constexpr int kChunkRows = 1024;   // rows per block in the multi-block path (one scatter round)
 
 template <int MAXL>
 __device__ void warp_topk(const float* __restrict__ lg, int E, int k, int32_t* __restrict__ ids,
@@ -254,10 +254,16 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int nb, int E, int32_t*
     const int e = threadIdx.x;
     int run = 0;
     if (e < E) {
-        for (int b = 0; b < nb; ++b) {
-            int c = counts[(size_t)b * E + e];
-            counts[(size_t)b * E + e] = run;
-            run += c;
+        for (int b0 = 0; b0 < nb; b0 += 8) {  // eight chunks' loads in flight
+            int c[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) c[j] = b0 + j < nb ? counts[(size_t)(b0 + j) * E + e] : 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (b0 + j < nb) {
+                    counts[(size_t)(b0 + j) * E + e] = run;
+                    run += c[j];
+                }
         }
     }
     int off;
