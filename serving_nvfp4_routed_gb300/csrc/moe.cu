@@ -95,6 +95,7 @@ MoeWs carve_moe(void* base, int T, int E, int k, int d, int F, int mode, size_t*
             w.xp_exp = c.take<int32_t>(R + 1);
             w.hh = c.take<uint16_t>(R * F);
             w.h_exp = c.take<int32_t>(R + 1);
+            if (tcm_supported(TCM_ROWS, d, F)) w.yrows = c.take<float>(R * d);
         }
     } else {
         w.xq = c.take<uint8_t>(R * (d / 2));
@@ -222,8 +223,12 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
     }
 
     if (use_tc(mode, T, E, top_k, d, F)) {
+        // the down projection writes w * y rows (summed per token in slot order
+        // afterwards) when the prompt-shaped kernel takes it, else it adds into
+        // a zeroed fp32 accumulator
+        const bool rows = ws.yrows != nullptr && tcm_supported(TCM_ROWS, d, F);
         // x -> f16 rows in expert order (and zero the combine accumulator)
-        launch_rows_to_f16(x, R, d, ws.xp, ws.xp_exp, ws.acc, d, s, ws.ra.row_to_slot, top_k, T);
+        launch_rows_to_f16(x, R, d, ws.xp, ws.xp_exp, rows ? nullptr : ws.acc, d, s, ws.ra.row_to_slot, top_k, T);
         const int max_tiles = R / kTcTokTile + std::min(E, R) + 1;
         // gate/up + SwiGLU -> h (bf16)
         TcmArgs g{};
@@ -274,12 +279,17 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
             u.a_codes[1] = u.a_codes[0];   u.a_scales[1] = u.a_scales[0];   u.a_ws2[1] = u.a_ws2[0];
             u.x_exp = ws.h_exp;
             u.h_out = nullptr;
-            u.acc_out = ws.acc;
+            u.acc_out = rows ? nullptr : ws.acc;
+            u.y_rows = rows ? ws.yrows : nullptr;
             u.row_to_slot = ws.ra.row_to_slot;
             u.topk_w = ws.ra.w;
             if (!make_tmap_rows_f16(&u.tmap_x, ws.hh, R, F) || !tcm_set_weights(&u, (long long)E * d))
                 return NVFP4_ERR_CUDA;
-            launch_tcm(TCM_COMBINE, 0, u, max_tiles * (d / 256), s);
+            launch_tcm(rows ? TCM_ROWS : TCM_COMBINE, 0, u, max_tiles * (d / 256), s);
+            if (rows) {
+                launch_sum_rows(ws.yrows, ws.ra.slot_to_row, T, top_k, d, out, s);
+                return last_launch_status();
+            }
         } else {
             TcArgs u{};
             u.top_k = top_k;

@@ -76,8 +76,11 @@ struct Geo {
     static constexpr int SD = SD0 > kGroups ? SD0 : kGroups;
     static constexpr int kRaw = kRawB + (AQ ? kRawA : 0);
     static constexpr int kSc = kScB + (AQ ? kScA : 0);
+    // fp32 row staging of the TCM_ROWS epilogue: 4 warps x 32 rows x 33 floats
+    static constexpr int kStaging = AQ ? 0 : 4 * 32 * 33 * 4;
     static constexpr int kSmem =
-        1024 + SA * kABytes + SB * kBBytes + SR * kRaw + SS * kSc + kMaxUnits * 16 + kTileCopy * 4;
+        1024 + SA * kABytes + SB * kBBytes + SR * kRaw + SS * kSc + kMaxUnits * 16 + kTileCopy * 4 + kStaging;
+    static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
 constexpr int kWarps = 24;
 constexpr int kThreads = kWarps * 32;
@@ -105,6 +108,7 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant_
     uint8_t* ring_s = ring_r + SR * kRaw;
     int4* s_units = reinterpret_cast<int4*>(ring_s + SS * kSc);  // {e, row0, row_end, f0}
     int* s_tiles = reinterpret_cast<int*>(s_units + kMaxUnits);
+    float* s_stage = reinterpret_cast<float*>(s_tiles + kTileCopy);  // [4 warps][32][33] (TCM_ROWS)
     __shared__ __align__(8) uint64_t bar_afull[SA], bar_bfull[SB], bar_done[SD], bar_acc_full[2], bar_acc_empty[2];
     __shared__ __align__(8) uint64_t bar_rfull[SR], bar_rempty[SR], bar_sfull[SS], bar_sempty[SS];
     __shared__ uint32_t s_tmem;
@@ -275,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant_
             size_t tok = 0;
             if (valid) {
                 rs = AQ ? a.x_gs[un.x] : exp2i(a.x_exp[row]);
-                if constexpr (EPI == TCM_COMBINE) {
+                if constexpr (EPI == TCM_COMBINE || EPI == TCM_ROWS) {
                     const int slot = a.row_to_slot[row];
                     tok = (size_t)(slot / a.top_k);
                     wt = a.topk_w[slot];
@@ -347,6 +351,25 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant_
                         dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
                         dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
                     }
+                }
+            } else if constexpr (EPI == TCM_ROWS) {
+                // w * y as fp32 rows by routed row: 32 rows x 32 columns per
+                // chunk through shared memory, then one whole row (128 bytes)
+                // per store instruction; a second kernel sums each token's rows
+                // in slot order (deterministic combine)
+                float* st = s_stage + (size_t)q * 32 * 33;
+                const int nvalid = min(32, un.z - (un.y + q * 32));  // rows of this warp in the unit
+                for (int cb = 0; cb < BN / 32; ++cb) {
+                    uint32_t r[32];
+                    tmem_ld32(tb + cb * 32, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        st[lane * 33 + c] = wt * __fmul_rn(__fmul_rn(__uint_as_float(r[c]), rs), w0);
+                    __syncwarp();
+                    float* ybase = a.y_rows + (size_t)(un.y + q * 32) * a.N + un.w + cb * 32 + lane;
+                    for (int j = 0; j < nvalid; ++j) ybase[(size_t)j * a.N] = st[j * 33 + lane];
+                    __syncwarp();
                 }
             } else {
                 for (int cb = 0; cb < BN / 32; ++cb) {
@@ -588,6 +611,7 @@ void launch_tcm(int epi, int a_nvfp4, const TcmArgs& a, int max_units, cudaStrea
     }
     if (epi == TCM_SWIGLU) return launch_tcm_t<TCM_SWIGLU, 0>(a, max_units, s, "tcm_gateup_w4a16");
     if (epi == TCM_COMBINE) return launch_tcm_t<TCM_COMBINE, 0>(a, max_units, s, "tcm_down_w4a16");
+    if (epi == TCM_ROWS) return launch_tcm_t<TCM_ROWS, 0>(a, max_units, s, "tcm_down_w4a16");
     if (epi == TCM_BF16) return launch_tcm_t<TCM_BF16, 0>(a, max_units, s, "tcm_linear_w4a16");
 }
 
