@@ -324,6 +324,36 @@ def time_steps(layer, steps, flush, start=0):
     return [a.elapsed_time(b) for a, b in evs]
 
 
+def time_router(layer, steps, flush):
+    """The BF16 router GEMM for the workload's tokens (d -> E logits), timed
+    like the layer (CUDA events per call, L2 flushed between calls).  It is
+    the step before the layer and reported beside it, not inside `value`:
+    the metric takes the router's logits as given."""
+    s = layer.shape
+    dev = layer.device
+    w = synth.make_weights(1, s.E, s.d, 777, dev)[0]
+    out = torch.empty(s.T, s.E, dtype=torch.float32, device=dev)
+    x = layer.batches[0][0]
+    for _ in range(3):
+        layer.lib.moe_router_logits(x, w, out=out)
+    stream = torch.cuda.current_stream()
+    ts = []
+    for i in range(steps):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        layer.lib.moe_router_logits(x, w, out=out)
+        b.record(stream)
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ts)
+    flops = 2.0 * s.T * s.d * s.E
+    nbytes = s.T * s.d * 2 + s.E * s.d * 2 + s.T * s.E * 4
+    return {"ms_per_call": ms, "tflops": flops / (ms / 1e3) / 1e12, "gbs": nbytes / (ms / 1e3) / 1e9,
+            "T": s.T, "d": s.d, "E": s.E}
+
+
 def time_e2e(layer, steps, flush):
     """Same metric with host buffers: pinned H2D of x and logits, the layer,
     D2H of the output, all inside the timed events."""
@@ -513,6 +543,7 @@ def run_ours(args):
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},
         "gpu_launches": launches,
+        "router_gemm": time_router(layer, max(3, args.steps), flush) if layer.kind != "dense" else None,
         "clocks": clk.summary(),
     }
     if args.sweep and args.workload == "decode64":

@@ -138,11 +138,26 @@ nvfp4_status nvfp4_quantize_act(const uint16_t* x_bf16, int M, int K,
                                 uint8_t* codes, uint8_t* scales, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * moe_router_logits -- the BF16 router GEMM in front of routing
+ * (TensorFold #308 "The checkpoint": the router is BF16, not NVFP4):
+ *   logits[t, e] = sum_k x[t, k] * w_router[e, k]     (fp32)
+ *   x_bf16 [T, d], w_router_bf16 [E, d], logits [T, E], all row-major,
+ *   device pointers owned by the caller, 16-byte aligned.
+ * Every bf16 product is exact in fp32; the k-sum is fp32 (tensor cores),
+ * so |logits - exact| <= d * 2^-24 * sum_k |x[t,k] w[e,k]|.
+ * d % 64 == 0, 1 <= E <= 512; T == 0 is a no-op.  d_status (nullable)
+ * receives NVFP4_ERR_TIMEOUT if a bounded wait expired.  Asynchronous on
+ * the stream; returns NVFP4_ERR_* for bad arguments before any launch.
+ * --------------------------------------------------------------------- */
+nvfp4_status moe_router_logits(const uint16_t* x_bf16, int T, int d, const uint16_t* w_router_bf16,
+                               int E, float* logits, int32_t* d_status, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * moe_route_permute -- the BF16 router's logits to expert-contiguous rows
  * (TensorFold #308: router BF16, routed experts through one grouped
  * kernel).  Per token t: softmax over the E logits, the top_k experts in
  * descending order (ties -> lower expert id), and their weights
- * renormalised over the chosen top_k (computed in fp64, stored fp32):
+ * renormalised over the chosen top_k (exp and the division in fp32):
  *   topk_ids [T, top_k] int32, topk_w [T, top_k] fp32.
  * Then a stable permutation of the R = T*top_k (token, slot) pairs by
  * expert (order: expert, token, slot):

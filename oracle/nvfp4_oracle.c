@@ -222,6 +222,29 @@ void orc_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t N, int6
 }
 
 /* ------------------------------------------------------------------ */
+/* Router GEMM ([TF308] "The checkpoint": the router is BF16):          */
+/*   logits[t][e] = sum_k x[t][k] * w[e][k]                             */
+/* as an fp64 loop in k order (every bf16 product is exact in fp64),    */
+/* and abs_sum[t][e] = sum_k |x[t][k] * w[e][k]|, the scale of the      */
+/* error bound of any fp32 evaluation of the same sum.                  */
+/* ------------------------------------------------------------------ */
+void orc_router_logits(const uint16_t* x, int64_t T, int64_t d, const uint16_t* w, int64_t E,
+                       double* logits, double* abs_sum) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t e = 0; e < E; ++e) {
+            double s = 0.0, a = 0.0;
+            for (int64_t k = 0; k < d; ++k) {
+                const double p = (double)bf16_bits_to_float(x[t * d + k]) * (double)bf16_bits_to_float(w[e * d + k]);
+                s += p;
+                a += fabs(p);
+            }
+            logits[t * E + e] = s;
+            abs_sum[t * E + e] = a;
+        }
+}
+
+/* ------------------------------------------------------------------ */
 /* Routing: softmax over E logits, top-k descending (ties -> lower      */
 /* expert id), weights renormalised over the k chosen:                  */
 /*   w_j = exp(l_j - l_max) / sum_{i in top-k} exp(l_i - l_max)         */

@@ -61,6 +61,7 @@ def bind(L):
     L.orc_quantize_rows.argtypes = [vp, i64, i64, vp, vp, vp]
     L.orc_dequantize.argtypes = [vp, vp, i64, i64, vp]
     L.orc_route.argtypes = [vp, i64, i32, i32, vp, vp, vp, vp, vp]
+    L.orc_router_logits.argtypes = [vp, i64, i64, vp, i64, vp, vp]
     L.orc_moe_layer.argtypes = [i32, vp, i64, i64, i64, i32, i32, vp, vp,
                                 vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                 vp, vp, vp, i64, vp, vp]
@@ -155,6 +156,19 @@ def dequantize(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
 # --------------------------------------------------------------------------
 # routing
 # --------------------------------------------------------------------------
+def router_logits(x_bf16_bits: np.ndarray, w_bf16_bits: np.ndarray):
+    """fp64 logits [T, E] = x @ w^T of bf16 bit patterns x [T, d], w [E, d],
+    and sum_k |x w| per element (the error-bound scale of an fp32 sum)."""
+    x = _c(x_bf16_bits, np.uint16)
+    w = _c(w_bf16_bits, np.uint16)
+    T, d = x.shape
+    E = w.shape[0]
+    out = np.zeros((T, E), np.float64)
+    absum = np.zeros((T, E), np.float64)
+    lib().orc_router_logits(_ptr(x), T, d, _ptr(w), E, _ptr(out), _ptr(absum))
+    return out, absum
+
+
 def route(logits: np.ndarray, top_k: int):
     """Softmax/top-k/renormalise, then the stable permutation by expert.
 

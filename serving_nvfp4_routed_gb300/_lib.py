@@ -27,7 +27,7 @@ EXPORTS = ("nvfp4_quantize_weights", "nvfp4_quantize_weights_workspace_size", "n
            "nvfp4_moe_workspace_size", "nvfp4_moe_workspace_views", "nvfp4_linear",
            "nvfp4_linear_workspace_size", "nvfp4_status_string", "nvfp4_launch_count",
            "nvfp4_profile_enable", "nvfp4_profile_collect", "nvfp4_quantize_weights_noalloc",
-           "nvfp4_quantize_weights_noalloc_max_batch", "nvfp4_selftest_bounded_wait")
+           "nvfp4_quantize_weights_noalloc_max_batch", "nvfp4_selftest_bounded_wait", "moe_router_logits")
 
 
 class Nvfp4Error(RuntimeError):
@@ -80,6 +80,7 @@ def load(path: str = LIB_PATH):
         L.nvfp4_status_string.restype = ctypes.c_char_p
         L.nvfp4_launch_count.restype = ctypes.c_uint64
         L.nvfp4_selftest_bounded_wait.argtypes = [vp, vp]
+        L.moe_router_logits.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp]
         L.nvfp4_profile_enable.argtypes = [i32]
         L.nvfp4_profile_collect.argtypes = [i32, ctypes.c_char_p, ctypes.POINTER(i32),
                                             ctypes.POINTER(ctypes.c_double)]
@@ -183,6 +184,21 @@ def nvfp4_quantize_act(x: torch.Tensor, input_scale: torch.Tensor, M: int | None
            L.nvfp4_quantize_act(_p(x.view(torch.int16)), M, K, _p(row_to_slot), top_k, _p(input_scale),
                                 _p(expert_offsets), E, _p(codes), _p(scales), _stream(stream)))
     return codes, scales
+
+
+def moe_router_logits(x: torch.Tensor, w_router: torch.Tensor, out=None, d_status=None, stream=None) -> torch.Tensor:
+    """fp32 logits [T, E] = x [T, d] (bf16) @ w_router [E, d] (bf16)^T."""
+    L = load()
+    _cuda(x, w_router)
+    x, w_router = x.contiguous(), w_router.contiguous()
+    T, d = x.shape
+    E = w_router.shape[0]
+    if out is None:
+        out = _empty((T, E), torch.float32, x.device)
+    _check("moe_router_logits",
+           L.moe_router_logits(_p(x), T, d, _p(w_router), E, _p(out), _p(d_status) if d_status is not None else None,
+                               _stream(stream)))
+    return out
 
 
 def moe_route_permute(logits: torch.Tensor, top_k: int, stream=None) -> dict:

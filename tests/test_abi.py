@@ -94,6 +94,12 @@ def test_other_host_validation(L):
     assert L.moe_route_permute(p, 4, 8, 9, p, p, p, p, p, p, big, None) == 2
     assert L.moe_route_permute(p, 4, 2000, 8, p, p, p, p, p, p, big, None) == 2
     assert L.moe_route_permute(p, 4, 8, 2, p, p, p, p, p, p, 0, None) == 4
+    assert L.moe_router_logits(p, 4, 100, p, 8, p, None, None) == 2  # d % 64
+    assert L.moe_router_logits(p, 4, 128, p, 600, p, None, None) == 2  # E > 512
+    assert L.moe_router_logits(p, -1, 128, p, 8, p, None, None) == 1
+    assert L.moe_router_logits(None, 4, 128, p, 8, p, None, None) == 1
+    assert L.moe_router_logits(_fake(0x10004), 4, 128, p, 8, p, None, None) == 3
+    assert L.moe_router_logits(p, 0, 128, p, 8, p, None, None) == 0  # no-op
     w = _lib._W(0x20000, 0x20000, 0x20000)
     assert L.nvfp4_linear(p, 4, 96, ctypes.byref(w), 16, None, p, p, big, None) == 2
     assert L.nvfp4_linear(p, 4, 64, ctypes.byref(w), 24, None, p, p, big, None) == 2
