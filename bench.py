@@ -354,6 +354,38 @@ def time_router(layer, steps, flush):
             "T": s.T, "d": s.d, "E": s.E}
 
 
+def time_shared(layer, steps, flush):
+    """The BF16 shared-expert MLP for the workload's tokens (ffn taken equal
+    to the routed experts': the pages give none), added into the layer's
+    output buffer; CUDA events per call, L2 flushed between calls.  Reported
+    beside the layer line, not inside `value`."""
+    s = layer.shape
+    dev = layer.device
+    Fs = s.F
+    wg, wu = (synth.make_weights(1, Fs, s.d, 779 + i, dev)[0] for i in range(2))
+    wd = synth.make_weights(1, s.d, Fs, 781, dev)[0]
+    x = layer.batches[0][0]
+    out = torch.zeros(s.T, s.d, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(max(16, layer.lib.load().moe_shared_expert_workspace_size(s.T, Fs)), dtype=torch.uint8,
+                     device=dev)
+    for _ in range(3):
+        layer.lib.moe_shared_expert(x, wg, wu, wd, out, ws=ws)
+    stream = torch.cuda.current_stream()
+    ts = []
+    for i in range(steps):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        layer.lib.moe_shared_expert(x, wg, wu, wd, out, ws=ws)
+        b.record(stream)
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ts)
+    flops = 2.0 * s.T * s.d * Fs * 3
+    return {"ms_per_call": ms, "tflops": flops / (ms / 1e3) / 1e12, "T": s.T, "d": s.d, "ffn": Fs}
+
+
 def time_recipe(layer, flush, reps=3):
     """The ModelOpt weight recipe (a load-time step, not inside `value`) on
     one projection bank of the workload, [E, ffn, d] bf16: CUDA events per
@@ -559,6 +591,9 @@ def run_ours(args):
                  "layer_frac_bf16": layer_tflops / bf16, "touched_experts": touched})
 
     recipe = time_recipe(layer, flush) if layer.kind != "dense" else None
+    shared = time_shared(layer, max(3, args.steps), flush) if layer.kind != "dense" else None
+    if shared:
+        shared["frac_bf16"] = shared["tflops"] / bf16
     if recipe:
         recipe["frac_hbm"] = recipe["gbs"] / hbm
     line = {
@@ -578,6 +613,7 @@ def run_ours(args):
         "gpu_launches": launches,
         "router_gemm": time_router(layer, max(3, args.steps), flush) if layer.kind != "dense" else None,
         "weight_recipe": recipe,
+        "shared_expert": shared,
         "clocks": clk.summary(),
     }
     if args.sweep and args.workload == "decode64":

@@ -153,6 +153,26 @@ nvfp4_status moe_router_logits(const uint16_t* x_bf16, int T, int d, const uint1
                                int E, float* logits, int32_t* d_status, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * moe_shared_expert -- the BF16 shared-expert MLP after the routed layer
+ * (TensorFold #308 "The checkpoint": the shared expert is BF16, next to the
+ * NVFP4 routed experts).  For every token t:
+ *   G = bf16(x Wg^T)   U = bf16(x Wu^T)   h = bf16(silu(G) * U)
+ *   out[t] = bf16(out[t] + h Wd^T)          (fp32 sums; out holds the
+ *                                            routed layer's bf16 result)
+ *   x_bf16 [T, d], w_gate_bf16 / w_up_bf16 [Fs, d], w_down_bf16 [d, Fs],
+ *   out_bf16 [T, d] read and written; row-major device pointers owned by
+ *   the caller, 16-byte aligned.  d % 256 == 0, Fs % 128 == 0.
+ *   ws: at least moe_shared_expert_workspace_size(T, Fs) bytes (h).
+ * Tensor cores (tcgen05, bf16 operands by TMA).  T == 0 is a no-op;
+ * d_status (nullable) receives NVFP4_ERR_TIMEOUT if a bounded wait expired.
+ * --------------------------------------------------------------------- */
+nvfp4_status moe_shared_expert(const uint16_t* x_bf16, int T, int d, const uint16_t* w_gate_bf16,
+                               const uint16_t* w_up_bf16, const uint16_t* w_down_bf16, int Fs,
+                               uint16_t* out_bf16, void* ws, size_t ws_bytes, int32_t* d_status,
+                               cudaStream_t stream);
+size_t moe_shared_expert_workspace_size(int T, int Fs);
+
+/* ------------------------------------------------------------------------
  * moe_route_permute -- the BF16 router's logits to expert-contiguous rows
  * (TensorFold #308: router BF16, routed experts through one grouped
  * kernel).  Per token t: softmax over the E logits, the top_k experts in

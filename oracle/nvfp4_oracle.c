@@ -399,6 +399,42 @@ void orc_moe_layer(int mode, const uint16_t* x, int64_t T, int64_t d, int64_t F,
 }
 
 /*
+ * BF16 shared-expert MLP after the weighted combine (the pages name the
+ * shared expert as BF16 next to the NVFP4 routed experts; the math is the
+ * plainest reading, with the routed layer's rounding points):
+ *   G = bf16(sum x*wg)   U = bf16(sum x*wu)   h = bf16(silu(G) * U)
+ *   out = bf16(routed + sum h*wd)
+ * x [T, d], wg, wu [Fs, d], wd [d, Fs], routed/out [T, d] (bf16 bits);
+ * fp64 sums in k order.
+ */
+void orc_shared_expert(const uint16_t* x, int64_t T, int64_t d, const uint16_t* wg, const uint16_t* wu,
+                       const uint16_t* wd, int64_t Fs, const uint16_t* routed, float* out) {
+#pragma omp parallel
+    {
+        double* h = (double*)malloc(sizeof(double) * (size_t)Fs);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t t = 0; t < T; ++t) {
+            for (int64_t f = 0; f < Fs; ++f) {
+                double g = 0.0, u = 0.0;
+                for (int64_t k = 0; k < d; ++k) {
+                    const double xv = bf16_bits_to_float(x[t * d + k]);
+                    g += xv * bf16_bits_to_float(wg[f * d + k]);
+                    u += xv * bf16_bits_to_float(wu[f * d + k]);
+                }
+                const double G = orc_round_bf16(g), U = orc_round_bf16(u);
+                h[f] = orc_round_bf16(silu(G) * U);
+            }
+            for (int64_t n = 0; n < d; ++n) {
+                double y = 0.0;
+                for (int64_t f = 0; f < Fs; ++f) y += h[f] * bf16_bits_to_float(wd[n * Fs + f]);
+                out[t * d + n] = (float)orc_round_bf16((double)bf16_bits_to_float(routed[t * d + n]) + y);
+            }
+        }
+        free(h);
+    }
+}
+
+/*
  * Dense NVFP4 linear over the bf16 rows x [M, K] (the dense MLP runs on it,
  * gate and up apart because their tensor scales differ).
  * Without w_up:  out = bf16(ws2 * sum x*w)                     [M, N]

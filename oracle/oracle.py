@@ -62,6 +62,7 @@ def bind(L):
     L.orc_dequantize.argtypes = [vp, vp, i64, i64, vp]
     L.orc_route.argtypes = [vp, i64, i32, i32, vp, vp, vp, vp, vp]
     L.orc_router_logits.argtypes = [vp, i64, i64, vp, i64, vp, vp]
+    L.orc_shared_expert.argtypes = [vp, i64, i64, vp, vp, vp, i64, vp, vp]
     L.orc_moe_layer.argtypes = [i32, vp, i64, i64, i64, i32, i32, vp, vp,
                                 vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                 vp, vp, vp, i64, vp, vp]
@@ -225,6 +226,19 @@ def moe_layer(mode: str, x_bf16_bits, ids, w, bank, tokens=None, is13=None, is2=
                         _ptr(is13) if m == 1 else None, _ptr(is2) if m == 1 else None,
                         _ptr(tokens), n, _ptr(out), _ptr(h))
     return (out, h) if want_h else out
+
+
+def shared_expert(x_bf16_bits, wg_bits, wu_bits, wd_bits, routed_bf16_bits):
+    """BF16 shared-expert MLP added to the routed output, fp32 [T, d] of
+    bf16 values: bf16(routed + bf16(silu(bf16 xWg^T) * bf16 xWu^T) Wd^T)."""
+    x = _c(x_bf16_bits, np.uint16)
+    wg, wu, wd = (_c(w, np.uint16) for w in (wg_bits, wu_bits, wd_bits))
+    r = _c(routed_bf16_bits, np.uint16)
+    T, d = x.shape
+    Fs = wg.shape[0]
+    out = np.zeros((T, d), np.float32)
+    lib().orc_shared_expert(_ptr(x), T, d, _ptr(wg), _ptr(wu), _ptr(wd), Fs, _ptr(r), _ptr(out))
+    return out
 
 
 def linear(x_bf16_bits, wq, ws, ws2, wup=None):

@@ -27,7 +27,8 @@ EXPORTS = ("nvfp4_quantize_weights", "nvfp4_quantize_weights_workspace_size", "n
            "nvfp4_moe_workspace_size", "nvfp4_moe_workspace_views", "nvfp4_linear",
            "nvfp4_linear_workspace_size", "nvfp4_status_string", "nvfp4_launch_count",
            "nvfp4_profile_enable", "nvfp4_profile_collect", "nvfp4_quantize_weights_noalloc",
-           "nvfp4_quantize_weights_noalloc_max_batch", "nvfp4_selftest_bounded_wait", "moe_router_logits")
+           "nvfp4_quantize_weights_noalloc_max_batch", "nvfp4_selftest_bounded_wait", "moe_router_logits",
+           "moe_shared_expert", "moe_shared_expert_workspace_size")
 
 
 class Nvfp4Error(RuntimeError):
@@ -81,6 +82,9 @@ def load(path: str = LIB_PATH):
         L.nvfp4_launch_count.restype = ctypes.c_uint64
         L.nvfp4_selftest_bounded_wait.argtypes = [vp, vp]
         L.moe_router_logits.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp]
+        L.moe_shared_expert.argtypes = [vp, i32, i32, vp, vp, vp, i32, vp, vp, sz, vp, vp]
+        L.moe_shared_expert_workspace_size.argtypes = [i32, i32]
+        L.moe_shared_expert_workspace_size.restype = sz
         L.nvfp4_profile_enable.argtypes = [i32]
         L.nvfp4_profile_collect.argtypes = [i32, ctypes.c_char_p, ctypes.POINTER(i32),
                                             ctypes.POINTER(ctypes.c_double)]
@@ -198,6 +202,25 @@ def moe_router_logits(x: torch.Tensor, w_router: torch.Tensor, out=None, d_statu
     _check("moe_router_logits",
            L.moe_router_logits(_p(x), T, d, _p(w_router), E, _p(out), _p(d_status) if d_status is not None else None,
                                _stream(stream)))
+    return out
+
+
+def moe_shared_expert(x: torch.Tensor, w_gate: torch.Tensor, w_up: torch.Tensor, w_down: torch.Tensor,
+                      out: torch.Tensor, ws=None, d_status=None, stream=None) -> torch.Tensor:
+    """out[T, d] (bf16, the routed layer's result) += the BF16 shared-expert
+    MLP of x [T, d]: bf16(silu(bf16 x Wg^T) * bf16 x Wu^T) Wd^T, in place."""
+    L = load()
+    _cuda(x, w_gate, w_up, w_down, out)
+    x, w_gate, w_up, w_down = (t.contiguous() for t in (x, w_gate, w_up, w_down))
+    assert out.is_contiguous()
+    T, d = x.shape
+    Fs = w_gate.shape[0]
+    wsb = L.moe_shared_expert_workspace_size(T, Fs)
+    if ws is None:
+        ws = _empty((max(wsb, 16),), torch.uint8, x.device)
+    _check("moe_shared_expert",
+           L.moe_shared_expert(_p(x), T, d, _p(w_gate), _p(w_up), _p(w_down), Fs, _p(out), _p(ws), ws.numel(),
+                               _p(d_status) if d_status is not None else None, _stream(stream)))
     return out
 
 

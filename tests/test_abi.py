@@ -100,6 +100,10 @@ def test_other_host_validation(L):
     assert L.moe_router_logits(None, 4, 128, p, 8, p, None, None) == 1
     assert L.moe_router_logits(_fake(0x10004), 4, 128, p, 8, p, None, None) == 3
     assert L.moe_router_logits(p, 0, 128, p, 8, p, None, None) == 0  # no-op
+    assert L.moe_shared_expert(p, 4, 384, p, p, p, 128, p, p, big, None, None) == 2  # d % 256
+    assert L.moe_shared_expert(p, 4, 256, p, p, p, 192, p, p, big, None, None) == 2  # Fs % 128
+    assert L.moe_shared_expert(p, 4, 256, p, p, p, 128, p, p, 0, None, None) == 4
+    assert L.moe_shared_expert(p, 0, 256, p, p, p, 128, p, p, 0, None, None) == 0  # no-op
     w = _lib._W(0x20000, 0x20000, 0x20000)
     assert L.nvfp4_linear(p, 4, 96, ctypes.byref(w), 16, None, p, p, big, None) == 2
     assert L.nvfp4_linear(p, 4, 64, ctypes.byref(w), 24, None, p, p, big, None) == 2
