@@ -2,8 +2,9 @@
 //   G = bf16(x Wg^T)   U = bf16(x Wu^T)   h = bf16(silu(G) * U)
 //   out = bf16(out + h Wd^T)          (out holds the routed layer's result)
 //
-// TensorFold issue #308, "The checkpoint": the shared expert is BF16 next to
-// the NVFP4 routed experts; it runs on every token, so it is two dense GEMMs.
+// TensorFold issue #308, "The checkpoint": the shared experts stay BF16 next
+// to the NVFP4 routed experts; "What the branch does": the shared expert runs
+// as a BF16 MLP.  It runs on every token, so it is two dense GEMMs.
 //
 // Both GEMMs: one CTA per (128 tokens, NT output columns) tile, NT = 256,
 // or 64 when the 256-wide tiles would leave most SMs idle (a decode batch:
