@@ -354,6 +354,39 @@ def time_router(layer, steps, flush):
             "T": s.T, "d": s.d, "E": s.E}
 
 
+def time_graph(layer, steps, flush):
+    """One layer call captured in a CUDA graph (inputs in the captured
+    buffers), replayed `steps` times: CUDA events per replay, L2 flushed
+    between replays.  The same work as a step, without host launch gaps."""
+    x_s, lg_s = (t.clone() for t in layer.batches[0])
+    layer.step(0, x_s, lg_s)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            layer.step(0, x_s, lg_s)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ts = []
+    for i in range(steps):
+        x, lg = layer.batches[(i + 1) % len(layer.batches)]
+        x_s.copy_(x)
+        lg_s.copy_(lg)
+        if flush is not None:
+            flush.fill_(i & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ts)
+    return {"ms_per_step": ms, "tokens_per_s": layer.shape.T / (ms / 1e3)}
+
+
 def time_shared(layer, steps, flush):
     """The BF16 shared-expert MLP for the workload's tokens (ffn taken equal
     to the routed experts': the pages give none), added into the layer's
@@ -590,6 +623,7 @@ def run_ours(args):
     roof.update({"layer_gbs": layer_gbs, "layer_frac_hbm": layer_gbs / hbm, "layer_tflops": layer_tflops,
                  "layer_frac_bf16": layer_tflops / bf16, "touched_experts": touched})
 
+    graph = time_graph(layer, max(3, args.steps), flush) if layer.kind != "dense" else None
     recipe = time_recipe(layer, flush) if layer.kind != "dense" else None
     shared = time_shared(layer, max(3, args.steps), flush) if layer.kind != "dense" else None
     if shared:
@@ -612,6 +646,7 @@ def run_ours(args):
                 "ms_per_step": e2e_ms},
         "gpu_launches": launches,
         "router_gemm": time_router(layer, max(3, args.steps), flush) if layer.kind != "dense" else None,
+        "graph_replay": graph,
         "weight_recipe": recipe,
         "shared_expert": shared,
         "clocks": clk.summary(),
