@@ -31,6 +31,11 @@
  * block scale = e4m3(block_amax / 6 / global), codes by round-to-nearest-even)
  * are the plainest ones and are listed with the rest in the design notes.
  *
+ * Beside the layer: the BF16 router GEMM (orc_router_logits: fp64 sums of
+ * exact bf16 products, and their |.| sums for the fp32 error bound) and the
+ * BF16 shared-expert MLP (orc_shared_expert: the same SwiGLU rounding points,
+ * added to the routed output and rounded once).
+ *
  * Rounding points (the same places the kernels round):
  *   G = bf16(ws2_g * sum x*w_g)   U = bf16(ws2_u * sum x*w_u)       (R1)
  *   h = bf16(silu(G) * U)                                            (R2)
