@@ -162,8 +162,8 @@ bool tcm_set_act(TcmArgs* a, const uint8_t* codes, const uint8_t* scales, long l
 void launch_tcm(int epi, int a_nvfp4, const TcmArgs& a, int max_units, cudaStream_t s);
 
 // ---- W4A4 prompt-shaped grouped GEMM on the block-scaled FP4 tensor cores ----
-// Same arguments as TcmArgs (NVFP4 rows: a_codes / x_gs); epi TCM_SWIGLU_Q,
-// TCM_ROWS or TCM_COMBINE.  Needs K % 256 == 0 and N % 16 (SwiGLU) / N % 32.
+// Same arguments as TcmArgs (NVFP4 rows: a_codes / x_gs); epi TCM_SWIGLU_Q
+// or TCM_ROWS.  Needs K % 256 == 0 and N % 16 (SwiGLU) / N % 32.
 bool tcq_supported(int epi, int N, int K);
 // Encodes the tensor maps this kernel uses (rows_w = E * N, rows_x = R).
 bool tcq_set_maps(TcmArgs* a, const uint8_t* x_codes, const uint8_t* x_scales, long long rows_x, long long rows_w);

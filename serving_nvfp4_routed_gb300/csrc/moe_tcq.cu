@@ -305,13 +305,8 @@ __global__ void __launch_bounds__(kThreads, 1) tcq_kernel(const __grid_constant_
             const int row = un.y + rr;
             const bool valid = row < un.z;
             float wt = 0.0f;
-            size_t tok = 0;
-            if constexpr (EPI == TCM_COMBINE || EPI == TCM_ROWS) {
-                if (valid) {
-                    const int slot = a.row_to_slot[row];
-                    tok = (size_t)(slot / a.top_k);
-                    wt = a.topk_w[slot];
-                }
+            if constexpr (EPI == TCM_ROWS) {
+                if (valid) wt = a.topk_w[a.row_to_slot[row]];
             }
             const float rs = a.x_gs[un.x];
             const float w0 = a.a_ws2[0][un.x], w1 = a.a_ws2[1][un.x];
@@ -375,24 +370,6 @@ __global__ void __launch_bounds__(kThreads, 1) tcq_kernel(const __grid_constant_
                     float* ybase = a.y_rows + (size_t)(un.y + q * 32) * a.N + un.w + cb * 32 + lane;
                     for (int j = 0; j < nvalid; ++j) ybase[(size_t)j * a.N] = st[j * kStageRow + lane];
                     __syncwarp();
-                }
-            } else {
-                for (int cb = 3 * half; cb < 3 * half + 3; ++cb) {
-                    if (un.w + cb * 32 >= a.N) break;  // columns past the expert's rows
-                    uint32_t r[32];
-                    tmem_ld32(tb + cb * 32, r);
-                    tmem_ld_wait();
-                    if (valid) {
-                        float4* dst = reinterpret_cast<float4*>(a.acc_out + tok * a.N + un.w + cb * 32);
-#pragma unroll
-                        for (int v = 0; v < 8; ++v) {
-                            float y[4];
-#pragma unroll
-                            for (int t = 0; t < 4; ++t)
-                                y[t] = wt * __fmul_rn(__fmul_rn(__uint_as_float(r[4 * v + t]), rs), w0);
-                            red_add_v4(reinterpret_cast<float*>(dst + v), y[0], y[1], y[2], y[3]);
-                        }
-                    }
                 }
             }
             tc_fence_before();
@@ -473,7 +450,6 @@ void launch_tcq(int epi, const TcmArgs& a, int max_tiles, cudaStream_t s) {
     const int slice = epi == TCM_SWIGLU_Q ? BH : BN;
     const int max_units = max_tiles * ((a.N + slice - 1) / slice);
     if (epi == TCM_SWIGLU_Q) return launch_tcq_t<TCM_SWIGLU_Q>(a, max_units, s, "tcq_gateup_w4a4");
-    if (epi == TCM_COMBINE) return launch_tcq_t<TCM_COMBINE>(a, max_units, s, "tcq_down_w4a4");
     if (epi == TCM_ROWS) return launch_tcq_t<TCM_ROWS>(a, max_units, s, "tcq_down_w4a4");
 }
 

@@ -9,7 +9,7 @@
 // rows), both exactly as stored and moved by TMA with 128-byte swizzle in
 // k-stages of 64 (one box each); an fp32 accumulator of EB columns in tensor
 // memory.  EB (a multiple of 32 dividing E rounded up to 32, at most 256) is
-// the largest that still gives every SM a CTA, else 32: a decode batch
+// the largest that still gives half the SMs a CTA, else 32: a decode batch
 // (one token tile) spreads the router matrix over E / 32 CTAs instead of
 // streaming it through one SM.  When that still leaves SMs idle, K is split
 // over a thread-block cluster of KS <= 8 CTAs: each stores its fp32 partial
@@ -220,9 +220,11 @@ extern "C" nvfp4_status moe_router_logits(const uint16_t* x_bf16, int T, int d, 
     a.E = E;
     const int nb = (E + kREGran - 1) / kREGran;  // 32-expert blocks
     const int m_tiles = (T + RM - 1) / RM;
-    int c = 1;  // blocks per CTA: the largest divisor of nb (<= 8) that still fills the SMs
+    // blocks per CTA: the largest divisor of nb (<= 8) that still gives half
+    // the SMs a CTA (N=32 MMAs are issue-bound, so fewer wider CTAs win)
+    int c = 1;
     for (int cand = 1; cand <= nb && cand * kREGran <= kRMaxEB; ++cand)
-        if (nb % cand == 0 && (long long)m_tiles * (nb / cand) >= num_sms()) c = cand;
+        if (nb % cand == 0 && (long long)m_tiles * (nb / cand) * 2 >= num_sms()) c = cand;
     a.EB = c * kREGran;
     a.e_blocks = nb / c;
     // split K over a cluster while the grid is under half the SMs
