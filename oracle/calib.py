@@ -22,6 +22,24 @@ import numpy as np
 from . import oracle
 
 
+# the card's converted layers: the base routed-expert layers 3..44
+ROUTED_LAYERS = range(3, 45)
+
+
+def layer_percentiles(layer: int) -> tuple[float, float]:
+    """(pct13, pct2) of the card's activation-scale policy for a routed layer
+    (model card "GLM-5.3-Flash-NVFP4-W4A4-Experts", the activation-scale
+    policy: p99 by default, p98 for w2 at layers 3-8, p98.9 for w2 at layers
+    24-44; gate/up always p99)."""
+    if layer not in ROUTED_LAYERS:
+        raise ValueError(f"layer {layer} is not a converted routed-expert layer (3..44)")
+    if layer <= 8:
+        return 99.0, 98.0
+    if layer >= 24:
+        return 99.0, 98.9
+    return 99.0, 99.0
+
+
 def _block_amax(rows: np.ndarray) -> np.ndarray:
     n, K = rows.shape
     return np.abs(rows.reshape(n, K // 16, 16)).max(axis=2).reshape(-1)

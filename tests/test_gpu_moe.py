@@ -276,3 +276,22 @@ def test_prompt_deterministic_and_chunk_invariant(orc, mode, monkeypatch):
     parts = torch.cat([run(x[:200].contiguous(), lg[:200].contiguous()),
                        run(x[200:].contiguous(), lg[200:].contiguous())])
     assert torch.equal(full.view(torch.int16), parts.view(torch.int16))
+
+
+@pytest.mark.parametrize("layer", [5, 30])
+@pytest.mark.parametrize("kpath", ["gemv", "tc"])
+def test_w4a4_layer_specific_calibration(orc, layer, kpath, monkeypatch):
+    """W4A4 with the card's layer-specific w2 percentiles (p98 at layer 5,
+    p98.9 at layer 30) on the decode and the prompt kernels, every token
+    against the oracle."""
+    monkeypatch.setenv("NVFP4_PATH", kpath)
+    T, E, k, d, F = 256, 16, 4, 512, 256
+    s = synth.MoEShape(T, d, E, k, F)
+    inp, gw, ob, r, tok = _setup(orc, s, seed=layer + 61, outlier=0.05)
+    xb = synth.bf16_bits(inp["x"])
+    p13, p2 = calib.layer_percentiles(layer)
+    is13, is2 = calib.calibrate(xb, inp["logits"].cpu().numpy(), k, ob, pct13=p13, pct2=p2)
+    out = lib.nvfp4_moe_w4a4(inp["x"], inp["logits"], k, gw, torch.from_numpy(is13).cuda(),
+                             torch.from_numpy(is2).cuda())
+    ref = orc.moe_layer("w4a4", xb, r["ids"], r["w"], ob, is13=is13, is2=is2)
+    assert_layer_close(bf16_to_f32(out), ref, f"w4a4 layer {layer} {kpath}")

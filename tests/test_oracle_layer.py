@@ -213,3 +213,35 @@ def test_calibration(orc, tiny):
     if unused:
         allrows = np.concatenate([bam[[t for t in range(s.T) if e in r["ids"][t]]].reshape(-1) for e in used])
         assert is13[unused[0]] == np.float32(np.percentile(allrows, 99) * 1.05 / 2688.0)
+
+
+def test_layer_percentile_policy():
+    """The card's activation-scale policy: p99 everywhere, except w2 at
+    p98 for layers 3-8 and p98.9 for layers 24-44; layers outside 3-44 are
+    not converted."""
+    for layer in range(3, 45):
+        p13, p2 = calib.layer_percentiles(layer)
+        assert p13 == 99.0
+        assert p2 == (98.0 if layer <= 8 else 98.9 if layer >= 24 else 99.0)
+    for bad in (0, 2, 45, 46):
+        with pytest.raises(ValueError):
+            calib.layer_percentiles(bad)
+
+
+def test_calibration_w2_percentile_variants(orc, tiny):
+    """w2 scales at the layer-specific percentiles equal the percentile of
+    the same h-row block amaxes, recomputed here; a lower percentile never
+    gives a larger scale; gate/up scales do not depend on it."""
+    s, inp, bank, xb, r = tiny
+    lg = inp["logits"].numpy()
+    base13, base2 = calib.calibrate(xb, lg, s.k, bank)
+    _, h = orc.moe_layer("w4a16", xb, r["ids"], r["w"], bank, want_h=True)
+    bam = np.abs(h.astype(np.float32).reshape(s.T, s.k, -1, 16)).max(-1)  # [T, k, F/16]
+    for layer in (5, 30):
+        p13, p2 = calib.layer_percentiles(layer)
+        is13, is2 = calib.calibrate(xb, lg, s.k, bank, pct13=p13, pct2=p2)
+        assert np.array_equal(is13, base13)
+        assert np.all(is2 <= base2)
+        for e in np.unique(r["ids"]):
+            sel = np.concatenate([bam[t, j] for t in range(s.T) for j in range(s.k) if r["ids"][t, j] == e])
+            assert is2[e] == np.float32(np.percentile(sel, p2) * 1.05 / 2688.0)
