@@ -6,7 +6,11 @@ One step = one call of the layer (route + permutation, gate/up + SwiGLU,
 down + weighted combine) over one batch of seeded synthetic tokens whose
 inputs are already resident in HBM.  The default workload is the
 decode-shaped layer (288 experts, top-8, d=4096, ffn=1536) at T=64; the
-line also carries a sweep over T in {1, 8, 32, 64}.  The L2 is flushed (a
+line also carries a sweep over T in {1, 8, 32, 64} and, under "workloads",
+the prompt-shaped layers (W4A16 T=4096; W4A4 T=8192 with calibrated static
+scales; skewed Zipf(1.2) popularity at T=16384, with and without a third of
+the experts masked, both modes) and the dense NVFP4 MLP, each with its own
+device time, end-to-end time, kernel split and binding roofline.  The L2 is flushed (a
 256 MB write) between timed steps, outside the timed events.
 
 Under torchrun every rank runs its own batch on its own GPU (no collective
@@ -145,6 +149,7 @@ WORKLOADS = {
     "skew_w4a16": (synth.SKEW, "w4a16", "zipf", 0.0),
     "skew_w4a4": (synth.SKEW, "w4a4", "zipf", 0.0),
     "skew_masked_w4a16": (synth.SKEW, "w4a16", "zipf_masked", 0.0),
+    "skew_masked_w4a4": (synth.SKEW, "w4a4", "zipf_masked", 0.0),
     "dense": (None, "w4a16", "dense", 0.05),
     # small prompt-shaped cases for full-metric ncu captures (not bench lines)
     "prompt_small_w4a16": (synth.PROMPT_SMALL, "w4a16", "normal", 0.05),
@@ -193,16 +198,40 @@ def recorded_traffic(kernel: str, workload: str):
     return None
 
 
-def synthetic_input_scales(x: torch.Tensor, E: int):
-    """Static input scales for timing runs: p99 of the 16-block max |x| of
-    the batch, x 1.05, / 2688, the same for every expert; the down-side
-    scale assumes h blocks of about the same size.  (Parity tests calibrate
-    per expert with the oracle instead; the scales only move saturation.)"""
-    bam = x[: min(1024, x.shape[0])].float().abs().view(-1, 16).amax(1)
-    p99 = torch.quantile(bam[: 1 << 20].cpu(), 0.99).item()
-    is13 = torch.full((E,), p99 * 1.05 / 2688.0, dtype=torch.float32, device=x.device)
-    is2 = torch.full((E,), 4.0 * 1.05 / 2688.0, dtype=torch.float32, device=x.device)
-    return is13, is2
+def calibrate_scales(lib, w, shape, device, seed, n=1024, pct=99.0, margin=1.05):
+    """Static W4A4 input scales of a layer (W4A4 model card, "Quantization
+    boundary": calibrated static activation scales, p99 with a 5 % margin),
+    computed with the library itself once, outside any timed region: a
+    seeded n-token draw of the layer's input distribution (N(0,1) rows, 5 %
+    of them x 8; normal router logits) runs through the W4A16 layer; per
+    expert and projection, the percentile (linear interpolation) of the
+    16-block maxima of the rows routed to it -- x rows for gate/up, the
+    layer's own h rows for down -- times 1.05 / 2688.  Experts the draw does
+    not reach take the percentile over all rows of that projection."""
+    s = shape
+    x = synth.make_x(n, s.d, seed, device, outlier_frac=0.05)
+    lg = synth.make_logits(n, s.E, seed + 1, device)
+    ws = lib.moe_workspace(n, s.E, s.k, s.d, s.F, "w4a16", device)
+    lib.nvfp4_moe_w4a16(x, lg, s.k, w, ws=ws)
+    v = lib.moe_workspace_views(ws, n, s.E, s.k, s.d, s.F, "w4a16")
+    h = lib.moe_workspace_intermediates(ws, n, s.E, s.k, s.d, s.F, "w4a16")["h"]
+    R = n * s.k
+    offs = v["offsets"].cpu().tolist()
+    rows = x[v["row_to_slot"].long() // s.k]
+    bx = rows.float().abs().view(R, s.d // 16, 16).amax(-1).double()
+    bh = h.float().abs().view(R, s.F // 16, 16).amax(-1).double()
+    q = pct / 100.0
+
+    def scales(b):
+        fb = torch.quantile(b.reshape(-1), q).item()
+        out = []
+        for e in range(s.E):
+            seg = b[offs[e]:offs[e + 1]]
+            p = torch.quantile(seg.reshape(-1), q).item() if seg.numel() else fb
+            out.append(p * margin / 2688.0)
+        return torch.tensor(out, dtype=torch.float32, device=device)
+
+    return scales(bx), scales(bh)
 
 
 class Layer:
@@ -228,7 +257,7 @@ class Layer:
             self.batches.append((x, lg))
         self.is13 = self.is2 = None
         if self.mode == "w4a4":
-            self.is13, self.is2 = synthetic_input_scales(self.batches[0][0], s.E)
+            self.is13, self.is2 = calibrate_scales(lib, self.w, s, device, seed * 100 + 99)
         self.ws = lib.moe_workspace(s.T, s.E, s.k, s.d, s.F, self.mode, device)
         self.out = torch.empty(s.T, s.d, dtype=torch.bfloat16, device=device)
 
@@ -246,6 +275,12 @@ class Layer:
         v = self.lib.moe_workspace_views(self.ws, s.T, s.E, s.k, s.d, s.F, self.mode)
         counts = torch.diff(v["offsets"]).cpu()
         return int((counts > 0).sum().item())
+
+    def mean_touched(self, start, steps):
+        """Touched experts averaged over the batches that `steps` steps from
+        `start` run (each batch routes to its own expert set)."""
+        per = [self.touched_experts(b) for b in range(len(self.batches))]
+        return statistics.mean(per[(start + i) % len(per)] for i in range(steps)), per
 
     def algorithmic_bytes(self, touched):
         s = self.shape
@@ -300,6 +335,9 @@ class DenseLayer:
 
     def touched_experts(self, i):
         return 1
+
+    def mean_touched(self, start, steps):
+        return 1, [1]
 
     def algorithmic_bytes(self, touched):
         s = self.shape
@@ -478,6 +516,17 @@ def time_e2e(layer, steps, flush):
     return statistics.mean(times), h2d, d2h
 
 
+def oracle_timing_scales(x, E):
+    """Static input scales for timing the oracle on W4A4 workloads: p99 of
+    the batch's 16-block maxima x 1.05 / 2688 for every expert, and a fixed
+    down-side scale.  The oracle takes no input from the library, and the
+    scales only move saturation, not the oracle's work."""
+    bam = np.abs(x[: min(1024, x.shape[0])].float().cpu().numpy()).reshape(-1, 16).max(1)
+    is13 = np.full(E, np.percentile(bam, 99) * 1.05 / 2688.0, np.float32)
+    is2 = np.full(E, 4.0 * 1.05 / 2688.0, np.float32)
+    return is13, is2
+
+
 def cpu_baseline(layer, seed, n_tokens=8):
     """The oracle (plain C, fp64, OpenMP on the host cores) on a bounded
     sample of the workload: `n_tokens` tokens of the first batch in a seeded
@@ -503,8 +552,9 @@ def cpu_baseline(layer, seed, n_tokens=8):
         ob[nm] = (codes, scales, ws2)
         del w
     torch.cuda.empty_cache()
-    is13 = None if layer.is13 is None else layer.is13.cpu().numpy()
-    is2 = None if layer.is2 is None else layer.is2.cpu().numpy()
+    is13 = is2 = None
+    if layer.mode == "w4a4":
+        is13, is2 = oracle_timing_scales(x, s.E)
     t0 = time.perf_counter()
     orc.moe_layer(layer.mode, xb, r["ids"], r["w"], ob, tokens=tok, is13=is13, is2=is2)
     elapsed = time.perf_counter() - t0
@@ -516,12 +566,124 @@ def cpu_baseline(layer, seed, n_tokens=8):
 
 def workload_config(layer, flush_mb):
     s = layer.shape
+    if layer.kind == "dense":
+        return {"workload": f"dense: NVFP4 MLP d={s.d} ffn={s.F} M={s.T}, gate/up with their own tensor scales, "
+                            "SwiGLU, down (two nvfp4_linear calls)",
+                "M": s.T, "d": s.d, "ffn": s.F, "mode": "w4a16",
+                "l2": f"flushed between steps ({flush_mb} MB write), outside the timed events",
+                "parallelism": "independent replicas (one batch per GPU)"}
     desc = {"w4a16": "W4A16", "w4a4": "W4A4"}[layer.mode]
-    return {"workload": f"{layer.name}: routed-expert NVFP4 layer {desc}, E={s.E} top-{s.k} d={s.d} "
-                        f"ffn={s.F} T={s.T}, logits {layer.kind}",
-            "T": s.T, "E": s.E, "top_k": s.k, "d": s.d, "ffn": s.F, "mode": layer.mode,
-            "l2": f"flushed between steps ({flush_mb} MB write), outside the timed events",
-            "parallelism": "independent replicas (one batch per GPU)"}
+    cfg = {"workload": f"{layer.name}: routed-expert NVFP4 layer {desc}, E={s.E} top-{s.k} d={s.d} "
+                       f"ffn={s.F} T={s.T}, logits {layer.kind}",
+           "T": s.T, "E": s.E, "top_k": s.k, "d": s.d, "ffn": s.F, "mode": layer.mode,
+           "l2": f"flushed between steps ({flush_mb} MB write), outside the timed events",
+           "parallelism": "independent replicas (one batch per GPU)"}
+    if layer.mode == "w4a4":
+        cfg["input_scale"] = ("per expert and projection: p99 of the routed rows' 16-block maxima x 1.05 / 2688 "
+                              "over a seeded 1024-token draw (h rows from the library's W4A16 layer)")
+    return cfg
+
+
+def kernel_roofline(layer, dom, dom_ms, touched, hbm, bf16, peak_kind, workload):
+    """The binding roofline of the dominant kernel's launches: algorithmic
+    bytes (touched experts' weights read once, the A rows, the output rows)
+    over the measured copy bandwidth, or algorithmic flops over the tensor
+    peak -- whichever floor is longer; the other is reported beside it."""
+    s_ = layer.shape
+    R = s_.T * s_.k if layer.kind != "dense" else s_.T
+    if dom.startswith(("tc_", "tcm_", "tcq_")):
+        nproj = 2 if "gateup" in dom else 1
+        dom_flops = 2.0 * R * s_.d * s_.F * nproj
+        achieved = dom_flops / (dom_ms / 1e3) / 1e12
+        fp4 = dom.startswith("tcq_")
+        peak = bf16 * FP4_BF16_RATIO if fp4 else bf16
+        kind = (f"{peak_kind} bf16 dense x nominal FP4/BF16 ratio {FP4_BF16_RATIO:g}, burst" if fp4
+                else f"{peak_kind} bf16 dense (f16 runs at the same rate), burst")
+        if layer.kind == "dense":
+            dom_bytes = (2 if nproj == 2 else 1) * s_.d * s_.F * 9 // 16 + s_.T * (s_.d + s_.F) * 2
+        elif nproj == 2:
+            dom_bytes = layer.gateup_bytes(touched)
+        else:
+            a_bytes = R * s_.F * (2 if layer.mode == "w4a16" else 9 / 16)
+            dom_bytes = int(touched * s_.d * s_.F * 9 // 16 + a_bytes + s_.T * s_.d * 2)
+        bytes_gbs = dom_bytes / (dom_ms / 1e3) / 1e9
+        if dom_bytes / hbm > dom_flops / (peak * 1e3):
+            return {"bound": "hbm", "kernel": dom, "achieved": bytes_gbs, "peak": hbm, "unit": "GB/s",
+                    "frac": bytes_gbs / hbm, "peak_kind": f"{peak_kind} (copy bandwidth, burst)",
+                    "traffic": recorded_traffic(dom, workload), "algorithmic_bytes_per_launch": dom_bytes,
+                    "tensor": {"achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                               "peak_kind": kind, "algorithmic_flops_per_launch": dom_flops}}
+        return {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "peak_kind": kind, "traffic": recorded_traffic(dom, workload),
+                "algorithmic_flops_per_launch": dom_flops,
+                "hbm": {"achieved": bytes_gbs, "peak": hbm, "unit": "GB/s", "frac": bytes_gbs / hbm,
+                        "algorithmic_bytes_per_launch": dom_bytes}}
+    if dom.startswith("gemv_down"):
+        dom_bytes = touched * s_.d * s_.F * 9 // 16 + (R * s_.F * 2 if layer.mode == "w4a16" else R * s_.F * 9 // 16)
+    else:
+        dom_bytes = layer.gateup_bytes(touched)
+    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+    return {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
+            "frac": achieved / hbm, "peak_kind": f"{peak_kind} (copy bandwidth, burst)",
+            "traffic": recorded_traffic(dom, workload), "algorithmic_bytes_per_launch": dom_bytes}
+
+
+def measure(layer, lib, args, flush, hbm, bf16, peak_kind, steps, world=1, dev=None):
+    """Time `steps` layer steps (CUDA events, L2 flushed between steps) with
+    the SM clocks sampled, then the same steps with per-launch events for
+    the kernel split, then the end-to-end variant with host buffers."""
+    for i in range(args.warmup):
+        layer.step(i)
+    torch.cuda.synchronize()
+    touched, per_batch = layer.mean_touched(0, steps)
+    launches0 = lib.launch_count()
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        times = time_steps(layer, steps, flush)
+    torch.cuda.synchronize()
+    barrier()
+    launches = lib.launch_count() - launches0
+    ms = statistics.mean(times)
+    value, ms_max = aggregate(layer.shape.T, ms, world, dev)
+    lib.profile_enable(True)
+    time_steps(layer, steps, flush)
+    lib.profile_enable(False)
+    prof = lib.profile_collect()
+    e2e_ms, h2d, d2h = time_e2e(layer, max(3, steps), flush)
+    e2e_value, _ = aggregate(layer.shape.T, e2e_ms, world, dev)
+    kernels = {k: {"launches": v[0], "ms_per_launch": v[1] / max(1, v[0])} for k, v in prof.items()}
+    dom = max(kernels, key=lambda k: kernels[k]["ms_per_launch"] * kernels[k]["launches"]) if kernels else "?"
+    dom_ms = kernels.get(dom, {"ms_per_launch": float("nan")})["ms_per_launch"]
+    roof = kernel_roofline(layer, dom, dom_ms, touched, hbm, bf16, peak_kind, layer.name)
+    total_bytes, R = layer.algorithmic_bytes(touched)
+    layer_gbs = total_bytes / (ms / 1e3) / 1e9
+    layer_tflops = layer.flops() / (ms / 1e3) / 1e12
+    fp4 = layer.mode == "w4a4" and any(k.startswith("tcq_") for k in kernels)
+    tpeak = bf16 * FP4_BF16_RATIO if fp4 else bf16
+    # the layer's own floor: the longer of its HBM and tensor floors
+    floor_ms = max(total_bytes / hbm / 1e6, layer.flops() / (tpeak * 1e9))
+    roof.update({"layer_gbs": layer_gbs, "layer_frac_hbm": layer_gbs / hbm, "layer_tflops": layer_tflops,
+                 "layer_frac_bf16": layer_tflops / bf16, "layer_frac_tensor": layer_tflops / tpeak,
+                 "layer_tensor_peak": "fp4 (measured bf16 x 6)" if fp4 else "bf16",
+                 "layer_floor_ms": floor_ms, "layer_frac_of_floor": floor_ms / ms,
+                 "touched_experts": touched, "touched_experts_per_batch": per_batch})
+    return {"value": value, "ms_per_step": ms_max, "times_ms": times, "launches": launches, "kernels": kernels,
+            "roofline": roof, "clocks": clk.summary(),
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms}}
+
+
+def dtype_of(layer, kernels):
+    if layer.mode == "w4a16":
+        return "e2m1+e4m3 weights, f16 mma, f32 accumulate"
+    if any(k.startswith("tcq_") for k in kernels):
+        return "e2m1+e4m3 weights and activations, block-scaled fp4 mma, f32 accumulate"
+    return "e2m1+e4m3 weights and activations, f16 mma, f32 accumulate"
+
+
+PROMPT_WORKLOADS = ("prefill_w4a16", "prefill_w4a4", "skew_w4a16", "skew_w4a4", "skew_masked_w4a16",
+                    "skew_masked_w4a4", "dense")
 
 
 def run_ours(args):
@@ -544,132 +706,66 @@ def run_ours(args):
     flush = torch.empty(flush_mb << 20, dtype=torch.uint8, device=dev)
     seed = 1001 + 17 * rank
     layer = (DenseLayer if args.workload == "dense" else Layer)(args.workload, lib, dev, seed)
+    m = measure(layer, lib, args, flush, hbm, bf16, peak_kind, args.steps, world, dev)
 
-    for i in range(args.warmup):
-        layer.step(i)
-    torch.cuda.synchronize()
-    touched = layer.touched_experts(0)
-
-    launches0 = lib.launch_count()
-    barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        times = time_steps(layer, args.steps, flush)
-    torch.cuda.synchronize()
-    barrier()
-    launches = lib.launch_count() - launches0
-    ms = statistics.mean(times)
-    value, ms_max = aggregate(layer.shape.T, ms, world, dev)
-
-    # per-kernel times (CUDA events around each launch, same stream, same steps)
-    lib.profile_enable(True)
-    time_steps(layer, args.steps, flush)
-    lib.profile_enable(False)
-    prof = lib.profile_collect()
-    e2e_ms, h2d, d2h = time_e2e(layer, max(3, args.steps), flush)
-    e2e_value, _ = aggregate(layer.shape.T, e2e_ms, world, dev)
-
-    total_bytes, R = layer.algorithmic_bytes(touched)
-    kernels = {k: {"launches": v[0], "ms_per_launch": v[1] / max(1, v[0])} for k, v in prof.items()}
-    dom = max(kernels, key=lambda k: kernels[k]["ms_per_launch"] * kernels[k]["launches"]) if kernels else "?"
-    s_ = layer.shape
-    dom_ms = kernels.get(dom, {"ms_per_launch": float("nan")})["ms_per_launch"]
-    if dom.startswith(("tc_", "tcm_", "tcq_")):
-        # tensor-bound, flops of one launch: f16 MMA (the bf16/f16 dense rate) or
-        # block-scaled FP4 MMA (tcq_*, against the FP4 dense rate)
-        nproj = 2 if "gateup" in dom else 1
-        rows = R if layer.kind != "dense" else s_.T
-        dom_flops = 2.0 * rows * s_.d * s_.F * nproj
-        achieved = dom_flops / (dom_ms / 1e3) / 1e12
-        fp4 = dom.startswith("tcq_")
-        peak = bf16 * FP4_BF16_RATIO if fp4 else bf16
-        kind = (f"{peak_kind} bf16 dense x nominal FP4/BF16 ratio {FP4_BF16_RATIO:g}, burst" if fp4
-                else f"{peak_kind} bf16 dense (f16 runs at the same rate), burst")
-        # the same launch's algorithmic HBM bytes: touched experts' weights read
-        # once, the A rows, the output rows
-        if layer.kind == "dense":
-            dom_bytes = (2 if nproj == 2 else 1) * s_.d * s_.F * 9 // 16 + s_.T * (s_.d + s_.F) * 2
-        elif nproj == 2:
-            dom_bytes = layer.gateup_bytes(touched)
-        else:
-            a_bytes = R * s_.F * (2 if layer.mode == "w4a16" else 9 / 16)
-            dom_bytes = int(touched * s_.d * s_.F * 9 // 16 + a_bytes + s_.T * s_.d * 2)
-        bytes_gbs = dom_bytes / (dom_ms / 1e3) / 1e9
-        # the binding roofline is the one with the longer floor for this launch
-        hbm_bound = dom_bytes / hbm > dom_flops / (peak * 1e3)
-        if hbm_bound:
-            roof = {"bound": "hbm", "kernel": dom, "achieved": bytes_gbs, "peak": hbm, "unit": "GB/s",
-                    "frac": bytes_gbs / hbm, "peak_kind": f"{peak_kind} (copy bandwidth, burst)",
-                    "traffic": recorded_traffic(dom, args.workload), "algorithmic_bytes_per_launch": dom_bytes,
-                    "tensor": {"achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                               "peak_kind": kind, "algorithmic_flops_per_launch": dom_flops}}
-        else:
-            roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak, "peak_kind": kind,
-                    "traffic": recorded_traffic(dom, args.workload), "algorithmic_flops_per_launch": dom_flops,
-                    "hbm": {"achieved": bytes_gbs, "peak": hbm, "unit": "GB/s", "frac": bytes_gbs / hbm,
-                            "algorithmic_bytes_per_launch": dom_bytes}}
-    else:
-        if dom.startswith("gemv_down"):
-            dom_bytes = touched * s_.d * s_.F * 9 // 16 + (R * s_.F * 2 if layer.mode == "w4a16" else R * s_.F * 9 // 16)
-        else:
-            dom_bytes = layer.gateup_bytes(touched)
-        achieved = dom_bytes / (dom_ms / 1e3) / 1e9
-        roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                "frac": achieved / hbm, "peak_kind": f"{peak_kind} (copy bandwidth, burst)",
-                "traffic": recorded_traffic(dom, args.workload), "algorithmic_bytes_per_launch": dom_bytes}
-    layer_gbs = total_bytes / (ms / 1e3) / 1e9
-    layer_tflops = layer.flops() / (ms / 1e3) / 1e12
-    roof.update({"layer_gbs": layer_gbs, "layer_frac_hbm": layer_gbs / hbm, "layer_tflops": layer_tflops,
-                 "layer_frac_bf16": layer_tflops / bf16, "touched_experts": touched})
-
-    graph = time_graph(layer, max(3, args.steps), flush) if layer.kind != "dense" else None
-    recipe = time_recipe(layer, flush) if layer.kind != "dense" else None
-    shared = time_shared(layer, max(3, args.steps), flush) if layer.kind != "dense" else None
-    if shared:
-        shared["frac_bf16"] = shared["tflops"] / bf16
-    if recipe:
-        recipe["frac_hbm"] = recipe["gbs"] / hbm
     line = {
         "metric": "MoE-layer tokens/s",
-        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": ("e2m1+e4m3 weights, f16 mma, f32 accumulate" if layer.mode == "w4a16"
-                  else "e2m1+e4m3 weights and activations, block-scaled fp4 mma, f32 accumulate"
-                  if any(k.startswith("tcq_") for k in kernels)
-                  else "e2m1+e4m3 weights and activations, f16 mma, f32 accumulate"),
+        "value": m["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": m["ms_per_step"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": dtype_of(layer, m["kernels"]),
         "data": "synthetic (seeded N(0,1) x and logits, N(0,0.02) bf16 weights quantised by the library)",
         "config": workload_config(layer, flush_mb),
-        "roofline": roof,
-        "kernels": kernels,
-        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms},
-        "gpu_launches": launches,
-        "router_gemm": time_router(layer, max(3, args.steps), flush) if layer.kind != "dense" else None,
-        "graph_replay": graph,
-        "weight_recipe": recipe,
-        "shared_expert": shared,
-        "clocks": clk.summary(),
+        "roofline": m["roofline"],
+        "kernels": m["kernels"],
+        "e2e": m["e2e"],
+        "gpu_launches": m["launches"],
+        "clocks": m["clocks"],
     }
+    if layer.kind != "dense":
+        line["router_gemm"] = time_router(layer, max(3, args.steps), flush)
+        line["graph_replay"] = time_graph(layer, max(3, args.steps), flush)
+        recipe = time_recipe(layer, flush)
+        recipe["frac_hbm"] = recipe["gbs"] / hbm
+        line["weight_recipe"] = recipe
+        shared = time_shared(layer, max(3, args.steps), flush)
+        shared["frac_bf16"] = shared["tflops"] / bf16
+        line["shared_expert"] = shared
     if args.sweep and args.workload == "decode64":
-        sweep = {}
+        sweep = {"decode64": {"tokens_per_s": m["value"] / world, "ms": m["ms_per_step"],
+                              "layer_frac": m["roofline"]["layer_frac_hbm"]}}
         for T in synth.DECODE_T:
             if T == 64:
-                sweep["decode64"] = {"tokens_per_s": layer.shape.T / (ms / 1e3), "layer_frac": layer_gbs / hbm}
                 continue
             sl = Layer(f"decode{T}", lib, dev, seed + T)
-            for i in range(args.warmup):
-                sl.step(i)
-            tch = sl.touched_experts(0)
-            tt = statistics.mean(time_steps(sl, args.steps, flush))
-            b, _ = sl.algorithmic_bytes(tch)
-            sweep[f"decode{T}"] = {"tokens_per_s": T / (tt / 1e3), "ms": tt, "touched_experts": tch,
-                                   "layer_gbs": b / (tt / 1e3) / 1e9, "layer_frac": b / (tt / 1e3) / 1e9 / hbm}
+            ms_ = measure(sl, lib, args, flush, hbm, bf16, peak_kind, args.steps)
+            sweep[f"decode{T}"] = {"tokens_per_s": T / (ms_["ms_per_step"] / 1e3), "ms": ms_["ms_per_step"],
+                                   "touched_experts": ms_["roofline"]["touched_experts"],
+                                   "layer_gbs": ms_["roofline"]["layer_gbs"],
+                                   "layer_frac": ms_["roofline"]["layer_frac_hbm"],
+                                   "kernels": ms_["kernels"], "e2e": ms_["e2e"], "clocks": ms_["clocks"]}
             del sl
             torch.cuda.empty_cache()
         line["sweep"] = sweep
-    if rank == 0 and not args.no_cpu_baseline and args.workload != "dense":
+    if rank == 0 and not args.no_cpu_baseline and layer.kind != "dense":
         line["cpu_baseline"] = cpu_baseline(layer, seed, n_tokens=args.cpu_tokens)
+    del layer
+    torch.cuda.empty_cache()
+    if args.workloads and args.workload == "decode64":
+        # the prompt-shaped half of the metric: the other configurations,
+        # each measured the same way (fewer steps: each step is milliseconds)
+        wl = {}
+        for name in PROMPT_WORKLOADS:
+            lay = (DenseLayer if name == "dense" else Layer)(name, lib, dev, seed + 7)
+            res = measure(lay, lib, args, flush, hbm, bf16, peak_kind, min(args.steps, args.prompt_steps), world,
+                          dev)
+            res.pop("times_ms")
+            res["tokens_per_s"] = res.pop("value")
+            res["config"] = workload_config(lay, flush_mb)
+            res["dtype"] = dtype_of(lay, res["kernels"])
+            wl[name] = res
+            del lay
+            torch.cuda.empty_cache()
+        line["workloads"] = wl
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -710,8 +806,7 @@ def run_reference(args):
         del w
     is13 = is2 = None
     if mode == "w4a4":
-        a, b = synthetic_input_scales(x, shape.E)
-        is13, is2 = a.cpu().numpy(), b.cpu().numpy()
+        is13, is2 = oracle_timing_scales(x, shape.E)
     times = []
     for i in range(args.warmup + args.steps):
         tok = np.sort(tok_all[i * per_step:(i + 1) * per_step]).astype(np.int32)
@@ -743,6 +838,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode64")
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
+    ap.add_argument("--no-workloads", dest="workloads", action="store_false",
+                    help="skip the prompt-shaped and dense workloads of the default run")
+    ap.add_argument("--prompt-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=8)
     ap.add_argument("--ref-tokens", type=int, default=4)

@@ -26,9 +26,12 @@
  *     enqueued.  Problems only the device can see (a user-supplied expert id
  *     out of range) are written to the optional int32 status word d_status
  *     as an nvfp4_status value; kernels never trap.
- *   - K (the reduction length of a GEMM) must be a multiple of 64; N (output
- *     features) a multiple of 16; row counts M or T may be 0 (no-op).
- *   - Inputs must be finite; NaN/Inf behaviour is unspecified.
+ *   - K (the reduction length of a GEMM) must be a multiple of 64 (the
+ *     decode-shaped kernel streams K in 64-wide chunks: 4 lanes x 16 values,
+ *     one e4m3 scale each); N (output features) a multiple of 16; row
+ *     counts M or T may be 0 (no-op).
+ *   - Activations and weights must be finite (their NaN/Inf behaviour is
+ *     unspecified); non-finite router logits follow moe_route_permute.
  *   - Workspace contents are scratch owned by the call until it completes on
  *     the stream; two calls that overlap on the GPU must not share one.
  */
@@ -86,7 +89,8 @@ typedef struct {
  *   w       [batch, N, K] bf16     codes [batch, N, K/2]   scales [batch, N, K/16]
  *   weight_scale_2 [batch] fp32
  *   ws      scratch of at least nvfp4_quantize_weights_workspace_size() bytes
- * K must be a multiple of 16.  Two device passes (global amax, then codes).
+ * K must be a multiple of 16 and batch at most 65535 (NVFP4_ERR_SHAPE
+ * otherwise).  Two device passes (global amax, then codes).
  * --------------------------------------------------------------------- */
 nvfp4_status nvfp4_quantize_weights(const uint16_t* w_bf16, int batch, int N, int K,
                                     uint8_t* codes, uint8_t* scales, float* weight_scale_2,
@@ -106,9 +110,11 @@ size_t nvfp4_quantize_weights_workspace_size(int batch, int N, int K);
  * call, 16 KB of device memory on every GPU that loads the library, held
  * until the process exits) and allocates nothing.
  *   - batch above the maximum: NVFP4_ERR_SHAPE, nothing enqueued.
- *   - The first call on a device (with that device current) looks up the
- *     array's device address (cudaGetSymbolAddress) and caches it; make
- *     that first call before any stream capture.
+ *   - Every call looks up the array's device address in the current
+ *     context (cudaGetSymbolAddress, with the caller's device current;
+ *     nothing is cached, so calls after cudaDeviceReset are served too).
+ *     The first call of a process on a device may load the library's
+ *     device code: make it before any stream capture.
  *   - All calls on a device share the one array: calls that can overlap on
  *     the GPU (other streams, other host threads) race; order them.
  *   - The scratch is cleared on each call; outputs as for
@@ -177,7 +183,10 @@ size_t moe_shared_expert_workspace_size(int T, int Fs);
  * (TensorFold #308: router BF16, routed experts through one grouped
  * kernel).  Per token t: softmax over the E logits, the top_k experts in
  * descending order (ties -> lower expert id), and their weights
- * renormalised over the chosen top_k (exp and the division in fp32):
+ * renormalised over the chosen top_k (exp, sum and division in fp64, one
+ * rounding to fp32).  NaN logits rank as -inf; a token whose top logit is
+ * +inf gives its +inf entries equal weights (the rest 0), one whose chosen
+ * logits are all -inf gets 1/top_k each:
  *   topk_ids [T, top_k] int32, topk_w [T, top_k] fp32.
  * Then a stable permutation of the R = T*top_k (token, slot) pairs by
  * expert (order: expert, token, slot):
@@ -231,6 +240,34 @@ nvfp4_status nvfp4_moe_workspace_views(void* ws, int T, int E, int top_k, int d,
                                        int32_t** topk_ids, float** topk_w,
                                        int32_t** expert_offsets, int32_t** row_to_slot,
                                        int32_t** slot_to_row);
+
+/* Device pointers to the per-row intermediates inside an nvfp4_moe
+ * workspace, as the last call that used it left them, rows in the permuted
+ * (expert-contiguous) order of row_to_slot (R = T * top_k rows):
+ *   mode 0 (W4A16): h_bf16 [R, F] = bf16(silu(G) * U);
+ *   mode 1 (W4A4):  xq [R, d/2], xs [R, d/16] (the NVFP4 x rows under
+ *                   input_scale_w13) and hq [R, F/2], hs [R, F/16] (h
+ *                   requantised under input_scale_w2).
+ * Pointers of the other mode are set to NULL; any output pointer may be
+ * NULL.  The pages have no counterpart: an inspection helper (the parity
+ * tests read the intermediates through it). */
+nvfp4_status nvfp4_moe_workspace_intermediates(void* ws, int T, int E, int top_k, int d, int F, int mode,
+                                               uint16_t** h_bf16, uint8_t** xq, uint8_t** xs,
+                                               uint8_t** hq, uint8_t** hs);
+
+/* ------------------------------------------------------------------------
+ * nvfp4_set_kernel_choice -- which kernels the later nvfp4_moe_* and
+ * nvfp4_linear calls of this process run (the pages have no counterpart):
+ *   0 = by shape (the default: the prompt-shaped tensor-core kernels once
+ *       the experts average 32 or more routed rows, else the decode-shaped
+ *       streaming kernels);
+ *   1 = the decode-shaped kernels for every shape;
+ *   2 = the prompt-shaped kernels wherever the shapes allow them.
+ * For tests and measurements that cover both kernels at one size.  Takes
+ * effect for calls made after it returns; returns NVFP4_ERR_INVALID_ARG
+ * for any other value.
+ * --------------------------------------------------------------------- */
+nvfp4_status nvfp4_set_kernel_choice(int choice);
 
 /* ------------------------------------------------------------------------
  * nvfp4_linear -- dense NVFP4 linear over bf16 rows (TensorFold #308: the

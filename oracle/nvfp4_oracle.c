@@ -45,6 +45,14 @@
  * scale, element / scale) is done in fp32 in the order the recipe states,
  * because that is the precision in which the codes are defined.
  *
+ * The layer groups its (token, slot) pairs by expert and dequantises each
+ * touched expert's three projections once (exact in fp32); every pair is
+ * then evaluated on its own with plain fp64 loops.  Besides the bf16
+ * outputs it can return each output's value before its final rounding and
+ * the sum of |terms| behind it (the scale of the error bound of an fp32
+ * evaluation), and the gate / up values before their rounding, which the
+ * parity tests use to tell a legitimate rounding flip from an error.
+ *
  * Build: gcc -O2 -fopenmp -ffp-contract=off -fPIC -shared (no fast-math).
  */
 #include <math.h>
@@ -254,14 +262,21 @@ void orc_router_logits(const uint16_t* x, int64_t T, int64_t d, const uint16_t* 
 /* expert id), weights renormalised over the k chosen:                  */
 /*   w_j = exp(l_j - l_max) / sum_{i in top-k} exp(l_i - l_max)         */
 /* (the softmax normaliser cancels).  fp64, stored as fp32.             */
+/* Non-finite logits (the pages never meet them; the reading taken):    */
+/* NaN ranks as -inf; if the top logit is +inf the +inf entries among   */
+/* the k share the weight equally and the rest get 0; if every chosen   */
+/* logit is -inf the k weights are 1/k.                                 */
 /* Then a stable counting sort of the T*k (token, slot) pairs by expert  */
 /* (order: expert, then token, then slot):                               */
 /*   offsets[e] = number of pairs routed to experts < e;                 */
 /*   row_to_slot[row] = t*k + slot;  slot_to_row[t*k + slot] = row.      */
 /* ------------------------------------------------------------------ */
+static double rank_key(float v) { return isnan(v) ? -INFINITY : (double)v; }
+
 void orc_route(const float* logits, int64_t T, int E, int k, int32_t* ids, float* w,
                int32_t* offsets, int32_t* row_to_slot, int32_t* slot_to_row) {
     char* chosen = (char*)malloc((size_t)E);
+    double* num = (double*)malloc(sizeof(double) * (size_t)k);
     for (int64_t t = 0; t < T; ++t) {
         const float* l = logits + t * E;
         memset(chosen, 0, (size_t)E);
@@ -269,17 +284,23 @@ void orc_route(const float* logits, int64_t T, int E, int k, int32_t* ids, float
             int best = -1;
             for (int e = 0; e < E; ++e) {
                 if (chosen[e]) continue;
-                if (best < 0 || l[e] > l[best]) best = e;
+                if (best < 0 || rank_key(l[e]) > rank_key(l[best])) best = e;
             }
             chosen[best] = 1;
             ids[t * k + j] = best;
         }
-        double lmax = (double)l[ids[t * k]];
+        const double lmax = rank_key(l[ids[t * k]]);
         double den = 0.0;
-        for (int j = 0; j < k; ++j) den += exp((double)l[ids[t * k + j]] - lmax);
-        for (int j = 0; j < k; ++j)
-            w[t * k + j] = (float)(exp((double)l[ids[t * k + j]] - lmax) / den);
+        for (int j = 0; j < k; ++j) {
+            const double lj = rank_key(l[ids[t * k + j]]);
+            if (lmax == INFINITY) num[j] = (lj == INFINITY) ? 1.0 : 0.0;
+            else if (lmax == -INFINITY) num[j] = 1.0;
+            else num[j] = exp(lj - lmax);
+            den += num[j];
+        }
+        for (int j = 0; j < k; ++j) w[t * k + j] = (float)(num[j] / den);
     }
+    free(num);
     free(chosen);
 
     int64_t R = T * k;
@@ -303,27 +324,71 @@ void orc_route(const float* logits, int64_t T, int E, int k, int32_t* ids, float
 /* ------------------------------------------------------------------ */
 static double silu(double g) { return g / (1.0 + exp(-g)); }
 
-/* One NVFP4 linear over one input vector a[K] (already dequantised, fp64):
- * out[n] = sum_k a[k] * dec(q[n,k]) * dec(s[n,k/16]) for n < N. */
-static void nvfp4_matvec(const double* a, const uint8_t* codes, const uint8_t* scales,
-                         int64_t N, int64_t K, double* out) {
+/* Dequantised weights of one [N, K] tensor without the tensor scale,
+ * dec(q) * dec(s) per element, as float: exact, since the product of an
+ * e2m1 value and an e4m3 value has at most 6 significant bits and lies in
+ * [2^-10, 2688]. */
+static void dequant_f32(const uint8_t* codes, const uint8_t* scales, int64_t N, int64_t K, float* out) {
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k) out[n * K + k] = (float)deq(codes, scales, K, n, k);
+}
+
+/* One linear over one input vector a[K] (fp64) and dequantised weights
+ * W [N, K]: out[n] = sum_k a[k] * W[n, k], an fp64 sum in k order (every
+ * product is exact in fp64).  abs_out, if not NULL, receives
+ * sum_k |a[k] * W[n, k]| (the scale of the error bound of any fp32
+ * evaluation of the same sum). */
+static void matvec(const double* a, const float* W, int64_t N, int64_t K, double* out, double* abs_out) {
     for (int64_t n = 0; n < N; ++n) {
-        double s = 0.0;
-        for (int64_t k = 0; k < K; ++k) s += a[k] * deq(codes, scales, K, n, k);
+        const float* wr = W + n * K;
+        double s = 0.0, sa = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            const double p = a[k] * (double)wr[k];
+            s += p;
+            sa += fabs(p);
+        }
         out[n] = s;
+        if (abs_out) abs_out[n] = sa;
     }
 }
 
 /* Quantise a float vector with tensor scale gs and return it dequantised
- * (dec(q) * dec(s), no tensor scale) in fp64. */
-static void quant_dequant(const float* v, int64_t K, float gs, double* out) {
+ * (dec(q) * dec(s), no tensor scale) in fp64; the codes and scales are
+ * also written to c / s when those are not NULL. */
+static void quant_dequant(const float* v, int64_t K, float gs, double* out, uint8_t* c_out, uint8_t* s_out) {
     uint8_t* c = (uint8_t*)malloc((size_t)(K / 2));
     uint8_t* s = (uint8_t*)malloc((size_t)(K / 16));
     quantize_row(v, K, gs, c, s);
     for (int64_t k = 0; k < K; ++k) out[k] = deq(c, s, K, 0, k);
+    if (c_out) memcpy(c_out, c, (size_t)(K / 2));
+    if (s_out) memcpy(s_out, s, (size_t)(K / 16));
     free(c);
     free(s);
 }
+
+/* Optional outputs of orc_moe_layer_ex (any pointer may be NULL); n is the
+ * number of listed tokens:
+ *   out_pre [n, d]    sum_j w_j * Y_j before the final bf16 rounding
+ *   out_abs [n, d]    sum_j |w_j| * scale_j * sum_f |h_f * W_d[.,f]|: the
+ *                     scale of the error bound of an fp32 evaluation
+ *   g_pre, u_pre [n, k, F]  the gate / up values before their bf16 rounding
+ *   g_abs, u_abs [n, k, F]  their sums of |terms| times the same scales
+ *   h  [n, k, F]      h (bf16 values)
+ *   xq, xs [n, k, d/2], [n, k, d/16]  W4A4: the pair's NVFP4 x row
+ *   hq, hs [n, k, F/2], [n, k, F/16]  W4A4: the pair's NVFP4 h row */
+typedef struct {
+    double* out_pre;
+    double* out_abs;
+    double* g_pre;
+    double* u_pre;
+    double* g_abs;
+    double* u_abs;
+    float* h;
+    uint8_t* xq;
+    uint8_t* xs;
+    uint8_t* hq;
+    uint8_t* hs;
+} orc_layer_extras;
 
 /*
  * Routed-expert MoE layer for the tokens listed in `tokens` (n_tokens of
@@ -333,8 +398,124 @@ static void quant_dequant(const float* v, int64_t K, float gs, double* out) {
  * Weight banks are stacked over experts: gate/up codes [E, F, d/2], scales
  * [E, F, d/16], ws2 [E]; down codes [E, d, F/2], scales [E, d, F/16].
  * out[i, :] receives bf16(sum_j w_j * Y_j) for token tokens[i] (as float).
- * h_out, if not NULL, receives h [n_tokens, k, F] (the bf16 values).
+ * The (token, slot) pairs are grouped by expert so that each touched
+ * expert's three projections are dequantised once; every pair is then
+ * evaluated on its own, with the same fp64 sums in the same order.
  */
+void orc_moe_layer_ex(int mode, const uint16_t* x, int64_t T, int64_t d, int64_t F, int E, int k,
+                      const int32_t* ids, const float* w,
+                      const uint8_t* gq, const uint8_t* gs, const float* g_ws2,
+                      const uint8_t* uq, const uint8_t* us, const float* u_ws2,
+                      const uint8_t* dq, const uint8_t* ds, const float* d_ws2,
+                      const float* is13, const float* is2,
+                      const int32_t* tokens, int64_t n_tokens, float* out, const orc_layer_extras* ex) {
+    (void)T;
+    const int64_t n_pairs = n_tokens * k;
+    /* Y_j of every (token, slot) pair (and the |term| sums), then the
+     * weighted sum over the slots in slot order. */
+    double* Y = (double*)malloc(sizeof(double) * (size_t)(n_pairs * d));
+    double* Ya = (double*)malloc(sizeof(double) * (size_t)(n_pairs * d));
+    /* pairs grouped by expert (counting sort, pair order kept) */
+    int64_t* cnt = (int64_t*)calloc((size_t)E + 1, sizeof(int64_t));
+    int64_t* order = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n_pairs > 0 ? n_pairs : 1));
+    for (int64_t p = 0; p < n_pairs; ++p) cnt[ids[(int64_t)tokens[p / k] * k + p % k] + 1]++;
+    for (int e = 0; e < E; ++e) cnt[e + 1] += cnt[e];
+    {
+        int64_t* fill = (int64_t*)malloc(sizeof(int64_t) * (size_t)E);
+        for (int e = 0; e < E; ++e) fill[e] = cnt[e];
+        for (int64_t p = 0; p < n_pairs; ++p) order[fill[ids[(int64_t)tokens[p / k] * k + p % k]]++] = p;
+        free(fill);
+    }
+#pragma omp parallel
+    {
+        float* Wg = (float*)malloc(sizeof(float) * (size_t)(F * d));
+        float* Wu = (float*)malloc(sizeof(float) * (size_t)(F * d));
+        float* Wd = (float*)malloc(sizeof(float) * (size_t)(d * F));
+        float* xrow = (float*)malloc(sizeof(float) * (size_t)d);
+        double* xa = (double*)malloc(sizeof(double) * (size_t)d);
+        double* sg = (double*)malloc(sizeof(double) * (size_t)F);
+        double* su = (double*)malloc(sizeof(double) * (size_t)F);
+        double* ag = (double*)malloc(sizeof(double) * (size_t)F);
+        double* au = (double*)malloc(sizeof(double) * (size_t)F);
+        float* h = (float*)malloc(sizeof(float) * (size_t)F);
+        double* ha = (double*)malloc(sizeof(double) * (size_t)F);
+        double* y = (double*)malloc(sizeof(double) * (size_t)d);
+        double* ya = (double*)malloc(sizeof(double) * (size_t)d);
+#pragma omp for schedule(dynamic, 1)
+        for (int e = 0; e < E; ++e) {
+            if (cnt[e + 1] == cnt[e]) continue;
+            dequant_f32(gq + (int64_t)e * F * (d / 2), gs + (int64_t)e * F * (d / 16), F, d, Wg);
+            dequant_f32(uq + (int64_t)e * F * (d / 2), us + (int64_t)e * F * (d / 16), F, d, Wu);
+            dequant_f32(dq + (int64_t)e * d * (F / 2), ds + (int64_t)e * d * (F / 16), d, F, Wd);
+            for (int64_t q = cnt[e]; q < cnt[e + 1]; ++q) {
+                const int64_t pair = order[q];
+                const int64_t i = pair / k;
+                const int64_t t = tokens[i];
+                for (int64_t n = 0; n < d; ++n) xrow[n] = bf16_bits_to_float(x[t * d + n]);
+                double xscale = 1.0;
+                if (mode == 1) {
+                    quant_dequant(xrow, d, is13[e], xa, ex && ex->xq ? ex->xq + pair * (d / 2) : NULL,
+                                  ex && ex->xs ? ex->xs + pair * (d / 16) : NULL);
+                    xscale = (double)is13[e];
+                } else {
+                    for (int64_t n = 0; n < d; ++n) xa[n] = (double)xrow[n];
+                }
+                matvec(xa, Wg, F, d, sg, ag);
+                matvec(xa, Wu, F, d, su, au);
+                for (int64_t f = 0; f < F; ++f) {
+                    const double gp = sg[f] * xscale * (double)g_ws2[e];
+                    const double up = su[f] * xscale * (double)u_ws2[e];
+                    const double G = orc_round_bf16(gp);
+                    const double U = orc_round_bf16(up);
+                    h[f] = (float)orc_round_bf16(silu(G) * U);
+                    if (ex) {
+                        const int64_t o = pair * F + f;
+                        if (ex->g_pre) ex->g_pre[o] = gp;
+                        if (ex->u_pre) ex->u_pre[o] = up;
+                        if (ex->g_abs) ex->g_abs[o] = ag[f] * xscale * (double)g_ws2[e];
+                        if (ex->u_abs) ex->u_abs[o] = au[f] * xscale * (double)u_ws2[e];
+                        if (ex->h) ex->h[o] = h[f];
+                    }
+                }
+                double hscale = 1.0;
+                if (mode == 1) {
+                    quant_dequant(h, F, is2[e], ha, ex && ex->hq ? ex->hq + pair * (F / 2) : NULL,
+                                  ex && ex->hs ? ex->hs + pair * (F / 16) : NULL);
+                    hscale = (double)is2[e];
+                } else {
+                    for (int64_t f = 0; f < F; ++f) ha[f] = (double)h[f];
+                }
+                matvec(ha, Wd, d, F, y, ya);
+                for (int64_t n = 0; n < d; ++n) {
+                    Y[pair * d + n] = y[n] * hscale * (double)d_ws2[e];
+                    Ya[pair * d + n] = ya[n] * hscale * (double)d_ws2[e];
+                }
+            }
+        }
+        free(Wg); free(Wu); free(Wd); free(xrow); free(xa); free(sg); free(su); free(ag); free(au);
+        free(h); free(ha); free(y); free(ya);
+    }
+    for (int64_t i = 0; i < n_tokens; ++i) {
+        int64_t t = tokens[i];
+        for (int64_t n = 0; n < d; ++n) {
+            double acc = 0.0, aabs = 0.0;
+            for (int j = 0; j < k; ++j) {
+                acc += (double)w[t * k + j] * Y[(i * k + j) * d + n];
+                aabs += fabs((double)w[t * k + j]) * Ya[(i * k + j) * d + n];
+            }
+            out[i * d + n] = (float)orc_round_bf16(acc);
+            if (ex && ex->out_pre) ex->out_pre[i * d + n] = acc;
+            if (ex && ex->out_abs) ex->out_abs[i * d + n] = aabs;
+        }
+    }
+    free(order);
+    free(cnt);
+    free(Y);
+    free(Ya);
+}
+
+/* The layer's plain form: out only, plus h [n_tokens, k, F] if h_out is
+ * not NULL. */
 void orc_moe_layer(int mode, const uint16_t* x, int64_t T, int64_t d, int64_t F, int E, int k,
                    const int32_t* ids, const float* w,
                    const uint8_t* gq, const uint8_t* gs, const float* g_ws2,
@@ -342,65 +523,11 @@ void orc_moe_layer(int mode, const uint16_t* x, int64_t T, int64_t d, int64_t F,
                    const uint8_t* dq, const uint8_t* ds, const float* d_ws2,
                    const float* is13, const float* is2,
                    const int32_t* tokens, int64_t n_tokens, float* out, float* h_out) {
-    (void)T;
-    (void)E;
-    /* Y_j of every (token, slot) pair, then the weighted sum over the slots
-     * in slot order.  Pairs are independent, so they are spread over the
-     * threads; the sum itself is sequential. */
-    double* Y = (double*)malloc(sizeof(double) * (size_t)(n_tokens * k * d));
-#pragma omp parallel
-    {
-        float* xrow = (float*)malloc(sizeof(float) * (size_t)d);
-        double* xa = (double*)malloc(sizeof(double) * (size_t)d);
-        double* sg = (double*)malloc(sizeof(double) * (size_t)F);
-        double* su = (double*)malloc(sizeof(double) * (size_t)F);
-        float* h = (float*)malloc(sizeof(float) * (size_t)F);
-        double* ha = (double*)malloc(sizeof(double) * (size_t)F);
-        double* y = (double*)malloc(sizeof(double) * (size_t)d);
-#pragma omp for schedule(dynamic, 1)
-        for (int64_t pair = 0; pair < n_tokens * k; ++pair) {
-            int64_t i = pair / k;
-            int j = (int)(pair % k);
-            int64_t t = tokens[i];
-            int e = ids[t * k + j];
-            for (int64_t n = 0; n < d; ++n) xrow[n] = bf16_bits_to_float(x[t * d + n]);
-            double xscale = 1.0;
-            if (mode == 1) {
-                quant_dequant(xrow, d, is13[e], xa);
-                xscale = (double)is13[e];
-            } else {
-                for (int64_t n = 0; n < d; ++n) xa[n] = (double)xrow[n];
-            }
-            nvfp4_matvec(xa, gq + (int64_t)e * F * (d / 2), gs + (int64_t)e * F * (d / 16), F, d, sg);
-            nvfp4_matvec(xa, uq + (int64_t)e * F * (d / 2), us + (int64_t)e * F * (d / 16), F, d, su);
-            for (int64_t f = 0; f < F; ++f) {
-                double G = orc_round_bf16(sg[f] * xscale * (double)g_ws2[e]);
-                double U = orc_round_bf16(su[f] * xscale * (double)u_ws2[e]);
-                h[f] = (float)orc_round_bf16(silu(G) * U);
-            }
-            if (h_out)
-                for (int64_t f = 0; f < F; ++f) h_out[(i * k + j) * F + f] = h[f];
-            double hscale = 1.0;
-            if (mode == 1) {
-                quant_dequant(h, F, is2[e], ha);
-                hscale = (double)is2[e];
-            } else {
-                for (int64_t f = 0; f < F; ++f) ha[f] = (double)h[f];
-            }
-            nvfp4_matvec(ha, dq + (int64_t)e * d * (F / 2), ds + (int64_t)e * d * (F / 16), d, F, y);
-            for (int64_t n = 0; n < d; ++n) Y[pair * d + n] = y[n] * hscale * (double)d_ws2[e];
-        }
-        free(xrow); free(xa); free(sg); free(su); free(h); free(ha); free(y);
-    }
-    for (int64_t i = 0; i < n_tokens; ++i) {
-        int64_t t = tokens[i];
-        for (int64_t n = 0; n < d; ++n) {
-            double acc = 0.0;
-            for (int j = 0; j < k; ++j) acc += (double)w[t * k + j] * Y[(i * k + j) * d + n];
-            out[i * d + n] = (float)orc_round_bf16(acc);
-        }
-    }
-    free(Y);
+    orc_layer_extras ex;
+    memset(&ex, 0, sizeof ex);
+    ex.h = h_out;
+    orc_moe_layer_ex(mode, x, T, d, F, E, k, ids, w, gq, gs, g_ws2, uq, us, u_ws2, dq, ds, d_ws2, is13, is2,
+                     tokens, n_tokens, out, &ex);
 }
 
 /*
@@ -410,33 +537,60 @@ void orc_moe_layer(int mode, const uint16_t* x, int64_t T, int64_t d, int64_t F,
  *   G = bf16(sum x*wg)   U = bf16(sum x*wu)   h = bf16(silu(G) * U)
  *   out = bf16(routed + sum h*wd)
  * x [T, d], wg, wu [Fs, d], wd [d, Fs], routed/out [T, d] (bf16 bits);
- * fp64 sums in k order.
+ * fp64 sums in k order.  Optional outputs (NULL to skip): out_pre [T, d]
+ * (routed + y before the final rounding), out_abs [T, d] (|routed| +
+ * sum |h wd|), g_pre / u_pre / g_abs / u_abs [T, Fs] (the gate / up sums
+ * before rounding and their sums of |terms|), h_out [T, Fs].
  */
-void orc_shared_expert(const uint16_t* x, int64_t T, int64_t d, const uint16_t* wg, const uint16_t* wu,
-                       const uint16_t* wd, int64_t Fs, const uint16_t* routed, float* out) {
+void orc_shared_expert_ex(const uint16_t* x, int64_t T, int64_t d, const uint16_t* wg, const uint16_t* wu,
+                          const uint16_t* wd, int64_t Fs, const uint16_t* routed, float* out, double* out_pre,
+                          double* out_abs, double* g_pre, double* u_pre, double* g_abs, double* u_abs,
+                          float* h_out) {
 #pragma omp parallel
     {
         double* h = (double*)malloc(sizeof(double) * (size_t)Fs);
 #pragma omp for schedule(dynamic, 1)
         for (int64_t t = 0; t < T; ++t) {
             for (int64_t f = 0; f < Fs; ++f) {
-                double g = 0.0, u = 0.0;
+                double g = 0.0, u = 0.0, ga = 0.0, ua = 0.0;
                 for (int64_t k = 0; k < d; ++k) {
                     const double xv = bf16_bits_to_float(x[t * d + k]);
-                    g += xv * bf16_bits_to_float(wg[f * d + k]);
-                    u += xv * bf16_bits_to_float(wu[f * d + k]);
+                    const double pg = xv * bf16_bits_to_float(wg[f * d + k]);
+                    const double pu = xv * bf16_bits_to_float(wu[f * d + k]);
+                    g += pg;
+                    u += pu;
+                    ga += fabs(pg);
+                    ua += fabs(pu);
                 }
                 const double G = orc_round_bf16(g), U = orc_round_bf16(u);
                 h[f] = orc_round_bf16(silu(G) * U);
+                if (g_pre) g_pre[t * Fs + f] = g;
+                if (u_pre) u_pre[t * Fs + f] = u;
+                if (g_abs) g_abs[t * Fs + f] = ga;
+                if (u_abs) u_abs[t * Fs + f] = ua;
+                if (h_out) h_out[t * Fs + f] = (float)h[f];
             }
             for (int64_t n = 0; n < d; ++n) {
-                double y = 0.0;
-                for (int64_t f = 0; f < Fs; ++f) y += h[f] * bf16_bits_to_float(wd[n * Fs + f]);
-                out[t * d + n] = (float)orc_round_bf16((double)bf16_bits_to_float(routed[t * d + n]) + y);
+                double y = 0.0, ya = 0.0;
+                for (int64_t f = 0; f < Fs; ++f) {
+                    const double p = h[f] * bf16_bits_to_float(wd[n * Fs + f]);
+                    y += p;
+                    ya += fabs(p);
+                }
+                const double r = (double)bf16_bits_to_float(routed[t * d + n]);
+                out[t * d + n] = (float)orc_round_bf16(r + y);
+                if (out_pre) out_pre[t * d + n] = r + y;
+                if (out_abs) out_abs[t * d + n] = fabs(r) + ya;
             }
         }
         free(h);
     }
+}
+
+/* The shared expert's plain form (out only). */
+void orc_shared_expert(const uint16_t* x, int64_t T, int64_t d, const uint16_t* wg, const uint16_t* wu,
+                       const uint16_t* wd, int64_t Fs, const uint16_t* routed, float* out) {
+    orc_shared_expert_ex(x, T, d, wg, wu, wd, Fs, routed, out, NULL, NULL, NULL, NULL, NULL, NULL, NULL);
 }
 
 /*
@@ -444,32 +598,64 @@ void orc_shared_expert(const uint16_t* x, int64_t T, int64_t d, const uint16_t* 
  * gate and up apart because their tensor scales differ).
  * Without w_up:  out = bf16(ws2 * sum x*w)                     [M, N]
  * With w_up:     out = bf16(silu(bf16(ws2*sum x*w)) * bf16(ws2u*sum x*wu))
+ * Optional outputs (NULL to skip), all [M, N] fp64: pre = the value before
+ * the final bf16 rounding; g_pre / u_pre = the gate / up values before
+ * their rounding, g_abs / u_abs their sums of |terms| times the tensor
+ * scale (without w_up only g_pre / g_abs are written, g_pre = pre).
  */
-void orc_linear(const uint16_t* x, int64_t M, int64_t K,
-                const uint8_t* wq, const uint8_t* ws, float ws2, int64_t N,
-                const uint8_t* uq, const uint8_t* us, float us2, float* out) {
+void orc_linear_ex(const uint16_t* x, int64_t M, int64_t K,
+                   const uint8_t* wq, const uint8_t* ws, float ws2, int64_t N,
+                   const uint8_t* uq, const uint8_t* us, float us2, float* out,
+                   double* pre, double* g_pre, double* u_pre, double* g_abs, double* u_abs) {
+    float* Wg = (float*)malloc(sizeof(float) * (size_t)(N * K));
+    float* Wu = uq ? (float*)malloc(sizeof(float) * (size_t)(N * K)) : NULL;
+    dequant_f32(wq, ws, N, K, Wg);
+    if (uq) dequant_f32(uq, us, N, K, Wu);
 #pragma omp parallel
     {
         double* xa = (double*)malloc(sizeof(double) * (size_t)K);
         double* sg = (double*)malloc(sizeof(double) * (size_t)N);
         double* su = (double*)malloc(sizeof(double) * (size_t)N);
+        double* ag = (double*)malloc(sizeof(double) * (size_t)N);
+        double* au = (double*)malloc(sizeof(double) * (size_t)N);
 #pragma omp for schedule(dynamic, 1)
         for (int64_t m = 0; m < M; ++m) {
             for (int64_t kk = 0; kk < K; ++kk) xa[kk] = (double)bf16_bits_to_float(x[m * K + kk]);
-            nvfp4_matvec(xa, wq, ws, N, K, sg);
+            matvec(xa, Wg, N, K, sg, ag);
             if (uq) {
-                nvfp4_matvec(xa, uq, us, N, K, su);
+                matvec(xa, Wu, N, K, su, au);
                 for (int64_t n = 0; n < N; ++n) {
-                    double G = orc_round_bf16(sg[n] * (double)ws2);
-                    double U = orc_round_bf16(su[n] * (double)us2);
-                    out[m * N + n] = (float)orc_round_bf16(silu(G) * U);
+                    const double gp = sg[n] * (double)ws2, up = su[n] * (double)us2;
+                    double G = orc_round_bf16(gp);
+                    double U = orc_round_bf16(up);
+                    const double hp = silu(G) * U;
+                    out[m * N + n] = (float)orc_round_bf16(hp);
+                    if (pre) pre[m * N + n] = hp;
+                    if (g_pre) g_pre[m * N + n] = gp;
+                    if (u_pre) u_pre[m * N + n] = up;
+                    if (g_abs) g_abs[m * N + n] = ag[n] * (double)ws2;
+                    if (u_abs) u_abs[m * N + n] = au[n] * (double)us2;
                 }
             } else {
-                for (int64_t n = 0; n < N; ++n) out[m * N + n] = (float)orc_round_bf16(sg[n] * (double)ws2);
+                for (int64_t n = 0; n < N; ++n) {
+                    const double gp = sg[n] * (double)ws2;
+                    out[m * N + n] = (float)orc_round_bf16(gp);
+                    if (pre) pre[m * N + n] = gp;
+                    if (g_pre) g_pre[m * N + n] = gp;
+                    if (g_abs) g_abs[m * N + n] = ag[n] * (double)ws2;
+                }
             }
         }
-        free(xa); free(sg); free(su);
+        free(xa); free(sg); free(su); free(ag); free(au);
     }
+    free(Wg);
+    free(Wu);
+}
+
+void orc_linear(const uint16_t* x, int64_t M, int64_t K,
+                const uint8_t* wq, const uint8_t* ws, float ws2, int64_t N,
+                const uint8_t* uq, const uint8_t* us, float us2, float* out) {
+    orc_linear_ex(x, M, K, wq, ws, ws2, N, uq, us, us2, out, NULL, NULL, NULL, NULL, NULL);
 }
 
 int orc_num_threads(void) {

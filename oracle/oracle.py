@@ -43,6 +43,12 @@ def _P(t):
     return ctypes.POINTER(t)
 
 
+class _LayerExtras(ctypes.Structure):
+    """Mirror of orc_layer_extras (optional outputs of orc_moe_layer_ex)."""
+    _fields_ = [(n, ctypes.c_void_p) for n in ("out_pre", "out_abs", "g_pre", "u_pre", "g_abs", "u_abs", "h",
+                                                 "xq", "xs", "hq", "hs")]
+
+
 def bind(L):
     """Declare the C signatures on a loaded oracle library."""
     i64, i32, f32 = ctypes.c_int64, ctypes.c_int, ctypes.c_float
@@ -63,10 +69,15 @@ def bind(L):
     L.orc_route.argtypes = [vp, i64, i32, i32, vp, vp, vp, vp, vp]
     L.orc_router_logits.argtypes = [vp, i64, i64, vp, i64, vp, vp]
     L.orc_shared_expert.argtypes = [vp, i64, i64, vp, vp, vp, i64, vp, vp]
+    L.orc_shared_expert_ex.argtypes = [vp, i64, i64, vp, vp, vp, i64, vp, vp] + [vp] * 7
     L.orc_moe_layer.argtypes = [i32, vp, i64, i64, i64, i32, i32, vp, vp,
                                 vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                 vp, vp, vp, i64, vp, vp]
+    L.orc_moe_layer_ex.argtypes = [i32, vp, i64, i64, i64, i32, i32, vp, vp,
+                                   vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                   vp, vp, vp, i64, vp, ctypes.POINTER(_LayerExtras)]
     L.orc_linear.argtypes = [vp, i64, i64, vp, vp, f32, i64, vp, vp, f32, vp]
+    L.orc_linear_ex.argtypes = [vp, i64, i64, vp, vp, f32, i64, vp, vp, f32, vp, vp, vp, vp, vp, vp]
     L.orc_num_threads.restype = i32
     return L
 
@@ -228,6 +239,47 @@ def moe_layer(mode: str, x_bf16_bits, ids, w, bank, tokens=None, is13=None, is2=
     return (out, h) if want_h else out
 
 
+def moe_layer_ex(mode: str, x_bf16_bits, ids, w, bank, tokens=None, is13=None, is2=None):
+    """The layer for ``tokens`` with every optional output (see
+    ``orc_moe_layer_ex``): dict with out [n, d] (bf16 values), out_pre and
+    out_abs [n, d] fp64, g_pre / u_pre / g_abs / u_abs [n, k, F] fp64,
+    h [n, k, F], and for W4A4 the pairs' NVFP4 rows xq [n, k, d/2],
+    xs [n, k, d/16], hq [n, k, F/2], hs [n, k, F/16]."""
+    x = _c(x_bf16_bits, np.uint16)
+    T, d = x.shape
+    ids = _c(ids, np.int32)
+    w = _c(w, np.float32)
+    k = ids.shape[1]
+    gq, gs, g2 = bank["gate"]
+    uq, us, u2 = bank["up"]
+    dq, ds, d2 = bank["down"]
+    E, F = gq.shape[0], gq.shape[1]
+    arrs = [_c(a, np.uint8) for a in (gq, gs, uq, us, dq, ds)]
+    ws2s = [_c(a, np.float32) for a in (g2, u2, d2)]
+    if tokens is None:
+        tokens = np.arange(T, dtype=np.int32)
+    tokens = _c(tokens, np.int32)
+    n = tokens.shape[0]
+    m = 0 if mode == "w4a16" else 1
+    if m == 1:
+        is13 = _c(is13, np.float32)
+        is2 = _c(is2, np.float32)
+    r = dict(out=np.zeros((n, d), np.float32), out_pre=np.zeros((n, d)), out_abs=np.zeros((n, d)),
+             g_pre=np.zeros((n, k, F)), u_pre=np.zeros((n, k, F)), g_abs=np.zeros((n, k, F)),
+             u_abs=np.zeros((n, k, F)), h=np.zeros((n, k, F), np.float32))
+    if m == 1:
+        r.update(xq=np.zeros((n, k, d // 2), np.uint8), xs=np.zeros((n, k, d // 16), np.uint8),
+                 hq=np.zeros((n, k, F // 2), np.uint8), hs=np.zeros((n, k, F // 16), np.uint8))
+    ex = _LayerExtras(*[_ptr(r.get(nm)) for nm, _ in _LayerExtras._fields_])
+    lib().orc_moe_layer_ex(m, _ptr(x), T, d, F, E, k, _ptr(ids), _ptr(w),
+                           _ptr(arrs[0]), _ptr(arrs[1]), _ptr(ws2s[0]),
+                           _ptr(arrs[2]), _ptr(arrs[3]), _ptr(ws2s[1]),
+                           _ptr(arrs[4]), _ptr(arrs[5]), _ptr(ws2s[2]),
+                           _ptr(is13) if m == 1 else None, _ptr(is2) if m == 1 else None,
+                           _ptr(tokens), n, _ptr(r["out"]), ctypes.byref(ex))
+    return r
+
+
 def shared_expert(x_bf16_bits, wg_bits, wu_bits, wd_bits, routed_bf16_bits):
     """BF16 shared-expert MLP added to the routed output, fp32 [T, d] of
     bf16 values: bf16(routed + bf16(silu(bf16 xWg^T) * bf16 xWu^T) Wd^T)."""
@@ -239,6 +291,23 @@ def shared_expert(x_bf16_bits, wg_bits, wu_bits, wd_bits, routed_bf16_bits):
     out = np.zeros((T, d), np.float32)
     lib().orc_shared_expert(_ptr(x), T, d, _ptr(wg), _ptr(wu), _ptr(wd), Fs, _ptr(r), _ptr(out))
     return out
+
+
+def shared_expert_ex(x_bf16_bits, wg_bits, wu_bits, wd_bits, routed_bf16_bits):
+    """``shared_expert`` with its optional outputs: dict with out, out_pre,
+    out_abs [T, d] and g_pre, u_pre, g_abs, u_abs, h [T, Fs]."""
+    x = _c(x_bf16_bits, np.uint16)
+    wg, wu, wd = (_c(w, np.uint16) for w in (wg_bits, wu_bits, wd_bits))
+    rt = _c(routed_bf16_bits, np.uint16)
+    T, d = x.shape
+    Fs = wg.shape[0]
+    r = dict(out=np.zeros((T, d), np.float32), out_pre=np.zeros((T, d)), out_abs=np.zeros((T, d)),
+             g_pre=np.zeros((T, Fs)), u_pre=np.zeros((T, Fs)), g_abs=np.zeros((T, Fs)), u_abs=np.zeros((T, Fs)),
+             h=np.zeros((T, Fs), np.float32))
+    lib().orc_shared_expert_ex(_ptr(x), T, d, _ptr(wg), _ptr(wu), _ptr(wd), Fs, _ptr(rt), _ptr(r["out"]),
+                               *[_ptr(r[n]) for n in ("out_pre", "out_abs", "g_pre", "u_pre", "g_abs", "u_abs",
+                                                      "h")])
+    return r
 
 
 def linear(x_bf16_bits, wq, ws, ws2, wup=None):
@@ -258,3 +327,26 @@ def linear(x_bf16_bits, wq, ws, ws2, wup=None):
     lib().orc_linear(_ptr(x), M, K, _ptr(wq), _ptr(ws), float(ws2), N, _ptr(uq), _ptr(us), u2,
                      _ptr(out))
     return out
+
+
+def linear_ex(x_bf16_bits, wq, ws, ws2, wup=None):
+    """``linear`` with its optional outputs: dict with out [M, N] (bf16
+    values), pre (before the final rounding), g_pre / g_abs and, with
+    ``wup``, u_pre / u_abs, all [M, N] fp64."""
+    x = _c(x_bf16_bits, np.uint16)
+    M, K = x.shape
+    wq = _c(wq, np.uint8)
+    ws = _c(ws, np.uint8)
+    N = wq.shape[0]
+    r = dict(out=np.zeros((M, N), np.float32), pre=np.zeros((M, N)), g_pre=np.zeros((M, N)),
+             g_abs=np.zeros((M, N)))
+    if wup is not None:
+        uq, us, u2 = _c(wup[0], np.uint8), _c(wup[1], np.uint8), float(wup[2])
+        r.update(u_pre=np.zeros((M, N)), u_abs=np.zeros((M, N)))
+    else:
+        uq = us = None
+        u2 = 0.0
+    lib().orc_linear_ex(_ptr(x), M, K, _ptr(wq), _ptr(ws), float(ws2), N, _ptr(uq), _ptr(us), u2,
+                        _ptr(r["out"]), _ptr(r["pre"]), _ptr(r["g_pre"]), _ptr(r.get("u_pre")),
+                        _ptr(r["g_abs"]), _ptr(r.get("u_abs")))
+    return r

@@ -6,6 +6,6 @@ The compute path is the CUDA library under ``csrc/`` (built in-tree by
 """
 from ._lib import (MoEWeights, NVFP4Tensor, Nvfp4Error, launch_count, load, moe_route_permute,  # noqa: F401
                    moe_router_logits, moe_shared_expert,
-                   moe_workspace, moe_workspace_size, moe_workspace_views, nvfp4_linear, nvfp4_moe_w4a4,
-                   nvfp4_moe_w4a16, nvfp4_quantize_act, nvfp4_quantize_weights, profile_collect,
-                   profile_enable, selftest_bounded_wait, status_string)
+                   moe_workspace, moe_workspace_intermediates, moe_workspace_size, moe_workspace_views,
+                   nvfp4_linear, nvfp4_moe_w4a4, nvfp4_moe_w4a16, nvfp4_quantize_act, nvfp4_quantize_weights,
+                   profile_collect, profile_enable, selftest_bounded_wait, set_kernel_choice, status_string)

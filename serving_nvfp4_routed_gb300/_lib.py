@@ -24,7 +24,8 @@ STATUS = {0: "NVFP4_OK", 1: "NVFP4_ERR_INVALID_ARG", 2: "NVFP4_ERR_SHAPE", 3: "N
 
 EXPORTS = ("nvfp4_quantize_weights", "nvfp4_quantize_weights_workspace_size", "nvfp4_quantize_act",
            "moe_route_permute", "moe_route_permute_workspace_size", "nvfp4_moe_w4a16", "nvfp4_moe_w4a4",
-           "nvfp4_moe_workspace_size", "nvfp4_moe_workspace_views", "nvfp4_linear",
+           "nvfp4_moe_workspace_size", "nvfp4_moe_workspace_views", "nvfp4_moe_workspace_intermediates",
+           "nvfp4_set_kernel_choice", "nvfp4_linear",
            "nvfp4_linear_workspace_size", "nvfp4_status_string", "nvfp4_launch_count",
            "nvfp4_profile_enable", "nvfp4_profile_collect", "nvfp4_quantize_weights_noalloc",
            "nvfp4_quantize_weights_noalloc_max_batch", "nvfp4_selftest_bounded_wait", "moe_router_logits",
@@ -74,6 +75,8 @@ def load(path: str = LIB_PATH):
         L.nvfp4_moe_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
         L.nvfp4_moe_workspace_size.restype = sz
         L.nvfp4_moe_workspace_views.argtypes = [vp, i32, i32, i32, i32, i32, i32] + [ctypes.POINTER(vp)] * 5
+        L.nvfp4_moe_workspace_intermediates.argtypes = [vp, i32, i32, i32, i32, i32, i32] + [ctypes.POINTER(vp)] * 5
+        L.nvfp4_set_kernel_choice.argtypes = [i32]
         L.nvfp4_linear.argtypes = [vp, i32, i32, ctypes.POINTER(_W), i32, ctypes.POINTER(_W), vp, vp, sz, vp]
         L.nvfp4_linear_workspace_size.argtypes = [i32, i32, i32]
         L.nvfp4_linear_workspace_size.restype = sz
@@ -270,6 +273,42 @@ def moe_workspace_views(ws: torch.Tensor, T, E, top_k, d, F, mode) -> dict:
     return dict(ids=view(ptrs[0], R, torch.int32).view(T, top_k), w=view(ptrs[1], R, torch.float32).view(T, top_k),
                 offsets=view(ptrs[2], E + 1, torch.int32), row_to_slot=view(ptrs[3], R, torch.int32),
                 slot_to_row=view(ptrs[4], R, torch.int32))
+
+
+def moe_workspace_intermediates(ws: torch.Tensor, T, E, top_k, d, F, mode) -> dict:
+    """Tensor views of the per-row intermediates inside an MoE workspace
+    (rows in the permuted, expert-contiguous order): W4A16 h [R, F] bf16;
+    W4A4 xq [R, d/2], xs [R, d/16], hq [R, F/2], hs [R, F/16] uint8."""
+    L = load()
+    ptrs = [ctypes.c_void_p() for _ in range(5)]
+    m = 0 if mode == "w4a16" else 1
+    _check("nvfp4_moe_workspace_intermediates",
+           L.nvfp4_moe_workspace_intermediates(_p(ws), T, E, top_k, d, F, m, *[ctypes.byref(p) for p in ptrs]))
+    base = ws.data_ptr()
+    R = T * top_k
+
+    def view(p, shape, dtype):
+        n = 1
+        for v in shape:
+            n *= v
+        esz = torch.tensor([], dtype=dtype).element_size()
+        off = p.value - base
+        return ws[off:off + n * esz].view(dtype).view(*shape)
+
+    if m == 0:
+        return dict(h=view(ptrs[0], (R, F), torch.bfloat16))
+    return dict(xq=view(ptrs[1], (R, d // 2), torch.uint8), xs=view(ptrs[2], (R, d // 16), torch.uint8),
+                hq=view(ptrs[3], (R, F // 2), torch.uint8), hs=view(ptrs[4], (R, F // 16), torch.uint8))
+
+
+KERNEL_CHOICE = {"auto": 0, "gemv": 1, "tc": 2}
+
+
+def set_kernel_choice(choice: str = "auto") -> None:
+    """Which kernels later layer / linear calls run: "auto" (by shape),
+    "gemv" (decode-shaped) or "tc" (prompt-shaped tensor-core kernels where
+    the shapes allow them).  Process-wide; for tests and measurements."""
+    _check("nvfp4_set_kernel_choice", load().nvfp4_set_kernel_choice(KERNEL_CHOICE[choice]))
 
 
 def _moe(mode, x, logits, top_k, weights: MoEWeights, is13=None, is2=None, out=None, ws=None,

@@ -1,5 +1,6 @@
 // api_common.cu -- status strings, launch accounting and optional per-kernel
 // event timing for libnvfp4moe.
+#include <atomic>
 #include <cstdlib>
 #include <cstring>
 #include <map>
@@ -15,6 +16,7 @@ namespace {
 
 std::mutex g_mu;
 unsigned long long g_launches = 0;
+std::atomic<int> g_kernel_choice{0};
 bool g_profile = false;
 
 struct Pending {
@@ -73,6 +75,8 @@ bool pdl_enabled() {
     return v == 1;
 }
 
+int kernel_choice() { return g_kernel_choice.load(std::memory_order_relaxed); }
+
 int num_sms() {
     static int n = 0;
     if (n == 0) {
@@ -108,6 +112,12 @@ extern "C" const char* nvfp4_status_string(nvfp4_status s) {
         case NVFP4_ERR_DEVICE_INPUT: return "NVFP4_ERR_DEVICE_INPUT";
     }
     return "NVFP4_ERR_UNKNOWN";
+}
+
+extern "C" nvfp4_status nvfp4_set_kernel_choice(int choice) {
+    if (choice < 0 || choice > 2) return NVFP4_ERR_INVALID_ARG;
+    g_kernel_choice.store(choice, std::memory_order_relaxed);
+    return NVFP4_OK;
 }
 
 extern "C" uint64_t nvfp4_launch_count(void) {

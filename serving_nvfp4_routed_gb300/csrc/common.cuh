@@ -20,6 +20,8 @@ void launch_begin(const char* name, cudaStream_t s);
 void launch_end(const char* name, cudaStream_t s);
 int num_sms();
 int device_cc_major();
+// nvfp4_set_kernel_choice: 0 by shape, 1 decode-shaped, 2 prompt-shaped.
+int kernel_choice();
 
 #define NVFP4_LAUNCH(name, stream, ...)            \
     do {                                           \

@@ -35,11 +35,15 @@ void launch_route(const float* logits, int T, int E, int top_k, RouteArrays ra, 
                   cudaStream_t s);
 
 void launch_zero(void* p, size_t bytes, cudaStream_t s);
-// The two passes of the weight recipe (defined in quant.cu).
-__global__ void tensor_amax_kernel(const uint16_t* __restrict__ w, size_t n_per, float* __restrict__ amax);
-__global__ void quantize_weights_kernel(const uint16_t* __restrict__ w, size_t n_per, int batch,
-                                        const float* __restrict__ amax, uint8_t* __restrict__ codes,
-                                        uint8_t* __restrict__ scales, float* __restrict__ ws2_out);
+// The weight recipe (quant.cu): argument checks, then the amax pass and the
+// block pass with `amax` ([batch] floats, cleared first) as scratch.  The
+// amax pass runs one grid row per tensor, so batch is limited to the grid's
+// y extent.
+constexpr int kMaxRecipeBatch = 65535;
+nvfp4_status check_weight_recipe(const uint16_t* w, int batch, int N, int K, const uint8_t* codes,
+                                 const uint8_t* scales, const float* weight_scale_2);
+nvfp4_status launch_weight_recipe(const uint16_t* w, int batch, int N, int K, float* amax, uint8_t* codes,
+                                  uint8_t* scales, float* weight_scale_2, cudaStream_t stream);
 void launch_quantize_act(const uint16_t* x, int M, int K, const int32_t* row_to_slot, int top_k,
                          const float* input_scale, const int32_t* offsets, int E, uint8_t* codes,
                          uint8_t* scales, cudaStream_t s);

@@ -8,11 +8,13 @@
 // (static input_scale).  Launch sequence of one layer call:
 //   route + permutation (also clears the counters)
 //   [W4A4: static-scale act-quant of the permuted rows]
-//   gate/up + SwiGLU (also zeroes the fp32 combine accumulator)
-//   down + weighted combine (fp32 red.add); the CTA that adds a token's last
-//   contribution writes that token's bf16 output row
+//   gate/up + SwiGLU (h per routed row; W4A4: h requantised to NVFP4)
+//   down + weighted top-k combine:
+//     decode-shaped kernels: fp32 red.add into a [T, d] accumulator, and the
+//       CTA that adds a token's last contribution writes its bf16 row;
+//     prompt-shaped kernels: w * y written per routed row, then each token's
+//       k rows summed in slot order (deterministic, chunk-invariant).
 #include <climits>
-#include <cstdlib>
 #include <cstring>
 
 #include "common.cuh"
@@ -43,13 +45,10 @@ struct MoeWs {
 
 bool tc_possible(int mode, int d, int F) { return mode == 0 && d % 128 == 0 && F % 128 == 0; }
 
-// NVFP4_PATH=gemv|tc forces a path (tests exercise both at every size).
+// nvfp4_set_kernel_choice: -1 by shape, 0 decode-shaped, 1 prompt-shaped.
 int forced_path() {
-    const char* e = std::getenv("NVFP4_PATH");
-    if (!e) return -1;
-    if (!std::strcmp(e, "gemv")) return 0;
-    if (!std::strcmp(e, "tc")) return 1;
-    return -1;
+    const int c = kernel_choice();
+    return c == 0 ? -1 : c - 1;
 }
 
 // Tensor cores once the experts average 32 or more routed rows.
@@ -440,6 +439,20 @@ extern "C" nvfp4_status nvfp4_moe_workspace_views(void* ws, int T, int E, int to
     if (expert_offsets) *expert_offsets = w.ra.offsets;
     if (row_to_slot) *row_to_slot = w.ra.row_to_slot;
     if (slot_to_row) *slot_to_row = w.ra.slot_to_row;
+    return NVFP4_OK;
+}
+
+extern "C" nvfp4_status nvfp4_moe_workspace_intermediates(void* ws, int T, int E, int top_k, int d, int F,
+                                                          int mode, uint16_t** h_bf16, uint8_t** xq, uint8_t** xs,
+                                                          uint8_t** hq, uint8_t** hs) {
+    if (!ws || T < 0 || E < 1 || top_k < 1 || d < 1 || F < 1 || (mode != 0 && mode != 1))
+        return NVFP4_ERR_INVALID_ARG;
+    MoeWs w = carve_moe(ws, T, E, top_k, d, F, mode, nullptr);
+    if (h_bf16) *h_bf16 = w.h;
+    if (xq) *xq = w.xq;
+    if (xs) *xs = w.xs;
+    if (hq) *hq = w.hq;
+    if (hs) *hs = w.hs;
     return NVFP4_OK;
 }
 

@@ -188,6 +188,34 @@ void launch_quantize_act(const uint16_t* x, int M, int K, const int32_t* row_to_
                             top_k, input_scale, offsets, E, codes, scales));
 }
 
+nvfp4_status check_weight_recipe(const uint16_t* w, int batch, int N, int K, const uint8_t* codes,
+                                 const uint8_t* scales, const float* weight_scale_2) {
+    if (batch < 0 || N < 0 || K < 0) return NVFP4_ERR_INVALID_ARG;
+    if (K % 16 != 0 || batch > kMaxRecipeBatch) return NVFP4_ERR_SHAPE;
+    if ((size_t)batch * N * K == 0) return NVFP4_OK;
+    if (!w || !codes || !scales || !weight_scale_2) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned16(w) || !aligned16(codes) || !aligned16(scales) || !aligned16(weight_scale_2))
+        return NVFP4_ERR_ALIGN;
+    return NVFP4_OK;
+}
+
+nvfp4_status launch_weight_recipe(const uint16_t* w, int batch, int N, int K, float* amax, uint8_t* codes,
+                                  uint8_t* scales, float* weight_scale_2, cudaStream_t stream) {
+    // the running maxima start from zero on every call
+    launch_zero(amax, sizeof(float) * batch, stream);
+    const size_t n_per = (size_t)N * K;
+    const int gx = (int)std::max<size_t>(
+        1, std::min<size_t>((n_per / 8 + 255) / 256, (size_t)num_sms() * 8 / std::max(1, batch) + 1));
+    NVFP4_LAUNCH("tensor_amax", stream,
+                 tensor_amax_kernel<<<dim3(gx, batch), 256, 0, stream>>>(w, n_per, amax));
+    const size_t total = n_per / 8 * batch;
+    const int grid = (int)std::min<size_t>((total + 255) / 256, (size_t)num_sms() * 16);
+    NVFP4_LAUNCH("quantize_weights", stream,
+                 quantize_weights_kernel<<<grid, 256, 0, stream>>>(w, n_per, batch, amax, codes, scales,
+                                                                   weight_scale_2));
+    return last_launch_status();
+}
+
 }  // namespace nvfp4
 
 using namespace nvfp4;
@@ -201,26 +229,12 @@ extern "C" size_t nvfp4_quantize_weights_workspace_size(int batch, int N, int K)
 extern "C" nvfp4_status nvfp4_quantize_weights(const uint16_t* w, int batch, int N, int K, uint8_t* codes,
                                                uint8_t* scales, float* weight_scale_2, void* ws,
                                                size_t ws_bytes, cudaStream_t stream) {
-    if (batch < 0 || N < 0 || K < 0) return NVFP4_ERR_INVALID_ARG;
-    if (K % 16 != 0) return NVFP4_ERR_SHAPE;
-    if ((size_t)batch * N * K == 0) return NVFP4_OK;
-    if (!w || !codes || !scales || !weight_scale_2 || !ws) return NVFP4_ERR_INVALID_ARG;
-    if (!aligned16(w) || !aligned16(codes) || !aligned16(scales) || !aligned16(weight_scale_2) ||
-        !aligned16(ws))
-        return NVFP4_ERR_ALIGN;
+    const nvfp4_status st = check_weight_recipe(w, batch, N, K, codes, scales, weight_scale_2);
+    if (st != NVFP4_OK || (size_t)batch * N * K == 0) return st;
+    if (!ws) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned16(ws)) return NVFP4_ERR_ALIGN;
     if (ws_bytes < nvfp4_quantize_weights_workspace_size(batch, N, K)) return NVFP4_ERR_WORKSPACE;
-    float* amax = static_cast<float*>(ws);
-    launch_zero(amax, sizeof(float) * batch, stream);
-    const size_t n_per = (size_t)N * K;
-    int gx = (int)std::max<size_t>(1, std::min<size_t>((n_per / 8 + 255) / 256, (size_t)num_sms() * 8 / std::max(1, batch) + 1));
-    NVFP4_LAUNCH("tensor_amax", stream,
-                 tensor_amax_kernel<<<dim3(gx, batch), 256, 0, stream>>>(w, n_per, amax));
-    size_t total = n_per / 8 * batch;
-    int grid = (int)std::min<size_t>((total + 255) / 256, (size_t)num_sms() * 16);
-    NVFP4_LAUNCH("quantize_weights", stream,
-                 quantize_weights_kernel<<<grid, 256, 0, stream>>>(w, n_per, batch, amax, codes, scales,
-                                                                   weight_scale_2));
-    return last_launch_status();
+    return launch_weight_recipe(w, batch, N, K, static_cast<float*>(ws), codes, scales, weight_scale_2, stream);
 }
 
 extern "C" nvfp4_status nvfp4_quantize_act(const uint16_t* x, int M, int K, const int32_t* row_to_slot,

@@ -13,12 +13,14 @@
 // held until the process exits) and allocates nothing at any call.
 //
 // The array's host-side name is not a device address: its device address is
-// looked up once per device with cudaGetSymbolAddress, on the first call
-// made while that device is current, and cached.  Every call on a device
-// shares the one array, so calls that may overlap on the GPU (two streams,
-// two host threads) race and must be ordered by the caller.
-#include <mutex>
-
+// looked up with cudaGetSymbolAddress on every call, with the caller's
+// device current (a host-side query that allocates nothing), so a call made
+// after cudaDeviceReset or under another context of the device still gets
+// the array of the context it runs in.  The first call of a process on a
+// device may load the library's device code (lazy module loading), so make
+// it before any stream capture.  Every call on a device shares the one
+// array, so calls that may overlap on the GPU (two streams, two host
+// threads) race and must be ordered by the caller.
 #include "common.cuh"
 #include "internal.cuh"
 
@@ -27,24 +29,14 @@ namespace nvfp4 {
 namespace {
 
 constexpr int kNoAllocMaxTensors = 4096;
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) float g_noalloc_amax[kNoAllocMaxTensors];
 
-std::mutex g_noalloc_mu;
-float* g_noalloc_ptr[kMaxDevices] = {};
-
-// Device address of g_noalloc_amax on the current device (nullptr on error).
+// Device address of g_noalloc_amax in the current context (nullptr on error).
 float* noalloc_scratch() {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    std::lock_guard<std::mutex> lk(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_amax) != cudaSuccess) return nullptr;
-        g_noalloc_ptr[dev] = static_cast<float*>(p);
-    }
-    return g_noalloc_ptr[dev];
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_amax) != cudaSuccess) return nullptr;
+    return static_cast<float*>(p);
 }
 
 }  // namespace
@@ -58,27 +50,10 @@ extern "C" int nvfp4_quantize_weights_noalloc_max_batch(void) { return kNoAllocM
 extern "C" nvfp4_status nvfp4_quantize_weights_noalloc(const uint16_t* w, int batch, int N, int K, uint8_t* codes,
                                                        uint8_t* scales, float* weight_scale_2,
                                                        cudaStream_t stream) {
-    if (batch < 0 || N < 0 || K < 0) return NVFP4_ERR_INVALID_ARG;
-    if (K % 16 != 0) return NVFP4_ERR_SHAPE;
     if (batch > kNoAllocMaxTensors) return NVFP4_ERR_SHAPE;  // beyond the built-in scratch
-    if ((size_t)batch * N * K == 0) return NVFP4_OK;
-    if (!w || !codes || !scales || !weight_scale_2) return NVFP4_ERR_INVALID_ARG;
-    if (!aligned16(w) || !aligned16(codes) || !aligned16(scales) || !aligned16(weight_scale_2))
-        return NVFP4_ERR_ALIGN;
+    const nvfp4_status st = check_weight_recipe(w, batch, N, K, codes, scales, weight_scale_2);
+    if (st != NVFP4_OK || (size_t)batch * N * K == 0) return st;
     float* amax = noalloc_scratch();
     if (!amax) return NVFP4_ERR_CUDA;
-    // the running maxima start from zero on every call (the array keeps the
-    // previous call's values)
-    launch_zero(amax, sizeof(float) * batch, stream);
-    const size_t n_per = (size_t)N * K;
-    const int gx = (int)std::max<size_t>(
-        1, std::min<size_t>((n_per / 8 + 255) / 256, (size_t)num_sms() * 8 / std::max(1, batch) + 1));
-    NVFP4_LAUNCH("tensor_amax", stream,
-                 tensor_amax_kernel<<<dim3(gx, batch), 256, 0, stream>>>(w, n_per, amax));
-    const size_t total = n_per / 8 * batch;
-    const int grid = (int)std::min<size_t>((total + 255) / 256, (size_t)num_sms() * 16);
-    NVFP4_LAUNCH("quantize_weights", stream,
-                 quantize_weights_kernel<<<grid, 256, 0, stream>>>(w, n_per, batch, amax, codes, scales,
-                                                                   weight_scale_2));
-    return last_launch_status();
+    return launch_weight_recipe(w, batch, N, K, amax, codes, scales, weight_scale_2, stream);
 }

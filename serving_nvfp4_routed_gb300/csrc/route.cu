@@ -8,7 +8,7 @@
 // weights renormalised over the k chosen) is the plain reading.
 //
 // Top-k: one warp per token, logits in registers, k rounds of a warp arg-max.
-// Weights: exp(l - l_max) / sum over the k, in fp32.
+// Weights: exp(l - l_max) / sum over the k, in fp64, rounded once to fp32.
 // Permutation (stable: expert, token, slot): a per-expert histogram, a
 // warp-scan exclusive prefix sum, and a scatter in which each row's position
 // is its expert's base + the count of equal experts before it -- within a warp
@@ -67,15 +67,21 @@ __device__ void warp_topk(const float* __restrict__ lg, int E, int k, int32_t* _
             my_id = bi;
         }
     }
-    // fp32: exp(l_j - l_max), summed over the k in slot order, divided
-    // (fp64 runs at a small fraction of the fp32 rate on this part)
+    // fp64: exp(l_j - l_max), summed over the k in slot order, divided, then
+    // rounded once to fp32 (only k exponentials per token).  Non-finite top
+    // logits: +inf entries share the weight equally; all -inf: 1/k each.
     const float m = __shfl_sync(0xffffffffu, my_v, 0);
-    const float ex = lane < k ? expf(my_v - m) : 0.0f;
-    float sum = 0.0f;
+    double ex = 0.0;
+    if (lane < k) {
+        if (m == INFINITY) ex = my_v == INFINITY ? 1.0 : 0.0;
+        else if (m == -INFINITY) ex = 1.0;
+        else ex = exp((double)my_v - (double)m);
+    }
+    double sum = 0.0;
     for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, ex, j);
     if (lane < k) {
         ids[lane] = my_id;
-        w[lane] = __fdiv_rn(ex, sum);
+        w[lane] = (float)(ex / sum);
     }
 }
 

@@ -89,6 +89,11 @@ def test_other_host_validation(L):
     assert L.nvfp4_quantize_weights(_fake(0x10004), 1, 4, 32, p, p, p, p, big, None) == 3
     assert L.nvfp4_quantize_weights(None, 1, 4, 32, p, p, p, p, big, None) == 1
     assert L.nvfp4_quantize_weights(p, 0, 4, 32, p, p, p, p, 0, None) == 0
+    assert L.nvfp4_quantize_weights(p, 65536, 4, 32, p, p, p, p, big, None) == 2  # one grid row per tensor
+    assert L.nvfp4_quantize_weights_noalloc(p, 4097, 4, 32, p, p, p, None) == 2  # beyond the fixed scratch
+    assert L.nvfp4_quantize_weights_noalloc(p, 1, 4, 24, p, p, p, None) == 2
+    assert L.nvfp4_set_kernel_choice(3) == 1 and L.nvfp4_set_kernel_choice(-1) == 1
+    assert L.nvfp4_set_kernel_choice(2) == 0 and L.nvfp4_set_kernel_choice(0) == 0
     assert L.nvfp4_quantize_act(p, 4, 40, None, 1, p, None, 0, p, p, None) == 2
     assert L.nvfp4_quantize_act(p, 4, 32, p, 0, p, None, 0, p, p, None) == 1
     assert L.moe_route_permute(p, 4, 8, 9, p, p, p, p, p, p, big, None) == 2

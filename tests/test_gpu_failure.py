@@ -9,7 +9,8 @@ import torch
 import serving_nvfp4_routed_gb300 as lib
 from serving_nvfp4_routed_gb300 import synth
 
-from gpu_util import assert_layer_close, bf16_to_f32, gpu_bank, oracle_bank
+from gpu_util import OracleBank, gpu_bank
+from layer_check import check_layer
 
 pytestmark = pytest.mark.gpu
 
@@ -24,7 +25,7 @@ def test_bounded_wait_reports_timeout_and_context_survives(orc):
     s = synth.TINY
     inp = synth.moe_inputs(s, 77, device="cuda")
     banks = {k: inp[k] for k in ("gate", "up", "down")}
-    out = lib.nvfp4_moe_w4a16(inp["x"], inp["logits"], s.k, gpu_bank(lib, banks))
-    r = orc.route(inp["logits"].cpu().numpy(), s.k)
-    ref = orc.moe_layer("w4a16", synth.bf16_bits(inp["x"]), r["ids"], r["w"], oracle_bank(orc, banks))
-    assert_layer_close(bf16_to_f32(out), ref, "after timeout")
+    ws = lib.moe_workspace(s.T, s.E, s.k, s.d, s.F, "w4a16", "cuda")
+    out = lib.nvfp4_moe_w4a16(inp["x"], inp["logits"], s.k, gpu_bank(lib, banks), ws=ws)
+    check_layer(orc, "w4a16", inp["x"], inp["logits"], s.k, OracleBank(orc, banks).get(), out, ws,
+                np.arange(s.T, dtype=np.int32), what="after timeout")

@@ -10,7 +10,8 @@ import torch
 import serving_nvfp4_routed_gb300 as lib
 from serving_nvfp4_routed_gb300 import synth
 
-from gpu_util import assert_layer_close, bf16_to_f32, gpu_bank, oracle_bank
+from gpu_util import OracleBank
+from layer_check import check_layer
 
 pytestmark = pytest.mark.gpu
 
@@ -30,13 +31,20 @@ def _capture(run, x_s, lg_s):
 
 
 @pytest.mark.parametrize("path,mode", [("tc", "w4a16"), ("tc", "w4a4"), ("gemv", "w4a16")])
-def test_layer_graph_replay(orc, path, mode, monkeypatch):
-    monkeypatch.setenv("NVFP4_PATH", path)
+def test_layer_graph_replay(orc, path, mode):
+    lib.set_kernel_choice(path)
+    try:
+        _graph_case(orc, path, mode)
+    finally:
+        lib.set_kernel_choice("auto")
+
+
+def _graph_case(orc, path, mode):
     T, E, k, d, F = 256, 16, 4, 512, 256
     s = synth.MoEShape(T, d, E, k, F)
     inp = synth.moe_inputs(s, 41, device="cuda", outlier_frac=0.05)
     banks = dict(gate=inp["gate"], up=inp["up"], down=inp["down"])
-    gw = gpu_bank(lib, banks)
+    gw = lib.MoEWeights(*(lib.nvfp4_quantize_weights(banks[n]) for n in ("gate", "up", "down")))
     is13 = torch.full((E,), 0.004, device="cuda")
     is2 = torch.full((E,), 0.001, device="cuda")
     out = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
@@ -59,7 +67,5 @@ def test_layer_graph_replay(orc, path, mode, monkeypatch):
         eager = run(x2, lg2).clone()
         assert torch.equal(got.view(torch.int16), eager.view(torch.int16))
     else:
-        r = orc.route(lg2.cpu().numpy(), k)
-        ob = oracle_bank(orc, banks, np.arange(E))
-        ref = orc.moe_layer("w4a16", synth.bf16_bits(x2), r["ids"], r["w"], ob)
-        assert_layer_close(bf16_to_f32(got), ref, "graph replay")
+        ob = OracleBank(orc, banks).get()
+        check_layer(orc, "w4a16", x2, lg2, k, ob, got, ws, np.arange(T, dtype=np.int32), what="graph replay")

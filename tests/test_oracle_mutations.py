@@ -22,12 +22,13 @@ MUTATIONS = {
     "e4m3 exponent bias 8": ("ldexp(1.0, e - 7)", "ldexp(1.0, e - 8)"),
     "global scale amax/2687": ("amax / 2688.0f", "amax / 2687.0f"),
     "odd index in the low nibble": ("(uint8_t)(q0 | (q1 << 4))", "(uint8_t)(q1 | (q0 << 4))"),
-    "gate and up transposed": ("nvfp4_matvec(xa, gq + (int64_t)e * F * (d / 2), gs + (int64_t)e * F * (d / 16), F, d, sg);",
-                               "nvfp4_matvec(xa, uq + (int64_t)e * F * (d / 2), us + (int64_t)e * F * (d / 16), F, d, sg);"),
+    "gate and up transposed": ("dequant_f32(gq + (int64_t)e * F * (d / 2), gs + (int64_t)e * F * (d / 16), F, d, Wg);",
+                               "dequant_f32(uq + (int64_t)e * F * (d / 2), us + (int64_t)e * F * (d / 16), F, d, Wg);"),
     "down weight_scale_2 dropped": ("y[n] * hscale * (double)d_ws2[e]", "y[n] * hscale"),
     "silu sign": ("return g / (1.0 + exp(-g));", "return g / (1.0 + exp(g));"),
-    "top-k ties to the higher id": ("if (best < 0 || l[e] > l[best]) best = e;", "if (best < 0 || l[e] >= l[best]) best = e;"),
-    "renormalised over all experts": ("den += exp((double)l[ids[t * k + j]] - lmax);", "den += exp((double)l[ids[t * k + j]] - lmax) * 1.5;"),
+    "top-k ties to the higher id": ("if (best < 0 || rank_key(l[e]) > rank_key(l[best])) best = e;",
+                                    "if (best < 0 || rank_key(l[e]) >= rank_key(l[best])) best = e;"),
+    "renormalised over all experts": ("den += num[j];", "den += num[j] * 1.5;"),
     "block scale without the /6": ("float sf = (bam / 6.0f) / gs;", "float sf = bam / gs;"),
     "permutation not stable": ("int64_t row = fill[ids[i]]++;", "int64_t row = offsets[ids[i] + 1] - 1 - (fill[ids[i]]++ - offsets[ids[i]]);"),
 }

@@ -70,3 +70,27 @@ def test_route_zipf_skew(orc):
     counts = np.sort(np.diff(r["offsets"]))[::-1]
     top3 = counts[:3].sum() / counts.sum()
     assert 0.2 < top3 < 0.35
+
+
+def test_route_non_finite_logits(orc):
+    """The reading for logits the pages never meet: NaN ranks as -inf; a
+    +inf top logit gives its +inf entries equal weights and the rest 0; a
+    token whose chosen logits are all -inf gets 1/k each.  Weights still sum
+    to 1 and no index leaves its range."""
+    lg = np.zeros((5, 12), np.float32)
+    lg[0] = -np.inf
+    lg[1, 4] = np.inf
+    lg[2, [2, 7, 11]] = np.inf
+    lg[3, :6] = np.nan
+    lg[3, 6:] = np.arange(6)
+    lg[4] = np.nan
+    r = orc.route(lg, 4)
+    assert np.all((r["ids"] >= 0) & (r["ids"] < 12))
+    np.testing.assert_array_equal(r["w"][0], np.full(4, 0.25, np.float32))
+    assert list(r["ids"][0]) == [0, 1, 2, 3]
+    assert list(r["ids"][1][:1]) == [4] and list(r["w"][1]) == [1, 0, 0, 0]
+    assert list(r["ids"][2][:3]) == [2, 7, 11]
+    np.testing.assert_array_equal(r["w"][2], np.array([1 / 3, 1 / 3, 1 / 3, 0], np.float32))
+    assert list(r["ids"][3]) == [11, 10, 9, 8]  # the NaN entries rank last
+    np.testing.assert_array_equal(r["w"][4], np.full(4, 0.25, np.float32))
+    assert np.all(np.abs(r["w"].astype(np.float64).sum(1) - 1) <= 4 * 2.0 ** -24)
