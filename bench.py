@@ -618,7 +618,11 @@ def kernel_roofline(layer, dom, dom_ms, touched, hbm, bf16, peak_kind, workload)
                 "algorithmic_flops_per_launch": dom_flops,
                 "hbm": {"achieved": bytes_gbs, "peak": hbm, "unit": "GB/s", "frac": bytes_gbs / hbm,
                         "algorithmic_bytes_per_launch": dom_bytes}}
-    if dom.startswith("gemv_down"):
+    if "gateup_down" in dom:
+        # the whole decode-shaped layer in one launch: every touched expert's
+        # three projections, x in, out and the routing arrays
+        dom_bytes = layer.algorithmic_bytes(touched)[0]
+    elif dom.startswith("gemv_down"):
         dom_bytes = touched * s_.d * s_.F * 9 // 16 + (R * s_.F * 2 if layer.mode == "w4a16" else R * s_.F * 9 // 16)
     else:
         dom_bytes = layer.gateup_bytes(touched)

@@ -39,8 +39,11 @@
  * Rounding points (the same places the kernels round):
  *   G = bf16(ws2_g * sum x*w_g)   U = bf16(ws2_u * sum x*w_u)       (R1)
  *   h = bf16(silu(G) * U)                                            (R2)
- *   Y = ws2_d * sum h*w_d   (unrounded)
+ *   Y = ws2_d * sum h*w_d   (unrounded; with the R3 switch, bf16(Y) (R3))
  *   out[t] = bf16(sum_j w_j * Y_j)                                   (R4)
+ * R3 is the rounding point of the kernels that keep each routed row's Y in
+ * bf16 for the slot-ordered combine (the prompt-shaped path); without it Y
+ * stays unrounded, as in the decode-shaped path.
  * All sums here are fp64.  Scale arithmetic that decides a code (block
  * scale, element / scale) is done in fp32 in the order the recipe states,
  * because that is the precision in which the codes are defined.
@@ -375,7 +378,9 @@ static void quant_dequant(const float* v, int64_t K, float gs, double* out, uint
  *   g_abs, u_abs [n, k, F]  their sums of |terms| times the same scales
  *   h  [n, k, F]      h (bf16 values)
  *   xq, xs [n, k, d/2], [n, k, d/16]  W4A4: the pair's NVFP4 x row
- *   hq, hs [n, k, F/2], [n, k, F/16]  W4A4: the pair's NVFP4 h row */
+ *   hq, hs [n, k, F/2], [n, k, F/16]  W4A4: the pair's NVFP4 h row
+ *   y_pre, y_abs [n, k, d]  each pair's Y before the R3 rounding and its
+ *                     scale * sum_f |h_f * W_d| */
 typedef struct {
     double* out_pre;
     double* out_abs;
@@ -388,6 +393,8 @@ typedef struct {
     uint8_t* xs;
     uint8_t* hq;
     uint8_t* hs;
+    double* y_pre;
+    double* y_abs;
 } orc_layer_extras;
 
 /*
@@ -397,7 +404,8 @@ typedef struct {
  * input_scale: is13[e] before gate/up, is2[e] before down).
  * Weight banks are stacked over experts: gate/up codes [E, F, d/2], scales
  * [E, F, d/16], ws2 [E]; down codes [E, d, F/2], scales [E, d, F/16].
- * out[i, :] receives bf16(sum_j w_j * Y_j) for token tokens[i] (as float).
+ * out[i, :] receives bf16(sum_j w_j * Y_j) for token tokens[i] (as float);
+ * round_y != 0 rounds each Y_j to bf16 first (R3).
  * The (token, slot) pairs are grouped by expert so that each touched
  * expert's three projections are dequantised once; every pair is then
  * evaluated on its own, with the same fp64 sums in the same order.
@@ -407,7 +415,7 @@ void orc_moe_layer_ex(int mode, const uint16_t* x, int64_t T, int64_t d, int64_t
                       const uint8_t* gq, const uint8_t* gs, const float* g_ws2,
                       const uint8_t* uq, const uint8_t* us, const float* u_ws2,
                       const uint8_t* dq, const uint8_t* ds, const float* d_ws2,
-                      const float* is13, const float* is2,
+                      const float* is13, const float* is2, int round_y,
                       const int32_t* tokens, int64_t n_tokens, float* out, const orc_layer_extras* ex) {
     (void)T;
     const int64_t n_pairs = n_tokens * k;
@@ -487,8 +495,11 @@ void orc_moe_layer_ex(int mode, const uint16_t* x, int64_t T, int64_t d, int64_t
                 }
                 matvec(ha, Wd, d, F, y, ya);
                 for (int64_t n = 0; n < d; ++n) {
-                    Y[pair * d + n] = y[n] * hscale * (double)d_ws2[e];
+                    const double yv = y[n] * hscale * (double)d_ws2[e];
+                    Y[pair * d + n] = round_y ? orc_round_bf16(yv) : yv;
                     Ya[pair * d + n] = ya[n] * hscale * (double)d_ws2[e];
+                    if (ex && ex->y_pre) ex->y_pre[pair * d + n] = yv;
+                    if (ex && ex->y_abs) ex->y_abs[pair * d + n] = Ya[pair * d + n];
                 }
             }
         }
@@ -526,7 +537,7 @@ void orc_moe_layer(int mode, const uint16_t* x, int64_t T, int64_t d, int64_t F,
     orc_layer_extras ex;
     memset(&ex, 0, sizeof ex);
     ex.h = h_out;
-    orc_moe_layer_ex(mode, x, T, d, F, E, k, ids, w, gq, gs, g_ws2, uq, us, u_ws2, dq, ds, d_ws2, is13, is2,
+    orc_moe_layer_ex(mode, x, T, d, F, E, k, ids, w, gq, gs, g_ws2, uq, us, u_ws2, dq, ds, d_ws2, is13, is2, 0,
                      tokens, n_tokens, out, &ex);
 }
 

@@ -46,7 +46,7 @@ def _P(t):
 class _LayerExtras(ctypes.Structure):
     """Mirror of orc_layer_extras (optional outputs of orc_moe_layer_ex)."""
     _fields_ = [(n, ctypes.c_void_p) for n in ("out_pre", "out_abs", "g_pre", "u_pre", "g_abs", "u_abs", "h",
-                                                 "xq", "xs", "hq", "hs")]
+                                                 "xq", "xs", "hq", "hs", "y_pre", "y_abs")]
 
 
 def bind(L):
@@ -75,7 +75,7 @@ def bind(L):
                                 vp, vp, vp, i64, vp, vp]
     L.orc_moe_layer_ex.argtypes = [i32, vp, i64, i64, i64, i32, i32, vp, vp,
                                    vp, vp, vp, vp, vp, vp, vp, vp, vp,
-                                   vp, vp, vp, i64, vp, ctypes.POINTER(_LayerExtras)]
+                                   vp, vp, i32, vp, i64, vp, ctypes.POINTER(_LayerExtras)]
     L.orc_linear.argtypes = [vp, i64, i64, vp, vp, f32, i64, vp, vp, f32, vp]
     L.orc_linear_ex.argtypes = [vp, i64, i64, vp, vp, f32, i64, vp, vp, f32, vp, vp, vp, vp, vp, vp]
     L.orc_num_threads.restype = i32
@@ -239,12 +239,14 @@ def moe_layer(mode: str, x_bf16_bits, ids, w, bank, tokens=None, is13=None, is2=
     return (out, h) if want_h else out
 
 
-def moe_layer_ex(mode: str, x_bf16_bits, ids, w, bank, tokens=None, is13=None, is2=None):
+def moe_layer_ex(mode: str, x_bf16_bits, ids, w, bank, tokens=None, is13=None, is2=None, round_y=False):
     """The layer for ``tokens`` with every optional output (see
     ``orc_moe_layer_ex``): dict with out [n, d] (bf16 values), out_pre and
     out_abs [n, d] fp64, g_pre / u_pre / g_abs / u_abs [n, k, F] fp64,
-    h [n, k, F], and for W4A4 the pairs' NVFP4 rows xq [n, k, d/2],
-    xs [n, k, d/16], hq [n, k, F/2], hs [n, k, F/16]."""
+    h [n, k, F], y_pre / y_abs [n, k, d] fp64, and for W4A4 the pairs'
+    NVFP4 rows xq [n, k, d/2], xs [n, k, d/16], hq [n, k, F/2],
+    hs [n, k, F/16].  round_y: each Y rounded to bf16 before the weighted
+    sum (the R3 rounding point of the prompt-shaped path)."""
     x = _c(x_bf16_bits, np.uint16)
     T, d = x.shape
     ids = _c(ids, np.int32)
@@ -266,7 +268,8 @@ def moe_layer_ex(mode: str, x_bf16_bits, ids, w, bank, tokens=None, is13=None, i
         is2 = _c(is2, np.float32)
     r = dict(out=np.zeros((n, d), np.float32), out_pre=np.zeros((n, d)), out_abs=np.zeros((n, d)),
              g_pre=np.zeros((n, k, F)), u_pre=np.zeros((n, k, F)), g_abs=np.zeros((n, k, F)),
-             u_abs=np.zeros((n, k, F)), h=np.zeros((n, k, F), np.float32))
+             u_abs=np.zeros((n, k, F)), h=np.zeros((n, k, F), np.float32), y_pre=np.zeros((n, k, d)),
+             y_abs=np.zeros((n, k, d)))
     if m == 1:
         r.update(xq=np.zeros((n, k, d // 2), np.uint8), xs=np.zeros((n, k, d // 16), np.uint8),
                  hq=np.zeros((n, k, F // 2), np.uint8), hs=np.zeros((n, k, F // 16), np.uint8))
@@ -275,7 +278,7 @@ def moe_layer_ex(mode: str, x_bf16_bits, ids, w, bank, tokens=None, is13=None, i
                            _ptr(arrs[0]), _ptr(arrs[1]), _ptr(ws2s[0]),
                            _ptr(arrs[2]), _ptr(arrs[3]), _ptr(ws2s[1]),
                            _ptr(arrs[4]), _ptr(arrs[5]), _ptr(ws2s[2]),
-                           _ptr(is13) if m == 1 else None, _ptr(is2) if m == 1 else None,
+                           _ptr(is13) if m == 1 else None, _ptr(is2) if m == 1 else None, 1 if round_y else 0,
                            _ptr(tokens), n, _ptr(r["out"]), ctypes.byref(ex))
     return r
 

@@ -96,6 +96,44 @@ size_t gemv_smem_bytes(int K);
 bool gemv_supported_k(int K);
 void launch_gemv(int bmode, int outmode, const GemvArgs& a, int max_work, cudaStream_t s);
 
+// ---- decode-shaped layer in one persistent launch (moe_decode.cu) ----
+struct DecodeArgs {
+    // stored weights as TMA tiles: codes / scales of gate and up [E*F rows],
+    // boxes of 64 rows x a K chunk; down [E*d rows], boxes of 128 rows
+    CUtensorMap tm_gate_c, tm_up_c, tm_gate_s, tm_up_s, tm_down_c, tm_down_s;
+    int d, F, top_k;
+    int gbu, gbd;                   // 64-feature blocks per gate/up item, 128-output blocks per down item
+    int kcu, kcd;                   // K chunk of a gate/up / down stage (set with the maps)
+    int slot_bytes;                 // set by the launcher
+    const int32_t* offsets;         // [E+1]
+    const int32_t* active;          // [E]
+    const int32_t* n_active;        // [1]
+    const int32_t* tile_start;      // [E+1] prefix of ceil(rows / kGemvTokTile)
+    const int32_t* row_to_slot;     // [R]
+    const int32_t* slot_to_row;     // [R]
+    const float* topk_w;            // [R]
+    const float *gate_ws2, *up_ws2, *down_ws2;  // [E]
+    const uint16_t* x;              // B_BF16: x [T, d] bf16
+    const uint8_t *xq, *xs;         // B_NVFP4: permuted NVFP4 rows [R, d/2], [R, d/16]
+    const float *is13, *is2;        // B_NVFP4: static input scales [E]
+    uint16_t* h;                    // B_BF16: h [R, F] bf16
+    uint8_t *hq, *hs;               // B_NVFP4: h requantised [R, F/2], [R, F/16]
+    float* yrows;                   // [R, d] w * y per routed row
+    uint16_t* out;                  // [T, d] bf16
+    int* counters;                  // [1] work item counter (zeroed before the launch)
+    int* tile_ready;                // [row tiles] gate/up items done (zeroed)
+    int* tok_done;                  // [T, d / 128] contributions per (token, output group) (zeroed)
+    int32_t* status;                // NVFP4_ERR_TIMEOUT if a bounded wait expired
+};
+// d and F multiples of 256 and the shared-memory ring fits.
+bool decode_supported(int d, int F);
+// Output groups of the finest split (sizes the tok_done counters).
+int decode_groups_d(int d);
+// Picks the K chunks and encodes the weight tensor maps.
+bool decode_set_maps(DecodeArgs* a, const nvfp4_moe_weights* w);
+void decode_pick_groups(int expected_tiles, int d, int F, int* gbu, int* gbd);
+void launch_decode(int bmode, const DecodeArgs& a, cudaStream_t s);
+
 // ---- prompt-shaped grouped GEMM (tcgen05, accumulators in TMEM) ----
 enum TcOut { TC_OUT_H = 0, TC_OUT_COMBINE = 1, TC_OUT_BF16 = 2 };
 
@@ -119,17 +157,19 @@ struct TcArgs {
     int32_t* status;             // optional: NVFP4_ERR_TIMEOUT if a bounded wait expired
 };
 
-// ---- prompt-shaped grouped GEMMs with the routed rows as M (tcgen05, N = 256) ----
+// ---- prompt-shaped grouped GEMMs with the routed rows as M (tcgen05) ----
 // SWIGLU: h = bf16(silu(bf16 G) * bf16 U); SWIGLU_Q: h requantised to NVFP4
-// (codes + e4m3 block scales under hq_gs); COMBINE: weighted red.add into
-// the fp32 accumulator; BF16: plain bf16 rows; ROWS: fp32 rows w * y by
-// routed row, summed per token afterwards (launch_sum_rows).
-enum TcmEpi { TCM_SWIGLU = 0, TCM_COMBINE = 1, TCM_BF16 = 2, TCM_SWIGLU_Q = 3, TCM_ROWS = 4 };
+// (codes + e4m3 block scales under hq_gs); BF16: plain bf16 rows; ROWS: bf16
+// rows y by routed row, summed per token with the routing weights afterwards
+// (launch_sum_rows).
+// The f16 kernel (tcm) takes SWIGLU, ROWS and BF16; the block-scaled FP4
+// kernel (tcq) SWIGLU_Q and ROWS.
+enum TcmEpi { TCM_SWIGLU = 0, TCM_BF16 = 2, TCM_SWIGLU_Q = 3, TCM_ROWS = 4 };
 
 struct TcmArgs {
-    CUtensorMap tmap_x;          // f16 rows [R, K] (expert order), box 64 x 128, 128-byte swizzle
-    CUtensorMap tmap_ac;         // NVFP4 rows instead (a_nvfp4): codes [R, K/2], box 32 x 128
-    CUtensorMap tmap_as;         //   and e4m3 scales [R, K/16], box 16 x 128
+    CUtensorMap tmap_x;          // tcm: f16 rows [R, K] (expert order), box 64 x 128, 128-byte swizzle
+    CUtensorMap tmap_ac;         // tcq: NVFP4 rows, codes [R, K/2]
+    CUtensorMap tmap_as;         //   and e4m3 scales [R, K/16]
     CUtensorMap tmap_wc[2];      // weight codes [E*N, K/2] uint8, box 32 x 128
     CUtensorMap tmap_ws[2];      // weight scales [E*N, K/16] uint8, box 16 x 128
     int K, N, top_k;             // N: features of one projection (gate/up: F, down: d)
@@ -143,11 +183,10 @@ struct TcmArgs {
     const int32_t* x_exp;        // [R] value of an f16 row = f16 * 2^x_exp[row]
     const float* x_gs;           // NVFP4 rows: [E] global scale of the rows of expert e
     uint16_t* h_out;             // TCM_SWIGLU: [R, N] bf16
-    float* acc_out;              // TCM_COMBINE: [T, N] fp32, zeroed before
-    const int32_t* row_to_slot;  // TCM_COMBINE: [R]
-    const float* topk_w;         // TCM_COMBINE: [T*k]
+    const int32_t* row_to_slot;  // TCM_ROWS: [R]
+    const float* topk_w;         // TCM_ROWS: [T*k]
     uint16_t* y_out;             // TCM_BF16: [R, N]
-    float* y_rows;               // TCM_ROWS: [R, N] fp32 w * y by routed row
+    uint16_t* y_rows;            // TCM_ROWS: [R, N] bf16 y by routed row (the weights are applied by sum_rows)
     uint8_t* hq_out;             // TCM_SWIGLU_Q: [R, N/2] codes
     uint8_t* hs_out;             //   [R, N/16] e4m3 block scales
     const float* hq_gs;          //   [E] global scale they are taken under
@@ -160,10 +199,8 @@ bool encode_tmap_u8(CUtensorMap* map, const void* base, unsigned long long inner
 bool tcm_supported(int epi, int N, int K);
 // Fills tmap_wc / tmap_ws from a_codes / a_scales (rows = E * N, K = a->K).
 bool tcm_set_weights(TcmArgs* a, long long rows);
-// Fills tmap_ac / tmap_as: NVFP4 activation rows [rows, a->K].
-bool tcm_set_act(TcmArgs* a, const uint8_t* codes, const uint8_t* scales, long long rows);
-// a_nvfp4: A rows are NVFP4 (tmap_ac / tmap_as, x_gs), else f16 (tmap_x, x_exp).
-void launch_tcm(int epi, int a_nvfp4, const TcmArgs& a, int max_units, cudaStream_t s);
+// A rows are f16 (tmap_x, x_exp).
+void launch_tcm(int epi, const TcmArgs& a, int max_units, cudaStream_t s);
 
 // ---- W4A4 prompt-shaped grouped GEMM on the block-scaled FP4 tensor cores ----
 // Same arguments as TcmArgs (NVFP4 rows: a_codes / x_gs); epi TCM_SWIGLU_Q
@@ -174,9 +211,10 @@ bool tcq_set_maps(TcmArgs* a, const uint8_t* x_codes, const uint8_t* x_scales, l
 // max_tiles bounds the 128-row tiles over all experts; the unit count
 // follows from the kernel's column slice.
 void launch_tcq(int epi, const TcmArgs& a, int max_tiles, cudaStream_t s);
-// out[t] = bf16(sum over slots j in order of y[slot_to_row[t * k + j]]), rows of d floats.
-void launch_sum_rows(const float* y, const int32_t* slot_to_row, int T, int k, int d, uint16_t* out,
-                     cudaStream_t s);
+// out[t] = bf16(sum over slots j in order of w[t*k + j] * y[slot_to_row[t*k + j]]),
+// y rows of d bf16 values, the sum in fp32.
+void launch_sum_rows(const uint16_t* y, const int32_t* slot_to_row, const float* topk_w, int T, int k, int d,
+                     uint16_t* out, cudaStream_t s);
 
 size_t tc_smem_bytes(int nproj);
 void launch_tc_gemm(int outmode, int nproj, const TcArgs& a, int max_units, cudaStream_t s);

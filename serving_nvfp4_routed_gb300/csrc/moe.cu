@@ -12,8 +12,9 @@
 //   down + weighted top-k combine:
 //     decode-shaped kernels: fp32 red.add into a [T, d] accumulator, and the
 //       CTA that adds a token's last contribution writes its bf16 row;
-//     prompt-shaped kernels: w * y written per routed row, then each token's
-//       k rows summed in slot order (deterministic, chunk-invariant).
+//     prompt-shaped kernels: y written per routed row in bf16, then each
+//       token's k rows weighted and summed in slot order (deterministic,
+//       chunk-invariant).
 #include <climits>
 #include <cstring>
 
@@ -34,8 +35,11 @@ struct MoeWs {
     uint8_t* hq;      // [R, F/2]   W4A4
     uint8_t* hs;      // [R, F/16]  W4A4
     float* acc;       // [T, d]
-    float* yrows;     // [R, d] W4A4 prompt path: w * y rows by routed row
-    int* clear;       // [kCounters + T]: work counters, then per-token completion counts
+    float* yrows;     // [R, d]: w * y fp32 rows (decode kernel) or bf16 y rows (prompt paths)
+    int* clear;       // zeroed by the route launch: work counters, per-token completion counts,
+                      // then (decode kernel) per-tile and per-(token, output group) counters
+    int* tile_ready;  // [max tiles]
+    int* tok_done;    // [T, d / 128]
     // prompt-shaped (tensor-core) path, W4A16
     uint16_t* xp;     // [R, d]  f16 x * 2^-s, rows in expert order
     int32_t* xp_exp;  // [R]
@@ -60,9 +64,9 @@ bool use_tc(int mode, int T, int E, int k, int d, int F) {
     return R >= 32LL * std::min<long long>(E, R);
 }
 
-// W4A4 on the tensor cores: NVFP4 activation rows fed to the same kernel.
+// W4A4 on the block-scaled FP4 tensor cores (K a multiple of 256 on both projections).
 bool use_tc_w4a4(int T, int E, int k, int d, int F) {
-    if (!tcm_supported(TCM_SWIGLU_Q, F, d) || !tcm_supported(TCM_COMBINE, d, F)) return false;
+    if (!tcq_supported(TCM_SWIGLU_Q, F, d) || !tcq_supported(TCM_ROWS, d, F)) return false;
     const int f = forced_path();
     if (f >= 0) return f == 1;
     const long long R = (long long)T * k;
@@ -83,10 +87,15 @@ MoeWs carve_moe(void* base, int T, int E, int k, int d, int F, int mode, size_t*
     w.ra.tile_start = c.take<int32_t>(E + 1);
     w.ra.tile_start_tc = c.take<int32_t>(E + 1);
     w.ra.counts = c.take<int32_t>(route_scratch_words(T, E, k) + 1);
-    w.clear = c.take<int>(kCounters + (size_t)T);
+    const size_t max_tiles = R / kGemvTokTile + std::min<size_t>(E, R) + 1;
+    const size_t n_clear = kCounters + (size_t)T + max_tiles + (size_t)T * decode_groups_d(d);
+    w.clear = c.take<int>(n_clear);
     w.ra.clear = w.clear;
-    w.ra.n_clear = kCounters + T;
+    w.ra.n_clear = (int)n_clear;
+    w.tile_ready = w.clear + kCounters + T;
+    w.tok_done = w.tile_ready + max_tiles;
     w.acc = c.take<float>((size_t)T * d);
+    w.yrows = c.take<float>(R * d);
     if (mode == 0) {
         w.h = c.take<uint16_t>(R * F);
         if (tc_possible(mode, d, F)) {
@@ -94,14 +103,12 @@ MoeWs carve_moe(void* base, int T, int E, int k, int d, int F, int mode, size_t*
             w.xp_exp = c.take<int32_t>(R + 1);
             w.hh = c.take<uint16_t>(R * F);
             w.h_exp = c.take<int32_t>(R + 1);
-            if (tcm_supported(TCM_ROWS, d, F)) w.yrows = c.take<float>(R * d);
         }
     } else {
         w.xq = c.take<uint8_t>(R * (d / 2));
         w.xs = c.take<uint8_t>(R * (d / 16));
         w.hq = c.take<uint8_t>(R * (F / 2));
         w.hs = c.take<uint8_t>(R * (F / 16));
-        if (tcq_supported(TCM_SWIGLU_Q, F, d) && tcq_supported(TCM_ROWS, d, F)) w.yrows = c.take<float>(R * d);
     }
     if (bytes) *bytes = align_up(c.off, 256);
     return w;
@@ -168,9 +175,6 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
 
     if (mode == 1 && use_tc_w4a4(T, E, top_k, d, F)) {
         const int max_tiles = R / kTcTokTile + std::min(E, R) + 1;
-        // block-scaled FP4 MMA when the shapes allow it, else f16 MMA of dequantised tiles
-        const bool fp4 = ws.yrows != nullptr;
-        if (!fp4) launch_zero(ws.acc, sizeof(float) * (size_t)T * d, s);
         // gate/up + SwiGLU, h requantised under the down projection's input scale
         TcmArgs g{};
         g.K = d;
@@ -187,14 +191,9 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
         g.hs_out = ws.hs;
         g.hq_gs = is2;
         g.status = d_status;
-        if (fp4) {
-            if (!tcq_set_maps(&g, ws.xq, ws.xs, R, (long long)E * F)) return NVFP4_ERR_CUDA;
-            launch_tcq(TCM_SWIGLU_Q, g, max_tiles, s);
-        } else {
-            if (!tcm_set_weights(&g, (long long)E * F) || !tcm_set_act(&g, ws.xq, ws.xs, R)) return NVFP4_ERR_CUDA;
-            launch_tcm(TCM_SWIGLU_Q, 1, g, max_tiles * (F / 128), s);
-        }
-        // down + weighted combine
+        if (!tcq_set_maps(&g, ws.xq, ws.xs, R, (long long)E * F)) return NVFP4_ERR_CUDA;
+        launch_tcq(TCM_SWIGLU_Q, g, max_tiles, s);
+        // down: w * y rows by routed row, then each token's slots summed in slot order
         TcmArgs u = g;
         u.K = F;
         u.N = d;
@@ -203,29 +202,21 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
         u.x_gs = is2;
         u.hq_out = nullptr;
         u.hs_out = nullptr;
-        u.acc_out = ws.acc;
         u.row_to_slot = ws.ra.row_to_slot;
         u.topk_w = ws.ra.w;
-        if (fp4) {
-            // w * y rows by routed row, then each token's slots summed in slot order
-            u.y_rows = ws.yrows;
-            u.acc_out = nullptr;
-            if (!tcq_set_maps(&u, ws.hq, ws.hs, R, (long long)E * d)) return NVFP4_ERR_CUDA;
-            launch_tcq(TCM_ROWS, u, max_tiles, s);
-            launch_sum_rows(ws.yrows, ws.ra.slot_to_row, T, top_k, d, out, s);
-        } else {
-            if (!tcm_set_weights(&u, (long long)E * d) || !tcm_set_act(&u, ws.hq, ws.hs, R)) return NVFP4_ERR_CUDA;
-            launch_tcm(TCM_COMBINE, 1, u, max_tiles * (d / 256), s);
-            launch_acc_to_bf16(ws.acc, (size_t)T * d, out, s);
-        }
+        u.y_rows = reinterpret_cast<uint16_t*>(ws.yrows);
+        if (!tcq_set_maps(&u, ws.hq, ws.hs, R, (long long)E * d)) return NVFP4_ERR_CUDA;
+        launch_tcq(TCM_ROWS, u, max_tiles, s);
+        launch_sum_rows(u.y_rows, ws.ra.slot_to_row, ws.ra.w, T, top_k, d, out, s);
         return last_launch_status();
     }
 
     if (use_tc(mode, T, E, top_k, d, F)) {
         // the down projection writes w * y rows (summed per token in slot order
-        // afterwards) when the prompt-shaped kernel takes it, else it adds into
-        // a zeroed fp32 accumulator
-        const bool rows = ws.yrows != nullptr && tcm_supported(TCM_ROWS, d, F);
+        // afterwards) when the prompt-shaped kernel takes its shape (K = F a
+        // multiple of 256), else the weights-as-M kernel adds into a zeroed
+        // fp32 accumulator
+        const bool rows = tcm_supported(TCM_ROWS, d, F);
         // x -> f16 rows in expert order (and zero the combine accumulator)
         launch_rows_to_f16(x, R, d, ws.xp, ws.xp_exp, rows ? nullptr : ws.acc, d, s, ws.ra.row_to_slot, top_k, T);
         const int max_tiles = R / kTcTokTile + std::min(E, R) + 1;
@@ -246,7 +237,7 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
         if (tcm_supported(TCM_SWIGLU, F, d)) {
             if (!make_tmap_rows_f16(&g.tmap_x, ws.xp, R, d) || !tcm_set_weights(&g, (long long)E * F))
                 return NVFP4_ERR_CUDA;
-            launch_tcm(TCM_SWIGLU, 0, g, max_tiles * (F / 128), s);
+            launch_tcm(TCM_SWIGLU, g, max_tiles * (F / 128), s);
         } else {
             TcArgs t{};
             t.top_k = top_k;
@@ -270,7 +261,7 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
         // h -> f16 rows
         launch_rows_to_f16(ws.h, R, F, ws.hh, ws.h_exp, nullptr, 0, s);
         // down + weighted combine
-        if (tcm_supported(TCM_COMBINE, d, F)) {
+        if (rows) {
             TcmArgs u = g;
             u.K = F;
             u.N = d;
@@ -278,17 +269,12 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
             u.a_codes[1] = u.a_codes[0];   u.a_scales[1] = u.a_scales[0];   u.a_ws2[1] = u.a_ws2[0];
             u.x_exp = ws.h_exp;
             u.h_out = nullptr;
-            u.acc_out = rows ? nullptr : ws.acc;
-            u.y_rows = rows ? ws.yrows : nullptr;
-            u.row_to_slot = ws.ra.row_to_slot;
-            u.topk_w = ws.ra.w;
+            u.y_rows = reinterpret_cast<uint16_t*>(ws.yrows);
             if (!make_tmap_rows_f16(&u.tmap_x, ws.hh, R, F) || !tcm_set_weights(&u, (long long)E * d))
                 return NVFP4_ERR_CUDA;
-            launch_tcm(rows ? TCM_ROWS : TCM_COMBINE, 0, u, max_tiles * (d / 256), s);
-            if (rows) {
-                launch_sum_rows(ws.yrows, ws.ra.slot_to_row, T, top_k, d, out, s);
-                return last_launch_status();
-            }
+            launch_tcm(TCM_ROWS, u, max_tiles * (d / 256), s);
+            launch_sum_rows(u.y_rows, ws.ra.slot_to_row, ws.ra.w, T, top_k, d, out, s);
+            return last_launch_status();
         } else {
             TcArgs u{};
             u.top_k = top_k;
@@ -314,6 +300,41 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
     }
 
     const int tiles = expected_tiles(R, E);
+    if (decode_supported(d, F)) {
+        // one persistent launch: gate/up + SwiGLU, then down + the slot-ordered combine
+        DecodeArgs da{};
+        da.d = d;
+        da.F = F;
+        da.top_k = top_k;
+        decode_pick_groups(tiles, d, F, &da.gbu, &da.gbd);
+        if (!decode_set_maps(&da, w)) return NVFP4_ERR_CUDA;
+        da.offsets = ws.ra.offsets;
+        da.active = ws.ra.active;
+        da.n_active = ws.ra.n_active;
+        da.tile_start = ws.ra.tile_start;
+        da.row_to_slot = ws.ra.row_to_slot;
+        da.slot_to_row = ws.ra.slot_to_row;
+        da.topk_w = ws.ra.w;
+        da.gate_ws2 = w->gate.weight_scale_2;
+        da.up_ws2 = w->up.weight_scale_2;
+        da.down_ws2 = w->down.weight_scale_2;
+        da.x = x;
+        da.xq = ws.xq;
+        da.xs = ws.xs;
+        da.is13 = is13;
+        da.is2 = is2;
+        da.h = ws.h;
+        da.hq = ws.hq;
+        da.hs = ws.hs;
+        da.yrows = ws.yrows;
+        da.out = out;
+        da.counters = ws.clear + 2;
+        da.tile_ready = ws.tile_ready;
+        da.tok_done = ws.tok_done;
+        da.status = d_status;
+        launch_decode(mode == 0 ? B_BF16 : B_NVFP4, da, s);
+        return last_launch_status();
+    }
     GemvArgs a = base_args(ws, top_k);
     // gate/up + SwiGLU (also zeroes the fp32 combine accumulator)
     a.K = d;
@@ -525,11 +546,11 @@ extern "C" nvfp4_status nvfp4_linear(const uint16_t* x, int M, int K, const nvfp
             g.a_codes[1] = w_up->codes;  g.a_scales[1] = w_up->scales;  g.a_ws2[1] = w_up->weight_scale_2;
             g.h_out = out;
             if (!tcm_set_weights(&g, N)) return NVFP4_ERR_CUDA;
-            launch_tcm(TCM_SWIGLU, 0, g, max_units, stream);
+            launch_tcm(TCM_SWIGLU, g, max_units, stream);
         } else if (tcm) {
             g.y_out = out;
             if (!tcm_set_weights(&g, N)) return NVFP4_ERR_CUDA;
-            launch_tcm(TCM_BF16, 0, g, (max_units + 1) / 2, stream);
+            launch_tcm(TCM_BF16, g, (max_units + 1) / 2, stream);
         } else if (w_up) {
             t.a_codes[1] = w_up->codes;  t.a_scales[1] = w_up->scales;  t.a_ws2[1] = w_up->weight_scale_2;
             t.h_out = out;

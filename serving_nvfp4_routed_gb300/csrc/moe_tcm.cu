@@ -11,14 +11,12 @@
 //   D[j, n] = sum_k X[row0 + j, k] * B[n, k]
 //   SwiGLU: B rows 0..127 = gate rows f0.., 128..255 = up rows f0.. of e, so
 //           the two halves of a SwiGLU pair sit in one TMEM lane;
-//   combine / bf16: B rows = 256 consecutive rows f0.. of one projection.
+//   down (bf16 y rows) / bf16: B rows = 256 consecutive rows f0.. of one projection.
 // One tcgen05.mma kind::f16 with M = 128, N = 256, K = 16 runs at the full
 // dense rate; N = 128 takes the same time, hence the 256-wide B.
 // A (rows): f16 copies of the activations (a per-row power of two taken out,
 //    exact), a 128 x 64 tile per k-stage by TMA with 128-byte swizzle, in a
-//    ring of SA stages; or (W4A4) NVFP4 rows whose codes and scales ride in
-//    the weight rings below and are dequantised to f16 (exact) by the same
-//    producer warps, the expert's global scale applied in the epilogue.
+//    ring of SA stages.
 // B (weights): the stored e2m1 codes (128 rows x 32 bytes per box) and e4m3
 //    scales (128 rows x 16 bytes, four k-stages) arrive by TMA in rings of
 //    SR and SS slots; sixteen producer warps in four groups, each taking
@@ -57,27 +55,24 @@ constexpr int SS = 2;              // raw scales ring depth (groups of four k-st
 constexpr int kABytes = BM * BK * 2;   // 16 KB
 constexpr int kBBytes = BN * BK * 2;   // 32 KB
 constexpr int kRawB = BN * BK / 2;     // 8 KB: two boxes of 128 weight rows x 32 bytes
-constexpr int kRawA = BM * BK / 2;     // 4 KB: NVFP4 rows, 128 x 32 bytes
 constexpr int kScB = BN * 16;          // 4 KB: two boxes of 128 weight rows x 16 bytes
-constexpr int kScA = BM * 16;          // 2 KB
 constexpr int kMaxUnits = 256;         // units per CTA (the host sizes the grid for it)
 constexpr int kTileCopy = kMaxExperts + 1;
 constexpr int kGroups = 4;                      // producer groups, one per k-stage residue
 constexpr int kGroupWarps = 16 / kGroups;  // warps that produce one k-stage
 static_assert(SR % kGroups == 0, "each raw slot must belong to one producer group");
-// Ring geometry of each A kind (AQ = 1: NVFP4 rows).
-template <int AQ>
+// Ring geometry.
 struct Geo {
-    static constexpr int SA = AQ ? 3 : 4;  // A (row) tiles
-    static constexpr int SB = 3;           // f16 weight tiles
+    static constexpr int SA = 4;  // A (row) tiles
+    static constexpr int SB = 3;  // f16 weight tiles
     static constexpr int SD0 = SA > SB ? SA : SB;
     // "stage done" barriers: at least every ring depth and the k-stage stride
     // between two waits of one producer group, so that parity waits stay in phase
     static constexpr int SD = SD0 > kGroups ? SD0 : kGroups;
-    static constexpr int kRaw = kRawB + (AQ ? kRawA : 0);
-    static constexpr int kSc = kScB + (AQ ? kScA : 0);
+    static constexpr int kRaw = kRawB;
+    static constexpr int kSc = kScB;
     // fp32 row staging of the TCM_ROWS epilogue: 4 warps x 32 rows x 33 floats
-    static constexpr int kStaging = AQ ? 0 : 4 * 32 * 33 * 4;
+    static constexpr int kStaging = 4 * 32 * 33 * 4;
     static constexpr int kSmem =
         1024 + SA * kABytes + SB * kBBytes + SR * kRaw + SS * kSc + kMaxUnits * 16 + kTileCopy * 4 + kStaging;
     static_assert(kSmem <= 227 * 1024, "shared memory budget");
@@ -96,9 +91,9 @@ __device__ __forceinline__ bool wait_done(const uint64_t* done, long long j, vol
     return mbar_wait(smem_u32(&done[j % SD]), (uint32_t)((j / SD) & 1), abort_flag, status);
 }
 
-template <int EPI, int AQ>
+template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant__ TcmArgs a) {
-    using G = Geo<AQ>;
+    using G = Geo;
     constexpr int SA = G::SA, SB = G::SB, SD = G::SD, kRaw = G::kRaw, kSc = G::kSc;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -117,7 +112,7 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant_
     grid_dep_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < SA; ++s) mbar_init(smem_u32(&bar_afull[s]), AQ ? kGroupWarps : 1);
+        for (int s = 0; s < SA; ++s) mbar_init(smem_u32(&bar_afull[s]), 1);
         for (int s = 0; s < SB; ++s) mbar_init(smem_u32(&bar_bfull[s]), kGroupWarps);
         for (int s = 0; s < SD; ++s) mbar_init(smem_u32(&bar_done[s]), 1);
         for (int s = 0; s < SR; ++s) {
@@ -139,7 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant_
 
     // ---- this CTA's work list ----
     const int n_active = *a.n_active;
-    constexpr bool kPair = EPI == TCM_SWIGLU || EPI == TCM_SWIGLU_Q;  // gate + up halves
+    constexpr bool kPair = EPI == TCM_SWIGLU;  // gate + up halves
     const int n_nt = kPair ? a.N / (BN / 2) : a.N / BN;  // B slices per expert
     for (int i = threadIdx.x; i <= n_active; i += kThreads) s_tiles[i] = a.tile_start[i];
     __syncthreads();
@@ -227,7 +222,6 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant_
                         uint8_t* dst = ring_s + ss * kSc;
                         tma_load_2d(smem_u32(dst), &a.tmap_ws[0], kc * 4, y0, bar);
                         tma_load_2d(smem_u32(dst + kScB / 2), ms1, kc * 4, y1, bar);
-                        if constexpr (AQ) tma_load_2d(smem_u32(dst + kScB), &a.tmap_as, kc * 4, un.y, bar);
                         ++g;
                     }
                     const int sr = (int)(i % SR);
@@ -241,14 +235,13 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant_
                     uint8_t* dst = ring_r + sr * kRaw;
                     tma_load_2d(smem_u32(dst), &a.tmap_wc[0], kc * 32, y0, bar);
                     tma_load_2d(smem_u32(dst + kRawB / 2), mc1, kc * 32, y1, bar);
-                    if constexpr (AQ) tma_load_2d(smem_u32(dst + kRawB), &a.tmap_ac, kc * 32, un.y, bar);
                 }
             }
         }
         __syncwarp();
     } else if (warp == kWarpTmaA) {
         // ---------------- A producer: routed f16 rows by TMA (one thread) ----------------
-        if (!AQ && lane == 0) {
+        if (lane == 0) {
             long long i = 0;
             for (int it = 0; it < n_units; ++it) {
                 const int row0 = s_units[it].y;
@@ -275,59 +268,12 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant_
             const int acc = it & 1;
             const int row = un.y + rr;
             const bool valid = row < un.z;
-            float rs = 0.0f, wt = 0.0f;
-            size_t tok = 0;
-            if (valid) {
-                rs = AQ ? a.x_gs[un.x] : exp2i(a.x_exp[row]);
-                if constexpr (EPI == TCM_COMBINE || EPI == TCM_ROWS) {
-                    const int slot = a.row_to_slot[row];
-                    tok = (size_t)(slot / a.top_k);
-                    wt = a.topk_w[slot];
-                }
-            }
+            const float rs = valid ? exp2i(a.x_exp[row]) : 0.0f;
             const float w0 = a.a_ws2[0][un.x], w1 = a.a_ws2[1][un.x];
             if (!mbar_wait(smem_u32(&bar_acc_full[acc]), (it >> 1) & 1, abort_flag, a.status, 64)) break;
             tc_fence_after();
             const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + acc * BN;
-            if constexpr (EPI == TCM_SWIGLU_Q) {
-                // h in 16-feature blocks, requantised to NVFP4 under hq_gs[e]
-                const float gs2 = a.hq_gs[un.x];
-                for (int cb = 0; cb < BN / 32; ++cb) {
-                    uint32_t g[16], u[16];
-                    tmem_ld16(tb + cb * 16, g);
-                    tmem_ld16(tb + BN / 2 + cb * 16, u);
-                    tmem_ld_wait();
-                    if (valid) {
-                        float hv[16];
-                        float m = 0.0f;
-#pragma unroll
-                        for (int t = 0; t < 16; ++t) {
-                            const float G = round_bf16(__fmul_rn(__fmul_rn(__uint_as_float(g[t]), rs), w0));
-                            const float U = round_bf16(__fmul_rn(__fmul_rn(__uint_as_float(u[t]), rs), w1));
-                            hv[t] = round_bf16(G / (1.0f + expf(-G)) * U);
-                            m = fmaxf(m, fabsf(hv[t]));
-                        }
-                        uint32_t sbyte = 0, q0 = 0, q1 = 0;
-                        if (gs2 > 0.0f) {
-                            sbyte = f32_to_e4m3(__fdiv_rn(__fdiv_rn(m, 6.0f), gs2));
-                            const float S = e4m3_to_f32(sbyte);
-                            if (S != 0.0f) {
-                                const float den = __fmul_rn(S, gs2), rden = __frcp_rn(den);
-#pragma unroll
-                                for (int t = 0; t < 8; t += 2) {
-                                    q0 |= e2m1x2_byte(e2m1_quotient(hv[t], den, rden),
-                                                      e2m1_quotient(hv[t + 1], den, rden)) << (4 * t);
-                                    q1 |= e2m1x2_byte(e2m1_quotient(hv[8 + t], den, rden),
-                                                      e2m1_quotient(hv[9 + t], den, rden)) << (4 * t);
-                                }
-                            }
-                        }
-                        const int f = un.w + cb * 16;
-                        *reinterpret_cast<uint2*>(a.hq_out + (size_t)row * (a.N / 2) + f / 2) = make_uint2(q0, q1);
-                        a.hs_out[(size_t)row * (a.N / 16) + f / 16] = (uint8_t)sbyte;
-                    }
-                }
-            } else if constexpr (EPI == TCM_SWIGLU) {
+            if constexpr (EPI == TCM_SWIGLU) {
                 for (int cb = 0; cb < BN / 32; ++cb) {
                     uint32_t g[16], u[16];
                     tmem_ld16(tb + cb * 16, g);
@@ -353,22 +299,24 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant_
                     }
                 }
             } else if constexpr (EPI == TCM_ROWS) {
-                // w * y as fp32 rows by routed row: 32 rows x 32 columns per
-                // chunk through shared memory, then one whole row (128 bytes)
-                // per store instruction; a second kernel sums each token's rows
-                // in slot order (deterministic combine)
+                // y = ws2 * x W^T as bf16 rows by routed row: 32 rows x 32 columns
+                // per chunk through shared memory, then two rows (2 x 64 bytes)
+                // per store instruction; a second kernel adds each token's k
+                // rows, weighted, in slot order (deterministic combine)
                 float* st = s_stage + (size_t)q * 32 * 33;
                 const int nvalid = min(32, un.z - (un.y + q * 32));  // rows of this warp in the unit
+                const int hr = lane >> 4, cl = (lane & 15) * 2;
                 for (int cb = 0; cb < BN / 32; ++cb) {
                     uint32_t r[32];
                     tmem_ld32(tb + cb * 32, r);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        st[lane * 33 + c] = wt * __fmul_rn(__fmul_rn(__uint_as_float(r[c]), rs), w0);
+                    for (int c = 0; c < 32; ++c) st[lane * 33 + c] = __fmul_rn(__fmul_rn(__uint_as_float(r[c]), rs), w0);
                     __syncwarp();
-                    float* ybase = a.y_rows + (size_t)(un.y + q * 32) * a.N + un.w + cb * 32 + lane;
-                    for (int j = 0; j < nvalid; ++j) ybase[(size_t)j * a.N] = st[j * 33 + lane];
+                    uint16_t* ybase = a.y_rows + (size_t)(un.y + q * 32) * a.N + un.w + cb * 32 + cl;
+                    for (int j = hr; j < nvalid; j += 2)
+                        *reinterpret_cast<uint32_t*>(ybase + (size_t)j * a.N) =
+                            (uint32_t)f32_to_bf16_bits(st[j * 33 + cl]) | ((uint32_t)f32_to_bf16_bits(st[j * 33 + cl + 1]) << 16);
                     __syncwarp();
                 }
             } else {
@@ -377,30 +325,17 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant_
                     tmem_ld32(tb + cb * 32, r);
                     tmem_ld_wait();
                     if (valid) {
-                        if constexpr (EPI == TCM_COMBINE) {
-                            float4* dst = reinterpret_cast<float4*>(a.acc_out + tok * a.N + un.w + cb * 32);
+                        uint32_t packed[16];
 #pragma unroll
-                            for (int v = 0; v < 8; ++v) {
-                                float y[4];
-#pragma unroll
-                                for (int t = 0; t < 4; ++t)
-                                    y[t] = wt * __fmul_rn(__fmul_rn(__uint_as_float(r[4 * v + t]), rs), w0);
-                                red_add_v4(reinterpret_cast<float*>(dst + v), y[0], y[1], y[2], y[3]);
-                            }
-                        } else {
-                            uint32_t packed[16];
-#pragma unroll
-                            for (int j = 0; j < 32; j += 2) {
-                                const float y0 = __fmul_rn(__fmul_rn(__uint_as_float(r[j]), rs), w0);
-                                const float y1 = __fmul_rn(__fmul_rn(__uint_as_float(r[j + 1]), rs), w0);
-                                packed[j / 2] = (uint32_t)f32_to_bf16_bits(y0) | ((uint32_t)f32_to_bf16_bits(y1) << 16);
-                            }
-                            uint4* dst = reinterpret_cast<uint4*>(a.y_out + (size_t)row * a.N + un.w + cb * 32);
-#pragma unroll
-                            for (int v = 0; v < 4; ++v)
-                                dst[v] =
-                                    make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+                        for (int j = 0; j < 32; j += 2) {
+                            const float y0 = __fmul_rn(__fmul_rn(__uint_as_float(r[j]), rs), w0);
+                            const float y1 = __fmul_rn(__fmul_rn(__uint_as_float(r[j + 1]), rs), w0);
+                            packed[j / 2] = (uint32_t)f32_to_bf16_bits(y0) | ((uint32_t)f32_to_bf16_bits(y1) << 16);
                         }
+                        uint4* dst = reinterpret_cast<uint4*>(a.y_out + (size_t)row * a.N + un.w + cb * 32);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
                     }
                 }
             }
@@ -411,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant_
     } else if (warp >= kWarpDeq) {
         // ---------------- producers: raw NVFP4 rows -> f16 tile rows ----------------
         // Group grp takes k-stage grp of every scale group (four k-stages);
-        // its 128 threads own two B rows each and (W4A4) one A row each.
+        // its 128 threads own two B rows each.
         // The proxy fence after the stage's smem stores also orders the
         // reads of the TMA-filled raw slots before their next fill, so the
         // raw slots are released together with the f16 tiles.
@@ -431,8 +366,6 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant_
                 const int q = grp;
                 const uint32_t sw0 = *reinterpret_cast<const uint32_t*>(ring_s + ss * kSc + tg * 16 + q * 4);
                 const uint32_t sw1 = *reinterpret_cast<const uint32_t*>(ring_s + ss * kSc + (tg + 128) * 16 + q * 4);
-                uint32_t asw = 0;
-                if constexpr (AQ) asw = *reinterpret_cast<const uint32_t*>(ring_s + ss * kSc + kScB + tg * 16 + q * 4);
                 const long long i = (long long)it * nk + kg * 4 + q;
                 const int sr = (int)(i % SR);
                 if (!mbar_wait(smem_u32(&bar_rfull[sr]), (uint32_t)((i / SR) & 1), abort_flag, a.status)) {
@@ -444,12 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant_
                 c[1] = *reinterpret_cast<const uint4*>(ring_r + sr * kRaw + tg * 32 + 16);
                 c[2] = *reinterpret_cast<const uint4*>(ring_r + sr * kRaw + (tg + 128) * 32);
                 c[3] = *reinterpret_cast<const uint4*>(ring_r + sr * kRaw + (tg + 128) * 32 + 16);
-                uint4 ca0 = make_uint4(0u, 0u, 0u, 0u), ca1 = ca0;
-                if constexpr (AQ) {
-                    ca0 = *reinterpret_cast<const uint4*>(ring_r + sr * kRaw + kRawB + tg * 32);
-                    ca1 = *reinterpret_cast<const uint4*>(ring_r + sr * kRaw + kRawB + tg * 32 + 16);
-                }
-                if (!wait_done<SD>(bar_done, i - (AQ ? (SA < SB ? SA : SB) : SB), abort_flag, a.status)) {
+                if (!wait_done<SD>(bar_done, i - SB, abort_flag, a.status)) {
                     ok = false;
                     break;
                 }
@@ -472,26 +400,10 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant_
                             hmul2_u32(f[0], S2), hmul2_u32(f[1], S2), hmul2_u32(f[2], S2), hmul2_u32(f[3], S2));
                     }
                 }
-                if constexpr (AQ) {
-                    uint8_t* arow = ring_a + (i % SA) * kABytes + tg * 128;
-                    const uint32_t SA01 = e4m3x2_to_f16x2(asw & 0xFFFFu), SA23 = e4m3x2_to_f16x2(asw >> 16);
-                    const uint32_t Sa[4] = {f16x2_bcast(SA01, 0), f16x2_bcast(SA01, 1), f16x2_bcast(SA23, 0),
-                                            f16x2_bcast(SA23, 1)};
-                    const uint32_t caw[8] = {ca0.x, ca0.y, ca0.z, ca0.w, ca1.x, ca1.y, ca1.z, ca1.w};
-#pragma unroll
-                    for (int w = 0; w < 8; ++w) {
-                        uint32_t f[4];
-                        e2m1x8_to_f16x8(caw[w], f);
-                        const uint32_t S2 = Sa[w >> 1];
-                        *reinterpret_cast<uint4*>(arow + ((w ^ (tg & 7)) << 4)) = make_uint4(
-                            hmul2_u32(f[0], S2), hmul2_u32(f[1], S2), hmul2_u32(f[2], S2), hmul2_u32(f[3], S2));
-                    }
-                }
                 fence_proxy_async();
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(smem_u32(&bar_bfull[i % SB]));
-                    if constexpr (AQ) mbar_arrive(smem_u32(&bar_afull[i % SA]));
                     mbar_arrive(smem_u32(&bar_rempty[sr]));
                     mbar_arrive(smem_u32(&bar_sempty[ss]));
                 }
@@ -511,10 +423,10 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant_
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
-template <int EPI, int AQ>
+template <int EPI>
 void launch_tcm_t(const TcmArgs& a, int max_units, cudaStream_t s, const char* name) {
-    auto kern = tcm_kernel<EPI, AQ>;
-    constexpr int smem = Geo<AQ>::kSmem;
+    auto kern = tcm_kernel<EPI>;
+    constexpr int smem = Geo::kSmem;
     static bool init = false;
     if (!init) {
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -586,7 +498,8 @@ bool make_tmap_weights(CUtensorMap* codes, CUtensorMap* scales, const uint8_t* c
 }
 
 bool tcm_supported(int epi, int N, int K) {
-    const bool pair = epi == TCM_SWIGLU || epi == TCM_SWIGLU_Q;
+    if (epi != TCM_SWIGLU && epi != TCM_ROWS && epi != TCM_BF16) return false;
+    const bool pair = epi == TCM_SWIGLU;
     return K % 256 == 0 && (pair ? N % (BN / 2) == 0 : N % BN == 0);
 }
 
@@ -598,21 +511,10 @@ bool tcm_set_weights(TcmArgs* a, long long rows) {
     return true;
 }
 
-bool tcm_set_act(TcmArgs* a, const uint8_t* codes, const uint8_t* scales, long long rows) {
-    init_encode();
-    return make_tmap_weights(&a->tmap_ac, &a->tmap_as, codes, scales, rows, a->K);
-}
-
-void launch_tcm(int epi, int a_nvfp4, const TcmArgs& a, int max_units, cudaStream_t s) {
-    if (a_nvfp4) {
-        if (epi == TCM_SWIGLU_Q) return launch_tcm_t<TCM_SWIGLU_Q, 1>(a, max_units, s, "tcm_gateup_w4a4");
-        if (epi == TCM_COMBINE) return launch_tcm_t<TCM_COMBINE, 1>(a, max_units, s, "tcm_down_w4a4");
-        return;
-    }
-    if (epi == TCM_SWIGLU) return launch_tcm_t<TCM_SWIGLU, 0>(a, max_units, s, "tcm_gateup_w4a16");
-    if (epi == TCM_COMBINE) return launch_tcm_t<TCM_COMBINE, 0>(a, max_units, s, "tcm_down_w4a16");
-    if (epi == TCM_ROWS) return launch_tcm_t<TCM_ROWS, 0>(a, max_units, s, "tcm_down_w4a16");
-    if (epi == TCM_BF16) return launch_tcm_t<TCM_BF16, 0>(a, max_units, s, "tcm_linear_w4a16");
+void launch_tcm(int epi, const TcmArgs& a, int max_units, cudaStream_t s) {
+    if (epi == TCM_SWIGLU) return launch_tcm_t<TCM_SWIGLU>(a, max_units, s, "tcm_gateup_w4a16");
+    if (epi == TCM_ROWS) return launch_tcm_t<TCM_ROWS>(a, max_units, s, "tcm_down_w4a16");
+    if (epi == TCM_BF16) return launch_tcm_t<TCM_BF16>(a, max_units, s, "tcm_linear_w4a16");
 }
 
 }  // namespace nvfp4

@@ -15,9 +15,9 @@
 //   SwiGLU: B rows 0..95 = gate rows f0.., 96..191 = up rows f0..;
 //   down: B rows = 192 consecutive rows f0.. of the down projection (the
 //   last unit of a row tile may reach past the expert's rows: those columns
-//   are computed and dropped); the epilogue writes fp32 rows w * y by routed
-//   row (staged through shared memory so that every store is a whole
-//   128-byte line) and a second kernel sums each token's slots in slot order.
+//   are computed and dropped); the epilogue writes bf16 rows y by routed row
+//   (staged through shared memory, two 64-byte row segments per store) and a
+//   second kernel adds each token's slots, weighted, in slot order.
 // One MMA has M = 128, N = 192, K = 64 (96 cycles at the full FP4 rate).
 // N = 192 rather than 128: a single issuing warp spends ~100 cycles per MMA
 // on issue, barrier and commit work, which a 64-cycle N = 128 MMA cannot
@@ -304,10 +304,6 @@ __global__ void __launch_bounds__(kThreads, 1) tcq_kernel(const __grid_constant_
             const int acc = it & 1;
             const int row = un.y + rr;
             const bool valid = row < un.z;
-            float wt = 0.0f;
-            if constexpr (EPI == TCM_ROWS) {
-                if (valid) wt = a.topk_w[a.row_to_slot[row]];
-            }
             const float rs = a.x_gs[un.x];
             const float w0 = a.a_ws2[0][un.x], w1 = a.a_ws2[1][un.x];
             if (!mbar_wait(smem_u32(&bar_acc_full[acc]), (it >> 1) & 1, abort_flag, a.status, 64)) break;
@@ -354,10 +350,11 @@ __global__ void __launch_bounds__(kThreads, 1) tcq_kernel(const __grid_constant_
                     }
                 }
             } else if constexpr (EPI == TCM_ROWS) {
-                // 32 rows x 32 columns per warp and chunk: through shared memory,
-                // then one whole row (128 bytes) per store instruction
+                // 32 rows x 32 columns per warp and chunk: y (fp32) through shared
+                // memory, then two bf16 rows (2 x 64 bytes) per store instruction
                 float* st = s_stage + (size_t)(half * 4 + q) * 32 * kStageRow;
                 const int nvalid = min(32, un.z - (un.y + q * 32));  // rows of this warp in the unit
+                const int hr = lane >> 4, cl = (lane & 15) * 2;
                 for (int cb = 3 * half; cb < 3 * half + 3; ++cb) {
                     if (un.w + cb * 32 >= a.N) break;  // columns past the expert's rows
                     uint32_t r[32];
@@ -365,10 +362,13 @@ __global__ void __launch_bounds__(kThreads, 1) tcq_kernel(const __grid_constant_
                     tmem_ld_wait();
 #pragma unroll
                     for (int c = 0; c < 32; ++c)
-                        st[lane * kStageRow + c] = wt * __fmul_rn(__fmul_rn(__uint_as_float(r[c]), rs), w0);
+                        st[lane * kStageRow + c] = __fmul_rn(__fmul_rn(__uint_as_float(r[c]), rs), w0);
                     __syncwarp();
-                    float* ybase = a.y_rows + (size_t)(un.y + q * 32) * a.N + un.w + cb * 32 + lane;
-                    for (int j = 0; j < nvalid; ++j) ybase[(size_t)j * a.N] = st[j * kStageRow + lane];
+                    uint16_t* ybase = a.y_rows + (size_t)(un.y + q * 32) * a.N + un.w + cb * 32 + cl;
+                    for (int j = hr; j < nvalid; j += 2)
+                        *reinterpret_cast<uint32_t*>(ybase + (size_t)j * a.N) =
+                            (uint32_t)f32_to_bf16_bits(st[j * kStageRow + cl]) |
+                            ((uint32_t)f32_to_bf16_bits(st[j * kStageRow + cl + 1]) << 16);
                     __syncwarp();
                 }
             }
@@ -387,9 +387,10 @@ __global__ void __launch_bounds__(kThreads, 1) tcq_kernel(const __grid_constant_
     grid_dep_launch();
 }
 
-// out[t][f] = bf16(sum_j y[slot_to_row[t*k + j]][f]) in slot order; 8 features per thread.
-__global__ void sum_rows_kernel(const float* __restrict__ y, const int32_t* __restrict__ slot_to_row, int T, int k,
-                                int d, uint16_t* __restrict__ out) {
+// out[t][f] = bf16(sum_j w[t*k + j] * y[slot_to_row[t*k + j]][f]), the
+// fp32 sum in slot order over bf16 y rows; 8 features per thread.
+__global__ void sum_rows_kernel(const uint16_t* __restrict__ y, const int32_t* __restrict__ slot_to_row,
+                                const float* __restrict__ topk_w, int T, int k, int d, uint16_t* __restrict__ out) {
     grid_dep_wait();
     const int per_row = d / 8;
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < (size_t)T * per_row;
@@ -400,10 +401,14 @@ __global__ void sum_rows_kernel(const float* __restrict__ y, const int32_t* __re
         for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
         for (int j = 0; j < k; ++j) {
             const size_t r = (size_t)slot_to_row[t * k + j];
-            const float4* src = reinterpret_cast<const float4*>(y + r * d + f);
-            const float4 p0 = __ldcs(src), p1 = __ldcs(src + 1);
-            acc[0] += p0.x; acc[1] += p0.y; acc[2] += p0.z; acc[3] += p0.w;
-            acc[4] += p1.x; acc[5] += p1.y; acc[6] += p1.z; acc[7] += p1.w;
+            const float wj = topk_w[t * k + j];
+            const uint4 p = __ldcs(reinterpret_cast<const uint4*>(y + r * d + f));
+            const uint32_t pw[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                acc[2 * q] += wj * bf16_bits_to_f32(pw[q] & 0xFFFFu);
+                acc[2 * q + 1] += wj * bf16_bits_to_f32(pw[q] >> 16);
+            }
         }
         uint4 o;
         o.x = (uint32_t)f32_to_bf16_bits(acc[0]) | ((uint32_t)f32_to_bf16_bits(acc[1]) << 16);
@@ -453,12 +458,13 @@ void launch_tcq(int epi, const TcmArgs& a, int max_tiles, cudaStream_t s) {
     if (epi == TCM_ROWS) return launch_tcq_t<TCM_ROWS>(a, max_units, s, "tcq_down_w4a4");
 }
 
-void launch_sum_rows(const float* y, const int32_t* slot_to_row, int T, int k, int d, uint16_t* out,
-                     cudaStream_t s) {
+void launch_sum_rows(const uint16_t* y, const int32_t* slot_to_row, const float* topk_w, int T, int k, int d,
+                     uint16_t* out, cudaStream_t s) {
     const size_t n = (size_t)T * (d / 8);
     if (n == 0) return;
     const int grid = (int)std::min<size_t>((n + 255) / 256, (size_t)num_sms() * 8);
-    NVFP4_LAUNCH("sum_rows", s, launch_pdl(sum_rows_kernel, dim3(grid), dim3(256), 0, s, y, slot_to_row, T, k, d, out));
+    NVFP4_LAUNCH("sum_rows", s, launch_pdl(sum_rows_kernel, dim3(grid), dim3(256), 0, s, y, slot_to_row, topk_w, T, k,
+                                           d, out));
 }
 
 }  // namespace nvfp4

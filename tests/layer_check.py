@@ -9,14 +9,21 @@ For the listed tokens:
     or lies in the interval the error model allows (gpu_util.h_interval);
   * the output satisfies gpu_util.assert_out_close with the bound
         (gamma(F) + (k + 2) 2^-24) * out_abs  +  effect of the h differences,
-    where out_abs is the oracle's sum_j |w_j| * scale * sum_f |h_f W_d|.
+    where out_abs is the oracle's sum_j |w_j| * scale * sum_f |h_f W_d|;
+  * paths that keep each routed row's y in bf16 (round_y, the prompt-shaped
+    kernels) round at R3 too: each kernel Y_j lies in
+    [bf16(y_j - e_j), bf16(y_j + e_j)] around the oracle's unrounded y_j,
+    e_j = gamma(F) * y_abs_j + 2^-23 |y_j| + the effect of the pair's h
+    differences, and the bound is sum_j |w_j| D_j + (k + 1) 2^-24
+    sum_j |w_j| (|bf16(y_j)| + D_j), D_j the widest distance from bf16(y_j)
+    to that interval's ends.
 """
 import numpy as np
 import torch
 
 import serving_nvfp4_routed_gb300 as lib
 from gpu_util import (U32, assert_h_in_interval, assert_out_close, bf16_to_f32, gamma, h_interval,
-                      nvfp4_block_feasible, unpack_codes)
+                      nvfp4_block_feasible, round_bf16, unpack_codes)
 from serving_nvfp4_routed_gb300 import synth
 
 
@@ -33,7 +40,7 @@ def _deq_rows(codes, scales):
     return E2M1[unpack_codes(codes)] * np.repeat(_e4m3(scales), 16, axis=-1)
 
 
-def check_layer(orc, mode, x, logits, k, ob, out, ws, tok, is13=None, is2=None, what=""):
+def check_layer(orc, mode, x, logits, k, ob, out, ws, tok, is13=None, is2=None, what="", round_y=False):
     """Compare the layer output `out` (GPU, [T, d] bf16, computed with the
     workspace `ws`) for tokens `tok` against the oracle; returns a report."""
     T, d = x.shape
@@ -44,7 +51,7 @@ def check_layer(orc, mode, x, logits, k, ob, out, ws, tok, is13=None, is2=None, 
     v = lib.moe_workspace_views(ws, T, E, k, d, F, mode)
     assert np.array_equal(v["ids"].cpu().numpy(), r["ids"]), f"{what}: routing ids"
     assert np.array_equal(v["slot_to_row"].cpu().numpy(), r["slot_to_row"]), f"{what}: permutation"
-    ex = orc.moe_layer_ex(mode, xb, r["ids"], r["w"], ob, tokens=tok, is13=is13, is2=is2)
+    ex = orc.moe_layer_ex(mode, xb, r["ids"], r["w"], ob, tokens=tok, is13=is13, is2=is2, round_y=round_y)
     n = len(tok)
     rows = r["slot_to_row"].reshape(T, k)[tok]  # [n, k] permuted row of each pair
     ids = r["ids"][tok]
@@ -76,17 +83,24 @@ def check_layer(orc, mode, x, logits, k, ob, out, ws, tok, is13=None, is2=None, 
                 f"{what}: NVFP4 h block (token {tok[i]}, slot {j}, block {b}) not reachable from the allowed h")
         delta = _deq_rows(hq, hs) - _deq_rows(ex["hq"], ex["hs"])
         scale_d = np.asarray(is2, np.float64)[ids]
-    # effect of the h differences on the output, through |W_d|
-    h_eff = np.zeros((n, d))
-    wts = r["w"][tok].astype(np.float64)
+    # effect of each pair's h differences on its y, through |W_d|
+    h_eff = np.zeros((n, k, d))
+    wts = np.abs(r["w"][tok].astype(np.float64))
     dq, dsc, d2 = ob["down"]
     cache = {}
     for i, j in zip(*np.nonzero(np.any(delta != 0, axis=-1))):
         e = int(ids[i, j])
         if e not in cache:
             cache[e] = np.abs(orc.dequantize(dq[e], dsc[e]))
-        h_eff[i] += abs(wts[i, j]) * float(d2[e]) * scale_d[i, j] * (cache[e] @ np.abs(delta[i, j]))
-    bound = (gamma(F) + (k + 2) * U32) * ex["out_abs"] + h_eff
+        h_eff[i, j] = float(d2[e]) * scale_d[i, j] * (cache[e] @ np.abs(delta[i, j]))
+    if round_y:
+        e_y = gamma(F) * ex["y_abs"] + 2 * U32 * np.abs(ex["y_pre"]) + h_eff
+        y_r = round_bf16(ex["y_pre"])
+        dist = np.maximum(y_r - round_bf16(ex["y_pre"] - e_y), round_bf16(ex["y_pre"] + e_y) - y_r)
+        bound = (np.einsum("nk,nkd->nd", wts, dist)
+                 + (k + 1) * U32 * np.einsum("nk,nkd->nd", wts, np.abs(y_r) + dist))
+    else:
+        bound = (gamma(F) + (k + 2) * U32) * ex["out_abs"] + np.einsum("nk,nkd->nd", wts, h_eff)
     got = bf16_to_f32(out)[tok]
     rep = assert_out_close(got, ex["out"], ex["out_pre"], bound, what)
     rep["h_pairs_differing"] = int(np.any(delta != 0, axis=-1).sum())

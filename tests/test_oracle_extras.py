@@ -80,6 +80,7 @@ def test_tolerance_helpers_accept_the_oracle_and_reject_a_real_miss(orc):
     bound = 1e-6 * ex["out_abs"]
     assert_out_close(ex["out"], ex["out"], ex["out_pre"], bound)
     # a one-step miss on the largest element, whose exact value is not near a midpoint
+    # (the bound is far below half a step there)
     out = ex["out"].astype(np.float64).copy()
     i = np.argmax(np.abs(out))
     step = np.ldexp(1.0, np.frexp(out.flat[i])[1] - 8)
@@ -108,3 +109,27 @@ def test_block_feasibility_accepts_the_oracle_blocks(orc):
                                     codes[t, j, sl])
     # a scale byte far above any reachable block maximum is rejected
     assert not nvfp4_block_feasible(orc, lo[t, j, :16], hi[t, j, :16], float(is2[e]), 0x7E, codes[t, j, :16])
+
+
+def test_round_y_switch(orc):
+    """y_pre is each pair's down projection (numpy over the dequantised
+    weights); with the R3 switch the output is bf16 of the slot-ordered
+    weighted sum of the bf16-rounded y, without it of the unrounded y."""
+    s, inp, bank, xb, r = _setup(orc, seed=21)
+    ex = orc.moe_layer_ex("w4a16", xb, r["ids"], r["w"], bank)
+    ex3 = orc.moe_layer_ex("w4a16", xb, r["ids"], r["w"], bank, round_y=True)
+    assert np.array_equal(ex["y_pre"], ex3["y_pre"]) and np.array_equal(ex["h"], ex3["h"])
+    dq, ds, d2 = bank["down"]
+    for t in range(s.T):
+        acc = np.zeros(s.d)
+        for j in range(s.k):
+            e = r["ids"][t, j]
+            Wd = _deq(dq[e], ds[e])
+            y = float(d2[e]) * (Wd @ ex["h"][t, j].astype(np.float64))
+            np.testing.assert_allclose(ex["y_pre"][t, j], y, rtol=1e-12, atol=1e-300)
+            np.testing.assert_allclose(ex["y_abs"][t, j], float(d2[e]) * (np.abs(Wd) @ np.abs(ex["h"][t, j])),
+                                       rtol=1e-12)
+            acc = acc + float(r["w"][t, j]) * round_bf16(ex3["y_pre"][t, j])
+        np.testing.assert_allclose(ex3["out_pre"][t], acc, rtol=1e-13, atol=1e-300)
+    assert np.array_equal(round_bf16(ex3["out_pre"]), ex3["out"])
+    assert not np.array_equal(ex["out_pre"], ex3["out_pre"])
