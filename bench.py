@@ -650,6 +650,10 @@ def measure(layer, lib, args, flush, hbm, bf16, peak_kind, steps, world=1, dev=N
     launches = lib.launch_count() - launches0
     ms = statistics.mean(times)
     value, ms_max = aggregate(layer.shape.T, ms, world, dev)
+    if args.lean:
+        # only the timed steps (for profiler captures): no per-launch events, no host-buffer run
+        return {"value": value, "ms_per_step": ms_max, "times_ms": times, "launches": launches, "kernels": {},
+                "roofline": {"touched_experts": touched}, "clocks": clk.summary(), "e2e": None}
     lib.profile_enable(True)
     time_steps(layer, steps, flush)
     lib.profile_enable(False)
@@ -725,7 +729,7 @@ def run_ours(args):
         "gpu_launches": m["launches"],
         "clocks": m["clocks"],
     }
-    if layer.kind != "dense":
+    if layer.kind != "dense" and not args.lean:
         line["router_gemm"] = time_router(layer, max(3, args.steps), flush)
         line["graph_replay"] = time_graph(layer, max(3, args.steps), flush)
         recipe = time_recipe(layer, flush)
@@ -845,6 +849,10 @@ def main(argv=None):
     ap.add_argument("--no-workloads", dest="workloads", action="store_false",
                     help="skip the prompt-shaped and dense workloads of the default run")
     ap.add_argument("--prompt-steps", type=int, default=10)
+    ap.add_argument("--lean", action="store_true",
+                    help="time the layer steps only (no kernel split, host-buffer run or side timings): for "
+                         "profiler captures, whose launch list then holds the warm-up, the touched-expert count "
+                         "(one step per input batch) and the timed steps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=8)
     ap.add_argument("--ref-tokens", type=int, default=4)

@@ -256,6 +256,29 @@ nvfp4_status nvfp4_moe_workspace_intermediates(void* ws, int T, int E, int top_k
                                                uint8_t** hq, uint8_t** hs);
 
 /* ------------------------------------------------------------------------
+ * moe_gather_rows / moe_combine_rows -- the two ends of an expert-parallel
+ * routed layer (W4A4 model card "GLM-5.3-Flash-NVFP4-W4A4-Experts",
+ * "Validation": the routed experts run expert-parallel over several GPUs;
+ * TensorFold #308 "What the branch does": the grouped kernel takes the
+ * routed rows expert by expert).  With the permutation of
+ * moe_route_permute (R = T * top_k rows, expert-contiguous):
+ *   moe_gather_rows:  rows_out[r] = x[row_to_slot[r] / top_k]   [R, d] bf16
+ *                     expert_of_row[r] = e, offsets[e] <= r < offsets[e+1]
+ *                     (nullable; then expert_offsets and E are unused)
+ *     -- the rows a rank sends, in order, to the ranks owning the experts;
+ *   moe_combine_rows: out[t] = bf16(sum_j topk_w[t, j] * y[slot_to_row[t*k + j]])
+ *                     (fp32, j in slot order), y bf16 [R, d] in the same
+ *                     row order -- the combine of the rows that come back.
+ * d % 8 == 0; device pointers owned by the caller, 16-byte aligned; T == 0
+ * is a no-op; asynchronous on the stream.
+ * --------------------------------------------------------------------- */
+nvfp4_status moe_gather_rows(const uint16_t* x_bf16, int T, int d, const int32_t* row_to_slot, int top_k,
+                             const int32_t* expert_offsets, int E, uint16_t* rows_out, int32_t* expert_of_row,
+                             cudaStream_t stream);
+nvfp4_status moe_combine_rows(const uint16_t* y_bf16, const int32_t* slot_to_row, const float* topk_w, int T,
+                              int top_k, int d, uint16_t* out_bf16, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * nvfp4_set_kernel_choice -- which kernels the later nvfp4_moe_* and
  * nvfp4_linear calls of this process run (the pages have no counterpart):
  *   0 = by shape (the default: the prompt-shaped tensor-core kernels once

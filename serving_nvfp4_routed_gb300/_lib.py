@@ -29,7 +29,7 @@ EXPORTS = ("nvfp4_quantize_weights", "nvfp4_quantize_weights_workspace_size", "n
            "nvfp4_linear_workspace_size", "nvfp4_status_string", "nvfp4_launch_count",
            "nvfp4_profile_enable", "nvfp4_profile_collect", "nvfp4_quantize_weights_noalloc",
            "nvfp4_quantize_weights_noalloc_max_batch", "nvfp4_selftest_bounded_wait", "moe_router_logits",
-           "moe_shared_expert", "moe_shared_expert_workspace_size")
+           "moe_shared_expert", "moe_shared_expert_workspace_size", "moe_gather_rows", "moe_combine_rows")
 
 
 class Nvfp4Error(RuntimeError):
@@ -77,6 +77,8 @@ def load(path: str = LIB_PATH):
         L.nvfp4_moe_workspace_views.argtypes = [vp, i32, i32, i32, i32, i32, i32] + [ctypes.POINTER(vp)] * 5
         L.nvfp4_moe_workspace_intermediates.argtypes = [vp, i32, i32, i32, i32, i32, i32] + [ctypes.POINTER(vp)] * 5
         L.nvfp4_set_kernel_choice.argtypes = [i32]
+        L.moe_gather_rows.argtypes = [vp, i32, i32, vp, i32, vp, i32, vp, vp, vp]
+        L.moe_combine_rows.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
         L.nvfp4_linear.argtypes = [vp, i32, i32, ctypes.POINTER(_W), i32, ctypes.POINTER(_W), vp, vp, sz, vp]
         L.nvfp4_linear_workspace_size.argtypes = [i32, i32, i32]
         L.nvfp4_linear_workspace_size.restype = sz
@@ -244,6 +246,38 @@ def moe_route_permute(logits: torch.Tensor, top_k: int, stream=None) -> dict:
                                _p(out["row_to_slot"]), _p(out["slot_to_row"]), _p(ws), wsb, _stream(stream)))
     out["row_to_slot"] = out["row_to_slot"][:R]
     out["slot_to_row"] = out["slot_to_row"][:R]
+    return out
+
+
+def moe_gather_rows(x: torch.Tensor, row_to_slot: torch.Tensor, top_k: int, expert_offsets=None, stream=None):
+    """Routed rows in the permutation's order: rows[r] = x[row_to_slot[r] // top_k]
+    (bf16 [R, d]), and with expert_offsets the expert of each row (int32 [R])."""
+    L = load()
+    _cuda(x, row_to_slot, expert_offsets)
+    x = x.contiguous()
+    T, d = x.shape
+    R = T * top_k
+    rows = _empty((R, d), torch.bfloat16, x.device)
+    eor = _empty((max(R, 1),), torch.int32, x.device) if expert_offsets is not None else None
+    E = 0 if expert_offsets is None else expert_offsets.numel() - 1
+    _check("moe_gather_rows",
+           L.moe_gather_rows(_p(x.view(torch.int16)), T, d, _p(row_to_slot), top_k, _p(expert_offsets), E,
+                             _p(rows.view(torch.int16)), _p(eor), _stream(stream)))
+    return rows, (eor[:R] if eor is not None else None)
+
+
+def moe_combine_rows(y: torch.Tensor, slot_to_row: torch.Tensor, topk_w: torch.Tensor, T: int, top_k: int,
+                     out=None, stream=None):
+    """out[t] = bf16(sum_j topk_w[t, j] * y[slot_to_row[t * k + j]]), fp32 in slot order."""
+    L = load()
+    _cuda(y, slot_to_row, topk_w, out)
+    y = y.contiguous()
+    d = y.shape[1]
+    if out is None:
+        out = _empty((T, d), torch.bfloat16, y.device)
+    _check("moe_combine_rows",
+           L.moe_combine_rows(_p(y.view(torch.int16)), _p(slot_to_row), _p(topk_w.contiguous()), T, top_k, d,
+                              _p(out.view(torch.int16)), _stream(stream)))
     return out
 
 

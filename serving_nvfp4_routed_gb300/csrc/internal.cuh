@@ -99,11 +99,10 @@ void launch_gemv(int bmode, int outmode, const GemvArgs& a, int max_work, cudaSt
 // ---- decode-shaped layer in one persistent launch (moe_decode.cu) ----
 struct DecodeArgs {
     // stored weights as TMA tiles: codes / scales of gate and up [E*F rows],
-    // boxes of 64 rows x a K chunk; down [E*d rows], boxes of 128 rows
+    // boxes of 128 rows x 256 K; down [E*d rows], boxes of 256 rows x 256 K
     CUtensorMap tm_gate_c, tm_up_c, tm_gate_s, tm_up_s, tm_down_c, tm_down_s;
     int d, F, top_k;
-    int gbu, gbd;                   // 64-feature blocks per gate/up item, 128-output blocks per down item
-    int kcu, kcd;                   // K chunk of a gate/up / down stage (set with the maps)
+    int gbu, gbd;                   // 128-feature blocks per gate/up item, 256-output blocks per down item
     int slot_bytes;                 // set by the launcher
     const int32_t* offsets;         // [E+1]
     const int32_t* active;          // [E]
@@ -122,14 +121,14 @@ struct DecodeArgs {
     uint16_t* out;                  // [T, d] bf16
     int* counters;                  // [1] work item counter (zeroed before the launch)
     int* tile_ready;                // [row tiles] gate/up items done (zeroed)
-    int* tok_done;                  // [T, d / 128] contributions per (token, output group) (zeroed)
+    int* tok_done;                  // [T, d / 256] contributions per (token, output group) (zeroed)
     int32_t* status;                // NVFP4_ERR_TIMEOUT if a bounded wait expired
 };
 // d and F multiples of 256 and the shared-memory ring fits.
 bool decode_supported(int d, int F);
 // Output groups of the finest split (sizes the tok_done counters).
 int decode_groups_d(int d);
-// Picks the K chunks and encodes the weight tensor maps.
+// Encodes the weight tensor maps.
 bool decode_set_maps(DecodeArgs* a, const nvfp4_moe_weights* w);
 void decode_pick_groups(int expected_tiles, int d, int F, int* gbu, int* gbd);
 void launch_decode(int bmode, const DecodeArgs& a, cudaStream_t s);

@@ -12,13 +12,13 @@
 // routed to its expert.  The stream is fed by TMA rather than by registers:
 //   * one CTA per SM; work items come from a device counter in order: every
 //     gate/up item (expert row tile of up to 8 routed rows x a group of
-//     64-feature blocks), then every down item (row tile x a group of
-//     128-output blocks);
-//   * a producer warp loads each stage -- 128 weight rows (64 gate + 64 up
-//     rows of one feature block, or 128 down rows) x a K chunk of the stored
+//     128-feature blocks), then every down item (row tile x a group of
+//     256-output blocks);
+//   * a producer warp loads each stage -- 256 weight rows (128 gate + 128
+//     up rows of one feature block, or 256 down rows) x 256 K of the stored
 //     codes and scales -- with tiled TMA into a ring of shared-memory slots,
 //     running ahead across items;
-//   * each of eight consumer warps owns 16 of the stage's rows (8 gate + 8
+//   * each of sixteen consumer warps owns 16 of the stage's rows (8 gate + 8
 //     up rows of the same features, so that SwiGLU stays in its registers)
 //     over every K chunk of the block: no partial sums to exchange.  It
 //     loads its codes and scales from shared memory into mma.sync m16n8k16
@@ -27,7 +27,7 @@
 //     them in registers (cvt e2m1x2 -> f16x2, times the block scale: exact)
 //     and multiplies the item's routed rows, staged once per item in shared
 //     memory as f16 (bf16 rows with a per-row power of two taken out, or
-//     NVFP4 rows dequantised exactly), on eight accumulator chains;
+//     NVFP4 rows dequantised exactly), on four accumulator chains;
 //   * gate/up writes h = bf16(silu(G) * U) (W4A4: requantised to NVFP4 under
 //     the down input scale) and, once an item is done, raises its row tile's
 //     counter;
@@ -50,16 +50,18 @@ namespace {
 
 using namespace tc;
 
-constexpr int kConsumers = 8;                    // consumer warps
+constexpr int kConsumers = 16;                   // consumer warps
 constexpr int kThreads = (kConsumers + 1) * 32;  // + one producer warp
 constexpr int kNS = 4;                           // ring slots
 constexpr int kRows = 16 * kConsumers;           // weight rows per stage
-constexpr int kFeatGU = kRows / 2;               // features per gate/up block (64 gate + 64 up rows)
+constexpr int kFeatGU = kRows / 2;               // features per gate/up block (128 gate + 128 up rows)
+constexpr int kChunk = 256;                      // K per stage (one 128-byte box row of codes)
 constexpr int kBarConsumers = 1;                 // named barrier of the consumer warps
-// Independent accumulator chains per warp: mma.sync has a long latency on
-// this part, and the stream keeps pace only with enough MMAs in flight
-// (measured: 2 chains per warp ran the layer at 40 % of HBM).
-constexpr int kChains = 8;
+// Independent accumulator chains per warp (mma.sync has a long latency on
+// this part).  Measured on GB300: with eight consumer warps the kernel was
+// bound by instruction latency (14 % warps active, 37 % issue active), so
+// sixteen warps share the stage, which caps a thread at 120 registers.
+constexpr int kChains = 4;
 
 struct Hdr {
     int kind;    // 0 gate/up, 1 down, -1 end of work
@@ -98,15 +100,25 @@ __device__ __forceinline__ uint32_t lds_scales(const uint8_t* p) {
     else return *p;
 }
 
-// Dequantised f16x2 words for k-steps jj and jj+1 (jj even) from code word
-// jj/2 of a lane: out[0] = phys 4jj..4jj+1, out[1] = 4jj+2..4jj+3, out[2],
-// out[3] the same for jj+1.  Both lie in the lane's 16-block jj/4.
-__device__ __forceinline__ void deq_word(uint32_t word, uint32_t sw, int jj, uint32_t out[4]) {
+// A lane's block scales as f16x2 pairs (the scale of block b in both
+// halves of S[b]) from the 4 bytes (CK = 256) or 1 byte (CK = 64) it loaded.
+template <int NB>
+__device__ __forceinline__ void block_scales(uint32_t sw, uint32_t (&S)[NB]) {
+    const uint32_t s01 = e4m3x2_to_f16x2(sw & 0xFFFFu);
+    S[0] = f16x2_bcast(s01, 0);
+    if constexpr (NB > 1) {
+        const uint32_t s23 = e4m3x2_to_f16x2(sw >> 16);
+        S[1] = f16x2_bcast(s01, 1);
+        S[2] = f16x2_bcast(s23, 0);
+        S[3] = f16x2_bcast(s23, 1);
+    }
+}
+
+// Dequantised f16x2 words of one code word (8 codes of one 16-block, block
+// scale S as f16x2): out[0] = phys 0..1, out[1] = 2..3, out[2] = 4..5, out[3] = 6..7.
+__device__ __forceinline__ void deq_word(uint32_t word, uint32_t S, uint32_t out[4]) {
     uint32_t f[4];
     e2m1x8_to_f16x8(word, f);
-    const int blk = jj >> 2;
-    const uint32_t s2 = e4m3x2_to_f16x2((sw >> (16 * (blk >> 1))) & 0xFFFFu);
-    const uint32_t S = f16x2_bcast(s2, blk & 1);
 #pragma unroll
     for (int i = 0; i < 4; ++i) out[i] = hmul2_u32(f[i], S);
 }
@@ -212,8 +224,10 @@ __device__ __forceinline__ void stage_mma(const uint8_t* c0, const uint8_t* c1, 
         uint32_t w0[C::CW], w1[C::CW];
         lds_codes<CK>(r0c + kb / 2, w0);
         lds_codes<CK>(r1c + kb / 2, w1);
-        const uint32_t x0s = lds_scales<CK>(r0s + kb / 16);
-        const uint32_t x1s = lds_scales<CK>(r1s + kb / 16);
+        constexpr int NB = C::TS / 16;  // 16-blocks per lane and chunk
+        uint32_t S0[NB], S1[NB];
+        block_scales<NB>(lds_scales<CK>(r0s + kb / 16), S0);
+        block_scales<NB>(lds_scales<CK>(r1s + kb / 16), S1);
         const int qb = (k0 + kb) / 8;
 #pragma unroll
         for (int jj = 0; jj < C::KS; jj += 2) {
@@ -221,8 +235,8 @@ __device__ __forceinline__ void stage_mma(const uint8_t* c0, const uint8_t* c1, 
             const uint32_t b0[2] = {bq.x, bq.y};
             const uint32_t b1[2] = {bq.z, bq.w};
             uint32_t x0[4], x1[4];
-            deq_word(w0[jj >> 1], x0s, jj, x0);
-            deq_word(w1[jj >> 1], x1s, jj, x1);
+            deq_word(w0[jj >> 1], S0[jj >> 2], x0);
+            deq_word(w1[jj >> 1], S1[jj >> 2], x1);
             const uint32_t af0[4] = {x0[0], x1[0], x0[1], x1[1]};
             const uint32_t af1[4] = {x0[2], x1[2], x0[3], x1[3]};
             mma_16816(acc[jj % kChains], af0, b0);
@@ -265,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     const int n_tiles = a.tile_start[n_active];
     const int nbu = a.F / kFeatGU, nbd = a.d / kRows;  // 64-feature / 128-output blocks
     const int ngu = nbu / a.gbu, ngd = nbd / a.gbd;    // item groups per tile
-    const int nchu = a.d / a.kcu, nchd = a.F / a.kcd;  // K chunks per block
+    const int nchu = a.d / kChunk, nchd = a.F / kChunk;  // K chunks per block
     const int nA = n_tiles * ngu, total = nA + n_tiles * ngd;
 
     if (warp == kConsumers) {
@@ -317,22 +331,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
                         h.f = blk * kFeatGU;
                         s_hdr[s] = h;
                         const int y = h.e * a.F + h.f;
-                        const uint32_t cb = kFeatGU * a.kcu / 2, sb = kFeatGU * a.kcu / 16;
+                        const uint32_t cb = kFeatGU * kChunk / 2, sb = kFeatGU * kChunk / 16;
                         mbar_arrive_expect_tx(full, 2 * (cb + sb));
-                        tma_load_2d(dst, &a.tm_gate_c, h.kc * (a.kcu / 2), y, full);
-                        tma_load_2d(dst + cb, &a.tm_up_c, h.kc * (a.kcu / 2), y, full);
-                        tma_load_2d(dst + 2 * cb, &a.tm_gate_s, h.kc * (a.kcu / 16), y, full);
-                        tma_load_2d(dst + 2 * cb + sb, &a.tm_up_s, h.kc * (a.kcu / 16), y, full);
+                        tma_load_2d(dst, &a.tm_gate_c, h.kc * (kChunk / 2), y, full);
+                        tma_load_2d(dst + cb, &a.tm_up_c, h.kc * (kChunk / 2), y, full);
+                        tma_load_2d(dst + 2 * cb, &a.tm_gate_s, h.kc * (kChunk / 16), y, full);
+                        tma_load_2d(dst + 2 * cb + sb, &a.tm_up_s, h.kc * (kChunk / 16), y, full);
                     } else {
                         const int blk = h.grp * a.gbd + j / nchd;
                         h.kc = j % nchd;
                         h.f = blk * kRows;
                         s_hdr[s] = h;
                         const int y = h.e * a.d + h.f;
-                        const uint32_t cb = kRows * a.kcd / 2, sb = kRows * a.kcd / 16;
+                        const uint32_t cb = kRows * kChunk / 2, sb = kRows * kChunk / 16;
                         mbar_arrive_expect_tx(full, cb + sb);
-                        tma_load_2d(dst, &a.tm_down_c, h.kc * (a.kcd / 2), y, full);
-                        tma_load_2d(dst + cb, &a.tm_down_s, h.kc * (a.kcd / 16), y, full);
+                        tma_load_2d(dst, &a.tm_down_c, h.kc * (kChunk / 2), y, full);
+                        tma_load_2d(dst + cb, &a.tm_down_s, h.kc * (kChunk / 16), y, full);
                     }
                 }
                 if (!ok || h.kind < 0) break;
@@ -408,16 +422,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
             const uint8_t* slot = ring + (size_t)s * a.slot_bytes;
             if (!down) {
                 // MMA rows 0-7: gate rows 8w..8w+7 of the block, rows 8-15: the up rows of the same features
-                const int cb = kFeatGU * a.kcu / 2, sb = kFeatGU * a.kcu / 16;
-                const uint8_t* gc = slot + 8 * warp * (a.kcu / 2);
-                const uint8_t* gs = slot + 2 * cb + 8 * warp * (a.kcu / 16);
-                stage_mma<CKG>(gc, gc + cb, gs, gs + sb, a.kcu, h.kc * a.kcu, Bs, a.d, lane, acc);
+                const int cb = kFeatGU * kChunk / 2, sb = kFeatGU * kChunk / 16;
+                const uint8_t* gc = slot + 8 * warp * (kChunk / 2);
+                const uint8_t* gs = slot + 2 * cb + 8 * warp * (kChunk / 16);
+                stage_mma<CKG>(gc, gc + cb, gs, gs + sb, kChunk, h.kc * kChunk, Bs, a.d, lane, acc);
             } else {
-                const int cb = kRows * a.kcd / 2;
-                const uint8_t* dc = slot + 16 * warp * (a.kcd / 2);
-                const uint8_t* ds = slot + cb + 16 * warp * (a.kcd / 16);
-                stage_mma<CKD>(dc, dc + 8 * (a.kcd / 2), ds, ds + 8 * (a.kcd / 16), a.kcd, h.kc * a.kcd, Bs, a.F,
-                               lane, acc);
+                const int cb = kRows * kChunk / 2;
+                const uint8_t* dc = slot + 16 * warp * (kChunk / 2);
+                const uint8_t* ds = slot + cb + 16 * warp * (kChunk / 16);
+                stage_mma<CKD>(dc, dc + 8 * (kChunk / 2), ds, ds + 8 * (kChunk / 16), kChunk, h.kc * kChunk, Bs,
+                               a.F, lane, acc);
             }
             // the slot is refilled by TMA (async proxy) after its release
             fence_proxy_async();
@@ -455,13 +469,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
                     if constexpr (BMODE == B_NVFP4) {
                         // an NVFP4 block of 16 features spans two warps: h goes
                         // through shared memory, then warp w requantises routed
-                        // row w of the block (lane b: features 16b .. 16b + 15)
+                        // row w % 8 of the block, blocks 4 (w / 8) .. + 3 (lane b
+                        // of those: features 16b .. 16b + 15)
 #pragma unroll
                         for (int cc = 0; cc < 2; ++cc) s_hx[(2 * c + cc) * kFeatGU + 8 * warp + g] = hv[cc];
                         consumer_sync();
-                        const int row = warp;
-                        if (row < cur.nrows && lane < kFeatGU / 16) {
-                            const int b = lane;
+                        const int row = warp % kGemvTokTile;
+                        constexpr int kBlkPerWarp = kFeatGU / 16 / (kConsumers / kGemvTokTile);
+                        if (row < cur.nrows && lane < kBlkPerWarp) {
+                            const int b = (warp / kGemvTokTile) * kBlkPerWarp + lane;
                             float v[16], m = 0.0f;
 #pragma unroll
                             for (int i = 0; i < 16; ++i) {
@@ -560,17 +576,14 @@ void launch_t(const DecodeArgs& a, size_t smem, cudaStream_t s, const char* name
 
 template <int BMODE>
 void launch_b(const DecodeArgs& a, size_t smem, cudaStream_t s, const char* name) {
-    const bool g256 = a.kcu % 256 == 0, d256 = a.kcd % 256 == 0;
-    if (g256 && d256) return launch_t<BMODE, 256, 256>(a, smem, s, name);
-    if (g256) return launch_t<BMODE, 256, 64>(a, smem, s, name);
-    if (d256) return launch_t<BMODE, 64, 256>(a, smem, s, name);
-    return launch_t<BMODE, 64, 64>(a, smem, s, name);
+    launch_t<BMODE, kChunk, kChunk>(a, smem, s, name);
 }
 
-// K chunk of a stage: 512 where K allows it, else 256.
-int k_chunk(int K) { return K % 512 == 0 ? 512 : 256; }
-
-int slot_bytes(int d, int F) { return kRows * std::max(k_chunk(d), k_chunk(F)) * 9 / 16; }
+int slot_bytes(int d, int F) {
+    (void)d;
+    (void)F;
+    return kRows * kChunk * 9 / 16;
+}
 
 size_t decode_smem(int d, int F) {
     return 128 + (size_t)kNS * slot_bytes(d, F) + (size_t)kGemvTokTile * std::max(d, F) * 2 +
@@ -591,22 +604,20 @@ int pick_blocks(int tiles, int nb, int per_sm) {
 bool decode_supported(int d, int F) {
     // the dynamic shared memory plus about 0.5 KB of static shared memory
     // within the 227 KB a CTA may opt in to
-    return d % 256 == 0 && F % 256 == 0 && d % kRows == 0 && F % kFeatGU == 0 &&
+    return d % kChunk == 0 && F % kChunk == 0 && d % kRows == 0 && F % kFeatGU == 0 &&
            decode_smem(d, F) + 1024 <= 227 * 1024;
 }
 
 int decode_groups_d(int d) { return std::max(1, d / kRows); }
 
 bool decode_set_maps(DecodeArgs* a, const nvfp4_moe_weights* w) {
-    a->kcu = k_chunk(a->d);
-    a->kcd = k_chunk(a->F);
     const unsigned long long E = (unsigned long long)w->E, d = a->d, F = a->F;
-    return encode_tmap_u8(&a->tm_gate_c, w->gate.codes, d / 2, E * F, a->kcu / 2, kFeatGU, false) &&
-           encode_tmap_u8(&a->tm_up_c, w->up.codes, d / 2, E * F, a->kcu / 2, kFeatGU, false) &&
-           encode_tmap_u8(&a->tm_gate_s, w->gate.scales, d / 16, E * F, a->kcu / 16, kFeatGU, false) &&
-           encode_tmap_u8(&a->tm_up_s, w->up.scales, d / 16, E * F, a->kcu / 16, kFeatGU, false) &&
-           encode_tmap_u8(&a->tm_down_c, w->down.codes, F / 2, E * d, a->kcd / 2, kRows, false) &&
-           encode_tmap_u8(&a->tm_down_s, w->down.scales, F / 16, E * d, a->kcd / 16, kRows, false);
+    return encode_tmap_u8(&a->tm_gate_c, w->gate.codes, d / 2, E * F, kChunk / 2, kFeatGU, false) &&
+           encode_tmap_u8(&a->tm_up_c, w->up.codes, d / 2, E * F, kChunk / 2, kFeatGU, false) &&
+           encode_tmap_u8(&a->tm_gate_s, w->gate.scales, d / 16, E * F, kChunk / 16, kFeatGU, false) &&
+           encode_tmap_u8(&a->tm_up_s, w->up.scales, d / 16, E * F, kChunk / 16, kFeatGU, false) &&
+           encode_tmap_u8(&a->tm_down_c, w->down.codes, F / 2, E * d, kChunk / 2, kRows, false) &&
+           encode_tmap_u8(&a->tm_down_s, w->down.scales, F / 16, E * d, kChunk / 16, kRows, false);
 }
 
 void decode_pick_groups(int expected_tiles, int d, int F, int* gbu, int* gbd) {
