@@ -709,6 +709,7 @@ def run_ours(args):
     barrier()
     import serving_nvfp4_routed_gb300 as lib
 
+    lib.set_kernel_choice({"auto": "auto", "split": "gemv_split", "fused": "gemv_fused"}[args.decode_form])
     hbm, bf16, peak_kind = peaks()
     flush_mb = 256
     flush = torch.empty(flush_mb << 20, dtype=torch.uint8, device=dev)
@@ -722,7 +723,7 @@ def run_ours(args):
         "ms_per_step": m["ms_per_step"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": dtype_of(layer, m["kernels"]),
         "data": "synthetic (seeded N(0,1) x and logits, N(0,0.02) bf16 weights quantised by the library)",
-        "config": workload_config(layer, flush_mb),
+        "config": dict(workload_config(layer, flush_mb), decode_form=args.decode_form),
         "roofline": m["roofline"],
         "kernels": m["kernels"],
         "e2e": m["e2e"],
@@ -761,6 +762,7 @@ def run_ours(args):
     if args.workloads and args.workload == "decode64":
         # the prompt-shaped half of the metric: the other configurations,
         # each measured the same way (fewer steps: each step is milliseconds)
+        lib.set_kernel_choice("auto")
         wl = {}
         for name in PROMPT_WORKLOADS:
             lay = (DenseLayer if name == "dense" else Layer)(name, lib, dev, seed + 7)
@@ -853,6 +855,8 @@ def main(argv=None):
                     help="time the layer steps only (no kernel split, host-buffer run or side timings): for "
                          "profiler captures, whose launch list then holds the warm-up, the touched-expert count "
                          "(one step per input batch) and the timed steps")
+    ap.add_argument("--decode-form", choices=("auto", "split", "fused"), default="auto",
+                    help="decode-shaped layer as the library picks it, as two launches, or as one")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=8)
     ap.add_argument("--ref-tokens", type=int, default=4)

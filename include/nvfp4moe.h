@@ -285,10 +285,15 @@ nvfp4_status moe_combine_rows(const uint16_t* y_bf16, const int32_t* slot_to_row
  *       the experts average 32 or more routed rows, else the decode-shaped
  *       streaming kernels);
  *   1 = the decode-shaped kernels for every shape;
- *   2 = the prompt-shaped kernels wherever the shapes allow them.
- * For tests and measurements that cover both kernels at one size.  Takes
- * effect for calls made after it returns; returns NVFP4_ERR_INVALID_ARG
- * for any other value.
+ *   2 = the prompt-shaped kernels wherever the shapes allow them;
+ *   3 = as 1, with the decode-shaped layer as two launches (gate/up, then
+ *       down + combine);
+ *   4 = as 1, with the decode-shaped layer as one persistent launch where
+ *       its shape allows it (d and F multiples of 256).
+ * Choices 0 and 1 take whichever decode-shaped form is faster for the
+ * shape.  For tests and measurements that cover every kernel at one size.
+ * Takes effect for calls made after it returns; returns
+ * NVFP4_ERR_INVALID_ARG for any other value.
  * --------------------------------------------------------------------- */
 nvfp4_status nvfp4_set_kernel_choice(int choice);
 

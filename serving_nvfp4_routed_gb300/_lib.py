@@ -335,13 +335,16 @@ def moe_workspace_intermediates(ws: torch.Tensor, T, E, top_k, d, F, mode) -> di
                 hq=view(ptrs[3], (R, F // 2), torch.uint8), hs=view(ptrs[4], (R, F // 16), torch.uint8))
 
 
-KERNEL_CHOICE = {"auto": 0, "gemv": 1, "tc": 2}
+KERNEL_CHOICE = {"auto": 0, "gemv": 1, "tc": 2, "gemv_split": 3, "gemv_fused": 4}
 
 
 def set_kernel_choice(choice: str = "auto") -> None:
     """Which kernels later layer / linear calls run: "auto" (by shape),
-    "gemv" (decode-shaped) or "tc" (prompt-shaped tensor-core kernels where
-    the shapes allow them).  Process-wide; for tests and measurements."""
+    "gemv" (decode-shaped), "tc" (prompt-shaped tensor-core kernels where
+    the shapes allow them), or one form of the decode-shaped layer:
+    "gemv_split" (gate/up and down as two launches) or "gemv_fused" (one
+    persistent launch, d and F multiples of 256).  Process-wide; for tests
+    and measurements."""
     _check("nvfp4_set_kernel_choice", load().nvfp4_set_kernel_choice(KERNEL_CHOICE[choice]))
 
 

@@ -115,7 +115,7 @@ extern "C" const char* nvfp4_status_string(nvfp4_status s) {
 }
 
 extern "C" nvfp4_status nvfp4_set_kernel_choice(int choice) {
-    if (choice < 0 || choice > 2) return NVFP4_ERR_INVALID_ARG;
+    if (choice < 0 || choice > 4) return NVFP4_ERR_INVALID_ARG;
     g_kernel_choice.store(choice, std::memory_order_relaxed);
     return NVFP4_OK;
 }

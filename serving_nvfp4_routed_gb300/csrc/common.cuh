@@ -20,7 +20,8 @@ void launch_begin(const char* name, cudaStream_t s);
 void launch_end(const char* name, cudaStream_t s);
 int num_sms();
 int device_cc_major();
-// nvfp4_set_kernel_choice: 0 by shape, 1 decode-shaped, 2 prompt-shaped.
+// nvfp4_set_kernel_choice: 0 by shape, 1 decode-shaped, 2 prompt-shaped,
+// 3 decode-shaped as two launches, 4 decode-shaped as one persistent launch.
 int kernel_choice();
 
 #define NVFP4_LAUNCH(name, stream, ...)            \

@@ -78,20 +78,21 @@ struct GemvArgs {
     uint8_t* hq_out;                // OUT_HQ: [R, N/2]
     uint8_t* hs_out;                // OUT_HQ: [R, N/16]
     const float* hq_gs;             // OUT_HQ: [E] next input scale
-    float* acc_out;                 // OUT_COMBINE: [T, N] fp32 (zeroed by the gate/up launch)
+    float* y_rows;                  // OUT_COMBINE: [R, N] w * y per routed row (fp32)
+    const int32_t* slot_to_row;     // OUT_COMBINE: [R]
     const float* topk_w;            // OUT_COMBINE: [T*k]
-    int* tok_done;                  // OUT_COMBINE: [T] completed contributions (zeroed before)
-    int done_target;                // OUT_COMBINE: contributions per token
+    int* tok_done;                  // OUT_COMBINE: [T, item groups] completed slots (zeroed before)
     uint16_t* out_bf16;             // OUT_COMBINE: [T, N] final bf16 rows
     uint16_t* y_out;                // OUT_BF16: [R, N]
-    float* zero_buf;                // zeroed (grid-stride) at kernel start, may be null
-    size_t zero_words;
     int* work_counter;              // zeroed before the launch
 };
 
 // ksplit chosen from the expected number of work items
 int gemv_pick_ksplit(int expected_tiles, int N, int nproj);
 int gemv_pick_group(int expected_tiles, int N, int ksplit, int nproj);
+// Work-item groups along N of a launch with these picks (one completion
+// counter per token and group in OUT_COMBINE).
+int gemv_item_groups(int N, int ksplit, int fb_group);
 size_t gemv_smem_bytes(int K);
 bool gemv_supported_k(int K);
 void launch_gemv(int bmode, int outmode, const GemvArgs& a, int max_work, cudaStream_t s);

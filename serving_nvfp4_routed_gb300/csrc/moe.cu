@@ -10,11 +10,12 @@
 //   [W4A4: static-scale act-quant of the permuted rows]
 //   gate/up + SwiGLU (h per routed row; W4A4: h requantised to NVFP4)
 //   down + weighted top-k combine:
-//     decode-shaped kernels: fp32 red.add into a [T, d] accumulator, and the
-//       CTA that adds a token's last contribution writes its bf16 row;
+//     decode-shaped kernels: w * y per routed row in fp32; the CTA that
+//       completes a token's last slot in a group of outputs sums the
+//       token's k rows there in slot order and writes them as bf16;
 //     prompt-shaped kernels: y written per routed row in bf16, then each
-//       token's k rows weighted and summed in slot order (deterministic,
-//       chunk-invariant).
+//       token's k rows weighted and summed in slot order.
+//   Both are deterministic (the same bits on every run).
 #include <climits>
 #include <cstring>
 
@@ -36,10 +37,10 @@ struct MoeWs {
     uint8_t* hs;      // [R, F/16]  W4A4
     float* acc;       // [T, d]
     float* yrows;     // [R, d]: w * y fp32 rows (decode kernel) or bf16 y rows (prompt paths)
-    int* clear;       // zeroed by the route launch: work counters, per-token completion counts,
-                      // then (decode kernel) per-tile and per-(token, output group) counters
+    int* clear;       // zeroed by the route launch (decode-shaped paths): work counters, then
+                      // per-tile and per-(token, output group) completion counters
     int* tile_ready;  // [max tiles]
-    int* tok_done;    // [T, d / 128]
+    int* tok_done;    // [T, d / 16]
     // prompt-shaped (tensor-core) path, W4A16
     uint16_t* xp;     // [R, d]  f16 x * 2^-s, rows in expert order
     int32_t* xp_exp;  // [R]
@@ -52,7 +53,16 @@ bool tc_possible(int mode, int d, int F) { return mode == 0 && d % 128 == 0 && F
 // nvfp4_set_kernel_choice: -1 by shape, 0 decode-shaped, 1 prompt-shaped.
 int forced_path() {
     const int c = kernel_choice();
-    return c == 0 ? -1 : c - 1;
+    return c == 0 ? -1 : (c == 2 ? 1 : 0);
+}
+
+// Decode-shaped layers: the persistent one-launch kernel or the two GEMV launches.
+bool use_fused_decode(int d, int F) {
+    if (!decode_supported(d, F)) return false;
+    const int c = kernel_choice();
+    if (c == 3) return false;
+    if (c == 4) return true;
+    return false;
 }
 
 // Tensor cores once the experts average 32 or more routed rows.
@@ -88,11 +98,11 @@ MoeWs carve_moe(void* base, int T, int E, int k, int d, int F, int mode, size_t*
     w.ra.tile_start_tc = c.take<int32_t>(E + 1);
     w.ra.counts = c.take<int32_t>(route_scratch_words(T, E, k) + 1);
     const size_t max_tiles = R / kGemvTokTile + std::min<size_t>(E, R) + 1;
-    const size_t n_clear = kCounters + (size_t)T + max_tiles + (size_t)T * decode_groups_d(d);
+    const size_t n_clear = kCounters + max_tiles + (size_t)T * std::max(decode_groups_d(d), d / 16);
     w.clear = c.take<int>(n_clear);
     w.ra.clear = w.clear;
     w.ra.n_clear = (int)n_clear;
-    w.tile_ready = w.clear + kCounters + T;
+    w.tile_ready = w.clear + kCounters;
     w.tok_done = w.tile_ready + max_tiles;
     w.acc = c.take<float>((size_t)T * d);
     w.yrows = c.take<float>(R * d);
@@ -168,12 +178,23 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
     if (d_status && !aligned16(d_status)) return NVFP4_ERR_ALIGN;
     const int E = w->E, d = w->d, F = w->F, R = T * top_k;
     MoeWs ws = carve_moe(wsp, T, E, top_k, d, F, mode, nullptr);
+    const bool prompt = mode == 1 ? use_tc_w4a4(T, E, top_k, d, F) : use_tc(mode, T, E, top_k, d, F);
+    const bool fused = !prompt && use_fused_decode(d, F);
+    const int tiles = expected_tiles(R, E);
+    // the decode-shaped down launch: K split and feature blocks per item
+    const int ks_d = gemv_pick_ksplit(tiles, d, 1);
+    const int grp_d = gemv_pick_group(tiles, d, ks_d, 1);
+    {   // counters the chosen path uses (the prompt-shaped kernels use none)
+        const size_t max_tiles = (size_t)R / kGemvTokTile + std::min(E, R) + 1;
+        const int groups = fused ? decode_groups_d(d) : gemv_item_groups(d, ks_d, grp_d);
+        ws.ra.n_clear = prompt ? 0 : (int)(kCounters + max_tiles + (size_t)T * groups);
+    }
 
     launch_route(logits, T, E, top_k, ws.ra, d_status, s);
     if (mode == 1)
         launch_quantize_act(x, R, d, ws.ra.row_to_slot, top_k, is13, ws.ra.offsets, E, ws.xq, ws.xs, s);
 
-    if (mode == 1 && use_tc_w4a4(T, E, top_k, d, F)) {
+    if (mode == 1 && prompt) {
         const int max_tiles = R / kTcTokTile + std::min(E, R) + 1;
         // gate/up + SwiGLU, h requantised under the down projection's input scale
         TcmArgs g{};
@@ -211,7 +232,7 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
         return last_launch_status();
     }
 
-    if (use_tc(mode, T, E, top_k, d, F)) {
+    if (prompt) {
         // the down projection writes w * y rows (summed per token in slot order
         // afterwards) when the prompt-shaped kernel takes its shape (K = F a
         // multiple of 256), else the weights-as-M kernel adds into a zeroed
@@ -299,8 +320,7 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
         return last_launch_status();
     }
 
-    const int tiles = expected_tiles(R, E);
-    if (decode_supported(d, F)) {
+    if (fused) {
         // one persistent launch: gate/up + SwiGLU, then down + the slot-ordered combine
         DecodeArgs da{};
         da.d = d;
@@ -345,8 +365,6 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
     a.a_codes[0] = w->gate.codes;  a.a_scales[0] = w->gate.scales;  a.a_ws2[0] = w->gate.weight_scale_2;
     a.a_codes[1] = w->up.codes;    a.a_scales[1] = w->up.scales;    a.a_ws2[1] = w->up.weight_scale_2;
     a.work_counter = ws.clear + 0;
-    a.zero_buf = ws.acc;
-    a.zero_words = (size_t)T * d;
     if (mode == 0) {
         a.b_bf16 = x;
         a.b_by_token = 1;
@@ -366,17 +384,14 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
     b.K = F;
     b.N = d;
     b.nproj = 1;
-    b.ksplit = gemv_pick_ksplit(tiles, d, 1);
-    b.fb_group = gemv_pick_group(tiles, d, b.ksplit, 1);
+    b.ksplit = ks_d;
+    b.fb_group = grp_d;
     b.a_codes[0] = w->down.codes;  b.a_scales[0] = w->down.scales;  b.a_ws2[0] = w->down.weight_scale_2;
     b.a_codes[1] = w->down.codes;  b.a_scales[1] = w->down.scales;  b.a_ws2[1] = w->down.weight_scale_2;
     b.work_counter = ws.clear + 1;
-    b.acc_out = ws.acc;
-    b.tok_done = ws.clear + kCounters;
-    {   // contributions per token: one per (slot, work item) over the d features
-        const int n_fb = d / (16 * (8 / b.ksplit));
-        b.done_target = top_k * ((n_fb + b.fb_group - 1) / b.fb_group);
-    }
+    b.y_rows = ws.yrows;
+    b.slot_to_row = ws.ra.slot_to_row;
+    b.tok_done = ws.tok_done;
     b.out_bf16 = out;
     if (mode == 0) {
         b.b_bf16 = ws.h;

@@ -28,10 +28,10 @@
 //     2^-39 * row max; 2^s is applied to the fp32 accumulator;
 //   * W4A4 activations are NVFP4 rows, dequantised to f16 like the weights
 //     (exact), and the static input_scale multiplies the accumulator;
-//   * epilogues: SwiGLU to bf16 h (with a running per-row max |h| for the
-//     down projection's row scale), SwiGLU + NVFP4 requantisation of h with
-//     the down input_scale (W4A4), or the weighted top-k combine into an fp32
-//     accumulator with red.add (down projection).
+//   * epilogues: SwiGLU to bf16 h, SwiGLU + NVFP4 requantisation of h with
+//     the down input_scale (W4A4), or (down projection) w * y per routed row
+//     in fp32; the CTA that completes a token's last slot in a group of
+//     outputs sums the token's k rows there in slot order (deterministic).
 #include <type_traits>
 
 #include "common.cuh"
@@ -99,7 +99,6 @@ __device__ __forceinline__ int bsw(int q, int g) {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-
 struct Item {
     int e, row0, nrows, fb, fb_end;  // feature blocks [fb, fb_end) share the staged rows
 };
@@ -125,12 +124,6 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
     const int g = lane >> 2, c = lane & 3;
     const int KSPL = a.ksplit, WF = kWarps / KSPL;
     const int wf = warp / KSPL, ks = warp % KSPL;
-
-    if (a.zero_buf) {
-        float4* z = reinterpret_cast<float4*>(a.zero_buf);
-        for (size_t i = blockIdx.x * (size_t)kThreads + tid; i < a.zero_words / 4; i += (size_t)gridDim.x * kThreads)
-            z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
 
     const int n_active = *a.n_active;
     const int total_tiles = a.tile_start[n_active];
@@ -398,14 +391,12 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
                         }
                     } else if constexpr (OUTMODE == OUT_COMBINE) {
                         if (valid) {
-                            const int slot = a.row_to_slot[r];
-                            const int t = slot / a.top_k;
-                            const float wt = a.topk_w[slot];
+                            const float wt = a.topk_w[a.row_to_slot[r]];
                             const float ws = a.a_ws2[0][e];
 #pragma unroll
                             for (int hf = 0; hf < 2; ++hf) {
                                 const float y = __fmul_rn(__fmul_rn(acc[0][2 * hf + cc], rs), ws);
-                                atomicAdd(a.acc_out + (size_t)t * a.N + n0 + g + 8 * hf, wt * y);
+                                a.y_rows[(size_t)r * a.N + n0 + g + 8 * hf] = wt * y;
                             }
                         }
                     } else {  // OUT_BF16
@@ -423,27 +414,38 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
 
             if (last) {
                 if constexpr (OUTMODE == OUT_COMBINE) {
-                    // the CTA that adds the last contribution to a token turns its
-                    // fp32 row into the bf16 output row
+                    // every slot of a token meets every item group once: the CTA
+                    // that completes a token's k-th slot in this group sums the
+                    // token's k rows over the group's outputs in slot order
+                    // (the same bits on every run) and writes them as bf16
                     __threadfence();
                     __syncthreads();
+                    const int grp = cur.fb / G;
                     if (tid < kGemvTokTile) {
                         int t = -1;
                         if (tid < nrows) {
                             const int tt = a.row_to_slot[row0 + tid] / a.top_k;
-                            if (atomicAdd(a.tok_done + tt, 1) == a.done_target - 1) t = tt;
+                            if (atomicAdd(a.tok_done + (size_t)tt * n_grp + grp, 1) == a.top_k - 1) t = tt;
                         }
                         s_fin[tid] = t;
                     }
                     __syncthreads();
+                    const int q0 = grp * G * FB / 4, q1 = min(n_fb, (grp + 1) * G) * FB / 4;
                     for (int i = 0; i < nrows; ++i) {
                         const int t = s_fin[i];
                         if (t < 0) continue;
                         __threadfence();
-                        const float4* src = reinterpret_cast<const float4*>(a.acc_out + (size_t)t * a.N);
                         uint2* dst = reinterpret_cast<uint2*>(a.out_bf16 + (size_t)t * a.N);
-                        for (int jx = tid; jx < a.N / 4; jx += kThreads) {
-                            const float4 v = __ldcg(src + jx);
+                        for (int jx = q0 + tid; jx < q1; jx += kThreads) {
+                            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                            for (int j = 0; j < a.top_k; ++j) {
+                                const float4 y = __ldcg(reinterpret_cast<const float4*>(
+                                    a.y_rows + (size_t)a.slot_to_row[t * a.top_k + j] * a.N) + jx);
+                                v.x += y.x;
+                                v.y += y.y;
+                                v.z += y.z;
+                                v.w += y.w;
+                            }
                             uint2 o;
                             o.x = (uint32_t)f32_to_bf16_bits(v.x) | ((uint32_t)f32_to_bf16_bits(v.y) << 16);
                             o.y = (uint32_t)f32_to_bf16_bits(v.z) | ((uint32_t)f32_to_bf16_bits(v.w) << 16);
@@ -509,6 +511,11 @@ int gemv_pick_group(int expected_tiles, int N, int ksplit, int nproj) {
     for (int c = 2; c <= 8; c *= 2)
         if ((long long)expected_tiles * ((n_fb + c - 1) / c) >= want) g = c;
     return g;
+}
+
+int gemv_item_groups(int N, int ksplit, int fb_group) {
+    const int n_fb = N / (16 * (kWarps / ksplit));
+    return (n_fb + fb_group - 1) / fb_group;
 }
 
 int gemv_pick_ksplit(int expected_tiles, int N, int nproj) {

@@ -92,7 +92,7 @@ def test_other_host_validation(L):
     assert L.nvfp4_quantize_weights(p, 65536, 4, 32, p, p, p, p, big, None) == 2  # one grid row per tensor
     assert L.nvfp4_quantize_weights_noalloc(p, 4097, 4, 32, p, p, p, None) == 2  # beyond the fixed scratch
     assert L.nvfp4_quantize_weights_noalloc(p, 1, 4, 24, p, p, p, None) == 2
-    assert L.nvfp4_set_kernel_choice(3) == 1 and L.nvfp4_set_kernel_choice(-1) == 1
+    assert L.nvfp4_set_kernel_choice(5) == 1 and L.nvfp4_set_kernel_choice(-1) == 1
     assert L.nvfp4_set_kernel_choice(2) == 0 and L.nvfp4_set_kernel_choice(0) == 0
     assert L.nvfp4_quantize_act(p, 4, 40, None, 1, p, None, 0, p, p, None) == 2
     assert L.nvfp4_quantize_act(p, 4, 32, p, 0, p, None, 0, p, p, None) == 1

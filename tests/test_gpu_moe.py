@@ -27,7 +27,7 @@ def tc_possible(mode, d, F):
 
 
 def expected_family(path, mode, T, E, k, d, F):
-    if not tc_possible(mode, d, F) or path == "gemv":
+    if not tc_possible(mode, d, F) or path.startswith("gemv"):
         return "gemv"
     if path == "tc":
         return "tc"
@@ -42,6 +42,17 @@ def bf16_rows(fam, mode, d, F):
     return fam == "tc" and (mode == "w4a4" or (d % 256 == 0 and F % 256 == 0))
 
 
+def assert_decode_form(names, path, d, F, what=""):
+    """A forced decode-shaped form ran: one persistent launch where d and F
+    are multiples of 256, else (and when the two launches are forced) the
+    gate/up and down GEMV launches."""
+    fused = [n for n in names if "gateup_down" in n]
+    if path == "gemv_split" or (path == "gemv_fused" and (d % 256 or F % 256)):
+        assert not fused, f"{what}: expected the two-launch form, launched {sorted(names)}"
+    elif path == "gemv_fused":
+        assert fused, f"{what}: expected the one-launch form, launched {sorted(names)}"
+
+
 def assert_family(names, fam, what=""):
     pre = ("gemv_",) if fam == "gemv" else ("tc_", "tcm_", "tcq_")
     gate = [n for n in names if n.startswith(pre) and "gateup" in n]
@@ -51,11 +62,12 @@ def assert_family(names, fam, what=""):
     assert not [n for n in names if n.startswith(other)], f"{what}: unexpected kernels {sorted(names)}"
 
 
-@pytest.fixture(params=["auto", "gemv", "tc"])
+@pytest.fixture(params=["auto", "gemv_split", "gemv_fused", "tc"])
 def path(request):
     """Run the test with the library's own choice of kernel and with each
     kernel forced (the tensor-core path needs d and F multiples of 128;
-    W4A4 on the tensor cores multiples of 256)."""
+    W4A4 on the tensor cores multiples of 256; the one-launch decode form
+    d and F multiples of 256)."""
     lib.set_kernel_choice(request.param)
     yield request.param
     lib.set_kernel_choice("auto")
@@ -104,6 +116,7 @@ def test_tiny(orc, path, mode):
     out, ws, names = _run(mode, inp["x"], inp["logits"], s.k, gw, is13, is2)
     fam = expected_family(path, mode, s.T, s.E, s.k, s.d, s.F)
     assert_family(names, fam, f"tiny {mode} {path}")
+    assert_decode_form(names, path, s.d, s.F, f"tiny {mode} {path}")
     check_layer(orc, mode, inp["x"], inp["logits"], s.k, ob, out, ws, np.arange(s.T, dtype=np.int32), is13, is2,
                 f"tiny {mode} {path}", round_y=bf16_rows(fam, mode, s.d, s.F))
 
@@ -118,12 +131,14 @@ def test_ragged_shapes_both_modes(orc, T, E, k, d, F, path):
     out, ws, names = _run("w4a16", inp["x"], inp["logits"], k, gw)
     fam = expected_family(path, "w4a16", T, E, k, d, F)
     assert_family(names, fam, "w4a16")
+    assert_decode_form(names, path, d, F, "w4a16")
     check_layer(orc, "w4a16", inp["x"], inp["logits"], k, ob, out, ws, tok, what=f"w4a16 {path}",
                 round_y=bf16_rows(fam, "w4a16", d, F))
     is13, is2 = calib.calibrate(xb, inp["logits"].cpu().numpy(), k, ob)
     out4, ws4, names4 = _run("w4a4", inp["x"], inp["logits"], k, gw, is13, is2)
     fam4 = expected_family(path, "w4a4", T, E, k, d, F)
     assert_family(names4, fam4, "w4a4")
+    assert_decode_form(names4, path, d, F, "w4a4")
     check_layer(orc, "w4a4", inp["x"], inp["logits"], k, ob, out4, ws4, tok, is13, is2, f"w4a4 {path}",
                 round_y=bf16_rows(fam4, "w4a4", d, F))
 
@@ -152,7 +167,7 @@ def full_calibration(orc, full):
     return _calibrate(orc, FULL, ob, 7001)
 
 
-def _full_case(orc, full, mode, T, kind, outlier, seed, scales=None, n_tok=32, fam="tc"):
+def _full_case(orc, full, mode, T, kind, outlier, seed, scales=None, n_tok=32, fam="tc", form=None):
     banks, gw, bank = full
     s = FULL
     x = synth.make_x(T, s.d, seed, "cuda", outlier_frac=outlier)
@@ -165,19 +180,48 @@ def _full_case(orc, full, mode, T, kind, outlier, seed, scales=None, n_tok=32, f
     is13, is2 = scales if scales is not None else (None, None)
     out, ws, names = _run(mode, x, logits, s.k, gw, is13, is2)
     assert_family(names, fam, f"{mode} T={T} {kind}")
+    if form:
+        assert_decode_form(names, form, s.d, s.F, f"{mode} T={T} {kind}")
     return check_layer(orc, mode, x, logits, s.k, ob, out, ws, tok, is13, is2, f"{mode} T={T} {kind}",
                        round_y=bf16_rows(fam, mode, s.d, s.F))
 
 
+@pytest.fixture(params=["gemv_split", "gemv_fused"])
+def decode_form(request):
+    lib.set_kernel_choice(request.param)
+    yield request.param
+    lib.set_kernel_choice("auto")
+
+
 @pytest.mark.parametrize("T", synth.DECODE_T)
-def test_decode_w4a16_every_token(orc, full, T):
-    """Decode-shaped layer at full size; every token against the oracle."""
-    _full_case(orc, full, "w4a16", T, "normal", 0.0, 1011 + T, n_tok=64, fam="gemv")
+def test_decode_w4a16_every_token(orc, full, T, decode_form):
+    """Decode-shaped layer at full size, in each of its two forms; every
+    token against the oracle."""
+    _full_case(orc, full, "w4a16", T, "normal", 0.0, 1011 + T, n_tok=64, fam="gemv", form=decode_form)
 
 
 @pytest.mark.parametrize("T", [8, 32])
-def test_decode_w4a4_calibrated(orc, full, full_calibration, T):
-    _full_case(orc, full, "w4a4", T, "normal", 0.05, 2001 + T, full_calibration, n_tok=64, fam="gemv")
+def test_decode_w4a4_calibrated(orc, full, full_calibration, T, decode_form):
+    _full_case(orc, full, "w4a4", T, "normal", 0.05, 2001 + T, full_calibration, n_tok=64, fam="gemv",
+               form=decode_form)
+
+
+@pytest.mark.parametrize("mode", ["w4a16", "w4a4"])
+def test_decode_deterministic(full, decode_form, mode):
+    """The decode-shaped combine sums each token's rows in slot order: two
+    calls on the same inputs give the same bits."""
+    banks, gw, bank = full
+    s = FULL
+    x = synth.make_x(64, s.d, 3301, "cuda")
+    lg = synth.make_logits(64, s.E, 3302, "cuda")
+    if mode == "w4a16":
+        run = lambda: lib.nvfp4_moe_w4a16(x, lg, s.k, gw)
+    else:
+        sc = torch.full((s.E,), 0.01, dtype=torch.float32, device="cuda")
+        run = lambda: lib.nvfp4_moe_w4a4(x, lg, s.k, gw, sc, sc)
+    a = run()
+    b = run()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
 @pytest.mark.parametrize("T", [1, 64])
