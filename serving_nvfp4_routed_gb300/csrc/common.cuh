@@ -166,8 +166,7 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
 
 // Broadcast the f16 in the low (hi=0) or high (hi=1) half to both halves.
 __device__ __forceinline__ uint32_t f16x2_bcast(uint32_t v, int hi) {
-    uint32_t h = hi ? (v >> 16) : (v & 0xFFFFu);
-    return h | (h << 16);
+    return __byte_perm(v, 0u, hi ? 0x3232u : 0x1010u);  // one byte permute
 }
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b16) { return __uint_as_float(b16 << 16); }

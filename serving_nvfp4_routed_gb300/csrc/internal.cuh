@@ -104,6 +104,7 @@ struct DecodeArgs {
     CUtensorMap tm_gate_c, tm_up_c, tm_gate_s, tm_up_s, tm_down_c, tm_down_s;
     int d, F, top_k;
     int gbu, gbd;                   // 128-feature blocks per gate/up item, 256-output blocks per down item
+    int chu, chd;                   // consecutive gate/up / down items a CTA takes per grab
     int slot_bytes;                 // set by the launcher
     const int32_t* offsets;         // [E+1]
     const int32_t* active;          // [E]
@@ -120,7 +121,7 @@ struct DecodeArgs {
     uint8_t *hq, *hs;               // B_NVFP4: h requantised [R, F/2], [R, F/16]
     float* yrows;                   // [R, d] w * y per routed row
     uint16_t* out;                  // [T, d] bf16
-    int* counters;                  // [1] work item counter (zeroed before the launch)
+    int* counters;                  // [2] gate/up and down item counters (zeroed before the launch)
     int* tile_ready;                // [row tiles] gate/up items done (zeroed)
     int* tok_done;                  // [T, d / 256] contributions per (token, output group) (zeroed)
     int32_t* status;                // NVFP4_ERR_TIMEOUT if a bounded wait expired
@@ -131,7 +132,9 @@ bool decode_supported(int d, int F);
 int decode_groups_d(int d);
 // Encodes the weight tensor maps.
 bool decode_set_maps(DecodeArgs* a, const nvfp4_moe_weights* w);
-void decode_pick_groups(int expected_tiles, int d, int F, int* gbu, int* gbd);
+// Item sizes and grab lengths for about `expected_tiles` row tiles (sets
+// gbu, gbd, chu, chd; d and F already set).
+void decode_pick_work(int expected_tiles, DecodeArgs* a);
 void launch_decode(int bmode, const DecodeArgs& a, cudaStream_t s);
 
 // ---- prompt-shaped grouped GEMM (tcgen05, accumulators in TMEM) ----

@@ -326,7 +326,7 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
         da.d = d;
         da.F = F;
         da.top_k = top_k;
-        decode_pick_groups(tiles, d, F, &da.gbu, &da.gbd);
+        decode_pick_work(tiles, &da);
         if (!decode_set_maps(&da, w)) return NVFP4_ERR_CUDA;
         da.offsets = ws.ra.offsets;
         da.active = ws.ra.active;

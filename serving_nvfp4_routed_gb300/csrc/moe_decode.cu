@@ -10,27 +10,29 @@
 // With a few tokens per expert the layer is a stream of 4.5-bit weights
 // (codes + e4m3 scales) from HBM, each read once for the handful of rows
 // routed to its expert.  The stream is fed by TMA rather than by registers:
-//   * one CTA per SM; work items come from a device counter in order: every
-//     gate/up item (expert row tile of up to 8 routed rows x a group of
-//     128-feature blocks), then every down item (row tile x a group of
-//     256-output blocks);
+//   * one CTA per SM; work items come from two device counters in runs of
+//     consecutive items: every gate/up item (expert row tile of up to 8
+//     routed rows x a group of 128-feature blocks), then every down item
+//     (row tile x a group of 256-output blocks); a CTA stages a row tile's
+//     rows once for the consecutive items it takes on that tile;
 //   * a producer warp loads each stage -- 256 weight rows (128 gate + 128
 //     up rows of one feature block, or 256 down rows) x 256 K of the stored
-//     codes and scales -- with tiled TMA into a ring of shared-memory slots,
-//     running ahead across items;
-//   * each of sixteen consumer warps owns 16 of the stage's rows (8 gate + 8
-//     up rows of the same features, so that SwiGLU stays in its registers)
-//     over every K chunk of the block: no partial sums to exchange.  It
-//     loads its codes and scales from shared memory into mma.sync m16n8k16
-//     A fragments (K permuted inside each 256-wide chunk so that every lane's
-//     codes are contiguous; the B rows use the same permutation), dequantises
-//     them in registers (cvt e2m1x2 -> f16x2, times the block scale: exact)
-//     and multiplies the item's routed rows, staged once per item in shared
-//     memory as f16 (bf16 rows with a per-row power of two taken out, or
-//     NVFP4 rows dequantised exactly), on four accumulator chains;
+//     codes and scales -- with tiled TMA into a ring of shared-memory slots
+//     (codes with the 128-byte swizzle), running ahead across items;
+//   * each of eight consumer warps owns 32 of the stage's rows as two m16
+//     tiles (gate/up: 8 gate + 8 up rows of the same features per tile, so
+//     that SwiGLU stays in its registers) over every K chunk of the block:
+//     no partial sums to exchange.  It loads its codes and scales from
+//     shared memory into mma.sync m16n8k16 A fragments (K permuted inside
+//     each 256-wide chunk so that every lane's codes are contiguous; the B
+//     rows use the same permutation), dequantises them in registers (cvt
+//     e2m1x2 -> f16x2, times the block scale: exact) and multiplies the row
+//     tile's routed rows, staged in shared memory as f16 (bf16 rows with a
+//     per-row power of two taken out, or NVFP4 rows dequantised exactly);
+//     each B fragment serves both tiles;
 //   * gate/up writes h = bf16(silu(G) * U) (W4A4: requantised to NVFP4 under
-//     the down input scale) and, once an item is done, raises its row tile's
-//     counter;
+//     the down input scale: a warp's 16 features are one NVFP4 block) and,
+//     once an item is done, raises its row tile's counter;
 //   * a down item waits (bounded) for its tile's counter before it stages h,
 //     while its weights are already streaming; it writes w * y per routed
 //     row (fp32) and counts each (token, output group); the CTA that adds a
@@ -50,18 +52,19 @@ namespace {
 
 using namespace tc;
 
-constexpr int kConsumers = 16;                   // consumer warps
+constexpr int kConsumers = 8;                    // consumer warps
 constexpr int kThreads = (kConsumers + 1) * 32;  // + one producer warp
 constexpr int kNS = 4;                           // ring slots
-constexpr int kRows = 16 * kConsumers;           // weight rows per stage
+constexpr int kWarpRows = 32;                    // weight rows per consumer warp: two m16 tiles
+constexpr int kRows = kWarpRows * kConsumers;    // weight rows per stage
 constexpr int kFeatGU = kRows / 2;               // features per gate/up block (128 gate + 128 up rows)
 constexpr int kChunk = 256;                      // K per stage (one 128-byte box row of codes)
 constexpr int kBarConsumers = 1;                 // named barrier of the consumer warps
-// Independent accumulator chains per warp (mma.sync has a long latency on
-// this part).  Measured on GB300: with eight consumer warps the kernel was
-// bound by instruction latency (14 % warps active, 37 % issue active), so
-// sixteen warps share the stage, which caps a thread at 120 registers.
-constexpr int kChains = 4;
+// Measured on GB300 (one CTA per SM): the layer is bound by the consumer
+// warps' instruction issue, not by the TMA stream (which alone reaches
+// about 90 % of the copy bandwidth).  A warp therefore takes 32 rows as two
+// m16 tiles: each B fragment it loads serves both, and the per-stage work
+// of a warp (wait, header, release) is spread over twice the weights.
 
 struct Hdr {
     int kind;    // 0 gate/up, 1 down, -1 end of work
@@ -81,15 +84,19 @@ struct Ch {
     static constexpr int CW = CB / 4;   // code words per lane per row
 };
 
+// A lane's codes of one stage row (CK = 256: 32 bytes, the 16-byte chunks
+// 2c and 2c + 1 of the 128-byte row, stored by TMA with the 128-byte swizzle:
+// chunk q of local row r at q ^ (r & 7), r & 7 == g for every warp's rows, so
+// that the eight rows a quarter warp reads land in distinct bank groups).
 template <int CK>
-__device__ __forceinline__ void lds_codes(const uint8_t* p, uint32_t* w) {
+__device__ __forceinline__ void lds_codes(const uint8_t* row, int g, int c, uint32_t* w) {
     if constexpr (CK == 256) {
-        const uint4 u0 = *reinterpret_cast<const uint4*>(p);
-        const uint4 u1 = *reinterpret_cast<const uint4*>(p + 16);
+        const uint4 u0 = *reinterpret_cast<const uint4*>(row + (((2 * c) ^ g) << 4));
+        const uint4 u1 = *reinterpret_cast<const uint4*>(row + (((2 * c + 1) ^ g) << 4));
         w[0] = u0.x; w[1] = u0.y; w[2] = u0.z; w[3] = u0.w;
         w[4] = u1.x; w[5] = u1.y; w[6] = u1.z; w[7] = u1.w;
     } else {
-        const uint2 u = *reinterpret_cast<const uint2*>(p);
+        const uint2 u = *reinterpret_cast<const uint2*>(row + 8 * c);
         w[0] = u.x; w[1] = u.y;
     }
 }
@@ -202,57 +209,50 @@ __device__ void stage_rows(const DecodeArgs& a, int K, int row0, int nrows, bool
     }
 }
 
-// One warp's share of a stage: MMA row g from codes c0 / scales s0, row
-// g + 8 from c1 / s1 (row pitches KC/2 and KC/16 bytes, as the TMA boxes
-// land); the stage covers K [k0, k0 + KC) of the staged B rows (row length
-// K); k-step i accumulates into chain i % kChains.
-template <int CK>
-__device__ __forceinline__ void stage_mma(const uint8_t* c0, const uint8_t* c1, const uint8_t* s0, const uint8_t* s1,
-                                          int KC, int k0, const uint4* Bs, int K, int lane,
-                                          float (&acc)[kChains][4]) {
-    using C = Ch<CK>;
+// One warp's share of a stage: two m16 tiles; tile t takes its MMA rows g
+// and g + 8 from the 128-byte code rows cr[t][0] and cr[t][1] (swizzled) and
+// the 16-byte scale rows sr[t][0] and sr[t][1].  The stage covers K
+// [k0, k0 + 256) of the staged B rows (row length K); k-step i of tile t
+// accumulates into acc[t][i & 1].
+__device__ __forceinline__ void stage_mma2(const uint8_t* const (&cr)[2][2], const uint8_t* const (&sr)[2][2], int k0,
+                                           const uint4* Bs, int K, int lane, float (&acc)[2][2][4]) {
+    using C = Ch<kChunk>;
     const int g = lane >> 2, c = lane & 3;
-    const int kb2 = KC / 2, ks16 = KC / 16;
-    const uint8_t* r0c = c0 + g * kb2;
-    const uint8_t* r1c = c1 + g * kb2;
-    const uint8_t* r0s = s0 + g * ks16;
-    const uint8_t* r1s = s1 + g * ks16;
-    const uint4* brow = Bs + (size_t)g * (K / 8);
-#pragma unroll 1
-    for (int kc = 0; kc < KC; kc += CK) {
-        const int kb = kc + c * C::TS;  // this lane's physical K inside the stage's chunk
-        uint32_t w0[C::CW], w1[C::CW];
-        lds_codes<CK>(r0c + kb / 2, w0);
-        lds_codes<CK>(r1c + kb / 2, w1);
-        constexpr int NB = C::TS / 16;  // 16-blocks per lane and chunk
-        uint32_t S0[NB], S1[NB];
-        block_scales<NB>(lds_scales<CK>(r0s + kb / 16), S0);
-        block_scales<NB>(lds_scales<CK>(r1s + kb / 16), S1);
-        const int qb = (k0 + kb) / 8;
+    uint32_t w[2][2][C::CW];
+    uint32_t S[2][2][4];
 #pragma unroll
-        for (int jj = 0; jj < C::KS; jj += 2) {
-            const uint4 bq = brow[bsw<CK>(qb + jj / 2, g)];
-            const uint32_t b0[2] = {bq.x, bq.y};
-            const uint32_t b1[2] = {bq.z, bq.w};
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            lds_codes<kChunk>(cr[t][r], g, c, w[t][r]);
+            block_scales<4>(lds_scales<kChunk>(sr[t][r] + 4 * c), S[t][r]);
+        }
+    const uint4* brow = Bs + (size_t)g * (K / 8);
+    const int qb = (k0 + c * C::TS) / 8;
+#pragma unroll
+    for (int jj = 0; jj < C::KS; jj += 2) {
+        const uint4 bq = brow[bsw<kChunk>(qb + jj / 2, g)];
+        const uint32_t b0[2] = {bq.x, bq.y};
+        const uint32_t b1[2] = {bq.z, bq.w};
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
             uint32_t x0[4], x1[4];
-            deq_word(w0[jj >> 1], S0[jj >> 2], x0);
-            deq_word(w1[jj >> 1], S1[jj >> 2], x1);
+            deq_word(w[t][0][jj >> 1], S[t][0][jj >> 2], x0);
+            deq_word(w[t][1][jj >> 1], S[t][1][jj >> 2], x1);
             const uint32_t af0[4] = {x0[0], x1[0], x0[1], x1[1]};
             const uint32_t af1[4] = {x0[2], x1[2], x0[3], x1[3]};
-            mma_16816(acc[jj % kChains], af0, b0);
-            mma_16816(acc[(jj + 1) % kChains], af1, b1);
+            mma_16816(acc[t][0], af0, b0);
+            mma_16816(acc[t][1], af1, b1);
         }
     }
 }
 
 template <int BMODE, int CKG, int CKD>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeArgs a) {
-    extern __shared__ __align__(128) uint8_t smem_raw[];
-    uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // the 128-byte swizzle repeats every 1024 bytes: slots start on that boundary
+    uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint4* Bs = reinterpret_cast<uint4*>(ring + (size_t)kNS * a.slot_bytes);
-    const int kmax = a.d > a.F ? a.d : a.F;
-    // W4A4: h of one 64-feature block [8 rows][64], exchanged between warps for the requantisation
-    float* s_hx = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(Bs) + (size_t)kGemvTokTile * kmax * 2);
     __shared__ __align__(8) uint64_t bar_full[kNS], bar_empty[kNS];
     __shared__ Hdr s_hdr[kNS];
     __shared__ float s_rowscale[kGemvTokTile];
@@ -287,8 +287,36 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         if (lane == 0) {
             long long st = 0;
             bool ok = true;
+            // items come in runs of consecutive indices (a.chu gate/up items,
+            // then a.chd down items per grab), so that a CTA mostly keeps one
+            // row tile's staged rows; every gate/up item is handed out before
+            // the first down item
+            int next = 0, run_end = 0;
+            bool down_phase = false;
             for (;;) {
-                const int item = atomicAdd(a.counters, 1);
+                int item = total;
+                if (next < run_end) {
+                    item = next++;
+                } else {
+                    if (!down_phase) {
+                        const int b = atomicAdd(a.counters, a.chu);
+                        if (b < nA) {
+                            next = b;
+                            run_end = min(nA, b + a.chu);
+                            item = next++;
+                        } else {
+                            down_phase = true;
+                        }
+                    }
+                    if (down_phase) {
+                        const int b = atomicAdd(a.counters + 1, a.chd);
+                        if (b < total - nA) {
+                            next = nA + b;
+                            run_end = nA + min(total - nA, b + a.chd);
+                            item = next++;
+                        }
+                    }
+                }
                 Hdr h{};
                 int nst = 1;
                 if (item >= total || *abort_flag) {
@@ -361,13 +389,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     } else {
         // ---------------- consumers ----------------
         const int g = lane >> 2, c = lane & 3;
-        float acc[kChains][4];
-#pragma unroll
-        for (int q = 0; q < kChains; ++q)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) acc[q][i] = 0.0f;
+        float acc[2][2][4];  // [tile][chain][fragment]
         long long st = 0;
         int par = 0;
+        int staged_tile = -1, staged_kind = -1;  // the rows now in Bs
         Hdr cur{};
         for (;;) {
             const int s = (int)(st % kNS);
@@ -376,9 +401,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
             const Hdr h = s_hdr[s];
             if (h.kind < 0) break;
             const bool down = h.kind == 1;
-            if (h.j == 0) {
-                // ---- a new item: stage its routed rows ----
-                cur = h;
+            if (h.j == 0) cur = h;
+            if (h.j == 0 && (h.tile != staged_tile || h.kind != staged_kind)) {
+                // ---- a new row tile: stage its routed rows ----
+                staged_tile = h.tile;
+                staged_kind = h.kind;
                 consumer_sync();  // the previous item's readers of Bs / s_rowscale are done
                 if (threadIdx.x < kGemvTokTile) s_amax[par ^ 1][threadIdx.x] = 0u;
                 if (down) {
@@ -411,27 +438,39 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
                 par ^= 1;
                 consumer_sync();
             }
-            // ---- this warp's 16 rows of the stage ----
+            // ---- this warp's 32 rows of the stage ----
             const int nch = down ? nchd : nchu;
             if (h.kc == 0) {
 #pragma unroll
-                for (int q = 0; q < kChains; ++q)
+                for (int t = 0; t < 2; ++t)
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) acc[q][i] = 0.0f;
+                    for (int q = 0; q < 2; ++q)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) acc[t][q][i] = 0.0f;
             }
             const uint8_t* slot = ring + (size_t)s * a.slot_bytes;
             if (!down) {
-                // MMA rows 0-7: gate rows 8w..8w+7 of the block, rows 8-15: the up rows of the same features
+                // tile t: MMA rows 0-7 are gate rows 16w + 8t .. + 7 of the
+                // block, rows 8-15 the up rows of the same features
                 const int cb = kFeatGU * kChunk / 2, sb = kFeatGU * kChunk / 16;
-                const uint8_t* gc = slot + 8 * warp * (kChunk / 2);
-                const uint8_t* gs = slot + 2 * cb + 8 * warp * (kChunk / 16);
-                stage_mma<CKG>(gc, gc + cb, gs, gs + sb, kChunk, h.kc * kChunk, Bs, a.d, lane, acc);
+                const int r0 = kWarpRows / 2 * warp + g;
+                const uint8_t* const cr[2][2] = {{slot + r0 * (kChunk / 2), slot + cb + r0 * (kChunk / 2)},
+                                                 {slot + (r0 + 8) * (kChunk / 2), slot + cb + (r0 + 8) * (kChunk / 2)}};
+                const uint8_t* const sr[2][2] = {
+                    {slot + 2 * cb + r0 * (kChunk / 16), slot + 2 * cb + sb + r0 * (kChunk / 16)},
+                    {slot + 2 * cb + (r0 + 8) * (kChunk / 16), slot + 2 * cb + sb + (r0 + 8) * (kChunk / 16)}};
+                stage_mma2(cr, sr, h.kc * kChunk, Bs, a.d, lane, acc);
             } else {
+                // tile t: MMA rows g and g + 8 are rows 32w + 16t + g and + 8
                 const int cb = kRows * kChunk / 2;
-                const uint8_t* dc = slot + 16 * warp * (kChunk / 2);
-                const uint8_t* ds = slot + cb + 16 * warp * (kChunk / 16);
-                stage_mma<CKD>(dc, dc + 8 * (kChunk / 2), ds, ds + 8 * (kChunk / 16), kChunk, h.kc * kChunk, Bs,
-                               a.F, lane, acc);
+                const int r0 = kWarpRows * warp + g;
+                const uint8_t* const cr[2][2] = {
+                    {slot + r0 * (kChunk / 2), slot + (r0 + 8) * (kChunk / 2)},
+                    {slot + (r0 + 16) * (kChunk / 2), slot + (r0 + 24) * (kChunk / 2)}};
+                const uint8_t* const sr[2][2] = {
+                    {slot + cb + r0 * (kChunk / 16), slot + cb + (r0 + 8) * (kChunk / 16)},
+                    {slot + cb + (r0 + 16) * (kChunk / 16), slot + cb + (r0 + 24) * (kChunk / 16)}};
+                stage_mma2(cr, sr, h.kc * kChunk, Bs, a.F, lane, acc);
             }
             // the slot is refilled by TMA (async proxy) after its release
             fence_proxy_async();
@@ -440,76 +479,75 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
 
             if (h.kc == nch - 1) {
                 // ---- this warp's rows of the block are complete: epilogue ----
-                float t[4];
+                float t4[2][4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    float v = acc[0][i];
+                for (int t = 0; t < 2; ++t)
 #pragma unroll
-                    for (int q = 1; q < kChains; ++q) v += acc[q][i];
-                    t[i] = v;
-                }
+                    for (int i = 0; i < 4; ++i) t4[t][i] = acc[t][0][i] + acc[t][1][i];
                 const int e = cur.e;
                 if (!down) {
-                    // lane (g, c): feature f + 8w + g; gate in t[cc], up in t[2 + cc] for row 2c + cc
-                    const int f = h.f + 8 * warp + g;
+                    // lane (g, c), tile t: feature f + 16w + 8t + g; gate in
+                    // t4[t][cc], up in t4[t][2 + cc] for row 2c + cc
+                    const int f0 = h.f + kWarpRows / 2 * warp;
                     const float wg = a.gate_ws2[e], wu = a.up_ws2[e];
-                    float hv[2];
 #pragma unroll
                     for (int cc = 0; cc < 2; ++cc) {
                         const int col = 2 * c + cc;
                         const bool valid = col < cur.nrows;
                         const float rs = BMODE == B_BF16 ? (valid ? s_rowscale[col] : 0.0f) : a.is13[e];
-                        const float G = round_bf16(__fmul_rn(__fmul_rn(t[cc], rs), wg));
-                        const float U = round_bf16(__fmul_rn(__fmul_rn(t[2 + cc], rs), wu));
-                        hv[cc] = valid ? round_bf16(G / (1.0f + expf(-G)) * U) : 0.0f;
-                        if constexpr (BMODE == B_BF16) {
-                            if (valid) a.h[(size_t)(cur.row0 + col) * a.F + f] = f32_to_bf16_bits(hv[cc]);
-                        }
-                    }
-                    if constexpr (BMODE == B_NVFP4) {
-                        // an NVFP4 block of 16 features spans two warps: h goes
-                        // through shared memory, then warp w requantises routed
-                        // row w % 8 of the block, blocks 4 (w / 8) .. + 3 (lane b
-                        // of those: features 16b .. 16b + 15)
+                        float hv[2];
 #pragma unroll
-                        for (int cc = 0; cc < 2; ++cc) s_hx[(2 * c + cc) * kFeatGU + 8 * warp + g] = hv[cc];
-                        consumer_sync();
-                        const int row = warp % kGemvTokTile;
-                        constexpr int kBlkPerWarp = kFeatGU / 16 / (kConsumers / kGemvTokTile);
-                        if (row < cur.nrows && lane < kBlkPerWarp) {
-                            const int b = (warp / kGemvTokTile) * kBlkPerWarp + lane;
-                            float v[16], m = 0.0f;
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                v[i] = s_hx[row * kFeatGU + 16 * b + i];
-                                m = fmaxf(m, fabsf(v[i]));
+                        for (int t = 0; t < 2; ++t) {
+                            const float G = round_bf16(__fmul_rn(__fmul_rn(t4[t][cc], rs), wg));
+                            const float U = round_bf16(__fmul_rn(__fmul_rn(t4[t][2 + cc], rs), wu));
+                            hv[t] = valid ? round_bf16(G / (1.0f + expf(-G)) * U) : 0.0f;
+                            if constexpr (BMODE == B_BF16) {
+                                if (valid) a.h[(size_t)(cur.row0 + col) * a.F + f0 + 8 * t + g] = f32_to_bf16_bits(hv[t]);
                             }
+                        }
+                        if constexpr (BMODE == B_NVFP4) {
+                            // the warp's 16 features are one NVFP4 block of h
+                            // for each row: tile t, lane g holds feature 8t + g
                             const float gs2 = a.is2[e];
-                            uint32_t sbyte = 0, q0 = 0, q1 = 0;
+                            float m = fmaxf(fabsf(hv[0]), fabsf(hv[1]));
+                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+                            uint32_t sbyte = 0, q[2] = {0u, 0u};
                             if (gs2 > 0.0f) {
                                 sbyte = f32_to_e4m3(__fdiv_rn(__fdiv_rn(m, 6.0f), gs2));
                                 const float S = e4m3_to_f32(sbyte);
                                 if (S != 0.0f) {
                                     const float den = __fmul_rn(S, gs2), rden = __frcp_rn(den);
-#pragma unroll
-                                    for (int i = 0; i < 8; i += 2) {
-                                        q0 |= e2m1x2_byte(e2m1_quotient(v[i], den, rden),
-                                                          e2m1_quotient(v[i + 1], den, rden)) << (4 * i);
-                                        q1 |= e2m1x2_byte(e2m1_quotient(v[8 + i], den, rden),
-                                                          e2m1_quotient(v[9 + i], den, rden)) << (4 * i);
-                                    }
+                                    const uint32_t byte = e2m1x2_byte(e2m1_quotient(hv[0], den, rden),
+                                                                      e2m1_quotient(hv[1], den, rden));
+                                    q[0] = byte & 0xFu;
+                                    q[1] = byte >> 4;
                                 }
                             }
-                            const size_t r = (size_t)(cur.row0 + row);
-                            const int fb = h.f + 16 * b;
-                            *reinterpret_cast<uint2*>(a.hq + r * (a.F / 2) + fb / 2) = make_uint2(q0, q1);
-                            a.hs[r * (a.F / 16) + fb / 16] = (uint8_t)sbyte;
+                            // byte k of the block: features 2k, 2k + 1 (tile k / 4,
+                            // lanes g = 2 (k % 4) and + 1); lane g = 0 gathers all eight
+                            uint32_t by[2];
+#pragma unroll
+                            for (int t = 0; t < 2; ++t)
+                                by[t] = q[t] | (__shfl_down_sync(0xffffffffu, q[t], 4) << 4);
+                            uint32_t wd[2];
+#pragma unroll
+                            for (int t = 0; t < 2; ++t) {
+                                wd[t] = by[t];
+#pragma unroll
+                                for (int k = 1; k < 4; ++k) wd[t] |= __shfl_sync(0xffffffffu, by[t], c + 8 * k) << (8 * k);
+                            }
+                            if (valid && g == 0) {
+                                const size_t r = (size_t)(cur.row0 + col);
+                                *reinterpret_cast<uint2*>(a.hq + r * (a.F / 2) + f0 / 2) = make_uint2(wd[0], wd[1]);
+                                a.hs[r * (a.F / 16) + f0 / 16] = (uint8_t)sbyte;
+                            }
                         }
-                        consumer_sync();  // s_hx is rewritten by the next block
                     }
                 } else {
-                    // lane (g, c): outputs n0 + g and n0 + g + 8 for rows 2c + cc
-                    const int n0 = h.f + 16 * warp;
+                    // lane (g, c), tile t: outputs n0 + 16t + g and + 8 for rows 2c + cc
+                    const int n0 = h.f + kWarpRows * warp;
                     const float wd = a.down_ws2[e];
 #pragma unroll
                     for (int cc = 0; cc < 2; ++cc) {
@@ -518,24 +556,34 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
                             const int r = cur.row0 + col;
                             const float rs = BMODE == B_BF16 ? s_rowscale[col] : a.is2[e];
                             const float wt = a.topk_w[a.row_to_slot[r]];
-                            a.yrows[(size_t)r * a.d + n0 + g] = wt * __fmul_rn(__fmul_rn(t[cc], rs), wd);
-                            a.yrows[(size_t)r * a.d + n0 + g + 8] = wt * __fmul_rn(__fmul_rn(t[2 + cc], rs), wd);
+                            float* yr = a.yrows + (size_t)r * a.d + n0 + g;
+#pragma unroll
+                            for (int t = 0; t < 2; ++t) {
+                                yr[16 * t] = wt * __fmul_rn(__fmul_rn(t4[t][cc], rs), wd);
+                                yr[16 * t + 8] = wt * __fmul_rn(__fmul_rn(t4[t][2 + cc], rs), wd);
+                            }
                         }
                     }
                 }
-                __threadfence();
             }
 
             if (h.j == h.nst - 1) {
                 // ---- the item is complete ----
-                consumer_sync();  // every epilogue write of the item is done (and fenced)
+                // every epilogue write of the item is done; the barrier plus a
+                // gpu-scope fence before each counter update publishes them
+                // (release), and readers fence after seeing the count (acquire)
+                consumer_sync();
                 if (!down) {
-                    if (threadIdx.x == 0) atomicAdd(a.tile_ready + cur.tile, 1);
+                    if (threadIdx.x == 0) {
+                        __threadfence();
+                        atomicAdd(a.tile_ready + cur.tile, 1);
+                    }
                 } else {
                     if (threadIdx.x < kGemvTokTile) {
                         int t = -1;
                         if (threadIdx.x < cur.nrows) {
                             const int tt = a.row_to_slot[cur.row0 + threadIdx.x] / a.top_k;
+                            __threadfence();
                             if (atomicAdd(a.tok_done + (size_t)tt * ngd + cur.grp, 1) == a.top_k - 1) t = tt;
                         }
                         s_fin[threadIdx.x] = t;
@@ -586,8 +634,7 @@ int slot_bytes(int d, int F) {
 }
 
 size_t decode_smem(int d, int F) {
-    return 128 + (size_t)kNS * slot_bytes(d, F) + (size_t)kGemvTokTile * std::max(d, F) * 2 +
-           (size_t)kGemvTokTile * kFeatGU * 4;
+    return 1024 + (size_t)kNS * slot_bytes(d, F) + (size_t)kGemvTokTile * std::max(d, F) * 2;
 }
 
 // Blocks per item: the most (a divisor of nb) that still gives every SM
@@ -612,17 +659,22 @@ int decode_groups_d(int d) { return std::max(1, d / kRows); }
 
 bool decode_set_maps(DecodeArgs* a, const nvfp4_moe_weights* w) {
     const unsigned long long E = (unsigned long long)w->E, d = a->d, F = a->F;
-    return encode_tmap_u8(&a->tm_gate_c, w->gate.codes, d / 2, E * F, kChunk / 2, kFeatGU, false) &&
-           encode_tmap_u8(&a->tm_up_c, w->up.codes, d / 2, E * F, kChunk / 2, kFeatGU, false) &&
+    return encode_tmap_u8(&a->tm_gate_c, w->gate.codes, d / 2, E * F, kChunk / 2, kFeatGU, true) &&
+           encode_tmap_u8(&a->tm_up_c, w->up.codes, d / 2, E * F, kChunk / 2, kFeatGU, true) &&
            encode_tmap_u8(&a->tm_gate_s, w->gate.scales, d / 16, E * F, kChunk / 16, kFeatGU, false) &&
            encode_tmap_u8(&a->tm_up_s, w->up.scales, d / 16, E * F, kChunk / 16, kFeatGU, false) &&
-           encode_tmap_u8(&a->tm_down_c, w->down.codes, F / 2, E * d, kChunk / 2, kRows, false) &&
+           encode_tmap_u8(&a->tm_down_c, w->down.codes, F / 2, E * d, kChunk / 2, kRows, true) &&
            encode_tmap_u8(&a->tm_down_s, w->down.scales, F / 16, E * d, kChunk / 16, kRows, false);
 }
 
-void decode_pick_groups(int expected_tiles, int d, int F, int* gbu, int* gbd) {
-    *gbu = pick_blocks(expected_tiles, F / kFeatGU, 12);
-    *gbd = pick_blocks(expected_tiles, d / kRows, 12);
+void decode_pick_work(int expected_tiles, DecodeArgs* a) {
+    const int nbu = a->F / kFeatGU, nbd = a->d / kRows;
+    a->gbu = pick_blocks(expected_tiles, nbu, 12);
+    a->gbd = pick_blocks(expected_tiles, nbd, 12);
+    // about six grabs per CTA and phase, never more than one tile's items
+    const long long n_u = (long long)expected_tiles * (nbu / a->gbu), n_d = (long long)expected_tiles * (nbd / a->gbd);
+    a->chu = (int)std::max(1LL, std::min<long long>(nbu / a->gbu, n_u / (6LL * num_sms())));
+    a->chd = (int)std::max(1LL, std::min<long long>(nbd / a->gbd, n_d / (6LL * num_sms())));
 }
 
 void launch_decode(int bmode, const DecodeArgs& args, cudaStream_t s) {
