@@ -31,7 +31,7 @@ def _check_shared(orc, x, wg, wu, wd, routed, out, ws, what):
 
 
 @pytest.mark.parametrize("T,d,Fs", [(1, 256, 128), (100, 512, 256), (300, 1024, 384), (129, 4096, 1536),
-                                    (1280, 2048, 256)])
+                                    (64, 4096, 1536), (1280, 2048, 256)])
 def test_shared_expert(orc, T, d, Fs):
     """Single and ragged token tiles, one and several column tiles in both
     GEMMs, K from 128 to 4096; the small batches run 64-wide tiles, the last
