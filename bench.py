@@ -7,9 +7,10 @@ down + weighted combine) over one batch of seeded synthetic tokens whose
 inputs are already resident in HBM.  The default workload is the
 decode-shaped layer (288 experts, top-8, d=4096, ffn=1536) at T=64; the
 line also carries a sweep over T in {1, 8, 32, 64} and, under "workloads",
-the prompt-shaped layers (W4A16 T=4096; W4A4 T=8192 with calibrated static
-scales; skewed Zipf(1.2) popularity at T=16384, with and without a third of
-the experts masked, both modes) and the dense NVFP4 MLP, each with its own
+the W4A4 decode-shaped layer at T=64 and the prompt-shaped layers (W4A16
+T=4096; W4A4 T=8192 with calibrated static scales; skewed Zipf(1.2)
+popularity at T=16384, with and without a third of the experts masked, both
+modes) and the dense NVFP4 MLP, each with its own
 device time, end-to-end time, kernel split and binding roofline.  The L2 is flushed (a
 256 MB write) between timed steps, outside the timed events.
 
@@ -144,6 +145,7 @@ WORKLOADS = {
     "decode8": (synth.decode(8), "w4a16", "normal", 0.0),
     "decode32": (synth.decode(32), "w4a16", "normal", 0.0),
     "decode64": (synth.decode(64), "w4a16", "normal", 0.0),
+    "decode64_w4a4": (synth.decode(64), "w4a4", "normal", 0.0),
     "prefill_w4a16": (synth.PREFILL_W4A16, "w4a16", "normal", 0.05),
     "prefill_w4a4": (synth.PREFILL_W4A4, "w4a4", "normal", 0.05),
     "skew_w4a16": (synth.SKEW, "w4a16", "zipf", 0.0),
@@ -692,6 +694,8 @@ def dtype_of(layer, kernels):
 
 PROMPT_WORKLOADS = ("prefill_w4a16", "prefill_w4a4", "skew_w4a16", "skew_w4a4", "skew_masked_w4a16",
                     "skew_masked_w4a4", "dense")
+# other layers measured beside the headline in the default run (decode steps)
+EXTRA_DECODE_WORKLOADS = ("decode64_w4a4",)
 
 
 def run_ours(args):
@@ -764,10 +768,10 @@ def run_ours(args):
         # each measured the same way (fewer steps: each step is milliseconds)
         lib.set_kernel_choice("auto")
         wl = {}
-        for name in PROMPT_WORKLOADS:
+        for name in EXTRA_DECODE_WORKLOADS + PROMPT_WORKLOADS:
             lay = (DenseLayer if name == "dense" else Layer)(name, lib, dev, seed + 7)
-            res = measure(lay, lib, args, flush, hbm, bf16, peak_kind, min(args.steps, args.prompt_steps), world,
-                          dev)
+            n_steps = args.steps if name in EXTRA_DECODE_WORKLOADS else min(args.steps, args.prompt_steps)
+            res = measure(lay, lib, args, flush, hbm, bf16, peak_kind, n_steps, world, dev)
             res.pop("times_ms")
             res["tokens_per_s"] = res.pop("value")
             res["config"] = workload_config(lay, flush_mb)
