@@ -93,61 +93,71 @@ __device__ void topk_dispatch(const float* lg, int E, int k, int32_t* ids, float
     else warp_topk<32>(lg, E, k, ids, w);
 }
 
-// Exclusive scan of one int per thread over the block (blockDim multiple of 32).
-__device__ int block_exclusive_scan(int v, int* tmp32, int& total) {
+// Exclusive scan of four ints per thread over the block in one pass
+// (blockDim multiple of 32): returns the prefix, `total` the block sums.
+__device__ int4 block_exclusive_scan4(int4 v, int4* tmp, int4& total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    int x = v;
+    int4 x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
+        const int4 y = make_int4(__shfl_up_sync(0xffffffffu, x.x, o), __shfl_up_sync(0xffffffffu, x.y, o),
+                                 __shfl_up_sync(0xffffffffu, x.z, o), __shfl_up_sync(0xffffffffu, x.w, o));
+        if (lane >= o) {
+            x.x += y.x;
+            x.y += y.y;
+            x.z += y.z;
+            x.w += y.w;
+        }
     }
-    if (lane == 31) tmp32[warp] = x;
+    if (lane == 31) tmp[warp] = x;
     __syncthreads();
     if (warp == 0) {
-        int s = lane < nw ? tmp32[lane] : 0;
+        int4 t = lane < nw ? tmp[lane] : make_int4(0, 0, 0, 0);
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            int y = __shfl_up_sync(0xffffffffu, s, o);
-            if (lane >= o) s += y;
+            const int4 y = make_int4(__shfl_up_sync(0xffffffffu, t.x, o), __shfl_up_sync(0xffffffffu, t.y, o),
+                                     __shfl_up_sync(0xffffffffu, t.z, o), __shfl_up_sync(0xffffffffu, t.w, o));
+            if (lane >= o) {
+                t.x += y.x;
+                t.y += y.y;
+                t.z += y.z;
+                t.w += y.w;
+            }
         }
-        tmp32[lane] = s;
+        tmp[lane] = t;
     }
     __syncthreads();
-    const int prefix = (warp > 0 ? tmp32[warp - 1] : 0) + x - v;
-    total = tmp32[nw - 1];
+    const int4 before = warp > 0 ? tmp[warp - 1] : make_int4(0, 0, 0, 0);
+    total = tmp[nw - 1];
     __syncthreads();
-    return prefix;
+    return make_int4(before.x + x.x - v.x, before.y + x.y - v.y, before.z + x.z - v.z, before.w + x.w - v.w);
 }
 
 // offsets / active list / gemv tile prefix from per-expert counts c (thread e
 // holds expert e; blockDim >= E).
-__device__ void write_group_meta(int c, int E, const RouteArrays& ra, int* tmp32, int& off_out) {
+__device__ void write_group_meta(int c, int E, const RouteArrays& ra, int4* tmp, int& off_out) {
     const int e = threadIdx.x;
-    int total;
-    const int off = block_exclusive_scan(e < E ? c : 0, tmp32, total);
-    if (e < E) ra.offsets[e] = off;
-    if (e == 0) ra.offsets[E] = total;
-    const int flag = (e < E && c > 0) ? 1 : 0;
-    int na;
-    const int aidx = block_exclusive_scan(flag, tmp32, na);
-    const int tiles = flag ? (c + kGemvTokTile - 1) / kGemvTokTile : 0;
-    int tt;
-    const int tpre = block_exclusive_scan(tiles, tmp32, tt);
-    const int tiles_tc = flag ? (c + kTcTokTile - 1) / kTcTokTile : 0;
-    int tt_tc;
-    const int tpre_tc = block_exclusive_scan(tiles_tc, tmp32, tt_tc);
+    const int cc = e < E ? c : 0;
+    const int flag = cc > 0 ? 1 : 0;
+    // one pass: offsets, active-list index, decode tiles, tensor-core tiles
+    int4 tot;
+    const int4 pre = block_exclusive_scan4(
+        make_int4(cc, flag, flag ? (cc + kGemvTokTile - 1) / kGemvTokTile : 0,
+                  flag ? (cc + kTcTokTile - 1) / kTcTokTile : 0),
+        tmp, tot);
+    if (e < E) ra.offsets[e] = pre.x;
+    if (e == 0) ra.offsets[E] = tot.x;
     if (flag) {
-        ra.active[aidx] = e;
-        ra.tile_start[aidx] = tpre;
-        if (ra.tile_start_tc) ra.tile_start_tc[aidx] = tpre_tc;
+        ra.active[pre.y] = e;
+        ra.tile_start[pre.y] = pre.z;
+        if (ra.tile_start_tc) ra.tile_start_tc[pre.y] = pre.w;
     }
     if (e == 0) {
-        *ra.n_active = na;
-        ra.tile_start[na] = tt;
-        if (ra.tile_start_tc) ra.tile_start_tc[na] = tt_tc;
+        *ra.n_active = tot.y;
+        ra.tile_start[tot.y] = tot.z;
+        if (ra.tile_start_tc) ra.tile_start_tc[tot.y] = tot.w;
     }
-    off_out = off;
+    off_out = pre.x;
 }
 
 // Scatter rows [row0, row1) in rounds of blockDim rows; run[e] holds the next
@@ -169,9 +179,10 @@ __device__ void scatter_rows(int row0, int row1, int E, const int32_t* __restric
             ra.slot_to_row[r] = pos;
         }
         __syncthreads();
+        const int nwu = min(nw, (row1 - base + 31) / 32);  // warps that held rows this round
         for (int e2 = threadIdx.x; e2 < E; e2 += blockDim.x) {
             int s = 0;
-            for (int w2 = 0; w2 < nw; ++w2) {
+            for (int w2 = 0; w2 < nwu; ++w2) {
                 s += wh[w2 * E + e2];
                 wh[w2 * E + e2] = 0;
             }
@@ -205,7 +216,7 @@ __global__ void __launch_bounds__(1024) route_perm_small_kernel(int T, int E, in
                                                                 int32_t* status, const float* logits) {
     __shared__ int run[kMaxExperts];
     __shared__ uint8_t wh[32 * kMaxExperts];
-    __shared__ int tmp32[32];
+    __shared__ int4 tmp32[32];
     grid_dep_wait();
     const int R = T * k;
     if (logits) {
@@ -255,7 +266,7 @@ __global__ void __launch_bounds__(1024) perm_count_kernel(const int32_t* __restr
 }
 
 __global__ void __launch_bounds__(1024) perm_scan_kernel(int nb, int E, int32_t* counts, RouteArrays ra) {
-    __shared__ int tmp32[32];
+    __shared__ int4 tmp32[32];
     grid_dep_wait();
     const int e = threadIdx.x;
     int run = 0;
