@@ -118,7 +118,13 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
     __shared__ int s_next;
     __shared__ int s_fin[kGemvTokTile];
 
-    grid_dep_wait();
+    // The routed layer's down projection (OUT_COMBINE) takes its first item
+    // and starts that item's weight loads before it waits for the gate/up
+    // launch: its routing arrays and work counter come from the route launch
+    // before that one, complete by the time any gate/up CTA lets dependents
+    // start; only the h rows it stages need the wait.
+    constexpr bool kEarly = OUTMODE == OUT_COMBINE;
+    if constexpr (!kEarly) grid_dep_wait();
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, c = lane & 3;
@@ -186,6 +192,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
         decode(item, cur);
         prefetch(cur);
     }
+    if constexpr (kEarly) grid_dep_wait();
 
     while (item < total) {
         // ---- stage the B rows of this item; the warps w with w % nrows == j stage row j
@@ -320,6 +327,11 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
                 prefetch(following);
             } else {
                 nitem = s_next;
+                // gate/up: a CTA without a further item lets the down launch
+                // start filling SMs while the last items finish
+                if constexpr (NPROJ == 2) {
+                    if (nitem >= total) grid_dep_launch();
+                }
                 if (nitem < total) {
                     decode(nitem, nxt);
                     prefetch(nxt);
