@@ -372,11 +372,14 @@ __global__ void __launch_bounds__(kThreads, 1) tcm_kernel(const __grid_constant_
                     ok = false;
                     break;
                 }
+                // 32-byte swizzle: half h of row r sits at h ^ (bit 2 of r)
+                // (rows tg and tg + 128 share that bit)
+                const int h0 = ((tg >> 2) & 1) << 4, h1 = 16 - h0;
                 uint4 c[4];
-                c[0] = *reinterpret_cast<const uint4*>(ring_r + sr * kRaw + tg * 32);
-                c[1] = *reinterpret_cast<const uint4*>(ring_r + sr * kRaw + tg * 32 + 16);
-                c[2] = *reinterpret_cast<const uint4*>(ring_r + sr * kRaw + (tg + 128) * 32);
-                c[3] = *reinterpret_cast<const uint4*>(ring_r + sr * kRaw + (tg + 128) * 32 + 16);
+                c[0] = *reinterpret_cast<const uint4*>(ring_r + sr * kRaw + tg * 32 + h0);
+                c[1] = *reinterpret_cast<const uint4*>(ring_r + sr * kRaw + tg * 32 + h1);
+                c[2] = *reinterpret_cast<const uint4*>(ring_r + sr * kRaw + (tg + 128) * 32 + h0);
+                c[3] = *reinterpret_cast<const uint4*>(ring_r + sr * kRaw + (tg + 128) * 32 + h1);
                 if (!wait_done<SD>(bar_done, i - SB, abort_flag, a.status)) {
                     ok = false;
                     break;
@@ -476,8 +479,11 @@ bool make_tmap_rows_f16(CUtensorMap* map, const void* base, int rows, int K) {
 }
 
 // The stored codes [rows, K/2] and scales [rows, K/16] of an NVFP4 tensor as
-// uint8 tensor maps: boxes of 128 rows x 32 bytes (one k-stage of codes) and
-// 128 rows x 16 bytes (four k-stages of scales), no swizzle.
+// uint8 tensor maps: boxes of 128 rows x 32 bytes (one k-stage of codes,
+// with the 32-byte swizzle: the two 16-byte halves of row r swap places
+// when bit 2 of r is set, so that the producers' 16-byte reads of eight
+// consecutive rows hit eight distinct bank groups) and 128 rows x 16 bytes
+// (four k-stages of scales), no swizzle.
 bool make_tmap_weights(CUtensorMap* codes, CUtensorMap* scales, const uint8_t* c, const uint8_t* sc, long long rows,
                        int K) {
     if (!g_encode || rows < 1 || K % 256 != 0 || !aligned16(c) || !aligned16(sc)) return false;
@@ -486,7 +492,7 @@ bool make_tmap_weights(CUtensorMap* codes, CUtensorMap* scales, const uint8_t* c
     const cuuint64_t cs[1] = {(cuuint64_t)K / 2};
     const cuuint32_t cb[2] = {32, 128};
     if (g_encode(codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(c), cd, cs, cb, estr,
-                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return false;
     const cuuint64_t sd[2] = {(cuuint64_t)K / 16, (cuuint64_t)rows};
