@@ -36,6 +36,7 @@
 
 #include "common.cuh"
 #include "internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace nvfp4 {
 
@@ -99,18 +100,34 @@ __device__ __forceinline__ int bsw(int q, int g) {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+
+// Shared-memory weight ring of the routed down projection (one projection,
+// 256-wide chunks): per warp kRingSlots slots of one chunk of its 16 rows
+// (codes, then scales), filled with cp.async by the lanes that read them.
+constexpr int kRingSlots = 4;
+constexpr int kRingSlotBytes = 2 * 32 * 32 + 2 * 32 * 4;  // 2304
+constexpr size_t ring_bytes() { return (size_t)kWarps * kRingSlots * kRingSlotBytes; }
+// The ring is used while two CTAs' row stage plus ring (and ~4 KB of static
+// shared memory each) fit in an SM: K up to 9216.
+bool ring_fits(int K) { return 2 * ((size_t)kGemvTokTile * K * 2 + ring_bytes() + 4096) <= 227 * 1024; }
 struct Item {
     int e, row0, nrows, fb, fb_end;  // feature blocks [fb, fb_end) share the staged rows
 };
 
-template <int CK, int BMODE, int OUTMODE, int NPROJ>
+template <int CK, int BMODE, int OUTMODE, int NPROJ, bool RING = false>
 __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
     using C = Chunk<CK>;
     // U chunks form a batch of weight loads; NBUF batches live in registers
     // as a ring, so that NBUF - 1 batches are in flight while one is consumed
-    // (the next work item's first batches go out before the epilogue)
+    // (the next work item's first batches go out before the epilogue).  The
+    // routed down projection keeps its batches in a shared-memory ring
+    // instead (cp.async; no registers held by the loads in flight), four
+    // slots deep: measured on GB300 its register ring left it bound by the
+    // latency of its weight loads at two batches in flight.
     constexpr int U = 1;
-    constexpr int NBUF = NPROJ == 2 ? 2 : 3;
+    constexpr bool kRing = RING;
+    static_assert(!RING || (OUTMODE == OUT_COMBINE && NPROJ == 1 && CK == 256), "the ring serves the down GEMV");
+    constexpr int NBUF = kRing ? kRingSlots : (NPROJ == 2 ? 2 : 3);
     extern __shared__ uint4 Bs[];          // [kGemvTokTile][K/8] granules of f16
     __shared__ float s_red[kWarps - 1][NPROJ * 4][32];
     __shared__ float s_rowscale[kGemvTokTile];
@@ -156,24 +173,50 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
         it.nrows = min(kGemvTokTile, a.offsets[it.e + 1] - it.row0);
     };
 
-    uint32_t acw[NBUF][U][NPROJ][2][C::CW];
-    uint32_t asw[NBUF][U][NPROJ][2];
+    uint32_t acw[kRing ? 1 : NBUF][U][NPROJ][2][C::CW];
+    uint32_t asw[kRing ? 1 : NBUF][U][NPROJ][2];
+    // ring slot b of this warp: codes [row half][lane][32 B] (the two 16-byte
+    // halves of lane l at h ^ bit 2 of l: conflict-free 16-byte reads), then
+    // scales [row half][lane][4 B]
+    uint8_t* wring = reinterpret_cast<uint8_t*>(Bs + (size_t)kGemvTokTile * (a.K / 8)) +
+                     (size_t)warp * kRingSlots * kRingSlotBytes;
+    const int hsw = ((lane >> 2) & 1) << 4;
     auto load_batch = [&](auto buf, const Item& it, int chb) {
         constexpr int B = decltype(buf)::value;
         const int n0 = it.fb * FB + wf * 16;
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int ch = chb + u * KSPL;
+        if constexpr (kRing) {
+            // one commit group per call, empty past the end, so that a
+            // batch is complete once NBUF - 1 later groups were committed
+            const int ch = chb;
             if (ch < nch) {
+                uint8_t* sl = wring + B * kRingSlotBytes;
                 const size_t kb = (size_t)ch * CK + (size_t)c * C::TS;
 #pragma unroll
-                for (int p = 0; p < NPROJ; ++p)
+                for (int hf = 0; hf < 2; ++hf) {
+                    const size_t row = (size_t)it.e * a.N + n0 + g + 8 * hf;
+                    const uint8_t* src = a.a_codes[0] + row * K2 + kb / 2;
+                    uint8_t* dst = sl + hf * 1024 + lane * 32;
+                    tc::cp_async16(tc::smem_u32(dst + hsw), src, 16);
+                    tc::cp_async16(tc::smem_u32(dst + (16 - hsw)), src + 16, 16);
+                    tc::cp_async4(tc::smem_u32(sl + 2048 + hf * 128 + lane * 4), a.a_scales[0] + row * K16 + kb / 16);
+                }
+            }
+            tc::cp_async_commit();
+        } else {
 #pragma unroll
-                    for (int hf = 0; hf < 2; ++hf) {
-                        const size_t row = (size_t)it.e * a.N + n0 + g + 8 * hf;
-                        load_codes<CK>(a.a_codes[p] + row * K2 + kb / 2, acw[B][u][p][hf]);
-                        asw[B][u][p][hf] = load_scales<CK>(a.a_scales[p] + row * K16 + kb / 16);
-                    }
+            for (int u = 0; u < U; ++u) {
+                const int ch = chb + u * KSPL;
+                if (ch < nch) {
+                    const size_t kb = (size_t)ch * CK + (size_t)c * C::TS;
+#pragma unroll
+                    for (int p = 0; p < NPROJ; ++p)
+#pragma unroll
+                        for (int hf = 0; hf < 2; ++hf) {
+                            const size_t row = (size_t)it.e * a.N + n0 + g + 8 * hf;
+                            load_codes<CK>(a.a_codes[p] + row * K2 + kb / 2, acw[B][u][p][hf]);
+                            asw[B][u][p][hf] = load_scales<CK>(a.a_scales[p] + row * K16 + kb / 16);
+                        }
+                }
             }
         }
     };
@@ -181,6 +224,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
     auto prefetch = [&](const Item& it) {
         load_batch(std::integral_constant<int, 0>{}, it, ks);
         if constexpr (NBUF > 2) load_batch(std::integral_constant<int, 1>{}, it, ks + U * KSPL);
+        if constexpr (NBUF > 3) load_batch(std::integral_constant<int, 2>{}, it, ks + 2 * U * KSPL);
     };
 
     if (tid == 0) s_next = atomicAdd(a.work_counter, 1);
@@ -261,6 +305,21 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
             const uint4* brow_s = Bs + (size_t)g * Kg;
             auto compute = [&](auto buf, int chb) {
                 constexpr int B = decltype(buf)::value;
+                if constexpr (kRing) {
+                    // this batch's copies have landed (NBUF - 1 later groups may not have)
+                    tc::cp_async_wait<NBUF - 1>();
+                    const uint8_t* sl = wring + B * kRingSlotBytes;
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const uint4 u0 = *reinterpret_cast<const uint4*>(sl + hf * 1024 + lane * 32 + hsw);
+                        const uint4 u1 = *reinterpret_cast<const uint4*>(sl + hf * 1024 + lane * 32 + (16 - hsw));
+                        uint32_t* w = acw[0][0][0][hf];
+                        w[0] = u0.x; w[1] = u0.y; w[2] = u0.z; w[3] = u0.w;
+                        w[4] = u1.x; w[5] = u1.y; w[6] = u1.z; w[7] = u1.w;
+                        asw[0][0][0][hf] = *reinterpret_cast<const uint32_t*>(sl + 2048 + hf * 128 + lane * 4);
+                    }
+                }
+                constexpr int BR = kRing ? 0 : B;  // register buffer the batch sits in
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int ch = chb + u * KSPL;
@@ -274,8 +333,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
 #pragma unroll
                         for (int p = 0; p < NPROJ; ++p) {
                             uint32_t r0[4], r1[4];
-                            deq_word(acw[B][u][p][0][jj >> 1], asw[B][u][p][0], jj, r0);
-                            deq_word(acw[B][u][p][1][jj >> 1], asw[B][u][p][1], jj, r1);
+                            deq_word(acw[BR][u][p][0][jj >> 1], asw[BR][u][p][0], jj, r0);
+                            deq_word(acw[BR][u][p][1][jj >> 1], asw[BR][u][p][1], jj, r1);
                             const uint32_t af0[4] = {r0[0], r1[0], r0[1], r1[1]};
                             const uint32_t af1[4] = {r0[2], r1[2], r0[3], r1[3]};
                             mma_16816(acc[p], af0, b0);
@@ -290,18 +349,28 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
                 constexpr std::integral_constant<int, 0> kB0{};
                 constexpr std::integral_constant<int, 1> kB1{};
                 constexpr std::integral_constant<int, 2 % NBUF> kB2{};
+                constexpr std::integral_constant<int, 3 % NBUF> kB3{};
                 const int step = U * KSPL;
+                // the ring's loads commit a group on every call (empty past the end)
+                auto load_ahead = [&](auto buf, int ch) {
+                    if (kRing || ch < nch) load_batch(buf, cur, ch);
+                };
                 for (int chb = ks; chb < nch; chb += NBUF * step) {
                     const int ld = (NBUF - 1) * step;  // distance of the batch loaded ahead
-                    if (chb + ld < nch) load_batch(std::integral_constant<int, NBUF - 1>{}, cur, chb + ld);
+                    load_ahead(std::integral_constant<int, NBUF - 1>{}, chb + ld);
                     compute(kB0, chb);
                     if (chb + step >= nch) break;
-                    if (chb + step + ld < nch) load_batch(kB0, cur, chb + step + ld);
+                    load_ahead(kB0, chb + step + ld);
                     compute(kB1, chb + step);
-                    if constexpr (NBUF == 3) {
+                    if constexpr (NBUF >= 3) {
                         if (chb + 2 * step >= nch) break;
-                        if (chb + 2 * step + ld < nch) load_batch(kB1, cur, chb + 2 * step + ld);
+                        load_ahead(kB1, chb + 2 * step + ld);
                         compute(kB2, chb + 2 * step);
+                    }
+                    if constexpr (NBUF == 4) {
+                        if (chb + 3 * step >= nch) break;
+                        load_ahead(kB2, chb + 3 * step + ld);
+                        compute(kB3, chb + 3 * step);
                     }
                 }
             }
@@ -478,18 +547,22 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
     grid_dep_launch();
 }
 
-template <int CK, int BMODE, int OUTMODE, int NPROJ>
+template <int CK, int BMODE, int OUTMODE, int NPROJ, bool RING = false>
 void launch_t(const GemvArgs& a, int max_work, cudaStream_t s, const char* name) {
-    auto kern = gemv_kernel<CK, BMODE, OUTMODE, NPROJ>;
+    auto kern = gemv_kernel<CK, BMODE, OUTMODE, NPROJ, RING>;
     static int per_sm = 0;
     if (per_sm == 0) {
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gemv_smem_bytes(12288));
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(RING ? gemv_smem_bytes(9216) + ring_bytes() : gemv_smem_bytes(12288)));
         int v = 0;
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kern, kThreads, gemv_smem_bytes(4096));
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kern, kThreads,
+                                                      RING ? gemv_smem_bytes(1536) + ring_bytes() : gemv_smem_bytes(4096));
         per_sm = v > 0 ? v : 1;
     }
-    const size_t smem = gemv_smem_bytes(a.K);
-    const int occ = smem > gemv_smem_bytes(4096) ? 1 : per_sm;
+    // the ring kernel runs two CTAs per SM (ring_fits), the others two while
+    // the row stage is at most 64 KB
+    const size_t smem = gemv_smem_bytes(a.K) + (RING ? ring_bytes() : 0);
+    const int occ = RING ? std::min(per_sm, 2) : (smem > gemv_smem_bytes(4096) ? 1 : per_sm);
     const int grid = std::max(1, std::min(max_work, occ * num_sms()));
     NVFP4_LAUNCH(name, s, launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, a));
 }
@@ -499,11 +572,19 @@ void launch_ck(int bmode, int outmode, const GemvArgs& a, int max_work, cudaStre
     const bool two = a.nproj == 2;
     if (bmode == B_BF16) {
         if (outmode == OUT_H && two) return launch_t<CK, B_BF16, OUT_H, 2>(a, max_work, s, "gemv_gateup_w4a16");
-        if (outmode == OUT_COMBINE) return launch_t<CK, B_BF16, OUT_COMBINE, 1>(a, max_work, s, "gemv_down_w4a16");
+        if (outmode == OUT_COMBINE) {
+            if (CK == 256 && ring_fits(a.K))
+                return launch_t<CK, B_BF16, OUT_COMBINE, 1, CK == 256>(a, max_work, s, "gemv_down_w4a16");
+            return launch_t<CK, B_BF16, OUT_COMBINE, 1>(a, max_work, s, "gemv_down_w4a16");
+        }
         if (outmode == OUT_BF16) return launch_t<CK, B_BF16, OUT_BF16, 1>(a, max_work, s, "gemv_linear_w4a16");
     } else {
         if (outmode == OUT_HQ && two) return launch_t<CK, B_NVFP4, OUT_HQ, 2>(a, max_work, s, "gemv_gateup_w4a4");
-        if (outmode == OUT_COMBINE) return launch_t<CK, B_NVFP4, OUT_COMBINE, 1>(a, max_work, s, "gemv_down_w4a4");
+        if (outmode == OUT_COMBINE) {
+            if (CK == 256 && ring_fits(a.K))
+                return launch_t<CK, B_NVFP4, OUT_COMBINE, 1, CK == 256>(a, max_work, s, "gemv_down_w4a4");
+            return launch_t<CK, B_NVFP4, OUT_COMBINE, 1>(a, max_work, s, "gemv_down_w4a4");
+        }
     }
 }
 
