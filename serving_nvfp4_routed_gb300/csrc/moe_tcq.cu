@@ -388,10 +388,14 @@ __global__ void __launch_bounds__(kThreads, 1) tcq_kernel(const __grid_constant_
 }
 
 // out[t][f] = bf16(sum_j w[t*k + j] * y[slot_to_row[t*k + j]][f]), the
-// fp32 sum in slot order over bf16 y rows; 8 features per thread.
+// fp32 sum in slot order over bf16 y rows; 8 features per thread.  KT = k
+// at compile time (0: any k): all of a token's row loads are then in flight
+// together.
+template <int KT>
 __global__ void sum_rows_kernel(const uint16_t* __restrict__ y, const int32_t* __restrict__ slot_to_row,
-                                const float* __restrict__ topk_w, int T, int k, int d, uint16_t* __restrict__ out) {
+                                const float* __restrict__ topk_w, int T, int k_rt, int d, uint16_t* __restrict__ out) {
     grid_dep_wait();
+    const int k = KT > 0 ? KT : k_rt;
     const int per_row = d / 8;
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < (size_t)T * per_row;
          i += (size_t)gridDim.x * blockDim.x) {
@@ -399,15 +403,29 @@ __global__ void sum_rows_kernel(const uint16_t* __restrict__ y, const int32_t* _
         float acc[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
-        for (int j = 0; j < k; ++j) {
-            const size_t r = (size_t)slot_to_row[t * k + j];
-            const float wj = topk_w[t * k + j];
-            const uint4 p = __ldcs(reinterpret_cast<const uint4*>(y + r * d + f));
+        auto add = [&](const uint4 p, float wj) {
             const uint32_t pw[4] = {p.x, p.y, p.z, p.w};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 acc[2 * q] += wj * bf16_bits_to_f32(pw[q] & 0xFFFFu);
                 acc[2 * q + 1] += wj * bf16_bits_to_f32(pw[q] >> 16);
+            }
+        };
+        if constexpr (KT > 0) {
+            uint4 p[KT];
+            float wv[KT];
+#pragma unroll
+            for (int j = 0; j < KT; ++j) {
+                const size_t r = (size_t)slot_to_row[t * KT + j];
+                wv[j] = topk_w[t * KT + j];
+                p[j] = __ldcs(reinterpret_cast<const uint4*>(y + r * d + f));
+            }
+#pragma unroll
+            for (int j = 0; j < KT; ++j) add(p[j], wv[j]);
+        } else {
+            for (int j = 0; j < k; ++j) {
+                const size_t r = (size_t)slot_to_row[t * k + j];
+                add(__ldcs(reinterpret_cast<const uint4*>(y + r * d + f)), topk_w[t * k + j]);
             }
         }
         uint4 o;
@@ -463,8 +481,13 @@ void launch_sum_rows(const uint16_t* y, const int32_t* slot_to_row, const float*
     const size_t n = (size_t)T * (d / 8);
     if (n == 0) return;
     const int grid = (int)std::min<size_t>((n + 255) / 256, (size_t)num_sms() * 8);
-    NVFP4_LAUNCH("sum_rows", s, launch_pdl(sum_rows_kernel, dim3(grid), dim3(256), 0, s, y, slot_to_row, topk_w, T, k,
-                                           d, out));
+    if (k == 8) {
+        NVFP4_LAUNCH("sum_rows", s, launch_pdl(sum_rows_kernel<8>, dim3(grid), dim3(256), 0, s, y, slot_to_row, topk_w,
+                                               T, k, d, out));
+    } else {
+        NVFP4_LAUNCH("sum_rows", s, launch_pdl(sum_rows_kernel<0>, dim3(grid), dim3(256), 0, s, y, slot_to_row, topk_w,
+                                               T, k, d, out));
+    }
 }
 
 }  // namespace nvfp4
