@@ -85,6 +85,12 @@ struct GemvArgs {
     uint16_t* out_bf16;             // OUT_COMBINE: [T, N] final bf16 rows
     uint16_t* y_out;                // OUT_BF16: [R, N]
     int* work_counter;              // zeroed before the launch
+    // L2 prefetch of the weight tiles ahead of the loads (gate/up, K not
+    // split over warps): one TMA tensor prefetch per projection, codes and
+    // scales, of the CTA's feature rows (boxes of 128 / 16 bytes x 128 rows),
+    // pf_dist chunks ahead (0: off)
+    CUtensorMap pf_codes[2], pf_scales[2];
+    int pf_dist;
 };
 
 // ksplit chosen from the expected number of work items

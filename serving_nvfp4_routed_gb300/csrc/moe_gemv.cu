@@ -115,7 +115,7 @@ struct Item {
 };
 
 template <int CK, int BMODE, int OUTMODE, int NPROJ, bool RING = false>
-__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant__ GemvArgs a) {
     using C = Chunk<CK>;
     // U chunks form a batch of weight loads; NBUF batches live in registers
     // as a ring, so that NBUF - 1 batches are in flight while one is consumed
@@ -173,6 +173,20 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
         it.nrows = min(kGemvTokTile, a.offsets[it.e + 1] - it.row0);
     };
 
+    // L2 prefetch (one thread, gate/up, K not split): chunk ch of the item's
+    // feature rows, both projections, codes and scales
+    auto l2_prefetch = [&](const Item& it, int ch) {
+        if constexpr (NPROJ == 2 && CK == 256) {
+            if (ch < nch) {
+                const int y = it.e * a.N + it.fb * FB;
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                    tc::tma_prefetch_2d(&a.pf_codes[p], ch * (CK / 2), y);
+                    tc::tma_prefetch_2d(&a.pf_scales[p], ch * (CK / 16), y);
+                }
+            }
+        }
+    };
     uint32_t acw[kRing ? 1 : NBUF][U][NPROJ][2][C::CW];
     uint32_t asw[kRing ? 1 : NBUF][U][NPROJ][2];
     // ring slot b of this warp: codes [row half][lane][32 B] (the two 16-byte
@@ -203,6 +217,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
             }
             tc::cp_async_commit();
         } else {
+            if (a.pf_dist > 0 && tid == 0) l2_prefetch(it, chb + a.pf_dist);
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int ch = chb + u * KSPL;
@@ -234,6 +249,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
     Item cur{};
     if (item < total) {
         decode(item, cur);
+        if (a.pf_dist > 0 && tid == 0)
+            for (int ch = 1; ch <= a.pf_dist; ++ch) l2_prefetch(cur, ch);
         prefetch(cur);
     }
     if constexpr (kEarly) grid_dep_wait();
@@ -403,6 +420,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
                 }
                 if (nitem < total) {
                     decode(nitem, nxt);
+                    if (a.pf_dist > 0 && tid == 0)
+                        for (int ch = 1; ch <= a.pf_dist; ++ch) l2_prefetch(nxt, ch);
                     prefetch(nxt);
                 }
             }

@@ -108,6 +108,12 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int 
         : "memory");
 }
 
+// L2 prefetch of one box of a tensor map (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_2d(const void* tmap, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(tmap), "r"(x), "r"(y)
+                 : "memory");
+}
+
 // ---- thread-block clusters: distributed shared memory ----
 // The address of `local` (this CTA's shared memory) in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t dsmem_addr(uint32_t local, uint32_t rank) {
