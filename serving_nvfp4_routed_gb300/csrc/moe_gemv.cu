@@ -173,14 +173,19 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
         it.nrows = min(kGemvTokTile, a.offsets[it.e + 1] - it.row0);
     };
 
-    // L2 prefetch (one thread, gate/up, K not split): chunk ch of the item's
-    // feature rows, both projections, codes and scales
-    auto l2_prefetch = [&](const Item& it, int ch) {
-        if constexpr (NPROJ == 2 && CK == 256) {
-            if (ch < nch) {
-                const int y = it.e * a.N + it.fb * FB;
+    // L2 prefetch (one thread, K not split over warps): chunk ch of the
+    // item's feature rows of block fb, every projection, codes and scales;
+    // past the block's last chunk, the item's next block
+    auto l2_prefetch = [&](const Item& it, int fb, int ch) {
+        if constexpr (CK == 256) {
+            if (ch >= nch) {
+                ch -= nch;
+                ++fb;
+            }
+            if (ch < nch && fb < it.fb_end) {
+                const int y = it.e * a.N + fb * FB;
 #pragma unroll
-                for (int p = 0; p < 2; ++p) {
+                for (int p = 0; p < NPROJ; ++p) {
                     tc::tma_prefetch_2d(&a.pf_codes[p], ch * (CK / 2), y);
                     tc::tma_prefetch_2d(&a.pf_scales[p], ch * (CK / 16), y);
                 }
@@ -202,6 +207,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
             // one commit group per call, empty past the end, so that a
             // batch is complete once NBUF - 1 later groups were committed
             const int ch = chb;
+            if (a.pf_dist > 0 && tid == 0) l2_prefetch(it, it.fb, chb + a.pf_dist);
             if (ch < nch) {
                 uint8_t* sl = wring + B * kRingSlotBytes;
                 const size_t kb = (size_t)ch * CK + (size_t)c * C::TS;
@@ -217,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
             }
             tc::cp_async_commit();
         } else {
-            if (a.pf_dist > 0 && tid == 0) l2_prefetch(it, chb + a.pf_dist);
+            if (a.pf_dist > 0 && tid == 0) l2_prefetch(it, it.fb, chb + a.pf_dist);
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int ch = chb + u * KSPL;
@@ -250,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
     if (item < total) {
         decode(item, cur);
         if (a.pf_dist > 0 && tid == 0)
-            for (int ch = 1; ch <= a.pf_dist; ++ch) l2_prefetch(cur, ch);
+            for (int ch = 1; ch <= a.pf_dist; ++ch) l2_prefetch(cur, cur.fb, ch);
         prefetch(cur);
     }
     if constexpr (kEarly) grid_dep_wait();
@@ -421,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
                 if (nitem < total) {
                     decode(nitem, nxt);
                     if (a.pf_dist > 0 && tid == 0)
-                        for (int ch = 1; ch <= a.pf_dist; ++ch) l2_prefetch(nxt, ch);
+                        for (int ch = 1; ch <= a.pf_dist; ++ch) l2_prefetch(nxt, nxt.fb, ch);
                     prefetch(nxt);
                 }
             }
