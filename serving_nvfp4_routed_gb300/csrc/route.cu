@@ -67,21 +67,40 @@ __device__ void warp_topk(const float* __restrict__ lg, int E, int k, int32_t* _
             my_id = bi;
         }
     }
-    // fp64: exp(l_j - l_max), summed over the k in slot order, divided, then
-    // rounded once to fp32 (only k exponentials per token).  Non-finite top
-    // logits: +inf entries share the weight equally; all -inf: 1/k each.
-    const float m = __shfl_sync(0xffffffffu, my_v, 0);
-    double ex = 0.0;
-    if (lane < k) {
-        if (m == INFINITY) ex = my_v == INFINITY ? 1.0 : 0.0;
-        else if (m == -INFINITY) ex = 1.0;
-        else ex = exp((double)my_v - (double)m);
-    }
-    double sum = 0.0;
-    for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, ex, j);
+    // the selected logits, in slot order; softmax_weights turns them into
+    // the routing weights
     if (lane < k) {
         ids[lane] = my_id;
-        w[lane] = (float)(ex / sum);
+        w[lane] = my_v;
+    }
+}
+
+// Routing weights of tokens [t0, t1) from their selected logits in w (slot 0
+// holds the largest): fp64 exp(l_j - l_max), summed over the k in slot order,
+// divided, rounded once to fp32.  Non-finite top logits: +inf entries share
+// the weight equally; all -inf: 1/k each.  Each warp takes floor(32 / k)
+// tokens at once (fp64 is slow on this part: a full warp of exponentials
+// instead of k lanes per token), so the calling block passes its warp index
+// and warp count.
+__device__ void softmax_weights(float* w, int t0, int t1, int k, int warp, int n_warps) {
+    const int lane = threadIdx.x & 31;
+    const int tpw = 32 / k;  // tokens per warp pass
+    const int tl = lane / k, j = lane % k;
+    for (int tb = t0 + warp * tpw; tb < t1; tb += n_warps * tpw) {  // warp-uniform trip count
+        const int t = tb + tl;
+        const bool live = tl < tpw && t < t1;
+        double ex = 0.0;
+        float v = 0.0f;
+        if (live) {
+            v = w[(size_t)t * k + j];
+            const float m = w[(size_t)t * k];
+            if (m == INFINITY) ex = v == INFINITY ? 1.0 : 0.0;
+            else if (m == -INFINITY) ex = 1.0;
+            else ex = exp((double)v - (double)m);
+        }
+        double sum = 0.0;
+        for (int jj = 0; jj < k; ++jj) sum += __shfl_sync(0xffffffffu, ex, (tl < tpw ? tl : 0) * k + jj);
+        if (live) w[(size_t)t * k + j] = (float)(ex / sum);
     }
 }
 
@@ -222,7 +241,8 @@ __global__ void __launch_bounds__(1024) route_perm_small_kernel(int T, int E, in
     if (logits) {
         for (int t = threadIdx.x >> 5; t < T; t += blockDim.x >> 5)
             topk_dispatch(logits + (size_t)t * E, E, k, ra.ids + (size_t)t * k, ra.w + (size_t)t * k);
-        __syncthreads();  // the block reads these ids below
+        __syncthreads();  // the block reads these ids and logits below
+        softmax_weights(ra.w, 0, T, k, threadIdx.x >> 5, blockDim.x >> 5);
     }
     if (given_ids) validate_ids(ra.ids, R, E, status);
     for (int i = threadIdx.x; i < E; i += blockDim.x) run[i] = 0;
@@ -243,8 +263,11 @@ __global__ void __launch_bounds__(1024) route_perm_small_kernel(int T, int E, in
 // One warp per token.
 __global__ void topk_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* ids, float* w) {
     grid_dep_wait();
-    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int nw = blockDim.x >> 5;
+    const int t0 = blockIdx.x * nw, t = t0 + (threadIdx.x >> 5);
     if (t < T) topk_dispatch(logits + (size_t)t * E, E, k, ids + (size_t)t * k, w + (size_t)t * k);
+    __syncthreads();  // the block's selected logits are written
+    softmax_weights(w, t0, min(T, t0 + nw), k, threadIdx.x >> 5, nw);
     grid_dep_launch();
 }
 
