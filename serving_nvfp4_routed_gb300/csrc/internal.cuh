@@ -144,7 +144,7 @@ void decode_pick_work(int expected_tiles, DecodeArgs* a);
 void launch_decode(int bmode, const DecodeArgs& a, cudaStream_t s);
 
 // ---- prompt-shaped grouped GEMM (tcgen05, accumulators in TMEM) ----
-enum TcOut { TC_OUT_H = 0, TC_OUT_COMBINE = 1, TC_OUT_BF16 = 2 };
+enum TcOut { TC_OUT_H = 0, TC_OUT_BF16 = 2 };
 
 struct TcArgs {
     int K, N, top_k;
@@ -160,8 +160,6 @@ struct TcArgs {
     const int32_t* b_exp;
     int b_by_token;              // B row = token of the permuted row (x) or the row itself (h)
     uint16_t* h_out;             // TC_OUT_H: [R, N] bf16 SwiGLU
-    float* acc_out;              // TC_OUT_COMBINE: [T, N] fp32, zeroed before
-    const float* topk_w;         // TC_OUT_COMBINE: [T*k]
     uint16_t* y_out;             // TC_OUT_BF16: [R, N]
     int32_t* status;             // optional: NVFP4_ERR_TIMEOUT if a bounded wait expired
 };
@@ -226,11 +224,11 @@ void launch_sum_rows(const uint16_t* y, const int32_t* slot_to_row, const float*
                      uint16_t* out, cudaStream_t s);
 
 size_t tc_smem_bytes(int nproj);
-void launch_tc_gemm(int outmode, int nproj, const TcArgs& a, int max_units, cudaStream_t s);
+void launch_tc_gemm(int outmode, int nproj, const TcArgs& a, int max_units, cudaStream_t s,
+                    bool routed_down = false);
 // dst row r = f16(src row (map ? map[r] / map_div : r) * 2^-s), exps[r] = s;
 // optionally zeroes row r of zero_rows (length zero_len) for r < zero_count.
 void launch_rows_to_f16(const uint16_t* src, int rows, int K, uint16_t* dst, int32_t* exps, float* zero_rows,
                         int zero_len, cudaStream_t s, const int32_t* map = nullptr, int map_div = 1,
                         int zero_count = -1);
-void launch_acc_to_bf16(const float* acc, size_t n, uint16_t* out, cudaStream_t s);
 }  // namespace nvfp4

@@ -39,7 +39,6 @@ struct MoeWs {
     uint8_t* xs;      // [R, d/16]  W4A4
     uint8_t* hq;      // [R, F/2]   W4A4
     uint8_t* hs;      // [R, F/16]  W4A4
-    float* acc;       // [T, d]
     float* yrows;     // [R, d]: w * y fp32 rows (decode kernel) or bf16 y rows (prompt paths)
     int* clear;       // zeroed by the route launch (decode-shaped paths): work counters, then
                       // per-tile and per-(token, output group) completion counters
@@ -108,7 +107,6 @@ MoeWs carve_moe(void* base, int T, int E, int k, int d, int F, int mode, size_t*
     w.ra.n_clear = (int)n_clear;
     w.tile_ready = w.clear + kCounters;
     w.tok_done = w.tile_ready + max_tiles;
-    w.acc = c.take<float>((size_t)T * d);
     w.yrows = c.take<float>(R * d);
     if (mode == 0) {
         w.h = c.take<uint16_t>(R * F);
@@ -243,7 +241,7 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
         // fp32 accumulator
         const bool rows = tcm_supported(TCM_ROWS, d, F);
         // x -> f16 rows in expert order (and zero the combine accumulator)
-        launch_rows_to_f16(x, R, d, ws.xp, ws.xp_exp, rows ? nullptr : ws.acc, d, s, ws.ra.row_to_slot, top_k, T);
+        launch_rows_to_f16(x, R, d, ws.xp, ws.xp_exp, nullptr, d, s, ws.ra.row_to_slot, top_k, T);
         const int max_tiles = R / kTcTokTile + std::min(E, R) + 1;
         // gate/up + SwiGLU -> h (bf16)
         TcmArgs g{};
@@ -308,7 +306,6 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
             u.n_active = ws.ra.n_active;
             u.tile_start = ws.ra.tile_start_tc;
             u.row_to_slot = ws.ra.row_to_slot;
-            u.topk_w = ws.ra.w;
             u.status = d_status;
             u.K = F;
             u.N = d;
@@ -317,10 +314,11 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
             u.b_f16 = ws.hh;
             u.b_exp = ws.h_exp;
             u.b_by_token = 0;
-            u.acc_out = ws.acc;
-            launch_tc_gemm(TC_OUT_COMBINE, 1, u, max_tiles * (d / 128), s);
+            // y in bf16 by routed row, then each token's rows in slot order
+            u.y_out = reinterpret_cast<uint16_t*>(ws.yrows);
+            launch_tc_gemm(TC_OUT_BF16, 1, u, max_tiles * (d / 128), s, true);
+            launch_sum_rows(u.y_out, ws.ra.slot_to_row, ws.ra.w, T, top_k, d, out, s);
         }
-        launch_acc_to_bf16(ws.acc, (size_t)T * d, out, s);
         return last_launch_status();
     }
 

@@ -20,8 +20,9 @@
 //    layout.  Both operands flow through mbarrier-guarded stage rings.
 // One thread issues tcgen05.mma kind::f16 (M=128, N=128, K=16, A from
 // TMEM) into fp32 accumulators in TMEM; four epilogue warps (one TMEM lane
-// quarter each) read them with tcgen05.ld and apply SwiGLU, the weighted
-// combine (red.add) or a plain bf16 store.
+// quarter each) read them with tcgen05.ld and apply SwiGLU or store bf16
+// rows (the routed layer's down projection: y by routed row, summed per
+// token in slot order by a second kernel).
 // Every mbarrier wait is bounded (about 2 s): on expiry the kernel records
 // NVFP4_ERR_TIMEOUT in the status word, every role leaves its loop, and the
 // CTA still frees its tensor memory before it exits.
@@ -99,8 +100,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const TcArgs a) 
     __shared__ int s_abort;
     __shared__ int s_brow[BN];
     __shared__ float s_rs[2][BN];   // epilogue: 2^exp of the column's B row (0 if the column is empty)
-    __shared__ int s_tok[2][BN];    // epilogue: token of the column (combine)
-    __shared__ float s_wt[2][BN];   // epilogue: routing weight of the column (combine)
 
     grid_dep_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -207,19 +206,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const TcArgs a) 
             const int acc = it % NACC;       // accumulator buffer
             {   // per-column row data of this unit, one column per thread
                 const int row = un.row0 + et;
-                float rs = 0.0f, wt = 0.0f;
-                int tok = 0;
-                if (row < un.row_end) {
-                    rs = exp2i(a.b_exp[brow_of(a, row)]);
-                    if constexpr (OUT == TC_OUT_COMBINE) {
-                        const int slot = a.row_to_slot[row];
-                        tok = slot / a.top_k;
-                        wt = a.topk_w[slot];
-                    }
-                }
+                float rs = 0.0f;
+                if (row < un.row_end) rs = exp2i(a.b_exp[brow_of(a, row)]);
                 s_rs[as][et] = rs;
-                s_tok[as][et] = tok;
-                s_wt[as][et] = wt;
             }
             named_bar(1, 128);
             if (!warp_wait(smem_u32(&bar_acc_full[acc]), (it / NACC) & 1, abort_flag, a.status, 128)) break;
@@ -246,9 +235,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const TcArgs a) 
                         const float U = round_bf16(__fmul_rn(__fmul_rn(__uint_as_float(r1[j]), rs), w1));
                         const float h = round_bf16(G / (1.0f + expf(-G)) * U);
                         a.h_out[(size_t)row * a.N + f] = f32_to_bf16_bits(h);
-                    } else if constexpr (OUT == TC_OUT_COMBINE) {
-                        const float y = __fmul_rn(__fmul_rn(__uint_as_float(r0[j]), rs), w0);
-                        atomicAdd(a.acc_out + (size_t)s_tok[as][col] * a.N + f, s_wt[as][col] * y);
                     } else {
                         a.y_out[(size_t)row * a.N + f] =
                             f32_to_bf16_bits(__fmul_rn(__fmul_rn(__uint_as_float(r0[j]), rs), w0));
@@ -469,26 +455,15 @@ __global__ void __launch_bounds__(kRowWarps * 32) rows_to_f16_warp_kernel(
     grid_dep_launch();
 }
 
-__global__ void acc_to_bf16_kernel(const float* __restrict__ acc, size_t n4, uint16_t* __restrict__ out) {
-    grid_dep_wait();
-    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
-        const float4 v = reinterpret_cast<const float4*>(acc)[i];
-        uint2 o;
-        o.x = (uint32_t)f32_to_bf16_bits(v.x) | ((uint32_t)f32_to_bf16_bits(v.y) << 16);
-        o.y = (uint32_t)f32_to_bf16_bits(v.z) | ((uint32_t)f32_to_bf16_bits(v.w) << 16);
-        reinterpret_cast<uint2*>(out)[i] = o;
-    }
-    grid_dep_launch();
-}
 
 }  // namespace
 
 size_t tc_smem_bytes(int nproj) { return nproj == 2 ? Cfg<2>::kSmem : Cfg<1>::kSmem; }
 
-void launch_tc_gemm(int outmode, int nproj, const TcArgs& a, int max_units, cudaStream_t s) {
+void launch_tc_gemm(int outmode, int nproj, const TcArgs& a, int max_units, cudaStream_t s, bool routed_down) {
     if (outmode == TC_OUT_H && nproj == 2) return launch_tc_t<TC_OUT_H, 2>(a, max_units, s, "tc_gateup_w4a16");
-    if (outmode == TC_OUT_COMBINE) return launch_tc_t<TC_OUT_COMBINE, 1>(a, max_units, s, "tc_down_w4a16");
-    if (outmode == TC_OUT_BF16) return launch_tc_t<TC_OUT_BF16, 1>(a, max_units, s, "tc_linear_w4a16");
+    if (outmode == TC_OUT_BF16)
+        return launch_tc_t<TC_OUT_BF16, 1>(a, max_units, s, routed_down ? "tc_down_w4a16" : "tc_linear_w4a16");
 }
 
 void launch_rows_to_f16(const uint16_t* src, int rows, int K, uint16_t* dst, int32_t* exps, float* zero_rows,
@@ -508,11 +483,5 @@ void launch_rows_to_f16(const uint16_t* src, int rows, int K, uint16_t* dst, int
                             zero_len, map, map_div, zero_count));
 }
 
-void launch_acc_to_bf16(const float* acc, size_t n, uint16_t* out, cudaStream_t s) {
-    const size_t n4 = n / 4;
-    if (n4 == 0) return;
-    const int grid = (int)std::min<size_t>((n4 + 255) / 256, (size_t)num_sms() * 8);
-    NVFP4_LAUNCH("acc_to_bf16", s, launch_pdl(acc_to_bf16_kernel, dim3(grid), dim3(256), 0, s, acc, n4, out));
-}
 
 }  // namespace nvfp4
