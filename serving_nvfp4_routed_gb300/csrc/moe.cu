@@ -367,13 +367,16 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
     a.a_codes[0] = w->gate.codes;  a.a_scales[0] = w->gate.scales;  a.a_ws2[0] = w->gate.weight_scale_2;
     a.a_codes[1] = w->up.codes;    a.a_scales[1] = w->up.scales;    a.a_ws2[1] = w->up.weight_scale_2;
     a.work_counter = ws.clear + 0;
-    if (a.ksplit == 1 && d % 256 == 0) {
-        // L2 prefetch of the CTA's 128 feature rows, kGemvPrefetch chunks ahead
+    if (d % 256 == 0 && a.ksplit == 1) {
+        // L2 prefetch of the CTA's feature rows (16 x 8 / ksplit of them),
+        // kGemvPrefetch of each warp's chunks ahead (measured slower when K
+        // is split over warps: the few-token shapes)
         const unsigned long long rows = (unsigned long long)E * F;
+        const unsigned fb_rows = 16u * (8u / (unsigned)a.ksplit);
         bool ok = true;
         for (int p = 0; p < 2 && ok; ++p)
-            ok = encode_tmap_u8(&a.pf_codes[p], a.a_codes[p], d / 2, rows, 128, 128, false) &&
-                 encode_tmap_u8(&a.pf_scales[p], a.a_scales[p], d / 16, rows, 16, 128, false);
+            ok = encode_tmap_u8(&a.pf_codes[p], a.a_codes[p], d / 2, rows, 128, fb_rows, false) &&
+                 encode_tmap_u8(&a.pf_scales[p], a.a_scales[p], d / 16, rows, 16, fb_rows, false);
         a.pf_dist = ok ? kGemvPrefetch : 0;
     }
     if (mode == 0) {

@@ -223,7 +223,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
             }
             tc::cp_async_commit();
         } else {
-            if (a.pf_dist > 0 && tid == 0) l2_prefetch(it, it.fb, chb + a.pf_dist);
+            // (warp 0 takes chunks 0, KSPL, ...: the CTA's chunks at that
+            // distance are the KSPL consecutive ones)
+            if (a.pf_dist > 0 && tid == 0)
+                for (int q = 0; q < KSPL; ++q) l2_prefetch(it, it.fb, chb + a.pf_dist * KSPL + q);
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int ch = chb + u * KSPL;
@@ -256,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
     if (item < total) {
         decode(item, cur);
         if (a.pf_dist > 0 && tid == 0)
-            for (int ch = 1; ch <= a.pf_dist; ++ch) l2_prefetch(cur, cur.fb, ch);
+            for (int ch = KSPL; ch < (a.pf_dist + 1) * KSPL; ++ch) l2_prefetch(cur, cur.fb, ch);
         prefetch(cur);
     }
     if constexpr (kEarly) grid_dep_wait();
@@ -427,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
                 if (nitem < total) {
                     decode(nitem, nxt);
                     if (a.pf_dist > 0 && tid == 0)
-                        for (int ch = 1; ch <= a.pf_dist; ++ch) l2_prefetch(nxt, nxt.fb, ch);
+                        for (int ch = KSPL; ch < (a.pf_dist + 1) * KSPL; ++ch) l2_prefetch(nxt, nxt.fb, ch);
                     prefetch(nxt);
                 }
             }
