@@ -168,11 +168,11 @@ def peaks():
 
 
 KERNEL_SOURCES = {
-    "gemv": ("moe_gemv.cu", "common.cuh", "internal.cuh"),
-    "decode": ("moe_decode.cu", "tc_ptx.cuh", "common.cuh", "internal.cuh"),
-    "tc": ("moe_tc.cu", "tc_ptx.cuh", "common.cuh", "internal.cuh"),
-    "tcm": ("moe_tcm.cu", "tc_ptx.cuh", "common.cuh", "internal.cuh"),
-    "tcq": ("moe_tcq.cu", "tc_ptx.cuh", "common.cuh", "internal.cuh"),
+    "gemv": ("moe_gemv.cu", "gemv.cuh", "tc_ptx.cuh", "common.cuh", "internal.cuh"),
+    "decode": ("moe_decode.cu", "decode.cuh", "tc_ptx.cuh", "common.cuh", "internal.cuh"),
+    "tc": ("moe_tc.cu", "tc.cuh", "tc_ptx.cuh", "common.cuh", "internal.cuh"),
+    "tcm": ("moe_tcm.cu", "tc.cuh", "tc_ptx.cuh", "common.cuh", "internal.cuh"),
+    "tcq": ("moe_tcq.cu", "tc.cuh", "tc_ptx.cuh", "common.cuh", "internal.cuh"),
 }
 # nominal dense FP4 : BF16 tensor rate (13.5 : 2.25 PFLOP/s); the FP4 peak is
 # the measured bf16 peak times this ratio

@@ -21,6 +21,9 @@
 
 #include "common.cuh"
 #include "internal.cuh"
+#include "gemv.cuh"
+#include "decode.cuh"
+#include "tc.cuh"
 
 namespace nvfp4 {
 

@@ -43,7 +43,7 @@
 // Every wait is bounded (about 2 s) and reports NVFP4_ERR_TIMEOUT; the
 // producer then waits (bounded) for its copies in flight before it exits.
 #include "common.cuh"
-#include "internal.cuh"
+#include "decode.cuh"
 #include "tc_ptx.cuh"
 
 namespace nvfp4 {

@@ -35,7 +35,7 @@
 #include <type_traits>
 
 #include "common.cuh"
-#include "internal.cuh"
+#include "gemv.cuh"
 #include "tc_ptx.cuh"
 
 namespace nvfp4 {

@@ -27,7 +27,7 @@
 // NVFP4_ERR_TIMEOUT in the status word, every role leaves its loop, and the
 // CTA still frees its tensor memory before it exits.
 #include "common.cuh"
-#include "internal.cuh"
+#include "tc.cuh"
 #include "tc_ptx.cuh"
 
 namespace nvfp4 {

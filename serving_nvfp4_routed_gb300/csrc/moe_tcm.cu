@@ -38,7 +38,7 @@
 #include <mutex>
 
 #include "common.cuh"
-#include "internal.cuh"
+#include "tc.cuh"
 #include "tc_ptx.cuh"
 
 namespace nvfp4 {

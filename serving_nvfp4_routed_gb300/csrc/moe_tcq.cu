@@ -42,7 +42,7 @@
 // the columns per thread).  mbarrier waits are bounded (about 2 s) and
 // report NVFP4_ERR_TIMEOUT.
 #include "common.cuh"
-#include "internal.cuh"
+#include "tc.cuh"
 #include "tc_ptx.cuh"
 
 namespace nvfp4 {
