@@ -6,21 +6,30 @@
 // to the NVFP4 routed experts; "What the branch does": the shared expert runs
 // as a BF16 MLP.  It runs on every token, so it is two dense GEMMs.
 //
-// Both GEMMs: one CTA per (128 tokens, NT output columns) tile, NT = 256,
-// or 64 when the 256-wide tiles would leave most SMs idle (a decode batch:
-// the weights are then spread over 4x as many CTAs); when even that leaves
-// SMs idle, K is split over a thread-block cluster of KS <= 8 CTAs, which
-// store their fp32 partial tiles in shared memory and, after a cluster
-// barrier, sum them in rank order through distributed shared memory, each
-// CTA for a slice of the tile's rows (deterministic, no workspace);
-// tcgen05.mma kind::f16 with bf16 A (rows) and bf16 B (weight rows) exactly
-// as stored, both moved by TMA (128-byte swizzle, k-stages of 64, a ring of
-// 4), M=128, N=NT, an fp32 accumulator in tensor memory.  Gate/up tile:
-// B rows 0..NT/2-1 = Wg rows f0.., NT/2..NT-1 = Wu rows f0.., so a token's gate
-// and up values for a feature share one TMEM lane and the SwiGLU is local
-// to the thread.  Warp 0 runs the MMA loop (one elected lane issues), warp
-// 1's lane 0 the TMA ring, warps 4-7 the epilogue (one token per lane).
-// mbarrier waits are bounded and report NVFP4_ERR_TIMEOUT.
+// Both GEMMs run on tcgen05.mma kind::f16 with bf16 operands exactly as
+// stored, moved by TMA (128-byte swizzle, k-stages of 64), an fp32
+// accumulator in tensor memory; warp 0 runs the MMA loop (one elected lane
+// issues), warp 1's lane 0 the TMA ring, warps 4-7 the epilogue.  mbarrier
+// waits are bounded and report NVFP4_ERR_TIMEOUT.
+//
+// Wide tiles (a prompt batch): one CTA per (128 tokens, 256 output columns)
+// tile, the tokens as the MMA's M and the weight rows as N (gate/up: B rows
+// 0..127 = Wg rows f0.., 128..255 = Wu rows f0.., so a token's gate and up
+// values for a feature share one TMEM lane and the SwiGLU is local to the
+// thread); a ring of 4 stages.
+//
+// Narrow tiles (a decode batch, whose 256-wide tiles would leave most SMs
+// idle): the weight rows are the MMA's M (128 rows: 64 gate + 64 up rows of
+// 64 features, or 128 down rows) and up to 128 tokens its N, so that a
+// stage carries 16 KB of weights next to the token rows and a deep ring
+// keeps ~150 KB of weights in flight per SM.  K is split over a
+// thread-block cluster of up to 8 CTAs (the widest split whose clusters are
+// all resident at once); each CTA stores its fp32 partial tile in shared
+// memory (over its drained ring) and, after a cluster barrier, the CTAs sum
+// the partials in rank order through distributed shared memory, each for a
+// slice of the tile's outputs (deterministic, no workspace).  The down
+// launch issues its first weight stages before it waits for the gate/up
+// launch (only the h rows depend on it).
 #include "common.cuh"
 #include "internal.cuh"
 #include "tc_ptx.cuh"
@@ -31,31 +40,36 @@ namespace {
 
 using namespace tc;
 
-constexpr int SM_ = 128;        // tokens per tile (MMA M)
-constexpr int SN = 256;         // widest tile (MMA N); shape rules refer to it
+constexpr int SM_ = 128;        // wide tiles: tokens per tile (MMA M); narrow tiles: weight rows (MMA M)
+constexpr int SN = 256;         // wide tiles: output columns per tile (MMA N); shape rules refer to it
 constexpr int SKS = 64;         // k per stage (128 bytes of bf16)
-constexpr int kSA = SM_ * SKS * 2;   // 16 KB
-// Stage ring: 4 deep for the 256-wide tiles; 8 deep for the 64-wide ones
-// (a decode batch), whose stages carry only 8 KB of weights next to the
-// 16 KB row tile, so that enough weight bytes are in flight per SM.
-template <int NT>
-struct SGeo {
-    static constexpr int kSB = NT * SKS * 2;
-    static constexpr int kStage = kSA + kSB;
-    static constexpr int SS = NT <= 64 ? 8 : 4;
-    static constexpr int kPart = SM_ * (NT + 1) * 4;        // fp32 partial tile (split K), padded rows
-    static constexpr int kSmem = 1024 + SS * kStage + (NT <= 64 ? kPart : 0);
-};
-constexpr int kMaxClusterSplit = 8;
+constexpr int kSA = SM_ * SKS * 2;   // 16 KB: the M-side operand of a stage
+constexpr int kSB = SN * SKS * 2;    // 32 KB: the wide tiles' weight rows of a stage
+constexpr int kWideStages = 4;
+constexpr int kWideSmem = 1024 + kWideStages * (kSA + kSB);
 constexpr int kSThreads = 256;
 enum { SH_SWIGLU = 0, SH_ADD = 1 };
 
+// Narrow tiles: ring stages of 16 KB of weights + NB token rows, as many as
+// fit in kNarrowRing (at most kNarrowMaxStages); the fp32 partial tile
+// [128][NB + 1] reuses the ring once the MMAs are done.
+constexpr int kNarrowMaxStages = 12;
+constexpr int kNarrowRing = 216 * 1024;
+constexpr int kNarrowSmemMax = 1024 + kNarrowRing;
+constexpr int kMaxClusterSplit = 8;
+__host__ __device__ constexpr int narrow_stage_bytes(int nb) { return kSA + nb * SKS * 2; }
+
 struct SharedArgs {
-    CUtensorMap tmap_a, tmap_b0, tmap_b1;  // A rows; B rows (gate/up: two maps; down: one map, two boxes)
+    CUtensorMap tmap_a, tmap_b0, tmap_b1;  // wide: A token rows, B weight rows (gate/up: two maps; down: one map,
+                                           // two boxes); narrow: A weight rows (gate/up: gate, up; down: b0),
+                                           // B token rows in tmap_a
     int T, K, N;                           // N: h features (gate/up) or d (down)
-    int ksplit;                            // CTAs of a cluster splitting K (1: no cluster)
-    int a_rows;                            // rows of the A box: T rounded up to 8, at most 128
-                                           // (the MMA's other rows hold stale data and are never stored)
+    int a_rows;                            // wide: rows of the token box (T rounded up to 8, at most 128; the
+                                           // MMA's other rows hold stale data and are never stored)
+    int nb;                                // narrow: tokens per tile (MMA N: 16, 32, 64 or 128)
+    int t_tiles;                           // narrow: token tiles
+    int ss;                                // narrow: ring stages
+    int ksplit;                            // narrow: CTAs of a cluster splitting K (1: no cluster)
     uint16_t* out;                         // gate/up: h [T, N]; down: out [T, N] (read and written)
     int32_t* status;
 };
@@ -65,14 +79,22 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-template <int EPI, int NT>
-__global__ void __launch_bounds__(kSThreads, 1) shared_kernel(const __grid_constant__ SharedArgs a) {
-    constexpr int kSB = SGeo<NT>::kSB, kSStage = SGeo<NT>::kStage, SS = SGeo<NT>::SS;
+// A bounded wait for a TMA copy still in flight when a CTA gives up, so that
+// no copy lands in the shared memory of a later CTA.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (!mbar_try(bar, parity) && clock64() - t0 < kWaitCycles) {
+    }
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kSThreads, 1) shared_wide_kernel(const __grid_constant__ SharedArgs a) {
+    constexpr int SS = kWideStages, NT = SN, kStage = kSA + kSB;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(8) uint64_t bar_full[SS], bar_done[SS], bar_acc;
     __shared__ uint32_t s_tmem;
-    __shared__ int s_abort;
+    __shared__ int s_abort, s_consumed, s_issued;
 
     grid_dep_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -83,6 +105,8 @@ __global__ void __launch_bounds__(kSThreads, 1) shared_kernel(const __grid_const
         }
         mbar_init(smem_u32(&bar_acc), 1);
         s_abort = 0;
+        s_consumed = 0;
+        s_issued = 0;
         mbar_fence_init();
     }
     if (warp == 0) tmem_alloc(smem_u32(&s_tmem), NT);
@@ -91,25 +115,20 @@ __global__ void __launch_bounds__(kSThreads, 1) shared_kernel(const __grid_const
     tc_fence_after();
     const uint32_t tmem = s_tmem;
     volatile int* abort_flag = &s_abort;
-    // CTAs of one cluster (k slices) are adjacent, then the tiles of one token block
-    const int KS = a.ksplit;
-    const int ks = blockIdx.x % KS, tile = blockIdx.x / KS;
-    const int nk_all = a.K / SKS;
-    const int kc0 = ks * nk_all / KS, nk = (ks + 1) * nk_all / KS - kc0;  // this CTA's k-stages
+    const int nk = a.K / SKS;
     constexpr int kCols = EPI == SH_SWIGLU ? NT / 2 : NT;  // output columns per tile
     const int n_tiles = a.N / kCols;
-    const int t0 = (tile / n_tiles) * SM_;  // tiles of one token block are adjacent (A stays in L2)
-    const int c0 = (tile % n_tiles) * kCols;
-    float* part = reinterpret_cast<float*>(smem + SS * kSStage);  // [SM_][NT + 1] when KS > 1
+    const int t0 = (blockIdx.x / n_tiles) * SM_;  // tiles of one token block are adjacent (A stays in L2)
+    const int c0 = (blockIdx.x % n_tiles) * kCols;
 
     if (warp == 0) {
         // ---------------- MMA: warp-uniform loop, one elected lane issues ----------------
-        int s = 0;
+        int s = 0, kc = 0;
         uint32_t par = 0;
-        for (int kc = 0; kc < nk; ++kc) {
+        for (; kc < nk; ++kc) {
             if (!warp_wait(smem_u32(&bar_full[s]), par, abort_flag, a.status)) break;
             tc_fence_after();
-            const uint32_t sa = smem_u32(smem + s * kSStage), sb = sa + kSA;
+            const uint32_t sa = smem_u32(smem + s * kStage), sb = sa + kSA;
             if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < SKS / 16; ++kk)
@@ -123,20 +142,22 @@ __global__ void __launch_bounds__(kSThreads, 1) shared_kernel(const __grid_const
                 par ^= 1;
             }
         }
+        if (lane == 0) s_consumed = kc;
         if (elect_one()) mma_commit(smem_u32(&bar_acc));
         __syncwarp();
     } else if (warp == 1) {
         // ---------------- operands by TMA (one thread) ----------------
         if (lane == 0) {
-            for (int kc = 0; kc < nk; ++kc) {
+            int kc = 0;
+            for (; kc < nk; ++kc) {
                 const int s = kc % SS;
                 if (kc >= SS &&
                     !mbar_wait(smem_u32(&bar_done[s]), (uint32_t)(((kc - SS) / SS) & 1), abort_flag, a.status))
                     break;
                 const uint32_t bar = smem_u32(&bar_full[s]);
-                const uint32_t dst = smem_u32(smem + s * kSStage);
+                const uint32_t dst = smem_u32(smem + s * kStage);
                 mbar_arrive_expect_tx(bar, (uint32_t)(a.a_rows * SKS * 2 + kSB));
-                const int kx = (kc0 + kc) * (SKS * 2);
+                const int kx = kc * (SKS * 2);
                 tma_load_2d(dst, &a.tmap_a, kx, t0, bar);
                 if (EPI == SH_SWIGLU) {
                     tma_load_2d(dst + kSA, &a.tmap_b0, kx, c0, bar);
@@ -146,6 +167,7 @@ __global__ void __launch_bounds__(kSThreads, 1) shared_kernel(const __grid_const
                     tma_load_2d(dst + kSA + kSB / 2, &a.tmap_b0, kx, c0 + NT / 2, bar);
                 }
             }
+            s_issued = kc;
         }
         __syncwarp();
     } else if (warp >= 4) {
@@ -155,16 +177,7 @@ __global__ void __launch_bounds__(kSThreads, 1) shared_kernel(const __grid_const
         if (warp_wait(smem_u32(&bar_acc), 0, abort_flag, a.status, 64)) {
             tc_fence_after();
             const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16);
-            if (NT <= 64 && KS > 1) {
-                // the partial tile, one padded row per lane (no bank conflicts)
-                for (int cb = 0; cb < NT; cb += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(tb + cb, r);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) part[(q * 32 + lane) * (NT + 1) + cb + j] = __uint_as_float(r[j]);
-                }
-            } else if constexpr (EPI == SH_SWIGLU) {
+            if constexpr (EPI == SH_SWIGLU) {
                 for (int cb = 0; cb < NT / 2; cb += 16) {
                     uint32_t g[16], u[16];
                     tmem_ld16(tb + cb, g);
@@ -217,43 +230,8 @@ __global__ void __launch_bounds__(kSThreads, 1) shared_kernel(const __grid_const
 
     tc_fence_before();
     __syncthreads();
-    if (NT <= 64 && KS > 1) {
-        // every CTA of the cluster gets here (no early exit); the partials are
-        // summed in rank order, each CTA taking a slice of the tile's valid
-        // rows; consecutive threads take consecutive columns of a row
-        cluster_barrier();
-        const int vr = min(SM_, a.T - t0), per = (vr + KS - 1) / KS;
-        const int r0 = ks * per, r1 = min(vr, r0 + per);
-        const uint32_t pl = smem_u32(part);
-        constexpr int kOut = EPI == SH_SWIGLU ? NT / 2 : NT;
-        for (int i = threadIdx.x; i < (r1 - r0) * kOut; i += kSThreads) {
-            const int rr = r0 + i / kOut, j = i % kOut, row = t0 + rr;
-            const uint32_t o0 = pl + (uint32_t)((rr * (NT + 1) + j) * 4);
-            // every rank's value is loaded first (all in flight), then summed in rank order
-            float v0[kMaxClusterSplit], v1[kMaxClusterSplit];
-#pragma unroll
-            for (int p = 0; p < kMaxClusterSplit; ++p)
-                if (p < KS) {
-                    v0[p] = ld_dsmem(dsmem_addr(o0, (uint32_t)p));
-                    if (EPI == SH_SWIGLU) v1[p] = ld_dsmem(dsmem_addr(o0 + (uint32_t)(NT / 2 * 4), (uint32_t)p));
-                }
-            float y0 = 0.0f, y1 = 0.0f;
-#pragma unroll
-            for (int p = 0; p < kMaxClusterSplit; ++p)
-                if (p < KS) {
-                    y0 += v0[p];
-                    if (EPI == SH_SWIGLU) y1 += v1[p];
-                }
-            if constexpr (EPI == SH_SWIGLU) {
-                const float G = round_bf16(y0), U = round_bf16(y1);
-                a.out[(size_t)row * a.N + c0 + j] = f32_to_bf16_bits(G / (1.0f + expf(-G)) * U);
-            } else {
-                uint16_t* o = a.out + (size_t)row * a.N + c0 + j;
-                *o = f32_to_bf16_bits(bf16_bits_to_f32(*o) + y0);
-            }
-        }
-        cluster_barrier();  // no CTA leaves while another still reads its partial
-    }
+    if (threadIdx.x == 32 && *abort_flag)  // copies still in flight land before the CTA leaves
+        for (int kc = s_consumed; kc < s_issued; ++kc) drain_wait(smem_u32(&bar_full[kc % SS]), (uint32_t)((kc / SS) & 1));
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, NT);
@@ -261,13 +239,233 @@ __global__ void __launch_bounds__(kSThreads, 1) shared_kernel(const __grid_const
     grid_dep_launch();
 }
 
-// Clusters of `ks` CTAs of this kernel that can be resident at once (the
-// shared memory allows one CTA per SM; a cluster's CTAs share a GPC).
-template <int EPI, int NT>
-int max_active_clusters(int ks) {
-    auto kern = shared_kernel<EPI, NT>;
-    constexpr int smem = SGeo<NT>::kSmem;
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+template <int EPI>
+__global__ void __launch_bounds__(kSThreads, 1) shared_narrow_kernel(const __grid_constant__ SharedArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ __align__(8) uint64_t bar_full[kNarrowMaxStages], bar_done[kNarrowMaxStages], bar_acc;
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_abort, s_consumed, s_issued;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int NB = a.nb, SS = a.ss, KS = a.ksplit;
+    const int kStage = narrow_stage_bytes(NB);
+    const uint32_t tcols = NB < 32 ? 32u : (uint32_t)NB;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < SS; ++s) {
+            mbar_init(smem_u32(&bar_full[s]), 1);
+            mbar_init(smem_u32(&bar_done[s]), 1);
+        }
+        mbar_init(smem_u32(&bar_acc), 1);
+        s_abort = 0;
+        s_consumed = 0;
+        s_issued = 0;
+        mbar_fence_init();
+    }
+    if (warp == 0) tmem_alloc(smem_u32(&s_tmem), tcols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    volatile int* abort_flag = &s_abort;
+    // the CTAs of one cluster (k slices) are adjacent, then the token tiles
+    // of one weight tile (its rows stay in L2 for them)
+    const int ks = blockIdx.x % KS, tile = blockIdx.x / KS;
+    const int tt = tile % a.t_tiles, wt = tile / a.t_tiles;
+    const int t0 = tt * NB;
+    constexpr int kRows = EPI == SH_SWIGLU ? SM_ / 2 : SM_;  // output features per tile
+    const int r0 = wt * kRows;                                // first output feature (= weight row of each map)
+    const int nk_all = a.K / SKS;
+    const int kc0 = ks * nk_all / KS, nk = (ks + 1) * nk_all / KS - kc0;  // this CTA's k-stages
+    const uint32_t stage_tx = (uint32_t)kStage;                          // whole boxes (rows past T are zero-filled)
+
+    if (warp == 0) {
+        // ---------------- MMA: warp-uniform loop, one elected lane issues ----------------
+        int s = 0, kc = 0;
+        uint32_t par = 0;
+        for (; kc < nk; ++kc) {
+            if (!warp_wait(smem_u32(&bar_full[s]), par, abort_flag, a.status)) break;
+            tc_fence_after();
+            const uint32_t sw = smem_u32(smem + s * kStage), sx = sw + kSA;
+            if (elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < SKS / 16; ++kk)
+                    mma_f16(tmem, sdesc_sw128(sw) + 2 * kk, sdesc_sw128(sx) + 2 * kk, idesc_bf16(SM_, NB),
+                            (kc | kk) != 0);
+                mma_commit(smem_u32(&bar_done[s]));
+            }
+            __syncwarp();
+            if (++s == SS) {
+                s = 0;
+                par ^= 1;
+            }
+        }
+        if (lane == 0) s_consumed = kc;
+        if (elect_one()) mma_commit(smem_u32(&bar_acc));
+        __syncwarp();
+        grid_dep_wait();  // (this warp reads no global memory before the output phase)
+    } else if (warp == 1) {
+        // ---------------- operands by TMA (one thread) ----------------
+        if (lane != 0) grid_dep_wait();
+        if (lane == 0) {
+            auto load_w = [&](int kc) {
+                const uint32_t bar = smem_u32(&bar_full[kc % SS]);
+                const uint32_t dst = smem_u32(smem + (kc % SS) * kStage);
+                const int kx = (kc0 + kc) * (SKS * 2);
+                if (EPI == SH_SWIGLU) {
+                    tma_load_2d(dst, &a.tmap_b0, kx, r0, bar);
+                    tma_load_2d(dst + kSA / 2, &a.tmap_b1, kx, r0, bar);
+                } else {
+                    tma_load_2d(dst, &a.tmap_b0, kx, r0, bar);
+                }
+            };
+            auto load_x = [&](int kc) {
+                const uint32_t bar = smem_u32(&bar_full[kc % SS]);
+                const uint32_t dst = smem_u32(smem + (kc % SS) * kStage) + kSA;
+                tma_load_2d(dst, &a.tmap_a, (kc0 + kc) * (SKS * 2), t0, bar);
+            };
+            // the down launch: its first weight stages do not depend on the
+            // gate/up launch, only the h rows do
+            const int pre = EPI == SH_ADD ? min(SS, nk) : 0;
+            for (int kc = 0; kc < pre; ++kc) {
+                mbar_arrive_expect_tx(smem_u32(&bar_full[kc]), stage_tx);
+                load_w(kc);
+            }
+            grid_dep_wait();
+            for (int kc = 0; kc < pre; ++kc) load_x(kc);
+            int kc = pre;
+            for (; kc < nk; ++kc) {
+                const int s = kc % SS;
+                if (kc >= SS &&
+                    !mbar_wait(smem_u32(&bar_done[s]), (uint32_t)(((kc - SS) / SS) & 1), abort_flag, a.status))
+                    break;
+                mbar_arrive_expect_tx(smem_u32(&bar_full[s]), stage_tx);
+                load_w(kc);
+                load_x(kc);
+            }
+            s_issued = kc;
+        }
+        __syncwarp();
+    } else {
+        grid_dep_wait();
+    }
+
+    // ---------------- the accumulator (or this CTA's partial) to shared memory ----------------
+    // part[t][r], t = token of the tile, r = weight row (TMEM lane): a warp's
+    // stores of one token are 32 consecutive floats; it reuses the ring,
+    // whose copies the MMAs have all consumed
+    float* part = reinterpret_cast<float*>(smem);
+    if (warp >= 4) {
+        const int q = warp - 4, r = q * 32 + lane;
+        if (warp_wait(smem_u32(&bar_acc), 0, abort_flag, a.status, 64)) {
+            tc_fence_after();
+            const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16);
+            for (int cb = 0; cb < NB; cb += 16) {
+                uint32_t v[16];
+                tmem_ld16(tb + cb, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) part[(cb + j) * SM_ + r] = __uint_as_float(v[j]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    grid_dep_launch();
+    if (KS > 1) cluster_barrier();
+
+    // ---------------- the tile's outputs: partials summed in rank order ----------------
+    // unit u of the tile: token t = u / (kRows / 4), features 4 (u % (kRows /
+    // 4)) .. +3 (consecutive threads, consecutive features of a token row:
+    // 16-byte loads of the partials, 8-byte stores); CTA ks of the cluster
+    // takes a contiguous slice of the units
+    {
+        constexpr int kUPT = kRows / 4;  // units per token
+        const int vt = min(NB, a.T - t0), total = kUPT * vt;
+        const int per = (total + KS - 1) / KS, u0 = ks * per, u1 = min(total, u0 + per);
+        const uint32_t pl = smem_u32(part);
+        auto ld_part = [&](int p, int t, int r) -> float4 {
+            const uint32_t o = pl + (uint32_t)((t * SM_ + r) * 4);
+            return KS > 1 ? ld_dsmem4(dsmem_addr(o, (uint32_t)p)) : *reinterpret_cast<const float4*>(part + t * SM_ + r);
+        };
+        constexpr int kBatch = 2;  // units per thread with all their loads in flight
+        for (int ub = u0 + threadIdx.x; ub < u1; ub += kBatch * kSThreads) {
+            float4 v0[kBatch][kMaxClusterSplit], v1[kBatch][kMaxClusterSplit];
+            uint2 ov[kBatch];
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) {
+                const int u = ub + b * kSThreads;
+                if (u < u1) {
+                    const int t = u / kUPT, f = (u % kUPT) * 4;
+#pragma unroll
+                    for (int p = 0; p < kMaxClusterSplit; ++p)
+                        if (p < KS) {
+                            v0[b][p] = ld_part(p, t, f);
+                            if (EPI == SH_SWIGLU) v1[b][p] = ld_part(p, t, kRows + f);
+                        }
+                    if (EPI == SH_ADD)
+                        ov[b] = *reinterpret_cast<const uint2*>(a.out + (size_t)(t0 + t) * a.N + r0 + f);
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) {
+                const int u = ub + b * kSThreads;
+                if (u < u1) {
+                    const int t = u / kUPT, f = (u % kUPT) * 4;
+                    float4 y0 = make_float4(0.f, 0.f, 0.f, 0.f), y1 = y0;
+#pragma unroll
+                    for (int p = 0; p < kMaxClusterSplit; ++p)
+                        if (p < KS) {
+                            y0.x += v0[b][p].x;
+                            y0.y += v0[b][p].y;
+                            y0.z += v0[b][p].z;
+                            y0.w += v0[b][p].w;
+                            if (EPI == SH_SWIGLU) {
+                                y1.x += v1[b][p].x;
+                                y1.y += v1[b][p].y;
+                                y1.z += v1[b][p].z;
+                                y1.w += v1[b][p].w;
+                            }
+                        }
+                    const float g4[4] = {y0.x, y0.y, y0.z, y0.w};
+                    uint32_t hw[4];
+                    if constexpr (EPI == SH_SWIGLU) {
+                        const float u4[4] = {y1.x, y1.y, y1.z, y1.w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const float G = round_bf16(g4[j]), U = round_bf16(u4[j]);
+                            hw[j] = f32_to_bf16_bits(G / (1.0f + expf(-G)) * U);
+                        }
+                    } else {
+                        const uint32_t o2[2] = {ov[b].x, ov[b].y};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint32_t ob = (o2[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
+                            hw[j] = f32_to_bf16_bits(bf16_bits_to_f32(ob) + g4[j]);
+                        }
+                    }
+                    *reinterpret_cast<uint2*>(a.out + (size_t)(t0 + t) * a.N + r0 + f) =
+                        make_uint2(hw[0] | (hw[1] << 16), hw[2] | (hw[3] << 16));
+                }
+            }
+        }
+    }
+    if (KS > 1) cluster_barrier();  // no CTA leaves while another still reads its partial
+    if (threadIdx.x == 32 && *abort_flag)  // copies still in flight land before the CTA leaves
+        for (int kc = s_consumed; kc < s_issued; ++kc) drain_wait(smem_u32(&bar_full[kc % SS]), (uint32_t)((kc / SS) & 1));
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, tcols);
+    }
+}
+
+// Clusters of `ks` narrow CTAs with `smem` bytes of dynamic shared memory
+// that can be resident at once (a cluster's CTAs share a GPC).
+template <int EPI>
+int max_active_clusters(int ks, int smem) {
+    auto kern = shared_narrow_kernel<EPI>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kNarrowSmemMax);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ks * num_sms());
     cfg.blockDim = dim3(kSThreads);
@@ -287,17 +485,8 @@ int max_active_clusters(int ks) {
     return n;
 }
 
-template <int EPI, int NT>
-nvfp4_status launch_shared(const SharedArgs& a, cudaStream_t s, const char* name) {
-    auto kern = shared_kernel<EPI, NT>;
-    constexpr int smem = SGeo<NT>::kSmem;
-    static bool init = false;
-    if (!init) {
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        init = true;
-    }
-    constexpr int kCols = EPI == SH_SWIGLU ? NT / 2 : NT;
-    const int grid = ((a.T + SM_ - 1) / SM_) * (a.N / kCols) * a.ksplit;
+nvfp4_status launch_cfg(void (*kern)(SharedArgs), int grid, int smem, int cluster, const SharedArgs& a,
+                        cudaStream_t s, const char* name) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kSThreads);
@@ -305,9 +494,9 @@ nvfp4_status launch_shared(const SharedArgs& a, cudaStream_t s, const char* name
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     int na = 0;
-    if (a.ksplit > 1) {
+    if (cluster > 1) {
         attr[na].id = cudaLaunchAttributeClusterDimension;
-        attr[na].val.clusterDim.x = a.ksplit;
+        attr[na].val.clusterDim.x = cluster;
         attr[na].val.clusterDim.y = 1;
         attr[na].val.clusterDim.z = 1;
         ++na;
@@ -321,6 +510,31 @@ nvfp4_status launch_shared(const SharedArgs& a, cudaStream_t s, const char* name
     cfg.numAttrs = na;
     NVFP4_LAUNCH(name, s, cudaLaunchKernelEx(&cfg, kern, a));
     return last_launch_status();
+}
+
+template <int EPI>
+nvfp4_status launch_wide(const SharedArgs& a, cudaStream_t s, const char* name) {
+    static bool init = false;
+    if (!init) {
+        cudaFuncSetAttribute(shared_wide_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kWideSmem);
+        init = true;
+    }
+    constexpr int kCols = EPI == SH_SWIGLU ? SN / 2 : SN;
+    const int grid = ((a.T + SM_ - 1) / SM_) * (a.N / kCols);
+    return launch_cfg(shared_wide_kernel<EPI>, grid, kWideSmem, 1, a, s, name);
+}
+
+template <int EPI>
+nvfp4_status launch_narrow(const SharedArgs& a, cudaStream_t s, const char* name) {
+    static bool init = false;
+    if (!init) {
+        cudaFuncSetAttribute(shared_narrow_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kNarrowSmemMax);
+        init = true;
+    }
+    const int smem = 1024 + a.ss * narrow_stage_bytes(a.nb);
+    constexpr int kRows = EPI == SH_SWIGLU ? SM_ / 2 : SM_;
+    const int grid = (a.N / kRows) * a.t_tiles * a.ksplit;
+    return launch_cfg(shared_narrow_kernel<EPI>, grid, smem, a.ksplit, a, s, name);
 }
 
 }  // namespace
@@ -347,55 +561,92 @@ extern "C" nvfp4_status moe_shared_expert(const uint16_t* x_bf16, int T, int d, 
         return NVFP4_ERR_ALIGN;
     if (ws_bytes < moe_shared_expert_workspace_size(T, Fs)) return NVFP4_ERR_WORKSPACE;
     uint16_t* h = static_cast<uint16_t*>(ws);
-    // 64-wide tiles when the 256-wide down tiles would leave half the SMs idle
     const int m_tiles = (T + SM_ - 1) / SM_;
+    // narrow tiles when the 256-wide down tiles would leave half the SMs idle
     const bool narrow = (long long)m_tiles * (d / SN) * 2 < num_sms();
-    // narrow tiles: split K over a cluster, the widest split whose clusters
-    // are all resident at once (one wave) and that leaves every CTA at least
-    // two k-stages (measured on GB300: a second wave of a few clusters
-    // doubles the launch's time)
-    static int clusters_gu[kMaxClusterSplit + 1] = {}, clusters_dn[kMaxClusterSplit + 1] = {};
-    auto pick_split = [&](long long ctas, int K, int* cache, bool gateup) {
+    if (!narrow) {
+        SharedArgs g{};  // gate/up + SwiGLU -> h [T, Fs]
+        g.T = T;
+        g.K = d;
+        g.N = Fs;
+        g.out = h;
+        g.status = d_status;
+        g.a_rows = std::min(SM_, (T + 7) / 8 * 8);
+        if (!encode_tmap_u8(&g.tmap_a, x_bf16, (unsigned long long)d * 2, (unsigned long long)T, SKS * 2, g.a_rows,
+                            true) ||
+            !encode_tmap_u8(&g.tmap_b0, w_gate_bf16, (unsigned long long)d * 2, (unsigned long long)Fs, SKS * 2,
+                            SN / 2, true) ||
+            !encode_tmap_u8(&g.tmap_b1, w_up_bf16, (unsigned long long)d * 2, (unsigned long long)Fs, SKS * 2,
+                            SN / 2, true))
+            return NVFP4_ERR_CUDA;
+        nvfp4_status st = launch_wide<SH_SWIGLU>(g, stream, "shared_gateup");
+        if (st != NVFP4_OK) return st;
+        SharedArgs u{};  // down, added into the routed output
+        u.T = T;
+        u.K = Fs;
+        u.N = d;
+        u.out = out_bf16;
+        u.status = d_status;
+        u.a_rows = g.a_rows;
+        if (!encode_tmap_u8(&u.tmap_a, h, (unsigned long long)Fs * 2, (unsigned long long)T, SKS * 2, u.a_rows,
+                            true) ||
+            !encode_tmap_u8(&u.tmap_b0, w_down_bf16, (unsigned long long)Fs * 2, (unsigned long long)d, SKS * 2,
+                            SN / 2, true))
+            return NVFP4_ERR_CUDA;
+        return launch_wide<SH_ADD>(u, stream, "shared_down");
+    }
+    // narrow tiles: tokens per tile, ring depth, and K split over a cluster
+    // -- the widest split whose clusters are all resident at once (one wave:
+    // measured on GB300, a second wave of a few clusters doubles a launch's
+    // time) and that leaves every CTA at least two k-stages
+    const int nb = T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : SM_;
+    const int nbi = nb == 16 ? 0 : nb == 32 ? 1 : nb == 64 ? 2 : 3;
+    const int t_tiles = (T + nb - 1) / nb;
+    const int ss = std::min(kNarrowMaxStages, kNarrowRing / narrow_stage_bytes(nb));
+    const int smem = 1024 + ss * narrow_stage_bytes(nb);
+    static int clusters[2][4][kMaxClusterSplit + 1] = {};
+    auto pick_split = [&](long long tiles, int K, int epi) {
         int ks = 1;
-        if (!narrow) return ks;
         for (int c = 2; c <= kMaxClusterSplit; ++c) {
-            if (K / SKS < 2 * c || ctas * c > num_sms()) continue;
-            if (cache[c] == 0)
-                cache[c] = gateup ? max_active_clusters<SH_SWIGLU, 64>(c) : max_active_clusters<SH_ADD, 64>(c);
-            if (ctas <= cache[c]) ks = c;
+            if (K / SKS < 2 * c || tiles * c > num_sms()) continue;
+            int& n = clusters[epi][nbi][c];
+            if (n == 0)
+                n = epi == SH_SWIGLU ? max_active_clusters<SH_SWIGLU>(c, smem) : max_active_clusters<SH_ADD>(c, smem);
+            if (tiles <= n) ks = c;
         }
         return ks;
     };
-    const unsigned bh = narrow ? 32 : SN / 2;  // B rows per TMA box
-    // gate/up + SwiGLU -> h [T, Fs]
-    SharedArgs g{};
+    SharedArgs g{};  // gate/up + SwiGLU -> h [T, Fs]
     g.T = T;
     g.K = d;
     g.N = Fs;
+    g.nb = nb;
+    g.t_tiles = t_tiles;
+    g.ss = ss;
     g.out = h;
     g.status = d_status;
-    const int a_rows = std::min(SM_, (T + 7) / 8 * 8);
-    g.a_rows = a_rows;
-    g.ksplit = pick_split((long long)m_tiles * (Fs / 32), d, clusters_gu, true);
-    if (!encode_tmap_u8(&g.tmap_a, x_bf16, (unsigned long long)d * 2, (unsigned long long)T, SKS * 2, a_rows, true) ||
-        !encode_tmap_u8(&g.tmap_b0, w_gate_bf16, (unsigned long long)d * 2, (unsigned long long)Fs, SKS * 2, bh,
+    g.ksplit = pick_split((long long)(Fs / (SM_ / 2)) * t_tiles, d, SH_SWIGLU);
+    if (!encode_tmap_u8(&g.tmap_a, x_bf16, (unsigned long long)d * 2, (unsigned long long)T, SKS * 2, nb, true) ||
+        !encode_tmap_u8(&g.tmap_b0, w_gate_bf16, (unsigned long long)d * 2, (unsigned long long)Fs, SKS * 2, SM_ / 2,
                         true) ||
-        !encode_tmap_u8(&g.tmap_b1, w_up_bf16, (unsigned long long)d * 2, (unsigned long long)Fs, SKS * 2, bh, true))
+        !encode_tmap_u8(&g.tmap_b1, w_up_bf16, (unsigned long long)d * 2, (unsigned long long)Fs, SKS * 2, SM_ / 2,
+                        true))
         return NVFP4_ERR_CUDA;
-    nvfp4_status st = narrow ? launch_shared<SH_SWIGLU, 64>(g, stream, "shared_gateup")
-                             : launch_shared<SH_SWIGLU, SN>(g, stream, "shared_gateup");
+    nvfp4_status st = launch_narrow<SH_SWIGLU>(g, stream, "shared_gateup");
     if (st != NVFP4_OK) return st;
-    // down, added into the routed output
-    SharedArgs u{};
+    SharedArgs u{};  // down, added into the routed output
     u.T = T;
     u.K = Fs;
     u.N = d;
+    u.nb = nb;
+    u.t_tiles = t_tiles;
+    u.ss = ss;
     u.out = out_bf16;
     u.status = d_status;
-    u.a_rows = a_rows;
-    u.ksplit = pick_split((long long)m_tiles * (d / 64), Fs, clusters_dn, false);
-    if (!encode_tmap_u8(&u.tmap_a, h, (unsigned long long)Fs * 2, (unsigned long long)T, SKS * 2, a_rows, true) ||
-        !encode_tmap_u8(&u.tmap_b0, w_down_bf16, (unsigned long long)Fs * 2, (unsigned long long)d, SKS * 2, bh, true))
+    u.ksplit = pick_split((long long)(d / SM_) * t_tiles, Fs, SH_ADD);
+    if (!encode_tmap_u8(&u.tmap_a, h, (unsigned long long)Fs * 2, (unsigned long long)T, SKS * 2, nb, true) ||
+        !encode_tmap_u8(&u.tmap_b0, w_down_bf16, (unsigned long long)Fs * 2, (unsigned long long)d, SKS * 2, SM_,
+                        true))
         return NVFP4_ERR_CUDA;
-    return narrow ? launch_shared<SH_ADD, 64>(u, stream, "shared_down") : launch_shared<SH_ADD, SN>(u, stream, "shared_down");
+    return launch_narrow<SH_ADD>(u, stream, "shared_down");
 }
