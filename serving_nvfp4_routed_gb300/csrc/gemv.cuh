@@ -10,6 +10,7 @@ enum OutMode { OUT_H = 0, OUT_HQ = 1, OUT_COMBINE = 2, OUT_BF16 = 3 };
 
 struct GemvArgs {
     int K, N, top_k;
+    int E;                          // experts: the routing arrays' length
     int nproj;                      // 2: gate+up (SwiGLU epilogue), 1: single projection
     int ksplit;                     // warps of a CTA splitting K (1, 2, 4 or 8)
     int fb_group;                   // feature blocks per work item (they share the staged rows)

@@ -151,9 +151,10 @@ nvfp4_status check_moe(const uint16_t* x, int T, int top_k, const nvfp4_moe_weig
     return NVFP4_OK;
 }
 
-GemvArgs base_args(const MoeWs& ws, int top_k) {
+GemvArgs base_args(const MoeWs& ws, int top_k, int E) {
     GemvArgs a{};
     a.top_k = top_k;
+    a.E = E;
     a.offsets = ws.ra.offsets;
     a.active = ws.ra.active;
     a.n_active = ws.ra.n_active;
@@ -360,7 +361,7 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
         launch_decode(mode == 0 ? B_BF16 : B_NVFP4, da, s);
         return last_launch_status();
     }
-    GemvArgs a = base_args(ws, top_k);
+    GemvArgs a = base_args(ws, top_k, E);
     // gate/up + SwiGLU (also zeroes the fp32 combine accumulator)
     a.K = d;
     a.N = F;
@@ -397,7 +398,7 @@ nvfp4_status run_moe(int mode, const uint16_t* x, int T, const float* logits, in
         launch_gemv(B_NVFP4, OUT_HQ, a, gemv_max_work(R, E, F), s);
     }
     // down + weighted combine; the last contribution to a token writes its bf16 row
-    GemvArgs b = base_args(ws, top_k);
+    GemvArgs b = base_args(ws, top_k, E);
     b.K = F;
     b.N = d;
     b.nproj = 1;
@@ -599,6 +600,7 @@ extern "C" nvfp4_status nvfp4_linear(const uint16_t* x, int M, int K, const nvfp
     a.K = K;
     a.N = N;
     a.top_k = 1;
+    a.E = 1;
     a.offsets = l.meta + 0;
     a.active = l.meta + 2;
     a.n_active = l.meta + 3;

@@ -106,10 +106,16 @@ constexpr int kWarps = kThreads / 32;
 // (codes, then scales), filled with cp.async by the lanes that read them.
 constexpr int kRingSlots = 4;
 constexpr int kRingSlotBytes = 2 * 32 * 32 + 2 * 32 * 4;  // 2304
-constexpr size_t ring_bytes() { return (size_t)kWarps * kRingSlots * kRingSlotBytes; }
-// The ring is used while two CTAs' row stage plus ring (and ~4 KB of static
-// shared memory each) fit in an SM: K up to 9216.
-bool ring_fits(int K) { return 2 * ((size_t)kGemvTokTile * K * 2 + ring_bytes() + 4096) <= 227 * 1024; }
+__host__ __device__ constexpr size_t ring_bytes() { return (size_t)kWarps * kRingSlots * kRingSlotBytes; }
+// Dynamic shared memory: the row stage [kGemvTokTile][K] f16, the ring
+// (kWarps x kRingSlots x 2304 B = 72 KB), the routing metadata (3 E + 2 ints).
+__host__ __device__ constexpr size_t gemv_smem_bytes_dev(int K) { return (size_t)kGemvTokTile * K * 2; }
+size_t meta_bytes(int E) { return ((size_t)(3 * E + 2) * 4 + 15) / 16 * 16; }
+// The ring is used while two CTAs' row stage, ring and metadata (and ~4 KB
+// of static shared memory each) fit in an SM: K up to ~2300 at E = 288.
+bool ring_fits(int K, int E) {
+    return 2 * (gemv_smem_bytes_dev(K) + ring_bytes() + meta_bytes(E) + 4096) <= 227 * 1024;
+}
 struct Item {
     int e, row0, nrows, fb, fb_end;  // feature blocks [fb, fb_end) share the staged rows
 };
@@ -134,6 +140,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
     __shared__ unsigned s_amax[kGemvTokTile];
     __shared__ int s_next;
     __shared__ int s_fin[kGemvTokTile];
+    __shared__ int s_nact;
 
     // The routed layer's down projection (OUT_COMBINE) takes its first item
     // and starts that item's weight loads before it waits for the gate/up
@@ -148,8 +155,24 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
     const int KSPL = a.ksplit, WF = kWarps / KSPL;
     const int wf = warp / KSPL, ks = warp % KSPL;
 
-    const int n_active = *a.n_active;
-    const int total_tiles = a.tile_start[n_active];
+    // the routing metadata, loaded once per CTA into the dynamic shared
+    // memory after the row stage and the ring (an item's decode is then free
+    // of dependent global loads): tile starts [E + 1], active experts [E],
+    // row offsets [E + 1]
+    int* s_ts = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(Bs) + gemv_smem_bytes_dev(a.K) +
+                                       (kRing ? ring_bytes() : 0));
+    int* s_act = s_ts + (a.E + 1);
+    int* s_off = s_act + a.E;
+    for (int i = tid; i <= a.E; i += kThreads) {
+        s_ts[i] = a.tile_start[i];
+        s_off[i] = a.offsets[i];
+        if (i < a.E) s_act[i] = a.active[i];
+    }
+    if (tid == 0) s_nact = *a.n_active;
+    if (tid < kGemvTokTile) s_amax[tid] = 0u;
+    __syncthreads();
+    const int n_active = s_nact;
+    const int total_tiles = s_ts[n_active];
     const int FB = 16 * WF;
     const int n_fb = a.N / FB;
     const int G = a.fb_group > 0 ? a.fb_group : 1;  // feature blocks per work item
@@ -166,11 +189,11 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
         int lo = 0, hi = n_active;  // largest ai with tile_start[ai] <= tile
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
-            if (a.tile_start[mid] <= tile) lo = mid; else hi = mid;
+            if (s_ts[mid] <= tile) lo = mid; else hi = mid;
         }
-        it.e = a.active[lo];
-        it.row0 = a.offsets[it.e] + (tile - a.tile_start[lo]) * kGemvTokTile;
-        it.nrows = min(kGemvTokTile, a.offsets[it.e + 1] - it.row0);
+        it.e = s_act[lo];
+        it.row0 = s_off[it.e] + (tile - s_ts[lo]) * kGemvTokTile;
+        it.nrows = min(kGemvTokTile, s_off[it.e + 1] - it.row0);
     };
 
     // L2 prefetch (one thread, K not split over warps): chunk ch of the
@@ -251,10 +274,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
         if constexpr (NBUF > 3) load_batch(std::integral_constant<int, 2>{}, it, ks + 2 * U * KSPL);
     };
 
-    if (tid == 0) s_next = atomicAdd(a.work_counter, 1);
-    if (tid < kGemvTokTile) s_amax[tid] = 0u;
-    __syncthreads();
-    int item = s_next;
+    // the first item is the CTA's own index, the others come from the counter
+    int item = blockIdx.x;
     Item cur{};
     if (item < total) {
         decode(item, cur);
@@ -317,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
             }
         }
         __syncthreads();
-        if (tid == 0) s_next = atomicAdd(a.work_counter, 1);  // next item, fetched while computing
+        if (tid == 0) s_next = (int)gridDim.x + atomicAdd(a.work_counter, 1);  // next item, fetched while computing
         int nitem = total;
         Item nxt{};
         for (;;) {  // the feature blocks of this item, all on the staged rows
@@ -578,19 +599,25 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
 template <int CK, int BMODE, int OUTMODE, int NPROJ, bool RING = false>
 void launch_t(const GemvArgs& a, int max_work, cudaStream_t s, const char* name) {
     auto kern = gemv_kernel<CK, BMODE, OUTMODE, NPROJ, RING>;
+    const size_t smem = gemv_smem_bytes(a.K) + (RING ? ring_bytes() : 0) + meta_bytes(a.E);
+    // the occupancy probe: the row stage of a typical K (down 1536, gate/up
+    // 4096) with the metadata of 288 experts
+    const size_t probe = gemv_smem_bytes(RING ? 1536 : 4096) + (RING ? ring_bytes() : 0) + meta_bytes(288);
+    // the dynamic shared-memory limit grows to the largest launch so far
+    static size_t attr = 0;
+    if (std::max(smem, probe) > attr) {
+        attr = std::max(smem, probe);
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attr);
+    }
     static int per_sm = 0;
     if (per_sm == 0) {
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(RING ? gemv_smem_bytes(9216) + ring_bytes() : gemv_smem_bytes(12288)));
         int v = 0;
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kern, kThreads,
-                                                      RING ? gemv_smem_bytes(1536) + ring_bytes() : gemv_smem_bytes(4096));
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kern, kThreads, probe);
         per_sm = v > 0 ? v : 1;
     }
     // the ring kernel runs two CTAs per SM (ring_fits), the others two while
     // the row stage is at most 64 KB
-    const size_t smem = gemv_smem_bytes(a.K) + (RING ? ring_bytes() : 0);
-    const int occ = RING ? std::min(per_sm, 2) : (smem > gemv_smem_bytes(4096) ? 1 : per_sm);
+    const int occ = RING ? std::min(per_sm, 2) : (2 * (smem + 8192) <= 227 * 1024 ? per_sm : 1);
     const int grid = std::max(1, std::min(max_work, occ * num_sms()));
     NVFP4_LAUNCH(name, s, launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, a));
 }
@@ -601,7 +628,7 @@ void launch_ck(int bmode, int outmode, const GemvArgs& a, int max_work, cudaStre
     if (bmode == B_BF16) {
         if (outmode == OUT_H && two) return launch_t<CK, B_BF16, OUT_H, 2>(a, max_work, s, "gemv_gateup_w4a16");
         if (outmode == OUT_COMBINE) {
-            if (CK == 256 && ring_fits(a.K))
+            if (CK == 256 && ring_fits(a.K, a.E))
                 return launch_t<CK, B_BF16, OUT_COMBINE, 1, CK == 256>(a, max_work, s, "gemv_down_w4a16");
             return launch_t<CK, B_BF16, OUT_COMBINE, 1>(a, max_work, s, "gemv_down_w4a16");
         }
@@ -609,7 +636,7 @@ void launch_ck(int bmode, int outmode, const GemvArgs& a, int max_work, cudaStre
     } else {
         if (outmode == OUT_HQ && two) return launch_t<CK, B_NVFP4, OUT_HQ, 2>(a, max_work, s, "gemv_gateup_w4a4");
         if (outmode == OUT_COMBINE) {
-            if (CK == 256 && ring_fits(a.K))
+            if (CK == 256 && ring_fits(a.K, a.E))
                 return launch_t<CK, B_NVFP4, OUT_COMBINE, 1, CK == 256>(a, max_work, s, "gemv_down_w4a4");
             return launch_t<CK, B_NVFP4, OUT_COMBINE, 1>(a, max_work, s, "gemv_down_w4a4");
         }
