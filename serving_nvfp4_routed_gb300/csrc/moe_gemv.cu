@@ -140,6 +140,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
     __shared__ unsigned s_amax[kGemvTokTile];
     __shared__ int s_next;
     __shared__ int s_fin[kGemvTokTile];
+    __shared__ float s_wt[kGemvTokTile];  // OUT_COMBINE: the routing weight of each of the item's rows
     __shared__ int s_nact;
 
     // The routed layer's down projection (OUT_COMBINE) takes its first item
@@ -286,6 +287,16 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
     if constexpr (kEarly) grid_dep_wait();
 
     while (item < total) {
+        // ---- the item's per-expert scales and (down) its rows' routing
+        // weights, loaded once here for every epilogue of the item
+        float it_ws[NPROJ];
+#pragma unroll
+        for (int p = 0; p < NPROJ; ++p) it_ws[p] = a.a_ws2[p][cur.e];
+        const float it_bgs = BMODE == B_NVFP4 ? a.b_gs[cur.e] : 0.0f;
+        const float it_hqgs = OUTMODE == OUT_HQ ? a.hq_gs[cur.e] : 0.0f;
+        if constexpr (OUTMODE == OUT_COMBINE) {
+            if (tid < cur.nrows) s_wt[tid] = a.topk_w[a.row_to_slot[cur.row0 + tid]];
+        }
         // ---- stage the B rows of this item; the warps w with w % nrows == j stage row j
         {
             const int j = warp % cur.nrows, gi = warp / cur.nrows;
@@ -473,9 +484,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
                     const int r = row0 + (valid ? col : 0);
                     float rs;  // takes the accumulator to x W^T (without the tensor scale)
                     if constexpr (BMODE == B_BF16) rs = valid ? s_rowscale[col] : 0.0f;
-                    else rs = a.b_gs[e];
+                    else rs = it_bgs;
                     if constexpr (OUTMODE == OUT_H || OUTMODE == OUT_HQ) {
-                        const float wg = a.a_ws2[0][e], wu = a.a_ws2[NPROJ - 1][e];
+                        const float wg = it_ws[0], wu = it_ws[NPROJ - 1];
                         float hv[2];
 #pragma unroll
                         for (int hf = 0; hf < 2; ++hf) {
@@ -492,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
                             }
                         } else {
                             // NVFP4 requantisation of h: this warp's 16 features are one block
-                            const float gs2 = a.hq_gs[e];
+                            const float gs2 = it_hqgs;
                             float m = fmaxf(fabsf(hv[0]), fabsf(hv[1]));
                             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
                             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
@@ -521,8 +532,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
                         }
                     } else if constexpr (OUTMODE == OUT_COMBINE) {
                         if (valid) {
-                            const float wt = a.topk_w[a.row_to_slot[r]];
-                            const float ws = a.a_ws2[0][e];
+                            const float wt = s_wt[col];
+                            const float ws = it_ws[0];
 #pragma unroll
                             for (int hf = 0; hf < 2; ++hf) {
                                 const float y = __fmul_rn(__fmul_rn(acc[0][2 * hf + cc], rs), ws);
@@ -531,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
                         }
                     } else {  // OUT_BF16
                         if (valid) {
-                            const float ws = a.a_ws2[0][e];
+                            const float ws = it_ws[0];
 #pragma unroll
                             for (int hf = 0; hf < 2; ++hf)
                                 a.y_out[(size_t)r * a.N + n0 + g + 8 * hf] =
