@@ -349,7 +349,14 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
             }
         }
         __syncthreads();
-        if (tid == 0) s_next = (int)gridDim.x + atomicAdd(a.work_counter, 1);  // next item, fetched while computing
+        if (tid == 0) {
+            const int nx = (int)gridDim.x + atomicAdd(a.work_counter, 1);  // next item, fetched while computing
+            s_next = nx;
+            // gate/up: a CTA on its last item lets the down launch start
+            // filling the SMs that CTAs leave while the last items finish
+            // (its CTAs wait for this launch's completion before they read h)
+            if (NPROJ == 2 && nx >= total) grid_dep_launch();
+        }
         int nitem = total;
         Item nxt{};
         for (;;) {  // the feature blocks of this item, all on the staged rows
@@ -454,11 +461,6 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
                 prefetch(following);
             } else {
                 nitem = s_next;
-                // gate/up: a CTA without a further item lets the down launch
-                // start filling SMs while the last items finish
-                if constexpr (NPROJ == 2) {
-                    if (nitem >= total) grid_dep_launch();
-                }
                 if (nitem < total) {
                     decode(nitem, nxt);
                     if (a.pf_dist > 0 && tid == 0)
