@@ -30,12 +30,14 @@ def _check_shared(orc, x, wg, wu, wd, routed, out, ws, what):
     return assert_out_close(bf16_to_f32(out), ex["out"], ex["out_pre"], bound, what)
 
 
-@pytest.mark.parametrize("T,d,Fs", [(1, 256, 128), (100, 512, 256), (300, 1024, 384), (129, 4096, 1536),
-                                    (64, 4096, 1536), (1280, 2048, 256)])
+@pytest.mark.parametrize("T,d,Fs", [(1, 256, 128), (24, 2048, 512), (100, 512, 256), (300, 1024, 384),
+                                    (129, 4096, 1536), (64, 4096, 1536), (1280, 2048, 256)])
 def test_shared_expert(orc, T, d, Fs):
-    """Single and ragged token tiles, one and several column tiles in both
-    GEMMs, K from 128 to 4096; the small batches run 64-wide tiles, the last
-    case (ten token tiles) the 256-wide ones."""
+    """Single and ragged token tiles, one and several weight tiles in both
+    GEMMs, K from 128 to 4096.  The small batches run the narrow tiles (the
+    weight rows as the MMA's M, 16, 32, 64 or 128 tokens as its N: T = 1,
+    24, 64 and the rest; K split over clusters of 1 to 8 CTAs), the last
+    case (ten 128-token tiles) the wide ones."""
     x = synth.make_x(T, d, seed=T + d, device="cuda", outlier_frac=0.05)
     wg = synth.make_weights(1, Fs, d, seed=Fs + 1, device="cuda")[0]
     wu = synth.make_weights(1, Fs, d, seed=Fs + 2, device="cuda")[0] * 2
@@ -70,3 +72,23 @@ def test_routed_layer_then_shared_expert(orc):
     lib.moe_shared_expert(inp["x"], wg, wu, wd, out, ws=wss)
     torch.cuda.synchronize()
     _check_shared(orc, inp["x"], wg, wu, wd, routed, out, wss, "block")
+
+
+def test_shared_expert_deterministic():
+    """The narrow tiles' split-K sums their partials in rank order: the same
+    output bits on every call (decode size, K split over clusters)."""
+    T, d, Fs = 64, 4096, 1536
+    x = synth.make_x(T, d, seed=7, device="cuda", outlier_frac=0.05)
+    wg = synth.make_weights(1, Fs, d, seed=8, device="cuda")[0]
+    wu = synth.make_weights(1, Fs, d, seed=9, device="cuda")[0]
+    wd = synth.make_weights(1, d, Fs, seed=10, device="cuda")[0]
+    routed = synth.make_x(T, d, seed=11, device="cuda")
+    ws = torch.empty(max(16, lib.load().moe_shared_expert_workspace_size(T, Fs)), dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(3):
+        out = routed.clone()
+        lib.moe_shared_expert(x, wg, wu, wd, out, ws=ws)
+        outs.append(out)
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
