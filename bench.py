@@ -179,14 +179,30 @@ KERNEL_SOURCES = {
 FP4_BF16_RATIO = 6.0
 
 
+def _code_only(text: str) -> str:
+    """Source text without // comments, trailing blanks and empty lines
+    (a comment edit does not change a kernel)."""
+    out = []
+    for line in text.splitlines():
+        i = line.find("//")
+        while i >= 0 and line.count('"', 0, i) % 2 == 1:  # inside a string literal
+            i = line.find("//", i + 2)
+        if i >= 0:
+            line = line[:i]
+        line = line.rstrip()
+        if line:
+            out.append(line)
+    return "\n".join(out)
+
+
 def kernel_source_hash(kernel: str):
-    """Hash of the source files a kernel is built from (its recorded DRAM
-    traffic is only reported while they are unchanged)."""
+    """Hash of the code of the source files a kernel is built from (its
+    recorded DRAM traffic is only reported while that code is unchanged)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "serving_nvfp4_routed_gb300", "csrc")
     family = "decode" if "gateup_down" in kernel else kernel.split("_")[0]
     for fn in KERNEL_SOURCES[family if family in KERNEL_SOURCES else "gemv"]:
-        h.update(open(os.path.join(csrc, fn), "rb").read())
+        h.update(_code_only(open(os.path.join(csrc, fn)).read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -9,11 +9,14 @@
 // With few tokens per expert the layer is a stream of 4.5-bit weights
 // (codes + e4m3 scales) from HBM; every weight is read once and used by the
 // handful of rows routed to its expert.  Design:
-//   * work item = (expert, 16 output features, up to 8 routed rows); work
-//     items are taken from an atomic counter so that CTAs stay busy;
-//   * the CTA's NW warps split K; each warp reduces its K range with
-//     mma.sync m16n8k16 (f32 accumulate) and the partial sums meet in shared
-//     memory;
+//   * work item = (expert, 16 x 8 / ksplit output features (down: up to 8
+//     such blocks), up to 8 routed rows); a CTA's first item is its own
+//     index, the others come from an atomic counter so that CTAs stay busy;
+//     the routing metadata sits in shared memory, so that an item's decode
+//     does no dependent global loads;
+//   * each warp takes 16 output features; when too few items exist to fill
+//     the GPU, ksplit warps split K and their partial sums (mma.sync
+//     m16n8k16, f32 accumulate) meet in shared memory;
 //   * K is permuted inside each CK-wide chunk so that lane quad c of a
 //     warp owns the contiguous physical range [c*CK/4, (c+1)*CK/4): every
 //     lane loads its weights with 16-byte loads straight into the mma
