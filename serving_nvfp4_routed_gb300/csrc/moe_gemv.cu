@@ -685,11 +685,13 @@ int gemv_item_groups(int N, int ksplit, int fb_group) {
 int gemv_pick_ksplit(int expected_tiles, int N, int nproj) {
     const long long want = num_sms();  // at least one work item per SM before K is split
     // gate/up with fewer than eight 128-feature items per SM (a few tokens):
-    // 64-feature items with K split over two warp halves, so that the items
-    // spread more evenly over the CTAs (measured at T=8: 111 -> 103 µs)
-    if (nproj == 2 && N % 128 == 0 && (long long)expected_tiles * (N / 128) >= want &&
-        (long long)expected_tiles * (N / 128) < 8LL * num_sms())
-        return 2;
+    // smaller items with K split over the warps, so that the items spread
+    // more evenly over the CTAs -- 64 features over two warp halves (T=8:
+    // 111 -> 103 µs), 32 features over four warp quarters below two such
+    // items per SM (T=2: 76.5 -> 72.6 µs; at T=8 it was slower)
+    const long long items128 = (long long)expected_tiles * (N / 128);
+    if (nproj == 2 && N % 128 == 0 && items128 >= want && items128 < 8LL * num_sms())
+        return items128 < 2LL * num_sms() ? 4 : 2;
     for (int wf = kWarps; wf >= 1; wf >>= 1) {
         const int FB = 16 * wf;
         if (N % FB != 0) continue;
