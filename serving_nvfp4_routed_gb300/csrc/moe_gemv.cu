@@ -156,6 +156,11 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, c = lane & 3;
+    // The B-fragment reads of a chunk hit granules qb + j (qb = this lane's
+    // first granule of the chunk, a multiple of 8 for CK = 256 and of 2 for
+    // CK = 64; j < 8): there bsw() flips the low bits of j by a mask fixed
+    // per lane, so the reads address qb + (j ^ kP).
+    const int kP = CK == 256 ? ((c << 1) | (g & 1)) : (g & 1);
     const int KSPL = a.ksplit, WF = kWarps / KSPL;
     const int wf = warp / KSPL, ks = warp % KSPL;
 
@@ -395,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
                     const int qb = (ch * CK + c * C::TS) / 8;
 #pragma unroll
                     for (int jj = 0; jj < C::KS; jj += 2) {
-                        const uint4 bq = brow_s[bsw<CK>(qb + jj / 2, g)];
+                        const uint4 bq = brow_s[qb + ((jj / 2) ^ kP)];  // = bsw(qb + jj / 2, g)
                         const uint32_t b0[2] = {bq.x, bq.y};
                         const uint32_t b1[2] = {bq.z, bq.w};
 #pragma unroll
