@@ -425,8 +425,37 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
                 constexpr std::integral_constant<int, 3 % NBUF> kB3{};
                 const int step = U * KSPL;
                 // the ring's loads commit a group on every call (empty past the end)
+                // the ring's loads of this block: the lane's row pointers
+                // once, then one chunk stride per batch (one commit group
+                // per call, empty past the end)
+                const uint8_t* rcp[2];
+                const uint8_t* rsp[2];
+                if constexpr (kRing) {
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const size_t row = (size_t)cur.e * a.N + n0 + g + 8 * hf;
+                        rcp[hf] = a.a_codes[0] + row * K2 + c * (C::TS / 2);
+                        rsp[hf] = a.a_scales[0] + row * K16 + c * (C::TS / 16);
+                    }
+                }
                 auto load_ahead = [&](auto buf, int ch) {
-                    if (kRing || ch < nch) load_batch(buf, cur, ch);
+                    if constexpr (kRing) {
+                        constexpr int B = decltype(buf)::value;
+                        if (ch < nch) {
+                            uint8_t* sl = wring + B * kRingSlotBytes;
+#pragma unroll
+                            for (int hf = 0; hf < 2; ++hf) {
+                                const uint8_t* src = rcp[hf] + ch * (CK / 2);
+                                uint8_t* dst = sl + hf * 1024 + lane * 32;
+                                tc::cp_async16(tc::smem_u32(dst + hsw), src, 16);
+                                tc::cp_async16(tc::smem_u32(dst + (16 - hsw)), src + 16, 16);
+                                tc::cp_async4(tc::smem_u32(sl + 2048 + hf * 128 + lane * 4), rsp[hf] + ch * (CK / 16));
+                            }
+                        }
+                        tc::cp_async_commit();
+                    } else {
+                        if (ch < nch) load_batch(buf, cur, ch);
+                    }
                 };
                 for (int chb = ks; chb < nch; chb += NBUF * step) {
                     const int ld = (NBUF - 1) * step;  // distance of the batch loaded ahead
