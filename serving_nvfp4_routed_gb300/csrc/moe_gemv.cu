@@ -255,9 +255,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
             }
             tc::cp_async_commit();
         } else {
-            // (warp 0 takes chunks 0, KSPL, ...: the CTA's chunks at that
-            // distance are the KSPL consecutive ones)
-            if (a.pf_dist > 0 && tid == 0)
+            // (the CTA's chunks at that distance are the KSPL consecutive
+            // ones; lane 0 of warp chb % 8 issues them, so that the warps
+            // share the extra instructions)
+            if (a.pf_dist > 0 && tid == 32 * (chb % kWarps))
                 for (int q = 0; q < KSPL; ++q) l2_prefetch(it, it.fb, chb + a.pf_dist * KSPL + q);
 #pragma unroll
             for (int u = 0; u < U; ++u) {
