@@ -371,11 +371,13 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
         for (;;) {  // the feature blocks of this item, all on the staged rows
             // ---- stream this warp's 16 features over its share of K
             const int n0 = cur.fb * FB + wf * 16;
-            float acc[NPROJ][4];
+            // two accumulator chains per projection (odd and even k-steps),
+            // summed after the K loop: half the dependent mma.sync chain
+            float acc[NPROJ][4], acc2[NPROJ][4];
 #pragma unroll
             for (int p = 0; p < NPROJ; ++p)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) acc[p][i] = 0.0f;
+                for (int i = 0; i < 4; ++i) acc[p][i] = acc2[p][i] = 0.0f;
             const uint4* brow_s = Bs + (size_t)g * Kg;
             auto compute = [&](auto buf, int chb) {
                 constexpr int B = decltype(buf)::value;
@@ -412,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
                             const uint32_t af0[4] = {r0[0], r1[0], r0[1], r1[1]};
                             const uint32_t af1[4] = {r0[2], r1[2], r0[3], r1[3]};
                             mma_16816(acc[p], af0, b0);
-                            mma_16816(acc[p], af1, b1);
+                            mma_16816(acc2[p], af1, b1);
                         }
                     }
                 }
@@ -477,6 +479,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
                     }
                 }
             }
+#pragma unroll
+            for (int p = 0; p < NPROJ; ++p)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[p][i] += acc2[p][i];
             const bool owner = ks == 0;
             if (KSPL > 1 && !owner) {
 #pragma unroll
