@@ -102,8 +102,9 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
 }
 
 // Eight fp32 -> eight e2m1 codes (round to nearest even, saturating to +-6),
-// element i in bits [4i, 4i+4).  The sign bit of every input is kept in its
-// code, so a value that rounds to zero from below gives -0 (code 8).
+// element i in bits [4i, 4i+4).  The conversion keeps the sign of an input
+// that rounds to zero (-0.1 and -0.0 give code 8, -0), as the format's
+// definition does: checked on sm_103a for -0.0, -1e-30, -0.1 and -0.25.
 __device__ __forceinline__ uint32_t f32x8_to_e2m1x8(const float v[8]) {
     uint32_t r;
     asm("{\n"
@@ -116,10 +117,7 @@ __device__ __forceinline__ uint32_t f32x8_to_e2m1x8(const float v[8]) {
         "}"
         : "=r"(r)
         : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
-    uint32_t sign = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) sign |= (__float_as_uint(v[i]) >> 31) << (4 * i + 3);
-    return r | sign;
+    return r;
 }
 
 // A quotient fl(v / d) for the e2m1 rounding that follows, given r = fl(1/d).
@@ -129,9 +127,12 @@ __device__ __forceinline__ uint32_t f32x8_to_e2m1x8(const float v[8]) {
 // boundaries (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5).  Only there (and for
 // inf / NaN, whose low significand bits are zero) is the correctly rounded
 // division taken, so the code is always that of fl(v / d).
+__device__ __forceinline__ bool e2m1_quotient_near(float q) {
+    return ((__float_as_uint(q) + 4u) & 0x1FFFFFu) <= 8u;
+}
 __device__ __forceinline__ float e2m1_quotient(float v, float d, float r) {
     const float q = __fmul_rn(v, r);
-    if (((__float_as_uint(q) + 4u) & 0x1FFFFFu) <= 8u) return __fdiv_rn(v, d);
+    if (e2m1_quotient_near(q)) return __fdiv_rn(v, d);
     return q;
 }
 
@@ -150,13 +151,13 @@ __device__ __forceinline__ void e2m1x8_to_f16x8(uint32_t w, uint32_t out[4]) {
         : "r"(w));
 }
 
-// e2m1 codes of two values as one byte (lo in the low nibble), sign kept.
+// e2m1 codes of two values as one byte (lo in the low nibble).
 __device__ __forceinline__ uint32_t e2m1x2_byte(float lo, float hi) {
     uint32_t r;
     asm("{\n.reg .b8 b;\ncvt.rn.satfinite.e2m1x2.f32 b, %1, %2;\nmov.b32 %0, {b, b, b, b};\n}"
         : "=r"(r)
         : "f"(hi), "f"(lo));
-    return (r & 0xFFu) | ((__float_as_uint(lo) >> 31) << 3) | ((__float_as_uint(hi) >> 31) << 7);
+    return r & 0xFFu;  // (the sign of a zero is kept, as in f32x8_to_e2m1x8)
 }
 
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {

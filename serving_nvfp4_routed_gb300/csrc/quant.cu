@@ -74,8 +74,16 @@ __device__ __forceinline__ uint32_t quant8(const float v[8], float denom) {
     if (denom == 0.0f) return 0u;
     const float r = __frcp_rn(denom);
     float q[8];
+    bool near = false;  // a product near a significand 1, 1.25, 1.5 or 1.75: divide there
 #pragma unroll
-    for (int i = 0; i < 8; ++i) q[i] = e2m1_quotient(v[i], denom, r);
+    for (int i = 0; i < 8; ++i) {
+        q[i] = __fmul_rn(v[i], r);
+        near |= e2m1_quotient_near(q[i]);
+    }
+    if (near) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = e2m1_quotient(v[i], denom, r);
+    }
     return f32x8_to_e2m1x8(q);
 }
 
@@ -131,17 +139,19 @@ __global__ void quantize_weights_kernel(const uint16_t* __restrict__ w, size_t n
 }
 
 // Output row r quantises source row src(r) with the input scale of the
-// expert whose row range holds r.  One warp per row (8 rows in flight per
-// CTA, grid-stride); the expert offsets are cached in shared memory for the
-// row's lookup; each lane takes whole 16-value blocks (32-byte loads, 8-byte
-// code and 1-byte scale stores).
+// expert whose row range holds r.  A warp takes a unit of `spu` segments of
+// one row, a segment being 32 16-value blocks (one per lane: 32-byte loads,
+// 8-byte code and 1-byte scale stores); units are grid-strided.  A few rows
+// (a decode batch) take one segment per unit so that every SM gets work;
+// many rows take whole rows.  The expert offsets are cached in shared
+// memory for the row's lookup.
 constexpr int kQaWarps = 8;
 constexpr int kQaMaxE = 1024;
 
 __global__ void __launch_bounds__(kQaWarps * 32) quantize_act_kernel(
     const uint16_t* __restrict__ x, int M, int K, const int32_t* __restrict__ row_to_slot, int top_k,
     const float* __restrict__ input_scale, const int32_t* __restrict__ offsets, int E, uint8_t* __restrict__ codes,
-    uint8_t* __restrict__ scales) {
+    uint8_t* __restrict__ scales, int spu) {
     __shared__ int s_off[kQaMaxE + 1];
     grid_dep_wait();
     const bool cached = offsets && E <= kQaMaxE;
@@ -150,7 +160,12 @@ __global__ void __launch_bounds__(kQaWarps * 32) quantize_act_kernel(
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nb = K / 16;
-    for (int r = blockIdx.x * kQaWarps + warp; r < M; r += gridDim.x * kQaWarps) {
+    const int nseg = (nb + 31) / 32;
+    const unsigned useg = (unsigned)((nseg + spu - 1) / spu);  // units per row
+    const unsigned units = (unsigned)M * useg;
+    for (unsigned u = blockIdx.x * kQaWarps + warp; u < units; u += gridDim.x * kQaWarps) {
+        const int r = (int)(u / useg);
+        const int seg0 = (int)(u % useg) * spu;
         const int src = row_to_slot ? row_to_slot[r] / top_k : r;
         float gs;
         if (offsets) {
@@ -164,7 +179,8 @@ __global__ void __launch_bounds__(kQaWarps * 32) quantize_act_kernel(
             gs = input_scale[0];
         }
         const uint16_t* xr = x + (size_t)src * K;
-        for (int b = lane; b < nb; b += 32) {
+        const int b1 = min(nb, (seg0 + spu) * 32);
+        for (int b = seg0 * 32 + lane; b < b1; b += 32) {
             float v0[8], v1[8], m0, m1;
             load_bf16x8(xr + (size_t)b * 16, v0, m0);
             load_bf16x8(xr + (size_t)b * 16 + 8, v1, m1);
@@ -182,10 +198,15 @@ void launch_quantize_act(const uint16_t* x, int M, int K, const int32_t* row_to_
                          const float* input_scale, const int32_t* offsets, int E, uint8_t* codes,
                          uint8_t* scales, cudaStream_t s) {
     if ((size_t)M * K == 0) return;
-    const int grid = std::min((M + kQaWarps - 1) / kQaWarps, num_sms() * 8);
+    const int cap = num_sms() * 8;  // CTAs
+    const int nseg = (K / 16 + 31) / 32;
+    // one segment per unit while the rows alone would leave warps idle
+    const int spu = (long long)M < (long long)cap * kQaWarps ? 1 : nseg;
+    const long long units = (long long)M * ((nseg + spu - 1) / spu);
+    const int grid = (int)std::min<long long>((units + kQaWarps - 1) / kQaWarps, cap);
     NVFP4_LAUNCH("quantize_act", s,
                  launch_pdl(quantize_act_kernel, dim3(grid), dim3(kQaWarps * 32), 0, s, x, M, K, row_to_slot,
-                            top_k, input_scale, offsets, E, codes, scales));
+                            top_k, input_scale, offsets, E, codes, scales, spu));
 }
 
 nvfp4_status check_weight_recipe(const uint16_t* w, int batch, int N, int K, const uint8_t* codes,

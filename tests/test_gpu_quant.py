@@ -68,7 +68,8 @@ def test_weight_recipe_full_bank_sampled(orc):
 
 @pytest.mark.parametrize("T,E,k,d,gs_kind", [(4, 8, 2, 256, "calib"), (64, 288, 8, 4096, "calib"),
                                              (33, 16, 4, 512, "tiny"), (17, 16, 3, 512, "huge"),
-                                             (600, 288, 8, 1024, "calib")])
+                                             (600, 288, 8, 1024, "calib"), (5, 16, 2, 1040, "calib"),
+                                             (1250, 16, 8, 1040, "calib")])
 def test_activation_quant_gathered_bit_exact(orc, T, E, k, d, gs_kind):
     x = synth.make_x(T, d, seed=T + d, device="cuda", outlier_frac=0.05)
     logits = synth.make_logits(T, E, seed=T, device="cuda")
