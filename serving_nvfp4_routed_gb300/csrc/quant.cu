@@ -8,8 +8,7 @@
 // static input_scale); recipe: section "What the branch does" (experts
 // packed by ModelOpt's recipe at load, one projection at a time).
 //
-// Each thread owns 8 consecutive inputs (one 16-byte load of bf16); the two
-// threads of a 16-block exchange their partial block amax with one shuffle.
+// Each thread owns whole 16-value blocks (two 16-byte loads of bf16).
 // The scale arithmetic is IEEE fp32 round-to-nearest in the recipe's order:
 //   sf = (bam / 6) / gs;  s = e4m3_rn_sat(sf);  q = e2m1_rn_sat(v / (S * gs))
 // so that codes and scales are bit-identical to the format's definition.
@@ -87,15 +86,6 @@ __device__ __forceinline__ uint32_t quant8(const float v[8], float denom) {
     return f32x8_to_e2m1x8(q);
 }
 
-// Block quantisation of 8 values held by this thread, given the 16-block's
-// amax and the tensor scale gs.  Returns the 8 packed codes and the scale byte.
-__device__ __forceinline__ void quant_half_block(const float v[8], float bam, float gs, uint32_t& codes,
-                                                 uint32_t& sbyte) {
-    float denom;
-    sbyte = block_scale(bam, gs, denom);
-    codes = quant8(v, denom);
-}
-
 __device__ __forceinline__ void unpack_bf16x8(const uint4 u, float v[8], float& amax) {
     const uint32_t ww[4] = {u.x, u.y, u.z, u.w};
     amax = 0.0f;
@@ -111,30 +101,28 @@ __device__ __forceinline__ void load_bf16x8(const uint16_t* p, float v[8], float
     unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(p)), v, amax);
 }
 
-__global__ void quantize_weights_kernel(const uint16_t* __restrict__ w, size_t n_per, int batch,
+// Tensor blockIdx.y: one thread per 16-value block (two 16-byte loads), the
+// blocks grid-strided over blockIdx.x; the tensor scale gs is taken once
+// per thread.
+__global__ void quantize_weights_kernel(const uint16_t* __restrict__ w, size_t n_per,
                                         const float* __restrict__ amax, uint8_t* __restrict__ codes,
                                         uint8_t* __restrict__ scales, float* __restrict__ ws2_out) {
-    const size_t halves_per = n_per / 8;
-    const size_t total = halves_per * (size_t)batch;
-    // warp-uniform trip count (the pair shuffle needs every lane); lanes past
-    // the end recompute element 0 and store nothing
-    for (size_t base = blockIdx.x * (size_t)blockDim.x + (threadIdx.x & ~31u); base < total;
-         base += (size_t)gridDim.x * blockDim.x) {
-        const size_t i = base + (threadIdx.x & 31);
-        const bool live = i < total;
-        const size_t ii = live ? i : 0;
-        const int b = (int)(ii / halves_per);
-        const float gs = __fdiv_rn(amax[b], 2688.0f);
-        float v[8], m;
-        load_bf16x8(w + ii * 8, v, m);
-        float bam = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-        uint32_t c, s;
-        quant_half_block(v, bam, gs, c, s);
-        if (live) {
-            reinterpret_cast<uint32_t*>(codes)[ii] = c;
-            if ((ii & 1) == 0) scales[ii / 2] = (uint8_t)s;
-            if (ii - (size_t)b * halves_per == 0) ws2_out[b] = gs;
-        }
+    const int b = blockIdx.y;
+    const float gs = __fdiv_rn(amax[b], 2688.0f);
+    if (blockIdx.x == 0 && threadIdx.x == 0) ws2_out[b] = gs;
+    const size_t nblk = n_per / 16;
+    const uint16_t* wb = w + (size_t)b * n_per;
+    uint8_t* cb = codes + (size_t)b * (n_per / 2);
+    uint8_t* sb = scales + (size_t)b * nblk;
+    for (size_t k = blockIdx.x * (size_t)blockDim.x + threadIdx.x; k < nblk; k += (size_t)gridDim.x * blockDim.x) {
+        float v0[8], v1[8], m0, m1;
+        load_bf16x8(wb + k * 16, v0, m0);
+        load_bf16x8(wb + k * 16 + 8, v1, m1);
+        float denom;
+        const uint32_t sbyte = block_scale(fmaxf(m0, m1), gs, denom);
+        const uint32_t c0 = quant8(v0, denom), c1 = quant8(v1, denom);
+        *reinterpret_cast<uint2*>(cb + k * 8) = make_uint2(c0, c1);
+        sb[k] = (uint8_t)sbyte;
     }
 }
 
@@ -229,11 +217,11 @@ nvfp4_status launch_weight_recipe(const uint16_t* w, int batch, int N, int K, fl
         1, std::min<size_t>((n_per / 8 + 255) / 256, (size_t)num_sms() * 8 / std::max(1, batch) + 1));
     NVFP4_LAUNCH("tensor_amax", stream,
                  tensor_amax_kernel<<<dim3(gx, batch), 256, 0, stream>>>(w, n_per, amax));
-    const size_t total = n_per / 8 * batch;
-    const int grid = (int)std::min<size_t>((total + 255) / 256, (size_t)num_sms() * 16);
+    const int qx = (int)std::max<size_t>(
+        1, std::min<size_t>((n_per / 16 + 255) / 256, (size_t)num_sms() * 16 / std::max(1, batch) + 1));
     NVFP4_LAUNCH("quantize_weights", stream,
-                 quantize_weights_kernel<<<grid, 256, 0, stream>>>(w, n_per, batch, amax, codes, scales,
-                                                                   weight_scale_2));
+                 quantize_weights_kernel<<<dim3(qx, batch), 256, 0, stream>>>(w, n_per, amax, codes, scales,
+                                                                              weight_scale_2));
     return last_launch_status();
 }
 
