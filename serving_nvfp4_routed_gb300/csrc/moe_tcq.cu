@@ -397,9 +397,9 @@ __global__ void sum_rows_kernel(const uint16_t* __restrict__ y, const int32_t* _
     grid_dep_wait();
     const int k = KT > 0 ? KT : k_rt;
     const int per_row = d / 8;
-    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < (size_t)T * per_row;
-         i += (size_t)gridDim.x * blockDim.x) {
-        const size_t t = i / per_row, f = (i % per_row) * 8;
+    const unsigned n = (unsigned)T * (unsigned)per_row;  // the launch keeps T * d / 8 below 2^32
+    for (unsigned i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        const size_t t = i / (unsigned)per_row, f = (i % (unsigned)per_row) * 8;
         float acc[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
@@ -480,7 +480,7 @@ void launch_sum_rows(const uint16_t* y, const int32_t* slot_to_row, const float*
                      uint16_t* out, cudaStream_t s) {
     const size_t n = (size_t)T * (d / 8);
     if (n == 0) return;
-    const int grid = (int)std::min<size_t>((n + 255) / 256, (size_t)num_sms() * 8);
+    const int grid = (int)std::min<size_t>((n + 255) / 256, (size_t)num_sms() * 16);
     if (k == 8) {
         NVFP4_LAUNCH("sum_rows", s, launch_pdl(sum_rows_kernel<8>, dim3(grid), dim3(256), 0, s, y, slot_to_row, topk_w,
                                                T, k, d, out));
