@@ -397,7 +397,7 @@ __global__ void sum_rows_kernel(const uint16_t* __restrict__ y, const int32_t* _
     grid_dep_wait();
     const int k = KT > 0 ? KT : k_rt;
     const int per_row = d / 8;
-    const unsigned n = (unsigned)T * (unsigned)per_row;  // the launch keeps T * d / 8 below 2^32
+    const unsigned n = (unsigned)T * (unsigned)per_row;  // below 2^31: the launch splits T
     for (unsigned i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
         const size_t t = i / (unsigned)per_row, f = (i % (unsigned)per_row) * 8;
         float acc[8];
@@ -478,15 +478,24 @@ void launch_tcq(int epi, const TcmArgs& a, int max_tiles, cudaStream_t s) {
 
 void launch_sum_rows(const uint16_t* y, const int32_t* slot_to_row, const float* topk_w, int T, int k, int d,
                      uint16_t* out, cudaStream_t s) {
-    const size_t n = (size_t)T * (d / 8);
-    if (n == 0) return;
-    const int grid = (int)std::min<size_t>((n + 255) / 256, (size_t)num_sms() * 16);
-    if (k == 8) {
-        NVFP4_LAUNCH("sum_rows", s, launch_pdl(sum_rows_kernel<8>, dim3(grid), dim3(256), 0, s, y, slot_to_row, topk_w,
-                                               T, k, d, out));
-    } else {
-        NVFP4_LAUNCH("sum_rows", s, launch_pdl(sum_rows_kernel<0>, dim3(grid), dim3(256), 0, s, y, slot_to_row, topk_w,
-                                               T, k, d, out));
+    if ((size_t)T * (d / 8) == 0) return;
+    // the kernel indexes (token, 8 features) in 32 bits: tokens in chunks
+    // of at most 2^31 such items
+    const int chunk = (int)std::min<size_t>((size_t)T, ((size_t)1 << 31) / (size_t)(d / 8));
+    for (int t0 = 0; t0 < T; t0 += chunk) {
+        const int tc = std::min(chunk, T - t0);
+        const size_t n = (size_t)tc * (d / 8);
+        const int grid = (int)std::min<size_t>((n + 255) / 256, (size_t)num_sms() * 16);
+        const int32_t* str = slot_to_row + (size_t)t0 * k;
+        const float* tw = topk_w + (size_t)t0 * k;
+        uint16_t* o = out + (size_t)t0 * d;
+        if (k == 8) {
+            NVFP4_LAUNCH("sum_rows", s,
+                         launch_pdl(sum_rows_kernel<8>, dim3(grid), dim3(256), 0, s, y, str, tw, tc, k, d, o));
+        } else {
+            NVFP4_LAUNCH("sum_rows", s,
+                         launch_pdl(sum_rows_kernel<0>, dim3(grid), dim3(256), 0, s, y, str, tw, tc, k, d, o));
+        }
     }
 }
 
